@@ -1,0 +1,247 @@
+"""Python binding of libeagle.so, the GB300 (sm_103a) tree-verify library.
+
+Argument marshalling only: every function here checks tensor devices, dtypes
+and shapes, derives the sizes the C ABI wants, and calls the C entry point of
+the same name on the current CUDA stream.  Every step of the computation runs
+in the library's CUDA kernels; there is no fallback.  If the shared library
+has not been built (see `build()`), the first call raises.
+
+Tensors are torch CUDA tensors (PyTorch is used for device memory and streams
+only).  Outputs are written in place into the tensors the caller passes.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+from typing import Optional
+
+__all__ = [
+    "EagleError", "build", "lib", "status_string", "version", "check_status",
+    "EAGLE_F32", "EAGLE_BF16", "LMHEAD_GREEDY", "LMHEAD_PROB", "SAMPLE_REPLACE",
+    "SAMPLE_NO_REPLACE", "eagle_tree_attn", "eagle_tree_attn_workspace_bytes",
+    "eagle_lmhead_softmax", "eagle_lmhead_workspace_bytes", "eagle_accept_greedy",
+    "eagle_accept_stochastic", "eagle_draft_expand", "eagle_draft_pool_bytes",
+]
+
+HERE = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(HERE, "libeagle.so")
+
+EAGLE_F32, EAGLE_BF16 = 0, 1
+LMHEAD_GREEDY, LMHEAD_PROB = 0, 1
+SAMPLE_REPLACE, SAMPLE_NO_REPLACE = 0, 1
+
+_STATUS = {0: "ok", 1: "invalid argument", 2: "invalid tree", 3: "unsupported shape",
+           4: "numeric error", 5: "device wait timed out", 6: "CUDA error",
+           7: "workspace too small"}
+
+
+class EagleError(RuntimeError):
+    def __init__(self, fn: str, code: int):
+        super().__init__(f"{fn}: {_STATUS.get(code, 'unknown')} (status {code})")
+        self.code = code
+
+
+_lib = None
+_i, _f, _p, _sz = ctypes.c_int, ctypes.c_float, ctypes.c_void_p, ctypes.c_size_t
+_SIGS = {
+    "eagle_status_string": ([_i], ctypes.c_char_p),
+    "eagle_version": ([], ctypes.c_char_p),
+    "eagle_tree_attn_workspace_bytes": ([_i] * 7, _sz),
+    "eagle_tree_attn": ([_i, _i, _i, _i, _i, _i, _f, _i, _i] + [_p] * 9 + [_p, _sz, _p, _p], _i),
+    "eagle_lmhead_workspace_bytes": ([_i, _i], _sz),
+    "eagle_lmhead_softmax": ([_i, _i, _i, _i, _f, _i] + [_p] * 8 + [_sz, _p, _p], _i),
+    "eagle_accept_greedy": ([_i, _i, _p, _p, _p, _p, _i, _p, _p, _p, _p, _p], _i),
+    "eagle_accept_stochastic": ([_i] * 5 + [_p] * 8 + [_i] + [_p] * 5, _i),
+    "eagle_draft_pool_bytes": ([_i] * 4, _sz),
+    "eagle_draft_expand": ([_i] * 6 + [_p] * 4 + [_sz] + [_p] * 8, _i),
+}
+
+
+def build(verbose: bool = False, force: bool = False) -> str:
+    """Compile the CUDA sources into libeagle.so (sm_103a) and return its path."""
+    from . import _build
+    return _build.build(verbose=verbose, force=force)
+
+
+def lib() -> ctypes.CDLL:
+    """The loaded shared library (raises if it was never built)."""
+    global _lib
+    if _lib is None:
+        if not os.path.exists(LIB_PATH):
+            raise RuntimeError(
+                f"{LIB_PATH} is missing: build the CUDA library first "
+                "(eagle_tree_verification_gb300.build())")
+        L = ctypes.CDLL(LIB_PATH)
+        for name, (args, res) in _SIGS.items():
+            fn = getattr(L, name)
+            fn.argtypes = args
+            fn.restype = res
+        _lib = L
+    return _lib
+
+
+def status_string(code: int) -> str:
+    return lib().eagle_status_string(int(code)).decode()
+
+
+def version() -> str:
+    return lib().eagle_version().decode()
+
+
+def check_status(status_tensor, fn: str = "device") -> None:
+    """Raise EagleError if a device status word is non-zero (synchronises)."""
+    code = int(status_tensor.view(-1)[0].item())
+    if code != 0:
+        raise EagleError(fn, code)
+
+
+# ---------------------------------------------------------------------------
+# marshalling helpers
+# ---------------------------------------------------------------------------
+def _torch():
+    import torch
+    return torch
+
+
+def _ptr(t) -> Optional[int]:
+    if t is None:
+        return None
+    if not t.is_cuda:
+        raise ValueError("expected a CUDA tensor")
+    if not t.is_contiguous():
+        raise ValueError("expected a contiguous tensor")
+    return t.data_ptr()
+
+
+def _dtype_code(t) -> int:
+    torch = _torch()
+    if t.dtype == torch.bfloat16:
+        return EAGLE_BF16
+    if t.dtype == torch.float32:
+        return EAGLE_F32
+    raise ValueError(f"unsupported dtype {t.dtype}")
+
+
+def _need(t, dtype, name):
+    if t is not None and t.dtype != dtype:
+        raise ValueError(f"{name}: expected {dtype}, got {t.dtype}")
+
+
+def _stream(stream) -> int:
+    torch = _torch()
+    s = torch.cuda.current_stream() if stream is None else stream
+    return s.cuda_stream
+
+
+def _call(name, *args):
+    rc = getattr(lib(), name)(*args)
+    if rc != 0:
+        raise EagleError(name, rc)
+
+
+# ---------------------------------------------------------------------------
+# entry points
+# ---------------------------------------------------------------------------
+def eagle_tree_attn_workspace_bytes(B, T, Hq, Hkv, D, max_nodes, max_kv) -> int:
+    return int(lib().eagle_tree_attn_workspace_bytes(B, T, Hq, Hkv, D, max_nodes, max_kv))
+
+
+def eagle_tree_attn(q, k_tree, v_tree, k_cache, v_cache, kv_off, tree_off, parent, out,
+                    status, *, max_nodes: int, max_kv: int, scale: Optional[float] = None,
+                    ws=None, stream=None) -> None:
+    """Tree-masked attention; see eagle_tree_attn in include/eagle.h.
+    q [T,Hq,D]; k_tree/v_tree [T,Hkv,D]; k_cache/v_cache [sum L,Hkv,D];
+    kv_off/tree_off [B+1] int32; parent [T] int32; out [T,Hq,D] fp32."""
+    torch = _torch()
+    T, Hq, D = q.shape
+    Hkv = k_tree.shape[1]
+    B = tree_off.numel() - 1
+    for name, t in (("k_tree", k_tree), ("v_tree", v_tree), ("k_cache", k_cache),
+                    ("v_cache", v_cache)):
+        _need(t, q.dtype, name)
+    for name, t in (("kv_off", kv_off), ("tree_off", tree_off), ("parent", parent)):
+        _need(t, torch.int32, name)
+    _need(out, torch.float32, "out")
+    ws_bytes = 0 if ws is None else ws.numel() * ws.element_size()
+    sc = (1.0 / D ** 0.5) if scale is None else float(scale)
+    _call("eagle_tree_attn", _dtype_code(q), B, T, Hq, Hkv, D, sc, max_nodes, max_kv,
+          _ptr(q), _ptr(k_tree), _ptr(v_tree), _ptr(k_cache), _ptr(v_cache), _ptr(kv_off),
+          _ptr(tree_off), _ptr(parent), _ptr(out), _ptr(ws), ws_bytes,
+          _ptr(status), _stream(stream))
+
+
+def eagle_lmhead_workspace_bytes(T, V) -> int:
+    return int(lib().eagle_lmhead_workspace_bytes(T, V))
+
+
+def eagle_lmhead_softmax(h, w, argmax, row_max, row_lse, top2_gap, q, ws, status, *,
+                         temperature: float = 1.0, stream=None) -> None:
+    """LM head + softmax statistics + argmax; q=None selects greedy mode
+    (no [T,V] output).  h [T,H]; w [V,H]; argmax [T] int32; row_max,
+    row_lse, top2_gap [T] fp32; q [T,V] fp32 or None."""
+    torch = _torch()
+    T, H = h.shape
+    V = w.shape[0]
+    _need(w, h.dtype, "w")
+    _need(argmax, torch.int32, "argmax")
+    for name, t in (("row_max", row_max), ("row_lse", row_lse), ("top2_gap", top2_gap), ("q", q)):
+        _need(t, torch.float32, name)
+    mode = LMHEAD_GREEDY if q is None else LMHEAD_PROB
+    _call("eagle_lmhead_softmax", _dtype_code(h), T, H, V, float(temperature), mode, _ptr(h),
+          _ptr(w), _ptr(argmax), _ptr(row_max), _ptr(row_lse), _ptr(top2_gap), _ptr(q),
+          _ptr(ws), ws.numel() * ws.element_size(), _ptr(status), _stream(stream))
+
+
+def eagle_accept_greedy(tree_off, parent, tokens, argmax, accept_len, accepted_nodes,
+                        out_tokens, status, *, max_nodes: int, max_depth: int,
+                        stream=None) -> None:
+    """Greedy tree walk.  accepted_nodes/out_tokens [B, max_depth+1] int32."""
+    torch = _torch()
+    B = tree_off.numel() - 1
+    for name, t in (("tree_off", tree_off), ("parent", parent), ("tokens", tokens),
+                    ("argmax", argmax), ("accept_len", accept_len),
+                    ("accepted_nodes", accepted_nodes), ("out_tokens", out_tokens)):
+        _need(t, torch.int32, name)
+    if accepted_nodes.numel() < B * (max_depth + 1) or out_tokens.numel() < B * (max_depth + 1):
+        raise ValueError("output rows must hold max_depth+1 entries per sequence")
+    _call("eagle_accept_greedy", B, max_nodes, _ptr(tree_off), _ptr(parent), _ptr(tokens),
+          _ptr(argmax), max_depth, _ptr(accept_len), _ptr(accepted_nodes), _ptr(out_tokens),
+          _ptr(status), _stream(stream))
+
+
+def eagle_accept_stochastic(tree_off, parent, tokens, q, p_rows, p_row_of_node, u_accept,
+                            u_sample, accept_len, accepted_nodes, out_tokens, status, *,
+                            max_nodes: int, max_depth: int, mode: int = SAMPLE_NO_REPLACE,
+                            stream=None) -> None:
+    """Multi-round stochastic walk.  q [T,V] fp32; p_rows [R,V] fp32."""
+    torch = _torch()
+    B = tree_off.numel() - 1
+    V = q.shape[1]
+    R = p_rows.shape[0]
+    for name, t in (("q", q), ("p_rows", p_rows), ("u_accept", u_accept),
+                    ("u_sample", u_sample)):
+        _need(t, torch.float32, name)
+    if p_rows.shape[1] != V:
+        raise ValueError("p_rows and q must have the same vocabulary")
+    if accepted_nodes.numel() < B * (max_depth + 1) or out_tokens.numel() < B * (max_depth + 1):
+        raise ValueError("output rows must hold max_depth+1 entries per sequence")
+    _call("eagle_accept_stochastic", B, max_nodes, V, R, int(mode), _ptr(tree_off), _ptr(parent),
+          _ptr(tokens), _ptr(q), _ptr(p_rows), _ptr(p_row_of_node), _ptr(u_accept),
+          _ptr(u_sample), max_depth, _ptr(accept_len), _ptr(accepted_nodes), _ptr(out_tokens),
+          _ptr(status), _stream(stream))
+
+
+def eagle_draft_pool_bytes(B, k, depth, V) -> int:
+    return int(lib().eagle_draft_pool_bytes(B, k, depth, V))
+
+
+def eagle_draft_expand(pool, status, *, B: int, V: int, k: int, depth: int, level: int = 0,
+                       finalize: bool = False, draft_logp=None, budget=None, root_token=None,
+                       tree_off=None, parent=None, tokens=None, node_depth=None, score=None,
+                       p_row_of_node=None, stream=None) -> None:
+    """EAGLE-2 expand (one level) or finalize; draft_logp [B, R, V] fp32 with
+    R = 1 + (depth-1)*k."""
+    _call("eagle_draft_expand", B, V, k, depth, int(level), int(bool(finalize)),
+          _ptr(draft_logp), _ptr(budget), _ptr(root_token), _ptr(pool),
+          pool.numel() * pool.element_size(), _ptr(tree_off), _ptr(parent), _ptr(tokens),
+          _ptr(node_depth), _ptr(score), _ptr(p_row_of_node), _ptr(status), _stream(stream))

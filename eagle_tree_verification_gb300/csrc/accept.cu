@@ -1,0 +1,524 @@
+// Acceptance walks of the tree-verify step.
+//
+// eagle_accept_greedy      [S4000] greedy-decoding paragraph; [EAGLE]
+//                          speculative-sampling paragraph (alpha -> alpha+1).
+// eagle_accept_stochastic  [S4000] random-decoding paragraph; [EAGLE]
+//                          "多轮投机采样"; [EAGLE-2] §2 basic principle.
+// (page titles are listed in include/eagle.h)
+//
+// The stochastic walk is sequential in the tree but every rejection needs a
+// full-vocabulary pass (residual max(0, q - p) and its normaliser).  One
+// thread-block cluster serves one sequence: the vocabulary row is split into
+// `slice`-sized pieces, one per CTA, held in shared memory for the whole
+// node, so each visited node's q and p rows are read from HBM exactly once
+// and every rejection round runs out of shared memory.  Per-round integer
+// sums are exchanged through distributed shared memory; every CTA then
+// takes the identical decision (the data it decides on is bit-identical),
+// so control flow stays uniform across the cluster without any spin-wait.
+#include <cooperative_groups.h>
+
+#include "common.cuh"
+
+namespace cg = cooperative_groups;
+using namespace eagle;
+
+namespace {
+
+constexpr int kStochThreads = 512;
+constexpr float kTwo40 = 1099511627776.0f;  // 2^40
+constexpr float kTwo24 = 16777216.0f;       // 2^24
+
+// ---------------------------------------------------------------------------
+// greedy
+// ---------------------------------------------------------------------------
+__global__ void __launch_bounds__(32)
+accept_greedy_kernel(int max_nodes, const int* __restrict__ tree_off,
+                     const int* __restrict__ parent, const int* __restrict__ tokens,
+                     const int* __restrict__ argmax, int max_depth,
+                     int* __restrict__ accept_len, int* __restrict__ accepted_nodes,
+                     int* __restrict__ out_tokens, int* status) {
+  extern __shared__ int sm[];
+  int* s_par = sm;
+  int* s_tok = sm + max_nodes;
+  const int b = blockIdx.x;
+  const int lane = threadIdx.x;
+  const int W = max_depth + 1;
+  int* o_nodes = accepted_nodes + (size_t)b * W;
+  int* o_tok = out_tokens + (size_t)b * W;
+  for (int i = lane; i < W; i += 32) {
+    o_nodes[i] = -1;
+    o_tok[i] = -1;
+  }
+  const int t0 = tree_off[b];
+  const int n = tree_off[b + 1] - t0;
+  if (n < 1 || n > max_nodes) {
+    if (lane == 0) {
+      fail(status, EAGLE_ERR_INVALID_TREE);
+      accept_len[b] = -1;
+    }
+    return;
+  }
+  bool bad = false;
+  for (int i = lane; i < n; i += 32) {
+    const int p = parent[t0 + i];
+    s_par[i] = p;
+    s_tok[i] = tokens[t0 + i];
+    bad |= (i == 0) ? (p != -1) : (p < 0 || p >= i);
+  }
+  if (__any_sync(0xffffffffu, bad)) {
+    if (lane == 0) {
+      fail(status, EAGLE_ERR_INVALID_TREE);
+      accept_len[b] = -1;
+    }
+    return;
+  }
+  __syncwarp();
+  int cur = 0, alpha = 0;
+  if (lane == 0) o_nodes[0] = 0;
+  while (true) {
+    const int want = argmax[t0 + cur];
+    int found = -1;
+    // children have larger indices than their parent (topological order)
+    for (int base = cur + 1; base < n; base += 32) {
+      const int i = base + lane;
+      const bool m = (i < n) && s_par[i] == cur && s_tok[i] == want;
+      const unsigned bal = __ballot_sync(0xffffffffu, m);
+      if (bal) {
+        found = base + __ffs(bal) - 1;
+        break;
+      }
+    }
+    if (found < 0) break;
+    if (alpha + 1 > max_depth) {
+      if (lane == 0) fail(status, EAGLE_ERR_INVALID_ARG);
+      break;
+    }
+    if (lane == 0) {
+      o_tok[alpha] = s_tok[found];
+      o_nodes[alpha + 1] = found;
+    }
+    ++alpha;
+    cur = found;
+  }
+  if (lane == 0) {
+    o_tok[alpha] = argmax[t0 + cur];
+    accept_len[b] = alpha;
+  }
+}
+
+// ---------------------------------------------------------------------------
+// stochastic
+// ---------------------------------------------------------------------------
+struct StochParams {
+  int max_nodes, V, R, mode, max_depth, slice;
+  const int* tree_off;
+  const int* parent;
+  const int* tokens;
+  const float* q;
+  const float* p_rows;
+  const int* p_row_of_node;
+  const float* u_accept;
+  const float* u_sample;
+  int* accept_len;
+  int* accepted_nodes;
+  int* out_tokens;
+  int* status;
+};
+
+// trunc(x * 2^40) for x in [0, 1]: the scaling by a power of two is exact.
+__device__ __forceinline__ unsigned long long fixed40(float x) {
+  return __float2ull_rz(x * kTwo40);
+}
+
+__device__ __forceinline__ bool is_prob(float x) { return x >= 0.f && x <= 1.f; }
+
+// Sum over the block; every thread gets the total.  s_tmp: 33 entries.
+__device__ unsigned long long block_sum_u64(unsigned long long v, unsigned long long* s_tmp) {
+  v = warp_sum_u64(v);
+  const int w = threadIdx.x >> 5, l = threadIdx.x & 31;
+  __syncthreads();
+  if (l == 0) s_tmp[w] = v;
+  __syncthreads();
+  if (w == 0) {
+    unsigned long long t = (l < (int)(blockDim.x >> 5)) ? s_tmp[l] : 0ull;
+    t = warp_sum_u64(t);
+    if (l == 0) s_tmp[32] = t;
+  }
+  __syncthreads();
+  return s_tmp[32];
+}
+
+// Exclusive scan over the block of one value per thread; returns the
+// exclusive prefix, *total receives the block sum.  s_tmp: 33 entries.
+__device__ unsigned long long block_excl_scan_u64(unsigned long long v, unsigned long long* s_tmp,
+                                                  unsigned long long* total) {
+  const int w = threadIdx.x >> 5, l = threadIdx.x & 31;
+  unsigned long long inc = v;
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    const unsigned long long y = __shfl_up_sync(0xffffffffu, inc, o);
+    if (l >= o) inc += y;
+  }
+  __syncthreads();
+  if (l == 31) s_tmp[w] = inc;
+  __syncthreads();
+  if (w == 0) {
+    const int nw = blockDim.x >> 5;
+    unsigned long long t = (l < nw) ? s_tmp[l] : 0ull;
+    unsigned long long ti = t;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const unsigned long long y = __shfl_up_sync(0xffffffffu, ti, o);
+      if (l >= o) ti += y;
+    }
+    if (l < nw) s_tmp[l] = ti - t;  // exclusive prefix of warp totals
+    if (l == 31) s_tmp[32] = ti;
+  }
+  __syncthreads();
+  *total = s_tmp[32];
+  return s_tmp[w] + inc - v;
+}
+
+// Sum of one u64 published by every CTA of the cluster (read through DSMEM).
+__device__ unsigned long long cluster_sum(cg::cluster_group& cluster, unsigned long long* s_slot,
+                                          unsigned CS, unsigned upto,
+                                          unsigned long long* s_bcast) {
+  if (threadIdx.x < 32) {
+    unsigned long long v = 0;
+    if (threadIdx.x < upto && threadIdx.x < CS)
+      v = *cluster.map_shared_rank(s_slot, threadIdx.x);
+    v = warp_sum_u64(v);
+    if (threadIdx.x == 0) *s_bcast = v;
+  }
+  __syncthreads();
+  return *s_bcast;
+}
+
+__global__ void __launch_bounds__(kStochThreads)
+accept_stochastic_kernel(const StochParams P) {
+  cg::cluster_group cluster = cg::this_cluster();
+  const unsigned rank = cluster.block_rank();
+  const unsigned CS = cluster.num_blocks();
+  const int b = blockIdx.x / CS;
+  const int tid = threadIdx.x;
+
+  extern __shared__ __align__(16) unsigned char smem_raw[];
+  float* qs = reinterpret_cast<float*>(smem_raw);
+  float* ps = qs + P.slice;
+  int* s_par = reinterpret_cast<int*>(ps + P.slice);
+  int* s_tok = s_par + P.max_nodes;
+  int* s_kids = s_tok + P.max_nodes;
+  __shared__ unsigned long long s_red[33];
+  __shared__ unsigned long long s_w, s_p, s_tot;  // published to the cluster
+  __shared__ unsigned long long s_bc0, s_bc1;
+  __shared__ int s_flag, s_nk;
+
+  const int v0 = (int)rank * P.slice;
+  const int nv = max(0, min(P.V, v0 + P.slice) - v0);
+  const int W = P.max_depth + 1;
+  const bool writer = (rank == 0);
+  int* o_nodes = P.accepted_nodes + (size_t)b * W;
+  int* o_tok = P.out_tokens + (size_t)b * W;
+  if (writer) {
+    for (int i = tid; i < W; i += blockDim.x) {
+      o_nodes[i] = -1;
+      o_tok[i] = -1;
+    }
+  }
+  const int t0 = P.tree_off[b];
+  const int n = P.tree_off[b + 1] - t0;
+  // All checks below read the same global data in every CTA, so the
+  // early exits are taken by the whole cluster together.
+  if (n < 1 || n > P.max_nodes) {
+    if (writer && tid == 0) {
+      fail(P.status, EAGLE_ERR_INVALID_TREE);
+      P.accept_len[b] = -1;
+    }
+    return;
+  }
+  if (tid == 0) s_flag = 0;
+  __syncthreads();
+  for (int i = tid; i < n; i += blockDim.x) {
+    const int p = P.parent[t0 + i];
+    const int tk = P.tokens[t0 + i];
+    s_par[i] = p;
+    s_tok[i] = tk;
+    if ((i == 0) ? (p != -1) : (p < 0 || p >= i)) atomicOr(&s_flag, 1);
+    if (i > 0 && (tk < 0 || tk >= P.V)) atomicOr(&s_flag, 2);
+  }
+  __syncthreads();
+  if (s_flag) {
+    if (writer && tid == 0) {
+      fail(P.status, (s_flag & 1) ? EAGLE_ERR_INVALID_TREE : EAGLE_ERR_INVALID_ARG);
+      P.accept_len[b] = -1;
+    }
+    return;
+  }
+
+  const bool no_replace = (P.mode == EAGLE_SAMPLE_NO_REPLACE);
+  const bool vec4 = ((P.V & 3) == 0);
+  int cur = 0, alpha = 0;
+  bool stop = false;
+  if (writer && tid == 0) o_nodes[0] = 0;
+
+  while (true) {
+    // No CTA may still read our slices (DSMEM) when we overwrite them.
+    cluster.sync();
+    if (tid == 0) {
+      int c = 0;
+      for (int i = cur + 1; i < n; ++i)
+        if (s_par[i] == cur) s_kids[c++] = i;
+      s_nk = c;
+    }
+    __syncthreads();
+    const int nk = s_nk;
+    int prow = -1;
+    if (nk > 0) {
+      prow = P.p_row_of_node[t0 + s_kids[0]];
+      if (prow < 0 || prow >= P.R) {  // uniform
+        if (writer && tid == 0) fail(P.status, EAGLE_ERR_INVALID_ARG);
+        stop = true;
+        break;
+      }
+    }
+    // Stage this CTA's slice of q[cur] (and of the draft row) in shared memory.
+    {
+      const float* qrow = P.q + (size_t)(t0 + cur) * P.V + v0;
+      const float* prw = P.p_rows + (size_t)max(prow, 0) * P.V + v0;
+      int bad = 0;
+      if (vec4) {
+        const int n4 = nv >> 2;
+        const float4* q4 = reinterpret_cast<const float4*>(qrow);
+        const float4* p4 = reinterpret_cast<const float4*>(prw);
+        for (int i = tid; i < n4; i += blockDim.x) {
+          const float4 a = __ldg(q4 + i);
+          reinterpret_cast<float4*>(qs)[i] = a;
+          bad |= !(is_prob(a.x) && is_prob(a.y) && is_prob(a.z) && is_prob(a.w));
+          if (nk > 0) {
+            const float4 c = __ldg(p4 + i);
+            reinterpret_cast<float4*>(ps)[i] = c;
+            bad |= !(is_prob(c.x) && is_prob(c.y) && is_prob(c.z) && is_prob(c.w));
+          }
+        }
+      } else {
+        for (int i = tid; i < nv; i += blockDim.x) {
+          const float a = qrow[i];
+          qs[i] = a;
+          bad |= !is_prob(a);
+          if (nk > 0) {
+            const float c = prw[i];
+            ps[i] = c;
+            bad |= !is_prob(c);
+          }
+        }
+      }
+      if (__syncthreads_or(bad) && tid == 0) fail(P.status, EAGLE_ERR_NUMERIC);
+    }
+
+    bool moved = false;
+    for (int j = 0; j < nk; ++j) {
+      const int c = s_kids[j];
+      const int t = s_tok[c];
+      cluster.sync();  // every slice holds round-k values
+      const unsigned owner = (unsigned)(t / P.slice);
+      const int off = t - (int)owner * P.slice;
+      const float qt = *cluster.map_shared_rank(qs + off, owner);
+      const float pt = *cluster.map_shared_rank(ps + off, owner);
+      const float ua = P.u_accept[t0 + c];
+      if (!(ua >= 0.f && ua < 1.f) && writer && tid == 0) fail(P.status, EAGLE_ERR_INVALID_ARG);
+      // exact: a product of two fp32 values is exact in fp64
+      const bool accept = (double)ua * (double)pt < (double)qt;
+      if (accept) {
+        if (alpha + 1 > P.max_depth) {
+          if (writer && tid == 0) fail(P.status, EAGLE_ERR_INVALID_ARG);
+          stop = true;
+          break;
+        }
+        if (writer && tid == 0) {
+          o_tok[alpha] = t;
+          o_nodes[alpha + 1] = c;
+        }
+        ++alpha;
+        cur = c;
+        moved = true;
+        break;
+      }
+      // rejected: integer normalisers of the residual (and of the draft row)
+      unsigned long long sw = 0, sp = 0;
+      for (int i = tid; i < nv; i += blockDim.x) {
+        const float qa = qs[i], pa = ps[i];
+        sw += fixed40(fmaxf(0.f, __fsub_rn(qa, pa)));
+        if (no_replace && v0 + i != t) sp += fixed40(pa);
+      }
+      sw = block_sum_u64(sw, s_red);
+      if (no_replace) sp = block_sum_u64(sp, s_red);
+      if (tid == 0) {
+        s_w = sw;
+        s_p = sp;
+      }
+      cluster.sync();
+      const unsigned long long Z = cluster_sum(cluster, &s_w, CS, CS, &s_bc0);
+      const unsigned long long SP = no_replace ? cluster_sum(cluster, &s_p, CS, CS, &s_bc1) : 0ull;
+      const float Zf = __ull2float_rn(Z);
+      const float SPf = __ull2float_rn(SP);
+      for (int i = tid; i < nv; i += blockDim.x) {
+        const float qa = qs[i], pa = ps[i];
+        if (Z > 0ull)
+          qs[i] = __fdiv_rn(__ull2float_rn(fixed40(fmaxf(0.f, __fsub_rn(qa, pa)))), Zf);
+        if (no_replace) {
+          const unsigned long long Pj = (v0 + i == t) ? 0ull : fixed40(pa);
+          ps[i] = (SP > 0ull) ? __fdiv_rn(__ull2float_rn(Pj), SPf) : 0.f;
+        }
+      }
+    }
+    if (moved) continue;
+    if (stop) break;
+
+    // Bonus token: inverse CDF of the current q over integer weights.
+    cluster.sync();  // updated slices complete
+    {
+      const int per = (nv + (int)blockDim.x - 1) / (int)blockDim.x;
+      const int c0 = min(nv, tid * per), c1 = min(nv, c0 + per);
+      unsigned long long mine = 0;
+      for (int i = c0; i < c1; ++i) mine += fixed40(qs[i]);
+      unsigned long long cta_total;
+      const unsigned long long excl = block_excl_scan_u64(mine, s_red, &cta_total);
+      if (tid == 0) s_tot = cta_total;
+      cluster.sync();
+      const unsigned long long before = cluster_sum(cluster, &s_tot, CS, rank, &s_bc0);
+      const unsigned long long Z = cluster_sum(cluster, &s_tot, CS, CS, &s_bc1);
+      const float us = P.u_sample[t0 + cur];
+      if (!(us >= 0.f && us < 1.f)) {
+        if (writer && tid == 0) fail(P.status, EAGLE_ERR_INVALID_ARG);
+      } else if (Z == 0ull) {
+        if (writer && tid == 0) fail(P.status, EAGLE_ERR_NUMERIC);
+      } else {
+        const unsigned long long U = (unsigned long long)__float2uint_rz(us * kTwo24);
+        const unsigned long long lo = U * Z;
+        const unsigned long long hi = __umul64hi(U, Z);
+        const unsigned long long target = (hi << 40) | (lo >> 24);
+        if (target >= before && target < before + cta_total) {
+          const unsigned long long local = target - before;
+          if (local >= excl && local < excl + mine) {
+            unsigned long long acc = excl;
+            for (int i = c0; i < c1; ++i) {
+              acc += fixed40(qs[i]);
+              if (acc > local) {
+                o_tok[alpha] = v0 + i;
+                break;
+              }
+            }
+          }
+        }
+      }
+    }
+    break;
+  }
+  if (writer && tid == 0) P.accept_len[b] = alpha;
+  // Keep this CTA's shared memory alive until every DSMEM read has finished.
+  cluster.sync();
+}
+
+// Largest cluster the device can co-schedule for this kernel and smem size.
+int pick_cluster(int V, int max_nodes, int* slice_out, size_t* smem_out) {
+  const size_t node_bytes = (size_t)max_nodes * 3 * sizeof(int);
+  const size_t budget = 200 * 1024;
+  for (int cs = 1; cs <= 16; cs <<= 1) {
+    int slice = (V + cs - 1) / cs;
+    slice = (slice + 3) & ~3;
+    const size_t smem = (size_t)slice * 2 * sizeof(float) + node_bytes;
+    // prefer slices of <= 8K floats (64 KB): up to three CTAs per SM
+    if (cs < 16 && slice > 8192) continue;
+    if (smem > budget) return -1;
+    *slice_out = slice;
+    *smem_out = smem;
+    return cs;
+  }
+  return -1;
+}
+
+}  // namespace
+
+extern "C" eagle_status eagle_accept_greedy(int B, int max_nodes, const int32_t* d_tree_off,
+                                            const int32_t* d_parent, const int32_t* d_tokens,
+                                            const int32_t* d_argmax, int max_depth,
+                                            int32_t* d_accept_len, int32_t* d_accepted_nodes,
+                                            int32_t* d_out_tokens, int* d_status,
+                                            eagle_stream_t stream) {
+  EAGLE_HOST_CHECK(B >= 0 && max_depth >= 0, EAGLE_ERR_INVALID_ARG);
+  EAGLE_HOST_CHECK(max_nodes >= 1 && max_nodes <= EAGLE_MAX_TREE_NODES, EAGLE_ERR_UNSUPPORTED);
+  if (B == 0) return EAGLE_OK;
+  EAGLE_HOST_CHECK(d_tree_off && d_parent && d_tokens && d_argmax && d_accept_len &&
+                       d_accepted_nodes && d_out_tokens && d_status,
+                   EAGLE_ERR_INVALID_ARG);
+  const size_t smem = (size_t)max_nodes * 2 * sizeof(int);
+  accept_greedy_kernel<<<B, 32, smem, (cudaStream_t)stream>>>(
+      max_nodes, d_tree_off, d_parent, d_tokens, d_argmax, max_depth, d_accept_len,
+      d_accepted_nodes, d_out_tokens, d_status);
+  return launch_status(cudaGetLastError());
+}
+
+extern "C" eagle_status eagle_accept_stochastic(
+    int B, int max_nodes, int V, int R, int mode, const int32_t* d_tree_off,
+    const int32_t* d_parent, const int32_t* d_tokens, const float* d_q, const float* d_p_rows,
+    const int32_t* d_p_row_of_node, const float* d_u_accept, const float* d_u_sample,
+    int max_depth, int32_t* d_accept_len, int32_t* d_accepted_nodes, int32_t* d_out_tokens,
+    int* d_status, eagle_stream_t stream) {
+  EAGLE_HOST_CHECK(B >= 0 && V >= 1 && R >= 0 && max_depth >= 0, EAGLE_ERR_INVALID_ARG);
+  EAGLE_HOST_CHECK(mode == EAGLE_SAMPLE_REPLACE || mode == EAGLE_SAMPLE_NO_REPLACE,
+                   EAGLE_ERR_INVALID_ARG);
+  EAGLE_HOST_CHECK(max_nodes >= 1 && max_nodes <= EAGLE_MAX_TREE_NODES, EAGLE_ERR_UNSUPPORTED);
+  if (B == 0) return EAGLE_OK;
+  EAGLE_HOST_CHECK(d_tree_off && d_parent && d_tokens && d_q && d_u_accept && d_u_sample &&
+                       d_p_row_of_node && d_accept_len && d_accepted_nodes && d_out_tokens &&
+                       d_status,
+                   EAGLE_ERR_INVALID_ARG);
+  EAGLE_HOST_CHECK(R == 0 || d_p_rows, EAGLE_ERR_INVALID_ARG);
+  EAGLE_HOST_CHECK(((V & 3) != 0) ||
+                       ((((uintptr_t)d_q) & 15) == 0 && (((uintptr_t)d_p_rows) & 15) == 0),
+                   EAGLE_ERR_INVALID_ARG);
+  int slice = 0;
+  size_t smem = 0;
+  const int cs = pick_cluster(V, max_nodes, &slice, &smem);
+  EAGLE_HOST_CHECK(cs > 0, EAGLE_ERR_UNSUPPORTED);
+  static bool attr_done = false;
+  if (!attr_done) {
+    cudaFuncSetAttribute(accept_stochastic_kernel, cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
+    cudaFuncSetAttribute(accept_stochastic_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                         200 * 1024);
+    attr_done = true;
+  }
+  StochParams P;
+  P.max_nodes = max_nodes;
+  P.V = V;
+  P.R = R;
+  P.mode = mode;
+  P.max_depth = max_depth;
+  P.slice = slice;
+  P.tree_off = d_tree_off;
+  P.parent = d_parent;
+  P.tokens = d_tokens;
+  P.q = d_q;
+  P.p_rows = d_p_rows;
+  P.p_row_of_node = d_p_row_of_node;
+  P.u_accept = d_u_accept;
+  P.u_sample = d_u_sample;
+  P.accept_len = d_accept_len;
+  P.accepted_nodes = d_accepted_nodes;
+  P.out_tokens = d_out_tokens;
+  P.status = d_status;
+
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3((unsigned)(B * cs), 1, 1);
+  cfg.blockDim = dim3(kStochThreads, 1, 1);
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = (cudaStream_t)stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeClusterDimension;
+  attr[0].val.clusterDim.x = (unsigned)cs;
+  attr[0].val.clusterDim.y = 1;
+  attr[0].val.clusterDim.z = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return launch_status(cudaLaunchKernelEx(&cfg, accept_stochastic_kernel, P));
+}

@@ -1,0 +1,67 @@
+// Shared device/host helpers of the tree-verify kernels (sm_103a).
+#pragma once
+
+#include <cuda_runtime.h>
+#include <cuda_bf16.h>
+#include <stdint.h>
+
+#include "../../include/eagle.h"
+
+#define EAGLE_HOST_CHECK(cond, code) \
+  do {                               \
+    if (!(cond)) return (code);      \
+  } while (0)
+
+namespace eagle {
+
+// Record the first device-side error of a call.
+__device__ __forceinline__ void fail(int* status, int code) {
+  if (status) atomicCAS(status, 0, code);
+}
+
+__device__ __forceinline__ float to_f32(float x) { return x; }
+__device__ __forceinline__ float to_f32(__nv_bfloat16 x) { return __bfloat162float(x); }
+
+// Total order on fp32 values as unsigned ints: larger float -> larger key.
+// -0 is folded onto +0 so that equal values compare equal.
+__device__ __forceinline__ uint32_t ordered_bits(float f) {
+  uint32_t b = __float_as_uint(f + 0.0f);
+  return (b & 0x80000000u) ? ~b : (b | 0x80000000u);
+}
+__device__ __forceinline__ float from_ordered_bits(uint32_t o) {
+  uint32_t b = (o & 0x80000000u) ? (o & 0x7fffffffu) : ~o;
+  return __uint_as_float(b);
+}
+
+// Key for "value descending, then index ascending" selection as a max.
+__device__ __forceinline__ unsigned long long desc_key(float v, uint32_t idx) {
+  return ((unsigned long long)ordered_bits(v) << 32) | (unsigned long long)(0xffffffffu - idx);
+}
+__device__ __forceinline__ uint32_t key_index(unsigned long long k) {
+  return 0xffffffffu - (uint32_t)(k & 0xffffffffull);
+}
+__device__ __forceinline__ float key_value(unsigned long long k) {
+  return from_ordered_bits((uint32_t)(k >> 32));
+}
+
+__device__ __forceinline__ unsigned long long warp_max_u64(unsigned long long v) {
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) {
+    unsigned long long w = __shfl_xor_sync(0xffffffffu, v, o);
+    v = w > v ? w : v;
+  }
+  return v;
+}
+__device__ __forceinline__ unsigned long long warp_sum_u64(unsigned long long v) {
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
+  return v;
+}
+
+inline eagle_status launch_status(cudaError_t e) {
+  return e == cudaSuccess ? EAGLE_OK : EAGLE_ERR_CUDA;
+}
+
+inline int ceil_div(long long a, long long b) { return (int)((a + b - 1) / b); }
+
+}  // namespace eagle

@@ -1,0 +1,405 @@
+// EAGLE-2 dynamic draft tree: expand (per-node top-k, cumulative scores,
+// beam frontier) and finalize (global top-budget rerank).
+// [EAGLE-2] §2 "EAGLE-2 的核心創新：動態草稿樹" items 1-3 (page title in
+// include/eagle.h): confidence per draft node, adaptive expansion, greedy
+// selection under a fixed draft-token budget.  A node's value is its
+// cumulative draft log-prob.
+//
+// One launch per level.  Every draft row is split into chunks spread over
+// the whole GPU (the rows are the only large data: F x V fp32 per level);
+// each CTA selects its chunk's top-k, the last CTA of a row (atomic ticket,
+// no waiting) merges the row, and the last row of a sequence builds the
+// children and the next frontier.  Selection keys are 64-bit integers
+// (ordered value bits | inverted index), so every tie rule is a plain max.
+#include <algorithm>
+
+#include "common.cuh"
+
+using namespace eagle;
+
+namespace {
+
+constexpr int kExpandThreads = 256;
+constexpr int kChunkMax = 8192;     // floats staged per CTA
+constexpr int kFinalThreads = 512;
+
+struct PoolLayout {
+  int P;         // candidate capacity per sequence
+  int rows_max;  // B * k
+  int S0, S1;    // chunks per row at level 0 / later levels
+  size_t off_row_cnt, off_seq_cnt, off_count, off_frontier, off_token, off_parent, off_depth,
+      off_prow, off_score, off_rowtop, off_partial, total;
+};
+
+int chunks_for(int rows, int V) {
+  int s = (304 + rows - 1) / rows;                 // ~2 CTAs per SM in total
+  s = std::max(s, (V + kChunkMax - 1) / kChunkMax);  // chunk fits in smem
+  s = std::min(s, std::max(1, V / 512));             // chunks of >= 512 tokens
+  return std::max(s, 1);
+}
+
+size_t align256(size_t x) { return (x + 255) & ~(size_t)255; }
+
+PoolLayout pool_layout(int B, int k, int depth, int V) {
+  PoolLayout L;
+  L.P = k + (depth - 1) * k * k;
+  L.rows_max = B * k;
+  L.S0 = chunks_for(B, V);
+  L.S1 = chunks_for(B * k, V);
+  const size_t parts = std::max((size_t)B * L.S0, (size_t)B * k * L.S1) * k;
+  size_t o = 0;
+  auto take = [&](size_t bytes) {
+    size_t at = o;
+    o = align256(o + bytes);
+    return at;
+  };
+  L.off_row_cnt = take((size_t)L.rows_max * 4);
+  L.off_seq_cnt = take((size_t)B * 4);
+  L.off_count = take((size_t)B * 4);
+  L.off_frontier = take((size_t)B * k * 4);
+  L.off_token = take((size_t)B * L.P * 4);
+  L.off_parent = take((size_t)B * L.P * 4);
+  L.off_depth = take((size_t)B * L.P * 4);
+  L.off_prow = take((size_t)B * L.P * 4);
+  L.off_score = take((size_t)B * L.P * 4);
+  L.off_rowtop = take((size_t)L.rows_max * k * 8);
+  L.off_partial = take(parts * 8);
+  L.total = o;
+  return L;
+}
+
+struct PoolPtrs {
+  int* row_cnt;
+  int* seq_cnt;
+  int* count;
+  int* frontier;
+  int* token;
+  int* parent;
+  int* depth;
+  int* prow;
+  float* score;
+  unsigned long long* rowtop;
+  unsigned long long* partial;
+};
+
+PoolPtrs pool_ptrs(void* base, const PoolLayout& L) {
+  char* c = static_cast<char*>(base);
+  PoolPtrs p;
+  p.row_cnt = reinterpret_cast<int*>(c + L.off_row_cnt);
+  p.seq_cnt = reinterpret_cast<int*>(c + L.off_seq_cnt);
+  p.count = reinterpret_cast<int*>(c + L.off_count);
+  p.frontier = reinterpret_cast<int*>(c + L.off_frontier);
+  p.token = reinterpret_cast<int*>(c + L.off_token);
+  p.parent = reinterpret_cast<int*>(c + L.off_parent);
+  p.depth = reinterpret_cast<int*>(c + L.off_depth);
+  p.prow = reinterpret_cast<int*>(c + L.off_prow);
+  p.score = reinterpret_cast<float*>(c + L.off_score);
+  p.rowtop = reinterpret_cast<unsigned long long*>(c + L.off_rowtop);
+  p.partial = reinterpret_cast<unsigned long long*>(c + L.off_partial);
+  return p;
+}
+
+// Block-wide max of one key per thread (every thread gets it).
+__device__ unsigned long long block_max_u64(unsigned long long v, unsigned long long* s_tmp) {
+  v = warp_max_u64(v);
+  const int w = threadIdx.x >> 5, l = threadIdx.x & 31;
+  __syncthreads();
+  if (l == 0) s_tmp[w] = v;
+  __syncthreads();
+  if (w == 0) {
+    unsigned long long t = (l < (int)(blockDim.x >> 5)) ? s_tmp[l] : 0ull;
+    t = warp_max_u64(t);
+    if (l == 0) s_tmp[32] = t;
+  }
+  __syncthreads();
+  return s_tmp[32];
+}
+
+struct LevelParams {
+  int B, V, k, F, R, S, level, P;
+  const float* logp;
+  PoolPtrs pool;
+  int* status;
+};
+
+__global__ void __launch_bounds__(kExpandThreads) expand_level_kernel(const LevelParams A) {
+  __shared__ float s_val[kChunkMax];
+  __shared__ unsigned long long s_tmp[33];
+  __shared__ unsigned long long s_sel[EAGLE_MAX_TOPK];
+  __shared__ unsigned long long s_cand[EAGLE_MAX_TOPK * EAGLE_MAX_TOPK];
+  __shared__ int s_last;
+
+  const int tid = threadIdx.x;
+  const int row = blockIdx.x / A.S;       // global frontier row: b * F + f
+  const int chunk = blockIdx.x % A.S;
+  const int b = row / A.F;
+  const int f = row % A.F;
+  const int local_row = (A.level == 0) ? 0 : 1 + (A.level - 1) * A.k + f;
+  const float* src = A.logp + ((size_t)b * A.R + local_row) * A.V;
+  const int csize = (A.V + A.S - 1) / A.S;
+  const int c0 = min(A.V, chunk * csize), c1 = min(A.V, c0 + csize);
+  const int n = c1 - c0;
+  const int k = A.k;
+
+  // ---- stage the chunk, checking for non-finite values
+  int bad = 0;
+  for (int i = tid; i < n; i += blockDim.x) {
+    const float x = src[c0 + i];
+    s_val[i] = x;
+    bad |= !isfinite(x);
+  }
+  if (__syncthreads_or(bad) && tid == 0) fail(A.status, EAGLE_ERR_NUMERIC);
+
+  // ---- chunk top-k: k rounds of a block max below the previous pick
+  unsigned long long last = ~0ull;
+  for (int r = 0; r < k; ++r) {
+    unsigned long long best = 0ull;
+    for (int i = tid; i < n; i += blockDim.x) {
+      const unsigned long long key = desc_key(s_val[i], (uint32_t)(c0 + i));
+      if (key < last && key > best) best = key;
+    }
+    best = block_max_u64(best, s_tmp);
+    if (tid == 0) s_sel[r] = best;  // 0 = no element left
+    last = best;
+  }
+  __syncthreads();
+  unsigned long long* part = A.pool.partial + ((size_t)row * A.S + chunk) * k;
+  for (int r = tid; r < k; r += blockDim.x) part[r] = s_sel[r];
+
+  // ---- last CTA of this row merges the chunk results
+  __threadfence();
+  __syncthreads();
+  if (tid == 0) {
+    const int prev = atomicAdd(&A.pool.row_cnt[row], 1);
+    s_last = (prev == A.S - 1);
+    if (s_last) A.pool.row_cnt[row] = 0;  // ready for the next level
+  }
+  __syncthreads();
+  if (!s_last) return;
+  __threadfence();
+  const unsigned long long* rparts = A.pool.partial + (size_t)row * A.S * k;
+  const int m = A.S * k;
+  last = ~0ull;
+  for (int r = 0; r < k; ++r) {
+    unsigned long long best = 0ull;
+    for (int i = tid; i < m; i += blockDim.x) {
+      const unsigned long long key = __ldcg(rparts + i);
+      if (key < last && key > best) best = key;
+    }
+    best = block_max_u64(best, s_tmp);
+    if (tid == 0) s_sel[r] = best;
+    last = best;
+  }
+  __syncthreads();
+  for (int r = tid; r < k; r += blockDim.x) A.pool.rowtop[(size_t)row * k + r] = s_sel[r];
+
+  // ---- last row of this sequence builds the children and the frontier
+  __threadfence();
+  __syncthreads();
+  if (tid == 0) {
+    const int prev = atomicAdd(&A.pool.seq_cnt[b], 1);
+    s_last = (prev == A.F - 1);
+    if (s_last) A.pool.seq_cnt[b] = 0;
+  }
+  __syncthreads();
+  if (!s_last) return;
+  __threadfence();
+  const int nc = A.F * k;  // children in creation order (f-major, rank-minor)
+  const int base = A.pool.count[b];
+  int* tok = A.pool.token + (size_t)b * A.P;
+  int* par = A.pool.parent + (size_t)b * A.P;
+  int* dep = A.pool.depth + (size_t)b * A.P;
+  int* prw = A.pool.prow + (size_t)b * A.P;
+  float* sco = A.pool.score + (size_t)b * A.P;
+  int* front = A.pool.frontier + (size_t)b * k;
+  for (int c = tid; c < nc; c += blockDim.x) {
+    const int ff = c / k, rr = c % k;
+    const unsigned long long key = __ldcg(A.pool.rowtop + ((size_t)(b * A.F + ff)) * k + rr);
+    const int pidx = (A.level == 0) ? -1 : __ldcg(front + ff);
+    const float pscore = (A.level == 0) ? 0.f : __ldcg(sco + pidx);
+    const float s = __fadd_rn(pscore, key_value(key));
+    const int at = base + c;
+    tok[at] = (int)key_index(key);
+    par[at] = pidx;
+    dep[at] = A.level + 1;
+    prw[at] = (A.level == 0) ? 0 : 1 + (A.level - 1) * k + ff;
+    sco[at] = s;
+    s_cand[c] = desc_key(s, (uint32_t)c);
+  }
+  __syncthreads();
+  // next frontier: rank of every child by (score desc, creation order)
+  for (int c = tid; c < nc; c += blockDim.x) {
+    const unsigned long long me = s_cand[c];
+    int rank = 0;
+    for (int j = 0; j < nc; ++j) rank += (s_cand[j] > me);
+    if (rank < k) front[rank] = base + c;
+  }
+  if (tid == 0) A.pool.count[b] = base + nc;
+}
+
+struct FinalParams {
+  int B, k, R, P;
+  const int* budget;
+  const int* root_token;
+  PoolPtrs pool;
+  int* tree_off;
+  int* parent;
+  int* tokens;
+  int* node_depth;
+  float* score;
+  int* p_row_of_node;
+  int* status;
+};
+
+__global__ void __launch_bounds__(kFinalThreads) expand_finalize_kernel(const FinalParams A) {
+  extern __shared__ __align__(16) unsigned char smem_raw[];
+  unsigned long long* s_key = reinterpret_cast<unsigned long long*>(smem_raw);
+  int* s_dep = reinterpret_cast<int*>(s_key + A.P);
+  int* s_sel = s_dep + A.P;
+  int* s_node = s_sel + A.P;
+  __shared__ int s_off, s_keep;
+  const int b = blockIdx.x;
+  const int tid = threadIdx.x;
+  const int n = A.pool.count[b];
+  if (tid == 0) {
+    int off = 0;
+    for (int j = 0; j < b; ++j) off += min(max(A.budget[j], 0), A.pool.count[j]) + 1;
+    s_off = off;
+    const int bud = A.budget[b];
+    if (bud < 0) fail(A.status, EAGLE_ERR_INVALID_ARG);
+    s_keep = min(max(bud, 0), n);
+    A.tree_off[b] = off;
+    if (b == A.B - 1) A.tree_off[A.B] = off + s_keep + 1;
+  }
+  const int* tok = A.pool.token + (size_t)b * A.P;
+  const int* par = A.pool.parent + (size_t)b * A.P;
+  const int* dep = A.pool.depth + (size_t)b * A.P;
+  const int* prw = A.pool.prow + (size_t)b * A.P;
+  const float* sco = A.pool.score + (size_t)b * A.P;
+  for (int i = tid; i < n; i += blockDim.x) {
+    s_key[i] = desc_key(sco[i], (uint32_t)i);
+    s_dep[i] = dep[i];
+  }
+  __syncthreads();
+  const int keep = s_keep, off = s_off;
+  // selection: the `keep` largest keys (score desc, creation order)
+  for (int i = tid; i < n; i += blockDim.x) {
+    const unsigned long long me = s_key[i];
+    int rank = 0;
+    for (int j = 0; j < n; ++j) rank += (s_key[j] > me);
+    s_sel[i] = (rank < keep);
+  }
+  __syncthreads();
+  // numbering of the kept nodes by (depth, score desc, creation order)
+  for (int i = tid; i < n; i += blockDim.x) {
+    if (!s_sel[i]) {
+      s_node[i] = -1;
+      continue;
+    }
+    const unsigned long long me = s_key[i];
+    const int d = s_dep[i];
+    int rank = 0;
+    for (int j = 0; j < n; ++j)
+      if (s_sel[j]) rank += (s_dep[j] < d) || (s_dep[j] == d && s_key[j] > me);
+    s_node[i] = 1 + rank;
+  }
+  __syncthreads();
+  for (int i = tid; i < n; i += blockDim.x) {
+    const int node = s_node[i];
+    if (node < 0) continue;
+    const int pp = par[i];
+    const int pnode = (pp < 0) ? 0 : s_node[pp];
+    if (pnode < 0) fail(A.status, EAGLE_ERR_INVALID_TREE);  // not parent-closed
+    const int at = off + node;
+    A.parent[at] = pnode;
+    A.tokens[at] = tok[i];
+    A.node_depth[at] = s_dep[i];
+    A.score[at] = sco[i];
+    A.p_row_of_node[at] = b * A.R + prw[i];
+  }
+  if (tid == 0) {
+    A.parent[off] = -1;
+    A.tokens[off] = A.root_token ? A.root_token[b] : -1;
+    A.node_depth[off] = 0;
+    A.score[off] = 0.f;
+    A.p_row_of_node[off] = -1;
+  }
+}
+
+}  // namespace
+
+extern "C" size_t eagle_draft_pool_bytes(int B, int k, int depth, int V) {
+  if (B < 1 || k < 1 || k > EAGLE_MAX_TOPK || depth < 1 || depth > EAGLE_MAX_DEPTH || V < k)
+    return 0;
+  return pool_layout(B, k, depth, V).total;
+}
+
+extern "C" eagle_status eagle_draft_expand(int B, int V, int k, int depth, int level,
+                                           int finalize, const float* d_draft_logp,
+                                           const int32_t* d_budget, const int32_t* d_root_token,
+                                           void* d_pool, size_t pool_bytes, int32_t* d_tree_off,
+                                           int32_t* d_parent, int32_t* d_tokens,
+                                           int32_t* d_node_depth, float* d_score,
+                                           int32_t* d_p_row_of_node, int* d_status,
+                                           eagle_stream_t stream) {
+  EAGLE_HOST_CHECK(B >= 1 && V >= 1, EAGLE_ERR_INVALID_ARG);
+  EAGLE_HOST_CHECK(k >= 1 && k <= EAGLE_MAX_TOPK && k <= V, EAGLE_ERR_UNSUPPORTED);
+  EAGLE_HOST_CHECK(depth >= 1 && depth <= EAGLE_MAX_DEPTH, EAGLE_ERR_UNSUPPORTED);
+  EAGLE_HOST_CHECK(d_pool && d_status, EAGLE_ERR_INVALID_ARG);
+  const PoolLayout L = pool_layout(B, k, depth, V);
+  EAGLE_HOST_CHECK(pool_bytes >= L.total, EAGLE_ERR_WORKSPACE);
+  EAGLE_HOST_CHECK(((uintptr_t)d_pool & 255) == 0, EAGLE_ERR_INVALID_ARG);
+  const PoolPtrs pp = pool_ptrs(d_pool, L);
+  cudaStream_t s = (cudaStream_t)stream;
+  const int R = 1 + (depth - 1) * k;
+  if (!finalize) {
+    EAGLE_HOST_CHECK(level >= 0 && level < depth, EAGLE_ERR_INVALID_ARG);
+    EAGLE_HOST_CHECK(d_draft_logp, EAGLE_ERR_INVALID_ARG);
+    if (level == 0) {
+      // fresh tree: zero the tickets and the pool fill counts
+      cudaError_t e = cudaMemsetAsync(static_cast<char*>(d_pool), 0, L.off_frontier, s);
+      if (e != cudaSuccess) return EAGLE_ERR_CUDA;
+    }
+    LevelParams A;
+    A.B = B;
+    A.V = V;
+    A.k = k;
+    A.F = (level == 0) ? 1 : k;
+    A.R = R;
+    A.S = (level == 0) ? L.S0 : L.S1;
+    A.level = level;
+    A.P = L.P;
+    A.logp = d_draft_logp;
+    A.pool = pp;
+    A.status = d_status;
+    const int grid = B * A.F * A.S;
+    expand_level_kernel<<<grid, kExpandThreads, 0, s>>>(A);
+    return launch_status(cudaGetLastError());
+  }
+  EAGLE_HOST_CHECK(d_budget && d_tree_off && d_parent && d_tokens && d_node_depth && d_score &&
+                       d_p_row_of_node,
+                   EAGLE_ERR_INVALID_ARG);
+  FinalParams F;
+  F.B = B;
+  F.k = k;
+  F.R = R;
+  F.P = L.P;
+  F.budget = d_budget;
+  F.root_token = d_root_token;
+  F.pool = pp;
+  F.tree_off = d_tree_off;
+  F.parent = d_parent;
+  F.tokens = d_tokens;
+  F.node_depth = d_node_depth;
+  F.score = d_score;
+  F.p_row_of_node = d_p_row_of_node;
+  F.status = d_status;
+  const size_t smem = (size_t)L.P * (8 + 4 + 4 + 4);
+  EAGLE_HOST_CHECK(smem <= 200 * 1024, EAGLE_ERR_UNSUPPORTED);
+  if (smem > 48 * 1024) {
+    cudaFuncSetAttribute(expand_finalize_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                         (int)smem);
+  }
+  expand_finalize_kernel<<<B, kFinalThreads, smem, s>>>(F);
+  return launch_status(cudaGetLastError());
+}

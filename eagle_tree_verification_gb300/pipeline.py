@@ -1,0 +1,192 @@
+"""One tree-verify step on the GPU: device buffers + the launch sequence.
+
+    draft tree   eagle_draft_expand (levels 0..depth-1, then finalize)
+                 -- or a caller-given tree (parent/tokens/p_row_of_node)
+    attention    eagle_tree_attn
+    LM head      eagle_lmhead_softmax (greedy: no [T,V] output; stochastic:
+                 writes q)
+    acceptance   eagle_accept_greedy | eagle_accept_stochastic
+
+Every launch goes through the C ABI on one stream with no host
+synchronisation, so `run()` can be captured into a CUDA graph (`capture()`).
+Sizes that decide grids (T, max_nodes, max_kv) are known on the host from
+the budgets and cache lengths; the kernels read the exact extents from the
+device offset arrays.
+"""
+from __future__ import annotations
+
+import dataclasses
+from typing import Dict, Optional, Sequence
+
+from . import (SAMPLE_NO_REPLACE, eagle_accept_greedy, eagle_accept_stochastic,
+               eagle_draft_expand, eagle_draft_pool_bytes, eagle_lmhead_softmax,
+               eagle_lmhead_workspace_bytes, eagle_tree_attn, eagle_tree_attn_workspace_bytes)
+
+
+@dataclasses.dataclass
+class StepShape:
+    B: int
+    Hq: int
+    Hkv: int
+    D: int
+    H: int
+    V: int
+    L: Sequence[int]                 # KV-cache length per sequence
+    n_nodes: Sequence[int]           # tree nodes per sequence, root included
+    rows: int                        # draft-distribution rows (all sequences)
+    max_depth: int
+    dtype: str = "bf16"              # "bf16" or "f32"
+    mode: str = "greedy"             # "greedy" or "stochastic"
+    temperature: float = 1.0
+    sample_mode: int = SAMPLE_NO_REPLACE
+    # EAGLE-2 tree build (k == 0: the caller supplies the tree)
+    k: int = 0
+    depth: int = 0
+    budget: Sequence[int] = ()
+
+    @property
+    def T(self) -> int:
+        return int(sum(self.n_nodes))
+
+
+class TreeVerifyStep:
+    """Owns the device tensors of one step and launches it."""
+
+    def __init__(self, shape: StepShape, device: str = "cuda"):
+        import torch
+        self.torch = torch
+        self.s = shape
+        s = shape
+        dev = torch.device(device)
+        dt = torch.bfloat16 if s.dtype == "bf16" else torch.float32
+        i32, f32 = torch.int32, torch.float32
+        T, sumL = s.T, int(sum(s.L))
+        self.max_nodes = int(max(s.n_nodes))
+        self.max_kv = int(max(s.L)) if len(s.L) else 0
+        z = lambda *shape_, dtype=f32: torch.zeros(shape_, dtype=dtype, device=dev)
+        # inputs
+        self.q = z(T, s.Hq, s.D, dtype=dt)
+        self.k_tree = z(T, s.Hkv, s.D, dtype=dt)
+        self.v_tree = z(T, s.Hkv, s.D, dtype=dt)
+        self.k_cache = z(max(sumL, 1), s.Hkv, s.D, dtype=dt)
+        self.v_cache = z(max(sumL, 1), s.Hkv, s.D, dtype=dt)
+        self.kv_off = z(s.B + 1, dtype=i32)
+        self.h = z(T, s.H, dtype=dt)
+        self.w_lm = z(s.V, s.H, dtype=dt)
+        self.p_rows = z(max(s.rows, 1), s.V)
+        self.draft_logp = z(max(s.rows, 1), s.V) if s.k else None
+        self.u_accept = z(T)
+        self.u_sample = z(T)
+        self.root_token = z(s.B, dtype=i32)
+        self.budget = z(s.B, dtype=i32)
+        # tree (written by the expand kernels, or loaded)
+        self.tree_off = z(s.B + 1, dtype=i32)
+        self.parent = z(T, dtype=i32)
+        self.tokens = z(T, dtype=i32)
+        self.node_depth = z(T, dtype=i32)
+        self.score = z(T)
+        self.p_row_of_node = z(T, dtype=i32)
+        self.pool = None
+        if s.k:
+            nbytes = eagle_draft_pool_bytes(s.B, s.k, s.depth, s.V)
+            if nbytes == 0:
+                raise ValueError("unsupported EAGLE-2 tree parameters")
+            self.pool = torch.zeros(nbytes, dtype=torch.uint8, device=dev)
+        # outputs / scratch
+        self.attn_out = z(T, s.Hq, s.D)
+        ws = eagle_tree_attn_workspace_bytes(s.B, T, s.Hq, s.Hkv, s.D, self.max_nodes, self.max_kv)
+        self.attn_ws = torch.zeros(max(ws, 16), dtype=torch.uint8, device=dev)
+        self.lm_ws = torch.zeros(max(eagle_lmhead_workspace_bytes(T, s.V), 16),
+                                 dtype=torch.uint8, device=dev)
+        self.argmax = z(T, dtype=i32)
+        self.row_max = z(T)
+        self.row_lse = z(T)
+        self.top2_gap = z(T)
+        self.q_prob = z(T, s.V) if s.mode == "stochastic" else None
+        W = s.max_depth + 1
+        self.accept_len = z(s.B, dtype=i32)
+        self.accepted_nodes = z(s.B, W, dtype=i32)
+        self.out_tokens = z(s.B, W, dtype=i32)
+        self.status = z(1, dtype=i32)
+
+    # ------------------------------------------------------------------
+    def load(self, arrays: Dict[str, object]) -> None:
+        """Copy host arrays (numpy or torch) into the device tensors with the
+        same names."""
+        torch = self.torch
+        for name, val in arrays.items():
+            t = getattr(self, name)
+            if t is None:
+                raise KeyError(f"{name} is not used by this step")
+            src = val if isinstance(val, torch.Tensor) else torch.from_numpy(val)
+            t.copy_(src.reshape(t.shape).to(t.dtype), non_blocking=False)
+
+    # ------------------------------------------------------------------
+    def run_expand(self, stream=None) -> None:
+        s = self.s
+        for lev in range(s.depth):
+            eagle_draft_expand(self.pool, self.status, B=s.B, V=s.V, k=s.k, depth=s.depth,
+                               level=lev, draft_logp=self.draft_logp, stream=stream)
+        eagle_draft_expand(self.pool, self.status, B=s.B, V=s.V, k=s.k, depth=s.depth,
+                           finalize=True, budget=self.budget, root_token=self.root_token,
+                           tree_off=self.tree_off, parent=self.parent, tokens=self.tokens,
+                           node_depth=self.node_depth, score=self.score,
+                           p_row_of_node=self.p_row_of_node, stream=stream)
+
+    def run_attn(self, stream=None) -> None:
+        eagle_tree_attn(self.q, self.k_tree, self.v_tree, self.k_cache, self.v_cache,
+                        self.kv_off, self.tree_off, self.parent, self.attn_out, self.status,
+                        max_nodes=self.max_nodes, max_kv=self.max_kv, ws=self.attn_ws,
+                        stream=stream)
+
+    def run_lmhead(self, stream=None) -> None:
+        eagle_lmhead_softmax(self.h, self.w_lm, self.argmax, self.row_max, self.row_lse,
+                             self.top2_gap, self.q_prob, self.lm_ws, self.status,
+                             temperature=self.s.temperature, stream=stream)
+
+    def run_accept(self, stream=None) -> None:
+        s = self.s
+        if s.mode == "greedy":
+            eagle_accept_greedy(self.tree_off, self.parent, self.tokens, self.argmax,
+                                self.accept_len, self.accepted_nodes, self.out_tokens,
+                                self.status, max_nodes=self.max_nodes, max_depth=s.max_depth,
+                                stream=stream)
+        else:
+            eagle_accept_stochastic(self.tree_off, self.parent, self.tokens, self.q_prob,
+                                    self.p_rows, self.p_row_of_node, self.u_accept,
+                                    self.u_sample, self.accept_len, self.accepted_nodes,
+                                    self.out_tokens, self.status, max_nodes=self.max_nodes,
+                                    max_depth=s.max_depth, mode=s.sample_mode, stream=stream)
+
+    def run(self, stream=None) -> None:
+        """The whole step: tree build (if EAGLE-2), attention, LM head, accept."""
+        if self.s.k:
+            self.run_expand(stream)
+        self.run_attn(stream)
+        self.run_lmhead(stream)
+        self.run_accept(stream)
+
+    def launches_per_step(self) -> int:
+        """Kernels launched by run() (the count the benchmark reports)."""
+        n = 0
+        if self.s.k:
+            n += self.s.depth + 1
+        n += 1                                   # attention
+        n += 2                                   # LM head tiles + finalize
+        n += 1                                   # acceptance
+        return n
+
+    def capture(self, stream=None):
+        """Capture run() into a CUDA graph (after one eager warm-up)."""
+        torch = self.torch
+        st = torch.cuda.Stream() if stream is None else stream
+        st.wait_stream(torch.cuda.current_stream())
+        with torch.cuda.stream(st):
+            self.run()
+        torch.cuda.current_stream().wait_stream(st)
+        torch.cuda.synchronize()
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g, stream=st):
+            self.run()
+        torch.cuda.synchronize()
+        return g

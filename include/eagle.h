@@ -1,0 +1,246 @@
+/*
+ * eagle.h -- C ABI of the EAGLE / EAGLE-2 tree-verify hot path on GB300
+ * (sm_103a).  One verify step is:
+ *
+ *   eagle_draft_expand   (every level, then finalize) -> draft tree
+ *   eagle_tree_attn      tree-masked attention of every tree node
+ *   eagle_lmhead_softmax LM-head logits, softmax statistics, argmax (and q)
+ *   eagle_accept_greedy  | eagle_accept_stochastic -> accepted tokens
+ *
+ * Sources, by page title and section:
+ *   [S4000]   大模型推理效率突破：EAGLE推测解码算法在摩尔线程GPU的实践与优化
+ *             (greedy-decoding and random-decoding paragraphs; "EAGLE的创新点"
+ *             list item 2, tree attention)
+ *   [EAGLE]   大模型推理效率无损提升3倍，滑铁卢大学、北京大学等机构发布EAGLE
+ *             (speculative-sampling paragraph; workflow paragraph; "树状生成结构";
+ *             "多轮投机采样")
+ *   [EAGLE-2] EAGLE-2：動態草稿樹讓 LLM 推論加速 4 倍而不失精度
+ *             (§2 "推測解碼的基礎原理"; §2 "EAGLE-2 的核心創新：動態草稿樹" items 1-3)
+ *
+ * Conventions shared by every entry point
+ *   - Pointers named d_* are DEVICE pointers, owned by the caller, and must
+ *     stay valid until the work queued on `stream` has finished.  The library
+ *     allocates no memory and keeps no per-call state; scratch space is passed
+ *     in by the caller (sizes from the *_bytes functions below).
+ *   - Every call is asynchronous on `stream` (a cudaStream_t; NULL means the
+ *     legacy default stream) and does no host synchronisation, so a whole step
+ *     can be captured in a CUDA graph.
+ *   - Host-checkable errors (NULL pointers, sizes out of range, unsupported
+ *     shapes) are returned at once and nothing is queued.  Errors that only
+ *     the device can see (malformed parent[] array, NaN/Inf or out-of-range
+ *     probabilities, index out of range) are written to *d_status (device
+ *     int, caller-zeroed; the first error code wins) and the outputs of that
+ *     sequence are unspecified.  A failed kernel launch returns
+ *     EAGLE_ERR_CUDA.
+ *   - Trees: nodes of sequence b are tree_off[b] .. tree_off[b+1]-1 of every
+ *     per-node array; parent[] holds LOCAL indices with parent[root] = -1 and
+ *     0 <= parent[i] < i for i > 0 (the root is local node 0).
+ *   - Row-major layouts everywhere; "[T,Hq,D]" means D is contiguous.
+ */
+#ifndef EAGLE_H_
+#define EAGLE_H_
+
+#include <stddef.h>
+#include <stdint.h>
+
+#if defined(__GNUC__)
+#define EAGLE_API __attribute__((visibility("default")))
+#else
+#define EAGLE_API
+#endif
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef struct CUstream_st *eagle_stream_t; /* same handle as cudaStream_t */
+
+typedef enum {
+  EAGLE_OK = 0,
+  EAGLE_ERR_INVALID_ARG = 1,  /* bad size, NULL pointer, index out of range  */
+  EAGLE_ERR_INVALID_TREE = 2, /* parent[] is not a rooted, topological tree  */
+  EAGLE_ERR_UNSUPPORTED = 3,  /* shape outside what the kernels implement    */
+  EAGLE_ERR_NUMERIC = 4,      /* NaN/Inf or probability outside [0,1]        */
+  EAGLE_ERR_TIMEOUT = 5,      /* a bounded device-side wait ran out          */
+  EAGLE_ERR_CUDA = 6,         /* CUDA launch/runtime error                   */
+  EAGLE_ERR_WORKSPACE = 7     /* workspace or pool smaller than required     */
+} eagle_status;
+
+typedef enum { EAGLE_F32 = 0, EAGLE_BF16 = 1 } eagle_dtype;
+typedef enum { EAGLE_LMHEAD_GREEDY = 0, EAGLE_LMHEAD_PROB = 1 } eagle_lmhead_mode;
+typedef enum { EAGLE_SAMPLE_REPLACE = 0, EAGLE_SAMPLE_NO_REPLACE = 1 } eagle_sample_mode;
+
+/* Limits of this implementation. */
+#define EAGLE_MAX_TREE_NODES 256  /* nodes per sequence, root included       */
+#define EAGLE_MAX_TOPK 32         /* EAGLE-2 top-k per expanded node          */
+#define EAGLE_MAX_DEPTH 16        /* EAGLE-2 expansion levels                 */
+
+/* Human-readable name of a status code (static string). */
+EAGLE_API const char *eagle_status_string(int status);
+/* Library version string (static). */
+EAGLE_API const char *eagle_version(void);
+
+/* ------------------------------------------------------------------------
+ * eagle_tree_attn -- tree-masked attention of every draft-tree node.
+ * [S4000] "EAGLE的创新点" item 2; [EAGLE] workflow paragraph: all root-to-leaf
+ * paths are verified by ONE forward pass whose attention mask lets node i
+ * see the cached context and exactly its own ancestors and itself.
+ *
+ *   out[t,h,:] = softmax_j( scale * q[t,h,:] . key_j ) value_j  over
+ *   keys j = [k_cache rows of t's sequence | k_tree rows of t's root..t path],
+ *   with kv head g = h / (Hq/Hkv) (grouped-query attention).
+ *
+ * dtype      EAGLE_BF16 (q, k_*, v_* bf16) or EAGLE_F32 (all fp32).
+ * B          sequences (>= 1).            T  total tree nodes (= tree_off[B]).
+ * Hq, Hkv    query / key-value heads; Hq % Hkv == 0.   D  head dim (64 or 128).
+ * scale      softmax scale (usually 1/sqrt(D)).
+ * max_nodes  upper bound on nodes of any one sequence (<= 256).
+ * max_kv     upper bound on any sequence's cache length (>= 0).
+ * d_q        [T,Hq,D];  d_k_tree, d_v_tree [T,Hkv,D] (K/V of the tree nodes).
+ * d_k_cache, d_v_cache  packed caches [kv_off[B],Hkv,D].
+ * d_kv_off   [B+1] int32, d_tree_off [B+1] int32, d_parent [T] int32 (local).
+ * d_out      [T,Hq,D] fp32, written.
+ * d_ws       scratch of eagle_tree_attn_workspace_bytes(...) bytes (may be
+ *            NULL if that size is 0); contents need no initialisation.
+ * Device errors: INVALID_TREE (malformed parent[] or a sequence with more
+ * than max_nodes nodes or a cache longer than max_kv).
+ * ---------------------------------------------------------------------- */
+EAGLE_API size_t eagle_tree_attn_workspace_bytes(int B, int T, int Hq, int Hkv, int D,
+                                       int max_nodes, int max_kv);
+EAGLE_API eagle_status eagle_tree_attn(eagle_dtype dtype, int B, int T, int Hq, int Hkv, int D,
+                             float scale, int max_nodes, int max_kv,
+                             const void *d_q, const void *d_k_tree, const void *d_v_tree,
+                             const void *d_k_cache, const void *d_v_cache,
+                             const int32_t *d_kv_off, const int32_t *d_tree_off,
+                             const int32_t *d_parent, float *d_out,
+                             void *d_ws, size_t ws_bytes, int *d_status,
+                             eagle_stream_t stream);
+
+/* ------------------------------------------------------------------------
+ * eagle_lmhead_softmax -- frozen LM head over every tree node.
+ * [EAGLE] workflow paragraph: the frozen classification head gives each
+ * node's next-token distribution, q = softmax(z / temperature), z = h W^T.
+ *
+ * dtype       EAGLE_BF16 (h, w bf16; fp32 accumulation) or EAGLE_F32.
+ * T, H, V     rows (tree nodes), hidden size, vocabulary.
+ * temperature > 0.
+ * mode        EAGLE_LMHEAD_GREEDY: no [T,V] tensor is written.
+ *             EAGLE_LMHEAD_PROB:   d_q [T,V] fp32 receives softmax(z/temp).
+ * d_h         [T,H];  d_w [V,H] (vocabulary-major, as stored by LM heads).
+ * d_argmax    [T] int32: argmax_v z[t,v], lowest index on ties.
+ * d_row_max   [T] fp32: max_v z.         d_row_lse [T] fp32: log sum exp(z/temp).
+ * d_top2_gap  [T] fp32: largest minus second-largest logit (0 on a tie).
+ * d_q         [T,V] fp32 or NULL in GREEDY mode.
+ * d_ws        scratch of eagle_lmhead_workspace_bytes(T, V) bytes.
+ * Device errors: NUMERIC (non-finite logit).
+ * ---------------------------------------------------------------------- */
+EAGLE_API size_t eagle_lmhead_workspace_bytes(int T, int V);
+EAGLE_API eagle_status eagle_lmhead_softmax(eagle_dtype dtype, int T, int H, int V, float temperature,
+                                  int mode, const void *d_h, const void *d_w,
+                                  int32_t *d_argmax, float *d_row_max, float *d_row_lse,
+                                  float *d_top2_gap, float *d_q, void *d_ws,
+                                  size_t ws_bytes, int *d_status, eagle_stream_t stream);
+
+/* ------------------------------------------------------------------------
+ * eagle_accept_greedy -- greedy tree walk.
+ * [S4000] greedy-decoding paragraph: match the target's most probable token
+ * from the first draft on and stop at the first mismatch; on a tree, move to
+ * the child (lowest node index) whose token equals argmax[cur].
+ * [EAGLE] speculative-sampling paragraph: alpha accepted -> alpha+1 tokens.
+ *
+ * d_tokens [T] int32 (token of every node; the root's is not compared),
+ * d_argmax [T] int32 (target argmax after each node).
+ * max_depth  output row width is max_depth+1; a walk deeper than max_depth
+ *            is a device INVALID_ARG error.
+ * Outputs (W = max_depth+1): d_accept_len [B] (alpha), d_accepted_nodes
+ * [B,W] (local node ids: root, then accepted nodes; -1 padded), d_out_tokens
+ * [B,W] (accepted tokens, then the bonus token; -1 padded).
+ * ---------------------------------------------------------------------- */
+EAGLE_API eagle_status eagle_accept_greedy(int B, int max_nodes, const int32_t *d_tree_off,
+                                 const int32_t *d_parent, const int32_t *d_tokens,
+                                 const int32_t *d_argmax, int max_depth,
+                                 int32_t *d_accept_len, int32_t *d_accepted_nodes,
+                                 int32_t *d_out_tokens, int *d_status,
+                                 eagle_stream_t stream);
+
+/* ------------------------------------------------------------------------
+ * eagle_accept_stochastic -- multi-round speculative sampling over the tree.
+ * [S4000] random-decoding paragraph (accept with min(1, q/p), otherwise
+ * resample from the corrected distribution); [EAGLE] "多轮投机采样" (applied
+ * recursively over the tree with the recorded draft probabilities);
+ * [EAGLE-2] §2 basic principle (output distribution equals the target's).
+ *
+ * At node cur: q_0 = q[cur], p_0 = p_rows[p_row_of_node[first child]]; for
+ * each child c (ascending index, token t):
+ *   accept iff (double)u_accept[c] * p_k[t] < (double)q_k[t];
+ *   on reject:  W_j = trunc(max(0, q_k[j]-p_k[j]) * 2^40), Z = sum W (exact),
+ *               q_{k+1}[j] = float(W_j) / float(Z)  (kept as q_k if Z == 0);
+ *               NO_REPLACE: P_j = trunc(p_k[j]*2^40), P_t = 0,
+ *               p_{k+1}[j] = float(P_j) / float(sum P) (0 if the sum is 0);
+ *               REPLACE: p_{k+1} = p_k.
+ * When every child is rejected, or cur is a leaf, the bonus token is drawn
+ * from q_final by inverse CDF over trunc(q*2^40): target =
+ * (trunc(u_sample[cur]*2^24) * Z) >> 24, token = first j whose inclusive
+ * prefix sum exceeds target.  All roundings are IEEE round-to-nearest, so
+ * decisions and tokens are reproducible bit for bit on any IEEE machine.
+ *
+ * V          vocabulary; R rows in d_p_rows.
+ * mode       EAGLE_SAMPLE_NO_REPLACE (siblings drawn without replacement, the
+ *            EAGLE-2 case) or EAGLE_SAMPLE_REPLACE (siblings drawn i.i.d.).
+ * d_q [T,V], d_p_rows [R,V] fp32 probabilities in [0,1];
+ * d_p_row_of_node [T] int32 global row of the distribution node i was drafted
+ * from; d_u_accept, d_u_sample [T] fp32 uniforms in [0,1).
+ * Outputs as eagle_accept_greedy.
+ * Device errors: NUMERIC (value outside [0,1] in a row the walk reads, or a
+ * final distribution without mass), INVALID_ARG (token/row/uniform out of
+ * range, walk deeper than max_depth), INVALID_TREE.
+ * ---------------------------------------------------------------------- */
+EAGLE_API eagle_status eagle_accept_stochastic(int B, int max_nodes, int V, int R, int mode,
+                                     const int32_t *d_tree_off, const int32_t *d_parent,
+                                     const int32_t *d_tokens, const float *d_q,
+                                     const float *d_p_rows, const int32_t *d_p_row_of_node,
+                                     const float *d_u_accept, const float *d_u_sample,
+                                     int max_depth, int32_t *d_accept_len,
+                                     int32_t *d_accepted_nodes, int32_t *d_out_tokens,
+                                     int *d_status, eagle_stream_t stream);
+
+/* ------------------------------------------------------------------------
+ * eagle_draft_expand -- EAGLE-2 dynamic draft tree: expand one level, or
+ * finalize (rerank under the budget and emit the tree).
+ * [EAGLE-2] §2 "EAGLE-2 的核心創新：動態草稿樹" items 1-3: per-node confidence,
+ * adaptive expansion, greedy selection under a fixed draft-token budget.
+ * A node's value is its cumulative draft log-prob.
+ *
+ * Expand (finalize == 0, level in [0, depth)): every frontier node takes the
+ * top-k tokens of its draft row (log-prob descending, token ascending);
+ * child score = fp32(parent score + logp); the next frontier is the top-k
+ * children by (score desc, creation order).  Draft rows:
+ *   d_draft_logp [B, R, V] fp32 with R = 1 + (depth-1)*k; level 0 reads row
+ *   0 (the root's), level d >= 1 reads rows 1+(d-1)*k+f for frontier rank f.
+ * Finalize (finalize == 1, after all `depth` levels): keep the top
+ * d_budget[b] pool nodes by (score desc, creation order), number them by
+ * (depth, score desc, creation order) after the root (node 0), and write
+ *   d_tree_off [B+1], d_parent [T] (local), d_tokens [T] (root: d_root_token[b]),
+ *   d_node_depth [T], d_score [T] (root 0), d_p_row_of_node [T] (global row
+ *   b*R + local row; root -1),
+ * where sequence b has min(budget[b], k + (depth-1)*k*k) + 1 nodes.
+ *
+ * d_pool: caller-owned scratch of eagle_draft_pool_bytes(B, k, depth, V)
+ * bytes, reused by all levels of one tree build (level 0 resets it).
+ * Arguments a role does not use may be NULL.  1 <= k <= min(32, V),
+ * 1 <= depth <= 16.
+ * Device errors: NUMERIC (non-finite log-prob), INVALID_ARG (negative budget).
+ * ---------------------------------------------------------------------- */
+EAGLE_API size_t eagle_draft_pool_bytes(int B, int k, int depth, int V);
+EAGLE_API eagle_status eagle_draft_expand(int B, int V, int k, int depth, int level, int finalize,
+                                const float *d_draft_logp, const int32_t *d_budget,
+                                const int32_t *d_root_token, void *d_pool, size_t pool_bytes,
+                                int32_t *d_tree_off, int32_t *d_parent, int32_t *d_tokens,
+                                int32_t *d_node_depth, float *d_score,
+                                int32_t *d_p_row_of_node, int *d_status,
+                                eagle_stream_t stream);
+
+#ifdef __cplusplus
+}
+#endif
+#endif /* EAGLE_H_ */

@@ -1,0 +1,92 @@
+"""GPU parity of tree attention against the oracle.
+
+Error metric per element: |g - r| / max(|r|, 1e-3 * rms(r over the head)),
+bounded by 2e-3 for bf16 inputs and 1e-5 for fp32."""
+import numpy as np
+import pytest
+
+import oracle as O
+import synth
+from gpu_common import attn_rel_err, cuda_ready, to_np, tol_for
+
+pytestmark = pytest.mark.gpu
+
+
+def _case(seed, dtype, Ls, levels_list, Hq, Hkv, D):
+    B = len(Ls)
+    parents = []
+    for b in range(B):
+        par, _ = synth.random_level_tree(seed + b, levels_list[b % len(levels_list)], 5)
+        parents.append(par)
+    sizes = [len(p) for p in parents]
+    T = sum(sizes)
+    tree_off = np.concatenate([[0], np.cumsum(sizes)]).astype(np.int32)
+    kv_off = np.concatenate([[0], np.cumsum(Ls)]).astype(np.int32)
+    cast = synth.to_bf16_values if dtype == "bf16" else (lambda a: a)
+    q = cast(synth.normal(seed, "q", (T, Hq, D)))
+    kt = cast(synth.normal(seed, "kt", (T, Hkv, D)))
+    vt = cast(synth.normal(seed, "vt", (T, Hkv, D)))
+    kc = cast(synth.normal(seed, "kc", (int(kv_off[-1]), Hkv, D)))
+    vc = cast(synth.normal(seed, "vc", (int(kv_off[-1]), Hkv, D)))
+    return q, kt, vt, kc, vc, kv_off, tree_off, np.concatenate(parents).astype(np.int32)
+
+
+def _run(E, dtype, q, kt, vt, kc, vc, kv_off, tree_off, parent):
+    import torch
+    tdt = torch.bfloat16 if dtype == "bf16" else torch.float32
+    dev = lambda a, t=tdt: torch.from_numpy(np.ascontiguousarray(a)).to(t).cuda()
+    T, Hq, D = q.shape
+    Hkv = kt.shape[1]
+    B = len(tree_off) - 1
+    max_nodes = int(np.max(np.diff(tree_off)))
+    max_kv = int(np.max(np.diff(kv_off)))
+    if kc.shape[0] == 0:
+        kc = np.zeros((1, Hkv, D), np.float32)
+        vc = kc
+    out = torch.full((T, Hq, D), -7.0, dtype=torch.float32, device="cuda")
+    ws_n = E.eagle_tree_attn_workspace_bytes(B, T, Hq, Hkv, D, max_nodes, max_kv)
+    ws = torch.empty(max(ws_n, 16), dtype=torch.uint8, device="cuda")
+    st = torch.zeros(1, dtype=torch.int32, device="cuda")
+    i32 = torch.int32
+    E.eagle_tree_attn(dev(q), dev(kt), dev(vt), dev(kc), dev(vc), dev(kv_off, i32),
+                      dev(tree_off, i32), dev(parent, i32), out, st, max_nodes=max_nodes,
+                      max_kv=max_kv, ws=ws)
+    torch.cuda.synchronize()
+    return to_np(out), int(st.item())
+
+
+@pytest.mark.parametrize("dtype,Ls,levels,Hq,Hkv,D", [
+    ("f32", [128], [(1, 4, 6, 6, 6, 3)], 4, 4, 64),                   # tiny fp32 layer
+    ("f32", [0, 1, 127, 129], [(1,), (1, 3, 3), (1, 5, 9, 2)], 8, 2, 128),
+    ("bf16", [300], [(1, 10, 20, 20, 10)], 32, 8, 128),              # GQA 32/8
+    ("bf16", [64, 0, 1000], [(1, 8, 8, 8, 8, 8, 8, 8, 8)], 64, 8, 128),  # GQA 64/8, 65 nodes
+    ("bf16", [2048], [(1, 10, 10, 10, 10, 10, 10)], 32, 32, 128),   # Vicuna-7B shaped (MHA)
+])
+def test_tree_attention_matches_oracle(dtype, Ls, levels, Hq, Hkv, D):
+    E = cuda_ready()
+    case = _case(len(Ls) * 31 + Hq, dtype, Ls, levels, Hq, Hkv, D)
+    got, st = _run(E, dtype, *case)
+    assert st == 0
+    ref = O.tree_attn(*case)
+    assert attn_rel_err(got, ref).max() <= tol_for(dtype)
+
+
+def test_tree_attention_long_cache_sampled_nodes():
+    # LLaMA-3-8B shaped: GQA 32/8, L = 8192, 65 nodes; the oracle checks a
+    # sample of nodes (including the root and the deepest leaf)
+    E = cuda_ready()
+    case = _case(3, "bf16", [8192], [(1, 8, 8, 8, 8, 8, 8, 8, 8)], 32, 8, 128)
+    got, st = _run(E, "bf16", *case)
+    assert st == 0
+    nodes = [0, 1, 17, 40, 64]
+    ref = O.tree_attn(*case, nodes=nodes)
+    assert attn_rel_err(got[nodes], ref[nodes]).max() <= 2e-3
+
+
+def test_malformed_parent_is_reported_on_the_device():
+    E = cuda_ready()
+    case = list(_case(9, "f32", [16], [(1, 3, 3)], 4, 4, 64))
+    case[-1] = case[-1].copy()
+    case[-1][4] = 5                         # parent not smaller than the child
+    _, st = _run(E, "f32", *case)
+    assert st == 2                          # EAGLE_ERR_INVALID_TREE

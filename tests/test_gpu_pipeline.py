@@ -1,0 +1,156 @@
+"""End-to-end verify steps on the five full-size workloads.
+
+Each workload runs through the C ABI exactly as the benchmark launches it
+(TreeVerifyStep.run: tree build, attention, LM head, acceptance).  Checked:
+  * the EAGLE-2 tree equals the oracle's (bit-exact);
+  * attention on sampled nodes, and the LM head on every row, within the
+    stated tolerances (argmax: outside near-ties);
+  * acceptance fed identical inputs (the oracle's argmax / q) is bit-exact;
+  * the GPU's own end-to-end accept lengths and tokens equal the oracle's,
+    except where a logged near-tie (top-2 logit gap < 1e-3, or an acceptance
+    test within 1e-4 relative of its threshold) explains the difference.
+Greedy workloads also run a planted variant: the tokens on one random
+root-to-leaf path are replaced by the oracle's argmax, so alpha spans the
+whole depth."""
+import numpy as np
+import pytest
+
+import oracle as O
+import synth
+from gpu_common import attn_rel_err, cuda_ready, load_step, step_shape, to_np
+
+pytestmark = [pytest.mark.gpu, pytest.mark.slow]
+
+NEAR_TIE = 1e-3
+WL = synth.workloads()
+
+
+def _oracle_tree(w, inp):
+    if w.tree == "eagle2":
+        return O.build_eagle2_tree(inp["draft_logp"], B=w.B, k=w.k, depth=w.depth,
+                                   budget=inp["budget"], root_token=inp["root_token"])
+    return {"tree_off": inp["tree_off"], "parent": inp["parent"], "tokens": inp["tokens"],
+            "p_row_of_node": inp["p_row_of_node"]}
+
+
+def _sample_nodes(tree_off, k_per_seq=2, seed=0):
+    g = np.random.default_rng(seed)
+    nodes = []
+    for b in range(len(tree_off) - 1):
+        t0, t1 = int(tree_off[b]), int(tree_off[b + 1])
+        nodes += [t0, t1 - 1] + list(g.integers(t0, t1, size=k_per_seq))
+    return sorted(set(int(x) for x in nodes))
+
+
+def _same_seq(got, ref, b):
+    return all(np.array_equal(g_[b], r_[b]) for g_, r_ in zip(got, ref))
+
+
+def _greedy_near_tie(tree_off, gap, walks, b):
+    t0 = int(tree_off[b])
+    return any(n >= 0 and gap[t0 + int(n)] < NEAR_TIE for n in walks)
+
+
+def _outputs(step):
+    return (to_np(step.accept_len), to_np(step.accepted_nodes), to_np(step.out_tokens))
+
+
+@pytest.mark.parametrize("name", list(WL))
+def test_workload_end_to_end(name):
+    import torch
+    E = cuda_ready()
+    from eagle_tree_verification_gb300.pipeline import TreeVerifyStep
+    w = WL[name]
+    inp = synth.make_inputs(w)
+    tree = _oracle_tree(w, inp)
+    T = int(tree["tree_off"][-1])
+    nodes = _sample_nodes(tree["tree_off"])
+    attn_ref = O.tree_attn(inp["q"], inp["k_tree"], inp["v_tree"], inp["k_cache"],
+                           inp["v_cache"], inp["kv_off"], tree["tree_off"], tree["parent"],
+                           nodes=nodes)
+    full = O.lmhead_softmax(inp["h"], inp["w_lm"], w.temperature,
+                            want_q=("stochastic" in w.modes))
+    tol = 2e-3 if w.dtype == "bf16" else 1e-5
+    for mode in w.modes:
+        step = TreeVerifyStep(step_shape(w, mode))
+        load_step(step, w, inp)
+        step.run()
+        torch.cuda.synchronize()
+        assert int(step.status.item()) == 0
+        # ---- tree
+        for nm in ("tree_off", "parent", "tokens", "p_row_of_node"):
+            np.testing.assert_array_equal(to_np(getattr(step, nm)), tree[nm], err_msg=nm)
+        # ---- attention on sampled nodes
+        assert attn_rel_err(to_np(step.attn_out)[nodes], attn_ref[nodes]).max() <= tol
+        # ---- LM head, every row
+        rm, lse, gapg, am = (to_np(step.row_max), to_np(step.row_lse), to_np(step.top2_gap),
+                             to_np(step.argmax))
+        sc = np.maximum(1.0, np.abs(full["row_max"]))
+        assert np.all(np.abs(rm - full["row_max"]) <= 1e-4 * sc)
+        assert np.all(np.abs(lse - full["row_lse"]) <= 1e-4 * np.maximum(1, np.abs(full["row_lse"])))
+        assert np.all(np.abs(gapg - full["top2_gap"]) <= 2e-4)
+        clear = full["top2_gap"] >= NEAR_TIE
+        np.testing.assert_array_equal(am[clear], full["argmax"][clear])
+        for r in np.nonzero(~clear)[0]:
+            assert full["z"][r, am[r]] >= full["z"][r].max() - NEAR_TIE
+        if mode == "stochastic":
+            qg = to_np(step.q_prob).astype(np.float64)
+            qr = full["q"].astype(np.float64)
+            m = qr >= 1e-30
+            assert (np.abs(qg[m] - qr[m]) / qr[m]).max() <= tol
+        # ---- acceptance
+        got = _outputs(step)
+        if mode == "greedy":
+            ref = O.accept_greedy(tree["tree_off"], tree["parent"], tree["tokens"],
+                                  full["argmax"], w.max_depth)
+            for b in range(w.B):
+                if not _same_seq(got, ref, b):
+                    assert _greedy_near_tie(tree["tree_off"], full["top2_gap"],
+                                            list(got[1][b]) + list(ref[1][b]), b), b
+            # identical inputs: the oracle's argmax into the GPU walk
+            step.argmax.copy_(torch.from_numpy(full["argmax"]))
+            step.run_accept()
+            torch.cuda.synchronize()
+            for g_, r_ in zip(_outputs(step), ref):
+                np.testing.assert_array_equal(g_, r_)
+            # planted: one root-to-leaf path carries the target's argmax
+            g = np.random.default_rng(7)
+            tokens = tree["tokens"].copy()
+            for b in range(w.B):
+                t0, t1 = int(tree["tree_off"][b]), int(tree["tree_off"][b + 1])
+                leaf = int(g.integers(t0, t1))
+                path = O.tree_path(tree["parent"][t0:t1], leaf - t0)
+                for a, c in zip(path[:-1], path[1:]):
+                    tokens[t0 + c] = full["argmax"][t0 + a]
+            step.tokens.copy_(torch.from_numpy(tokens))
+            step.run_lmhead()
+            step.run_accept()
+            torch.cuda.synchronize()
+            ref_p = O.accept_greedy(tree["tree_off"], tree["parent"], tokens, full["argmax"],
+                                    w.max_depth)
+            got_p = _outputs(step)
+            for b in range(w.B):
+                if not _same_seq(got_p, ref_p, b):
+                    assert _greedy_near_tie(tree["tree_off"], full["top2_gap"],
+                                            list(got_p[1][b]) + list(ref_p[1][b]), b), b
+            assert ref_p[0].max() >= 2
+        else:
+            trace = []
+            ref = O.accept_stochastic(tree["tree_off"], tree["parent"], tree["tokens"], full["q"],
+                                      inp["p_rows"], tree["p_row_of_node"], inp["u_accept"],
+                                      inp["u_sample"], w.max_depth, trace=trace)
+            for b in range(w.B):
+                if not _same_seq(got, ref, b):
+                    t0 = int(tree["tree_off"][b])
+                    margins = [abs(float(inp["u_accept"][t0 + c]) * pt - qt) / max(qt, 1e-30)
+                               for (bb, cur, c, t, qt, pt, a) in trace if bb == b]
+                    assert margins and min(margins) < 1e-4, b
+            # identical inputs: the oracle's q into the GPU walk
+            step.q_prob.copy_(torch.from_numpy(full["q"]))
+            step.run_accept()
+            torch.cuda.synchronize()
+            for g_, r_ in zip(_outputs(step), ref):
+                np.testing.assert_array_equal(g_, r_)
+        assert int(step.status.item()) == 0
+        del step
+        torch.cuda.empty_cache()
