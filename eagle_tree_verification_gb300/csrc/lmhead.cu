@@ -5,15 +5,26 @@
 // [EAGLE] workflow paragraph (page title in include/eagle.h): the frozen LM
 // head gives the next-token distribution of every node.
 //
-// Two kernels:
-//   lmhead_tile_kernel     one CTA per (vocab tile, row tile): fp32-accumulated
-//                          GEMM over H, then per-(row, vocab tile) partial
-//                          statistics; in PROB mode it also writes z.
+// Kernels:
+//   lmhead_tc_kernel       bf16, up to 128 rows: persistent tcgen05 GEMM.  Each
+//                          CTA owns a contiguous slice of the vocabulary and
+//                          streams its rows of W once through a TMA ring;
+//                          tree rows sit on TMEM lanes, so every thread owns
+//                          one row and its softmax statistics are thread-local.
+//                          One partial per (row, CTA).
+//   lmhead_tile_kernel     CUDA-core fallback for fp32 inputs (tensor cores
+//                          would round them to tf32) and for more than 128
+//                          rows: per-(row, 64-vocab tile) partials.
 //   lmhead_finalize_kernel per (row, vocab chunk): combines the partials of
 //                          the row; in PROB mode rewrites z as softmax(z/T).
 #include <math.h>
 
+#include <algorithm>
+
+#include <cudaTypedefs.h>
+
 #include "common.cuh"
+#include "tc.cuh"
 
 using namespace eagle;
 
@@ -165,10 +176,9 @@ lmhead_finalize_kernel(int T, int V, float temperature, const Partial* __restric
   idx = s_idx;
   // second largest and the rescaled sum of exponentials
   float second = -INFINITY, s = 0.f;
-  const int arg_tile = idx / kVT;
   for (int t = tid; t < n_vtiles; t += blockDim.x) {
     const Partial p = pr[t];
-    second = fmaxf(second, (t == arg_tile) ? p.second : p.m);
+    second = fmaxf(second, (p.idx == idx) ? p.second : p.m);
     s += p.s * expf(__fdiv_rn(p.m - m, temperature));
   }
 #pragma unroll
@@ -207,11 +217,300 @@ lmhead_finalize_kernel(int T, int V, float temperature, const Partial* __restric
   }
 }
 
+
+// ---------------------------------------------------------------------------
+// tcgen05 path
+// ---------------------------------------------------------------------------
+constexpr int kTcThreads = 192;   // warp 0 TMA, warp 1 MMA, warps 2-5 epilogue
+constexpr int kBK = 64;           // bf16 per 128-byte swizzled row
+constexpr int kTileV = 128;       // vocab rows per MMA (the MMA's N)
+constexpr int kGroup = 4;         // tiles accumulated at once: 4 x 128 TMEM columns
+constexpr int kHStages = 3;
+constexpr int kWStages = 9;
+constexpr int kBlockBytes = 128 * 128;  // 128 rows x 128 bytes
+constexpr size_t kTcSmem = 1024 + (size_t)(kHStages + kWStages) * kBlockBytes + 512;
+
+struct TcShared {
+  uint64_t h_full[kHStages], h_empty[kHStages];
+  uint64_t w_full[kWStages], w_empty[kWStages];
+  uint64_t tmem_full, tmem_empty, drain;
+  uint32_t tmem_base;
+  int abort_flag;
+  int consumed_w, consumed_h;
+};
+
+__global__ void __launch_bounds__(kTcThreads, 1)
+lmhead_tc_kernel(const __grid_constant__ CUtensorMap map_h, const __grid_constant__ CUtensorMap map_w,
+                 int T, int H, int V, float temperature, float* __restrict__ z_out,
+                 Partial* __restrict__ part, int n_units, int* status) {
+  extern __shared__ __align__(1024) unsigned char smem_raw[];
+  unsigned char* base = reinterpret_cast<unsigned char*>(
+      (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~(uintptr_t)1023);
+  unsigned char* h_smem = base;
+  unsigned char* w_smem = base + kHStages * kBlockBytes;
+  TcShared* sh = reinterpret_cast<TcShared*>(w_smem + kWStages * kBlockBytes);
+
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int G = gridDim.x;
+  // this CTA's slice of the vocabulary, in units of 16 rows
+  const int u0 = (int)((long long)n_units * blockIdx.x / G);
+  const int u1 = (int)((long long)n_units * (blockIdx.x + 1) / G);
+  const int r_begin = u0 * 16, r_end = u1 * 16;
+  const int n_tiles = (r_end - r_begin + kTileV - 1) / kTileV;
+  const int n_groups = (n_tiles + kGroup - 1) / kGroup;
+  const int KB = (H + kBK - 1) / kBK;
+
+  if (threadIdx.x == 0) {
+    for (int i = 0; i < kHStages; ++i) {
+      tc::mbar_init(&sh->h_full[i], 1);
+      tc::mbar_init(&sh->h_empty[i], 1);
+    }
+    for (int i = 0; i < kWStages; ++i) {
+      tc::mbar_init(&sh->w_full[i], 1);
+      tc::mbar_init(&sh->w_empty[i], 1);
+    }
+    tc::mbar_init(&sh->tmem_full, 1);
+    tc::mbar_init(&sh->tmem_empty, 4);
+    tc::mbar_init(&sh->drain, 1);
+    sh->abort_flag = 0;
+    sh->consumed_w = 0;
+    sh->consumed_h = 0;
+    tc::fence_barrier_init();
+  }
+  if (warp == 1) {
+    tc::tmem_alloc(&sh->tmem_base, 512);
+    tc::tmem_relinquish();
+  }
+  if (warp == 0 && lane == 0) {
+    tc::prefetch_tensormap(&map_h);
+    tc::prefetch_tensormap(&map_w);
+  }
+  tc::fence_before_thread_sync();
+  __syncthreads();
+  tc::fence_after_thread_sync();
+  const uint32_t tmem = sh->tmem_base;
+  volatile int* abort_flag = &sh->abort_flag;
+
+  if (warp == 0) {
+    // ------------------------------------------------------------ producer
+    if (lane == 0) {
+      const uint64_t pol_w = tc::policy_evict_first();
+      const uint64_t pol_h = tc::policy_evict_last();
+      int hs = 0, ws = 0, issued_h = 0, issued_w = 0;
+      uint32_t hph = 0, wph = 0;
+      bool ok = true;
+      for (int g = 0; g < n_groups && ok; ++g) {
+        const int j0 = g * kGroup, j1 = min(n_tiles, j0 + kGroup);
+        for (int kb = 0; kb < KB && ok; ++kb) {
+          if (!(ok = tc::mbar_wait(&sh->h_empty[hs], hph ^ 1, abort_flag, status))) break;
+          tc::mbar_arrive_expect_tx(&sh->h_full[hs], kBlockBytes);
+          tc::tma_load_2d_hint(h_smem + hs * kBlockBytes, &map_h, &sh->h_full[hs], kb * kBK, 0,
+                               pol_h);
+          ++issued_h;
+          if (++hs == kHStages) { hs = 0; hph ^= 1; }
+          for (int j = j0; j < j1; ++j) {
+            const int row0 = r_begin + j * kTileV;
+            const int rows = min(kTileV, r_end - row0);
+            if (!(ok = tc::mbar_wait(&sh->w_empty[ws], wph ^ 1, abort_flag, status))) break;
+            tc::mbar_arrive_expect_tx(&sh->w_full[ws], rows * 128);
+            for (int u = 0; u < rows; u += 16)
+              tc::tma_load_2d_hint(w_smem + ws * kBlockBytes + u * 128, &map_w, &sh->w_full[ws],
+                                   kb * kBK, row0 + u, pol_w);
+            ++issued_w;
+            if (++ws == kWStages) { ws = 0; wph ^= 1; }
+          }
+        }
+      }
+      if (!ok) {
+        // let every copy still in flight land before the CTA exits
+        int never = 0;
+        for (int i = *(volatile int*)&sh->consumed_w; i < issued_w; ++i)
+          tc::mbar_wait(&sh->w_full[i % kWStages], (i / kWStages) & 1, &never, nullptr,
+                        200000000ll);
+        for (int i = *(volatile int*)&sh->consumed_h; i < issued_h; ++i)
+          tc::mbar_wait(&sh->h_full[i % kHStages], (i / kHStages) & 1, &never, nullptr,
+                        200000000ll);
+      }
+    }
+  } else if (warp == 1) {
+    // ------------------------------------------------------------ MMA issuer
+    if (lane == 0) {
+      int hs = 0, ws = 0;
+      uint32_t hph = 0, wph = 0, tph = 0;
+      bool ok = true;
+      for (int g = 0; g < n_groups && ok; ++g) {
+        const int j0 = g * kGroup, j1 = min(n_tiles, j0 + kGroup);
+        if (!(ok = tc::mbar_wait(&sh->tmem_empty, tph ^ 1, abort_flag, status))) break;
+        tph ^= 1;
+        tc::fence_after_thread_sync();
+        for (int kb = 0; kb < KB && ok; ++kb) {
+          if (!(ok = tc::mbar_wait(&sh->h_full[hs], hph, abort_flag, status))) break;
+          const uint32_t a_base = tc::smem_u32(h_smem + hs * kBlockBytes);
+          for (int j = j0; j < j1; ++j) {
+            const int rows = min(kTileV, r_end - (r_begin + j * kTileV));
+            if (!(ok = tc::mbar_wait(&sh->w_full[ws], wph, abort_flag, status))) break;
+            tc::fence_after_thread_sync();
+            const uint32_t b_base = tc::smem_u32(w_smem + ws * kBlockBytes);
+            const uint32_t idesc = tc::idesc_bf16_f32(128, rows);
+#pragma unroll
+            for (int k16 = 0; k16 < kBK / 16; ++k16) {
+              tc::mma_f16(tmem + (uint32_t)((j - j0) * kTileV),
+                          tc::desc_kmajor_sw128(a_base + k16 * 32),
+                          tc::desc_kmajor_sw128(b_base + k16 * 32), idesc,
+                          (kb > 0 || k16 > 0) ? 1u : 0u);
+            }
+            tc::mma_commit(&sh->w_empty[ws]);
+            *(volatile int*)&sh->consumed_w += 1;
+            if (++ws == kWStages) { ws = 0; wph ^= 1; }
+          }
+          if (!ok) break;
+          tc::mma_commit(&sh->h_empty[hs]);
+          *(volatile int*)&sh->consumed_h += 1;
+          if (++hs == kHStages) { hs = 0; hph ^= 1; }
+        }
+        if (ok) tc::mma_commit(&sh->tmem_full);
+      }
+      // every MMA issued by this thread has finished before TMEM is freed
+      tc::mma_commit(&sh->drain);
+      int never = 0;
+      tc::mbar_wait(&sh->drain, 0, &never, nullptr, 200000000ll);
+    }
+  } else {
+    // ------------------------------------------------------------ epilogue
+    const int quad = warp & 3;
+    const int t = quad * 32 + lane;   // tree row held by this thread
+    const bool row_ok = t < T;
+    const float k2 = 1.4426950408889634f / temperature;   // log2(e) / temperature
+    const bool vec = ((V & 3) == 0);
+    float m = -INFINITY, s = 0.f, second = -INFINITY;
+    int idx = 0x7fffffff;
+    bool bad = false;
+    uint32_t tph = 0;
+    for (int g = 0; g < n_groups; ++g) {
+      const int j0 = g * kGroup, j1 = min(n_tiles, j0 + kGroup);
+      // every lane waits; the warp proceeds only if all of them saw the phase
+      const bool got = tc::mbar_wait(&sh->tmem_full, tph, abort_flag, status);
+      if (!__all_sync(0xffffffffu, got)) break;
+      tph ^= 1;
+      tc::fence_after_thread_sync();
+      for (int j = j0; j < j1; ++j) {
+        const int row0 = r_begin + j * kTileV;
+        const int rows = min(kTileV, r_end - row0);
+        for (int c = 0; c < rows; c += 32) {
+          float v[32];
+          tc::tmem_ld_32x32b_x32(tmem + ((uint32_t)(quad * 32) << 16) + (uint32_t)((j - j0) * kTileV + c), v);
+          const int vb = row0 + c;
+          const int nvalid = min(min(32, rows - c), V - vb);
+          if (!row_ok || nvalid <= 0) continue;
+          if (z_out) {
+            float* dst = z_out + (size_t)t * V + vb;
+            if (vec && nvalid == 32) {
+#pragma unroll
+              for (int i = 0; i < 32; i += 4)
+                *reinterpret_cast<float4*>(dst + i) = make_float4(v[i], v[i + 1], v[i + 2], v[i + 3]);
+            } else {
+#pragma unroll
+              for (int i = 0; i < 32; ++i)
+                if (i < nvalid) dst[i] = v[i];
+            }
+          }
+          float cm = -INFINITY, cs = -INFINITY;
+          int ci = 0;
+#pragma unroll
+          for (int i = 0; i < 32; ++i) {
+            const float x = (i < nvalid) ? v[i] : -INFINITY;
+            if (i < nvalid) bad |= !isfinite(x);
+            if (x > cm) {
+              cs = cm;
+              cm = x;
+              ci = i;
+            } else if (x > cs) {
+              cs = x;
+            }
+          }
+          if (cm > m) {
+            second = fmaxf(m, cs);
+            const float mn = cm;
+            s = (m == -INFINITY) ? 0.f : s * exp2f((m - mn) * k2);
+            m = mn;
+            idx = vb + ci;
+          } else {
+            second = fmaxf(second, cm);
+          }
+          float acc = 0.f;
+#pragma unroll
+          for (int i = 0; i < 32; ++i)
+            if (i < nvalid) acc += exp2f((v[i] - m) * k2);
+          s += acc;
+        }
+      }
+      tc::fence_before_thread_sync();
+      __syncwarp();
+      if (lane == 0) tc::mbar_arrive(&sh->tmem_empty);
+    }
+    if (bad) fail(status, EAGLE_ERR_NUMERIC);
+    if (row_ok) {
+      Partial p;
+      p.m = m;
+      p.s = s;
+      p.second = second;
+      p.idx = (m == -INFINITY) ? 0x7fffffff : idx;
+      part[(size_t)t * G + blockIdx.x] = p;
+    }
+  }
+  tc::fence_before_thread_sync();
+  __syncthreads();
+  if (warp == 1) {
+    tc::fence_after_thread_sync();
+    tc::tmem_dealloc(tmem, 512);
+  }
+}
+
+PFN_cuTensorMapEncodeTiled_v12000 get_encode() {
+  static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+  if (!fn) {
+    void* p = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault,
+                                         &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
+  }
+  return fn;
+}
+
+// 2-D bf16 tensor [rows, cols] (cols contiguous), 128-byte swizzled boxes of
+// 64 columns x box_rows rows; out-of-range elements read as zero.
+bool make_map_bf16(CUtensorMap* map, const void* ptr, int rows, int cols, int box_rows) {
+  auto enc = get_encode();
+  if (!enc) return false;
+  cuuint64_t dims[2] = {(cuuint64_t)cols, (cuuint64_t)rows};
+  cuuint64_t strides[1] = {(cuuint64_t)cols * 2};
+  cuuint32_t box[2] = {(cuuint32_t)kBK, (cuuint32_t)box_rows};
+  cuuint32_t estr[2] = {1, 1};
+  return enc(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(ptr), dims, strides, box,
+             estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+             CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+int sm_count() {
+  static int n = 0;
+  if (!n) {
+    int dev = 0;
+    cudaGetDevice(&dev);
+    cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev);
+    if (n <= 0) n = 148;
+  }
+  return n;
+}
+
 }  // namespace
 
+// One partial per (row, vocab tile of 64) on the CUDA-core path and per
+// (row, CTA) on the tensor-core path, whose CTAs each own at least 16 rows.
 extern "C" size_t eagle_lmhead_workspace_bytes(int T, int V) {
   if (T < 0 || V < 1) return 0;
-  return (size_t)T * ((V + kVT - 1) / kVT) * sizeof(Partial);
+  return (size_t)T * ((V + 15) / 16) * sizeof(Partial);
 }
 
 extern "C" eagle_status eagle_lmhead_softmax(eagle_dtype dtype, int T, int H, int V,
@@ -232,9 +531,33 @@ extern "C" eagle_status eagle_lmhead_softmax(eagle_dtype dtype, int T, int H, in
   EAGLE_HOST_CHECK(mode == EAGLE_LMHEAD_GREEDY || d_q, EAGLE_ERR_INVALID_ARG);
   EAGLE_HOST_CHECK(ws_bytes >= eagle_lmhead_workspace_bytes(T, V) && d_ws, EAGLE_ERR_WORKSPACE);
   cudaStream_t s = (cudaStream_t)stream;
-  const int n_vtiles = (V + kVT - 1) / kVT;
   Partial* part = static_cast<Partial*>(d_ws);
   float* z = (mode == EAGLE_LMHEAD_PROB) ? d_q : nullptr;
+  const bool tc_ok = dtype == EAGLE_BF16 && T <= 128 && (H % 8) == 0 &&
+                     (((uintptr_t)d_h | (uintptr_t)d_w) & 15) == 0 &&
+                     (!z || ((uintptr_t)z & 15) == 0);
+  if (tc_ok) {
+    CUtensorMap map_h, map_w;
+    if (!make_map_bf16(&map_h, d_h, T, H, 128) || !make_map_bf16(&map_w, d_w, V, H, 16))
+      return EAGLE_ERR_CUDA;
+    static bool attr = false;
+    if (!attr) {
+      if (cudaFuncSetAttribute(lmhead_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                               (int)kTcSmem) != cudaSuccess)
+        return EAGLE_ERR_CUDA;
+      attr = true;
+    }
+    const int n_units = (V + 15) / 16;
+    const int grid = std::min(sm_count(), n_units);
+    lmhead_tc_kernel<<<grid, kTcThreads, kTcSmem, s>>>(map_h, map_w, T, H, V, temperature, z,
+                                                        part, n_units, d_status);
+    if (cudaGetLastError() != cudaSuccess) return EAGLE_ERR_CUDA;
+    dim3 fgrid(T, z ? (V + kFinChunk - 1) / kFinChunk : 1);
+    lmhead_finalize_kernel<<<fgrid, kFinThreads, 0, s>>>(T, V, temperature, part, grid, d_argmax,
+                                                         d_row_max, d_row_lse, d_top2_gap, z);
+    return launch_status(cudaGetLastError());
+  }
+  const int n_vtiles = (V + kVT - 1) / kVT;
   dim3 grid(n_vtiles, (T + kRT - 1) / kRT);
   if (dtype == EAGLE_BF16)
     lmhead_tile_kernel<__nv_bfloat16><<<grid, kTileThreads, 0, s>>>(

@@ -1,7 +1,9 @@
 """GPU parity of tree attention against the oracle.
 
-Error metric per element: |g - r| / max(|r|, 1e-3 * rms(r over the head)),
-bounded by 2e-3 for bf16 inputs and 1e-5 for fp32."""
+Error metric per element: |g - r| / max(|r|, rms(r over the head)), bounded
+by 2e-3 for bf16 inputs and 1e-5 for fp32.  The mask itself is checked by an
+invariant that holds at any size: changing the keys/values of one node must
+leave every node outside its subtree bit-for-bit unchanged."""
 import numpy as np
 import pytest
 
@@ -90,3 +92,24 @@ def test_malformed_parent_is_reported_on_the_device():
     case[-1][4] = 5                         # parent not smaller than the child
     _, st = _run(E, "f32", *case)
     assert st == 2                          # EAGLE_ERR_INVALID_TREE
+
+
+@pytest.mark.parametrize("dtype,L,Hq,Hkv", [("bf16", 8192, 32, 8), ("f32", 129, 8, 2)])
+def test_changing_one_branch_leaves_the_rest_of_the_tree_unchanged(dtype, L, Hq, Hkv):
+    # node i must see exactly the cache and its own root-to-i path: perturb
+    # the K/V of one node and compare every other node's output bit for bit
+    E = cuda_ready()
+    case = list(_case(17, dtype, [L], [(1, 8, 8, 8, 8, 8, 8, 8, 8)], Hq, Hkv, 128))
+    base, st = _run(E, dtype, *case)
+    assert st == 0
+    parent = case[-1]
+    victim = 9                                   # a depth-2 node
+    for which in (1, 2):                         # keys, then values
+        c2 = [a.copy() if i in (1, 2) else a for i, a in enumerate(case)]
+        c2[which][victim] = -c2[which][victim] + 0.5
+        out, st = _run(E, dtype, *c2)
+        assert st == 0
+        for i in range(len(parent)):
+            inside = victim in O.tree_path(parent, i)
+            same = np.array_equal(out[i], base[i])
+            assert same != inside, (which, i)
