@@ -21,6 +21,7 @@ __all__ = [
     "SAMPLE_NO_REPLACE", "eagle_tree_attn", "eagle_tree_attn_workspace_bytes",
     "eagle_lmhead_softmax", "eagle_lmhead_workspace_bytes", "eagle_accept_greedy",
     "eagle_accept_stochastic", "eagle_draft_expand", "eagle_draft_pool_bytes",
+    "eagle_lmhead_softmax_noalloc", "eagle_lmhead_noalloc_max_scratch_bytes",
 ]
 
 HERE = os.path.dirname(os.path.abspath(__file__))
@@ -53,6 +54,8 @@ _SIGS = {
     "eagle_accept_greedy": ([_i, _i, _p, _p, _p, _p, _i, _p, _p, _p, _p, _p], _i),
     "eagle_accept_stochastic": ([_i] * 5 + [_p] * 8 + [_i] + [_p] * 5, _i),
     "eagle_draft_pool_bytes": ([_i] * 4, _sz),
+    "eagle_lmhead_noalloc_max_scratch_bytes": ([], _sz),
+    "eagle_lmhead_softmax_noalloc": ([_i, _i, _i, _i, _f, _i] + [_p] * 9, _i),
     "eagle_draft_expand": ([_i] * 6 + [_p] * 4 + [_sz] + [_p] * 8, _i),
 }
 
@@ -190,6 +193,29 @@ def eagle_lmhead_softmax(h, w, argmax, row_max, row_lse, top2_gap, q, ws, status
     _call("eagle_lmhead_softmax", _dtype_code(h), T, H, V, float(temperature), mode, _ptr(h),
           _ptr(w), _ptr(argmax), _ptr(row_max), _ptr(row_lse), _ptr(top2_gap), _ptr(q),
           _ptr(ws), ws.numel() * ws.element_size(), _ptr(status), _stream(stream))
+
+
+def eagle_lmhead_noalloc_max_scratch_bytes() -> int:
+    return int(lib().eagle_lmhead_noalloc_max_scratch_bytes())
+
+
+def eagle_lmhead_softmax_noalloc(h, w, argmax, row_max, row_lse, top2_gap, q, status, *,
+                                 temperature: float = 1.0, stream=None) -> None:
+    """eagle_lmhead_softmax without a workspace: for callers that cannot
+    allocate scratch memory (see include/eagle.h).  Its scratch is a fixed
+    16 MiB array inside the library, shared by every call; calls that may
+    overlap on the GPU race on it."""
+    torch = _torch()
+    T, H = h.shape
+    V = w.shape[0]
+    _need(w, h.dtype, "w")
+    _need(argmax, torch.int32, "argmax")
+    for name, t in (("row_max", row_max), ("row_lse", row_lse), ("top2_gap", top2_gap), ("q", q)):
+        _need(t, torch.float32, name)
+    mode = LMHEAD_GREEDY if q is None else LMHEAD_PROB
+    _call("eagle_lmhead_softmax_noalloc", _dtype_code(h), T, H, V, float(temperature), mode,
+          _ptr(h), _ptr(w), _ptr(argmax), _ptr(row_max), _ptr(row_lse), _ptr(top2_gap), _ptr(q),
+          _ptr(status), _stream(stream))
 
 
 def eagle_accept_greedy(tree_off, parent, tokens, argmax, accept_len, accepted_nodes,

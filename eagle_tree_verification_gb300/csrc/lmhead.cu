@@ -575,3 +575,66 @@ extern "C" eagle_status eagle_lmhead_softmax(eagle_dtype dtype, int T, int H, in
                                                        d_top2_gap, z);
   return launch_status(cudaGetLastError());
 }
+
+// ---------------------------------------------------------------------------
+// Allocation-free variant of eagle_lmhead_softmax.
+//
+// The per-row partial statistics live in a fixed array in the library's own
+// device memory instead of a caller-provided workspace.  Every GPU that
+// loads the library holds this array until the process exits.
+// ---------------------------------------------------------------------------
+#include <mutex>
+
+namespace {
+
+constexpr size_t kNoAllocScratchBytes = (size_t)16 << 20;  // 16 MiB
+constexpr int kMaxDevices = 64;
+
+static __device__ __align__(256) unsigned char g_lmhead_scratch[kNoAllocScratchBytes];
+
+// Device address of g_lmhead_scratch, resolved once per device with that
+// device current (the host-side symbol is only a stand-in, not an address).
+void* noalloc_scratch(int* err) {
+  static std::mutex mu;
+  static void* ptr[kMaxDevices] = {};
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) {
+    *err = EAGLE_ERR_CUDA;
+    return nullptr;
+  }
+  std::lock_guard<std::mutex> lock(mu);
+  if (!ptr[dev]) {
+    void* p = nullptr;
+    if (cudaGetSymbolAddress(&p, g_lmhead_scratch) != cudaSuccess || !p) {
+      *err = EAGLE_ERR_CUDA;
+      return nullptr;
+    }
+    ptr[dev] = p;
+  }
+  return ptr[dev];
+}
+
+}  // namespace
+
+extern "C" size_t eagle_lmhead_noalloc_max_scratch_bytes(void) { return kNoAllocScratchBytes; }
+
+extern "C" eagle_status eagle_lmhead_softmax_noalloc(eagle_dtype dtype, int T, int H, int V,
+                                                     float temperature, int mode,
+                                                     const void* d_h, const void* d_w,
+                                                     int32_t* d_argmax, float* d_row_max,
+                                                     float* d_row_lse, float* d_top2_gap,
+                                                     float* d_q, int* d_status,
+                                                     eagle_stream_t stream) {
+  EAGLE_HOST_CHECK(T >= 0 && V >= 1, EAGLE_ERR_INVALID_ARG);
+  // the partials of this call must fit the fixed scratch array
+  const size_t need = eagle_lmhead_workspace_bytes(T, V);
+  EAGLE_HOST_CHECK(need <= kNoAllocScratchBytes, EAGLE_ERR_WORKSPACE);
+  int err = EAGLE_OK;
+  void* scratch = noalloc_scratch(&err);
+  if (!scratch) return (eagle_status)err;
+  // nothing in the scratch needs clearing: every partial the finalize pass
+  // reads is written earlier in the same call
+  return eagle_lmhead_softmax(dtype, T, H, V, temperature, mode, d_h, d_w, d_argmax, d_row_max,
+                              d_row_lse, d_top2_gap, d_q, scratch, kNoAllocScratchBytes, d_status,
+                              stream);
+}

@@ -142,6 +142,41 @@ EAGLE_API eagle_status eagle_lmhead_softmax(eagle_dtype dtype, int T, int H, int
                                   size_t ws_bytes, int *d_status, eagle_stream_t stream);
 
 /* ------------------------------------------------------------------------
+ * eagle_lmhead_softmax_noalloc -- eagle_lmhead_softmax without a workspace
+ * argument.  The paper has no counterpart to this entry point.
+ *
+ * Some callers cannot hand the library a scratch buffer: code that runs
+ * while a CUDA graph is being captured in a mode that forbids cudaMalloc,
+ * plain-C hosts without an allocator of their own, or serving loops that run
+ * under a framework's pooled allocator and may not allocate (or pay the
+ * device synchronisation an allocation can cause) in the middle of a step.
+ * This entry point keeps the LM head's per-row partial statistics in a
+ * fixed array of the library's own device memory instead, and otherwise
+ * takes the same arguments and produces the same results as
+ * eagle_lmhead_softmax.  It calls no allocating routine.
+ *
+ *   - Limit: the call needs eagle_lmhead_workspace_bytes(T, V) bytes of
+ *     scratch; above eagle_lmhead_noalloc_max_scratch_bytes() (16 MiB) it
+ *     returns EAGLE_ERR_WORKSPACE and queues nothing.
+ *   - Every GPU that loads the library holds the 16 MiB array until the
+ *     process exits.
+ *   - The first call on each device looks up the array's device address
+ *     (with that device current); make that first call before any stream
+ *     capture on the device.
+ *   - All calls share the one array and it keeps the last call's contents.
+ *     Calls whose work can overlap on a GPU (different streams without
+ *     ordering between them) race on it and give undefined results; order
+ *     them on one stream or with events.
+ * ---------------------------------------------------------------------- */
+EAGLE_API size_t eagle_lmhead_noalloc_max_scratch_bytes(void);
+EAGLE_API eagle_status eagle_lmhead_softmax_noalloc(eagle_dtype dtype, int T, int H, int V,
+                                          float temperature, int mode, const void *d_h,
+                                          const void *d_w, int32_t *d_argmax,
+                                          float *d_row_max, float *d_row_lse,
+                                          float *d_top2_gap, float *d_q, int *d_status,
+                                          eagle_stream_t stream);
+
+/* ------------------------------------------------------------------------
  * eagle_accept_greedy -- greedy tree walk.
  * [S4000] greedy-decoding paragraph: match the target's most probable token
  * from the first draft on and stop at the first mismatch; on a tree, move to
