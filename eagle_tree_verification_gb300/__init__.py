@@ -48,7 +48,8 @@ _SIGS = {
     "eagle_status_string": ([_i], ctypes.c_char_p),
     "eagle_version": ([], ctypes.c_char_p),
     "eagle_tree_attn_workspace_bytes": ([_i] * 7, _sz),
-    "eagle_tree_attn": ([_i, _i, _i, _i, _i, _i, _f, _i, _i] + [_p] * 9 + [_p, _sz, _p, _p], _i),
+    "eagle_tree_attn": ([_i, _i, _i, _i, _i, _i, _f, _i, _i, _i] + [_p] * 9 + [_p, _sz, _p, _p],
+                        _i),
     "eagle_lmhead_workspace_bytes": ([_i, _i], _sz),
     "eagle_lmhead_softmax": ([_i, _i, _i, _i, _f, _i] + [_p] * 8 + [_sz, _p, _p], _i),
     "eagle_accept_greedy": ([_i, _i, _p, _p, _p, _p, _i, _p, _p, _p, _p, _p], _i),
@@ -168,6 +169,7 @@ def eagle_tree_attn(q, k_tree, v_tree, k_cache, v_cache, kv_off, tree_off, paren
     ws_bytes = 0 if ws is None else ws.numel() * ws.element_size()
     sc = (1.0 / D ** 0.5) if scale is None else float(scale)
     _call("eagle_tree_attn", _dtype_code(q), B, T, Hq, Hkv, D, sc, max_nodes, max_kv,
+          k_cache.shape[0],
           _ptr(q), _ptr(k_tree), _ptr(v_tree), _ptr(k_cache), _ptr(v_cache), _ptr(kv_off),
           _ptr(tree_off), _ptr(parent), _ptr(out), _ptr(ws), ws_bytes,
           _ptr(status), _stream(stream))

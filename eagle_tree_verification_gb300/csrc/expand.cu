@@ -21,20 +21,22 @@ namespace {
 
 constexpr int kExpandThreads = 256;
 constexpr int kChunkMax = 8192;     // floats staged per CTA
-constexpr int kFinalThreads = 512;
+constexpr int kFinalThreads = 256;
+constexpr int kMaxChunks = 64;      // chunks per row (V <= 64 * 8192)
 
 struct PoolLayout {
   int P;         // candidate capacity per sequence
   int rows_max;  // B * k
   int S0, S1;    // chunks per row at level 0 / later levels
-  size_t off_row_cnt, off_seq_cnt, off_count, off_frontier, off_token, off_parent, off_depth,
-      off_prow, off_score, off_rowtop, off_partial, total;
+  size_t off_row_cnt, off_seq_cnt, off_fin_cnt, off_count, off_frontier, off_token, off_parent,
+      off_depth, off_prow, off_score, off_sel, off_rowtop, off_partial, total;
 };
 
 int chunks_for(int rows, int V) {
-  int s = (304 + rows - 1) / rows;                 // ~2 CTAs per SM in total
-  s = std::max(s, (V + kChunkMax - 1) / kChunkMax);  // chunk fits in smem
+  int s = (304 + rows - 1) / rows;                   // ~2 CTAs per SM in total
+  s = std::min(s, kMaxChunks);                       // row merge fits in smem
   s = std::min(s, std::max(1, V / 512));             // chunks of >= 512 tokens
+  s = std::max(s, (V + kChunkMax - 1) / kChunkMax);  // chunk fits in smem
   return std::max(s, 1);
 }
 
@@ -55,6 +57,7 @@ PoolLayout pool_layout(int B, int k, int depth, int V) {
   };
   L.off_row_cnt = take((size_t)L.rows_max * 4);
   L.off_seq_cnt = take((size_t)B * 4);
+  L.off_fin_cnt = take((size_t)B * 4);
   L.off_count = take((size_t)B * 4);
   L.off_frontier = take((size_t)B * k * 4);
   L.off_token = take((size_t)B * L.P * 4);
@@ -62,6 +65,7 @@ PoolLayout pool_layout(int B, int k, int depth, int V) {
   L.off_depth = take((size_t)B * L.P * 4);
   L.off_prow = take((size_t)B * L.P * 4);
   L.off_score = take((size_t)B * L.P * 4);
+  L.off_sel = take((size_t)B * L.P * 4);
   L.off_rowtop = take((size_t)L.rows_max * k * 8);
   L.off_partial = take(parts * 8);
   L.total = o;
@@ -71,6 +75,7 @@ PoolLayout pool_layout(int B, int k, int depth, int V) {
 struct PoolPtrs {
   int* row_cnt;
   int* seq_cnt;
+  int* fin_cnt;
   int* count;
   int* frontier;
   int* token;
@@ -78,6 +83,7 @@ struct PoolPtrs {
   int* depth;
   int* prow;
   float* score;
+  int* sel;
   unsigned long long* rowtop;
   unsigned long long* partial;
 };
@@ -87,6 +93,7 @@ PoolPtrs pool_ptrs(void* base, const PoolLayout& L) {
   PoolPtrs p;
   p.row_cnt = reinterpret_cast<int*>(c + L.off_row_cnt);
   p.seq_cnt = reinterpret_cast<int*>(c + L.off_seq_cnt);
+  p.fin_cnt = reinterpret_cast<int*>(c + L.off_fin_cnt);
   p.count = reinterpret_cast<int*>(c + L.off_count);
   p.frontier = reinterpret_cast<int*>(c + L.off_frontier);
   p.token = reinterpret_cast<int*>(c + L.off_token);
@@ -94,25 +101,10 @@ PoolPtrs pool_ptrs(void* base, const PoolLayout& L) {
   p.depth = reinterpret_cast<int*>(c + L.off_depth);
   p.prow = reinterpret_cast<int*>(c + L.off_prow);
   p.score = reinterpret_cast<float*>(c + L.off_score);
+  p.sel = reinterpret_cast<int*>(c + L.off_sel);
   p.rowtop = reinterpret_cast<unsigned long long*>(c + L.off_rowtop);
   p.partial = reinterpret_cast<unsigned long long*>(c + L.off_partial);
   return p;
-}
-
-// Block-wide max of one key per thread (every thread gets it).
-__device__ unsigned long long block_max_u64(unsigned long long v, unsigned long long* s_tmp) {
-  v = warp_max_u64(v);
-  const int w = threadIdx.x >> 5, l = threadIdx.x & 31;
-  __syncthreads();
-  if (l == 0) s_tmp[w] = v;
-  __syncthreads();
-  if (w == 0) {
-    unsigned long long t = (l < (int)(blockDim.x >> 5)) ? s_tmp[l] : 0ull;
-    t = warp_max_u64(t);
-    if (l == 0) s_tmp[32] = t;
-  }
-  __syncthreads();
-  return s_tmp[32];
 }
 
 struct LevelParams {
@@ -122,14 +114,47 @@ struct LevelParams {
   int* status;
 };
 
+// Top-k keys of `n` candidates produced by key_of(i), by one warp: k rounds
+// of a warp max below the previous pick (no block barrier).  Lane 0 writes
+// the picks to out[0..k); 0 marks "nothing left".
+template <typename KeyOf>
+__device__ __forceinline__ void warp_topk(int n, int k, KeyOf key_of, unsigned long long* out) {
+  const int lane = threadIdx.x & 31;
+  unsigned long long last = ~0ull;
+  for (int r = 0; r < k; ++r) {
+    unsigned long long best = 0ull;
+    for (int i = lane; i < n; i += 32) {
+      const unsigned long long key = key_of(i);
+      if (key < last && key > best) best = key;
+    }
+    best = warp_max_u64(best);
+    if (lane == 0) out[r] = best;
+    last = best;
+  }
+}
+
+// Top-k of `n` candidate keys held in shared memory, by the whole block:
+// every warp selects from its slice, then warp 0 merges the warps' picks.
+__device__ void block_topk_smem(const unsigned long long* cand, int n, int k,
+                                unsigned long long* s_wtop, unsigned long long* out) {
+  const int warp = threadIdx.x >> 5, nw = blockDim.x >> 5;
+  const int per = (n + nw - 1) / nw;
+  const int lo = min(n, warp * per), cnt = min(n, lo + per) - lo;
+  warp_topk(cnt, k, [&](int i) { return cand[lo + i]; }, s_wtop + warp * k);
+  __syncthreads();
+  if (warp == 0) warp_topk(nw * k, k, [&](int i) { return s_wtop[i]; }, out);
+  __syncthreads();
+}
+
 __global__ void __launch_bounds__(kExpandThreads) expand_level_kernel(const LevelParams A) {
-  __shared__ float s_val[kChunkMax];
-  __shared__ unsigned long long s_tmp[33];
+  __shared__ __align__(16) float s_val[kChunkMax];
+  __shared__ unsigned long long s_wtop[(kExpandThreads / 32) * EAGLE_MAX_TOPK];
   __shared__ unsigned long long s_sel[EAGLE_MAX_TOPK];
   __shared__ unsigned long long s_cand[EAGLE_MAX_TOPK * EAGLE_MAX_TOPK];
   __shared__ int s_last;
 
   const int tid = threadIdx.x;
+  const int warp = tid >> 5, nw = blockDim.x >> 5;
   const int row = blockIdx.x / A.S;       // global frontier row: b * F + f
   const int chunk = blockIdx.x % A.S;
   const int b = row / A.F;
@@ -144,27 +169,26 @@ __global__ void __launch_bounds__(kExpandThreads) expand_level_kernel(const Leve
   // ---- stage the chunk, checking for non-finite values
   int bad = 0;
   for (int i = tid; i < n; i += blockDim.x) {
-    const float x = src[c0 + i];
+    const float x = __ldg(src + c0 + i);
     s_val[i] = x;
     bad |= !isfinite(x);
   }
   if (__syncthreads_or(bad) && tid == 0) fail(A.status, EAGLE_ERR_NUMERIC);
 
-  // ---- chunk top-k: k rounds of a block max below the previous pick
-  unsigned long long last = ~0ull;
-  for (int r = 0; r < k; ++r) {
-    unsigned long long best = 0ull;
-    for (int i = tid; i < n; i += blockDim.x) {
-      const unsigned long long key = desc_key(s_val[i], (uint32_t)(c0 + i));
-      if (key < last && key > best) best = key;
+  // ---- chunk top-k: each warp a slice, then warp 0 merges
+  {
+    const int per = (n + nw - 1) / nw;
+    const int lo = min(n, warp * per), cnt = min(n, lo + per) - lo;
+    warp_topk(cnt, k, [&](int i) { return desc_key(s_val[lo + i], (uint32_t)(c0 + lo + i)); },
+              s_wtop + warp * k);
+    __syncthreads();
+    if (warp == 0) {
+      unsigned long long* part = A.pool.partial + ((size_t)row * A.S + chunk) * k;
+      warp_topk(nw * k, k, [&](int i) { return s_wtop[i]; }, s_sel);
+      __syncwarp();
+      for (int r = tid; r < k; r += 32) part[r] = s_sel[r];
     }
-    best = block_max_u64(best, s_tmp);
-    if (tid == 0) s_sel[r] = best;  // 0 = no element left
-    last = best;
   }
-  __syncthreads();
-  unsigned long long* part = A.pool.partial + ((size_t)row * A.S + chunk) * k;
-  for (int r = tid; r < k; r += blockDim.x) part[r] = s_sel[r];
 
   // ---- last CTA of this row merges the chunk results
   __threadfence();
@@ -177,20 +201,14 @@ __global__ void __launch_bounds__(kExpandThreads) expand_level_kernel(const Leve
   __syncthreads();
   if (!s_last) return;
   __threadfence();
-  const unsigned long long* rparts = A.pool.partial + (size_t)row * A.S * k;
-  const int m = A.S * k;
-  last = ~0ull;
-  for (int r = 0; r < k; ++r) {
-    unsigned long long best = 0ull;
-    for (int i = tid; i < m; i += blockDim.x) {
-      const unsigned long long key = __ldcg(rparts + i);
-      if (key < last && key > best) best = key;
-    }
-    best = block_max_u64(best, s_tmp);
-    if (tid == 0) s_sel[r] = best;
-    last = best;
+  {
+    unsigned long long* s_keys = reinterpret_cast<unsigned long long*>(s_val);
+    const unsigned long long* rparts = A.pool.partial + (size_t)row * A.S * k;
+    const int m = A.S * k;                 // <= kMaxChunks * 32 keys = 16 KB
+    for (int i = tid; i < m; i += blockDim.x) s_keys[i] = __ldcg(rparts + i);
+    __syncthreads();
+    block_topk_smem(s_keys, m, k, s_wtop, s_sel);
   }
-  __syncthreads();
   for (int r = tid; r < k; r += blockDim.x) A.pool.rowtop[(size_t)row * k + r] = s_sel[r];
 
   // ---- last row of this sequence builds the children and the frontier
@@ -251,73 +269,88 @@ struct FinalParams {
   int* status;
 };
 
+// Selection: CTA (b, y) ranks candidates y*256 .. y*256+255 of sequence b
+// against all pool entries by (score desc, creation order) and flags the
+// top `budget`.  The last CTA of the sequence numbers the kept nodes by
+// (depth, score desc, creation order) and writes the tree.
 __global__ void __launch_bounds__(kFinalThreads) expand_finalize_kernel(const FinalParams A) {
   extern __shared__ __align__(16) unsigned char smem_raw[];
-  unsigned long long* s_key = reinterpret_cast<unsigned long long*>(smem_raw);
-  int* s_dep = reinterpret_cast<int*>(s_key + A.P);
-  int* s_sel = s_dep + A.P;
-  int* s_node = s_sel + A.P;
-  __shared__ int s_off, s_keep;
+  unsigned long long* s_key = reinterpret_cast<unsigned long long*>(smem_raw);  // [P]
+  int* s_list = reinterpret_cast<int*>(s_key + A.P);                            // [P]
+  int* s_num = s_list + A.P;                                                    // [P]
+  __shared__ int s_last, s_nsel;
   const int b = blockIdx.x;
   const int tid = threadIdx.x;
   const int n = A.pool.count[b];
-  if (tid == 0) {
-    int off = 0;
-    for (int j = 0; j < b; ++j) off += min(max(A.budget[j], 0), A.pool.count[j]) + 1;
-    s_off = off;
-    const int bud = A.budget[b];
-    if (bud < 0) fail(A.status, EAGLE_ERR_INVALID_ARG);
-    s_keep = min(max(bud, 0), n);
-    A.tree_off[b] = off;
-    if (b == A.B - 1) A.tree_off[A.B] = off + s_keep + 1;
+  const int bud = A.budget[b];
+  const int keep = min(max(bud, 0), n);
+  const float* sco = A.pool.score + (size_t)b * A.P;
+  int* sel = A.pool.sel + (size_t)b * A.P;
+  for (int i = tid; i < n; i += blockDim.x) s_key[i] = desc_key(sco[i], (uint32_t)i);
+  __syncthreads();
+  const int i = blockIdx.y * blockDim.x + tid;
+  if (i < n) {
+    const unsigned long long me = s_key[i];
+    int rank = 0;
+    for (int j = 0; j < n; ++j) rank += (s_key[j] > me);
+    sel[i] = (rank < keep);
   }
+  __threadfence();
+  __syncthreads();
+  if (tid == 0) {
+    const int prev = atomicAdd(&A.pool.fin_cnt[b], 1);
+    s_last = (prev == (int)gridDim.y - 1);
+    if (s_last) A.pool.fin_cnt[b] = 0;
+    s_nsel = 0;
+  }
+  __syncthreads();
+  if (!s_last) return;
+  __threadfence();
+  if (tid == 0 && bud < 0) fail(A.status, EAGLE_ERR_INVALID_ARG);
+  for (int j = tid; j < n; j += blockDim.x)
+    if (__ldcg(sel + j)) s_list[atomicAdd(&s_nsel, 1)] = j;
+  __syncthreads();
+  const int ns = s_nsel;
   const int* tok = A.pool.token + (size_t)b * A.P;
   const int* par = A.pool.parent + (size_t)b * A.P;
   const int* dep = A.pool.depth + (size_t)b * A.P;
   const int* prw = A.pool.prow + (size_t)b * A.P;
-  const float* sco = A.pool.score + (size_t)b * A.P;
-  for (int i = tid; i < n; i += blockDim.x) {
-    s_key[i] = desc_key(sco[i], (uint32_t)i);
-    s_dep[i] = dep[i];
-  }
-  __syncthreads();
-  const int keep = s_keep, off = s_off;
-  // selection: the `keep` largest keys (score desc, creation order)
-  for (int i = tid; i < n; i += blockDim.x) {
-    const unsigned long long me = s_key[i];
+  int off = 0;
+  for (int j = 0; j < b; ++j) off += min(max(A.budget[j], 0), A.pool.count[j]) + 1;
+  // node number of every kept entry: 1 + rank by (depth, score desc, creation)
+  for (int a = tid; a < ns; a += blockDim.x) {
+    const int ia = s_list[a];
+    const int da = dep[ia];
+    const unsigned long long ka = s_key[ia];
     int rank = 0;
-    for (int j = 0; j < n; ++j) rank += (s_key[j] > me);
-    s_sel[i] = (rank < keep);
-  }
-  __syncthreads();
-  // numbering of the kept nodes by (depth, score desc, creation order)
-  for (int i = tid; i < n; i += blockDim.x) {
-    if (!s_sel[i]) {
-      s_node[i] = -1;
-      continue;
+    for (int c = 0; c < ns; ++c) {
+      const int ic = s_list[c];
+      const int dc = dep[ic];
+      rank += (dc < da) || (dc == da && s_key[ic] > ka);
     }
-    const unsigned long long me = s_key[i];
-    const int d = s_dep[i];
-    int rank = 0;
-    for (int j = 0; j < n; ++j)
-      if (s_sel[j]) rank += (s_dep[j] < d) || (s_dep[j] == d && s_key[j] > me);
-    s_node[i] = 1 + rank;
+    s_num[a] = 1 + rank;
   }
   __syncthreads();
-  for (int i = tid; i < n; i += blockDim.x) {
-    const int node = s_node[i];
-    if (node < 0) continue;
-    const int pp = par[i];
-    const int pnode = (pp < 0) ? 0 : s_node[pp];
-    if (pnode < 0) fail(A.status, EAGLE_ERR_INVALID_TREE);  // not parent-closed
-    const int at = off + node;
+  for (int a = tid; a < ns; a += blockDim.x) {
+    const int ia = s_list[a];
+    const int pp = par[ia];
+    int pnode = 0;
+    if (pp >= 0) {
+      pnode = -1;
+      for (int c = 0; c < ns; ++c)
+        if (s_list[c] == pp) pnode = s_num[c];
+      if (pnode < 0) fail(A.status, EAGLE_ERR_INVALID_TREE);  // not parent-closed
+    }
+    const int at = off + s_num[a];
     A.parent[at] = pnode;
-    A.tokens[at] = tok[i];
-    A.node_depth[at] = s_dep[i];
-    A.score[at] = sco[i];
-    A.p_row_of_node[at] = b * A.R + prw[i];
+    A.tokens[at] = tok[ia];
+    A.node_depth[at] = dep[ia];
+    A.score[at] = sco[ia];
+    A.p_row_of_node[at] = b * A.R + prw[ia];
   }
   if (tid == 0) {
+    A.tree_off[b] = off;
+    if (b == A.B - 1) A.tree_off[A.B] = off + ns + 1;
     A.parent[off] = -1;
     A.tokens[off] = A.root_token ? A.root_token[b] : -1;
     A.node_depth[off] = 0;
@@ -329,7 +362,8 @@ __global__ void __launch_bounds__(kFinalThreads) expand_finalize_kernel(const Fi
 }  // namespace
 
 extern "C" size_t eagle_draft_pool_bytes(int B, int k, int depth, int V) {
-  if (B < 1 || k < 1 || k > EAGLE_MAX_TOPK || depth < 1 || depth > EAGLE_MAX_DEPTH || V < k)
+  if (B < 1 || k < 1 || k > EAGLE_MAX_TOPK || depth < 1 || depth > EAGLE_MAX_DEPTH || V < k ||
+      V > kMaxChunks * kChunkMax)
     return 0;
   return pool_layout(B, k, depth, V).total;
 }
@@ -345,6 +379,7 @@ extern "C" eagle_status eagle_draft_expand(int B, int V, int k, int depth, int l
   EAGLE_HOST_CHECK(B >= 1 && V >= 1, EAGLE_ERR_INVALID_ARG);
   EAGLE_HOST_CHECK(k >= 1 && k <= EAGLE_MAX_TOPK && k <= V, EAGLE_ERR_UNSUPPORTED);
   EAGLE_HOST_CHECK(depth >= 1 && depth <= EAGLE_MAX_DEPTH, EAGLE_ERR_UNSUPPORTED);
+  EAGLE_HOST_CHECK(V <= kMaxChunks * kChunkMax, EAGLE_ERR_UNSUPPORTED);
   EAGLE_HOST_CHECK(d_pool && d_status, EAGLE_ERR_INVALID_ARG);
   const PoolLayout L = pool_layout(B, k, depth, V);
   EAGLE_HOST_CHECK(pool_bytes >= L.total, EAGLE_ERR_WORKSPACE);
@@ -394,12 +429,13 @@ extern "C" eagle_status eagle_draft_expand(int B, int V, int k, int depth, int l
   F.score = d_score;
   F.p_row_of_node = d_p_row_of_node;
   F.status = d_status;
-  const size_t smem = (size_t)L.P * (8 + 4 + 4 + 4);
+  const size_t smem = (size_t)L.P * (8 + 4 + 4);
   EAGLE_HOST_CHECK(smem <= 200 * 1024, EAGLE_ERR_UNSUPPORTED);
-  if (smem > 48 * 1024) {
+  if (smem > 40 * 1024) {
     cudaFuncSetAttribute(expand_finalize_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                          (int)smem);
   }
-  expand_finalize_kernel<<<B, kFinalThreads, smem, s>>>(F);
+  dim3 fgrid(B, (L.P + kFinalThreads - 1) / kFinalThreads);
+  expand_finalize_kernel<<<fgrid, kFinalThreads, smem, s>>>(F);
   return launch_status(cudaGetLastError());
 }

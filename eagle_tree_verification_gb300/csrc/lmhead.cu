@@ -220,52 +220,77 @@ lmhead_finalize_kernel(int T, int V, float temperature, const Partial* __restric
 
 // ---------------------------------------------------------------------------
 // tcgen05 path
+//
+// MMA D[t, v] = sum_k h[t, k] W[v, k]: M = 128 tree rows (TMEM lanes; rows at
+// or past T are don't-care), N = 32 vocabulary rows per block, K in blocks of
+// 256 (four 64-element chunks, each a 128-byte-swizzled K-major tile).  A W
+// stage is 32 rows x 4 chunks = 16 KB whose per-row 512 bytes are contiguous
+// in HBM (four TMA boxes issued back to back); the h stage holds only the
+// real tree rows (T rounded up to 8).
 // ---------------------------------------------------------------------------
 constexpr int kTcThreads = 192;   // warp 0 TMA, warp 1 MMA, warps 2-5 epilogue
-constexpr int kBK = 64;           // bf16 per 128-byte swizzled row
-constexpr int kTileV = 128;       // vocab rows per MMA (the MMA's N)
-constexpr int kGroup = 4;         // tiles accumulated at once: 4 x 128 TMEM columns
-constexpr int kHStages = 3;
-constexpr int kWStages = 9;
-constexpr int kBlockBytes = 128 * 128;  // 128 rows x 128 bytes
-constexpr size_t kTcSmem = 1024 + (size_t)(kHStages + kWStages) * kBlockBytes + 512;
+constexpr int kBK = 64;           // bf16 per 128-byte swizzled row (one chunk)
+constexpr int kChunks = 4;        // chunks per K block (K block = 256)
+constexpr int kRowsBlk = 32;      // vocabulary rows per block (the MMA's N)
+constexpr int kMaxBlocks = 16;    // blocks accumulated at once: 16 x 32 TMEM columns
+constexpr int kHStages = 2;
+constexpr int kMaxWStages = 16;
+constexpr int kWStageBytes = kRowsBlk * 128 * kChunks;   // 16 KB
+constexpr size_t kSmemLimit = 227 * 1024;
+constexpr size_t kTcSharedBytes = 512;
 
 struct TcShared {
   uint64_t h_full[kHStages], h_empty[kHStages];
-  uint64_t w_full[kWStages], w_empty[kWStages];
+  uint64_t w_full[kMaxWStages], w_empty[kMaxWStages];
   uint64_t tmem_full, tmem_empty, drain;
   uint32_t tmem_base;
   int abort_flag;
   int consumed_w, consumed_h;
 };
 
+struct TcLayout {
+  int t_pad, h_stage_bytes, w_stages;
+  size_t smem;
+};
+
+TcLayout tc_layout(int T) {
+  TcLayout L;
+  L.t_pad = ((T + 7) / 8) * 8;
+  L.h_stage_bytes = L.t_pad * 128 * kChunks;
+  const size_t fixed = 1024 + (size_t)kHStages * L.h_stage_bytes + kTcSharedBytes;
+  L.w_stages = (int)std::min<size_t>(kMaxWStages, (kSmemLimit - fixed) / kWStageBytes);
+  L.smem = fixed + (size_t)L.w_stages * kWStageBytes;
+  return L;
+}
+
 __global__ void __launch_bounds__(kTcThreads, 1)
 lmhead_tc_kernel(const __grid_constant__ CUtensorMap map_h, const __grid_constant__ CUtensorMap map_w,
                  int T, int H, int V, float temperature, float* __restrict__ z_out,
-                 Partial* __restrict__ part, int n_units, int* status) {
+                 Partial* __restrict__ part, int n_units, int h_stage_bytes, int w_stages,
+                 int* status) {
   extern __shared__ __align__(1024) unsigned char smem_raw[];
   unsigned char* base = reinterpret_cast<unsigned char*>(
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~(uintptr_t)1023);
   unsigned char* h_smem = base;
-  unsigned char* w_smem = base + kHStages * kBlockBytes;
-  TcShared* sh = reinterpret_cast<TcShared*>(w_smem + kWStages * kBlockBytes);
+  unsigned char* w_smem = base + kHStages * h_stage_bytes;
+  TcShared* sh = reinterpret_cast<TcShared*>(w_smem + (size_t)w_stages * kWStageBytes);
+  const int h_chunk_bytes = h_stage_bytes / kChunks;     // t_pad rows x 128 B
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int G = gridDim.x;
-  // this CTA's slice of the vocabulary, in units of 16 rows
+  // this CTA's slice of the vocabulary, in blocks of 32 rows
   const int u0 = (int)((long long)n_units * blockIdx.x / G);
   const int u1 = (int)((long long)n_units * (blockIdx.x + 1) / G);
-  const int r_begin = u0 * 16, r_end = u1 * 16;
-  const int n_tiles = (r_end - r_begin + kTileV - 1) / kTileV;
-  const int n_groups = (n_tiles + kGroup - 1) / kGroup;
-  const int KB = (H + kBK - 1) / kBK;
+  const int n_blocks = u1 - u0;
+  const int n_groups = (n_blocks + kMaxBlocks - 1) / kMaxBlocks;
+  const int KB = (H + kBK * kChunks - 1) / (kBK * kChunks);
 
   if (threadIdx.x == 0) {
     for (int i = 0; i < kHStages; ++i) {
       tc::mbar_init(&sh->h_full[i], 1);
       tc::mbar_init(&sh->h_empty[i], 1);
     }
-    for (int i = 0; i < kWStages; ++i) {
+    for (int i = 0; i < w_stages; ++i) {
       tc::mbar_init(&sh->w_full[i], 1);
       tc::mbar_init(&sh->w_empty[i], 1);
     }
@@ -300,24 +325,25 @@ lmhead_tc_kernel(const __grid_constant__ CUtensorMap map_h, const __grid_constan
       uint32_t hph = 0, wph = 0;
       bool ok = true;
       for (int g = 0; g < n_groups && ok; ++g) {
-        const int j0 = g * kGroup, j1 = min(n_tiles, j0 + kGroup);
+        const int b0 = g * kMaxBlocks, b1 = min(n_blocks, b0 + kMaxBlocks);
         for (int kb = 0; kb < KB && ok; ++kb) {
           if (!(ok = tc::mbar_wait(&sh->h_empty[hs], hph ^ 1, abort_flag, status))) break;
-          tc::mbar_arrive_expect_tx(&sh->h_full[hs], kBlockBytes);
-          tc::tma_load_2d_hint(h_smem + hs * kBlockBytes, &map_h, &sh->h_full[hs], kb * kBK, 0,
-                               pol_h);
+          tc::mbar_arrive_expect_tx(&sh->h_full[hs], (uint32_t)h_stage_bytes);
+          for (int c = 0; c < kChunks; ++c)
+            tc::tma_load_2d_hint(h_smem + hs * h_stage_bytes + c * h_chunk_bytes, &map_h,
+                                 &sh->h_full[hs], (kb * kChunks + c) * kBK, 0, pol_h);
           ++issued_h;
           if (++hs == kHStages) { hs = 0; hph ^= 1; }
-          for (int j = j0; j < j1; ++j) {
-            const int row0 = r_begin + j * kTileV;
-            const int rows = min(kTileV, r_end - row0);
+          for (int blk = b0; blk < b1; ++blk) {
+            const int row0 = (u0 + blk) * kRowsBlk;
             if (!(ok = tc::mbar_wait(&sh->w_empty[ws], wph ^ 1, abort_flag, status))) break;
-            tc::mbar_arrive_expect_tx(&sh->w_full[ws], rows * 128);
-            for (int u = 0; u < rows; u += 16)
-              tc::tma_load_2d_hint(w_smem + ws * kBlockBytes + u * 128, &map_w, &sh->w_full[ws],
-                                   kb * kBK, row0 + u, pol_w);
+            tc::mbar_arrive_expect_tx(&sh->w_full[ws], kWStageBytes);
+            unsigned char* dst = w_smem + (size_t)ws * kWStageBytes;
+            for (int c = 0; c < kChunks; ++c)
+              tc::tma_load_2d_hint(dst + c * (kRowsBlk * 128), &map_w, &sh->w_full[ws],
+                                   (kb * kChunks + c) * kBK, row0, pol_w);
             ++issued_w;
-            if (++ws == kWStages) { ws = 0; wph ^= 1; }
+            if (++ws == w_stages) { ws = 0; wph ^= 1; }
           }
         }
       }
@@ -325,7 +351,7 @@ lmhead_tc_kernel(const __grid_constant__ CUtensorMap map_h, const __grid_constan
         // let every copy still in flight land before the CTA exits
         int never = 0;
         for (int i = *(volatile int*)&sh->consumed_w; i < issued_w; ++i)
-          tc::mbar_wait(&sh->w_full[i % kWStages], (i / kWStages) & 1, &never, nullptr,
+          tc::mbar_wait(&sh->w_full[i % w_stages], (i / w_stages) & 1, &never, nullptr,
                         200000000ll);
         for (int i = *(volatile int*)&sh->consumed_h; i < issued_h; ++i)
           tc::mbar_wait(&sh->h_full[i % kHStages], (i / kHStages) & 1, &never, nullptr,
@@ -337,31 +363,33 @@ lmhead_tc_kernel(const __grid_constant__ CUtensorMap map_h, const __grid_constan
     if (lane == 0) {
       int hs = 0, ws = 0;
       uint32_t hph = 0, wph = 0, tph = 0;
+      const uint32_t idesc = tc::idesc_bf16_f32(128, kRowsBlk);
       bool ok = true;
       for (int g = 0; g < n_groups && ok; ++g) {
-        const int j0 = g * kGroup, j1 = min(n_tiles, j0 + kGroup);
+        const int b0 = g * kMaxBlocks, b1 = min(n_blocks, b0 + kMaxBlocks);
         if (!(ok = tc::mbar_wait(&sh->tmem_empty, tph ^ 1, abort_flag, status))) break;
         tph ^= 1;
         tc::fence_after_thread_sync();
         for (int kb = 0; kb < KB && ok; ++kb) {
           if (!(ok = tc::mbar_wait(&sh->h_full[hs], hph, abort_flag, status))) break;
-          const uint32_t a_base = tc::smem_u32(h_smem + hs * kBlockBytes);
-          for (int j = j0; j < j1; ++j) {
-            const int rows = min(kTileV, r_end - (r_begin + j * kTileV));
+          const uint32_t a_base = tc::smem_u32(h_smem + hs * h_stage_bytes);
+          for (int blk = b0; blk < b1; ++blk) {
             if (!(ok = tc::mbar_wait(&sh->w_full[ws], wph, abort_flag, status))) break;
             tc::fence_after_thread_sync();
-            const uint32_t b_base = tc::smem_u32(w_smem + ws * kBlockBytes);
-            const uint32_t idesc = tc::idesc_bf16_f32(128, rows);
+            const uint32_t b_base = tc::smem_u32(w_smem + (size_t)ws * kWStageBytes);
+            const uint32_t d = tmem + (uint32_t)((blk - b0) * kRowsBlk);
 #pragma unroll
-            for (int k16 = 0; k16 < kBK / 16; ++k16) {
-              tc::mma_f16(tmem + (uint32_t)((j - j0) * kTileV),
-                          tc::desc_kmajor_sw128(a_base + k16 * 32),
-                          tc::desc_kmajor_sw128(b_base + k16 * 32), idesc,
-                          (kb > 0 || k16 > 0) ? 1u : 0u);
+            for (int c = 0; c < kChunks; ++c) {
+#pragma unroll
+              for (int k16 = 0; k16 < kBK / 16; ++k16) {
+                tc::mma_f16(d, tc::desc_kmajor_sw128(a_base + c * h_chunk_bytes + k16 * 32),
+                            tc::desc_kmajor_sw128(b_base + c * (kRowsBlk * 128) + k16 * 32), idesc,
+                            (kb > 0 || c > 0 || k16 > 0) ? 1u : 0u);
+              }
             }
             tc::mma_commit(&sh->w_empty[ws]);
             *(volatile int*)&sh->consumed_w += 1;
-            if (++ws == kWStages) { ws = 0; wph ^= 1; }
+            if (++ws == w_stages) { ws = 0; wph ^= 1; }
           }
           if (!ok) break;
           tc::mma_commit(&sh->h_empty[hs]);
@@ -387,62 +415,57 @@ lmhead_tc_kernel(const __grid_constant__ CUtensorMap map_h, const __grid_constan
     bool bad = false;
     uint32_t tph = 0;
     for (int g = 0; g < n_groups; ++g) {
-      const int j0 = g * kGroup, j1 = min(n_tiles, j0 + kGroup);
+      const int b0 = g * kMaxBlocks, b1 = min(n_blocks, b0 + kMaxBlocks);
       // every lane waits; the warp proceeds only if all of them saw the phase
       const bool got = tc::mbar_wait(&sh->tmem_full, tph, abort_flag, status);
       if (!__all_sync(0xffffffffu, got)) break;
       tph ^= 1;
       tc::fence_after_thread_sync();
-      for (int j = j0; j < j1; ++j) {
-        const int row0 = r_begin + j * kTileV;
-        const int rows = min(kTileV, r_end - row0);
-        for (int c = 0; c < rows; c += 32) {
-          float v[32];
-          tc::tmem_ld_32x32b_x32(tmem + ((uint32_t)(quad * 32) << 16) + (uint32_t)((j - j0) * kTileV + c), v);
-          const int vb = row0 + c;
-          const int nvalid = min(min(32, rows - c), V - vb);
-          if (!row_ok || nvalid <= 0) continue;
-          if (z_out) {
-            float* dst = z_out + (size_t)t * V + vb;
-            if (vec && nvalid == 32) {
+      for (int blk = b0; blk < b1; ++blk) {
+        float v[32];
+        tc::tmem_ld_32x32b_x32(tmem + ((uint32_t)(quad * 32) << 16) + (uint32_t)((blk - b0) * kRowsBlk), v);
+        const int vb = (u0 + blk) * kRowsBlk;
+        const int nvalid = min(32, V - vb);
+        if (!row_ok || nvalid <= 0) continue;
+        if (z_out) {
+          float* dst = z_out + (size_t)t * V + vb;
+          if (vec && nvalid == 32) {
 #pragma unroll
-              for (int i = 0; i < 32; i += 4)
-                *reinterpret_cast<float4*>(dst + i) = make_float4(v[i], v[i + 1], v[i + 2], v[i + 3]);
-            } else {
-#pragma unroll
-              for (int i = 0; i < 32; ++i)
-                if (i < nvalid) dst[i] = v[i];
-            }
-          }
-          float cm = -INFINITY, cs = -INFINITY;
-          int ci = 0;
-#pragma unroll
-          for (int i = 0; i < 32; ++i) {
-            const float x = (i < nvalid) ? v[i] : -INFINITY;
-            if (i < nvalid) bad |= !isfinite(x);
-            if (x > cm) {
-              cs = cm;
-              cm = x;
-              ci = i;
-            } else if (x > cs) {
-              cs = x;
-            }
-          }
-          if (cm > m) {
-            second = fmaxf(m, cs);
-            const float mn = cm;
-            s = (m == -INFINITY) ? 0.f : s * exp2f((m - mn) * k2);
-            m = mn;
-            idx = vb + ci;
+            for (int i = 0; i < 32; i += 4)
+              *reinterpret_cast<float4*>(dst + i) = make_float4(v[i], v[i + 1], v[i + 2], v[i + 3]);
           } else {
-            second = fmaxf(second, cm);
-          }
-          float acc = 0.f;
 #pragma unroll
-          for (int i = 0; i < 32; ++i)
-            if (i < nvalid) acc += exp2f((v[i] - m) * k2);
-          s += acc;
+            for (int i = 0; i < 32; ++i)
+              if (i < nvalid) dst[i] = v[i];
+          }
         }
+        float cm = -INFINITY, cs = -INFINITY;
+        int ci = 0;
+#pragma unroll
+        for (int i = 0; i < 32; ++i) {
+          const float x = (i < nvalid) ? v[i] : -INFINITY;
+          if (i < nvalid) bad |= !isfinite(x);
+          if (x > cm) {
+            cs = cm;
+            cm = x;
+            ci = i;
+          } else if (x > cs) {
+            cs = x;
+          }
+        }
+        if (cm > m) {
+          second = fmaxf(m, cs);
+          s = (m == -INFINITY) ? 0.f : s * exp2f((m - cm) * k2);
+          m = cm;
+          idx = vb + ci;
+        } else {
+          second = fmaxf(second, cm);
+        }
+        float acc = 0.f;
+#pragma unroll
+        for (int i = 0; i < 32; ++i)
+          if (i < nvalid) acc += exp2f((v[i] - m) * k2);
+        s += acc;
       }
       tc::fence_before_thread_sync();
       __syncwarp();
@@ -537,20 +560,22 @@ extern "C" eagle_status eagle_lmhead_softmax(eagle_dtype dtype, int T, int H, in
                      (((uintptr_t)d_h | (uintptr_t)d_w) & 15) == 0 &&
                      (!z || ((uintptr_t)z & 15) == 0);
   if (tc_ok) {
+    const TcLayout TL = tc_layout(T);
     CUtensorMap map_h, map_w;
-    if (!make_map_bf16(&map_h, d_h, T, H, 128) || !make_map_bf16(&map_w, d_w, V, H, 16))
+    if (!make_map_bf16(&map_h, d_h, T, H, TL.t_pad) || !make_map_bf16(&map_w, d_w, V, H, kRowsBlk))
       return EAGLE_ERR_CUDA;
     static bool attr = false;
     if (!attr) {
       if (cudaFuncSetAttribute(lmhead_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                               (int)kTcSmem) != cudaSuccess)
+                               (int)kSmemLimit) != cudaSuccess)
         return EAGLE_ERR_CUDA;
       attr = true;
     }
-    const int n_units = (V + 15) / 16;
+    const int n_units = (V + kRowsBlk - 1) / kRowsBlk;
     const int grid = std::min(sm_count(), n_units);
-    lmhead_tc_kernel<<<grid, kTcThreads, kTcSmem, s>>>(map_h, map_w, T, H, V, temperature, z,
-                                                        part, n_units, d_status);
+    lmhead_tc_kernel<<<grid, kTcThreads, TL.smem, s>>>(map_h, map_w, T, H, V, temperature, z,
+                                                        part, n_units, TL.h_stage_bytes,
+                                                        TL.w_stages, d_status);
     if (cudaGetLastError() != cudaSuccess) return EAGLE_ERR_CUDA;
     dim3 fgrid(T, z ? (V + kFinChunk - 1) / kFinChunk : 1);
     lmhead_finalize_kernel<<<fgrid, kFinThreads, 0, s>>>(T, V, temperature, part, grid, d_argmax,

@@ -96,19 +96,22 @@ EAGLE_API const char *eagle_version(void);
  * scale      softmax scale (usually 1/sqrt(D)).
  * max_nodes  upper bound on nodes of any one sequence (<= 256).
  * max_kv     upper bound on any sequence's cache length (>= 0).
+ * kv_rows    rows held by d_k_cache / d_v_cache (= kv_off[B]); nothing past
+ *            them is ever read.
  * d_q        [T,Hq,D];  d_k_tree, d_v_tree [T,Hkv,D] (K/V of the tree nodes).
  * d_k_cache, d_v_cache  packed caches [kv_off[B],Hkv,D].
  * d_kv_off   [B+1] int32, d_tree_off [B+1] int32, d_parent [T] int32 (local).
  * d_out      [T,Hq,D] fp32, written.
- * d_ws       scratch of eagle_tree_attn_workspace_bytes(...) bytes (may be
- *            NULL if that size is 0); contents need no initialisation.
+ * d_ws       scratch of eagle_tree_attn_workspace_bytes(...) bytes, 256-byte
+ *            aligned (may be NULL if that size is 0); contents need no
+ *            initialisation.
  * Device errors: INVALID_TREE (malformed parent[] or a sequence with more
  * than max_nodes nodes or a cache longer than max_kv).
  * ---------------------------------------------------------------------- */
 EAGLE_API size_t eagle_tree_attn_workspace_bytes(int B, int T, int Hq, int Hkv, int D,
                                        int max_nodes, int max_kv);
 EAGLE_API eagle_status eagle_tree_attn(eagle_dtype dtype, int B, int T, int Hq, int Hkv, int D,
-                             float scale, int max_nodes, int max_kv,
+                             float scale, int max_nodes, int max_kv, int kv_rows,
                              const void *d_q, const void *d_k_tree, const void *d_v_tree,
                              const void *d_k_cache, const void *d_v_cache,
                              const int32_t *d_kv_off, const int32_t *d_tree_off,

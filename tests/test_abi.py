@@ -55,11 +55,11 @@ def test_host_argument_checks_return_before_any_device_work(E):
     L = E.lib()
     null = None
     # head dim 96 is not implemented
-    assert L.eagle_tree_attn(1, 1, 4, 4, 4, 96, 0.1, 4, 0, *([null] * 9), null, 0, null, null) == 3
+    assert L.eagle_tree_attn(1, 1, 4, 4, 4, 96, 0.1, 4, 0, 0, *([null] * 9), null, 0, null, null) == 3
     # Hq not a multiple of Hkv
-    assert L.eagle_tree_attn(1, 1, 4, 6, 4, 128, 0.1, 4, 0, *([null] * 9), null, 0, null, null) == 3
+    assert L.eagle_tree_attn(1, 1, 4, 6, 4, 128, 0.1, 4, 0, 0, *([null] * 9), null, 0, null, null) == 3
     # NULL pointers with work to do
-    assert L.eagle_tree_attn(1, 1, 4, 4, 4, 128, 0.1, 4, 0, *([null] * 9), null, 0, null, null) == 1
+    assert L.eagle_tree_attn(1, 1, 4, 4, 4, 128, 0.1, 4, 0, 0, *([null] * 9), null, 0, null, null) == 1
     # more nodes than the implementation allows
     assert L.eagle_accept_greedy(1, 257, *([null] * 4), 3, *([null] * 5)) == 3
     # temperature must be positive
