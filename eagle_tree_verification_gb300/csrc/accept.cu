@@ -9,12 +9,13 @@
 // The stochastic walk is sequential in the tree but every rejection needs a
 // full-vocabulary pass (residual max(0, q - p) and its normaliser).  One
 // thread-block cluster serves one sequence: the vocabulary row is split into
-// `slice`-sized pieces, one per CTA, held in shared memory for the whole
-// node, so each visited node's q and p rows are read from HBM exactly once
-// and every rejection round runs out of shared memory.  Per-round integer
-// sums are exchanged through distributed shared memory; every CTA then
-// takes the identical decision (the data it decides on is bit-identical),
-// so control flow stays uniform across the cluster without any spin-wait.
+// `slice`-sized pieces, one per CTA, held in registers for the whole node,
+// so each visited node's q and p rows are read from HBM exactly once and
+// every rejection round runs out of registers.  Each round publishes its
+// integer sums (and the tested token's values) through distributed shared
+// memory behind one cluster barrier; every CTA then takes the identical
+// decision (the data it decides on is bit-identical), so control flow stays
+// uniform across the cluster without any spin-wait.
 #include <cooperative_groups.h>
 
 #include "common.cuh"
@@ -125,27 +126,51 @@ struct StochParams {
   int* status;
 };
 
-// trunc(x * 2^40) for x in [0, 1]: the scaling by a power of two is exact.
-__device__ __forceinline__ unsigned long long fixed40(float x) {
-  return __float2ull_rz(x * kTwo40);
-}
-
 __device__ __forceinline__ bool is_prob(float x) { return x >= 0.f && x <= 1.f; }
 
-// Sum over the block; every thread gets the total.  s_tmp: 33 entries.
-__device__ unsigned long long block_sum_u64(unsigned long long v, unsigned long long* s_tmp) {
-  v = warp_sum_u64(v);
+// Fixed-point weights.  For r in [0, 1], x = r * 2^40 is exact in fp32.
+// W = trunc(x) as an integer, and fp32(W) rounded to nearest, computed with
+// 32-bit operations only: below 2^23 x fits a 32-bit truncation; from 2^23
+// on every fp32 value is an integer, so W = x and fp32(W) = x.
+__device__ __forceinline__ unsigned long long fixed40_int(float r) {
+  const float x = r * kTwo40;
+  if (x < 8388608.f) return (unsigned long long)__float2uint_rz(x);
+  const uint32_t bits = __float_as_uint(x);
+  const int e = (int)(bits >> 23) - 127;                       // 23 .. 40
+  const unsigned long long m = (bits & 0x7fffffu) | 0x800000u;
+  return m << (e - 23);
+}
+__device__ __forceinline__ float fixed40_f(float r) {
+  const float x = r * kTwo40;
+  return (x < 8388608.f) ? __uint2float_rn(__float2uint_rz(x)) : x;
+}
+
+// Two sums over the block at once; every thread gets both totals.
+__device__ void block_sum2_u64(unsigned long long& a, unsigned long long& b,
+                               unsigned long long* s_tmp /* 66 */) {
+  a = warp_sum_u64(a);
+  b = warp_sum_u64(b);
   const int w = threadIdx.x >> 5, l = threadIdx.x & 31;
   __syncthreads();
-  if (l == 0) s_tmp[w] = v;
-  __syncthreads();
-  if (w == 0) {
-    unsigned long long t = (l < (int)(blockDim.x >> 5)) ? s_tmp[l] : 0ull;
-    t = warp_sum_u64(t);
-    if (l == 0) s_tmp[32] = t;
+  if (l == 0) {
+    s_tmp[w] = a;
+    s_tmp[33 + w] = b;
   }
   __syncthreads();
-  return s_tmp[32];
+  if (w == 0) {
+    const int nw = blockDim.x >> 5;
+    unsigned long long x = (l < nw) ? s_tmp[l] : 0ull;
+    unsigned long long y = (l < nw) ? s_tmp[33 + l] : 0ull;
+    x = warp_sum_u64(x);
+    y = warp_sum_u64(y);
+    if (l == 0) {
+      s_tmp[32] = x;
+      s_tmp[65] = y;
+    }
+  }
+  __syncthreads();
+  a = s_tmp[32];
+  b = s_tmp[65];
 }
 
 // Exclusive scan over the block of one value per thread; returns the
@@ -179,21 +204,15 @@ __device__ unsigned long long block_excl_scan_u64(unsigned long long v, unsigned
   return s_tmp[w] + inc - v;
 }
 
-// Sum of one u64 published by every CTA of the cluster (read through DSMEM).
-__device__ unsigned long long cluster_sum(cg::cluster_group& cluster, unsigned long long* s_slot,
-                                          unsigned CS, unsigned upto,
-                                          unsigned long long* s_bcast) {
-  if (threadIdx.x < 32) {
-    unsigned long long v = 0;
-    if (threadIdx.x < upto && threadIdx.x < CS)
-      v = *cluster.map_shared_rank(s_slot, threadIdx.x);
-    v = warp_sum_u64(v);
-    if (threadIdx.x == 0) *s_bcast = v;
-  }
-  __syncthreads();
-  return *s_bcast;
-}
+// What each CTA publishes to the cluster in one rejection round.
+struct RoundSlot {
+  unsigned long long w;   // sum of the residual weights of this CTA's slice
+  unsigned long long p;   // sum of the draft weights (rejected token excluded)
+  float qt, pt;           // q_k[t], p_k[t] if this CTA owns the tested token t
+};
 
+// Element e of thread `tid` is vocabulary entry v0 + tid + kStochThreads*e.
+template <int E>
 __global__ void __launch_bounds__(kStochThreads)
 accept_stochastic_kernel(const StochParams P) {
   cg::cluster_group cluster = cg::this_cluster();
@@ -203,14 +222,15 @@ accept_stochastic_kernel(const StochParams P) {
   const int tid = threadIdx.x;
 
   extern __shared__ __align__(16) unsigned char smem_raw[];
-  float* qs = reinterpret_cast<float*>(smem_raw);
-  float* ps = qs + P.slice;
-  int* s_par = reinterpret_cast<int*>(ps + P.slice);
+  float* s_q = reinterpret_cast<float*>(smem_raw);            // slice, for sampling
+  int* s_par = reinterpret_cast<int*>(s_q + P.slice);
   int* s_tok = s_par + P.max_nodes;
   int* s_kids = s_tok + P.max_nodes;
-  __shared__ unsigned long long s_red[33];
-  __shared__ unsigned long long s_w, s_p, s_tot;  // published to the cluster
-  __shared__ unsigned long long s_bc0, s_bc1;
+  __shared__ unsigned long long s_red[66];
+  __shared__ RoundSlot s_slot[2];            // double-buffered by round parity
+  __shared__ unsigned long long s_tot;
+  __shared__ unsigned long long s_bc[2];
+  __shared__ float s_test[2];
   __shared__ int s_flag, s_nk;
 
   const int v0 = (int)rank * P.slice;
@@ -227,8 +247,8 @@ accept_stochastic_kernel(const StochParams P) {
   }
   const int t0 = P.tree_off[b];
   const int n = P.tree_off[b + 1] - t0;
-  // All checks below read the same global data in every CTA, so the
-  // early exits are taken by the whole cluster together.
+  // All checks below read the same global data in every CTA, so the early
+  // exits are taken by the whole cluster together.
   if (n < 1 || n > P.max_nodes) {
     if (writer && tid == 0) {
       fail(P.status, EAGLE_ERR_INVALID_TREE);
@@ -239,11 +259,11 @@ accept_stochastic_kernel(const StochParams P) {
   if (tid == 0) s_flag = 0;
   __syncthreads();
   for (int i = tid; i < n; i += blockDim.x) {
-    const int p = P.parent[t0 + i];
+    const int pp = P.parent[t0 + i];
     const int tk = P.tokens[t0 + i];
-    s_par[i] = p;
+    s_par[i] = pp;
     s_tok[i] = tk;
-    if ((i == 0) ? (p != -1) : (p < 0 || p >= i)) atomicOr(&s_flag, 1);
+    if ((i == 0) ? (pp != -1) : (pp < 0 || pp >= i)) atomicOr(&s_flag, 1);
     if (i > 0 && (tk < 0 || tk >= P.V)) atomicOr(&s_flag, 2);
   }
   __syncthreads();
@@ -256,14 +276,12 @@ accept_stochastic_kernel(const StochParams P) {
   }
 
   const bool no_replace = (P.mode == EAGLE_SAMPLE_NO_REPLACE);
-  const bool vec4 = ((P.V & 3) == 0);
-  int cur = 0, alpha = 0;
+  float q[E], p[E];
+  int cur = 0, alpha = 0, par = 0;
   bool stop = false;
   if (writer && tid == 0) o_nodes[0] = 0;
 
   while (true) {
-    // No CTA may still read our slices (DSMEM) when we overwrite them.
-    cluster.sync();
     if (tid == 0) {
       int c = 0;
       for (int i = cur + 1; i < n; ++i)
@@ -272,7 +290,7 @@ accept_stochastic_kernel(const StochParams P) {
     }
     __syncthreads();
     const int nk = s_nk;
-    int prow = -1;
+    int prow = 0;
     if (nk > 0) {
       prow = P.p_row_of_node[t0 + s_kids[0]];
       if (prow < 0 || prow >= P.R) {  // uniform
@@ -281,34 +299,22 @@ accept_stochastic_kernel(const StochParams P) {
         break;
       }
     }
-    // Stage this CTA's slice of q[cur] (and of the draft row) in shared memory.
+    // this CTA's slice of q[cur] (and of the draft row) into registers
     {
       const float* qrow = P.q + (size_t)(t0 + cur) * P.V + v0;
-      const float* prw = P.p_rows + (size_t)max(prow, 0) * P.V + v0;
+      const float* prw = P.p_rows + (size_t)prow * P.V + v0;
       int bad = 0;
-      if (vec4) {
-        const int n4 = nv >> 2;
-        const float4* q4 = reinterpret_cast<const float4*>(qrow);
-        const float4* p4 = reinterpret_cast<const float4*>(prw);
-        for (int i = tid; i < n4; i += blockDim.x) {
-          const float4 a = __ldg(q4 + i);
-          reinterpret_cast<float4*>(qs)[i] = a;
-          bad |= !(is_prob(a.x) && is_prob(a.y) && is_prob(a.z) && is_prob(a.w));
+#pragma unroll
+      for (int e = 0; e < E; ++e) {
+        const int i = tid + e * kStochThreads;
+        q[e] = 0.f;
+        p[e] = 0.f;
+        if (i < nv) {
+          q[e] = __ldg(qrow + i);
+          bad |= !is_prob(q[e]);
           if (nk > 0) {
-            const float4 c = __ldg(p4 + i);
-            reinterpret_cast<float4*>(ps)[i] = c;
-            bad |= !(is_prob(c.x) && is_prob(c.y) && is_prob(c.z) && is_prob(c.w));
-          }
-        }
-      } else {
-        for (int i = tid; i < nv; i += blockDim.x) {
-          const float a = qrow[i];
-          qs[i] = a;
-          bad |= !is_prob(a);
-          if (nk > 0) {
-            const float c = prw[i];
-            ps[i] = c;
-            bad |= !is_prob(c);
+            p[e] = __ldg(prw + i);
+            bad |= !is_prob(p[e]);
           }
         }
       }
@@ -319,11 +325,45 @@ accept_stochastic_kernel(const StochParams P) {
     for (int j = 0; j < nk; ++j) {
       const int c = s_kids[j];
       const int t = s_tok[c];
-      cluster.sync();  // every slice holds round-k values
-      const unsigned owner = (unsigned)(t / P.slice);
-      const int off = t - (int)owner * P.slice;
-      const float qt = *cluster.map_shared_rank(qs + off, owner);
-      const float pt = *cluster.map_shared_rank(ps + off, owner);
+      // sums as if child c were rejected, and the tested values q_k[t], p_k[t]
+      unsigned long long sw = 0, sp = 0;
+#pragma unroll
+      for (int e = 0; e < E; ++e) {
+        const int i = tid + e * kStochThreads;
+        sw += fixed40_int(fmaxf(0.f, __fsub_rn(q[e], p[e])));
+        if (no_replace && v0 + i != t) sp += fixed40_int(p[e]);
+        if (i < nv && v0 + i == t) {
+          s_slot[par].qt = q[e];
+          s_slot[par].pt = p[e];
+        }
+      }
+      block_sum2_u64(sw, sp, s_red);
+      if (tid == 0) {
+        s_slot[par].w = sw;
+        s_slot[par].p = sp;
+      }
+      cluster.sync();
+      if (tid < 32) {
+        unsigned long long a = 0, bb = 0;
+        if (tid < (int)CS) {
+          const RoundSlot* r = cluster.map_shared_rank(&s_slot[par], tid);
+          a = r->w;
+          bb = r->p;
+        }
+        a = warp_sum_u64(a);
+        bb = warp_sum_u64(bb);
+        if (tid == 0) {
+          s_bc[0] = a;
+          s_bc[1] = bb;
+          const RoundSlot* o = cluster.map_shared_rank(&s_slot[par], (unsigned)(t / P.slice));
+          s_test[0] = o->qt;
+          s_test[1] = o->pt;
+        }
+      }
+      __syncthreads();
+      const unsigned long long Z = s_bc[0], SP = s_bc[1];
+      const float qt = s_test[0], pt = s_test[1];
+      par ^= 1;
       const float ua = P.u_accept[t0 + c];
       if (!(ua >= 0.f && ua < 1.f) && writer && tid == 0) fail(P.status, EAGLE_ERR_INVALID_ARG);
       // exact: a product of two fp32 values is exact in fp64
@@ -343,50 +383,52 @@ accept_stochastic_kernel(const StochParams P) {
         moved = true;
         break;
       }
-      // rejected: integer normalisers of the residual (and of the draft row)
-      unsigned long long sw = 0, sp = 0;
-      for (int i = tid; i < nv; i += blockDim.x) {
-        const float qa = qs[i], pa = ps[i];
-        sw += fixed40(fmaxf(0.f, __fsub_rn(qa, pa)));
-        if (no_replace && v0 + i != t) sp += fixed40(pa);
-      }
-      sw = block_sum_u64(sw, s_red);
-      if (no_replace) sp = block_sum_u64(sp, s_red);
-      if (tid == 0) {
-        s_w = sw;
-        s_p = sp;
-      }
-      cluster.sync();
-      const unsigned long long Z = cluster_sum(cluster, &s_w, CS, CS, &s_bc0);
-      const unsigned long long SP = no_replace ? cluster_sum(cluster, &s_p, CS, CS, &s_bc1) : 0ull;
+      // rejected: q_{k+1} = fp32(W)/fp32(Z), p_{k+1} likewise (NO_REPLACE)
       const float Zf = __ull2float_rn(Z);
       const float SPf = __ull2float_rn(SP);
-      for (int i = tid; i < nv; i += blockDim.x) {
-        const float qa = qs[i], pa = ps[i];
-        if (Z > 0ull)
-          qs[i] = __fdiv_rn(__ull2float_rn(fixed40(fmaxf(0.f, __fsub_rn(qa, pa)))), Zf);
-        if (no_replace) {
-          const unsigned long long Pj = (v0 + i == t) ? 0ull : fixed40(pa);
-          ps[i] = (SP > 0ull) ? __fdiv_rn(__ull2float_rn(Pj), SPf) : 0.f;
-        }
+#pragma unroll
+      for (int e = 0; e < E; ++e) {
+        const int i = tid + e * kStochThreads;
+        const float qa = q[e], pa = p[e];
+        if (Z > 0ull) q[e] = __fdiv_rn(fixed40_f(fmaxf(0.f, __fsub_rn(qa, pa))), Zf);
+        if (no_replace)
+          p[e] = (v0 + i == t || SP == 0ull) ? 0.f : __fdiv_rn(fixed40_f(pa), SPf);
       }
     }
     if (moved) continue;
     if (stop) break;
 
     // Bonus token: inverse CDF of the current q over integer weights.
-    cluster.sync();  // updated slices complete
+#pragma unroll
+    for (int e = 0; e < E; ++e) {
+      const int i = tid + e * kStochThreads;
+      if (i < nv) s_q[i] = q[e];
+    }
+    __syncthreads();
     {
       const int per = (nv + (int)blockDim.x - 1) / (int)blockDim.x;
       const int c0 = min(nv, tid * per), c1 = min(nv, c0 + per);
       unsigned long long mine = 0;
-      for (int i = c0; i < c1; ++i) mine += fixed40(qs[i]);
+      for (int i = c0; i < c1; ++i) mine += fixed40_int(s_q[i]);
       unsigned long long cta_total;
       const unsigned long long excl = block_excl_scan_u64(mine, s_red, &cta_total);
       if (tid == 0) s_tot = cta_total;
       cluster.sync();
-      const unsigned long long before = cluster_sum(cluster, &s_tot, CS, rank, &s_bc0);
-      const unsigned long long Z = cluster_sum(cluster, &s_tot, CS, CS, &s_bc1);
+      if (tid < 32) {
+        unsigned long long all = 0, before = 0;
+        if (tid < (int)CS) {
+          all = *cluster.map_shared_rank(&s_tot, tid);
+          before = (tid < (int)rank) ? all : 0ull;
+        }
+        all = warp_sum_u64(all);
+        before = warp_sum_u64(before);
+        if (tid == 0) {
+          s_bc[0] = before;
+          s_bc[1] = all;
+        }
+      }
+      __syncthreads();
+      const unsigned long long before = s_bc[0], Z = s_bc[1];
       const float us = P.u_sample[t0 + cur];
       if (!(us >= 0.f && us < 1.f)) {
         if (writer && tid == 0) fail(P.status, EAGLE_ERR_INVALID_ARG);
@@ -402,7 +444,7 @@ accept_stochastic_kernel(const StochParams P) {
           if (local >= excl && local < excl + mine) {
             unsigned long long acc = excl;
             for (int i = c0; i < c1; ++i) {
-              acc += fixed40(qs[i]);
+              acc += fixed40_int(s_q[i]);
               if (acc > local) {
                 o_tok[alpha] = v0 + i;
                 break;
@@ -419,19 +461,17 @@ accept_stochastic_kernel(const StochParams P) {
   cluster.sync();
 }
 
-// Largest cluster the device can co-schedule for this kernel and smem size.
-int pick_cluster(int V, int max_nodes, int* slice_out, size_t* smem_out) {
-  const size_t node_bytes = (size_t)max_nodes * 3 * sizeof(int);
-  const size_t budget = 200 * 1024;
+// Cluster size and per-thread element count for a vocabulary: slices of
+// at most 512 x 32 entries; prefer <= 512 x 16 (registers), up to 16 CTAs.
+int pick_cluster(int V, int* slice_out, int* elems_out) {
   for (int cs = 1; cs <= 16; cs <<= 1) {
     int slice = (V + cs - 1) / cs;
     slice = (slice + 3) & ~3;
-    const size_t smem = (size_t)slice * 2 * sizeof(float) + node_bytes;
-    // prefer slices of <= 8K floats (64 KB): up to three CTAs per SM
-    if (cs < 16 && slice > 8192) continue;
-    if (smem > budget) return -1;
+    const int e = (slice + kStochThreads - 1) / kStochThreads;
+    if (e > 16 && cs < 16) continue;
+    if (e > 32) return -1;
     *slice_out = slice;
-    *smem_out = smem;
+    *elems_out = e <= 4 ? 4 : e <= 8 ? 8 : e <= 16 ? 16 : 32;
     return cs;
   }
   return -1;
@@ -474,19 +514,20 @@ extern "C" eagle_status eagle_accept_stochastic(
                        d_status,
                    EAGLE_ERR_INVALID_ARG);
   EAGLE_HOST_CHECK(R == 0 || d_p_rows, EAGLE_ERR_INVALID_ARG);
-  EAGLE_HOST_CHECK(((V & 3) != 0) ||
-                       ((((uintptr_t)d_q) & 15) == 0 && (((uintptr_t)d_p_rows) & 15) == 0),
-                   EAGLE_ERR_INVALID_ARG);
-  int slice = 0;
-  size_t smem = 0;
-  const int cs = pick_cluster(V, max_nodes, &slice, &smem);
+  int slice = 0, elems = 0;
+  const int cs = pick_cluster(V, &slice, &elems);
   EAGLE_HOST_CHECK(cs > 0, EAGLE_ERR_UNSUPPORTED);
-  static bool attr_done = false;
-  if (!attr_done) {
-    cudaFuncSetAttribute(accept_stochastic_kernel, cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
-    cudaFuncSetAttribute(accept_stochastic_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                         200 * 1024);
-    attr_done = true;
+  const size_t smem = (size_t)slice * sizeof(float) + (size_t)max_nodes * 3 * sizeof(int);
+  void (*kern)(const StochParams) = elems == 4    ? accept_stochastic_kernel<4>
+                                    : elems == 8  ? accept_stochastic_kernel<8>
+                                    : elems == 16 ? accept_stochastic_kernel<16>
+                                                  : accept_stochastic_kernel<32>;
+  static bool attr_done[4] = {false, false, false, false};
+  const int ai = elems == 4 ? 0 : elems == 8 ? 1 : elems == 16 ? 2 : 3;
+  if (!attr_done[ai]) {
+    cudaFuncSetAttribute(kern, cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
+    cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, 160 * 1024);
+    attr_done[ai] = true;
   }
   StochParams P;
   P.max_nodes = max_nodes;
@@ -520,5 +561,5 @@ extern "C" eagle_status eagle_accept_stochastic(
   attr[0].val.clusterDim.z = 1;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
-  return launch_status(cudaLaunchKernelEx(&cfg, accept_stochastic_kernel, P));
+  return launch_status(cudaLaunchKernelEx(&cfg, kern, P));
 }
