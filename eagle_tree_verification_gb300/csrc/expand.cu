@@ -114,35 +114,57 @@ struct LevelParams {
   int* status;
 };
 
-// Top-k keys of `n` candidates produced by key_of(i), by one warp: k rounds
-// of a warp max below the previous pick (no block barrier).  Lane 0 writes
-// the picks to out[0..k); 0 marks "nothing left".
-template <typename KeyOf>
-__device__ __forceinline__ void warp_topk(int n, int k, KeyOf key_of, unsigned long long* out) {
-  const int lane = threadIdx.x & 31;
-  unsigned long long last = ~0ull;
-  for (int r = 0; r < k; ++r) {
-    unsigned long long best = 0ull;
-    for (int i = lane; i < n; i += 32) {
-      const unsigned long long key = key_of(i);
-      if (key < last && key > best) best = key;
-    }
-    best = warp_max_u64(best);
-    if (lane == 0) out[r] = best;
-    last = best;
-  }
+__device__ __forceinline__ unsigned long long shfl_u64(unsigned long long v, int src) {
+  return __shfl_sync(0xffffffffu, v, src);
+}
+__device__ __forceinline__ unsigned long long shfl_up_u64(unsigned long long v, int d) {
+  return __shfl_up_sync(0xffffffffu, v, d);
 }
 
-// Top-k of `n` candidate keys held in shared memory, by the whole block:
-// every warp selects from its slice, then warp 0 merges the warps' picks.
+// Top-k keys of `n` candidates produced by key_of(i), by one warp in one
+// pass.  Lane j holds the j-th largest key seen so far (0 = empty); a batch
+// of 32 candidates is filtered by one ballot against the current k-th key,
+// and the few survivors are inserted by shifting the list down one lane.
+// Keys are unique, so the order is total.  Returns this lane's list entry.
+template <typename KeyOf>
+__device__ __forceinline__ unsigned long long warp_topk_list(int n, int k, KeyOf key_of) {
+  const int lane = threadIdx.x & 31;
+  unsigned long long mine = 0ull, thr = 0ull;
+  for (int base = 0; base < n; base += 32) {
+    const int i = base + lane;
+    const unsigned long long key = (i < n) ? key_of(i) : 0ull;
+    unsigned bal = __ballot_sync(0xffffffffu, key > thr);
+    while (bal) {
+      const int src = __ffs(bal) - 1;
+      bal &= bal - 1;
+      const unsigned long long cand = shfl_u64(key, src);
+      if (cand <= thr) continue;  // uniform: the threshold may have risen
+      const int pos = __popc(__ballot_sync(0xffffffffu, lane < k && mine > cand));
+      const unsigned long long up = shfl_up_u64(mine, 1);
+      if (lane < k) {
+        if (lane > pos) mine = up;
+        else if (lane == pos) mine = cand;
+      }
+      thr = shfl_u64(mine, k - 1);
+    }
+  }
+  return mine;
+}
+
+// Top-k of `n` keys in shared memory by the whole block: every warp selects
+// from its slice, then warp 0 merges the warps' lists into out[0..k).
 __device__ void block_topk_smem(const unsigned long long* cand, int n, int k,
                                 unsigned long long* s_wtop, unsigned long long* out) {
-  const int warp = threadIdx.x >> 5, nw = blockDim.x >> 5;
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31, nw = blockDim.x >> 5;
   const int per = (n + nw - 1) / nw;
   const int lo = min(n, warp * per), cnt = min(n, lo + per) - lo;
-  warp_topk(cnt, k, [&](int i) { return cand[lo + i]; }, s_wtop + warp * k);
+  const unsigned long long mine = warp_topk_list(cnt, k, [&](int i) { return cand[lo + i]; });
+  if (lane < k) s_wtop[warp * k + lane] = mine;
   __syncthreads();
-  if (warp == 0) warp_topk(nw * k, k, [&](int i) { return s_wtop[i]; }, out);
+  if (warp == 0) {
+    const unsigned long long top = warp_topk_list(nw * k, k, [&](int i) { return s_wtop[i]; });
+    if (lane < k) out[lane] = top;
+  }
   __syncthreads();
 }
 
@@ -177,16 +199,18 @@ __global__ void __launch_bounds__(kExpandThreads) expand_level_kernel(const Leve
 
   // ---- chunk top-k: each warp a slice, then warp 0 merges
   {
+    const int lane = tid & 31;
     const int per = (n + nw - 1) / nw;
     const int lo = min(n, warp * per), cnt = min(n, lo + per) - lo;
-    warp_topk(cnt, k, [&](int i) { return desc_key(s_val[lo + i], (uint32_t)(c0 + lo + i)); },
-              s_wtop + warp * k);
+    const unsigned long long mine = warp_topk_list(
+        cnt, k, [&](int i) { return desc_key(s_val[lo + i], (uint32_t)(c0 + lo + i)); });
+    if (lane < k) s_wtop[warp * k + lane] = mine;
     __syncthreads();
     if (warp == 0) {
       unsigned long long* part = A.pool.partial + ((size_t)row * A.S + chunk) * k;
-      warp_topk(nw * k, k, [&](int i) { return s_wtop[i]; }, s_sel);
-      __syncwarp();
-      for (int r = tid; r < k; r += 32) part[r] = s_sel[r];
+      const unsigned long long top =
+          warp_topk_list(nw * k, k, [&](int i) { return s_wtop[i]; });
+      if (lane < k) part[lane] = top;
     }
   }
 
@@ -249,6 +273,7 @@ __global__ void __launch_bounds__(kExpandThreads) expand_level_kernel(const Leve
   for (int c = tid; c < nc; c += blockDim.x) {
     const unsigned long long me = s_cand[c];
     int rank = 0;
+#pragma unroll 8
     for (int j = 0; j < nc; ++j) rank += (s_cand[j] > me);
     if (rank < k) front[rank] = base + c;
   }
@@ -291,9 +316,16 @@ __global__ void __launch_bounds__(kFinalThreads) expand_finalize_kernel(const Fi
   const int i = blockIdx.y * blockDim.x + tid;
   if (i < n) {
     const unsigned long long me = s_key[i];
-    int rank = 0;
-    for (int j = 0; j < n; ++j) rank += (s_key[j] > me);
-    sel[i] = (rank < keep);
+    int r0 = 0, r1 = 0, r2 = 0, r3 = 0;
+    int j = 0;
+    for (; j + 4 <= n; j += 4) {
+      r0 += (s_key[j] > me);
+      r1 += (s_key[j + 1] > me);
+      r2 += (s_key[j + 2] > me);
+      r3 += (s_key[j + 3] > me);
+    }
+    for (; j < n; ++j) r0 += (s_key[j] > me);
+    sel[i] = (r0 + r1 + r2 + r3 < keep);
   }
   __threadfence();
   __syncthreads();

@@ -6,15 +6,15 @@
 // head gives the next-token distribution of every node.
 //
 // Kernels:
-//   lmhead_tc_kernel       bf16, up to 128 rows: persistent tcgen05 GEMM.  Each
+//   lmhead_tc_kernel       bf16, 128 rows per launch: persistent tcgen05 GEMM.  Each
 //                          CTA owns a contiguous slice of the vocabulary and
 //                          streams its rows of W once through a TMA ring;
 //                          tree rows sit on TMEM lanes, so every thread owns
 //                          one row and its softmax statistics are thread-local.
 //                          One partial per (row, CTA).
-//   lmhead_tile_kernel     CUDA-core fallback for fp32 inputs (tensor cores
-//                          would round them to tf32) and for more than 128
-//                          rows: per-(row, 64-vocab tile) partials.
+//   lmhead_tile_kernel     CUDA-core kernel for fp32 inputs (tensor cores
+//                          would round them to tf32): per-(row, 64-vocab
+//                          tile) partials.
 //   lmhead_finalize_kernel per (row, vocab chunk): combines the partials of
 //                          the row; in PROB mode rewrites z as softmax(z/T).
 #include <math.h>
@@ -265,9 +265,10 @@ TcLayout tc_layout(int T) {
 
 __global__ void __launch_bounds__(kTcThreads, 1)
 lmhead_tc_kernel(const __grid_constant__ CUtensorMap map_h, const __grid_constant__ CUtensorMap map_w,
-                 int T, int H, int V, float temperature, float* __restrict__ z_out,
-                 Partial* __restrict__ part, int n_units, int h_stage_bytes, int w_stages,
-                 int* status) {
+                 const __grid_constant__ CUtensorMap map_h3,
+                 const __grid_constant__ CUtensorMap map_w3, int use3d, int T, int H, int V,
+                 float temperature, float* __restrict__ z_out, Partial* __restrict__ part,
+                 int n_units, int h_stage_bytes, int w_stages, int* status) {
   extern __shared__ __align__(1024) unsigned char smem_raw[];
   unsigned char* base = reinterpret_cast<unsigned char*>(
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~(uintptr_t)1023);
@@ -307,8 +308,8 @@ lmhead_tc_kernel(const __grid_constant__ CUtensorMap map_h, const __grid_constan
     tc::tmem_relinquish();
   }
   if (warp == 0 && lane == 0) {
-    tc::prefetch_tensormap(&map_h);
-    tc::prefetch_tensormap(&map_w);
+    tc::prefetch_tensormap(use3d ? &map_h3 : &map_h);
+    tc::prefetch_tensormap(use3d ? &map_w3 : &map_w);
   }
   tc::fence_before_thread_sync();
   __syncthreads();
@@ -329,9 +330,14 @@ lmhead_tc_kernel(const __grid_constant__ CUtensorMap map_h, const __grid_constan
         for (int kb = 0; kb < KB && ok; ++kb) {
           if (!(ok = tc::mbar_wait(&sh->h_empty[hs], hph ^ 1, abort_flag, status))) break;
           tc::mbar_arrive_expect_tx(&sh->h_full[hs], (uint32_t)h_stage_bytes);
-          for (int c = 0; c < kChunks; ++c)
-            tc::tma_load_2d_hint(h_smem + hs * h_stage_bytes + c * h_chunk_bytes, &map_h,
-                                 &sh->h_full[hs], (kb * kChunks + c) * kBK, 0, pol_h);
+          if (use3d) {
+            tc::tma_load_3d_hint(h_smem + hs * h_stage_bytes, &map_h3, &sh->h_full[hs], 0, 0,
+                                 kb * kChunks, pol_h);
+          } else {
+            for (int c = 0; c < kChunks; ++c)
+              tc::tma_load_2d_hint(h_smem + hs * h_stage_bytes + c * h_chunk_bytes, &map_h,
+                                   &sh->h_full[hs], (kb * kChunks + c) * kBK, 0, pol_h);
+          }
           ++issued_h;
           if (++hs == kHStages) { hs = 0; hph ^= 1; }
           for (int blk = b0; blk < b1; ++blk) {
@@ -339,9 +345,14 @@ lmhead_tc_kernel(const __grid_constant__ CUtensorMap map_h, const __grid_constan
             if (!(ok = tc::mbar_wait(&sh->w_empty[ws], wph ^ 1, abort_flag, status))) break;
             tc::mbar_arrive_expect_tx(&sh->w_full[ws], kWStageBytes);
             unsigned char* dst = w_smem + (size_t)ws * kWStageBytes;
-            for (int c = 0; c < kChunks; ++c)
-              tc::tma_load_2d_hint(dst + c * (kRowsBlk * 128), &map_w, &sh->w_full[ws],
-                                   (kb * kChunks + c) * kBK, row0, pol_w);
+            if (use3d) {
+              // one box: 32 rows x 4 chunks, 512 contiguous bytes of each row
+              tc::tma_load_3d_hint(dst, &map_w3, &sh->w_full[ws], 0, row0, kb * kChunks, pol_w);
+            } else {
+              for (int c = 0; c < kChunks; ++c)
+                tc::tma_load_2d_hint(dst + c * (kRowsBlk * 128), &map_w, &sh->w_full[ws],
+                                     (kb * kChunks + c) * kBK, row0, pol_w);
+            }
             ++issued_w;
             if (++ws == w_stages) { ws = 0; wph ^= 1; }
           }
@@ -516,6 +527,22 @@ bool make_map_bf16(CUtensorMap* map, const void* ptr, int rows, int cols, int bo
              CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
+// The same [rows, cols] bf16 tensor seen as {64 elements, rows, cols/64
+// chunks} (chunk stride 128 bytes): one box of box_rows x `chunks` lands in
+// shared memory as `chunks` consecutive [box_rows][128 B] swizzled tiles.
+bool make_map_bf16_chunked(CUtensorMap* map, const void* ptr, int rows, int cols, int box_rows,
+                           int chunks) {
+  auto enc = get_encode();
+  if (!enc || cols % kBK) return false;
+  cuuint64_t dims[3] = {(cuuint64_t)kBK, (cuuint64_t)rows, (cuuint64_t)(cols / kBK)};
+  cuuint64_t strides[2] = {(cuuint64_t)cols * 2, (cuuint64_t)kBK * 2};
+  cuuint32_t box[3] = {(cuuint32_t)kBK, (cuuint32_t)box_rows, (cuuint32_t)chunks};
+  cuuint32_t estr[3] = {1, 1, 1};
+  return enc(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(ptr), dims, strides, box,
+             estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+             CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
 int sm_count() {
   static int n = 0;
   if (!n) {
@@ -556,14 +583,13 @@ extern "C" eagle_status eagle_lmhead_softmax(eagle_dtype dtype, int T, int H, in
   cudaStream_t s = (cudaStream_t)stream;
   Partial* part = static_cast<Partial*>(d_ws);
   float* z = (mode == EAGLE_LMHEAD_PROB) ? d_q : nullptr;
-  const bool tc_ok = dtype == EAGLE_BF16 && T <= 128 && (H % 8) == 0 &&
+  const bool tc_ok = dtype == EAGLE_BF16 && (H % 8) == 0 &&
                      (((uintptr_t)d_h | (uintptr_t)d_w) & 15) == 0 &&
                      (!z || ((uintptr_t)z & 15) == 0);
   if (tc_ok) {
-    const TcLayout TL = tc_layout(T);
-    CUtensorMap map_h, map_w;
-    if (!make_map_bf16(&map_h, d_h, T, H, TL.t_pad) || !make_map_bf16(&map_w, d_w, V, H, kRowsBlk))
-      return EAGLE_ERR_CUDA;
+    CUtensorMap map_w, map_w3;
+    if (!make_map_bf16(&map_w, d_w, V, H, kRowsBlk)) return EAGLE_ERR_CUDA;
+    const bool w3 = make_map_bf16_chunked(&map_w3, d_w, V, H, kRowsBlk, kChunks);
     static bool attr = false;
     if (!attr) {
       if (cudaFuncSetAttribute(lmhead_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
@@ -573,10 +599,20 @@ extern "C" eagle_status eagle_lmhead_softmax(eagle_dtype dtype, int T, int H, in
     }
     const int n_units = (V + kRowsBlk - 1) / kRowsBlk;
     const int grid = std::min(sm_count(), n_units);
-    lmhead_tc_kernel<<<grid, kTcThreads, TL.smem, s>>>(map_h, map_w, T, H, V, temperature, z,
-                                                        part, n_units, TL.h_stage_bytes,
-                                                        TL.w_stages, d_status);
-    if (cudaGetLastError() != cudaSuccess) return EAGLE_ERR_CUDA;
+    // one pass over W per 128 tree rows (the MMA's M)
+    for (int r0 = 0; r0 < T; r0 += 128) {
+      const int Ts = std::min(128, T - r0);
+      const TcLayout TL = tc_layout(Ts);
+      const __nv_bfloat16* hs = static_cast<const __nv_bfloat16*>(d_h) + (size_t)r0 * H;
+      CUtensorMap map_h, map_h3;
+      if (!make_map_bf16(&map_h, hs, Ts, H, TL.t_pad)) return EAGLE_ERR_CUDA;
+      const bool use3d = w3 && make_map_bf16_chunked(&map_h3, hs, Ts, H, TL.t_pad, kChunks);
+      lmhead_tc_kernel<<<grid, kTcThreads, TL.smem, s>>>(
+          map_h, map_w, use3d ? map_h3 : map_h, use3d ? map_w3 : map_w, use3d ? 1 : 0, Ts, H, V,
+          temperature, z ? z + (size_t)r0 * V : nullptr, part + (size_t)r0 * grid, n_units,
+          TL.h_stage_bytes, TL.w_stages, d_status);
+      if (cudaGetLastError() != cudaSuccess) return EAGLE_ERR_CUDA;
+    }
     dim3 fgrid(T, z ? (V + kFinChunk - 1) / kFinChunk : 1);
     lmhead_finalize_kernel<<<fgrid, kFinThreads, 0, s>>>(T, V, temperature, part, grid, d_argmax,
                                                          d_row_max, d_row_lse, d_top2_gap, z);

@@ -135,23 +135,27 @@ eagle_status launch_warp(int D, int B, int T, int Hq, int Hkv, float scale, int 
 // ---------------------------------------------------------------------------
 // tcgen05 path (bf16, D = 128)
 // ---------------------------------------------------------------------------
-constexpr int kAttThreads = 192;        // warp 0 TMA, warp 1 MMA, warps 2-5 rows
+constexpr int kAttThreads = 320;        // warp 0 TMA, warp 1 MMA, warps 2-9 rows
+constexpr float kRescaleLog2 = 8.f;     // rescale O only when the max grows by > 2^8
 constexpr int kKeyBlk = 128;            // keys per block (the S MMA's N)
 constexpr int kHalfBytes = 128 * 128;   // 128 rows x 64 bf16 (one swizzle atom wide)
 constexpr int kTileBytes = 2 * kHalfBytes;  // 128 rows x 128 bf16
 constexpr int kTargetCtas = 152;        // SMs of a GB300
-constexpr size_t kAttSmem = 1024 + 7 * (size_t)kTileBytes + 1536;
+constexpr size_t kAttSmem = 1024 + 7 * (size_t)kTileBytes + 1280;
 
 struct AttShared {
   uint64_t q_full;
   uint64_t k_full[2], k_empty[2], v_full[2], v_empty[2];
   uint64_t s_full[2], s_empty[2];
-  uint64_t p_full, o_full, o_empty, drain;
+  uint64_t p_full, p_free, o_done, drain;
+  uint64_t xbar, fbar, tbar0, tbar1;   // row-thread exchanges and the merge ticket
   uint32_t tmem_base;
   int abort_flag;
   int is_last;
-  int par[EAGLE_MAX_TREE_NODES];
+  float xchg[2][128];   // per-row values exchanged between the two column halves
 };
+
+static_assert(sizeof(AttShared) <= 1280, "AttShared must fit its shared-memory slot");
 
 struct AttPlan {
   int G, MT, NC, CK;  // heads per kv head, row tiles, cache chunks, keys per chunk
@@ -216,6 +220,26 @@ __device__ __forceinline__ uint64_t desc_mnmajor_sw128(uint32_t smem_addr, uint3
   return d;
 }
 
+__device__ __forceinline__ void tmem_st_32x32b_x32(uint32_t taddr, const float (&v)[32]) {
+  asm volatile(
+      "tcgen05.st.sync.aligned.32x32b.x32.b32 [%0], "
+      "{%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,%16,"
+      "%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31,%32};" ::"r"(taddr),
+      "r"(__float_as_uint(v[0])), "r"(__float_as_uint(v[1])), "r"(__float_as_uint(v[2])),
+      "r"(__float_as_uint(v[3])), "r"(__float_as_uint(v[4])), "r"(__float_as_uint(v[5])),
+      "r"(__float_as_uint(v[6])), "r"(__float_as_uint(v[7])), "r"(__float_as_uint(v[8])),
+      "r"(__float_as_uint(v[9])), "r"(__float_as_uint(v[10])), "r"(__float_as_uint(v[11])),
+      "r"(__float_as_uint(v[12])), "r"(__float_as_uint(v[13])), "r"(__float_as_uint(v[14])),
+      "r"(__float_as_uint(v[15])), "r"(__float_as_uint(v[16])), "r"(__float_as_uint(v[17])),
+      "r"(__float_as_uint(v[18])), "r"(__float_as_uint(v[19])), "r"(__float_as_uint(v[20])),
+      "r"(__float_as_uint(v[21])), "r"(__float_as_uint(v[22])), "r"(__float_as_uint(v[23])),
+      "r"(__float_as_uint(v[24])), "r"(__float_as_uint(v[25])), "r"(__float_as_uint(v[26])),
+      "r"(__float_as_uint(v[27])), "r"(__float_as_uint(v[28])), "r"(__float_as_uint(v[29])),
+      "r"(__float_as_uint(v[30])), "r"(__float_as_uint(v[31]))
+      : "memory");
+  asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
+}
+
 __global__ void __launch_bounds__(kAttThreads, 1)
 tree_attn_tc_kernel(const __grid_constant__ CUtensorMap map_q,
                     const __grid_constant__ CUtensorMap map_kc,
@@ -273,16 +297,19 @@ tree_attn_tc_kernel(const __grid_constant__ CUtensorMap map_q,
       tc::mbar_init(&sh->v_full[i], 1);
       tc::mbar_init(&sh->v_empty[i], 1);
       tc::mbar_init(&sh->s_full[i], 1);
-      tc::mbar_init(&sh->s_empty[i], 4);
+      tc::mbar_init(&sh->s_empty[i], 8);
     }
-    tc::mbar_init(&sh->p_full, 4);
-    tc::mbar_init(&sh->o_full, 1);
-    tc::mbar_init(&sh->o_empty, 4);
+    tc::mbar_init(&sh->p_full, 8);
+    tc::mbar_init(&sh->p_free, 1);
+    tc::mbar_init(&sh->o_done, 1);
     tc::mbar_init(&sh->drain, 1);
+    tc::mbar_init(&sh->xbar, 256);
+    tc::mbar_init(&sh->fbar, 256);
+    tc::mbar_init(&sh->tbar0, 256);
+    tc::mbar_init(&sh->tbar1, 1);
     sh->abort_flag = 0;
     tc::fence_barrier_init();
   }
-  for (int i = threadIdx.x; i < n; i += blockDim.x) sh->par[i] = A.parent[t0 + i];
   if (warp == 1) {
     tc::tmem_alloc(&sh->tmem_base, 512);
     tc::tmem_relinquish();
@@ -302,14 +329,14 @@ tree_attn_tc_kernel(const __grid_constant__ CUtensorMap map_q,
       const int node0 = t0 + mt * nodes_per_tile;
       tc::tma_load_3d(q_sm, &map_q, &sh->q_full, 0, g * A.G, node0);
       tc::tma_load_3d(q_sm + kHalfBytes, &map_q, &sh->q_full, 64, g * A.G, node0);
-      uint32_t eph[2] = {0, 0};
+      uint32_t eph = 0;   // bit st: phase parity of stage st's empty barriers
       int issued = 0;
       for (int j = 0; j < nblk && ok; ++j) {
         const int st = j & 1;
         if (j >= 2) {
-          if (!(ok = tc::mbar_wait(&sh->k_empty[st], eph[st], abort_flag, status))) break;
-          if (!(ok = tc::mbar_wait(&sh->v_empty[st], eph[st], abort_flag, status))) break;
-          eph[st] ^= 1;
+          if (!(ok = tc::mbar_wait(&sh->k_empty[st], (eph >> st) & 1u, abort_flag, status))) break;
+          if (!(ok = tc::mbar_wait(&sh->v_empty[st], (eph >> st) & 1u, abort_flag, status))) break;
+          eph ^= 1u << st;
         }
         const CUtensorMap* mk = (j < n_cache_blk) ? &map_kc : &map_kt;
         const CUtensorMap* mv = (j < n_cache_blk) ? &map_vc : &map_vt;
@@ -344,16 +371,16 @@ tree_attn_tc_kernel(const __grid_constant__ CUtensorMap map_q,
       const uint32_t p_addr = tc::smem_u32(p_sm);
       const uint32_t pl_addr = tc::smem_u32(pl_sm);
       bool ok = tc::mbar_wait(&sh->q_full, 0, abort_flag, status);
-      uint32_t kph[2] = {0, 0}, vph[2] = {0, 0}, seph[2] = {0, 0};
-      uint32_t pph = 0, oeph = 0;
+      uint32_t kph = 0, vph = 0, seph = 0;   // bit st: phase parity per stage
+      uint32_t pph = 0;
       auto issue_s = [&](int j) -> bool {
         const int st = j & 1;
         if (j >= 2) {
-          if (!tc::mbar_wait(&sh->s_empty[st], seph[st], abort_flag, status)) return false;
-          seph[st] ^= 1;
+          if (!tc::mbar_wait(&sh->s_empty[st], (seph >> st) & 1u, abort_flag, status)) return false;
+          seph ^= 1u << st;
         }
-        if (!tc::mbar_wait(&sh->k_full[st], kph[st], abort_flag, status)) return false;
-        kph[st] ^= 1;
+        if (!tc::mbar_wait(&sh->k_full[st], (kph >> st) & 1u, abort_flag, status)) return false;
+        kph ^= 1u << st;
         tc::fence_after_thread_sync();
         const uint32_t k_addr = tc::smem_u32(k_sm + st * kTileBytes);
 #pragma unroll
@@ -372,15 +399,11 @@ tree_attn_tc_kernel(const __grid_constant__ CUtensorMap map_q,
         const int st = j & 1;
         if (!(ok = tc::mbar_wait(&sh->p_full, pph, abort_flag, status))) break;
         pph ^= 1;
-        if (!(ok = tc::mbar_wait(&sh->v_full[st], vph[st], abort_flag, status))) break;
-        vph[st] ^= 1;
-        if (j >= 1) {
-          if (!(ok = tc::mbar_wait(&sh->o_empty, oeph, abort_flag, status))) break;
-          oeph ^= 1;
-        }
+        if (!(ok = tc::mbar_wait(&sh->v_full[st], (vph >> st) & 1u, abort_flag, status))) break;
+        vph ^= 1u << st;
         tc::fence_after_thread_sync();
         const uint32_t v_addr = tc::smem_u32(v_sm + st * kTileBytes);
-        // O = P_hi V + P_lo V: A = P parts (K-major, keys contiguous),
+        // O += P_hi V + P_lo V: A = P parts (K-major, keys contiguous),
         // B = V (MN-major: one 128-byte row per key and d-half)
 #pragma unroll
         for (int part = 0; part < 2; ++part) {
@@ -390,24 +413,29 @@ tree_attn_tc_kernel(const __grid_constant__ CUtensorMap map_q,
             const uint32_t a_off = (uint32_t)((k16 >> 2) * kHalfBytes + (k16 & 3) * 32);
             tc::mma_f16(tmem + 256u, tc::desc_kmajor_sw128(pa + a_off),
                         desc_mnmajor_sw128(v_addr + (uint32_t)(k16 * 16 * 128), kHalfBytes),
-                        idesc_o, (part > 0 || k16 > 0) ? 1u : 0u);
+                        idesc_o, (j > 0 || part > 0 || k16 > 0) ? 1u : 0u);
           }
         }
-        tc::mma_commit(&sh->o_full);
+        tc::mma_commit(&sh->p_free);
         tc::mma_commit(&sh->v_empty[st]);
       }
+      if (ok) tc::mma_commit(&sh->o_done);
       tc::mma_commit(&sh->drain);
       int never = 0;
       tc::mbar_wait(&sh->drain, 0, &never, nullptr, 200000000ll);
     }
   } else {
     // ------------------------------------------------------------ rows
+    // two threads per query row: half 0 owns key columns / d columns 0-63,
+    // half 1 owns 64-127
     const int quad = warp & 3;
+    const int half = (warp - 2) >> 2;
     const int r = quad * 32 + lane;                   // row in the tile
     const int qrow = mt * 128 + r;                    // (node, head) row of (b, g)
     const int node = qrow / A.G, hh = qrow % A.G;
     const bool row_ok = node < n;
-    // ancestor-or-self bitset of this row's node (up to 256 nodes)
+    // ancestor-or-self bits of this row's node for the key columns this
+    // thread owns: word w covers tree nodes 32*w .. 32*w+31
     uint32_t anc[EAGLE_MAX_TREE_NODES / 32];
 #pragma unroll
     for (int w = 0; w < EAGLE_MAX_TREE_NODES / 32; ++w) anc[w] = 0u;
@@ -417,92 +445,96 @@ tree_attn_tc_kernel(const __grid_constant__ CUtensorMap map_q,
 #pragma unroll
         for (int w = 0; w < EAGLE_MAX_TREE_NODES / 32; ++w)
           if ((j >> 5) == w) anc[w] |= 1u << (j & 31);
-        const int p = sh->par[j];
+        const int p = __ldg(A.parent + t0 + j);
         if ((j == 0) ? (p != -1) : (p < 0 || p >= j) || ++steps > n) {
-          fail(status, EAGLE_ERR_INVALID_TREE);
+          if (half == 0) fail(status, EAGLE_ERR_INVALID_TREE);
           break;
         }
         j = p;
       }
     }
-    const uint32_t p_row = tc::smem_u32(p_sm) + (uint32_t)(r * 128);
-    const uint32_t pl_row = tc::smem_u32(pl_sm) + (uint32_t)(r * 128);
-    const uint32_t taddr_row = tmem + ((uint32_t)(quad * 32) << 16);
-    float o[128];
-#pragma unroll
-    for (int d = 0; d < 128; ++d) o[d] = 0.f;
-    float m = -INFINITY, l = 0.f, corr_prev = 1.f;
-    uint32_t sph[2] = {0, 0}, oph = 0;
+    const uint32_t p_row = tc::smem_u32(p_sm) + (uint32_t)(half * kHalfBytes + r * 128);
+    const uint32_t pl_row = tc::smem_u32(pl_sm) + (uint32_t)(half * kHalfBytes + r * 128);
+    const uint32_t trow = tmem + ((uint32_t)(quad * 32) << 16);
+    const uint32_t o_addr = trow + 256u + (uint32_t)(half * 64);
+    float m = -INFINITY, l = 0.f;   // l: this half's share of the normaliser
+    uint32_t sph = 0, pfph = 0;   // sph bit st: phase parity of s_full[st]
     bool ok = true;
     for (int j = 0; j < nblk && ok; ++j) {
       const int st = j & 1;
-      if (j >= 1) {
-        // fold the previous block's P V into the output row; this also
-        // frees the P buffer
-        const bool got = tc::mbar_wait(&sh->o_full, oph, abort_flag, status);
-        if (!(ok = __all_sync(0xffffffffu, got))) break;
-        oph ^= 1;
-        tc::fence_after_thread_sync();
-#pragma unroll
-        for (int cc = 0; cc < 4; ++cc) {
-          float v[32];
-          tc::tmem_ld_32x32b_x32(taddr_row + 256u + (uint32_t)(cc * 32), v);
-#pragma unroll
-          for (int i = 0; i < 32; ++i) o[cc * 32 + i] = fmaf(o[cc * 32 + i], corr_prev, v[i]);
-        }
-        tc::fence_before_thread_sync();
-        __syncwarp();
-        if (lane == 0) tc::mbar_arrive(&sh->o_empty);
-      }
-      const bool got = tc::mbar_wait(&sh->s_full[st], sph[st], abort_flag, status);
+      const bool got = tc::mbar_wait(&sh->s_full[st], (sph >> st) & 1u, abort_flag, status);
       if (!(ok = __all_sync(0xffffffffu, got))) break;
-      sph[st] ^= 1;
+      sph ^= 1u << st;
       tc::fence_after_thread_sync();
       const bool tree_blk = j >= n_cache_blk;
       const int tb = tree_blk ? j - n_cache_blk : 0;          // tree block 0 or 1
-      const int key0 = tree_blk ? tb * kKeyBlk : key_begin + j * kKeyBlk;
+      const int key0 = (tree_blk ? tb * kKeyBlk : key_begin + j * kKeyBlk) + half * 64;
       const int key_lim = tree_blk ? n : key_end;
-      const uint32_t s_addr = taddr_row + (uint32_t)(st * 128);
-      // pass 1: block max over this row's visible keys
+      const uint32_t s_addr = trow + (uint32_t)(st * 128 + half * 64);
+      float v0[32], v1[32];
+      tc::tmem_ld_32x32b_x32(s_addr, v0);
+      tc::tmem_ld_32x32b_x32(s_addr + 32u, v1);
+      // bitset words for key columns half*64 .. +63 of tree block tb (static indices)
+      const uint32_t w0 = !tree_blk ? 0xffffffffu
+                          : tb ? (half ? anc[6] : anc[4]) : (half ? anc[2] : anc[0]);
+      const uint32_t w1 = !tree_blk ? 0xffffffffu
+                          : tb ? (half ? anc[7] : anc[5]) : (half ? anc[3] : anc[1]);
+      const int nv0 = min(32, max(0, key_lim - key0));
+      const int nv1 = min(32, max(0, key_lim - key0 - 32));
       float bm = -INFINITY;
 #pragma unroll
-      for (int cc = 0; cc < 4; ++cc) {
-        float v[32];
-        tc::tmem_ld_32x32b_x32(s_addr + (uint32_t)(cc * 32), v);
-        const uint32_t word = tree_blk ? (tb ? anc[4 + cc] : anc[cc]) : 0xffffffffu;
-#pragma unroll
-        for (int i = 0; i < 32; ++i) {
-          const bool vis = (key0 + cc * 32 + i < key_lim) && ((word >> i) & 1u);
-          if (vis) bm = fmaxf(bm, v[i] * A.scale_log2);
-        }
+      for (int i = 0; i < 32; ++i) {
+        if (i < nv0 && ((w0 >> i) & 1u)) bm = fmaxf(bm, v0[i]);
+        if (i < nv1 && ((w1 >> i) & 1u)) bm = fmaxf(bm, v1[i]);
       }
+      bm *= A.scale_log2;
+      // the previous PV product must be complete before P, O or the exchange
+      // slot (read by the other half before it released that product) is reused
+      if (j >= 1) {
+        const bool g2 = tc::mbar_wait(&sh->p_free, pfph, abort_flag, status);
+        if (!(ok = __all_sync(0xffffffffu, g2))) break;
+        pfph ^= 1;
+        tc::fence_after_thread_sync();
+      }
+      // the row's block max: combine with the other half
+      sh->xchg[half][r] = bm;
+      tc::mbar_arrive(&sh->xbar);
+      const bool g3 = tc::mbar_wait(&sh->xbar, (uint32_t)(j & 1), abort_flag, status);
+      if (!(ok = __all_sync(0xffffffffu, g3))) break;
+      bm = fmaxf(bm, sh->xchg[half ^ 1][r]);
       const float mn = fmaxf(m, bm);
-      const float corr = (mn == -INFINITY) ? 1.f : exp2f(m - mn);
-      // pass 2: P = exp2(s - m), bf16, into the swizzled P tile
-      float psum = 0.f;
+      const bool first = (m == -INFINITY);
+      const bool rescale = !first && (mn > m + kRescaleLog2);
+      const float mu = (first || rescale) ? mn : m;     // reference max for this block's P
+      if (rescale) {
+        const float f = exp2f(m - mu);
+        float o[32];
 #pragma unroll
-      for (int cc = 0; cc < 4; ++cc) {
-        float v[32];
-        tc::tmem_ld_32x32b_x32(s_addr + (uint32_t)(cc * 32), v);
-        const uint32_t word = tree_blk ? (tb ? anc[4 + cc] : anc[cc]) : 0xffffffffu;
-        // p = hi + lo with hi = bf16(p), lo = bf16(p - hi): the two PV
-        // products together weight V with ~16 significant bits
+        for (int cc = 0; cc < 2; ++cc) {
+          tc::tmem_ld_32x32b_x32(o_addr + (uint32_t)(cc * 32), o);
+#pragma unroll
+          for (int i = 0; i < 32; ++i) o[i] *= f;
+          tmem_st_32x32b_x32(o_addr + (uint32_t)(cc * 32), o);
+        }
+        l *= f;
+      }
+      // P = exp2(s - mu) split into bf16 hi + lo, into the swizzled P tiles
+      float psum = 0.f;
+      auto emit = [&](float (&v)[32], int nvc, uint32_t wc, int cc) {
         float lo[32];
 #pragma unroll
         for (int i = 0; i < 32; ++i) {
-          const bool vis = (key0 + cc * 32 + i < key_lim) && ((word >> i) & 1u);
-          const float pv = vis ? exp2f(v[i] * A.scale_log2 - mn) : 0.f;
+          const bool vis = (i < nvc) && ((wc >> i) & 1u);
+          const float pv = vis ? exp2f(fmaf(v[i], A.scale_log2, -mu)) : 0.f;
           const float hi = __bfloat162float(__float2bfloat16_rn(pv));
-          lo[i] = __bfloat162float(__float2bfloat16_rn(pv - hi));
+          lo[i] = pv - hi;
           v[i] = hi;
-          psum += hi + lo[i];   // the normaliser sums exactly what PV uses
+          psum += pv;
         }
-        // keys cc*32 .. cc*32+31 -> half (cc / 2), 16-byte units (cc & 1) * 4 + u
 #pragma unroll
         for (int u = 0; u < 4; ++u) {
-          const int unit = (cc & 1) * 4 + u;
-          const uint32_t off = (uint32_t)((cc >> 1) * kHalfBytes) +
-                               (uint32_t)(((unit ^ (r & 7)) & 7) * 16);
+          const int unit = cc * 4 + u;   // 16-byte unit of this half's 128-byte row
+          const uint32_t off = (uint32_t)(((unit ^ (r & 7)) & 7) * 16);
           st_shared_v4(p_row + off, pack_bf16(v[u * 8 + 0], v[u * 8 + 1]),
                        pack_bf16(v[u * 8 + 2], v[u * 8 + 3]), pack_bf16(v[u * 8 + 4], v[u * 8 + 5]),
                        pack_bf16(v[u * 8 + 6], v[u * 8 + 7]));
@@ -511,10 +543,11 @@ tree_attn_tc_kernel(const __grid_constant__ CUtensorMap map_q,
                        pack_bf16(lo[u * 8 + 4], lo[u * 8 + 5]),
                        pack_bf16(lo[u * 8 + 6], lo[u * 8 + 7]));
         }
-      }
-      l = l * corr + psum;
-      m = mn;
-      corr_prev = corr;
+      };
+      emit(v0, nv0, w0, 0);
+      emit(v1, nv1, w1, 1);
+      l += psum;
+      m = mu;
       fence_proxy_async_smem();
       tc::fence_before_thread_sync();
       __syncwarp();
@@ -523,72 +556,103 @@ tree_attn_tc_kernel(const __grid_constant__ CUtensorMap map_q,
         tc::mbar_arrive(&sh->p_full);
       }
     }
+    // ---- the output rows: O (in TMEM) / l
+    float o0[32], o1[32];
     if (ok && nblk > 0) {
-      const bool got = tc::mbar_wait(&sh->o_full, oph, abort_flag, status);
+      const bool got = tc::mbar_wait(&sh->o_done, 0, abort_flag, status);
       if ((ok = __all_sync(0xffffffffu, got))) {
         tc::fence_after_thread_sync();
-#pragma unroll
-        for (int cc = 0; cc < 4; ++cc) {
-          float v[32];
-          tc::tmem_ld_32x32b_x32(taddr_row + 256u + (uint32_t)(cc * 32), v);
-#pragma unroll
-          for (int i = 0; i < 32; ++i) o[cc * 32 + i] = fmaf(o[cc * 32 + i], corr_prev, v[i]);
-        }
+        tc::tmem_ld_32x32b_x32(o_addr, o0);
+        tc::tmem_ld_32x32b_x32(o_addr + 32u, o1);
       }
     }
-    // ---- results: final row, or a partial to be merged
+    if (!ok) {
+#pragma unroll
+      for (int i = 0; i < 32; ++i) o0[i] = o1[i] = 0.f;
+    }
+    // full normaliser = this half's share + the other half's (the slot is
+    // free: the other half read it before releasing the last PV product)
+    sh->xchg[half][r] = l;
+    tc::mbar_arrive(&sh->fbar);
+    {
+      const bool got = tc::mbar_wait(&sh->fbar, 0, abort_flag, status);
+      ok = __all_sync(0xffffffffu, got) && ok;
+    }
+    const float l_row = l + sh->xchg[half ^ 1][r];
     const int h = g * A.G + hh;
-    float* orow = A.out + ((size_t)(t0 + node) * A.Hq + h) * 128;
+    float* orow = A.out + ((size_t)(t0 + node) * A.Hq + h) * 128 + half * 64;
     if (n_chunks == 1) {
       if (row_ok && ok) {
-        const float inv = 1.f / l;
+        const float inv = 1.f / l_row;
 #pragma unroll
-        for (int d = 0; d < 128; d += 4)
+        for (int d = 0; d < 32; d += 4) {
           *reinterpret_cast<float4*>(orow + d) =
-              make_float4(o[d] * inv, o[d + 1] * inv, o[d + 2] * inv, o[d + 3] * inv);
+              make_float4(o0[d] * inv, o0[d + 1] * inv, o0[d + 2] * inv, o0[d + 3] * inv);
+          *reinterpret_cast<float4*>(orow + 32 + d) =
+              make_float4(o1[d] * inv, o1[d + 1] * inv, o1[d + 2] * inv, o1[d + 3] * inv);
+        }
       }
     } else {
-      float* po = A.part_o + ((size_t)item_id * 128 + r) * 128;
-      A.part_ml[(size_t)item_id * 128 + r] = make_float2(m, l);
+      float* po = A.part_o + ((size_t)item_id * 128 + r) * 128 + half * 64;
+      if (half == 0) A.part_ml[(size_t)item_id * 128 + r] = make_float2(m, l_row);
 #pragma unroll
-      for (int d = 0; d < 128; d += 4)
-        *reinterpret_cast<float4*>(po + d) = make_float4(o[d], o[d + 1], o[d + 2], o[d + 3]);
-      __threadfence();
-      asm volatile("bar.sync 1, 128;" ::: "memory");
-      if (r == 0) {
-        const int prev = atomicAdd(&A.counters[tile_id], 1);
-        sh->is_last = (prev == n_chunks - 1);
-        if (sh->is_last) A.counters[tile_id] = 0;
+      for (int d = 0; d < 32; d += 4) {
+        *reinterpret_cast<float4*>(po + d) = make_float4(o0[d], o0[d + 1], o0[d + 2], o0[d + 3]);
+        *reinterpret_cast<float4*>(po + 32 + d) =
+            make_float4(o1[d], o1[d + 1], o1[d + 2], o1[d + 3]);
       }
-      asm volatile("bar.sync 1, 128;" ::: "memory");
-      if (sh->is_last && row_ok) {
+      __threadfence();
+      tc::mbar_arrive(&sh->tbar0);
+      if (threadIdx.x == 64) {
+        // every row thread's partial is written: take the ticket
+        int never = 0;
+        sh->is_last = 0;
+        if (tc::mbar_wait(&sh->tbar0, 0, abort_flag, status)) {
+          const int prev = atomicAdd(&A.counters[tile_id], 1);
+          sh->is_last = (prev == n_chunks - 1);
+          if (sh->is_last) A.counters[tile_id] = 0;
+        }
+        (void)never;
+        tc::mbar_arrive(&sh->tbar1);
+      }
+      const bool got_t = tc::mbar_wait(&sh->tbar1, 0, abort_flag, status);
+      if (got_t && sh->is_last && row_ok) {
         __threadfence();
         float M = -INFINITY;
         for (int cc = 0; cc < n_chunks; ++cc)
           M = fmaxf(M, __ldcg(&A.part_ml[((size_t)(tile_id * A.NC + cc)) * 128 + r]).x);
         float Lsum = 0.f;
 #pragma unroll
-        for (int d = 0; d < 128; ++d) o[d] = 0.f;
+        for (int d = 0; d < 32; ++d) o0[d] = o1[d] = 0.f;
         for (int cc = 0; cc < n_chunks; ++cc) {
           const size_t it = (size_t)(tile_id * A.NC + cc);
           const float2 ml = __ldcg(&A.part_ml[it * 128 + r]);
-          const float w = (ml.x == -INFINITY) ? 0.f : exp2f(ml.x - M);
-          Lsum += ml.y * w;
-          const float4* src = reinterpret_cast<const float4*>(A.part_o + (it * 128 + r) * 128);
+          const float wgt = (ml.x == -INFINITY) ? 0.f : exp2f(ml.x - M);
+          Lsum += ml.y * wgt;
+          const float4* src =
+              reinterpret_cast<const float4*>(A.part_o + (it * 128 + r) * 128 + half * 64);
 #pragma unroll
-          for (int d = 0; d < 32; ++d) {
+          for (int d = 0; d < 8; ++d) {
             const float4 x = __ldcg(src + d);
-            o[4 * d] = fmaf(x.x, w, o[4 * d]);
-            o[4 * d + 1] = fmaf(x.y, w, o[4 * d + 1]);
-            o[4 * d + 2] = fmaf(x.z, w, o[4 * d + 2]);
-            o[4 * d + 3] = fmaf(x.w, w, o[4 * d + 3]);
+            o0[4 * d] = fmaf(x.x, wgt, o0[4 * d]);
+            o0[4 * d + 1] = fmaf(x.y, wgt, o0[4 * d + 1]);
+            o0[4 * d + 2] = fmaf(x.z, wgt, o0[4 * d + 2]);
+            o0[4 * d + 3] = fmaf(x.w, wgt, o0[4 * d + 3]);
+            const float4 y = __ldcg(src + 8 + d);
+            o1[4 * d] = fmaf(y.x, wgt, o1[4 * d]);
+            o1[4 * d + 1] = fmaf(y.y, wgt, o1[4 * d + 1]);
+            o1[4 * d + 2] = fmaf(y.z, wgt, o1[4 * d + 2]);
+            o1[4 * d + 3] = fmaf(y.w, wgt, o1[4 * d + 3]);
           }
         }
         const float inv = 1.f / Lsum;
 #pragma unroll
-        for (int d = 0; d < 128; d += 4)
+        for (int d = 0; d < 32; d += 4) {
           *reinterpret_cast<float4*>(orow + d) =
-              make_float4(o[d] * inv, o[d + 1] * inv, o[d + 2] * inv, o[d + 3] * inv);
+              make_float4(o0[d] * inv, o0[d + 1] * inv, o0[d + 2] * inv, o0[d + 3] * inv);
+          *reinterpret_cast<float4*>(orow + 32 + d) =
+              make_float4(o1[d] * inv, o1[d + 1] * inv, o1[d + 2] * inv, o1[d + 3] * inv);
+        }
       }
     }
   }

@@ -172,7 +172,10 @@ class TreeVerifyStep:
         if self.s.k:
             n += self.s.depth + 1
         n += 1                                   # attention
-        n += 2                                   # LM head tiles + finalize
+        if self.s.dtype == "bf16":               # LM head: one pass per 128 rows
+            n += (self.s.T + 127) // 128 + 1     # ... + finalize
+        else:
+            n += 2                               # LM head tiles + finalize
         n += 1                                   # acceptance
         return n
 

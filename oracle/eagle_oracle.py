@@ -326,8 +326,10 @@ def _check_row(x: np.ndarray, what: str):
         raise OracleNumericError(f"{what} row has a value outside [0,1]")
 
 
-def _sample_fixed(qrow: np.ndarray, u: np.float32) -> int:
-    """Inverse-CDF sample from an fp32 distribution over integer weights."""
+def _sample_fixed(qrow: np.ndarray, u: np.float32, info: Optional[dict] = None) -> int:
+    """Inverse-CDF sample from an fp32 distribution over integer weights.
+    If `info` is given it receives the target and the chosen token's CDF
+    interval [lo, hi) (integers), for diagnosing near-ties."""
     Wq = _fixed40(qrow)
     Z = int(Wq.sum(dtype=np.uint64))
     if Z == 0:
@@ -337,7 +339,10 @@ def _sample_fixed(qrow: np.ndarray, u: np.float32) -> int:
         raise ValueError("u_sample outside [0,1)")
     target = (U * Z) >> U_BITS
     csum = np.cumsum(Wq, dtype=np.uint64)
-    return int(np.searchsorted(csum, np.uint64(target), side="right"))
+    tok = int(np.searchsorted(csum, np.uint64(target), side="right"))
+    if info is not None:
+        info.update(target=target, Z=Z, lo=int(csum[tok]) - int(Wq[tok]), hi=int(csum[tok]))
+    return tok
 
 
 def accept_stochastic(tree_off, parent, tokens, q, p_rows, p_row_of_node,
@@ -413,7 +418,10 @@ def accept_stochastic(tree_off, parent, tokens, q, p_rows, p_row_of_node,
                         pk = _normalise(P, SP) if SP > 0 else np.zeros_like(pk)
             if moved:
                 continue
-            out_tok[b, alpha] = _sample_fixed(qk, np.float32(u_sample[t0 + cur]))
+            info = {} if trace is not None else None
+            out_tok[b, alpha] = _sample_fixed(qk, np.float32(u_sample[t0 + cur]), info)
+            if trace is not None:
+                trace.append((b, cur, "sample", info))
             break
         acc_len[b] = alpha
     return acc_len, acc_nodes, out_tok

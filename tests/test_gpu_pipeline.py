@@ -7,8 +7,11 @@ Each workload runs through the C ABI exactly as the benchmark launches it
     stated tolerances (argmax: outside near-ties);
   * acceptance fed identical inputs (the oracle's argmax / q) is bit-exact;
   * the GPU's own end-to-end accept lengths and tokens equal the oracle's,
-    except where a logged near-tie (top-2 logit gap < 1e-3, or an acceptance
-    test within 1e-4 relative of its threshold) explains the difference.
+    except where a logged near-tie explains the difference: a top-2 logit
+    gap < 1e-3, an acceptance test within 1e-4 relative of its threshold,
+    or a bonus-token sample whose target lies within 1e-4 of the total mass
+    of an end of the chosen token's CDF interval (q computed on two machines
+    differs by ~1e-6 relative, which moves the CDF by that much).
 Greedy workloads also run a planted variant: the tokens on one random
 root-to-leaf path are replaced by the oracle's argmax, so alpha spans the
 whole depth."""
@@ -142,9 +145,20 @@ def test_workload_end_to_end(name):
             for b in range(w.B):
                 if not _same_seq(got, ref, b):
                     t0 = int(tree["tree_off"][b])
-                    margins = [abs(float(inp["u_accept"][t0 + c]) * pt - qt) / max(qt, 1e-30)
-                               for (bb, cur, c, t, qt, pt, a) in trace if bb == b]
-                    assert margins and min(margins) < 1e-4, b
+                    margins = []
+                    for ent in trace:
+                        if ent[0] != b:
+                            continue
+                        if ent[2] == "sample":
+                            # inverse-CDF near-tie: target near an interval end
+                            i = ent[3]
+                            margins.append(min(i["target"] - i["lo"], i["hi"] - 1 - i["target"])
+                                           / i["Z"])
+                        else:
+                            (_, cur, c, t, qt, pt, a) = ent
+                            margins.append(abs(float(inp["u_accept"][t0 + c]) * pt - qt)
+                                           / max(qt, 1e-30))
+                    assert margins and min(margins) < 1e-4, (b, margins)
             # identical inputs: the oracle's q into the GPU walk
             step.q_prob.copy_(torch.from_numpy(full["q"]))
             step.run_accept()
