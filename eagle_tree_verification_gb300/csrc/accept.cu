@@ -383,16 +383,16 @@ accept_stochastic_kernel(const StochParams P) {
         moved = true;
         break;
       }
-      // rejected: q_{k+1} = fp32(W)/fp32(Z), p_{k+1} likewise (NO_REPLACE)
-      const float Zf = __ull2float_rn(Z);
-      const float SPf = __ull2float_rn(SP);
+      // rejected: q_{k+1} = fp32(W) * rn(1/fp32(Z)), p_{k+1} likewise
+      // (NO_REPLACE); every operation rounds to nearest once
+      const float rz = (Z > 0ull) ? __frcp_rn(__ull2float_rn(Z)) : 0.f;
+      const float rsp = (SP > 0ull) ? __frcp_rn(__ull2float_rn(SP)) : 0.f;
 #pragma unroll
       for (int e = 0; e < E; ++e) {
         const int i = tid + e * kStochThreads;
         const float qa = q[e], pa = p[e];
-        if (Z > 0ull) q[e] = __fdiv_rn(fixed40_f(fmaxf(0.f, __fsub_rn(qa, pa))), Zf);
-        if (no_replace)
-          p[e] = (v0 + i == t || SP == 0ull) ? 0.f : __fdiv_rn(fixed40_f(pa), SPf);
+        if (Z > 0ull) q[e] = __fmul_rn(fixed40_f(fmaxf(0.f, __fsub_rn(qa, pa))), rz);
+        if (no_replace) p[e] = (v0 + i == t) ? 0.f : __fmul_rn(fixed40_f(pa), rsp);
       }
     }
     if (moved) continue;

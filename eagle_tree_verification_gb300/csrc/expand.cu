@@ -5,12 +5,15 @@
 // selection under a fixed draft-token budget.  A node's value is its
 // cumulative draft log-prob.
 //
-// One launch per level.  Every draft row is split into chunks spread over
-// the whole GPU (the rows are the only large data: F x V fp32 per level);
-// each CTA selects its chunk's top-k, the last CTA of a row (atomic ticket,
-// no waiting) merges the row, and the last row of a sequence builds the
-// children and the next frontier.  Selection keys are 64-bit integers
-// (ordered value bits | inverted index), so every tie rule is a plain max.
+// Two launches per level.  The level's draft rows (the only large data:
+// F x V fp32) are cut into chunks spread over the whole GPU; each CTA stages
+// its chunk in shared memory and writes the chunk's top-k list.  Then one
+// CTA per sequence merges every row's chunk lists (one warp per row, many
+// loads in flight) and builds the children and the next frontier.  The
+// finalize is one CTA per sequence working in shared memory.  Selection keys
+// are 64-bit integers (ordered value bits | inverted index), so every tie
+// rule is a plain max, and a warp keeps its running top-k as a sorted list
+// across its lanes.
 #include <algorithm>
 
 #include "common.cuh"
@@ -21,15 +24,15 @@ namespace {
 
 constexpr int kExpandThreads = 256;
 constexpr int kChunkMax = 8192;     // floats staged per CTA
-constexpr int kFinalThreads = 256;
+constexpr int kFinalThreads = 1024;
 constexpr int kMaxChunks = 64;      // chunks per row (V <= 64 * 8192)
 
 struct PoolLayout {
   int P;         // candidate capacity per sequence
   int rows_max;  // B * k
   int S0, S1;    // chunks per row at level 0 / later levels
-  size_t off_row_cnt, off_seq_cnt, off_fin_cnt, off_count, off_frontier, off_token, off_parent,
-      off_depth, off_prow, off_score, off_sel, off_rowtop, off_partial, total;
+  size_t off_count, off_frontier, off_token, off_parent, off_depth, off_prow, off_score,
+      off_partial, total;
 };
 
 int chunks_for(int rows, int V) {
@@ -55,9 +58,6 @@ PoolLayout pool_layout(int B, int k, int depth, int V) {
     o = align256(o + bytes);
     return at;
   };
-  L.off_row_cnt = take((size_t)L.rows_max * 4);
-  L.off_seq_cnt = take((size_t)B * 4);
-  L.off_fin_cnt = take((size_t)B * 4);
   L.off_count = take((size_t)B * 4);
   L.off_frontier = take((size_t)B * k * 4);
   L.off_token = take((size_t)B * L.P * 4);
@@ -65,17 +65,12 @@ PoolLayout pool_layout(int B, int k, int depth, int V) {
   L.off_depth = take((size_t)B * L.P * 4);
   L.off_prow = take((size_t)B * L.P * 4);
   L.off_score = take((size_t)B * L.P * 4);
-  L.off_sel = take((size_t)B * L.P * 4);
-  L.off_rowtop = take((size_t)L.rows_max * k * 8);
   L.off_partial = take(parts * 8);
   L.total = o;
   return L;
 }
 
 struct PoolPtrs {
-  int* row_cnt;
-  int* seq_cnt;
-  int* fin_cnt;
   int* count;
   int* frontier;
   int* token;
@@ -83,17 +78,12 @@ struct PoolPtrs {
   int* depth;
   int* prow;
   float* score;
-  int* sel;
-  unsigned long long* rowtop;
   unsigned long long* partial;
 };
 
 PoolPtrs pool_ptrs(void* base, const PoolLayout& L) {
   char* c = static_cast<char*>(base);
   PoolPtrs p;
-  p.row_cnt = reinterpret_cast<int*>(c + L.off_row_cnt);
-  p.seq_cnt = reinterpret_cast<int*>(c + L.off_seq_cnt);
-  p.fin_cnt = reinterpret_cast<int*>(c + L.off_fin_cnt);
   p.count = reinterpret_cast<int*>(c + L.off_count);
   p.frontier = reinterpret_cast<int*>(c + L.off_frontier);
   p.token = reinterpret_cast<int*>(c + L.off_token);
@@ -101,8 +91,6 @@ PoolPtrs pool_ptrs(void* base, const PoolLayout& L) {
   p.depth = reinterpret_cast<int*>(c + L.off_depth);
   p.prow = reinterpret_cast<int*>(c + L.off_prow);
   p.score = reinterpret_cast<float*>(c + L.off_score);
-  p.sel = reinterpret_cast<int*>(c + L.off_sel);
-  p.rowtop = reinterpret_cast<unsigned long long*>(c + L.off_rowtop);
   p.partial = reinterpret_cast<unsigned long long*>(c + L.off_partial);
   return p;
 }
@@ -121,18 +109,13 @@ __device__ __forceinline__ unsigned long long shfl_up_u64(unsigned long long v, 
   return __shfl_up_sync(0xffffffffu, v, d);
 }
 
-// Top-k keys of `n` candidates produced by key_of(i), by one warp in one
-// pass.  Lane j holds the j-th largest key seen so far (0 = empty); a batch
-// of 32 candidates is filtered by one ballot against the current k-th key,
-// and the few survivors are inserted by shifting the list down one lane.
-// Keys are unique, so the order is total.  Returns this lane's list entry.
-template <typename KeyOf>
-__device__ __forceinline__ unsigned long long warp_topk_list(int n, int k, KeyOf key_of) {
-  const int lane = threadIdx.x & 31;
+// Warp-wide running top-k: lane j holds the j-th largest key seen (0 =
+// empty), `thr` the k-th (0 while fewer than k).  Feeds 32 keys (one per
+// lane) at a time.
+struct WarpTopk {
   unsigned long long mine = 0ull, thr = 0ull;
-  for (int base = 0; base < n; base += 32) {
-    const int i = base + lane;
-    const unsigned long long key = (i < n) ? key_of(i) : 0ull;
+  __device__ __forceinline__ void feed(unsigned long long key, int k) {
+    const int lane = threadIdx.x & 31;
     unsigned bal = __ballot_sync(0xffffffffu, key > thr);
     while (bal) {
       const int src = __ffs(bal) - 1;
@@ -148,35 +131,13 @@ __device__ __forceinline__ unsigned long long warp_topk_list(int n, int k, KeyOf
       thr = shfl_u64(mine, k - 1);
     }
   }
-  return mine;
-}
+};
 
-// Top-k of `n` keys in shared memory by the whole block: every warp selects
-// from its slice, then warp 0 merges the warps' lists into out[0..k).
-__device__ void block_topk_smem(const unsigned long long* cand, int n, int k,
-                                unsigned long long* s_wtop, unsigned long long* out) {
-  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31, nw = blockDim.x >> 5;
-  const int per = (n + nw - 1) / nw;
-  const int lo = min(n, warp * per), cnt = min(n, lo + per) - lo;
-  const unsigned long long mine = warp_topk_list(cnt, k, [&](int i) { return cand[lo + i]; });
-  if (lane < k) s_wtop[warp * k + lane] = mine;
-  __syncthreads();
-  if (warp == 0) {
-    const unsigned long long top = warp_topk_list(nw * k, k, [&](int i) { return s_wtop[i]; });
-    if (lane < k) out[lane] = top;
-  }
-  __syncthreads();
-}
-
-__global__ void __launch_bounds__(kExpandThreads) expand_level_kernel(const LevelParams A) {
+// Level kernel 1: top-k of one chunk of one draft row per CTA.
+__global__ void __launch_bounds__(kExpandThreads) expand_chunk_kernel(const LevelParams A) {
   __shared__ __align__(16) float s_val[kChunkMax];
   __shared__ unsigned long long s_wtop[(kExpandThreads / 32) * EAGLE_MAX_TOPK];
-  __shared__ unsigned long long s_sel[EAGLE_MAX_TOPK];
-  __shared__ unsigned long long s_cand[EAGLE_MAX_TOPK * EAGLE_MAX_TOPK];
-  __shared__ int s_last;
-
-  const int tid = threadIdx.x;
-  const int warp = tid >> 5, nw = blockDim.x >> 5;
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5, nw = blockDim.x >> 5;
   const int row = blockIdx.x / A.S;       // global frontier row: b * F + f
   const int chunk = blockIdx.x % A.S;
   const int b = row / A.F;
@@ -187,66 +148,72 @@ __global__ void __launch_bounds__(kExpandThreads) expand_level_kernel(const Leve
   const int c0 = min(A.V, chunk * csize), c1 = min(A.V, c0 + csize);
   const int n = c1 - c0;
   const int k = A.k;
-
-  // ---- stage the chunk, checking for non-finite values
+  // stage the chunk (vectorised when the row and the chunk are 16-byte aligned)
   int bad = 0;
-  for (int i = tid; i < n; i += blockDim.x) {
-    const float x = __ldg(src + c0 + i);
-    s_val[i] = x;
-    bad |= !isfinite(x);
-  }
-  if (__syncthreads_or(bad) && tid == 0) fail(A.status, EAGLE_ERR_NUMERIC);
-
-  // ---- chunk top-k: each warp a slice, then warp 0 merges
-  {
-    const int lane = tid & 31;
-    const int per = (n + nw - 1) / nw;
-    const int lo = min(n, warp * per), cnt = min(n, lo + per) - lo;
-    const unsigned long long mine = warp_topk_list(
-        cnt, k, [&](int i) { return desc_key(s_val[lo + i], (uint32_t)(c0 + lo + i)); });
-    if (lane < k) s_wtop[warp * k + lane] = mine;
-    __syncthreads();
-    if (warp == 0) {
-      unsigned long long* part = A.pool.partial + ((size_t)row * A.S + chunk) * k;
-      const unsigned long long top =
-          warp_topk_list(nw * k, k, [&](int i) { return s_wtop[i]; });
-      if (lane < k) part[lane] = top;
+  if (((A.V | csize) & 3) == 0) {
+    const float4* s4 = reinterpret_cast<const float4*>(src + c0);
+    for (int i = tid; i < (n >> 2); i += blockDim.x) {
+      const float4 x = __ldg(s4 + i);
+      reinterpret_cast<float4*>(s_val)[i] = x;
+      bad |= !(isfinite(x.x) && isfinite(x.y) && isfinite(x.z) && isfinite(x.w));
+    }
+  } else {
+    for (int i = tid; i < n; i += blockDim.x) {
+      const float x = __ldg(src + c0 + i);
+      s_val[i] = x;
+      bad |= !isfinite(x);
     }
   }
+  if (__syncthreads_or(bad) && tid == 0) fail(A.status, EAGLE_ERR_NUMERIC);
+  // each warp a contiguous slice, then warp 0 merges the warps' lists
+  const int per = (n + nw - 1) / nw;
+  const int lo = min(n, warp * per), cnt = min(n, lo + per) - lo;
+  WarpTopk wt;
+  for (int base = 0; base < cnt; base += 32) {
+    const int i = base + lane;
+    wt.feed(i < cnt ? desc_key(s_val[lo + i], (uint32_t)(c0 + lo + i)) : 0ull, k);
+  }
+  if (lane < k) s_wtop[warp * k + lane] = wt.mine;
+  __syncthreads();
+  if (warp == 0) {
+    WarpTopk m;
+    for (int base = 0; base < nw * k; base += 32) {
+      const int i = base + lane;
+      m.feed(i < nw * k ? s_wtop[i] : 0ull, k);
+    }
+    if (lane < k) A.pool.partial[((size_t)row * A.S + chunk) * k + lane] = m.mine;
+  }
+}
 
-  // ---- last CTA of this row merges the chunk results
-  __threadfence();
-  __syncthreads();
-  if (tid == 0) {
-    const int prev = atomicAdd(&A.pool.row_cnt[row], 1);
-    s_last = (prev == A.S - 1);
-    if (s_last) A.pool.row_cnt[row] = 0;  // ready for the next level
-  }
-  __syncthreads();
-  if (!s_last) return;
-  __threadfence();
-  {
-    unsigned long long* s_keys = reinterpret_cast<unsigned long long*>(s_val);
-    const unsigned long long* rparts = A.pool.partial + (size_t)row * A.S * k;
-    const int m = A.S * k;                 // <= kMaxChunks * 32 keys = 16 KB
-    for (int i = tid; i < m; i += blockDim.x) s_keys[i] = __ldcg(rparts + i);
-    __syncthreads();
-    block_topk_smem(s_keys, m, k, s_wtop, s_sel);
-  }
-  for (int r = tid; r < k; r += blockDim.x) A.pool.rowtop[(size_t)row * k + r] = s_sel[r];
+// Level kernel 2 (one CTA per sequence): merge every row's chunk lists
+// (one warp per row) and build the children and the next frontier.
+constexpr int kMergeThreads = 512;
+constexpr int kMergeBatch = 8;          // 32-key batches loaded before use
 
-  // ---- last row of this sequence builds the children and the frontier
-  __threadfence();
-  __syncthreads();
-  if (tid == 0) {
-    const int prev = atomicAdd(&A.pool.seq_cnt[b], 1);
-    s_last = (prev == A.F - 1);
-    if (s_last) A.pool.seq_cnt[b] = 0;
+__global__ void __launch_bounds__(kMergeThreads) expand_merge_kernel(const LevelParams A) {
+  __shared__ unsigned long long s_row[EAGLE_MAX_TOPK][EAGLE_MAX_TOPK];
+  __shared__ unsigned long long s_cand[EAGLE_MAX_TOPK * EAGLE_MAX_TOPK];
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5, nw = blockDim.x >> 5;
+  const int b = blockIdx.x;
+  const int k = A.k, F = A.F;
+  const int n = A.S * k;                  // candidates per row
+  for (int f = warp; f < F; f += nw) {
+    const unsigned long long* src = A.pool.partial + (size_t)(b * F + f) * n;
+    WarpTopk wt;
+    for (int base0 = 0; base0 < n; base0 += 32 * kMergeBatch) {
+      unsigned long long buf[kMergeBatch];
+#pragma unroll
+      for (int j = 0; j < kMergeBatch; ++j) {
+        const int i = base0 + j * 32 + lane;
+        buf[j] = (i < n) ? __ldcg(src + i) : 0ull;
+      }
+#pragma unroll
+      for (int j = 0; j < kMergeBatch; ++j) wt.feed(buf[j], k);
+    }
+    if (lane < k) s_row[f][lane] = wt.mine;
   }
   __syncthreads();
-  if (!s_last) return;
-  __threadfence();
-  const int nc = A.F * k;  // children in creation order (f-major, rank-minor)
+  const int nc = F * k;  // children in creation order (f-major, rank-minor)
   const int base = A.pool.count[b];
   int* tok = A.pool.token + (size_t)b * A.P;
   int* par = A.pool.parent + (size_t)b * A.P;
@@ -256,17 +223,17 @@ __global__ void __launch_bounds__(kExpandThreads) expand_level_kernel(const Leve
   int* front = A.pool.frontier + (size_t)b * k;
   for (int c = tid; c < nc; c += blockDim.x) {
     const int ff = c / k, rr = c % k;
-    const unsigned long long key = __ldcg(A.pool.rowtop + ((size_t)(b * A.F + ff)) * k + rr);
-    const int pidx = (A.level == 0) ? -1 : __ldcg(front + ff);
-    const float pscore = (A.level == 0) ? 0.f : __ldcg(sco + pidx);
-    const float s = __fadd_rn(pscore, key_value(key));
+    const unsigned long long key = s_row[ff][rr];
+    const int pidx = (A.level == 0) ? -1 : front[ff];
+    const float pscore = (A.level == 0) ? 0.f : sco[pidx];
+    const float sc = __fadd_rn(pscore, key_value(key));
     const int at = base + c;
     tok[at] = (int)key_index(key);
     par[at] = pidx;
     dep[at] = A.level + 1;
     prw[at] = (A.level == 0) ? 0 : 1 + (A.level - 1) * k + ff;
-    sco[at] = s;
-    s_cand[c] = desc_key(s, (uint32_t)c);
+    sco[at] = sc;
+    s_cand[c] = desc_key(sc, (uint32_t)c);
   }
   __syncthreads();
   // next frontier: rank of every child by (score desc, creation order)
@@ -294,27 +261,32 @@ struct FinalParams {
   int* status;
 };
 
-// Selection: CTA (b, y) ranks candidates y*256 .. y*256+255 of sequence b
-// against all pool entries by (score desc, creation order) and flags the
-// top `budget`.  The last CTA of the sequence numbers the kept nodes by
-// (depth, score desc, creation order) and writes the tree.
+// Finalize, one CTA per sequence: rank every pool entry by (score desc,
+// creation order), keep the top `budget`, number the kept nodes by (depth,
+// score desc, creation order) and write the tree.
 __global__ void __launch_bounds__(kFinalThreads) expand_finalize_kernel(const FinalParams A) {
   extern __shared__ __align__(16) unsigned char smem_raw[];
   unsigned long long* s_key = reinterpret_cast<unsigned long long*>(smem_raw);  // [P]
   int* s_list = reinterpret_cast<int*>(s_key + A.P);                            // [P]
   int* s_num = s_list + A.P;                                                    // [P]
-  __shared__ int s_last, s_nsel;
+  int* s_node = s_num + A.P;                                                    // [P]
+  __shared__ int s_nsel;
   const int b = blockIdx.x;
   const int tid = threadIdx.x;
   const int n = A.pool.count[b];
   const int bud = A.budget[b];
   const int keep = min(max(bud, 0), n);
   const float* sco = A.pool.score + (size_t)b * A.P;
-  int* sel = A.pool.sel + (size_t)b * A.P;
-  for (int i = tid; i < n; i += blockDim.x) s_key[i] = desc_key(sco[i], (uint32_t)i);
+  if (tid == 0) {
+    s_nsel = 0;
+    if (bud < 0) fail(A.status, EAGLE_ERR_INVALID_ARG);
+  }
+  for (int i = tid; i < n; i += blockDim.x) {
+    s_key[i] = desc_key(sco[i], (uint32_t)i);
+    s_node[i] = -1;
+  }
   __syncthreads();
-  const int i = blockIdx.y * blockDim.x + tid;
-  if (i < n) {
+  for (int i = tid; i < n; i += blockDim.x) {
     const unsigned long long me = s_key[i];
     int r0 = 0, r1 = 0, r2 = 0, r3 = 0;
     int j = 0;
@@ -325,22 +297,8 @@ __global__ void __launch_bounds__(kFinalThreads) expand_finalize_kernel(const Fi
       r3 += (s_key[j + 3] > me);
     }
     for (; j < n; ++j) r0 += (s_key[j] > me);
-    sel[i] = (r0 + r1 + r2 + r3 < keep);
+    if (r0 + r1 + r2 + r3 < keep) s_list[atomicAdd(&s_nsel, 1)] = i;
   }
-  __threadfence();
-  __syncthreads();
-  if (tid == 0) {
-    const int prev = atomicAdd(&A.pool.fin_cnt[b], 1);
-    s_last = (prev == (int)gridDim.y - 1);
-    if (s_last) A.pool.fin_cnt[b] = 0;
-    s_nsel = 0;
-  }
-  __syncthreads();
-  if (!s_last) return;
-  __threadfence();
-  if (tid == 0 && bud < 0) fail(A.status, EAGLE_ERR_INVALID_ARG);
-  for (int j = tid; j < n; j += blockDim.x)
-    if (__ldcg(sel + j)) s_list[atomicAdd(&s_nsel, 1)] = j;
   __syncthreads();
   const int ns = s_nsel;
   const int* tok = A.pool.token + (size_t)b * A.P;
@@ -357,22 +315,17 @@ __global__ void __launch_bounds__(kFinalThreads) expand_finalize_kernel(const Fi
     int rank = 0;
     for (int c = 0; c < ns; ++c) {
       const int ic = s_list[c];
-      const int dc = dep[ic];
-      rank += (dc < da) || (dc == da && s_key[ic] > ka);
+      rank += (dep[ic] < da) || (dep[ic] == da && s_key[ic] > ka);
     }
     s_num[a] = 1 + rank;
+    s_node[ia] = 1 + rank;
   }
   __syncthreads();
   for (int a = tid; a < ns; a += blockDim.x) {
     const int ia = s_list[a];
     const int pp = par[ia];
-    int pnode = 0;
-    if (pp >= 0) {
-      pnode = -1;
-      for (int c = 0; c < ns; ++c)
-        if (s_list[c] == pp) pnode = s_num[c];
-      if (pnode < 0) fail(A.status, EAGLE_ERR_INVALID_TREE);  // not parent-closed
-    }
+    const int pnode = (pp < 0) ? 0 : s_node[pp];
+    if (pnode < 0) fail(A.status, EAGLE_ERR_INVALID_TREE);  // not parent-closed
     const int at = off + s_num[a];
     A.parent[at] = pnode;
     A.tokens[at] = tok[ia];
@@ -423,7 +376,7 @@ extern "C" eagle_status eagle_draft_expand(int B, int V, int k, int depth, int l
     EAGLE_HOST_CHECK(level >= 0 && level < depth, EAGLE_ERR_INVALID_ARG);
     EAGLE_HOST_CHECK(d_draft_logp, EAGLE_ERR_INVALID_ARG);
     if (level == 0) {
-      // fresh tree: zero the tickets and the pool fill counts
+      // fresh tree: zero the pool fill counts
       cudaError_t e = cudaMemsetAsync(static_cast<char*>(d_pool), 0, L.off_frontier, s);
       if (e != cudaSuccess) return EAGLE_ERR_CUDA;
     }
@@ -439,8 +392,9 @@ extern "C" eagle_status eagle_draft_expand(int B, int V, int k, int depth, int l
     A.logp = d_draft_logp;
     A.pool = pp;
     A.status = d_status;
-    const int grid = B * A.F * A.S;
-    expand_level_kernel<<<grid, kExpandThreads, 0, s>>>(A);
+    expand_chunk_kernel<<<B * A.F * A.S, kExpandThreads, 0, s>>>(A);
+    if (cudaGetLastError() != cudaSuccess) return EAGLE_ERR_CUDA;
+    expand_merge_kernel<<<B, kMergeThreads, 0, s>>>(A);
     return launch_status(cudaGetLastError());
   }
   EAGLE_HOST_CHECK(d_budget && d_tree_off && d_parent && d_tokens && d_node_depth && d_score &&
@@ -461,13 +415,12 @@ extern "C" eagle_status eagle_draft_expand(int B, int V, int k, int depth, int l
   F.score = d_score;
   F.p_row_of_node = d_p_row_of_node;
   F.status = d_status;
-  const size_t smem = (size_t)L.P * (8 + 4 + 4);
+  const size_t smem = (size_t)L.P * (8 + 4 + 4 + 4);
   EAGLE_HOST_CHECK(smem <= 200 * 1024, EAGLE_ERR_UNSUPPORTED);
   if (smem > 40 * 1024) {
     cudaFuncSetAttribute(expand_finalize_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                          (int)smem);
   }
-  dim3 fgrid(B, (L.P + kFinalThreads - 1) / kFinalThreads);
-  expand_finalize_kernel<<<fgrid, kFinalThreads, smem, s>>>(F);
+  expand_finalize_kernel<<<B, kFinalThreads, smem, s>>>(F);
   return launch_status(cudaGetLastError());
 }

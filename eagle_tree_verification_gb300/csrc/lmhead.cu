@@ -222,20 +222,21 @@ lmhead_finalize_kernel(int T, int V, float temperature, const Partial* __restric
 // tcgen05 path
 //
 // MMA D[t, v] = sum_k h[t, k] W[v, k]: M = 128 tree rows (TMEM lanes; rows at
-// or past T are don't-care), N = 32 vocabulary rows per block, K in blocks of
-// 256 (four 64-element chunks, each a 128-byte-swizzled K-major tile).  A W
-// stage is 32 rows x 4 chunks = 16 KB whose per-row 512 bytes are contiguous
-// in HBM (four TMA boxes issued back to back); the h stage holds only the
-// real tree rows (T rounded up to 8).
+// or past T are don't-care), N = one vocabulary block of up to 256 rows, K in
+// 64-element chunks (128-byte-swizzled K-major tiles).  Each CTA owns a
+// balanced slice of the vocabulary in units of 32 rows, cut into blocks of at
+// most 256 rows; two blocks (512 TMEM columns) are accumulated per pass over
+// K.  A W stage is one chunk of one block (<= 32 KB, TMA boxes of 32 rows);
+// an h stage is one chunk of the real tree rows (T rounded up to 8).
 // ---------------------------------------------------------------------------
 constexpr int kTcThreads = 192;   // warp 0 TMA, warp 1 MMA, warps 2-5 epilogue
 constexpr int kBK = 64;           // bf16 per 128-byte swizzled row (one chunk)
-constexpr int kChunks = 4;        // chunks per K block (K block = 256)
-constexpr int kRowsBlk = 32;      // vocabulary rows per block (the MMA's N)
-constexpr int kMaxBlocks = 16;    // blocks accumulated at once: 16 x 32 TMEM columns
-constexpr int kHStages = 2;
-constexpr int kMaxWStages = 16;
-constexpr int kWStageBytes = kRowsBlk * 128 * kChunks;   // 16 KB
+constexpr int kUnit = 32;         // vocabulary rows per TMA box
+constexpr int kBlkMax = 256;      // vocabulary rows per MMA (its N)
+constexpr int kGroupBlocks = 2;   // blocks per pass over K: 2 x 256 TMEM columns
+constexpr int kHStages = 4;
+constexpr int kMaxWStages = 8;
+constexpr int kWStageBytes = kBlkMax * 128;              // 32 KB
 constexpr size_t kSmemLimit = 227 * 1024;
 constexpr size_t kTcSharedBytes = 512;
 
@@ -256,7 +257,7 @@ struct TcLayout {
 TcLayout tc_layout(int T) {
   TcLayout L;
   L.t_pad = ((T + 7) / 8) * 8;
-  L.h_stage_bytes = L.t_pad * 128 * kChunks;
+  L.h_stage_bytes = L.t_pad * 128;
   const size_t fixed = 1024 + (size_t)kHStages * L.h_stage_bytes + kTcSharedBytes;
   L.w_stages = (int)std::min<size_t>(kMaxWStages, (kSmemLimit - fixed) / kWStageBytes);
   L.smem = fixed + (size_t)L.w_stages * kWStageBytes;
@@ -265,26 +266,26 @@ TcLayout tc_layout(int T) {
 
 __global__ void __launch_bounds__(kTcThreads, 1)
 lmhead_tc_kernel(const __grid_constant__ CUtensorMap map_h, const __grid_constant__ CUtensorMap map_w,
-                 const __grid_constant__ CUtensorMap map_h3,
-                 const __grid_constant__ CUtensorMap map_w3, int use3d, int T, int H, int V,
-                 float temperature, float* __restrict__ z_out, Partial* __restrict__ part,
-                 int n_units, int h_stage_bytes, int w_stages, int* status) {
+                 int T, int H, int V, float temperature, float* __restrict__ z_out,
+                 Partial* __restrict__ part, int n_units, int h_stage_bytes, int w_stages,
+                 int* status) {
   extern __shared__ __align__(1024) unsigned char smem_raw[];
   unsigned char* base = reinterpret_cast<unsigned char*>(
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~(uintptr_t)1023);
   unsigned char* h_smem = base;
   unsigned char* w_smem = base + kHStages * h_stage_bytes;
   TcShared* sh = reinterpret_cast<TcShared*>(w_smem + (size_t)w_stages * kWStageBytes);
-  const int h_chunk_bytes = h_stage_bytes / kChunks;     // t_pad rows x 128 B
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int G = gridDim.x;
-  // this CTA's slice of the vocabulary, in blocks of 32 rows
+  // this CTA's slice of the vocabulary: rows [r_begin, r_end), 32-row units
   const int u0 = (int)((long long)n_units * blockIdx.x / G);
   const int u1 = (int)((long long)n_units * (blockIdx.x + 1) / G);
-  const int n_blocks = u1 - u0;
-  const int n_groups = (n_blocks + kMaxBlocks - 1) / kMaxBlocks;
-  const int KB = (H + kBK * kChunks - 1) / (kBK * kChunks);
+  const int r_begin = u0 * kUnit, r_end = u1 * kUnit;
+  const int n_blocks = (r_end - r_begin + kBlkMax - 1) / kBlkMax;
+  const int n_groups = (n_blocks + kGroupBlocks - 1) / kGroupBlocks;
+  const int KB = (H + kBK - 1) / kBK;
+  auto blk_rows = [&](int blk) { return min(kBlkMax, r_end - (r_begin + blk * kBlkMax)); };
 
   if (threadIdx.x == 0) {
     for (int i = 0; i < kHStages; ++i) {
@@ -308,8 +309,8 @@ lmhead_tc_kernel(const __grid_constant__ CUtensorMap map_h, const __grid_constan
     tc::tmem_relinquish();
   }
   if (warp == 0 && lane == 0) {
-    tc::prefetch_tensormap(use3d ? &map_h3 : &map_h);
-    tc::prefetch_tensormap(use3d ? &map_w3 : &map_w);
+    tc::prefetch_tensormap(&map_h);
+    tc::prefetch_tensormap(&map_w);
   }
   tc::fence_before_thread_sync();
   __syncthreads();
@@ -326,33 +327,23 @@ lmhead_tc_kernel(const __grid_constant__ CUtensorMap map_h, const __grid_constan
       uint32_t hph = 0, wph = 0;
       bool ok = true;
       for (int g = 0; g < n_groups && ok; ++g) {
-        const int b0 = g * kMaxBlocks, b1 = min(n_blocks, b0 + kMaxBlocks);
+        const int b0 = g * kGroupBlocks, b1 = min(n_blocks, b0 + kGroupBlocks);
         for (int kb = 0; kb < KB && ok; ++kb) {
           if (!(ok = tc::mbar_wait(&sh->h_empty[hs], hph ^ 1, abort_flag, status))) break;
           tc::mbar_arrive_expect_tx(&sh->h_full[hs], (uint32_t)h_stage_bytes);
-          if (use3d) {
-            tc::tma_load_3d_hint(h_smem + hs * h_stage_bytes, &map_h3, &sh->h_full[hs], 0, 0,
-                                 kb * kChunks, pol_h);
-          } else {
-            for (int c = 0; c < kChunks; ++c)
-              tc::tma_load_2d_hint(h_smem + hs * h_stage_bytes + c * h_chunk_bytes, &map_h,
-                                   &sh->h_full[hs], (kb * kChunks + c) * kBK, 0, pol_h);
-          }
+          tc::tma_load_2d_hint(h_smem + hs * h_stage_bytes, &map_h, &sh->h_full[hs], kb * kBK, 0,
+                               pol_h);
           ++issued_h;
           if (++hs == kHStages) { hs = 0; hph ^= 1; }
           for (int blk = b0; blk < b1; ++blk) {
-            const int row0 = (u0 + blk) * kRowsBlk;
+            const int row0 = r_begin + blk * kBlkMax;
+            const int rows = blk_rows(blk);
             if (!(ok = tc::mbar_wait(&sh->w_empty[ws], wph ^ 1, abort_flag, status))) break;
-            tc::mbar_arrive_expect_tx(&sh->w_full[ws], kWStageBytes);
+            tc::mbar_arrive_expect_tx(&sh->w_full[ws], (uint32_t)(rows * 128));
             unsigned char* dst = w_smem + (size_t)ws * kWStageBytes;
-            if (use3d) {
-              // one box: 32 rows x 4 chunks, 512 contiguous bytes of each row
-              tc::tma_load_3d_hint(dst, &map_w3, &sh->w_full[ws], 0, row0, kb * kChunks, pol_w);
-            } else {
-              for (int c = 0; c < kChunks; ++c)
-                tc::tma_load_2d_hint(dst + c * (kRowsBlk * 128), &map_w, &sh->w_full[ws],
-                                     (kb * kChunks + c) * kBK, row0, pol_w);
-            }
+            for (int u = 0; u < rows; u += kUnit)
+              tc::tma_load_2d_hint(dst + u * 128, &map_w, &sh->w_full[ws], kb * kBK, row0 + u,
+                                   pol_w);
             ++issued_w;
             if (++ws == w_stages) { ws = 0; wph ^= 1; }
           }
@@ -374,10 +365,9 @@ lmhead_tc_kernel(const __grid_constant__ CUtensorMap map_h, const __grid_constan
     if (lane == 0) {
       int hs = 0, ws = 0;
       uint32_t hph = 0, wph = 0, tph = 0;
-      const uint32_t idesc = tc::idesc_bf16_f32(128, kRowsBlk);
       bool ok = true;
       for (int g = 0; g < n_groups && ok; ++g) {
-        const int b0 = g * kMaxBlocks, b1 = min(n_blocks, b0 + kMaxBlocks);
+        const int b0 = g * kGroupBlocks, b1 = min(n_blocks, b0 + kGroupBlocks);
         if (!(ok = tc::mbar_wait(&sh->tmem_empty, tph ^ 1, abort_flag, status))) break;
         tph ^= 1;
         tc::fence_after_thread_sync();
@@ -388,16 +378,13 @@ lmhead_tc_kernel(const __grid_constant__ CUtensorMap map_h, const __grid_constan
             if (!(ok = tc::mbar_wait(&sh->w_full[ws], wph, abort_flag, status))) break;
             tc::fence_after_thread_sync();
             const uint32_t b_base = tc::smem_u32(w_smem + (size_t)ws * kWStageBytes);
-            const uint32_t d = tmem + (uint32_t)((blk - b0) * kRowsBlk);
+            const uint32_t idesc = tc::idesc_bf16_f32(128, blk_rows(blk));
+            const uint32_t d = tmem + (uint32_t)((blk - b0) * kBlkMax);
 #pragma unroll
-            for (int c = 0; c < kChunks; ++c) {
-#pragma unroll
-              for (int k16 = 0; k16 < kBK / 16; ++k16) {
-                tc::mma_f16(d, tc::desc_kmajor_sw128(a_base + c * h_chunk_bytes + k16 * 32),
-                            tc::desc_kmajor_sw128(b_base + c * (kRowsBlk * 128) + k16 * 32), idesc,
-                            (kb > 0 || c > 0 || k16 > 0) ? 1u : 0u);
-              }
-            }
+            for (int k16 = 0; k16 < kBK / 16; ++k16)
+              tc::mma_f16(d, tc::desc_kmajor_sw128(a_base + k16 * 32),
+                          tc::desc_kmajor_sw128(b_base + k16 * 32), idesc,
+                          (kb > 0 || k16 > 0) ? 1u : 0u);
             tc::mma_commit(&sh->w_empty[ws]);
             *(volatile int*)&sh->consumed_w += 1;
             if (++ws == w_stages) { ws = 0; wph ^= 1; }
@@ -426,57 +413,61 @@ lmhead_tc_kernel(const __grid_constant__ CUtensorMap map_h, const __grid_constan
     bool bad = false;
     uint32_t tph = 0;
     for (int g = 0; g < n_groups; ++g) {
-      const int b0 = g * kMaxBlocks, b1 = min(n_blocks, b0 + kMaxBlocks);
+      const int b0 = g * kGroupBlocks, b1 = min(n_blocks, b0 + kGroupBlocks);
       // every lane waits; the warp proceeds only if all of them saw the phase
       const bool got = tc::mbar_wait(&sh->tmem_full, tph, abort_flag, status);
       if (!__all_sync(0xffffffffu, got)) break;
       tph ^= 1;
       tc::fence_after_thread_sync();
       for (int blk = b0; blk < b1; ++blk) {
-        float v[32];
-        tc::tmem_ld_32x32b_x32(tmem + ((uint32_t)(quad * 32) << 16) + (uint32_t)((blk - b0) * kRowsBlk), v);
-        const int vb = (u0 + blk) * kRowsBlk;
-        const int nvalid = min(32, V - vb);
-        if (!row_ok || nvalid <= 0) continue;
-        if (z_out) {
-          float* dst = z_out + (size_t)t * V + vb;
-          if (vec && nvalid == 32) {
+        const int rows = blk_rows(blk);
+        for (int c = 0; c < rows; c += 32) {
+          float v[32];
+          tc::tmem_ld_32x32b_x32(tmem + ((uint32_t)(quad * 32) << 16) +
+                                     (uint32_t)((blk - b0) * kBlkMax + c), v);
+          const int vb = r_begin + blk * kBlkMax + c;
+          const int nvalid = min(min(32, rows - c), V - vb);
+          if (!row_ok || nvalid <= 0) continue;
+          if (z_out) {
+            float* dst = z_out + (size_t)t * V + vb;
+            if (vec && nvalid == 32) {
 #pragma unroll
-            for (int i = 0; i < 32; i += 4)
-              *reinterpret_cast<float4*>(dst + i) = make_float4(v[i], v[i + 1], v[i + 2], v[i + 3]);
+              for (int i = 0; i < 32; i += 4)
+                *reinterpret_cast<float4*>(dst + i) = make_float4(v[i], v[i + 1], v[i + 2], v[i + 3]);
+            } else {
+#pragma unroll
+              for (int i = 0; i < 32; ++i)
+                if (i < nvalid) dst[i] = v[i];
+            }
+          }
+          float cm = -INFINITY, cs = -INFINITY;
+          int ci = 0;
+#pragma unroll
+          for (int i = 0; i < 32; ++i) {
+            const float x = (i < nvalid) ? v[i] : -INFINITY;
+            if (i < nvalid) bad |= !isfinite(x);
+            if (x > cm) {
+              cs = cm;
+              cm = x;
+              ci = i;
+            } else if (x > cs) {
+              cs = x;
+            }
+          }
+          if (cm > m) {
+            second = fmaxf(m, cs);
+            s = (m == -INFINITY) ? 0.f : s * exp2f((m - cm) * k2);
+            m = cm;
+            idx = vb + ci;
           } else {
-#pragma unroll
-            for (int i = 0; i < 32; ++i)
-              if (i < nvalid) dst[i] = v[i];
+            second = fmaxf(second, cm);
           }
-        }
-        float cm = -INFINITY, cs = -INFINITY;
-        int ci = 0;
+          float acc = 0.f;
 #pragma unroll
-        for (int i = 0; i < 32; ++i) {
-          const float x = (i < nvalid) ? v[i] : -INFINITY;
-          if (i < nvalid) bad |= !isfinite(x);
-          if (x > cm) {
-            cs = cm;
-            cm = x;
-            ci = i;
-          } else if (x > cs) {
-            cs = x;
-          }
+          for (int i = 0; i < 32; ++i)
+            if (i < nvalid) acc += exp2f((v[i] - m) * k2);
+          s += acc;
         }
-        if (cm > m) {
-          second = fmaxf(m, cs);
-          s = (m == -INFINITY) ? 0.f : s * exp2f((m - cm) * k2);
-          m = cm;
-          idx = vb + ci;
-        } else {
-          second = fmaxf(second, cm);
-        }
-        float acc = 0.f;
-#pragma unroll
-        for (int i = 0; i < 32; ++i)
-          if (i < nvalid) acc += exp2f((v[i] - m) * k2);
-        s += acc;
       }
       tc::fence_before_thread_sync();
       __syncwarp();
@@ -527,22 +518,6 @@ bool make_map_bf16(CUtensorMap* map, const void* ptr, int rows, int cols, int bo
              CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
-// The same [rows, cols] bf16 tensor seen as {64 elements, rows, cols/64
-// chunks} (chunk stride 128 bytes): one box of box_rows x `chunks` lands in
-// shared memory as `chunks` consecutive [box_rows][128 B] swizzled tiles.
-bool make_map_bf16_chunked(CUtensorMap* map, const void* ptr, int rows, int cols, int box_rows,
-                           int chunks) {
-  auto enc = get_encode();
-  if (!enc || cols % kBK) return false;
-  cuuint64_t dims[3] = {(cuuint64_t)kBK, (cuuint64_t)rows, (cuuint64_t)(cols / kBK)};
-  cuuint64_t strides[2] = {(cuuint64_t)cols * 2, (cuuint64_t)kBK * 2};
-  cuuint32_t box[3] = {(cuuint32_t)kBK, (cuuint32_t)box_rows, (cuuint32_t)chunks};
-  cuuint32_t estr[3] = {1, 1, 1};
-  return enc(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(ptr), dims, strides, box,
-             estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
-             CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
-}
-
 int sm_count() {
   static int n = 0;
   if (!n) {
@@ -587,9 +562,8 @@ extern "C" eagle_status eagle_lmhead_softmax(eagle_dtype dtype, int T, int H, in
                      (((uintptr_t)d_h | (uintptr_t)d_w) & 15) == 0 &&
                      (!z || ((uintptr_t)z & 15) == 0);
   if (tc_ok) {
-    CUtensorMap map_w, map_w3;
-    if (!make_map_bf16(&map_w, d_w, V, H, kRowsBlk)) return EAGLE_ERR_CUDA;
-    const bool w3 = make_map_bf16_chunked(&map_w3, d_w, V, H, kRowsBlk, kChunks);
+    CUtensorMap map_w;
+    if (!make_map_bf16(&map_w, d_w, V, H, kUnit)) return EAGLE_ERR_CUDA;
     static bool attr = false;
     if (!attr) {
       if (cudaFuncSetAttribute(lmhead_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
@@ -597,20 +571,18 @@ extern "C" eagle_status eagle_lmhead_softmax(eagle_dtype dtype, int T, int H, in
         return EAGLE_ERR_CUDA;
       attr = true;
     }
-    const int n_units = (V + kRowsBlk - 1) / kRowsBlk;
+    const int n_units = (V + kUnit - 1) / kUnit;
     const int grid = std::min(sm_count(), n_units);
     // one pass over W per 128 tree rows (the MMA's M)
     for (int r0 = 0; r0 < T; r0 += 128) {
       const int Ts = std::min(128, T - r0);
       const TcLayout TL = tc_layout(Ts);
       const __nv_bfloat16* hs = static_cast<const __nv_bfloat16*>(d_h) + (size_t)r0 * H;
-      CUtensorMap map_h, map_h3;
+      CUtensorMap map_h;
       if (!make_map_bf16(&map_h, hs, Ts, H, TL.t_pad)) return EAGLE_ERR_CUDA;
-      const bool use3d = w3 && make_map_bf16_chunked(&map_h3, hs, Ts, H, TL.t_pad, kChunks);
       lmhead_tc_kernel<<<grid, kTcThreads, TL.smem, s>>>(
-          map_h, map_w, use3d ? map_h3 : map_h, use3d ? map_w3 : map_w, use3d ? 1 : 0, Ts, H, V,
-          temperature, z ? z + (size_t)r0 * V : nullptr, part + (size_t)r0 * grid, n_units,
-          TL.h_stage_bytes, TL.w_stages, d_status);
+          map_h, map_w, Ts, H, V, temperature, z ? z + (size_t)r0 * V : nullptr,
+          part + (size_t)r0 * grid, n_units, TL.h_stage_bytes, TL.w_stages, d_status);
       if (cudaGetLastError() != cudaSuccess) return EAGLE_ERR_CUDA;
     }
     dim3 fgrid(T, z ? (V + kFinChunk - 1) / kFinChunk : 1);

@@ -40,16 +40,19 @@ its reason, in the design notes):
       - test:    accept child c (token t) iff u_accept[c] * p_k[t] < q_k[t],
                  evaluated exactly (fp32 x fp32 is exact in fp64);
       - reject:  r = max(0, q_k - p_k) (fp32), W = trunc(r * 2^40) (integer),
-                 Z = sum W (exact), q_{k+1} = fp32(W) / fp32(Z);
+                 Z = sum W (exact), q_{k+1} = fp32(W) * rn(1 / fp32(Z));
                  Z == 0 keeps q_{k+1} = q_k;
       - p update, NO_REPLACE (siblings drawn without replacement): P =
                  trunc(p_k * 2^40) with the rejected token's entry zeroed,
-                 p_{k+1} = fp32(P) / fp32(sum P)  (all zero if the sum is 0);
+                 p_{k+1} = fp32(P) * rn(1 / fp32(sum P))  (all zero if the sum
+                 is 0);
                  REPLACE (siblings drawn i.i.d.): p_{k+1} = p_k;
       - stop:    sample from q_final by inverse CDF over W = trunc(q*2^40):
                  U = trunc(u_sample*2^24), target = (U*Z) >> 24, token =
                  smallest j whose inclusive prefix sum exceeds target.
-    Mass below 2^-40 per token is dropped (at most V*2^-40 in total).
+    Mass below 2^-40 per token is dropped (at most V*2^-40 in total).  Every
+    operation rounds to nearest once (rn), so the result is reproducible bit
+    for bit; the normalised value is within 1.5 ulp of fp32(W) / fp32(Z).
   * EAGLE-2 expand/rerank: a node's value is its cumulative draft log-prob
     (the log of the product of draft confidences along its path).  Level d:
     every frontier node takes the top-k tokens of its draft row (value
@@ -315,10 +318,12 @@ def _fixed40(x: np.ndarray) -> np.ndarray:
 
 
 def _normalise(Wint: np.ndarray, Z: int) -> np.ndarray:
-    """fp32(W) / fp32(Z), both conversions and the division round to nearest.
-    W <= 2^40 < 2^53, so W -> fp64 is exact and fp64 -> fp32 rounds once."""
+    """fp32(W) * (1 / fp32(Z)): the conversions, the reciprocal and the
+    product each round to nearest once.  W <= 2^40 < 2^53, so W -> fp64 is
+    exact and fp64 -> fp32 rounds once."""
     wf = Wint.astype(np.float64).astype(np.float32)
-    return (wf / f32_of_int(Z)).astype(np.float32)
+    rz = np.float32(np.float32(1.0) / f32_of_int(Z))
+    return (wf * rz).astype(np.float32)
 
 
 def _check_row(x: np.ndarray, what: str):
