@@ -5,15 +5,17 @@
 // selection under a fixed draft-token budget.  A node's value is its
 // cumulative draft log-prob.
 //
-// Two launches per level.  The level's draft rows (the only large data:
-// F x V fp32) are cut into chunks spread over the whole GPU; each CTA stages
-// its chunk in shared memory and writes the chunk's top-k list.  Then one
-// CTA per sequence merges every row's chunk lists (one warp per row, many
-// loads in flight) and builds the children and the next frontier.  The
-// finalize is one CTA per sequence working in shared memory.  Selection keys
-// are 64-bit integers (ordered value bits | inverted index), so every tie
-// rule is a plain max, and a warp keeps its running top-k as a sorted list
-// across its lanes.
+// One launch per level.  The level's draft rows (the only large data:
+// F x V fp32) are cut into chunks spread over the whole GPU; each CTA keeps
+// its chunk in registers and finds the chunk's exact top-k with a threshold:
+// the k-th largest of 32 group maxima is a lower bound of the chunk's k-th
+// largest key, so only the few keys above it take part in the exact rank
+// count.  The last CTA of a sequence to finish (an atomic ticket) merges the
+// rows' chunk lists the same way (one warp per row), then builds the
+// children and the next frontier.  The finalize is one CTA per sequence: a
+// radix select of the budget-th largest score key, then the numbering.
+// Selection keys are 64-bit integers (ordered value bits | inverted index),
+// so every tie rule is a plain integer comparison and all keys are distinct.
 #include <algorithm>
 
 #include "common.cuh"
@@ -22,36 +24,50 @@ using namespace eagle;
 
 namespace {
 
-constexpr int kExpandThreads = 256;
-constexpr int kChunkMax = 8192;     // floats staged per CTA
+constexpr int kLvThreads = 512;
+constexpr int kLvWarps = kLvThreads / 32;
+constexpr int kGroups = 32;            // half-warp groups per CTA (>= any k)
+constexpr int kCandCap = kLvThreads;   // chunk candidates held at once
+constexpr int kMaxVec = 4;             // float4 loads per thread
+constexpr int kMaxLevelCtas = 1216;    // 8 per SM before chunks grow
+constexpr int kRowCap = 128;           // row-merge candidates held at once
+constexpr int kMergeRegs = 8;          // chunk-list keys per lane kept in registers
 constexpr int kFinalThreads = 1024;
-constexpr int kMaxChunks = 64;      // chunks per row (V <= 64 * 8192)
+constexpr int kMaxV = 1 << 19;
+// Bound-raising rounds never exceed (keys / (cap - k)); past these limits a
+// selection stops with EAGLE_ERR_TIMEOUT instead of looping.
+constexpr int kChunkRounds = 32;   // keys per chunk <= 8192, cap - k >= 480
+constexpr int kRowRounds = 128;    // keys per row <= 8192, cap - k >= 96
 
-struct PoolLayout {
-  int P;         // candidate capacity per sequence
-  int rows_max;  // B * k
-  int S0, S1;    // chunks per row at level 0 / later levels
-  size_t off_count, off_frontier, off_token, off_parent, off_depth, off_prow, off_score,
-      off_partial, total;
+struct ChunkPlan {
+  int vec;  // float4 loads per thread
+  int S;    // chunks per row
 };
 
-int chunks_for(int rows, int V) {
-  int s = (304 + rows - 1) / rows;                   // ~2 CTAs per SM in total
-  s = std::min(s, kMaxChunks);                       // row merge fits in smem
-  s = std::min(s, std::max(1, V / 512));             // chunks of >= 512 tokens
-  s = std::max(s, (V + kChunkMax - 1) / kChunkMax);  // chunk fits in smem
-  return std::max(s, 1);
+ChunkPlan chunk_plan(int rows, int V) {
+  ChunkPlan p{1, 1};
+  for (p.vec = 1;; p.vec *= 2) {
+    p.S = ceil_div(V, (long long)kLvThreads * 4 * p.vec);
+    if (p.vec == kMaxVec || (long long)rows * p.S <= kMaxLevelCtas) break;
+  }
+  return p;
 }
 
 size_t align256(size_t x) { return (x + 255) & ~(size_t)255; }
 
+struct PoolLayout {
+  int P;             // candidate capacity per sequence
+  ChunkPlan c0, c1;  // level 0 / later levels
+  size_t off_count, off_ticket, off_frontier, off_fscore, off_token, off_parent, off_depth,
+      off_prow, off_score, off_partial, total;
+};
+
 PoolLayout pool_layout(int B, int k, int depth, int V) {
   PoolLayout L;
   L.P = k + (depth - 1) * k * k;
-  L.rows_max = B * k;
-  L.S0 = chunks_for(B, V);
-  L.S1 = chunks_for(B * k, V);
-  const size_t parts = std::max((size_t)B * L.S0, (size_t)B * k * L.S1) * k;
+  L.c0 = chunk_plan(B, V);
+  L.c1 = chunk_plan(B * k, V);
+  const size_t parts = std::max((size_t)B * L.c0.S, (size_t)B * k * L.c1.S) * k;
   size_t o = 0;
   auto take = [&](size_t bytes) {
     size_t at = o;
@@ -59,7 +75,9 @@ PoolLayout pool_layout(int B, int k, int depth, int V) {
     return at;
   };
   L.off_count = take((size_t)B * 4);
+  L.off_ticket = take((size_t)B * 4);
   L.off_frontier = take((size_t)B * k * 4);
+  L.off_fscore = take((size_t)B * k * 4);
   L.off_token = take((size_t)B * L.P * 4);
   L.off_parent = take((size_t)B * L.P * 4);
   L.off_depth = take((size_t)B * L.P * 4);
@@ -71,21 +89,25 @@ PoolLayout pool_layout(int B, int k, int depth, int V) {
 }
 
 struct PoolPtrs {
-  int* count;
-  int* frontier;
+  int* count;     // [B] pool fill
+  int* ticket;    // [B] CTAs of the running level that have finished
+  int* frontier;  // [B, k] pool index of the frontier, by rank
+  float* fscore;  // [B, k] its score
   int* token;
   int* parent;
   int* depth;
   int* prow;
   float* score;
-  unsigned long long* partial;
+  unsigned long long* partial;  // chunk top-k lists
 };
 
 PoolPtrs pool_ptrs(void* base, const PoolLayout& L) {
   char* c = static_cast<char*>(base);
   PoolPtrs p;
   p.count = reinterpret_cast<int*>(c + L.off_count);
+  p.ticket = reinterpret_cast<int*>(c + L.off_ticket);
   p.frontier = reinterpret_cast<int*>(c + L.off_frontier);
+  p.fscore = reinterpret_cast<float*>(c + L.off_fscore);
   p.token = reinterpret_cast<int*>(c + L.off_token);
   p.parent = reinterpret_cast<int*>(c + L.off_parent);
   p.depth = reinterpret_cast<int*>(c + L.off_depth);
@@ -97,152 +119,287 @@ PoolPtrs pool_ptrs(void* base, const PoolLayout& L) {
 
 struct LevelParams {
   int B, V, k, F, R, S, level, P;
+  bool vec_ok;  // rows 16-byte aligned: float4 loads
   const float* logp;
   PoolPtrs pool;
   int* status;
 };
 
-__device__ __forceinline__ unsigned long long shfl_u64(unsigned long long v, int src) {
-  return __shfl_sync(0xffffffffu, v, src);
+__device__ __forceinline__ unsigned long long umax64(unsigned long long a, unsigned long long b) {
+  return a > b ? a : b;
 }
-__device__ __forceinline__ unsigned long long shfl_up_u64(unsigned long long v, int d) {
-  return __shfl_up_sync(0xffffffffu, v, d);
+__device__ __forceinline__ unsigned lanemask_lt() {
+  return (1u << (threadIdx.x & 31)) - 1u;
 }
 
-// Warp-wide running top-k: lane j holds the j-th largest key seen (0 =
-// empty), `thr` the k-th (0 while fewer than k).  Feeds 32 keys (one per
-// lane) at a time.
-struct WarpTopk {
-  unsigned long long mine = 0ull, thr = 0ull;
-  __device__ __forceinline__ void feed(unsigned long long key, int k) {
-    const int lane = threadIdx.x & 31;
-    unsigned bal = __ballot_sync(0xffffffffu, key > thr);
-    while (bal) {
-      const int src = __ffs(bal) - 1;
-      bal &= bal - 1;
-      const unsigned long long cand = shfl_u64(key, src);
-      if (cand <= thr) continue;  // uniform: the threshold may have risen
-      const int pos = __popc(__ballot_sync(0xffffffffu, lane < k && mine > cand));
-      const unsigned long long up = shfl_up_u64(mine, 1);
-      if (lane < k) {
-        if (lane > pos) mine = up;
-        else if (lane == pos) mine = cand;
-      }
-      thr = shfl_u64(mine, k - 1);
-    }
-  }
+// The key of the first lane named in `bal` (warp-uniform), or `fallback`
+// when `bal` is empty or that key is the empty key 0.  Callers pass 1 as the
+// fallback bound: every real key (never 0) is at least 1.
+__device__ __forceinline__ unsigned long long pick_lane(unsigned bal, unsigned long long v,
+                                                        unsigned long long fallback) {
+  const int src = bal ? __ffs(bal) - 1 : 0;
+  const unsigned long long got = __shfl_sync(0xffffffffu, v, src);
+  return (bal && got) ? got : fallback;
+}
+
+struct MergeShared {
+  unsigned long long lane_max[kLvWarps][32];
+  unsigned long long cand[kLvWarps][kRowCap];
+  unsigned long long row[EAGLE_MAX_TOPK][EAGLE_MAX_TOPK];
+  unsigned long long child[EAGLE_MAX_TOPK * EAGLE_MAX_TOPK];
+  int fidx[EAGLE_MAX_TOPK];
+  float fsc[EAGLE_MAX_TOPK];
+  int base;
 };
 
-// Level kernel 1: top-k of one chunk of one draft row per CTA.
-__global__ void __launch_bounds__(kExpandThreads) expand_chunk_kernel(const LevelParams A) {
-  __shared__ __align__(16) float s_val[kChunkMax];
-  __shared__ unsigned long long s_wtop[(kExpandThreads / 32) * EAGLE_MAX_TOPK];
-  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5, nw = blockDim.x >> 5;
-  const int row = blockIdx.x / A.S;       // global frontier row: b * F + f
-  const int chunk = blockIdx.x % A.S;
-  const int b = row / A.F;
-  const int f = row % A.F;
-  const int local_row = (A.level == 0) ? 0 : 1 + (A.level - 1) * A.k + f;
-  const float* src = A.logp + ((size_t)b * A.R + local_row) * A.V;
-  const int csize = (A.V + A.S - 1) / A.S;
-  const int c0 = min(A.V, chunk * csize), c1 = min(A.V, c0 + csize);
-  const int n = c1 - c0;
-  const int k = A.k;
-  // stage the chunk (vectorised when the row and the chunk are 16-byte aligned)
-  int bad = 0;
-  if (((A.V | csize) & 3) == 0) {
-    const float4* s4 = reinterpret_cast<const float4*>(src + c0);
-    for (int i = tid; i < (n >> 2); i += blockDim.x) {
-      const float4 x = __ldg(s4 + i);
-      reinterpret_cast<float4*>(s_val)[i] = x;
-      bad |= !(isfinite(x.x) && isfinite(x.y) && isfinite(x.z) && isfinite(x.w));
+// Exact top-k (descending) of n keys at `src` (written by other CTAs: read
+// through L2) by one warp; out[0..k) in order, 0 where fewer than k keys.
+__device__ void warp_row_topk(const unsigned long long* src, int n, int k,
+                              unsigned long long* lane_max, unsigned long long* cand,
+                              unsigned long long* out, int* status) {
+  const int lane = threadIdx.x & 31;
+  const bool cached = n <= 32 * kMergeRegs;
+  unsigned long long reg[kMergeRegs];
+  unsigned long long lmax = 0;
+  if (cached) {
+#pragma unroll
+    for (int r = 0; r < kMergeRegs; ++r) {
+      const int i = r * 32 + lane;
+      reg[r] = (i < n) ? __ldcg(src + i) : 0ull;
+      lmax = umax64(lmax, reg[r]);
     }
   } else {
-    for (int i = tid; i < n; i += blockDim.x) {
-      const float x = __ldg(src + c0 + i);
-      s_val[i] = x;
-      bad |= !isfinite(x);
+    for (int i = lane; i < n; i += 32) lmax = umax64(lmax, __ldcg(src + i));
+  }
+  // lower bound of the k-th largest: the k-th largest lane maximum
+  lane_max[lane] = lmax;
+  __syncwarp();
+  int rank = 0;
+#pragma unroll 8
+  for (int j = 0; j < 32; ++j) rank += (lane_max[j] > lmax);
+  unsigned long long tau = pick_lane(__ballot_sync(0xffffffffu, rank == k - 1), lmax, 1ull);
+  int cnt;
+  for (int round = 0;; ++round) {
+    cnt = 0;
+    auto offer = [&](unsigned long long key) {
+      const bool pred = key >= tau;
+      const unsigned bal = __ballot_sync(0xffffffffu, pred);
+      const int pos = cnt + __popc(bal & lanemask_lt());
+      if (pred && pos < kRowCap) cand[pos] = key;
+      cnt += __popc(bal);
+    };
+    if (cached) {
+#pragma unroll
+      for (int r = 0; r < kMergeRegs; ++r) offer(reg[r]);
+    } else {
+      for (int i0 = 0; i0 < n; i0 += 32) offer(i0 + lane < n ? __ldcg(src + i0 + lane) : 0ull);
     }
-  }
-  if (__syncthreads_or(bad) && tid == 0) fail(A.status, EAGLE_ERR_NUMERIC);
-  // each warp a contiguous slice, then warp 0 merges the warps' lists
-  const int per = (n + nw - 1) / nw;
-  const int lo = min(n, warp * per), cnt = min(n, lo + per) - lo;
-  WarpTopk wt;
-  for (int base = 0; base < cnt; base += 32) {
-    const int i = base + lane;
-    wt.feed(i < cnt ? desc_key(s_val[lo + i], (uint32_t)(c0 + lo + i)) : 0ull, k);
-  }
-  if (lane < k) s_wtop[warp * k + lane] = wt.mine;
-  __syncthreads();
-  if (warp == 0) {
-    WarpTopk m;
-    for (int base = 0; base < nw * k; base += 32) {
-      const int i = base + lane;
-      m.feed(i < nw * k ? s_wtop[i] : 0ull, k);
+    __syncwarp();
+    if (cnt <= kRowCap) break;
+    if (round == kRowRounds) {
+      if (lane == 0) fail(status, EAGLE_ERR_TIMEOUT);
+      cnt = kRowCap;
+      break;
     }
-    if (lane < k) A.pool.partial[((size_t)row * A.S + chunk) * k + lane] = m.mine;
+    // too many: the k-th largest of the held ones is a higher lower bound
+    // (each round drops at least kRowCap - k keys)
+    unsigned long long m[kRowCap / 32];
+    int rk[kRowCap / 32];
+#pragma unroll
+    for (int t = 0; t < kRowCap / 32; ++t) {
+      m[t] = cand[t * 32 + lane];
+      rk[t] = 0;
+    }
+    for (int j = 0; j < kRowCap; ++j) {
+      const unsigned long long c = cand[j];
+#pragma unroll
+      for (int t = 0; t < kRowCap / 32; ++t) rk[t] += (c > m[t]);
+    }
+    __syncwarp();
+    unsigned long long nt = 0;
+#pragma unroll
+    for (int t = 0; t < kRowCap / 32; ++t)
+      nt = umax64(nt, pick_lane(__ballot_sync(0xffffffffu, rk[t] == k - 1), m[t], 0ull));
+    tau = nt;
   }
+  for (int t = lane; t < cnt; t += 32) {
+    const unsigned long long me = cand[t];
+    int r = 0;
+    for (int j = 0; j < cnt; ++j) r += (cand[j] > me);
+    if (r < k) out[r] = me;
+  }
+  for (int t = cnt + lane; t < k; t += 32) out[t] = 0ull;
+  __syncwarp();
 }
 
-// Level kernel 2 (one CTA per sequence): merge every row's chunk lists
-// (one warp per row) and build the children and the next frontier.
-constexpr int kMergeThreads = 512;
-constexpr int kMergeBatch = 8;          // 32-key batches loaded before use
-
-__global__ void __launch_bounds__(kMergeThreads) expand_merge_kernel(const LevelParams A) {
-  __shared__ unsigned long long s_row[EAGLE_MAX_TOPK][EAGLE_MAX_TOPK];
-  __shared__ unsigned long long s_cand[EAGLE_MAX_TOPK * EAGLE_MAX_TOPK];
-  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5, nw = blockDim.x >> 5;
-  const int b = blockIdx.x;
-  const int k = A.k, F = A.F;
-  const int n = A.S * k;                  // candidates per row
-  for (int f = warp; f < F; f += nw) {
-    const unsigned long long* src = A.pool.partial + (size_t)(b * F + f) * n;
-    WarpTopk wt;
-    for (int base0 = 0; base0 < n; base0 += 32 * kMergeBatch) {
-      unsigned long long buf[kMergeBatch];
+// One level.  CTA (row, chunk): exact top-k of the chunk -> partial list.
+// The sequence's last CTA: per-row top-k, children, next frontier.
+template <int VEC>
+__global__ void __launch_bounds__(kLvThreads, 2) expand_level_kernel(const LevelParams A) {
+  __shared__ unsigned long long s_grp[kGroups];
+  __shared__ unsigned long long s_cand[kCandCap];
+  __shared__ unsigned long long s_tau;
+  __shared__ int s_cnt, s_last;
+  __shared__ MergeShared M;
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  const int row = blockIdx.x / A.S, chunk = blockIdx.x % A.S;
+  const int b = row / A.F, f = row % A.F;
+  const int k = A.k;
+  const int local_row = (A.level == 0) ? 0 : 1 + (A.level - 1) * k + f;
+  const float* src = A.logp + ((size_t)b * A.R + local_row) * A.V;
+  const int c0 = chunk * (kLvThreads * 4 * VEC);
+  // ---- chunk in registers: element c0 + (j * threads + tid) * 4 + e
+  float v[VEC][4];
+  bool bad = false;
 #pragma unroll
-      for (int j = 0; j < kMergeBatch; ++j) {
-        const int i = base0 + j * 32 + lane;
-        buf[j] = (i < n) ? __ldcg(src + i) : 0ull;
-      }
+  for (int j = 0; j < VEC; ++j) {
+    const int i0 = c0 + (j * kLvThreads + tid) * 4;
+    if (A.vec_ok && i0 + 4 <= A.V) {
+      const float4 x = __ldg(reinterpret_cast<const float4*>(src + i0));
+      v[j][0] = x.x;
+      v[j][1] = x.y;
+      v[j][2] = x.z;
+      v[j][3] = x.w;
+    } else {
 #pragma unroll
-      for (int j = 0; j < kMergeBatch; ++j) wt.feed(buf[j], k);
+      for (int e = 0; e < 4; ++e) v[j][e] = (i0 + e < A.V) ? __ldg(src + i0 + e) : 0.f;
     }
-    if (lane < k) s_row[f][lane] = wt.mine;
+  }
+  auto key_of = [&](int j, int e) -> unsigned long long {
+    const int i = c0 + (j * kLvThreads + tid) * 4 + e;
+    return (i < A.V) ? desc_key(v[j][e], (uint32_t)i) : 0ull;
+  };
+  unsigned long long tmax = 0;
+#pragma unroll
+  for (int j = 0; j < VEC; ++j)
+#pragma unroll
+    for (int e = 0; e < 4; ++e) {
+      const int i = c0 + (j * kLvThreads + tid) * 4 + e;
+      if (i < A.V) bad |= !isfinite(v[j][e]);
+      tmax = umax64(tmax, key_of(j, e));
+    }
+#pragma unroll
+  for (int o = 8; o > 0; o >>= 1) tmax = umax64(tmax, __shfl_xor_sync(0xffffffffu, tmax, o));
+  if ((lane & 15) == 0) s_grp[warp * 2 + (lane >> 4)] = tmax;
+  if (tid == 0) s_cnt = 0;
+  if (__syncthreads_or(bad) && tid == 0) fail(A.status, EAGLE_ERR_NUMERIC);
+  if (warp == 0) {
+    // the k-th largest group maximum: k distinct keys of the chunk reach it
+    const unsigned long long g = s_grp[lane];
+    int rank = 0;
+#pragma unroll 8
+    for (int i = 0; i < kGroups; ++i) rank += (s_grp[i] > g);
+    const unsigned long long t = pick_lane(__ballot_sync(0xffffffffu, rank == k - 1), g, 1ull);
+    if (lane == 0) s_tau = t;
   }
   __syncthreads();
+  unsigned long long tau = s_tau;
+  int cnt;
+  for (int round = 0;; ++round) {
+#pragma unroll
+    for (int j = 0; j < VEC; ++j)
+#pragma unroll
+      for (int e = 0; e < 4; ++e) {
+        const unsigned long long key = key_of(j, e);
+        const bool pred = key >= tau;
+        const unsigned bal = __ballot_sync(0xffffffffu, pred);
+        if (bal) {
+          const int leader = __ffs(bal) - 1;
+          int base = 0;
+          if (lane == leader) base = atomicAdd(&s_cnt, __popc(bal));
+          base = __shfl_sync(0xffffffffu, base, leader);
+          const int pos = base + __popc(bal & lanemask_lt());
+          if (pred && pos < kCandCap) s_cand[pos] = key;
+        }
+      }
+    __syncthreads();
+    cnt = s_cnt;
+    if (cnt <= kCandCap) break;
+    if (round == kChunkRounds) {
+      if (tid == 0) fail(A.status, EAGLE_ERR_TIMEOUT);
+      cnt = kCandCap;
+      break;
+    }
+    // too many: raise the bound to the k-th largest of the held ones
+    // (each round drops at least kCandCap - k keys)
+    const unsigned long long me = s_cand[tid];
+    int rank = 0;
+    for (int i = 0; i < kCandCap; ++i) rank += (s_cand[i] > me);
+    __syncthreads();
+    if (rank == k - 1) s_tau = me;
+    if (tid == 0) s_cnt = 0;
+    __syncthreads();
+    tau = s_tau;
+  }
+  unsigned long long* part = A.pool.partial + ((size_t)row * A.S + chunk) * k;
+  if (tid < cnt) {
+    const unsigned long long me = s_cand[tid];
+    int rank = 0;
+    for (int i = 0; i < cnt; ++i) rank += (s_cand[i] > me);
+    if (rank < k) part[rank] = me;
+  } else if (tid < k) {
+    part[tid] = 0ull;  // fewer than k tokens in this chunk
+  }
+  // ---- the sequence's last CTA merges
+  __threadfence();
+  __syncthreads();
+  if (tid == 0) {
+    const int t = atomicAdd(&A.pool.ticket[b], 1);
+    s_last = (t == A.F * A.S - 1);
+  }
+  __syncthreads();
+  if (!s_last) return;
+  __threadfence();
+  const int F = A.F;
+  int* front = A.pool.frontier + (size_t)b * k;
+  float* fsc = A.pool.fscore + (size_t)b * k;
+  if (tid < F) {
+    M.fidx[tid] = (A.level == 0) ? -1 : __ldcg(front + tid);
+    M.fsc[tid] = (A.level == 0) ? 0.f : __ldcg(fsc + tid);
+  }
+  if (tid == 0) {
+    M.base = __ldcg(A.pool.count + b);
+    A.pool.ticket[b] = 0;  // ready for the next level
+  }
+  const int n = A.S * k;
+  for (int ff = warp; ff < F; ff += kLvWarps)
+    warp_row_topk(A.pool.partial + (size_t)(b * F + ff) * n, n, k, M.lane_max[warp],
+                  M.cand[warp], M.row[ff], A.status);
+  __syncthreads();
   const int nc = F * k;  // children in creation order (f-major, rank-minor)
-  const int base = A.pool.count[b];
+  const int base = M.base;
+  if (base < 0 || base + nc > A.P) {  // more levels than the pool was sized for
+    if (tid == 0) fail(A.status, EAGLE_ERR_INVALID_ARG);
+    return;
+  }
   int* tok = A.pool.token + (size_t)b * A.P;
   int* par = A.pool.parent + (size_t)b * A.P;
   int* dep = A.pool.depth + (size_t)b * A.P;
   int* prw = A.pool.prow + (size_t)b * A.P;
   float* sco = A.pool.score + (size_t)b * A.P;
-  int* front = A.pool.frontier + (size_t)b * k;
-  for (int c = tid; c < nc; c += blockDim.x) {
+  for (int c = tid; c < nc; c += kLvThreads) {
     const int ff = c / k, rr = c % k;
-    const unsigned long long key = s_row[ff][rr];
-    const int pidx = (A.level == 0) ? -1 : front[ff];
-    const float pscore = (A.level == 0) ? 0.f : sco[pidx];
-    const float sc = __fadd_rn(pscore, key_value(key));
+    const unsigned long long key = M.row[ff][rr];
+    const float sc = __fadd_rn(M.fsc[ff], key_value(key));
     const int at = base + c;
     tok[at] = (int)key_index(key);
-    par[at] = pidx;
+    par[at] = M.fidx[ff];
     dep[at] = A.level + 1;
     prw[at] = (A.level == 0) ? 0 : 1 + (A.level - 1) * k + ff;
     sco[at] = sc;
-    s_cand[c] = desc_key(sc, (uint32_t)c);
+    M.child[c] = desc_key(sc, (uint32_t)c);
   }
   __syncthreads();
   // next frontier: rank of every child by (score desc, creation order)
-  for (int c = tid; c < nc; c += blockDim.x) {
-    const unsigned long long me = s_cand[c];
+  for (int c = tid; c < nc; c += kLvThreads) {
+    const unsigned long long me = M.child[c];
     int rank = 0;
 #pragma unroll 8
-    for (int j = 0; j < nc; ++j) rank += (s_cand[j] > me);
-    if (rank < k) front[rank] = base + c;
+    for (int j = 0; j < nc; ++j) rank += (M.child[j] > me);
+    if (rank < k) {
+      front[rank] = base + c;
+      fsc[rank] = key_value(me);
+    }
   }
   if (tid == 0) A.pool.count[b] = base + nc;
 }
@@ -261,76 +418,121 @@ struct FinalParams {
   int* status;
 };
 
-// Finalize, one CTA per sequence: rank every pool entry by (score desc,
-// creation order), keep the top `budget`, number the kept nodes by (depth,
-// score desc, creation order) and write the tree.
+// Finalize, one CTA per sequence: keep the `budget` pool entries of largest
+// key (score desc, creation order) -- a radix select of the budget-th key --
+// number the kept nodes by (depth, score desc, creation order) and write the
+// tree.
 __global__ void __launch_bounds__(kFinalThreads) expand_finalize_kernel(const FinalParams A) {
   extern __shared__ __align__(16) unsigned char smem_raw[];
   unsigned long long* s_key = reinterpret_cast<unsigned long long*>(smem_raw);  // [P]
-  int* s_list = reinterpret_cast<int*>(s_key + A.P);                            // [P]
-  int* s_num = s_list + A.P;                                                    // [P]
-  int* s_node = s_num + A.P;                                                    // [P]
-  __shared__ int s_nsel;
+  int* s_dep = reinterpret_cast<int*>(s_key + A.P);                             // [P]
+  int* s_node = s_dep + A.P;                                                    // [P]
+  int* s_list = s_node + A.P;                                                   // [P]
+  __shared__ int s_hist[256];
+  __shared__ int s_digit, s_rem, s_eq, s_nsel, s_off;
   const int b = blockIdx.x;
-  const int tid = threadIdx.x;
-  const int n = A.pool.count[b];
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  const int n = max(0, min(A.pool.count[b], A.P));
   const int bud = A.budget[b];
   const int keep = min(max(bud, 0), n);
   const float* sco = A.pool.score + (size_t)b * A.P;
+  const int* dep = A.pool.depth + (size_t)b * A.P;
   if (tid == 0) {
     s_nsel = 0;
     if (bud < 0) fail(A.status, EAGLE_ERR_INVALID_ARG);
   }
+  if (warp == 1) {
+    // node offset of this sequence: sum over earlier sequences of kept + root
+    int off = 0;
+    for (int j = lane; j < b; j += 32)
+      off += min(max(A.budget[j], 0), max(0, min(A.pool.count[j], A.P))) + 1;
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) off += __shfl_xor_sync(0xffffffffu, off, o);
+    if (lane == 0) s_off = off;
+  }
   for (int i = tid; i < n; i += blockDim.x) {
     s_key[i] = desc_key(sco[i], (uint32_t)i);
+    s_dep[i] = dep[i];
     s_node[i] = -1;
   }
-  __syncthreads();
-  for (int i = tid; i < n; i += blockDim.x) {
-    const unsigned long long me = s_key[i];
-    int r0 = 0, r1 = 0, r2 = 0, r3 = 0;
-    int j = 0;
-    for (; j + 4 <= n; j += 4) {
-      r0 += (s_key[j] > me);
-      r1 += (s_key[j + 1] > me);
-      r2 += (s_key[j + 2] > me);
-      r3 += (s_key[j + 3] > me);
+  // radix select (8 bits at a time, high to low) of the keep-th largest key
+  unsigned long long prefix = 0, mask = 0;
+  int rem = keep;
+  if (keep > 0 && keep < n) {
+    for (int shift = 56; shift >= 0; shift -= 8) {
+      if (tid < 256) s_hist[tid] = 0;
+      __syncthreads();
+      for (int i = tid; i < n; i += blockDim.x) {
+        const unsigned long long key = s_key[i];
+        if ((key & mask) == prefix) atomicAdd(&s_hist[(int)(key >> shift) & 255], 1);
+      }
+      __syncthreads();
+      if (warp == 0) {
+        int h[8], tot = 0;
+#pragma unroll
+        for (int d = 0; d < 8; ++d) {
+          h[d] = s_hist[lane * 8 + d];
+          tot += h[d];
+        }
+        int incl = tot;  // sum over this lane and the lanes above it
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1) {
+          const int t = __shfl_down_sync(0xffffffffu, incl, o);
+          if (lane + o < 32) incl += t;
+        }
+        int above = incl - tot;
+#pragma unroll
+        for (int d = 7; d >= 0; --d) {
+          if (above < rem && rem <= above + h[d]) {
+            s_digit = lane * 8 + d;
+            s_rem = rem - above;
+            s_eq = h[d];
+          }
+          above += h[d];
+        }
+      }
+      __syncthreads();
+      prefix |= (unsigned long long)s_digit << shift;
+      mask |= 255ull << shift;
+      rem = s_rem;
+      if (s_eq == rem) break;  // every key under this prefix is kept
     }
-    for (; j < n; ++j) r0 += (s_key[j] > me);
-    if (r0 + r1 + r2 + r3 < keep) s_list[atomicAdd(&s_nsel, 1)] = i;
   }
+  // kept: keys >= the threshold (prefix, low bits zero), exactly `keep` of them
+  const unsigned long long tau = (keep == 0) ? ~0ull : (keep == n ? 1ull : prefix);
+  __syncthreads();
+  for (int i = tid; i < n; i += blockDim.x)
+    if (keep > 0 && s_key[i] >= tau) s_list[atomicAdd(&s_nsel, 1)] = i;
   __syncthreads();
   const int ns = s_nsel;
-  const int* tok = A.pool.token + (size_t)b * A.P;
-  const int* par = A.pool.parent + (size_t)b * A.P;
-  const int* dep = A.pool.depth + (size_t)b * A.P;
-  const int* prw = A.pool.prow + (size_t)b * A.P;
-  int off = 0;
-  for (int j = 0; j < b; ++j) off += min(max(A.budget[j], 0), A.pool.count[j]) + 1;
+  const int off = s_off;
   // node number of every kept entry: 1 + rank by (depth, score desc, creation)
   for (int a = tid; a < ns; a += blockDim.x) {
     const int ia = s_list[a];
-    const int da = dep[ia];
+    const int da = s_dep[ia];
     const unsigned long long ka = s_key[ia];
     int rank = 0;
     for (int c = 0; c < ns; ++c) {
       const int ic = s_list[c];
-      rank += (dep[ic] < da) || (dep[ic] == da && s_key[ic] > ka);
+      const int dc = s_dep[ic];
+      rank += (dc < da) || (dc == da && s_key[ic] > ka);
     }
-    s_num[a] = 1 + rank;
     s_node[ia] = 1 + rank;
   }
   __syncthreads();
+  const int* tok = A.pool.token + (size_t)b * A.P;
+  const int* par = A.pool.parent + (size_t)b * A.P;
+  const int* prw = A.pool.prow + (size_t)b * A.P;
   for (int a = tid; a < ns; a += blockDim.x) {
     const int ia = s_list[a];
     const int pp = par[ia];
-    const int pnode = (pp < 0) ? 0 : s_node[pp];
+    const int pnode = (pp < 0) ? 0 : (pp < n ? s_node[pp] : -1);
     if (pnode < 0) fail(A.status, EAGLE_ERR_INVALID_TREE);  // not parent-closed
-    const int at = off + s_num[a];
+    const int at = off + s_node[ia];
     A.parent[at] = pnode;
     A.tokens[at] = tok[ia];
-    A.node_depth[at] = dep[ia];
-    A.score[at] = sco[ia];
+    A.node_depth[at] = s_dep[ia];
+    A.score[at] = key_value(s_key[ia]);
     A.p_row_of_node[at] = b * A.R + prw[ia];
   }
   if (tid == 0) {
@@ -348,7 +550,7 @@ __global__ void __launch_bounds__(kFinalThreads) expand_finalize_kernel(const Fi
 
 extern "C" size_t eagle_draft_pool_bytes(int B, int k, int depth, int V) {
   if (B < 1 || k < 1 || k > EAGLE_MAX_TOPK || depth < 1 || depth > EAGLE_MAX_DEPTH || V < k ||
-      V > kMaxChunks * kChunkMax)
+      V > kMaxV)
     return 0;
   return pool_layout(B, k, depth, V).total;
 }
@@ -364,7 +566,7 @@ extern "C" eagle_status eagle_draft_expand(int B, int V, int k, int depth, int l
   EAGLE_HOST_CHECK(B >= 1 && V >= 1, EAGLE_ERR_INVALID_ARG);
   EAGLE_HOST_CHECK(k >= 1 && k <= EAGLE_MAX_TOPK && k <= V, EAGLE_ERR_UNSUPPORTED);
   EAGLE_HOST_CHECK(depth >= 1 && depth <= EAGLE_MAX_DEPTH, EAGLE_ERR_UNSUPPORTED);
-  EAGLE_HOST_CHECK(V <= kMaxChunks * kChunkMax, EAGLE_ERR_UNSUPPORTED);
+  EAGLE_HOST_CHECK(V <= kMaxV, EAGLE_ERR_UNSUPPORTED);
   EAGLE_HOST_CHECK(d_pool && d_status, EAGLE_ERR_INVALID_ARG);
   const PoolLayout L = pool_layout(B, k, depth, V);
   EAGLE_HOST_CHECK(pool_bytes >= L.total, EAGLE_ERR_WORKSPACE);
@@ -376,25 +578,30 @@ extern "C" eagle_status eagle_draft_expand(int B, int V, int k, int depth, int l
     EAGLE_HOST_CHECK(level >= 0 && level < depth, EAGLE_ERR_INVALID_ARG);
     EAGLE_HOST_CHECK(d_draft_logp, EAGLE_ERR_INVALID_ARG);
     if (level == 0) {
-      // fresh tree: zero the pool fill counts
+      // fresh tree: zero the pool fill counts and the level tickets
       cudaError_t e = cudaMemsetAsync(static_cast<char*>(d_pool), 0, L.off_frontier, s);
       if (e != cudaSuccess) return EAGLE_ERR_CUDA;
     }
+    const ChunkPlan cp = (level == 0) ? L.c0 : L.c1;
     LevelParams A;
     A.B = B;
     A.V = V;
     A.k = k;
     A.F = (level == 0) ? 1 : k;
     A.R = R;
-    A.S = (level == 0) ? L.S0 : L.S1;
+    A.S = cp.S;
     A.level = level;
     A.P = L.P;
+    A.vec_ok = (V % 4 == 0) && ((uintptr_t)d_draft_logp % 16 == 0);
     A.logp = d_draft_logp;
     A.pool = pp;
     A.status = d_status;
-    expand_chunk_kernel<<<B * A.F * A.S, kExpandThreads, 0, s>>>(A);
-    if (cudaGetLastError() != cudaSuccess) return EAGLE_ERR_CUDA;
-    expand_merge_kernel<<<B, kMergeThreads, 0, s>>>(A);
+    const int grid = B * A.F * A.S;
+    switch (cp.vec) {
+      case 1: expand_level_kernel<1><<<grid, kLvThreads, 0, s>>>(A); break;
+      case 2: expand_level_kernel<2><<<grid, kLvThreads, 0, s>>>(A); break;
+      default: expand_level_kernel<4><<<grid, kLvThreads, 0, s>>>(A); break;
+    }
     return launch_status(cudaGetLastError());
   }
   EAGLE_HOST_CHECK(d_budget && d_tree_off && d_parent && d_tokens && d_node_depth && d_score &&

@@ -170,7 +170,7 @@ class TreeVerifyStep:
         """Kernels launched by run() (the count the benchmark reports)."""
         n = 0
         if self.s.k:
-            n += 2 * self.s.depth + 1            # chunk + merge per level, finalize
+            n += self.s.depth + 1                # one per level, finalize
         n += 1                                   # attention
         if self.s.dtype == "bf16":               # LM head: one pass per 128 rows
             n += (self.s.T + 127) // 128 + 1     # ... + finalize

@@ -79,3 +79,41 @@ def test_expand_reports_non_finite_log_probs():
     lp[0, 17] = np.nan
     _, st = _gpu_tree(E, lp, B, V, k, depth, [5], [0])
     assert st == 4                            # EAGLE_ERR_NUMERIC
+
+
+@pytest.mark.parametrize("B,V,k,depth,budgets,order", [
+    (1, 40000, 32, 3, [300], "random"),       # many chunk-list keys above the first bound
+    (1, 32000, 10, 3, [40], "descending"),    # one chunk holds every top key
+    (2, 9000, 7, 3, [30, 50], "ascending"),   # top keys at the row's ragged end
+])
+def test_expand_concentrated_top_keys(B, V, k, depth, budgets, order):
+    # Rows whose top keys crowd into one chunk (sorted rows) or into many
+    # chunk lists at once (k = 32): the selection bounds must be raised
+    # several times before the exact rank count; the tree must not change.
+    E = cuda_ready()
+    R = 1 + (depth - 1) * k
+    lp, _ = synth.draft_rows(V + k, "concentrated", B * R, V, 3.0)
+    if order != "random":
+        lp = np.sort(lp, axis=1)
+        if order == "descending":
+            lp = lp[:, ::-1].copy()
+    ref = O.build_eagle2_tree(lp, B=B, k=k, depth=depth, budget=budgets,
+                              root_token=list(range(B)))
+    got, st = _gpu_tree(E, lp, B, V, k, depth, budgets, list(range(B)))
+    assert st == 0
+    for name in ("tree_off", "parent", "tokens", "p_row_of_node", "score"):
+        np.testing.assert_array_equal(got[name], ref[name], err_msg=name)
+    np.testing.assert_array_equal(got["node_depth"], ref["depth"])
+
+
+def test_expand_all_equal_rows():
+    # every log-prob equal: the order is decided by token index alone
+    E = cuda_ready()
+    B, V, k, depth = 1, 20000, 12, 3
+    R = 1 + (depth - 1) * k
+    lp = np.full((B * R, V), -np.log(V), dtype=np.float32)
+    ref = O.build_eagle2_tree(lp, B=B, k=k, depth=depth, budget=[100], root_token=[0])
+    got, st = _gpu_tree(E, lp, B, V, k, depth, [100], [0])
+    assert st == 0
+    for name in ("tree_off", "parent", "tokens", "p_row_of_node", "score"):
+        np.testing.assert_array_equal(got[name], ref[name], err_msg=name)
