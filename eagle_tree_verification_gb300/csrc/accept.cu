@@ -38,6 +38,7 @@ accept_greedy_kernel(int max_nodes, const int* __restrict__ tree_off,
                      const int* __restrict__ argmax, int max_depth,
                      int* __restrict__ accept_len, int* __restrict__ accepted_nodes,
                      int* __restrict__ out_tokens, int* status) {
+  pdl_begin();
   extern __shared__ int sm[];
   int* s_par = sm;
   int* s_tok = sm + max_nodes;
@@ -215,6 +216,7 @@ struct RoundSlot {
 template <int E>
 __global__ void __launch_bounds__(kStochThreads)
 accept_stochastic_kernel(const StochParams P) {
+  pdl_begin();
   cg::cluster_group cluster = cg::this_cluster();
   const unsigned rank = cluster.block_rank();
   const unsigned CS = cluster.num_blocks();
@@ -492,10 +494,10 @@ extern "C" eagle_status eagle_accept_greedy(int B, int max_nodes, const int32_t*
                        d_accepted_nodes && d_out_tokens && d_status,
                    EAGLE_ERR_INVALID_ARG);
   const size_t smem = (size_t)max_nodes * 2 * sizeof(int);
-  accept_greedy_kernel<<<B, 32, smem, (cudaStream_t)stream>>>(
-      max_nodes, d_tree_off, d_parent, d_tokens, d_argmax, max_depth, d_accept_len,
-      d_accepted_nodes, d_out_tokens, d_status);
-  return launch_status(cudaGetLastError());
+  return launch_status(launch_pdl(accept_greedy_kernel, dim3(B), dim3(32), smem,
+                                  (cudaStream_t)stream, max_nodes, d_tree_off, d_parent,
+                                  d_tokens, d_argmax, max_depth, d_accept_len, d_accepted_nodes,
+                                  d_out_tokens, d_status));
 }
 
 extern "C" eagle_status eagle_accept_stochastic(
@@ -554,12 +556,14 @@ extern "C" eagle_status eagle_accept_stochastic(
   cfg.blockDim = dim3(kStochThreads, 1, 1);
   cfg.dynamicSmemBytes = smem;
   cfg.stream = (cudaStream_t)stream;
-  cudaLaunchAttribute attr[1];
+  cudaLaunchAttribute attr[2];
   attr[0].id = cudaLaunchAttributeClusterDimension;
   attr[0].val.clusterDim.x = (unsigned)cs;
   attr[0].val.clusterDim.y = 1;
   attr[0].val.clusterDim.z = 1;
+  attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[1].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
-  cfg.numAttrs = 1;
+  cfg.numAttrs = 2;
   return launch_status(cudaLaunchKernelEx(&cfg, kern, P));
 }

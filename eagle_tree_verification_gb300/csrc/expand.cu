@@ -29,7 +29,7 @@ constexpr int kLvWarps = kLvThreads / 32;
 constexpr int kGroups = 32;            // half-warp groups per CTA (>= any k)
 constexpr int kCandCap = kLvThreads;   // chunk candidates held at once
 constexpr int kMaxVec = 4;             // float4 loads per thread
-constexpr int kMaxLevelCtas = 1216;    // 8 per SM before chunks grow
+constexpr int kOneWave = 304;          // two resident CTAs on each of 152 SMs
 constexpr int kRowCap = 128;           // row-merge candidates held at once
 constexpr int kMergeRegs = 8;          // chunk-list keys per lane kept in registers
 constexpr int kFinalThreads = 1024;
@@ -44,11 +44,13 @@ struct ChunkPlan {
   int S;    // chunks per row
 };
 
+// Smallest chunks that still fit the level in one wave of CTAs (more chunks
+// mean more lists to merge); the largest chunks when nothing fits.
 ChunkPlan chunk_plan(int rows, int V) {
   ChunkPlan p{1, 1};
   for (p.vec = 1;; p.vec *= 2) {
     p.S = ceil_div(V, (long long)kLvThreads * 4 * p.vec);
-    if (p.vec == kMaxVec || (long long)rows * p.S <= kMaxLevelCtas) break;
+    if (p.vec == kMaxVec || (long long)rows * p.S <= kOneWave) break;
   }
   return p;
 }
@@ -158,18 +160,22 @@ __device__ void warp_row_topk(const unsigned long long* src, int n, int k,
                               unsigned long long* lane_max, unsigned long long* cand,
                               unsigned long long* out, int* status) {
   const int lane = threadIdx.x & 31;
-  const bool cached = n <= 32 * kMergeRegs;
+  // keys in tiles of 32 x kMergeRegs, loads of a tile in flight together;
+  // a single tile stays in registers for the second pass
+  const int ntiles = (n + 32 * kMergeRegs - 1) / (32 * kMergeRegs);
   unsigned long long reg[kMergeRegs];
-  unsigned long long lmax = 0;
-  if (cached) {
+  auto load_tile = [&](int tile) {
 #pragma unroll
     for (int r = 0; r < kMergeRegs; ++r) {
-      const int i = r * 32 + lane;
+      const int i = (tile * kMergeRegs + r) * 32 + lane;
       reg[r] = (i < n) ? __ldcg(src + i) : 0ull;
-      lmax = umax64(lmax, reg[r]);
     }
-  } else {
-    for (int i = lane; i < n; i += 32) lmax = umax64(lmax, __ldcg(src + i));
+  };
+  unsigned long long lmax = 0;
+  for (int tile = 0; tile < ntiles; ++tile) {
+    load_tile(tile);
+#pragma unroll
+    for (int r = 0; r < kMergeRegs; ++r) lmax = umax64(lmax, reg[r]);
   }
   // lower bound of the k-th largest: the k-th largest lane maximum
   lane_max[lane] = lmax;
@@ -188,11 +194,10 @@ __device__ void warp_row_topk(const unsigned long long* src, int n, int k,
       if (pred && pos < kRowCap) cand[pos] = key;
       cnt += __popc(bal);
     };
-    if (cached) {
+    for (int tile = 0; tile < ntiles; ++tile) {
+      if (ntiles > 1) load_tile(tile);
 #pragma unroll
       for (int r = 0; r < kMergeRegs; ++r) offer(reg[r]);
-    } else {
-      for (int i0 = 0; i0 < n; i0 += 32) offer(i0 + lane < n ? __ldcg(src + i0 + lane) : 0ull);
     }
     __syncwarp();
     if (cnt <= kRowCap) break;
@@ -225,6 +230,7 @@ __device__ void warp_row_topk(const unsigned long long* src, int n, int k,
   for (int t = lane; t < cnt; t += 32) {
     const unsigned long long me = cand[t];
     int r = 0;
+#pragma unroll 8
     for (int j = 0; j < cnt; ++j) r += (cand[j] > me);
     if (r < k) out[r] = me;
   }
@@ -236,8 +242,10 @@ __device__ void warp_row_topk(const unsigned long long* src, int n, int k,
 // The sequence's last CTA: per-row top-k, children, next frontier.
 template <int VEC>
 __global__ void __launch_bounds__(kLvThreads, 2) expand_level_kernel(const LevelParams A) {
+  pdl_begin();
   __shared__ unsigned long long s_grp[kGroups];
   __shared__ unsigned long long s_cand[kCandCap];
+  __shared__ unsigned long long s_top[EAGLE_MAX_TOPK];
   __shared__ unsigned long long s_tau;
   __shared__ int s_cnt, s_last;
   __shared__ MergeShared M;
@@ -283,17 +291,15 @@ __global__ void __launch_bounds__(kLvThreads, 2) expand_level_kernel(const Level
   if ((lane & 15) == 0) s_grp[warp * 2 + (lane >> 4)] = tmax;
   if (tid == 0) s_cnt = 0;
   if (__syncthreads_or(bad) && tid == 0) fail(A.status, EAGLE_ERR_NUMERIC);
-  if (warp == 0) {
-    // the k-th largest group maximum: k distinct keys of the chunk reach it
+  // every warp: the k-th largest group maximum (k distinct keys reach it)
+  unsigned long long tau;
+  {
     const unsigned long long g = s_grp[lane];
     int rank = 0;
 #pragma unroll 8
     for (int i = 0; i < kGroups; ++i) rank += (s_grp[i] > g);
-    const unsigned long long t = pick_lane(__ballot_sync(0xffffffffu, rank == k - 1), g, 1ull);
-    if (lane == 0) s_tau = t;
+    tau = pick_lane(__ballot_sync(0xffffffffu, rank == k - 1), g, 1ull);
   }
-  __syncthreads();
-  unsigned long long tau = s_tau;
   int cnt;
   for (int round = 0;; ++round) {
 #pragma unroll
@@ -324,6 +330,7 @@ __global__ void __launch_bounds__(kLvThreads, 2) expand_level_kernel(const Level
     // (each round drops at least kCandCap - k keys)
     const unsigned long long me = s_cand[tid];
     int rank = 0;
+#pragma unroll 8
     for (int i = 0; i < kCandCap; ++i) rank += (s_cand[i] > me);
     __syncthreads();
     if (rank == k - 1) s_tau = me;
@@ -331,25 +338,30 @@ __global__ void __launch_bounds__(kLvThreads, 2) expand_level_kernel(const Level
     __syncthreads();
     tau = s_tau;
   }
-  unsigned long long* part = A.pool.partial + ((size_t)row * A.S + chunk) * k;
   if (tid < cnt) {
     const unsigned long long me = s_cand[tid];
     int rank = 0;
+#pragma unroll 8
     for (int i = 0; i < cnt; ++i) rank += (s_cand[i] > me);
-    if (rank < k) part[rank] = me;
+    if (rank < k) s_top[rank] = me;
   } else if (tid < k) {
-    part[tid] = 0ull;  // fewer than k tokens in this chunk
+    s_top[tid] = 0ull;  // fewer than k tokens in this chunk
   }
-  // ---- the sequence's last CTA merges
-  __threadfence();
   __syncthreads();
-  if (tid == 0) {
-    const int t = atomicAdd(&A.pool.ticket[b], 1);
-    s_last = (t == A.F * A.S - 1);
+  // ---- publish the chunk list; the sequence's last CTA merges
+  if (warp == 0) {
+    unsigned long long* part = A.pool.partial + ((size_t)row * A.S + chunk) * k;
+    if (lane < k) part[lane] = s_top[lane];
+    __threadfence();
+    __syncwarp();
+    if (lane == 0) {
+      const int t = atomicAdd(&A.pool.ticket[b], 1);
+      __threadfence();
+      s_last = (t == A.F * A.S - 1);
+    }
   }
   __syncthreads();
   if (!s_last) return;
-  __threadfence();
   const int F = A.F;
   int* front = A.pool.frontier + (size_t)b * k;
   float* fsc = A.pool.fscore + (size_t)b * k;
@@ -390,13 +402,19 @@ __global__ void __launch_bounds__(kLvThreads, 2) expand_level_kernel(const Level
     M.child[c] = desc_key(sc, (uint32_t)c);
   }
   __syncthreads();
-  // next frontier: rank of every child by (score desc, creation order)
-  for (int c = tid; c < nc; c += kLvThreads) {
-    const unsigned long long me = M.child[c];
+  // next frontier: rank of every child by (score desc, creation order);
+  // gs lanes share one child's count
+  int gs = 1;
+  while (gs < 32 && 2 * gs * nc <= kLvThreads) gs *= 2;
+  const int sub = lane & (gs - 1);
+  for (int c0 = 0; c0 < nc; c0 += kLvThreads / gs) {
+    const int c = c0 + tid / gs;
+    const unsigned long long me = (c < nc) ? M.child[c] : ~0ull;
     int rank = 0;
-#pragma unroll 8
-    for (int j = 0; j < nc; ++j) rank += (M.child[j] > me);
-    if (rank < k) {
+#pragma unroll 4
+    for (int j = sub; j < nc; j += gs) rank += (M.child[j] > me);
+    for (int o = gs >> 1; o > 0; o >>= 1) rank += __shfl_xor_sync(0xffffffffu, rank, o);
+    if (c < nc && sub == 0 && rank < k) {
       front[rank] = base + c;
       fsc[rank] = key_value(me);
     }
@@ -423,6 +441,7 @@ struct FinalParams {
 // number the kept nodes by (depth, score desc, creation order) and write the
 // tree.
 __global__ void __launch_bounds__(kFinalThreads) expand_finalize_kernel(const FinalParams A) {
+  pdl_begin();
   extern __shared__ __align__(16) unsigned char smem_raw[];
   unsigned long long* s_key = reinterpret_cast<unsigned long long*>(smem_raw);  // [P]
   int* s_dep = reinterpret_cast<int*>(s_key + A.P);                             // [P]
@@ -462,9 +481,12 @@ __global__ void __launch_bounds__(kFinalThreads) expand_finalize_kernel(const Fi
     for (int shift = 56; shift >= 0; shift -= 8) {
       if (tid < 256) s_hist[tid] = 0;
       __syncthreads();
-      for (int i = tid; i < n; i += blockDim.x) {
-        const unsigned long long key = s_key[i];
-        if ((key & mask) == prefix) atomicAdd(&s_hist[(int)(key >> shift) & 255], 1);
+      for (int i0 = 0; i0 < n; i0 += blockDim.x) {   // uniform trip count
+        const int i = i0 + tid;
+        const unsigned long long key = (i < n) ? s_key[i] : 0ull;
+        const int bin = (i < n && (key & mask) == prefix) ? (int)(key >> shift) & 255 : 256;
+        const unsigned peers = __match_any_sync(0xffffffffu, bin);
+        if (bin < 256 && lane == __ffs(peers) - 1) atomicAdd(&s_hist[bin], __popc(peers));
       }
       __syncthreads();
       if (warp == 0) {
@@ -506,18 +528,25 @@ __global__ void __launch_bounds__(kFinalThreads) expand_finalize_kernel(const Fi
   __syncthreads();
   const int ns = s_nsel;
   const int off = s_off;
-  // node number of every kept entry: 1 + rank by (depth, score desc, creation)
-  for (int a = tid; a < ns; a += blockDim.x) {
-    const int ia = s_list[a];
-    const int da = s_dep[ia];
-    const unsigned long long ka = s_key[ia];
+  // node number of every kept entry: 1 + rank by (depth, score desc,
+  // creation); gs lanes share one entry's count
+  int gs = 1;
+  while (gs < 32 && 2 * gs * ns <= kFinalThreads) gs *= 2;
+  const int sub = lane & (gs - 1);
+  for (int a0 = 0; a0 < ns; a0 += kFinalThreads / gs) {
+    const int a = a0 + tid / gs;
+    const int ia = (a < ns) ? s_list[a] : 0;
+    const int da = (a < ns) ? s_dep[ia] : 0;
+    const unsigned long long ka = (a < ns) ? s_key[ia] : 0ull;
     int rank = 0;
-    for (int c = 0; c < ns; ++c) {
+#pragma unroll 4
+    for (int c = sub; c < ns; c += gs) {
       const int ic = s_list[c];
       const int dc = s_dep[ic];
       rank += (dc < da) || (dc == da && s_key[ic] > ka);
     }
-    s_node[ia] = 1 + rank;
+    for (int o = gs >> 1; o > 0; o >>= 1) rank += __shfl_xor_sync(0xffffffffu, rank, o);
+    if (a < ns && sub == 0) s_node[ia] = 1 + rank;
   }
   __syncthreads();
   const int* tok = A.pool.token + (size_t)b * A.P;
@@ -596,13 +625,11 @@ extern "C" eagle_status eagle_draft_expand(int B, int V, int k, int depth, int l
     A.logp = d_draft_logp;
     A.pool = pp;
     A.status = d_status;
-    const int grid = B * A.F * A.S;
-    switch (cp.vec) {
-      case 1: expand_level_kernel<1><<<grid, kLvThreads, 0, s>>>(A); break;
-      case 2: expand_level_kernel<2><<<grid, kLvThreads, 0, s>>>(A); break;
-      default: expand_level_kernel<4><<<grid, kLvThreads, 0, s>>>(A); break;
-    }
-    return launch_status(cudaGetLastError());
+    const dim3 grid(B * A.F * A.S);
+    void (*kern)(const LevelParams) = (cp.vec == 1)   ? expand_level_kernel<1>
+                                      : (cp.vec == 2) ? expand_level_kernel<2>
+                                                      : expand_level_kernel<4>;
+    return launch_status(launch_pdl(kern, grid, dim3(kLvThreads), 0, s, A));
   }
   EAGLE_HOST_CHECK(d_budget && d_tree_off && d_parent && d_tokens && d_node_depth && d_score &&
                        d_p_row_of_node,
@@ -628,6 +655,6 @@ extern "C" eagle_status eagle_draft_expand(int B, int V, int k, int depth, int l
     cudaFuncSetAttribute(expand_finalize_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                          (int)smem);
   }
-  expand_finalize_kernel<<<B, kFinalThreads, smem, s>>>(F);
-  return launch_status(cudaGetLastError());
+  return launch_status(launch_pdl(expand_finalize_kernel, dim3(B), dim3(kFinalThreads), smem, s,
+                                  F));
 }

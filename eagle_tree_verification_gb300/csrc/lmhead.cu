@@ -50,6 +50,7 @@ __global__ void __launch_bounds__(kTileThreads)
 lmhead_tile_kernel(int T, int H, int V, float temperature, const TIn* __restrict__ h,
                    const TIn* __restrict__ w, float* __restrict__ z_out,
                    Partial* __restrict__ part, int n_vtiles, int* status) {
+  pdl_begin();
   __shared__ float Ws[kKC][kVT + 1];
   __shared__ float Hs[kKC][kRT + 1];
   __shared__ float Zs[kRT][kVT + 1];
@@ -131,6 +132,7 @@ __global__ void __launch_bounds__(kFinThreads)
 lmhead_finalize_kernel(int T, int V, float temperature, const Partial* __restrict__ part,
                        int n_vtiles, int32_t* argmax, float* row_max, float* row_lse,
                        float* top2_gap, float* q) {
+  pdl_begin();
   __shared__ float s_f[32];
   __shared__ int s_i[32];
   __shared__ float s_m, s_lse;
@@ -269,6 +271,7 @@ lmhead_tc_kernel(const __grid_constant__ CUtensorMap map_h, const __grid_constan
                  int T, int H, int V, float temperature, float* __restrict__ z_out,
                  Partial* __restrict__ part, int n_units, int h_stage_bytes, int w_stages,
                  int* status) {
+  pdl_begin();
   extern __shared__ __align__(1024) unsigned char smem_raw[];
   unsigned char* base = reinterpret_cast<unsigned char*>(
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~(uintptr_t)1023);
@@ -580,33 +583,33 @@ extern "C" eagle_status eagle_lmhead_softmax(eagle_dtype dtype, int T, int H, in
       const __nv_bfloat16* hs = static_cast<const __nv_bfloat16*>(d_h) + (size_t)r0 * H;
       CUtensorMap map_h;
       if (!make_map_bf16(&map_h, hs, Ts, H, TL.t_pad)) return EAGLE_ERR_CUDA;
-      lmhead_tc_kernel<<<grid, kTcThreads, TL.smem, s>>>(
-          map_h, map_w, Ts, H, V, temperature, z ? z + (size_t)r0 * V : nullptr,
-          part + (size_t)r0 * grid, n_units, TL.h_stage_bytes, TL.w_stages, d_status);
-      if (cudaGetLastError() != cudaSuccess) return EAGLE_ERR_CUDA;
+      if (launch_pdl(lmhead_tc_kernel, dim3(grid), dim3(kTcThreads), TL.smem, s, map_h, map_w,
+                     Ts, H, V, temperature, z ? z + (size_t)r0 * V : nullptr,
+                     part + (size_t)r0 * grid, n_units, TL.h_stage_bytes, TL.w_stages,
+                     d_status) != cudaSuccess)
+        return EAGLE_ERR_CUDA;
     }
     dim3 fgrid(T, z ? (V + kFinChunk - 1) / kFinChunk : 1);
-    lmhead_finalize_kernel<<<fgrid, kFinThreads, 0, s>>>(T, V, temperature, part, grid, d_argmax,
-                                                         d_row_max, d_row_lse, d_top2_gap, z);
-    return launch_status(cudaGetLastError());
+    return launch_status(launch_pdl(lmhead_finalize_kernel, fgrid, dim3(kFinThreads), 0, s, T, V,
+                                    temperature, (const Partial*)part, grid, d_argmax, d_row_max,
+                                    d_row_lse, d_top2_gap, z));
   }
   const int n_vtiles = (V + kVT - 1) / kVT;
   dim3 grid(n_vtiles, (T + kRT - 1) / kRT);
+  cudaError_t e;
   if (dtype == EAGLE_BF16)
-    lmhead_tile_kernel<__nv_bfloat16><<<grid, kTileThreads, 0, s>>>(
-        T, H, V, temperature, static_cast<const __nv_bfloat16*>(d_h),
-        static_cast<const __nv_bfloat16*>(d_w), z, part, n_vtiles, d_status);
+    e = launch_pdl(lmhead_tile_kernel<__nv_bfloat16>, grid, dim3(kTileThreads), 0, s, T, H, V,
+                   temperature, static_cast<const __nv_bfloat16*>(d_h),
+                   static_cast<const __nv_bfloat16*>(d_w), z, part, n_vtiles, d_status);
   else
-    lmhead_tile_kernel<float><<<grid, kTileThreads, 0, s>>>(
-        T, H, V, temperature, static_cast<const float*>(d_h), static_cast<const float*>(d_w), z,
-        part, n_vtiles, d_status);
-  cudaError_t e = cudaGetLastError();
+    e = launch_pdl(lmhead_tile_kernel<float>, grid, dim3(kTileThreads), 0, s, T, H, V,
+                   temperature, static_cast<const float*>(d_h), static_cast<const float*>(d_w), z,
+                   part, n_vtiles, d_status);
   if (e != cudaSuccess) return EAGLE_ERR_CUDA;
   dim3 fgrid(T, z ? (V + kFinChunk - 1) / kFinChunk : 1);
-  lmhead_finalize_kernel<<<fgrid, kFinThreads, 0, s>>>(T, V, temperature, part, n_vtiles,
-                                                       d_argmax, d_row_max, d_row_lse,
-                                                       d_top2_gap, z);
-  return launch_status(cudaGetLastError());
+  return launch_status(launch_pdl(lmhead_finalize_kernel, fgrid, dim3(kFinThreads), 0, s, T, V,
+                                  temperature, (const Partial*)part, n_vtiles, d_argmax,
+                                  d_row_max, d_row_lse, d_top2_gap, z));
 }
 
 // ---------------------------------------------------------------------------

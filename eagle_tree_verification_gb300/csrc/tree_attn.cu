@@ -44,6 +44,7 @@ tree_attn_warp_kernel(int B, int T, int Hq, int Hkv, float scale, int max_nodes,
                       const TIn* __restrict__ v_cache, const int* __restrict__ kv_off,
                       const int* __restrict__ tree_off, const int* __restrict__ parent,
                       float* __restrict__ out, int* status) {
+  pdl_begin();
   constexpr int PER = D / 32;
   const int warp = blockIdx.x * kWarpsPerBlock + (threadIdx.x >> 5);
   const int lane = threadIdx.x & 31;
@@ -121,15 +122,10 @@ eagle_status launch_warp(int D, int B, int T, int Hq, int Hkv, float scale, int 
   const TIn* VT = static_cast<const TIn*>(vt);
   const TIn* KC = static_cast<const TIn*>(kc);
   const TIn* VC = static_cast<const TIn*>(vc);
-  if (D == 64)
-    tree_attn_warp_kernel<TIn, 64><<<grid, kWarpsPerBlock * 32, 0, s>>>(
-        B, T, Hq, Hkv, scale, max_nodes, max_kv, Q, KT, VT, KC, VC, kv_off, tree_off, parent, out,
-        status);
-  else
-    tree_attn_warp_kernel<TIn, 128><<<grid, kWarpsPerBlock * 32, 0, s>>>(
-        B, T, Hq, Hkv, scale, max_nodes, max_kv, Q, KT, VT, KC, VC, kv_off, tree_off, parent, out,
-        status);
-  return launch_status(cudaGetLastError());
+  auto kern = (D == 64) ? tree_attn_warp_kernel<TIn, 64> : tree_attn_warp_kernel<TIn, 128>;
+  return launch_status(launch_pdl(kern, dim3(grid), dim3(kWarpsPerBlock * 32), 0, s, B, T, Hq,
+                                  Hkv, scale, max_nodes, max_kv, Q, KT, VT, KC, VC, kv_off,
+                                  tree_off, parent, out, status));
 }
 
 // ---------------------------------------------------------------------------
@@ -246,6 +242,7 @@ tree_attn_tc_kernel(const __grid_constant__ CUtensorMap map_q,
                     const __grid_constant__ CUtensorMap map_vc,
                     const __grid_constant__ CUtensorMap map_kt,
                     const __grid_constant__ CUtensorMap map_vt, const AttParams A) {
+  pdl_begin();
   extern __shared__ __align__(1024) unsigned char smem_raw[];
   unsigned char* base = reinterpret_cast<unsigned char*>(
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~(uintptr_t)1023);
@@ -779,8 +776,8 @@ extern "C" eagle_status eagle_tree_attn(eagle_dtype dtype, int B, int T, int Hq,
     if (cudaMemsetAsync(ws, 0, (size_t)B * Hkv * P.MT * sizeof(int), s) != cudaSuccess)
       return EAGLE_ERR_CUDA;
     const int grid = B * Hkv * P.NC * P.MT;
-    tree_attn_tc_kernel<<<grid, kAttThreads, kAttSmem, s>>>(mq, mkc, mvc, mkt, mvt, A);
-    return launch_status(cudaGetLastError());
+    return launch_status(launch_pdl(tree_attn_tc_kernel, dim3(grid), dim3(kAttThreads), kAttSmem,
+                                    s, mq, mkc, mvc, mkt, mvt, A));
   }
   if (dtype == EAGLE_BF16)
     return launch_warp<__nv_bfloat16>(D, B, T, Hq, Hkv, scale, max_nodes, max_kv, d_q, d_k_tree,
