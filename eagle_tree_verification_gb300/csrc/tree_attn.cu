@@ -25,12 +25,14 @@
 
 #include <algorithm>
 
+#include <cooperative_groups.h>
 #include <cudaTypedefs.h>
 
 #include "common.cuh"
 #include "tc.cuh"
 
 using namespace eagle;
+namespace cg = cooperative_groups;
 
 namespace {
 
@@ -137,42 +139,40 @@ constexpr int kKeyBlk = 128;            // keys per block (the S MMA's N)
 constexpr int kHalfBytes = 128 * 128;   // 128 rows x 64 bf16 (one swizzle atom wide)
 constexpr int kTileBytes = 2 * kHalfBytes;  // 128 rows x 128 bf16
 constexpr int kTargetCtas = 152;        // SMs of a GB300
-constexpr size_t kAttSmem = 1024 + 7 * (size_t)kTileBytes + 1280;
+constexpr int kMaxSplit = 8;            // cache chunks of one tile: one portable cluster
+constexpr size_t kAttSharedBytes = 5120;
+// Q, two K stages, two V stages; the merge reuses the K stages for O rows
+constexpr size_t kAttSmem = 1024 + 5 * (size_t)kTileBytes + kAttSharedBytes;
 
 struct AttShared {
   uint64_t q_full;
   uint64_t k_full[2], k_empty[2], v_full[2], v_empty[2];
-  uint64_t s_full[2], s_empty[2];
-  uint64_t p_full, p_free, o_done, drain;
-  uint64_t xbar, fbar, tbar0, tbar1;   // row-thread exchanges and the merge ticket
+  uint64_t s_full[2], p_full[2];   // per TMEM slot: S ready / P written
+  uint64_t pv_done, o_done, drain;
+  uint64_t xbar, fbar;             // row-half exchanges
   uint32_t tmem_base;
   int abort_flag;
-  int is_last;
-  float xchg[2][128];   // per-row values exchanged between the two column halves
+  float xchg[2][2][128];           // [block parity][half][row]
+  float2 ml[128];                  // (m, l) of every row, read by the cluster
+  int par[EAGLE_MAX_TREE_NODES];   // parent[] of the sequence
 };
 
-static_assert(sizeof(AttShared) <= 1280, "AttShared must fit its shared-memory slot");
+static_assert(sizeof(AttShared) <= kAttSharedBytes, "AttShared must fit its shared-memory slot");
 
 struct AttPlan {
   int G, MT, NC, CK;  // heads per kv head, row tiles, cache chunks, keys per chunk
-  size_t off_ml, off_o, total;
 };
 
 AttPlan att_plan(int B, int Hq, int Hkv, int max_nodes, int max_kv) {
   AttPlan P;
   P.G = Hq / Hkv;
   P.MT = (max_nodes * P.G + 127) / 128;
-  const int per_chunk_items = std::max(1, B * Hkv * P.MT);
-  int nc = std::max(1, kTargetCtas / per_chunk_items);
+  const int tiles = std::max(1, B * Hkv * P.MT);
+  const int nc = std::min(kMaxSplit, std::max(1, kTargetCtas / tiles));
   int ck = (max_kv + nc - 1) / nc;
   ck = std::max(256, ((ck + kKeyBlk - 1) / kKeyBlk) * kKeyBlk);
   P.CK = ck;
   P.NC = std::max(1, (max_kv + ck - 1) / ck);
-  const size_t tiles = (size_t)B * Hkv * P.MT;
-  const size_t items = tiles * P.NC;
-  P.off_ml = ((tiles * 4) + 255) & ~(size_t)255;
-  P.off_o = P.off_ml + ((items * 128 * 8 + 255) & ~(size_t)255);
-  P.total = P.off_o + items * 128 * 128 * 4;
   return P;
 }
 
@@ -183,21 +183,9 @@ struct AttParams {
   const int* tree_off;
   const int* parent;
   float* out;
-  int* counters;       // [B*Hkv*MT]
-  float2* part_ml;     // [items][128] (m, l)
-  float* part_o;       // [items][128][128]
   int* status;
 };
 
-__device__ __forceinline__ void st_shared_v4(uint32_t addr, uint32_t a, uint32_t b, uint32_t c,
-                                             uint32_t d) {
-  asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(addr), "r"(a), "r"(b), "r"(c),
-               "r"(d)
-               : "memory");
-}
-__device__ __forceinline__ void fence_proxy_async_smem() {
-  asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
-}
 __device__ __forceinline__ uint32_t pack_bf16(float a, float b) {
   __nv_bfloat162 v = __floats2bfloat162_rn(a, b);
   return *reinterpret_cast<uint32_t*>(&v);
@@ -216,6 +204,27 @@ __device__ __forceinline__ uint64_t desc_mnmajor_sw128(uint32_t smem_addr, uint3
   return d;
 }
 
+// D[tmem] (+)= A[tmem] * B[smem]: A (M x K, K-major, two 16-bit elements per
+// 32-bit column) is read from tensor memory.
+__device__ __forceinline__ void mma_f16_tmem_a(uint32_t d_tmem, uint32_t a_tmem, uint64_t b_desc,
+                                               uint32_t idesc, uint32_t accumulate) {
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "setp.ne.b32 p, %4, 0;\n\t"
+      "tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n\t}" ::"r"(d_tmem),
+      "r"(a_tmem), "l"(b_desc), "r"(idesc), "r"(accumulate)
+      : "memory");
+}
+
+__device__ __forceinline__ void tmem_st_32x32b_x16(uint32_t taddr, const uint32_t (&v)[16]) {
+  asm volatile(
+      "tcgen05.st.sync.aligned.32x32b.x16.b32 [%0], "
+      "{%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,%16};" ::"r"(taddr),
+      "r"(v[0]), "r"(v[1]), "r"(v[2]), "r"(v[3]), "r"(v[4]), "r"(v[5]), "r"(v[6]), "r"(v[7]),
+      "r"(v[8]), "r"(v[9]), "r"(v[10]), "r"(v[11]), "r"(v[12]), "r"(v[13]), "r"(v[14]),
+      "r"(v[15])
+      : "memory");
+}
 __device__ __forceinline__ void tmem_st_32x32b_x32(uint32_t taddr, const float (&v)[32]) {
   asm volatile(
       "tcgen05.st.sync.aligned.32x32b.x32.b32 [%0], "
@@ -233,9 +242,15 @@ __device__ __forceinline__ void tmem_st_32x32b_x32(uint32_t taddr, const float (
       "r"(__float_as_uint(v[27])), "r"(__float_as_uint(v[28])), "r"(__float_as_uint(v[29])),
       "r"(__float_as_uint(v[30])), "r"(__float_as_uint(v[31]))
       : "memory");
+}
+__device__ __forceinline__ void tmem_wait_st() {
   asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
 }
 
+// One CTA per (sequence, kv head, 128-row tile, cache chunk); the chunks of
+// a tile form a thread-block cluster and merge their partial softmax rows
+// through distributed shared memory.  TMEM: S slots at columns 0 / 128 (P,
+// as bf16 hi | lo halves, overwrites its S slot), O at column 256.
 __global__ void __launch_bounds__(kAttThreads, 1)
 tree_attn_tc_kernel(const __grid_constant__ CUtensorMap map_q,
                     const __grid_constant__ CUtensorMap map_kc,
@@ -249,43 +264,43 @@ tree_attn_tc_kernel(const __grid_constant__ CUtensorMap map_q,
   unsigned char* q_sm = base;                       // [2 halves][128 rows][128 B]
   unsigned char* k_sm = base + kTileBytes;          // 2 stages
   unsigned char* v_sm = base + 3 * kTileBytes;      // 2 stages
-  unsigned char* p_sm = base + 5 * kTileBytes;      // P, high bf16 part
-  unsigned char* pl_sm = base + 6 * kTileBytes;     // P, low bf16 part
-  AttShared* sh = reinterpret_cast<AttShared*>(base + 7 * kTileBytes);
+  AttShared* sh = reinterpret_cast<AttShared*>(base + 5 * kTileBytes);
+  float4* obuf = reinterpret_cast<float4*>(k_sm);   // merge: [128 rows][32 float4], swizzled
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  // work item: ((b * Hkv + g) * NC + c) * MT + mt  (row tiles of one chunk adjacent)
-  int item = blockIdx.x;
-  const int mt = item % A.MT;
-  item /= A.MT;
-  const int c = item % A.NC;
-  item /= A.NC;
-  const int g = item % A.Hkv;
-  const int b = item / A.Hkv;
-  const int tile_id = (b * A.Hkv + g) * A.MT + mt;
-  const int item_id = tile_id * A.NC + c;
+  // work item: tile * NC + c, the cache chunks of a tile adjacent (one cluster)
+  const int c = blockIdx.x % A.NC;
+  int tile = blockIdx.x / A.NC;
+  const int mt = tile % A.MT;
+  const int g = (tile / A.MT) % A.Hkv;
+  const int b = tile / (A.MT * A.Hkv);
 
   const int t0 = A.tree_off[b];
   const int n = A.tree_off[b + 1] - t0;
   const int kv0 = A.kv_off[b];
   const int L = A.kv_off[b + 1] - kv0;
   const bool bad_seq = (n < 1 || n > A.max_nodes || L < 0 || L > A.max_kv);
-  // chunks that carry cache keys of this sequence; the last one also takes
-  // the tree keys
-  const int n_chunks = bad_seq ? 1 : max(1, (L + A.CK - 1) / A.CK);
   const int nodes_per_tile = 128 / A.G;
-  const bool tile_used = !bad_seq && mt * nodes_per_tile < n;
-  if (c >= n_chunks || !tile_used) {
+  // the whole cluster (same tile) leaves together
+  if (bad_seq || mt * nodes_per_tile >= n) {
     if (bad_seq && c == 0 && mt == 0 && threadIdx.x == 0) fail(A.status, EAGLE_ERR_INVALID_TREE);
     return;
   }
+  // chunks that carry cache keys of this sequence; the last one also takes
+  // the tree keys
+  const int n_chunks = max(1, (L + A.CK - 1) / A.CK);
   const int key_begin = c * A.CK;
   const int key_end = min(L, key_begin + A.CK);
-  const int n_cache_blk = (key_end - key_begin + kKeyBlk - 1) / kKeyBlk;
+  const int n_cache_blk = (key_end > key_begin) ? (key_end - key_begin + kKeyBlk - 1) / kKeyBlk : 0;
   const bool with_tree = (c == n_chunks - 1);
   const int n_tree_blk = with_tree ? (n + kKeyBlk - 1) / kKeyBlk : 0;
   const int nblk = n_cache_blk + n_tree_blk;
+  // row quads (32 rows) holding at least one node of the tile
+  int active_quads = 0;
+  for (int q = 0; q < 4; ++q) active_quads += ((mt * 128 + q * 32) / A.G < n);
+  const int active_warps = 2 * active_quads;
 
+  for (int i = threadIdx.x; i < n; i += kAttThreads) sh->par[i] = A.parent[t0 + i];
   if (threadIdx.x == 0) {
     tc::mbar_init(&sh->q_full, 1);
     for (int i = 0; i < 2; ++i) {
@@ -294,16 +309,13 @@ tree_attn_tc_kernel(const __grid_constant__ CUtensorMap map_q,
       tc::mbar_init(&sh->v_full[i], 1);
       tc::mbar_init(&sh->v_empty[i], 1);
       tc::mbar_init(&sh->s_full[i], 1);
-      tc::mbar_init(&sh->s_empty[i], 8);
+      tc::mbar_init(&sh->p_full[i], active_warps);
     }
-    tc::mbar_init(&sh->p_full, 8);
-    tc::mbar_init(&sh->p_free, 1);
+    tc::mbar_init(&sh->pv_done, 1);
     tc::mbar_init(&sh->o_done, 1);
     tc::mbar_init(&sh->drain, 1);
-    tc::mbar_init(&sh->xbar, 256);
-    tc::mbar_init(&sh->fbar, 256);
-    tc::mbar_init(&sh->tbar0, 256);
-    tc::mbar_init(&sh->tbar1, 1);
+    tc::mbar_init(&sh->xbar, 32 * active_warps);
+    tc::mbar_init(&sh->fbar, 32 * active_warps);
     sh->abort_flag = 0;
     tc::fence_barrier_init();
   }
@@ -314,25 +326,36 @@ tree_attn_tc_kernel(const __grid_constant__ CUtensorMap map_q,
   tc::fence_before_thread_sync();
   __syncthreads();
   tc::fence_after_thread_sync();
-  const uint32_t tmem = sh->tmem_base;     // S[0] at +0, S[1] at +128, O at +256
+  const uint32_t tmem = sh->tmem_base;
   volatile int* abort_flag = &sh->abort_flag;
   int* status = A.status;
 
+  // row-thread state carried into the merge
+  const int quad = warp & 3;
+  const int half = (warp - 2) >> 2;
+  const int r = quad * 32 + lane;                   // row in the tile
+  const bool row_warp = warp >= 2 && quad < active_quads;
+  float o0[32], o1[32];
+  float m = -INFINITY, l_row = 0.f;
+  bool ok = true;
+#pragma unroll
+  for (int i = 0; i < 32; ++i) o0[i] = o1[i] = 0.f;
+
   if (warp == 0) {
     // ------------------------------------------------------------ TMA
-    if (lane == 0) {
-      bool ok = true;
+    if (lane == 0 && nblk > 0) {
+      bool tok = true;
       tc::mbar_arrive_expect_tx(&sh->q_full, kTileBytes);
       const int node0 = t0 + mt * nodes_per_tile;
       tc::tma_load_3d(q_sm, &map_q, &sh->q_full, 0, g * A.G, node0);
       tc::tma_load_3d(q_sm + kHalfBytes, &map_q, &sh->q_full, 64, g * A.G, node0);
       uint32_t eph = 0;   // bit st: phase parity of stage st's empty barriers
       int issued = 0;
-      for (int j = 0; j < nblk && ok; ++j) {
+      for (int j = 0; j < nblk && tok; ++j) {
         const int st = j & 1;
         if (j >= 2) {
-          if (!(ok = tc::mbar_wait(&sh->k_empty[st], (eph >> st) & 1u, abort_flag, status))) break;
-          if (!(ok = tc::mbar_wait(&sh->v_empty[st], (eph >> st) & 1u, abort_flag, status))) break;
+          if (!(tok = tc::mbar_wait(&sh->k_empty[st], (eph >> st) & 1u, abort_flag, status))) break;
+          if (!(tok = tc::mbar_wait(&sh->v_empty[st], (eph >> st) & 1u, abort_flag, status))) break;
           eph ^= 1u << st;
         }
         const CUtensorMap* mk = (j < n_cache_blk) ? &map_kc : &map_kt;
@@ -349,7 +372,7 @@ tree_attn_tc_kernel(const __grid_constant__ CUtensorMap map_q,
         tc::tma_load_3d(vd + kHalfBytes, mv, &sh->v_full[st], 64, g, row);
         ++issued;
       }
-      if (!ok) {
+      if (!tok) {
         // let the copies in flight (at most the last two blocks) land
         int never = 0;
         tc::mbar_wait(&sh->q_full, 0, &never, nullptr, 200000000ll);
@@ -362,77 +385,73 @@ tree_attn_tc_kernel(const __grid_constant__ CUtensorMap map_q,
   } else if (warp == 1) {
     // ------------------------------------------------------------ MMA
     if (lane == 0) {
-      const uint32_t idesc_s = tc::idesc_bf16_f32(128, kKeyBlk);
-      const uint32_t idesc_o = tc::idesc_bf16_f32(128, 128) | (1u << 16);  // B is MN-major
-      const uint32_t q_addr = tc::smem_u32(q_sm);
-      const uint32_t p_addr = tc::smem_u32(p_sm);
-      const uint32_t pl_addr = tc::smem_u32(pl_sm);
-      bool ok = tc::mbar_wait(&sh->q_full, 0, abort_flag, status);
-      uint32_t kph = 0, vph = 0, seph = 0;   // bit st: phase parity per stage
-      uint32_t pph = 0;
-      auto issue_s = [&](int j) -> bool {
-        const int st = j & 1;
-        if (j >= 2) {
-          if (!tc::mbar_wait(&sh->s_empty[st], (seph >> st) & 1u, abort_flag, status)) return false;
-          seph ^= 1u << st;
-        }
-        if (!tc::mbar_wait(&sh->k_full[st], (kph >> st) & 1u, abort_flag, status)) return false;
-        kph ^= 1u << st;
-        tc::fence_after_thread_sync();
-        const uint32_t k_addr = tc::smem_u32(k_sm + st * kTileBytes);
-#pragma unroll
-        for (int k16 = 0; k16 < 8; ++k16) {
-          const uint32_t off = (uint32_t)((k16 >> 2) * kHalfBytes + (k16 & 3) * 32);
-          tc::mma_f16(tmem + (uint32_t)(st * 128), tc::desc_kmajor_sw128(q_addr + off),
-                      tc::desc_kmajor_sw128(k_addr + off), idesc_s, k16 > 0 ? 1u : 0u);
-        }
-        tc::mma_commit(&sh->s_full[st]);
-        tc::mma_commit(&sh->k_empty[st]);
-        return true;
-      };
-      if (ok && nblk > 0) ok = issue_s(0);
-      for (int j = 0; j < nblk && ok; ++j) {
-        if (j + 1 < nblk && !(ok = issue_s(j + 1))) break;
-        const int st = j & 1;
-        if (!(ok = tc::mbar_wait(&sh->p_full, pph, abort_flag, status))) break;
-        pph ^= 1;
-        if (!(ok = tc::mbar_wait(&sh->v_full[st], (vph >> st) & 1u, abort_flag, status))) break;
-        vph ^= 1u << st;
-        tc::fence_after_thread_sync();
-        const uint32_t v_addr = tc::smem_u32(v_sm + st * kTileBytes);
-        // O += P_hi V + P_lo V: A = P parts (K-major, keys contiguous),
-        // B = V (MN-major: one 128-byte row per key and d-half)
-#pragma unroll
-        for (int part = 0; part < 2; ++part) {
-          const uint32_t pa = part ? pl_addr : p_addr;
+      if (nblk > 0) {
+        const uint32_t idesc_s = tc::idesc_bf16_f32(128, kKeyBlk);
+        const uint32_t idesc_o = tc::idesc_bf16_f32(128, 128) | (1u << 16);  // B is MN-major
+        const uint32_t q_addr = tc::smem_u32(q_sm);
+        bool mok = tc::mbar_wait(&sh->q_full, 0, abort_flag, status);
+        uint32_t kph = 0, vph = 0, pph = 0;   // bit st: phase parity per stage / slot
+        auto issue_s = [&](int j) -> bool {
+          const int st = j & 1;
+          if (!tc::mbar_wait(&sh->k_full[st], (kph >> st) & 1u, abort_flag, status)) return false;
+          kph ^= 1u << st;
+          tc::fence_after_thread_sync();
+          const uint32_t k_addr = tc::smem_u32(k_sm + st * kTileBytes);
 #pragma unroll
           for (int k16 = 0; k16 < 8; ++k16) {
-            const uint32_t a_off = (uint32_t)((k16 >> 2) * kHalfBytes + (k16 & 3) * 32);
-            tc::mma_f16(tmem + 256u, tc::desc_kmajor_sw128(pa + a_off),
-                        desc_mnmajor_sw128(v_addr + (uint32_t)(k16 * 16 * 128), kHalfBytes),
-                        idesc_o, (j > 0 || part > 0 || k16 > 0) ? 1u : 0u);
+            const uint32_t off = (uint32_t)((k16 >> 2) * kHalfBytes + (k16 & 3) * 32);
+            tc::mma_f16(tmem + (uint32_t)(st * 128), tc::desc_kmajor_sw128(q_addr + off),
+                        tc::desc_kmajor_sw128(k_addr + off), idesc_s, k16 > 0 ? 1u : 0u);
+          }
+          tc::mma_commit(&sh->s_full[st]);
+          tc::mma_commit(&sh->k_empty[st]);
+          return true;
+        };
+        if (mok) mok = issue_s(0);
+        if (mok && nblk > 1) mok = issue_s(1);
+        for (int j = 0; j < nblk && mok; ++j) {
+          const int st = j & 1;
+          if (!(mok = tc::mbar_wait(&sh->p_full[st], (pph >> st) & 1u, abort_flag, status))) break;
+          pph ^= 1u << st;
+          if (!(mok = tc::mbar_wait(&sh->v_full[st], (vph >> st) & 1u, abort_flag, status))) break;
+          vph ^= 1u << st;
+          tc::fence_after_thread_sync();
+          const uint32_t v_addr = tc::smem_u32(v_sm + st * kTileBytes);
+          // O += P_hi V + P_lo V: A = P from its TMEM slot (hi columns +0,
+          // lo +64), B = V (MN-major: one 128-byte row per key and d-half)
+#pragma unroll
+          for (int part = 0; part < 2; ++part) {
+#pragma unroll
+            for (int k16 = 0; k16 < 8; ++k16) {
+              const uint32_t a_tm = tmem + (uint32_t)(st * 128 + part * 64 + k16 * 8);
+              mma_f16_tmem_a(tmem + 256u, a_tm,
+                             desc_mnmajor_sw128(v_addr + (uint32_t)(k16 * 16 * 128), kHalfBytes),
+                             idesc_o, (j > 0 || part > 0 || k16 > 0) ? 1u : 0u);
+            }
+          }
+          tc::mma_commit(&sh->pv_done);
+          tc::mma_commit(&sh->v_empty[st]);
+          if (j + 2 < nblk) {
+            // slot st is free once this PV has read P
+            if (!(mok = tc::mbar_wait(&sh->pv_done, (uint32_t)(j & 1), abort_flag, status))) break;
+            if (!(mok = issue_s(j + 2))) break;
           }
         }
-        tc::mma_commit(&sh->p_free);
-        tc::mma_commit(&sh->v_empty[st]);
+        if (mok) tc::mma_commit(&sh->o_done);
       }
-      if (ok) tc::mma_commit(&sh->o_done);
       tc::mma_commit(&sh->drain);
       int never = 0;
       tc::mbar_wait(&sh->drain, 0, &never, nullptr, 200000000ll);
     }
-  } else {
+  } else if (row_warp) {
     // ------------------------------------------------------------ rows
     // two threads per query row: half 0 owns key columns / d columns 0-63,
     // half 1 owns 64-127
-    const int quad = warp & 3;
-    const int half = (warp - 2) >> 2;
-    const int r = quad * 32 + lane;                   // row in the tile
     const int qrow = mt * 128 + r;                    // (node, head) row of (b, g)
-    const int node = qrow / A.G, hh = qrow % A.G;
+    const int node = qrow / A.G;
     const bool row_ok = node < n;
-    // ancestor-or-self bits of this row's node for the key columns this
-    // thread owns: word w covers tree nodes 32*w .. 32*w+31
+    // ancestor-or-self bits of this row's node: word w covers tree nodes
+    // 32*w .. 32*w+31
     uint32_t anc[EAGLE_MAX_TREE_NODES / 32];
 #pragma unroll
     for (int w = 0; w < EAGLE_MAX_TREE_NODES / 32; ++w) anc[w] = 0u;
@@ -442,7 +461,7 @@ tree_attn_tc_kernel(const __grid_constant__ CUtensorMap map_q,
 #pragma unroll
         for (int w = 0; w < EAGLE_MAX_TREE_NODES / 32; ++w)
           if ((j >> 5) == w) anc[w] |= 1u << (j & 31);
-        const int p = __ldg(A.parent + t0 + j);
+        const int p = sh->par[j];
         if ((j == 0) ? (p != -1) : (p < 0 || p >= j) || ++steps > n) {
           if (half == 0) fail(status, EAGLE_ERR_INVALID_TREE);
           break;
@@ -450,13 +469,10 @@ tree_attn_tc_kernel(const __grid_constant__ CUtensorMap map_q,
         j = p;
       }
     }
-    const uint32_t p_row = tc::smem_u32(p_sm) + (uint32_t)(half * kHalfBytes + r * 128);
-    const uint32_t pl_row = tc::smem_u32(pl_sm) + (uint32_t)(half * kHalfBytes + r * 128);
     const uint32_t trow = tmem + ((uint32_t)(quad * 32) << 16);
     const uint32_t o_addr = trow + 256u + (uint32_t)(half * 64);
-    float m = -INFINITY, l = 0.f;   // l: this half's share of the normaliser
-    uint32_t sph = 0, pfph = 0;   // sph bit st: phase parity of s_full[st]
-    bool ok = true;
+    float l = 0.f;   // this half's share of the normaliser
+    uint32_t sph = 0;   // bit st: phase parity of s_full[st]
     for (int j = 0; j < nblk && ok; ++j) {
       const int st = j & 1;
       const bool got = tc::mbar_wait(&sh->s_full[st], (sph >> st) & 1u, abort_flag, status);
@@ -485,26 +501,26 @@ tree_attn_tc_kernel(const __grid_constant__ CUtensorMap map_q,
         if (i < nv1 && ((w1 >> i) & 1u)) bm = fmaxf(bm, v1[i]);
       }
       bm *= A.scale_log2;
-      // the previous PV product must be complete before P, O or the exchange
-      // slot (read by the other half before it released that product) is reused
-      if (j >= 1) {
-        const bool g2 = tc::mbar_wait(&sh->p_free, pfph, abort_flag, status);
-        if (!(ok = __all_sync(0xffffffffu, g2))) break;
-        pfph ^= 1;
-        tc::fence_after_thread_sync();
-      }
-      // the row's block max: combine with the other half
-      sh->xchg[half][r] = bm;
+      // the row's block max: combine with the other half (both halves have
+      // read their S columns once the exchange completes, so P may then
+      // overwrite the slot)
+      sh->xchg[j & 1][half][r] = bm;
       tc::mbar_arrive(&sh->xbar);
       const bool g3 = tc::mbar_wait(&sh->xbar, (uint32_t)(j & 1), abort_flag, status);
       if (!(ok = __all_sync(0xffffffffu, g3))) break;
-      bm = fmaxf(bm, sh->xchg[half ^ 1][r]);
+      bm = fmaxf(bm, sh->xchg[j & 1][half ^ 1][r]);
       const float mn = fmaxf(m, bm);
       const bool first = (m == -INFINITY);
       const bool rescale = !first && (mn > m + kRescaleLog2);
       const float mu = (first || rescale) ? mn : m;     // reference max for this block's P
-      if (rescale) {
-        const float f = exp2f(m - mu);
+      if (__any_sync(0xffffffffu, rescale)) {
+        // O must hold every earlier block (the S of this block was issued
+        // after the PV two blocks back, so the previous PV is the only one
+        // that may still run)
+        const bool g4 = tc::mbar_wait(&sh->pv_done, (uint32_t)((j - 1) & 1), abort_flag, status);
+        if (!(ok = __all_sync(0xffffffffu, g4))) break;
+        tc::fence_after_thread_sync();
+        const float f = rescale ? exp2f(m - mu) : 1.f;
         float o[32];
 #pragma unroll
         for (int cc = 0; cc < 2; ++cc) {
@@ -515,46 +531,35 @@ tree_attn_tc_kernel(const __grid_constant__ CUtensorMap map_q,
         }
         l *= f;
       }
-      // P = exp2(s - mu) split into bf16 hi + lo, into the swizzled P tiles
+      // P = exp2(s - mu) as bf16 hi + lo into this block's TMEM slot: hi
+      // columns half*32 .., lo columns 64 + half*32 ..
       float psum = 0.f;
-      auto emit = [&](float (&v)[32], int nvc, uint32_t wc, int cc) {
-        float lo[32];
+      auto emit = [&](const float (&v)[32], int nvc, uint32_t wc, int cc) {
+        uint32_t hi[16], lo[16];
 #pragma unroll
-        for (int i = 0; i < 32; ++i) {
-          const bool vis = (i < nvc) && ((wc >> i) & 1u);
-          const float pv = vis ? exp2f(fmaf(v[i], A.scale_log2, -mu)) : 0.f;
-          const float hi = __bfloat162float(__float2bfloat16_rn(pv));
-          lo[i] = pv - hi;
-          v[i] = hi;
-          psum += pv;
+        for (int i = 0; i < 16; ++i) {
+          const int e0 = 2 * i, e1 = 2 * i + 1;
+          const float p0 = (e0 < nvc && ((wc >> e0) & 1u)) ? exp2f(fmaf(v[e0], A.scale_log2, -mu)) : 0.f;
+          const float p1 = (e1 < nvc && ((wc >> e1) & 1u)) ? exp2f(fmaf(v[e1], A.scale_log2, -mu)) : 0.f;
+          const uint32_t h = pack_bf16(p0, p1);
+          hi[i] = h;
+          lo[i] = pack_bf16(p0 - __uint_as_float(h << 16), p1 - __uint_as_float(h & 0xffff0000u));
+          psum += p0 + p1;
         }
-#pragma unroll
-        for (int u = 0; u < 4; ++u) {
-          const int unit = cc * 4 + u;   // 16-byte unit of this half's 128-byte row
-          const uint32_t off = (uint32_t)(((unit ^ (r & 7)) & 7) * 16);
-          st_shared_v4(p_row + off, pack_bf16(v[u * 8 + 0], v[u * 8 + 1]),
-                       pack_bf16(v[u * 8 + 2], v[u * 8 + 3]), pack_bf16(v[u * 8 + 4], v[u * 8 + 5]),
-                       pack_bf16(v[u * 8 + 6], v[u * 8 + 7]));
-          st_shared_v4(pl_row + off, pack_bf16(lo[u * 8 + 0], lo[u * 8 + 1]),
-                       pack_bf16(lo[u * 8 + 2], lo[u * 8 + 3]),
-                       pack_bf16(lo[u * 8 + 4], lo[u * 8 + 5]),
-                       pack_bf16(lo[u * 8 + 6], lo[u * 8 + 7]));
-        }
+        const uint32_t col = trow + (uint32_t)(st * 128 + half * 32 + cc * 16);
+        tmem_st_32x32b_x16(col, hi);
+        tmem_st_32x32b_x16(col + 64u, lo);
       };
       emit(v0, nv0, w0, 0);
       emit(v1, nv1, w1, 1);
+      tmem_wait_st();
       l += psum;
       m = mu;
-      fence_proxy_async_smem();
       tc::fence_before_thread_sync();
       __syncwarp();
-      if (lane == 0) {
-        tc::mbar_arrive(&sh->s_empty[st]);
-        tc::mbar_arrive(&sh->p_full);
-      }
+      if (lane == 0) tc::mbar_arrive(&sh->p_full[st]);
     }
-    // ---- the output rows: O (in TMEM) / l
-    float o0[32], o1[32];
+    // ---- this CTA's O rows (unnormalised) and the row normaliser
     if (ok && nblk > 0) {
       const bool got = tc::mbar_wait(&sh->o_done, 0, abort_flag, status);
       if ((ok = __all_sync(0xffffffffu, got))) {
@@ -566,20 +571,25 @@ tree_attn_tc_kernel(const __grid_constant__ CUtensorMap map_q,
     if (!ok) {
 #pragma unroll
       for (int i = 0; i < 32; ++i) o0[i] = o1[i] = 0.f;
+      m = -INFINITY;
+      l = 0.f;
     }
-    // full normaliser = this half's share + the other half's (the slot is
-    // free: the other half read it before releasing the last PV product)
-    sh->xchg[half][r] = l;
+    sh->xchg[nblk & 1][half][r] = l;
     tc::mbar_arrive(&sh->fbar);
     {
       const bool got = tc::mbar_wait(&sh->fbar, 0, abort_flag, status);
       ok = __all_sync(0xffffffffu, got) && ok;
     }
-    const float l_row = l + sh->xchg[half ^ 1][r];
-    const int h = g * A.G + hh;
-    float* orow = A.out + ((size_t)(t0 + node) * A.Hq + h) * 128 + half * 64;
-    if (n_chunks == 1) {
-      if (row_ok && ok) {
+    l_row = l + sh->xchg[nblk & 1][half ^ 1][r];
+  }
+
+  // ---------------------------------------------------------------- output
+  if (A.NC == 1) {
+    if (row_warp) {
+      const int qrow = mt * 128 + r;
+      const int node = qrow / A.G, hh = qrow % A.G;
+      if (node < n && ok) {
+        float* orow = A.out + ((size_t)(t0 + node) * A.Hq + g * A.G + hh) * 128 + half * 64;
         const float inv = 1.f / l_row;
 #pragma unroll
         for (int d = 0; d < 32; d += 4) {
@@ -589,69 +599,55 @@ tree_attn_tc_kernel(const __grid_constant__ CUtensorMap map_q,
               make_float4(o1[d] * inv, o1[d + 1] * inv, o1[d + 2] * inv, o1[d + 3] * inv);
         }
       }
-    } else {
-      float* po = A.part_o + ((size_t)item_id * 128 + r) * 128 + half * 64;
-      if (half == 0) A.part_ml[(size_t)item_id * 128 + r] = make_float2(m, l_row);
-#pragma unroll
-      for (int d = 0; d < 32; d += 4) {
-        *reinterpret_cast<float4*>(po + d) = make_float4(o0[d], o0[d + 1], o0[d + 2], o0[d + 3]);
-        *reinterpret_cast<float4*>(po + 32 + d) =
-            make_float4(o1[d], o1[d + 1], o1[d + 2], o1[d + 3]);
+    }
+  } else {
+    // merge the cluster's chunks: out = sum_c exp2(m_c - M) O_c / sum_c exp2(m_c - M) l_c
+    cg::cluster_group cluster = cg::this_cluster();
+    if (row_warp && half == 0) sh->ml[r] = make_float2(m, l_row);
+    cluster.sync();
+    if (row_warp) {
+      float M = -INFINITY;
+      for (int cc = 0; cc < A.NC; ++cc)
+        M = fmaxf(M, cluster.map_shared_rank(&sh->ml[r], cc)->x);
+      float Lsum = 0.f;
+      for (int cc = 0; cc < A.NC; ++cc) {
+        const float2 ml = *cluster.map_shared_rank(&sh->ml[r], cc);
+        Lsum += (ml.x == -INFINITY) ? 0.f : ml.y * exp2f(ml.x - M);
       }
-      __threadfence();
-      tc::mbar_arrive(&sh->tbar0);
-      if (threadIdx.x == 64) {
-        // every row thread's partial is written: take the ticket
-        int never = 0;
-        sh->is_last = 0;
-        if (tc::mbar_wait(&sh->tbar0, 0, abort_flag, status)) {
-          const int prev = atomicAdd(&A.counters[tile_id], 1);
-          sh->is_last = (prev == n_chunks - 1);
-          if (sh->is_last) A.counters[tile_id] = 0;
-        }
-        (void)never;
-        tc::mbar_arrive(&sh->tbar1);
+      const float f = (m == -INFINITY || !(Lsum > 0.f)) ? 0.f : exp2f(m - M) / Lsum;
+#pragma unroll
+      for (int i = 0; i < 8; ++i) {
+        const int c4 = half * 16 + i;
+        obuf[r * 32 + (c4 ^ (r & 31))] =
+            make_float4(o0[4 * i] * f, o0[4 * i + 1] * f, o0[4 * i + 2] * f, o0[4 * i + 3] * f);
       }
-      const bool got_t = tc::mbar_wait(&sh->tbar1, 0, abort_flag, status);
-      if (got_t && sh->is_last && row_ok) {
-        __threadfence();
-        float M = -INFINITY;
-        for (int cc = 0; cc < n_chunks; ++cc)
-          M = fmaxf(M, __ldcg(&A.part_ml[((size_t)(tile_id * A.NC + cc)) * 128 + r]).x);
-        float Lsum = 0.f;
 #pragma unroll
-        for (int d = 0; d < 32; ++d) o0[d] = o1[d] = 0.f;
-        for (int cc = 0; cc < n_chunks; ++cc) {
-          const size_t it = (size_t)(tile_id * A.NC + cc);
-          const float2 ml = __ldcg(&A.part_ml[it * 128 + r]);
-          const float wgt = (ml.x == -INFINITY) ? 0.f : exp2f(ml.x - M);
-          Lsum += ml.y * wgt;
-          const float4* src =
-              reinterpret_cast<const float4*>(A.part_o + (it * 128 + r) * 128 + half * 64);
-#pragma unroll
-          for (int d = 0; d < 8; ++d) {
-            const float4 x = __ldcg(src + d);
-            o0[4 * d] = fmaf(x.x, wgt, o0[4 * d]);
-            o0[4 * d + 1] = fmaf(x.y, wgt, o0[4 * d + 1]);
-            o0[4 * d + 2] = fmaf(x.z, wgt, o0[4 * d + 2]);
-            o0[4 * d + 3] = fmaf(x.w, wgt, o0[4 * d + 3]);
-            const float4 y = __ldcg(src + 8 + d);
-            o1[4 * d] = fmaf(y.x, wgt, o1[4 * d]);
-            o1[4 * d + 1] = fmaf(y.y, wgt, o1[4 * d + 1]);
-            o1[4 * d + 2] = fmaf(y.z, wgt, o1[4 * d + 2]);
-            o1[4 * d + 3] = fmaf(y.w, wgt, o1[4 * d + 3]);
-          }
-        }
-        const float inv = 1.f / Lsum;
-#pragma unroll
-        for (int d = 0; d < 32; d += 4) {
-          *reinterpret_cast<float4*>(orow + d) =
-              make_float4(o0[d] * inv, o0[d + 1] * inv, o0[d + 2] * inv, o0[d + 3] * inv);
-          *reinterpret_cast<float4*>(orow + 32 + d) =
-              make_float4(o1[d] * inv, o1[d + 1] * inv, o1[d + 2] * inv, o1[d + 3] * inv);
-        }
+      for (int i = 0; i < 8; ++i) {
+        const int c4 = half * 16 + 8 + i;
+        obuf[r * 32 + (c4 ^ (r & 31))] =
+            make_float4(o1[4 * i] * f, o1[4 * i + 1] * f, o1[4 * i + 2] * f, o1[4 * i + 3] * f);
       }
     }
+    cluster.sync();
+    // this CTA's share of the rows: sum the cluster's scaled O rows
+    const int R0 = (128 * c) / A.NC, R1 = (128 * (c + 1)) / A.NC;
+    for (int idx = threadIdx.x; idx < (R1 - R0) * 32; idx += kAttThreads) {
+      const int row = R0 + idx / 32, c4 = idx % 32;
+      const int qrow = mt * 128 + row;
+      const int node = qrow / A.G, hh = qrow % A.G;
+      if (node >= n) continue;
+      float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+      for (int cc = 0; cc < A.NC; ++cc) {
+        const float4 x = *cluster.map_shared_rank(&obuf[row * 32 + (c4 ^ (row & 31))], cc);
+        acc.x += x.x;
+        acc.y += x.y;
+        acc.z += x.z;
+        acc.w += x.w;
+      }
+      *reinterpret_cast<float4*>(A.out + ((size_t)(t0 + node) * A.Hq + g * A.G + hh) * 128 +
+                                 c4 * 4) = acc;
+    }
+    cluster.sync();   // no CTA leaves while others read its shared memory
   }
   tc::fence_before_thread_sync();
   __syncthreads();
@@ -697,14 +693,18 @@ bool tc_shape_ok(eagle_dtype dtype, int Hq, int Hkv, int D) {
 
 }  // namespace
 
-// Scratch of the tensor-core path (split-K partials and merge tickets); the
-// CUDA-core path needs none.  Depends on shapes only, not on the device.
+// Neither path needs global scratch: the tensor-core path merges its cache
+// chunks inside a thread-block cluster.
 extern "C" size_t eagle_tree_attn_workspace_bytes(int B, int T, int Hq, int Hkv, int D,
                                                   int max_nodes, int max_kv) {
+  (void)B;
   (void)T;
-  if (B < 1 || Hq < 1 || Hkv < 1 || Hq % Hkv || max_nodes < 1 || max_kv < 0) return 0;
-  if (!tc_shape_ok(EAGLE_BF16, Hq, Hkv, D)) return 0;
-  return att_plan(B, Hq, Hkv, max_nodes, max_kv).total;
+  (void)Hq;
+  (void)Hkv;
+  (void)D;
+  (void)max_nodes;
+  (void)max_kv;
+  return 0;
 }
 
 extern "C" eagle_status eagle_tree_attn(eagle_dtype dtype, int B, int T, int Hq, int Hkv, int D,
@@ -729,13 +729,12 @@ extern "C" eagle_status eagle_tree_attn(eagle_dtype dtype, int B, int T, int Hq,
   EAGLE_HOST_CHECK(ws_bytes >= eagle_tree_attn_workspace_bytes(B, T, Hq, Hkv, D, max_nodes, max_kv),
                    EAGLE_ERR_WORKSPACE);
   EAGLE_HOST_CHECK(kv_rows >= 0, EAGLE_ERR_INVALID_ARG);
+  (void)d_ws;
   cudaStream_t s = (cudaStream_t)stream;
   const uintptr_t align = (uintptr_t)d_q | (uintptr_t)d_k_tree | (uintptr_t)d_v_tree |
                           (uintptr_t)d_k_cache | (uintptr_t)d_v_cache | (uintptr_t)d_out;
   if (tc_shape_ok(dtype, Hq, Hkv, D) && (align & 15) == 0) {
     const AttPlan P = att_plan(B, Hq, Hkv, max_nodes, max_kv);
-    EAGLE_HOST_CHECK(d_ws && ws_bytes >= P.total, EAGLE_ERR_WORKSPACE);
-    EAGLE_HOST_CHECK(((uintptr_t)d_ws & 255) == 0, EAGLE_ERR_INVALID_ARG);
     CUtensorMap mq, mkc, mvc, mkt, mvt;
     const void* kc = (kv_rows > 0) ? d_k_cache : d_k_tree;   // never read when empty
     const void* vc = (kv_rows > 0) ? d_v_cache : d_v_tree;
@@ -753,7 +752,6 @@ extern "C" eagle_status eagle_tree_attn(eagle_dtype dtype, int B, int T, int Hq,
         return EAGLE_ERR_CUDA;
       attr = true;
     }
-    char* ws = static_cast<char*>(d_ws);
     AttParams A;
     A.B = B;
     A.Hq = Hq;
@@ -769,15 +767,22 @@ extern "C" eagle_status eagle_tree_attn(eagle_dtype dtype, int B, int T, int Hq,
     A.tree_off = d_tree_off;
     A.parent = d_parent;
     A.out = d_out;
-    A.counters = reinterpret_cast<int*>(ws);
-    A.part_ml = reinterpret_cast<float2*>(ws + P.off_ml);
-    A.part_o = reinterpret_cast<float*>(ws + P.off_o);
     A.status = d_status;
-    if (cudaMemsetAsync(ws, 0, (size_t)B * Hkv * P.MT * sizeof(int), s) != cudaSuccess)
-      return EAGLE_ERR_CUDA;
-    const int grid = B * Hkv * P.NC * P.MT;
-    return launch_status(launch_pdl(tree_attn_tc_kernel, dim3(grid), dim3(kAttThreads), kAttSmem,
-                                    s, mq, mkc, mvc, mkt, mvt, A));
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3((unsigned)(B * Hkv * P.MT * P.NC));
+    cfg.blockDim = dim3(kAttThreads);
+    cfg.dynamicSmemBytes = kAttSmem;
+    cfg.stream = s;
+    cudaLaunchAttribute attrs[2];
+    attrs[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attrs[0].val.programmaticStreamSerializationAllowed = 1;
+    attrs[1].id = cudaLaunchAttributeClusterDimension;
+    attrs[1].val.clusterDim.x = (unsigned)P.NC;
+    attrs[1].val.clusterDim.y = 1;
+    attrs[1].val.clusterDim.z = 1;
+    cfg.attrs = attrs;
+    cfg.numAttrs = (P.NC > 1) ? 2 : 1;
+    return launch_status(cudaLaunchKernelEx(&cfg, tree_attn_tc_kernel, mq, mkc, mvc, mkt, mvt, A));
   }
   if (dtype == EAGLE_BF16)
     return launch_warp<__nv_bfloat16>(D, B, T, Hq, Hkv, scale, max_nodes, max_kv, d_q, d_k_tree,

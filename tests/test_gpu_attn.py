@@ -113,3 +113,23 @@ def test_changing_one_branch_leaves_the_rest_of_the_tree_unchanged(dtype, L, Hq,
             inside = victim in O.tree_path(parent, i)
             same = np.array_equal(out[i], base[i])
             assert same != inside, (which, i)
+
+
+def test_rising_scores_force_output_rescaling():
+    # Scores climb ~20 nats across every cache chunk, so the running row max
+    # grows by more than 2^8 (log2 units) several times inside one CTA: the
+    # kernel's deferred rescaling of O must keep the result exact.  Eight
+    # heads and L = 8192 also give the largest split of one row tile (8
+    # chunks, one cluster of 8).
+    E = cuda_ready()
+    q, kt, vt, kc, vc, kv_off, tree_off, parent = _case(23, "bf16", [8192], [(1, 10, 10)], 8, 8,
+                                                        128)
+    q = synth.to_bf16_values(q + 1.0)
+    ramp = (np.arange(8192, dtype=np.float64) / 8192.0 * 2000.0 / 128.0)[:, None, None]
+    kc = synth.to_bf16_values(0.1 * kc + ramp)
+    case = (q, kt, vt, kc, vc, kv_off, tree_off, parent)
+    got, st = _run(E, "bf16", *case)
+    assert st == 0
+    nodes = list(range(0, 21, 4))
+    ref = O.tree_attn(*case, nodes=nodes)
+    assert attn_rel_err(got[nodes], ref[nodes]).max() <= 2e-3
