@@ -149,10 +149,10 @@ struct AttShared {
   uint64_t k_full[2], k_empty[2], v_full[2], v_empty[2];
   uint64_t s_full[2], p_full[2];   // per TMEM slot: S ready / P written
   uint64_t pv_done, o_done, drain;
-  uint64_t xbar, fbar;             // row-half exchanges
+  uint64_t fbar;                   // row-half exchange after the key loop
   uint32_t tmem_base;
   int abort_flag;
-  float xchg[2][2][128];           // [block parity][half][row]
+  float xchg[2][2][128];           // [m | l][half][row]
   float2 ml[128];                  // (m, l) of every row, read by the cluster
   int par[EAGLE_MAX_TREE_NODES];   // parent[] of the sequence
 };
@@ -185,6 +185,14 @@ struct AttParams {
   float* out;
   int* status;
 };
+
+// 2^x by the SFU's approximate exponential (relative error about 2^-22;
+// subnormal results flush to zero, 2^-inf = 0).
+__device__ __forceinline__ float ex2_approx(float x) {
+  float y;
+  asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+  return y;
+}
 
 __device__ __forceinline__ uint32_t pack_bf16(float a, float b) {
   __nv_bfloat162 v = __floats2bfloat162_rn(a, b);
@@ -249,8 +257,12 @@ __device__ __forceinline__ void tmem_wait_st() {
 
 // One CTA per (sequence, kv head, 128-row tile, cache chunk); the chunks of
 // a tile form a thread-block cluster and merge their partial softmax rows
-// through distributed shared memory.  TMEM: S slots at columns 0 / 128 (P,
-// as bf16 hi | lo halves, overwrites its S slot), O at column 256.
+// through distributed shared memory.  Two threads per query row, one per
+// half of every key block; each half keeps its own running max, sum and
+// output accumulator, so the halves never wait for each other inside the
+// key loop and are merged once at the end.  TMEM columns: S slots 0 / 128
+// (P overwrites the half's own S columns: bf16 hi at +0, lo at +32), O of
+// key half 0 at 256, of key half 1 at 384.
 __global__ void __launch_bounds__(kAttThreads, 1)
 tree_attn_tc_kernel(const __grid_constant__ CUtensorMap map_q,
                     const __grid_constant__ CUtensorMap map_kc,
@@ -270,7 +282,7 @@ tree_attn_tc_kernel(const __grid_constant__ CUtensorMap map_q,
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   // work item: tile * NC + c, the cache chunks of a tile adjacent (one cluster)
   const int c = blockIdx.x % A.NC;
-  int tile = blockIdx.x / A.NC;
+  const int tile = blockIdx.x / A.NC;
   const int mt = tile % A.MT;
   const int g = (tile / A.MT) % A.Hkv;
   const int b = tile / (A.MT * A.Hkv);
@@ -299,8 +311,27 @@ tree_attn_tc_kernel(const __grid_constant__ CUtensorMap map_q,
   int active_quads = 0;
   for (int q = 0; q < 4; ++q) active_quads += ((mt * 128 + q * 32) / A.G < n);
   const int active_warps = 2 * active_quads;
+  volatile int* abort_flag = &sh->abort_flag;
+  int* status = A.status;
 
-  for (int i = threadIdx.x; i < n; i += kAttThreads) sh->par[i] = A.parent[t0 + i];
+  auto block_row = [&](int j) {   // first key row of block j in its tensor
+    return (j < n_cache_blk) ? kv0 + key_begin + j * kKeyBlk : t0 + (j - n_cache_blk) * kKeyBlk;
+  };
+  auto load_kv = [&](int j) {
+    const int st = j & 1;
+    const CUtensorMap* mk = (j < n_cache_blk) ? &map_kc : &map_kt;
+    const CUtensorMap* mv = (j < n_cache_blk) ? &map_vc : &map_vt;
+    const int row = block_row(j);
+    unsigned char* kd = k_sm + st * kTileBytes;
+    unsigned char* vd = v_sm + st * kTileBytes;
+    tc::mbar_arrive_expect_tx(&sh->k_full[st], kTileBytes);
+    tc::tma_load_3d(kd, mk, &sh->k_full[st], 0, g, row);
+    tc::tma_load_3d(kd + kHalfBytes, mk, &sh->k_full[st], 64, g, row);
+    tc::mbar_arrive_expect_tx(&sh->v_full[st], kTileBytes);
+    tc::tma_load_3d(vd, mv, &sh->v_full[st], 0, g, row);
+    tc::tma_load_3d(vd + kHalfBytes, mv, &sh->v_full[st], 64, g, row);
+  };
+
   if (threadIdx.x == 0) {
     tc::mbar_init(&sh->q_full, 1);
     for (int i = 0; i < 2; ++i) {
@@ -314,11 +345,19 @@ tree_attn_tc_kernel(const __grid_constant__ CUtensorMap map_q,
     tc::mbar_init(&sh->pv_done, 1);
     tc::mbar_init(&sh->o_done, 1);
     tc::mbar_init(&sh->drain, 1);
-    tc::mbar_init(&sh->xbar, 32 * active_warps);
     tc::mbar_init(&sh->fbar, 32 * active_warps);
     sh->abort_flag = 0;
     tc::fence_barrier_init();
+    // the first copies start before the rest of the set-up
+    if (nblk > 0) {
+      tc::mbar_arrive_expect_tx(&sh->q_full, kTileBytes);
+      const int node0 = t0 + mt * nodes_per_tile;
+      tc::tma_load_3d(q_sm, &map_q, &sh->q_full, 0, g * A.G, node0);
+      tc::tma_load_3d(q_sm + kHalfBytes, &map_q, &sh->q_full, 64, g * A.G, node0);
+      for (int j = 0; j < min(2, nblk); ++j) load_kv(j);
+    }
   }
+  for (int i = threadIdx.x; i < n; i += kAttThreads) sh->par[i] = A.parent[t0 + i];
   if (warp == 1) {
     tc::tmem_alloc(&sh->tmem_base, 512);
     tc::tmem_relinquish();
@@ -327,49 +366,28 @@ tree_attn_tc_kernel(const __grid_constant__ CUtensorMap map_q,
   __syncthreads();
   tc::fence_after_thread_sync();
   const uint32_t tmem = sh->tmem_base;
-  volatile int* abort_flag = &sh->abort_flag;
-  int* status = A.status;
 
   // row-thread state carried into the merge
   const int quad = warp & 3;
-  const int half = (warp - 2) >> 2;
+  const int half = (warp - 2) >> 2;                 // key half of every block
   const int r = quad * 32 + lane;                   // row in the tile
   const bool row_warp = warp >= 2 && quad < active_quads;
-  float o0[32], o1[32];
-  float m = -INFINITY, l_row = 0.f;
+  float o0[32], o1[32];                             // output columns half*64 .. +63
+  float m_row = -INFINITY, l_row = 0.f;
   bool ok = true;
-#pragma unroll
-  for (int i = 0; i < 32; ++i) o0[i] = o1[i] = 0.f;
 
   if (warp == 0) {
     // ------------------------------------------------------------ TMA
-    if (lane == 0 && nblk > 0) {
+    if (lane == 0 && nblk > 2) {
       bool tok = true;
-      tc::mbar_arrive_expect_tx(&sh->q_full, kTileBytes);
-      const int node0 = t0 + mt * nodes_per_tile;
-      tc::tma_load_3d(q_sm, &map_q, &sh->q_full, 0, g * A.G, node0);
-      tc::tma_load_3d(q_sm + kHalfBytes, &map_q, &sh->q_full, 64, g * A.G, node0);
       uint32_t eph = 0;   // bit st: phase parity of stage st's empty barriers
-      int issued = 0;
-      for (int j = 0; j < nblk && tok; ++j) {
+      int issued = 2;
+      for (int j = 2; j < nblk && tok; ++j) {
         const int st = j & 1;
-        if (j >= 2) {
-          if (!(tok = tc::mbar_wait(&sh->k_empty[st], (eph >> st) & 1u, abort_flag, status))) break;
-          if (!(tok = tc::mbar_wait(&sh->v_empty[st], (eph >> st) & 1u, abort_flag, status))) break;
-          eph ^= 1u << st;
-        }
-        const CUtensorMap* mk = (j < n_cache_blk) ? &map_kc : &map_kt;
-        const CUtensorMap* mv = (j < n_cache_blk) ? &map_vc : &map_vt;
-        const int row = (j < n_cache_blk) ? kv0 + key_begin + j * kKeyBlk
-                                          : t0 + (j - n_cache_blk) * kKeyBlk;
-        unsigned char* kd = k_sm + st * kTileBytes;
-        unsigned char* vd = v_sm + st * kTileBytes;
-        tc::mbar_arrive_expect_tx(&sh->k_full[st], kTileBytes);
-        tc::tma_load_3d(kd, mk, &sh->k_full[st], 0, g, row);
-        tc::tma_load_3d(kd + kHalfBytes, mk, &sh->k_full[st], 64, g, row);
-        tc::mbar_arrive_expect_tx(&sh->v_full[st], kTileBytes);
-        tc::tma_load_3d(vd, mv, &sh->v_full[st], 0, g, row);
-        tc::tma_load_3d(vd + kHalfBytes, mv, &sh->v_full[st], 64, g, row);
+        if (!(tok = tc::mbar_wait(&sh->k_empty[st], (eph >> st) & 1u, abort_flag, status))) break;
+        if (!(tok = tc::mbar_wait(&sh->v_empty[st], (eph >> st) & 1u, abort_flag, status))) break;
+        eph ^= 1u << st;
+        load_kv(j);
         ++issued;
       }
       if (!tok) {
@@ -417,16 +435,20 @@ tree_attn_tc_kernel(const __grid_constant__ CUtensorMap map_q,
           vph ^= 1u << st;
           tc::fence_after_thread_sync();
           const uint32_t v_addr = tc::smem_u32(v_sm + st * kTileBytes);
-          // O += P_hi V + P_lo V: A = P from its TMEM slot (hi columns +0,
-          // lo +64), B = V (MN-major: one 128-byte row per key and d-half)
+          // O_h += P_hi V_h + P_lo V_h for key half h: A = P from the half's
+          // TMEM columns, B = V rows of that half (MN-major, 128-byte rows)
 #pragma unroll
-          for (int part = 0; part < 2; ++part) {
+          for (int h = 0; h < 2; ++h) {
 #pragma unroll
-            for (int k16 = 0; k16 < 8; ++k16) {
-              const uint32_t a_tm = tmem + (uint32_t)(st * 128 + part * 64 + k16 * 8);
-              mma_f16_tmem_a(tmem + 256u, a_tm,
-                             desc_mnmajor_sw128(v_addr + (uint32_t)(k16 * 16 * 128), kHalfBytes),
-                             idesc_o, (j > 0 || part > 0 || k16 > 0) ? 1u : 0u);
+            for (int part = 0; part < 2; ++part) {
+#pragma unroll
+              for (int kk = 0; kk < 4; ++kk) {
+                const uint32_t a_tm = tmem + (uint32_t)(st * 128 + h * 64 + part * 32 + kk * 8);
+                const uint32_t key = (uint32_t)(h * 64 + kk * 16);
+                mma_f16_tmem_a(tmem + 256u + (uint32_t)(h * 128), a_tm,
+                               desc_mnmajor_sw128(v_addr + key * 128u, kHalfBytes), idesc_o,
+                               (j > 0 || part > 0 || kk > 0) ? 1u : 0u);
+              }
             }
           }
           tc::mma_commit(&sh->pv_done);
@@ -445,8 +467,6 @@ tree_attn_tc_kernel(const __grid_constant__ CUtensorMap map_q,
     }
   } else if (row_warp) {
     // ------------------------------------------------------------ rows
-    // two threads per query row: half 0 owns key columns / d columns 0-63,
-    // half 1 owns 64-127
     const int qrow = mt * 128 + r;                    // (node, head) row of (b, g)
     const int node = qrow / A.G;
     const bool row_ok = node < n;
@@ -470,8 +490,8 @@ tree_attn_tc_kernel(const __grid_constant__ CUtensorMap map_q,
       }
     }
     const uint32_t trow = tmem + ((uint32_t)(quad * 32) << 16);
-    const uint32_t o_addr = trow + 256u + (uint32_t)(half * 64);
-    float l = 0.f;   // this half's share of the normaliser
+    const uint32_t o_own = trow + 256u + (uint32_t)(half * 128);   // this key half's O
+    float m = -INFINITY, l = 0.f;   // this key half's running max (log2 units) and sum
     uint32_t sph = 0;   // bit st: phase parity of s_full[st]
     for (int j = 0; j < nblk && ok; ++j) {
       const int st = j & 1;
@@ -494,64 +514,68 @@ tree_attn_tc_kernel(const __grid_constant__ CUtensorMap map_q,
                           : tb ? (half ? anc[7] : anc[5]) : (half ? anc[3] : anc[1]);
       const int nv0 = min(32, max(0, key_lim - key0));
       const int nv1 = min(32, max(0, key_lim - key0 - 32));
-      float bm = -INFINITY;
+      if (tree_blk || nv1 < 32) {
+        // masked or ragged block (warp-uniform): hidden scores become -inf
 #pragma unroll
-      for (int i = 0; i < 32; ++i) {
-        if (i < nv0 && ((w0 >> i) & 1u)) bm = fmaxf(bm, v0[i]);
-        if (i < nv1 && ((w1 >> i) & 1u)) bm = fmaxf(bm, v1[i]);
+        for (int i = 0; i < 32; ++i) {
+          if (!(i < nv0 && ((w0 >> i) & 1u))) v0[i] = -INFINITY;
+          if (!(i < nv1 && ((w1 >> i) & 1u))) v1[i] = -INFINITY;
+        }
       }
-      bm *= A.scale_log2;
-      // the row's block max: combine with the other half (both halves have
-      // read their S columns once the exchange completes, so P may then
-      // overwrite the slot)
-      sh->xchg[j & 1][half][r] = bm;
-      tc::mbar_arrive(&sh->xbar);
-      const bool g3 = tc::mbar_wait(&sh->xbar, (uint32_t)(j & 1), abort_flag, status);
-      if (!(ok = __all_sync(0xffffffffu, g3))) break;
-      bm = fmaxf(bm, sh->xchg[j & 1][half ^ 1][r]);
+      float bm0 = v0[0], bm1 = v1[0];
+#pragma unroll
+      for (int i = 1; i < 32; ++i) {
+        bm0 = fmaxf(bm0, v0[i]);
+        bm1 = fmaxf(bm1, v1[i]);
+      }
+      const float bm = fmaxf(bm0, bm1) * A.scale_log2;
       const float mn = fmaxf(m, bm);
       const bool first = (m == -INFINITY);
       const bool rescale = !first && (mn > m + kRescaleLog2);
       const float mu = (first || rescale) ? mn : m;     // reference max for this block's P
       if (__any_sync(0xffffffffu, rescale)) {
-        // O must hold every earlier block (the S of this block was issued
-        // after the PV two blocks back, so the previous PV is the only one
-        // that may still run)
+        // O_h must hold every earlier block (the S of this block was issued
+        // after the PV two blocks back, so only the previous PV may still run)
         const bool g4 = tc::mbar_wait(&sh->pv_done, (uint32_t)((j - 1) & 1), abort_flag, status);
         if (!(ok = __all_sync(0xffffffffu, g4))) break;
         tc::fence_after_thread_sync();
-        const float f = rescale ? exp2f(m - mu) : 1.f;
+        const float f = rescale ? ex2_approx(m - mu) : 1.f;
         float o[32];
 #pragma unroll
-        for (int cc = 0; cc < 2; ++cc) {
-          tc::tmem_ld_32x32b_x32(o_addr + (uint32_t)(cc * 32), o);
+        for (int cc = 0; cc < 4; ++cc) {
+          tc::tmem_ld_32x32b_x32(o_own + (uint32_t)(cc * 32), o);
 #pragma unroll
           for (int i = 0; i < 32; ++i) o[i] *= f;
-          tmem_st_32x32b_x32(o_addr + (uint32_t)(cc * 32), o);
+          tmem_st_32x32b_x32(o_own + (uint32_t)(cc * 32), o);
         }
         l *= f;
       }
-      // P = exp2(s - mu) as bf16 hi + lo into this block's TMEM slot: hi
-      // columns half*32 .., lo columns 64 + half*32 ..
+      // P = exp2(s - mu) = hi + lo, both bf16: hi keeps the top 16 bits of
+      // the fp32 value, lo = P - hi (exact in fp32) truncated the same way;
+      // |P - hi - lo| < 2^-14 P.  hi to the half's columns +0.., lo +32..
       float psum = 0.f;
-      auto emit = [&](const float (&v)[32], int nvc, uint32_t wc, int cc) {
+      // a half-row with nothing visible yet keeps mu = -inf: its scores are
+      // all -inf, and any finite offset gives P = 0
+      const float neg_mu = (mu == -INFINITY) ? 0.f : -mu;
+      auto emit = [&](const float (&v)[32], int cc) {
         uint32_t hi[16], lo[16];
 #pragma unroll
         for (int i = 0; i < 16; ++i) {
-          const int e0 = 2 * i, e1 = 2 * i + 1;
-          const float p0 = (e0 < nvc && ((wc >> e0) & 1u)) ? exp2f(fmaf(v[e0], A.scale_log2, -mu)) : 0.f;
-          const float p1 = (e1 < nvc && ((wc >> e1) & 1u)) ? exp2f(fmaf(v[e1], A.scale_log2, -mu)) : 0.f;
-          const uint32_t h = pack_bf16(p0, p1);
-          hi[i] = h;
-          lo[i] = pack_bf16(p0 - __uint_as_float(h << 16), p1 - __uint_as_float(h & 0xffff0000u));
+          const float p0 = ex2_approx(fmaf(v[2 * i], A.scale_log2, neg_mu));
+          const float p1 = ex2_approx(fmaf(v[2 * i + 1], A.scale_log2, neg_mu));
+          const uint32_t b0 = __float_as_uint(p0), b1 = __float_as_uint(p1);
+          hi[i] = __byte_perm(b0, b1, 0x7632);
+          const float r0 = p0 - __uint_as_float(b0 & 0xffff0000u);
+          const float r1 = p1 - __uint_as_float(b1 & 0xffff0000u);
+          lo[i] = __byte_perm(__float_as_uint(r0), __float_as_uint(r1), 0x7632);
           psum += p0 + p1;
         }
-        const uint32_t col = trow + (uint32_t)(st * 128 + half * 32 + cc * 16);
+        const uint32_t col = trow + (uint32_t)(st * 128 + half * 64 + cc * 16);
         tmem_st_32x32b_x16(col, hi);
-        tmem_st_32x32b_x16(col + 64u, lo);
+        tmem_st_32x32b_x16(col + 32u, lo);
       };
-      emit(v0, nv0, w0, 0);
-      emit(v1, nv1, w1, 1);
+      emit(v0, 0);
+      emit(v1, 1);
       tmem_wait_st();
       l += psum;
       m = mu;
@@ -559,28 +583,49 @@ tree_attn_tc_kernel(const __grid_constant__ CUtensorMap map_q,
       __syncwarp();
       if (lane == 0) tc::mbar_arrive(&sh->p_full[st]);
     }
-    // ---- this CTA's O rows (unnormalised) and the row normaliser
-    if (ok && nblk > 0) {
-      const bool got = tc::mbar_wait(&sh->o_done, 0, abort_flag, status);
-      if ((ok = __all_sync(0xffffffffu, got))) {
-        tc::fence_after_thread_sync();
-        tc::tmem_ld_32x32b_x32(o_addr, o0);
-        tc::tmem_ld_32x32b_x32(o_addr + 32u, o1);
-      }
-    }
     if (!ok) {
-#pragma unroll
-      for (int i = 0; i < 32; ++i) o0[i] = o1[i] = 0.f;
       m = -INFINITY;
       l = 0.f;
     }
-    sh->xchg[nblk & 1][half][r] = l;
+    // ---- merge the two key halves: (m, l) exchange, then this thread's
+    // output columns half*64 .. +63 from both accumulators
+    sh->xchg[0][half][r] = m;
+    sh->xchg[1][half][r] = l;
     tc::mbar_arrive(&sh->fbar);
-    {
-      const bool got = tc::mbar_wait(&sh->fbar, 0, abort_flag, status);
-      ok = __all_sync(0xffffffffu, got) && ok;
+    const bool gf = tc::mbar_wait(&sh->fbar, 0, abort_flag, status);
+    ok = __all_sync(0xffffffffu, gf) && ok;
+    const float mo = sh->xchg[0][half ^ 1][r], lo_ = sh->xchg[1][half ^ 1][r];
+    const float M = fmaxf(m, mo);
+    const float ws = (m == -INFINITY) ? 0.f : ex2_approx(m - M);
+    const float wo = (mo == -INFINITY) ? 0.f : ex2_approx(mo - M);
+    m_row = M;
+    l_row = ws * l + wo * lo_;
+    bool have_o = false;
+    if (ok && nblk > 0) {
+      const bool got = tc::mbar_wait(&sh->o_done, 0, abort_flag, status);
+      if ((ok = __all_sync(0xffffffffu, got))) {
+        have_o = true;
+        tc::fence_after_thread_sync();
+        const uint32_t o_oth = trow + 256u + (uint32_t)((half ^ 1) * 128);
+        float t[32];
+        tc::tmem_ld_32x32b_x32(o_own + (uint32_t)(half * 64), o0);
+        tc::tmem_ld_32x32b_x32(o_oth + (uint32_t)(half * 64), t);
+#pragma unroll
+        for (int i = 0; i < 32; ++i) o0[i] = ws * o0[i] + wo * t[i];
+        tc::tmem_ld_32x32b_x32(o_own + (uint32_t)(half * 64 + 32), o1);
+        tc::tmem_ld_32x32b_x32(o_oth + (uint32_t)(half * 64 + 32), t);
+#pragma unroll
+        for (int i = 0; i < 32; ++i) o1[i] = ws * o1[i] + wo * t[i];
+      }
     }
-    l_row = l + sh->xchg[nblk & 1][half ^ 1][r];
+    if (!have_o) {
+#pragma unroll
+      for (int i = 0; i < 32; ++i) o0[i] = o1[i] = 0.f;
+    }
+    if (!ok) {
+      m_row = -INFINITY;
+      l_row = 0.f;
+    }
   }
 
   // ---------------------------------------------------------------- output
@@ -601,51 +646,61 @@ tree_attn_tc_kernel(const __grid_constant__ CUtensorMap map_q,
       }
     }
   } else {
-    // merge the cluster's chunks: out = sum_c exp2(m_c - M) O_c / sum_c exp2(m_c - M) l_c
+    // merge the cluster's chunks: out = sum_c 2^(m_c - M) O_c / sum_c 2^(m_c - M) l_c
     cg::cluster_group cluster = cg::this_cluster();
-    if (row_warp && half == 0) sh->ml[r] = make_float2(m, l_row);
-    cluster.sync();
     if (row_warp) {
-      float M = -INFINITY;
-      for (int cc = 0; cc < A.NC; ++cc)
-        M = fmaxf(M, cluster.map_shared_rank(&sh->ml[r], cc)->x);
-      float Lsum = 0.f;
-      for (int cc = 0; cc < A.NC; ++cc) {
-        const float2 ml = *cluster.map_shared_rank(&sh->ml[r], cc);
-        Lsum += (ml.x == -INFINITY) ? 0.f : ml.y * exp2f(ml.x - M);
-      }
-      const float f = (m == -INFINITY || !(Lsum > 0.f)) ? 0.f : exp2f(m - M) / Lsum;
+      if (half == 0) sh->ml[r] = make_float2(m_row, l_row);
 #pragma unroll
       for (int i = 0; i < 8; ++i) {
         const int c4 = half * 16 + i;
-        obuf[r * 32 + (c4 ^ (r & 31))] =
-            make_float4(o0[4 * i] * f, o0[4 * i + 1] * f, o0[4 * i + 2] * f, o0[4 * i + 3] * f);
+        obuf[r * 32 + (c4 ^ (r & 31))] = make_float4(o0[4 * i], o0[4 * i + 1], o0[4 * i + 2],
+                                                     o0[4 * i + 3]);
       }
 #pragma unroll
       for (int i = 0; i < 8; ++i) {
         const int c4 = half * 16 + 8 + i;
-        obuf[r * 32 + (c4 ^ (r & 31))] =
-            make_float4(o1[4 * i] * f, o1[4 * i + 1] * f, o1[4 * i + 2] * f, o1[4 * i + 3] * f);
+        obuf[r * 32 + (c4 ^ (r & 31))] = make_float4(o1[4 * i], o1[4 * i + 1], o1[4 * i + 2],
+                                                     o1[4 * i + 3]);
       }
     }
     cluster.sync();
-    // this CTA's share of the rows: sum the cluster's scaled O rows
+    // this CTA's share of the rows, all loads of an item in flight together
     const int R0 = (128 * c) / A.NC, R1 = (128 * (c + 1)) / A.NC;
     for (int idx = threadIdx.x; idx < (R1 - R0) * 32; idx += kAttThreads) {
       const int row = R0 + idx / 32, c4 = idx % 32;
       const int qrow = mt * 128 + row;
       const int node = qrow / A.G, hh = qrow % A.G;
       if (node >= n) continue;
-      float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
-      for (int cc = 0; cc < A.NC; ++cc) {
-        const float4 x = *cluster.map_shared_rank(&obuf[row * 32 + (c4 ^ (row & 31))], cc);
-        acc.x += x.x;
-        acc.y += x.y;
-        acc.z += x.z;
-        acc.w += x.w;
+      float2 ml[kMaxSplit];
+      float4 x[kMaxSplit];
+#pragma unroll
+      for (int cc = 0; cc < kMaxSplit; ++cc) {
+        if (cc < A.NC) {
+          ml[cc] = *cluster.map_shared_rank(&sh->ml[row], cc);
+          x[cc] = *cluster.map_shared_rank(&obuf[row * 32 + (c4 ^ (row & 31))], cc);
+        }
       }
+      float M = -INFINITY;
+#pragma unroll
+      for (int cc = 0; cc < kMaxSplit; ++cc)
+        if (cc < A.NC) M = fmaxf(M, ml[cc].x);
+      float Ls = 0.f;
+      float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll
+      for (int cc = 0; cc < kMaxSplit; ++cc) {
+        if (cc < A.NC && ml[cc].x != -INFINITY) {
+          const float w = ex2_approx(ml[cc].x - M);
+          Ls += w * ml[cc].y;
+          acc.x += w * x[cc].x;
+          acc.y += w * x[cc].y;
+          acc.z += w * x[cc].z;
+          acc.w += w * x[cc].w;
+        }
+      }
+      const float inv = 1.f / Ls;
       *reinterpret_cast<float4*>(A.out + ((size_t)(t0 + node) * A.Hq + g * A.G + hh) * 128 +
-                                 c4 * 4) = acc;
+                                 c4 * 4) =
+          make_float4(acc.x * inv, acc.y * inv, acc.z * inv, acc.w * inv);
     }
     cluster.sync();   // no CTA leaves while others read its shared memory
   }
