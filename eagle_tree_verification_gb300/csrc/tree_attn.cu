@@ -141,6 +141,11 @@ constexpr int kTileBytes = 2 * kHalfBytes;  // 128 rows x 128 bf16
 constexpr int kTargetCtas = 152;        // SMs of a GB300
 constexpr int kMaxSplit = 8;            // cache chunks of one tile: one portable cluster
 constexpr size_t kAttSharedBytes = 5120;
+// cluster merge inside the K/V stage memory: O rows [NC][rows per owner][32]
+// float4 (at most 136 x 512 B), then (max, sum) pairs
+constexpr int kMergeMlOffset = 73728;
+static_assert(kMergeMlOffset >= (128 + kMaxSplit) * 512, "merge rows overlap the (max, sum) pairs");
+static_assert(kMergeMlOffset + (128 + kMaxSplit) * 8 <= 4 * kTileBytes, "merge exceeds the K/V stages");
 // Q, two K stages, two V stages; the merge reuses the K stages for O rows
 constexpr size_t kAttSmem = 1024 + 5 * (size_t)kTileBytes + kAttSharedBytes;
 
@@ -317,19 +322,21 @@ tree_attn_tc_kernel(const __grid_constant__ CUtensorMap map_q,
   auto block_row = [&](int j) {   // first key row of block j in its tensor
     return (j < n_cache_blk) ? kv0 + key_begin + j * kKeyBlk : t0 + (j - n_cache_blk) * kKeyBlk;
   };
-  auto load_kv = [&](int j) {
+  auto load_k = [&](int j) {
     const int st = j & 1;
-    const CUtensorMap* mk = (j < n_cache_blk) ? &map_kc : &map_kt;
-    const CUtensorMap* mv = (j < n_cache_blk) ? &map_vc : &map_vt;
-    const int row = block_row(j);
     unsigned char* kd = k_sm + st * kTileBytes;
-    unsigned char* vd = v_sm + st * kTileBytes;
+    const CUtensorMap* mk = (j < n_cache_blk) ? &map_kc : &map_kt;
     tc::mbar_arrive_expect_tx(&sh->k_full[st], kTileBytes);
-    tc::tma_load_3d(kd, mk, &sh->k_full[st], 0, g, row);
-    tc::tma_load_3d(kd + kHalfBytes, mk, &sh->k_full[st], 64, g, row);
+    tc::tma_load_3d(kd, mk, &sh->k_full[st], 0, g, block_row(j));
+    tc::tma_load_3d(kd + kHalfBytes, mk, &sh->k_full[st], 64, g, block_row(j));
+  };
+  auto load_v = [&](int j) {
+    const int st = j & 1;
+    unsigned char* vd = v_sm + st * kTileBytes;
+    const CUtensorMap* mv = (j < n_cache_blk) ? &map_vc : &map_vt;
     tc::mbar_arrive_expect_tx(&sh->v_full[st], kTileBytes);
-    tc::tma_load_3d(vd, mv, &sh->v_full[st], 0, g, row);
-    tc::tma_load_3d(vd + kHalfBytes, mv, &sh->v_full[st], 64, g, row);
+    tc::tma_load_3d(vd, mv, &sh->v_full[st], 0, g, block_row(j));
+    tc::tma_load_3d(vd + kHalfBytes, mv, &sh->v_full[st], 64, g, block_row(j));
   };
 
   if (threadIdx.x == 0) {
@@ -354,7 +361,10 @@ tree_attn_tc_kernel(const __grid_constant__ CUtensorMap map_q,
       const int node0 = t0 + mt * nodes_per_tile;
       tc::tma_load_3d(q_sm, &map_q, &sh->q_full, 0, g * A.G, node0);
       tc::tma_load_3d(q_sm + kHalfBytes, &map_q, &sh->q_full, 64, g * A.G, node0);
-      for (int j = 0; j < min(2, nblk); ++j) load_kv(j);
+      for (int j = 0; j < min(2, nblk); ++j) {
+        load_k(j);
+        load_v(j);
+      }
     }
   }
   for (int i = threadIdx.x; i < n; i += kAttThreads) sh->par[i] = A.parent[t0 + i];
@@ -379,25 +389,34 @@ tree_attn_tc_kernel(const __grid_constant__ CUtensorMap map_q,
   if (warp == 0) {
     // ------------------------------------------------------------ TMA
     if (lane == 0 && nblk > 2) {
+      // K slots free after S, V slots only after PV: K(j+1) goes out before
+      // V(j), the order in which the two kinds of slot are released
       bool tok = true;
-      uint32_t eph = 0;   // bit st: phase parity of stage st's empty barriers
-      int issued = 2;
-      for (int j = 2; j < nblk && tok; ++j) {
-        const int st = j & 1;
-        if (!(tok = tc::mbar_wait(&sh->k_empty[st], (eph >> st) & 1u, abort_flag, status))) break;
-        if (!(tok = tc::mbar_wait(&sh->v_empty[st], (eph >> st) & 1u, abort_flag, status))) break;
-        eph ^= 1u << st;
-        load_kv(j);
-        ++issued;
+      uint32_t kph = 0, vph = 0;   // bit st: phase parity of the empty barriers
+      int nk = 2, nv = 2;          // blocks issued
+      auto next_k = [&]() -> bool {
+        const int st = nk & 1;
+        if (!tc::mbar_wait(&sh->k_empty[st], (kph >> st) & 1u, abort_flag, status)) return false;
+        kph ^= 1u << st;
+        load_k(nk++);
+        return true;
+      };
+      tok = next_k();
+      while (tok && nv < nblk) {
+        if (nk < nblk && !(tok = next_k())) break;
+        const int st = nv & 1;
+        if (!(tok = tc::mbar_wait(&sh->v_empty[st], (vph >> st) & 1u, abort_flag, status))) break;
+        vph ^= 1u << st;
+        load_v(nv++);
       }
       if (!tok) {
-        // let the copies in flight (at most the last two blocks) land
+        // let the copies in flight (at most the last two of each kind) land
         int never = 0;
         tc::mbar_wait(&sh->q_full, 0, &never, nullptr, 200000000ll);
-        for (int j = max(0, issued - 2); j < issued; ++j) {
+        for (int j = max(0, nk - 2); j < nk; ++j)
           tc::mbar_wait(&sh->k_full[j & 1], (j >> 1) & 1, &never, nullptr, 200000000ll);
+        for (int j = max(0, nv - 2); j < nv; ++j)
           tc::mbar_wait(&sh->v_full[j & 1], (j >> 1) & 1, &never, nullptr, 200000000ll);
-        }
       }
     }
   } else if (warp == 1) {
@@ -646,63 +665,61 @@ tree_attn_tc_kernel(const __grid_constant__ CUtensorMap map_q,
       }
     }
   } else {
-    // merge the cluster's chunks: out = sum_c 2^(m_c - M) O_c / sum_c 2^(m_c - M) l_c
+    // merge the cluster's chunks: out = sum_c 2^(m_c - M) O_c / sum_c 2^(m_c - M) l_c.
+    // Rows [R0(c), R0(c+1)) belong to CTA c; every CTA pushes its partial
+    // rows into the owner's K/V stage memory (free once the whole cluster
+    // is past its key loop), and owners combine from local shared memory.
     cg::cluster_group cluster = cg::this_cluster();
+    const int NC = A.NC;
+    const int RPO = (128 + NC - 1) / NC;            // rows per owner, at most
+    float4* mbuf = reinterpret_cast<float4*>(k_sm);                   // [NC][RPO][32]
+    float2* mlbuf = reinterpret_cast<float2*>(k_sm + kMergeMlOffset); // [NC][RPO]
+    auto row0 = [&](int cc) { return (128 * cc) / NC; };
+    cluster.sync();
     if (row_warp) {
-      if (half == 0) sh->ml[r] = make_float2(m_row, l_row);
+      int owner = 0;
+      while (owner + 1 < NC && row0(owner + 1) <= r) ++owner;
+      const int lrow = r - row0(owner);
+      float4* dst = cluster.map_shared_rank(mbuf, owner) + (size_t)(c * RPO + lrow) * 32;
 #pragma unroll
       for (int i = 0; i < 8; ++i) {
         const int c4 = half * 16 + i;
-        obuf[r * 32 + (c4 ^ (r & 31))] = make_float4(o0[4 * i], o0[4 * i + 1], o0[4 * i + 2],
-                                                     o0[4 * i + 3]);
+        dst[c4 ^ (lrow & 31)] = make_float4(o0[4 * i], o0[4 * i + 1], o0[4 * i + 2], o0[4 * i + 3]);
       }
 #pragma unroll
       for (int i = 0; i < 8; ++i) {
         const int c4 = half * 16 + 8 + i;
-        obuf[r * 32 + (c4 ^ (r & 31))] = make_float4(o1[4 * i], o1[4 * i + 1], o1[4 * i + 2],
-                                                     o1[4 * i + 3]);
+        dst[c4 ^ (lrow & 31)] = make_float4(o1[4 * i], o1[4 * i + 1], o1[4 * i + 2], o1[4 * i + 3]);
       }
+      if (half == 0) cluster.map_shared_rank(mlbuf, owner)[c * RPO + lrow] = make_float2(m_row, l_row);
     }
     cluster.sync();
-    // this CTA's share of the rows, all loads of an item in flight together
-    const int R0 = (128 * c) / A.NC, R1 = (128 * (c + 1)) / A.NC;
+    const int R0 = row0(c), R1 = row0(c + 1);
     for (int idx = threadIdx.x; idx < (R1 - R0) * 32; idx += kAttThreads) {
-      const int row = R0 + idx / 32, c4 = idx % 32;
-      const int qrow = mt * 128 + row;
+      const int lrow = idx / 32, c4 = idx % 32;
+      const int qrow = mt * 128 + R0 + lrow;
       const int node = qrow / A.G, hh = qrow % A.G;
       if (node >= n) continue;
-      float2 ml[kMaxSplit];
-      float4 x[kMaxSplit];
-#pragma unroll
-      for (int cc = 0; cc < kMaxSplit; ++cc) {
-        if (cc < A.NC) {
-          ml[cc] = *cluster.map_shared_rank(&sh->ml[row], cc);
-          x[cc] = *cluster.map_shared_rank(&obuf[row * 32 + (c4 ^ (row & 31))], cc);
-        }
-      }
       float M = -INFINITY;
-#pragma unroll
-      for (int cc = 0; cc < kMaxSplit; ++cc)
-        if (cc < A.NC) M = fmaxf(M, ml[cc].x);
+      for (int cc = 0; cc < NC; ++cc) M = fmaxf(M, mlbuf[cc * RPO + lrow].x);
       float Ls = 0.f;
       float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
-#pragma unroll
-      for (int cc = 0; cc < kMaxSplit; ++cc) {
-        if (cc < A.NC && ml[cc].x != -INFINITY) {
-          const float w = ex2_approx(ml[cc].x - M);
-          Ls += w * ml[cc].y;
-          acc.x += w * x[cc].x;
-          acc.y += w * x[cc].y;
-          acc.z += w * x[cc].z;
-          acc.w += w * x[cc].w;
-        }
+      for (int cc = 0; cc < NC; ++cc) {
+        const float2 ml = mlbuf[cc * RPO + lrow];
+        if (ml.x == -INFINITY) continue;
+        const float w = ex2_approx(ml.x - M);
+        const float4 x = mbuf[(cc * RPO + lrow) * 32 + (c4 ^ (lrow & 31))];
+        Ls += w * ml.y;
+        acc.x += w * x.x;
+        acc.y += w * x.y;
+        acc.z += w * x.z;
+        acc.w += w * x.w;
       }
       const float inv = 1.f / Ls;
       *reinterpret_cast<float4*>(A.out + ((size_t)(t0 + node) * A.Hq + g * A.G + hh) * 128 +
                                  c4 * 4) =
           make_float4(acc.x * inv, acc.y * inv, acc.z * inv, acc.w * inv);
     }
-    cluster.sync();   // no CTA leaves while others read its shared memory
   }
   tc::fence_before_thread_sync();
   __syncthreads();
