@@ -152,7 +152,8 @@ constexpr size_t kAttSmem = 1024 + 5 * (size_t)kTileBytes + kAttSharedBytes;
 struct AttShared {
   uint64_t q_full;
   uint64_t k_full[2], k_empty[2], v_full[2], v_empty[2];
-  uint64_t s_full[2], p_full[2];   // per TMEM slot: S ready / P written
+  uint64_t s_full, s_empty;        // S ready / read by every row warp
+  uint64_t p_full;                 // P written by every row warp
   uint64_t pv_done, o_done, drain;
   uint64_t fbar;                   // row-half exchange after the key loop
   uint32_t tmem_base;
@@ -168,12 +169,14 @@ struct AttPlan {
   int G, MT, NC, CK;  // heads per kv head, row tiles, cache chunks, keys per chunk
 };
 
-AttPlan att_plan(int B, int Hq, int Hkv, int max_nodes, int max_kv) {
+// `split_cap`: the largest number of cache chunks per row tile whose
+// clusters all fit on the GPU at once.
+AttPlan att_plan(int B, int Hq, int Hkv, int max_nodes, int max_kv, int split_cap) {
   AttPlan P;
   P.G = Hq / Hkv;
   P.MT = (max_nodes * P.G + 127) / 128;
   const int tiles = std::max(1, B * Hkv * P.MT);
-  const int nc = std::min(kMaxSplit, std::max(1, kTargetCtas / tiles));
+  const int nc = std::min(split_cap, std::max(1, kTargetCtas / tiles));
   int ck = (max_kv + nc - 1) / nc;
   ck = std::max(256, ((ck + kKeyBlk - 1) / kKeyBlk) * kKeyBlk);
   P.CK = ck;
@@ -265,9 +268,9 @@ __device__ __forceinline__ void tmem_wait_st() {
 // through distributed shared memory.  Two threads per query row, one per
 // half of every key block; each half keeps its own running max, sum and
 // output accumulator, so the halves never wait for each other inside the
-// key loop and are merged once at the end.  TMEM columns: S slots 0 / 128
-// (P overwrites the half's own S columns: bf16 hi at +0, lo at +32), O of
-// key half 0 at 256, of key half 1 at 384.
+// key loop and are merged once at the end.  TMEM columns: S at 0 (refilled
+// with the next block as soon as every row has read it), P at 128 (per key
+// half: bf16 hi at +0, lo at +32), O of key half 0 at 256, of half 1 at 384.
 __global__ void __launch_bounds__(kAttThreads, 1)
 tree_attn_tc_kernel(const __grid_constant__ CUtensorMap map_q,
                     const __grid_constant__ CUtensorMap map_kc,
@@ -346,9 +349,10 @@ tree_attn_tc_kernel(const __grid_constant__ CUtensorMap map_q,
       tc::mbar_init(&sh->k_empty[i], 1);
       tc::mbar_init(&sh->v_full[i], 1);
       tc::mbar_init(&sh->v_empty[i], 1);
-      tc::mbar_init(&sh->s_full[i], 1);
-      tc::mbar_init(&sh->p_full[i], active_warps);
     }
+    tc::mbar_init(&sh->s_full, 1);
+    tc::mbar_init(&sh->s_empty, active_warps);
+    tc::mbar_init(&sh->p_full, active_warps);
     tc::mbar_init(&sh->pv_done, 1);
     tc::mbar_init(&sh->o_done, 1);
     tc::mbar_init(&sh->drain, 1);
@@ -427,7 +431,7 @@ tree_attn_tc_kernel(const __grid_constant__ CUtensorMap map_q,
         const uint32_t idesc_o = tc::idesc_bf16_f32(128, 128) | (1u << 16);  // B is MN-major
         const uint32_t q_addr = tc::smem_u32(q_sm);
         bool mok = tc::mbar_wait(&sh->q_full, 0, abort_flag, status);
-        uint32_t kph = 0, vph = 0, pph = 0;   // bit st: phase parity per stage / slot
+        uint32_t kph = 0, vph = 0;   // bit st: phase parity per stage
         auto issue_s = [&](int j) -> bool {
           const int st = j & 1;
           if (!tc::mbar_wait(&sh->k_full[st], (kph >> st) & 1u, abort_flag, status)) return false;
@@ -437,19 +441,22 @@ tree_attn_tc_kernel(const __grid_constant__ CUtensorMap map_q,
 #pragma unroll
           for (int k16 = 0; k16 < 8; ++k16) {
             const uint32_t off = (uint32_t)((k16 >> 2) * kHalfBytes + (k16 & 3) * 32);
-            tc::mma_f16(tmem + (uint32_t)(st * 128), tc::desc_kmajor_sw128(q_addr + off),
+            tc::mma_f16(tmem, tc::desc_kmajor_sw128(q_addr + off),
                         tc::desc_kmajor_sw128(k_addr + off), idesc_s, k16 > 0 ? 1u : 0u);
           }
-          tc::mma_commit(&sh->s_full[st]);
+          tc::mma_commit(&sh->s_full);
           tc::mma_commit(&sh->k_empty[st]);
           return true;
         };
         if (mok) mok = issue_s(0);
-        if (mok && nblk > 1) mok = issue_s(1);
         for (int j = 0; j < nblk && mok; ++j) {
           const int st = j & 1;
-          if (!(mok = tc::mbar_wait(&sh->p_full[st], (pph >> st) & 1u, abort_flag, status))) break;
-          pph ^= 1u << st;
+          if (j + 1 < nblk) {
+            // the next S goes into the slot as soon as every row has read this one
+            if (!(mok = tc::mbar_wait(&sh->s_empty, (uint32_t)(j & 1), abort_flag, status))) break;
+            if (!(mok = issue_s(j + 1))) break;
+          }
+          if (!(mok = tc::mbar_wait(&sh->p_full, (uint32_t)(j & 1), abort_flag, status))) break;
           if (!(mok = tc::mbar_wait(&sh->v_full[st], (vph >> st) & 1u, abort_flag, status))) break;
           vph ^= 1u << st;
           tc::fence_after_thread_sync();
@@ -462,7 +469,7 @@ tree_attn_tc_kernel(const __grid_constant__ CUtensorMap map_q,
             for (int part = 0; part < 2; ++part) {
 #pragma unroll
               for (int kk = 0; kk < 4; ++kk) {
-                const uint32_t a_tm = tmem + (uint32_t)(st * 128 + h * 64 + part * 32 + kk * 8);
+                const uint32_t a_tm = tmem + (uint32_t)(128 + h * 64 + part * 32 + kk * 8);
                 const uint32_t key = (uint32_t)(h * 64 + kk * 16);
                 mma_f16_tmem_a(tmem + 256u + (uint32_t)(h * 128), a_tm,
                                desc_mnmajor_sw128(v_addr + key * 128u, kHalfBytes), idesc_o,
@@ -472,11 +479,6 @@ tree_attn_tc_kernel(const __grid_constant__ CUtensorMap map_q,
           }
           tc::mma_commit(&sh->pv_done);
           tc::mma_commit(&sh->v_empty[st]);
-          if (j + 2 < nblk) {
-            // slot st is free once this PV has read P
-            if (!(mok = tc::mbar_wait(&sh->pv_done, (uint32_t)(j & 1), abort_flag, status))) break;
-            if (!(mok = issue_s(j + 2))) break;
-          }
         }
         if (mok) tc::mma_commit(&sh->o_done);
       }
@@ -511,21 +513,22 @@ tree_attn_tc_kernel(const __grid_constant__ CUtensorMap map_q,
     const uint32_t trow = tmem + ((uint32_t)(quad * 32) << 16);
     const uint32_t o_own = trow + 256u + (uint32_t)(half * 128);   // this key half's O
     float m = -INFINITY, l = 0.f;   // this key half's running max (log2 units) and sum
-    uint32_t sph = 0;   // bit st: phase parity of s_full[st]
     for (int j = 0; j < nblk && ok; ++j) {
-      const int st = j & 1;
-      const bool got = tc::mbar_wait(&sh->s_full[st], (sph >> st) & 1u, abort_flag, status);
+      const bool got = tc::mbar_wait(&sh->s_full, (uint32_t)(j & 1), abort_flag, status);
       if (!(ok = __all_sync(0xffffffffu, got))) break;
-      sph ^= 1u << st;
       tc::fence_after_thread_sync();
       const bool tree_blk = j >= n_cache_blk;
       const int tb = tree_blk ? j - n_cache_blk : 0;          // tree block 0 or 1
       const int key0 = (tree_blk ? tb * kKeyBlk : key_begin + j * kKeyBlk) + half * 64;
       const int key_lim = tree_blk ? n : key_end;
-      const uint32_t s_addr = trow + (uint32_t)(st * 128 + half * 64);
+      const uint32_t s_addr = trow + (uint32_t)(half * 64);
       float v0[32], v1[32];
       tc::tmem_ld_32x32b_x32(s_addr, v0);
       tc::tmem_ld_32x32b_x32(s_addr + 32u, v1);
+      // the S slot may take the next block
+      tc::fence_before_thread_sync();
+      __syncwarp();
+      if (lane == 0) tc::mbar_arrive(&sh->s_empty);
       // bitset words for key columns half*64 .. +63 of tree block tb (static indices)
       const uint32_t w0 = !tree_blk ? 0xffffffffu
                           : tb ? (half ? anc[6] : anc[4]) : (half ? anc[2] : anc[0]);
@@ -552,12 +555,14 @@ tree_attn_tc_kernel(const __grid_constant__ CUtensorMap map_q,
       const bool first = (m == -INFINITY);
       const bool rescale = !first && (mn > m + kRescaleLog2);
       const float mu = (first || rescale) ? mn : m;     // reference max for this block's P
-      if (__any_sync(0xffffffffu, rescale)) {
-        // O_h must hold every earlier block (the S of this block was issued
-        // after the PV two blocks back, so only the previous PV may still run)
+      if (j >= 1) {
+        // the previous PV has read P and finished O (every earlier PV was
+        // waited for one block before)
         const bool g4 = tc::mbar_wait(&sh->pv_done, (uint32_t)((j - 1) & 1), abort_flag, status);
         if (!(ok = __all_sync(0xffffffffu, g4))) break;
         tc::fence_after_thread_sync();
+      }
+      if (__any_sync(0xffffffffu, rescale)) {
         const float f = rescale ? ex2_approx(m - mu) : 1.f;
         float o[32];
 #pragma unroll
@@ -589,7 +594,7 @@ tree_attn_tc_kernel(const __grid_constant__ CUtensorMap map_q,
           lo[i] = __byte_perm(__float_as_uint(r0), __float_as_uint(r1), 0x7632);
           psum += p0 + p1;
         }
-        const uint32_t col = trow + (uint32_t)(st * 128 + half * 64 + cc * 16);
+        const uint32_t col = trow + (uint32_t)(128 + half * 64 + cc * 16);
         tmem_st_32x32b_x16(col, hi);
         tmem_st_32x32b_x16(col + 32u, lo);
       };
@@ -600,7 +605,7 @@ tree_attn_tc_kernel(const __grid_constant__ CUtensorMap map_q,
       m = mu;
       tc::fence_before_thread_sync();
       __syncwarp();
-      if (lane == 0) tc::mbar_arrive(&sh->p_full[st]);
+      if (lane == 0) tc::mbar_arrive(&sh->p_full);
     }
     if (!ok) {
       m = -INFINITY;
@@ -757,6 +762,38 @@ bool make_map_3d(CUtensorMap* map, const void* ptr, int rows, int heads, int box
              CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
+// Largest cluster size <= kMaxSplit such that `tiles` clusters of the
+// attention kernel are resident at once (one wave), per device.
+int split_cap_for(int tiles) {
+  static int cache[64][kMaxSplit + 1];
+  static bool filled[64];
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return 1;
+  if (!filled[dev]) {
+    for (int nc = 1; nc <= kMaxSplit; ++nc) {
+      cudaLaunchConfig_t cfg = {};
+      cfg.gridDim = dim3((unsigned)nc);
+      cfg.blockDim = dim3(kAttThreads);
+      cfg.dynamicSmemBytes = kAttSmem;
+      cudaLaunchAttribute at[1];
+      at[0].id = cudaLaunchAttributeClusterDimension;
+      at[0].val.clusterDim.x = (unsigned)nc;
+      at[0].val.clusterDim.y = 1;
+      at[0].val.clusterDim.z = 1;
+      cfg.attrs = at;
+      cfg.numAttrs = 1;
+      int q = 0;
+      if (cudaOccupancyMaxActiveClusters(&q, tree_attn_tc_kernel, &cfg) != cudaSuccess) q = 0;
+      cache[dev][nc] = q;
+    }
+    (void)cudaGetLastError();
+    filled[dev] = true;
+  }
+  int nc = kMaxSplit;
+  while (nc > 1 && cache[dev][nc] < tiles) --nc;
+  return nc;
+}
+
 bool tc_shape_ok(eagle_dtype dtype, int Hq, int Hkv, int D) {
   if (dtype != EAGLE_BF16 || D != 128) return false;
   const int G = Hq / Hkv;
@@ -806,7 +843,16 @@ extern "C" eagle_status eagle_tree_attn(eagle_dtype dtype, int B, int T, int Hq,
   const uintptr_t align = (uintptr_t)d_q | (uintptr_t)d_k_tree | (uintptr_t)d_v_tree |
                           (uintptr_t)d_k_cache | (uintptr_t)d_v_cache | (uintptr_t)d_out;
   if (tc_shape_ok(dtype, Hq, Hkv, D) && (align & 15) == 0) {
-    const AttPlan P = att_plan(B, Hq, Hkv, max_nodes, max_kv);
+    static bool attr = false;
+    if (!attr) {
+      if (cudaFuncSetAttribute(tree_attn_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                               (int)kAttSmem) != cudaSuccess)
+        return EAGLE_ERR_CUDA;
+      attr = true;
+    }
+    const int G = Hq / Hkv;
+    const int tiles = B * Hkv * ((max_nodes * G + 127) / 128);
+    const AttPlan P = att_plan(B, Hq, Hkv, max_nodes, max_kv, split_cap_for(tiles));
     CUtensorMap mq, mkc, mvc, mkt, mvt;
     const void* kc = (kv_rows > 0) ? d_k_cache : d_k_tree;   // never read when empty
     const void* vc = (kv_rows > 0) ? d_v_cache : d_v_tree;
@@ -817,13 +863,6 @@ extern "C" eagle_status eagle_tree_attn(eagle_dtype dtype, int B, int T, int Hq,
         !make_map_3d(&mkt, d_k_tree, T, Hkv, 1, kKeyBlk) ||
         !make_map_3d(&mvt, d_v_tree, T, Hkv, 1, kKeyBlk))
       return EAGLE_ERR_CUDA;
-    static bool attr = false;
-    if (!attr) {
-      if (cudaFuncSetAttribute(tree_attn_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                               (int)kAttSmem) != cudaSuccess)
-        return EAGLE_ERR_CUDA;
-      attr = true;
-    }
     AttParams A;
     A.B = B;
     A.Hq = Hq;
