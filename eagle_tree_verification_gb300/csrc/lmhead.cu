@@ -224,60 +224,96 @@ lmhead_finalize_kernel(int T, int V, float temperature, const Partial* __restric
 // tcgen05 path
 //
 // MMA D[t, v] = sum_k h[t, k] W[v, k]: M = 128 tree rows (TMEM lanes; rows at
-// or past T are don't-care), N = one vocabulary block of up to 256 rows, K in
-// 64-element chunks (128-byte-swizzled K-major tiles).  Each CTA owns a
-// balanced slice of the vocabulary in units of 32 rows, cut into blocks of at
-// most 256 rows; two blocks (512 TMEM columns) are accumulated per pass over
-// K.  A W stage is one chunk of one block (<= 32 KB, TMA boxes of 32 rows);
-// an h stage is one chunk of the real tree rows (T rounded up to 8).
+// or past T are don't-care), N = one vocabulary block of up to `blk` rows
+// (128 or 256), K in 64-element chunks (128-byte-swizzled K-major tiles).
+// Each CTA owns a balanced slice of the vocabulary in units of 32 rows, cut
+// into blocks.  Two TMEM accumulators alternate between blocks, so the
+// softmax epilogue of one block overlaps the MMAs of the next.  A W stage is one chunk
+// of one block (<= blk x 128 bytes, TMA boxes of 32 rows); an h stage is one
+// chunk of the real tree rows (T rounded up to 8).  W never depends on an
+// earlier kernel, so the first W stages are requested before the kernel
+// waits for its predecessor.
 // ---------------------------------------------------------------------------
-constexpr int kTcThreads = 192;   // warp 0 TMA, warp 1 MMA, warps 2-5 epilogue
+constexpr int kTcThreads = 320;   // warp 0 TMA, warp 1 MMA, warps 2-9 epilogue
+constexpr int kEpiWarps = 8;      // two per TMEM lane quarter, one per column half
 constexpr int kBK = 64;           // bf16 per 128-byte swizzled row (one chunk)
 constexpr int kUnit = 32;         // vocabulary rows per TMA box
-constexpr int kBlkMax = 256;      // vocabulary rows per MMA (its N)
-constexpr int kGroupBlocks = 2;   // blocks per pass over K: 2 x 256 TMEM columns
+constexpr int kBlkMax = 256;      // vocabulary rows per MMA (its N), at most
 constexpr int kHStages = 4;
-constexpr int kMaxWStages = 8;
-constexpr int kWStageBytes = kBlkMax * 128;              // 32 KB
+constexpr int kMaxWStages = 12;
 constexpr size_t kSmemLimit = 227 * 1024;
-constexpr size_t kTcSharedBytes = 512;
+constexpr size_t kTcSharedBytes = 1024 + 2 * 128 * 16;
 
 struct TcShared {
   uint64_t h_full[kHStages], h_empty[kHStages];
   uint64_t w_full[kMaxWStages], w_empty[kMaxWStages];
-  uint64_t tmem_full, tmem_empty, drain;
+  uint64_t tmem_full[2], tmem_empty[2], xbar, drain;
   uint32_t tmem_base;
   int abort_flag;
   int consumed_w, consumed_h;
+  Partial xchg[128];   // column half 1's partial of every row
 };
 
 struct TcLayout {
-  int t_pad, h_stage_bytes, w_stages;
+  int t_pad, h_stage_bytes, blk, w_stage_bytes, w_stages;
   size_t smem;
 };
 
-TcLayout tc_layout(int T) {
+// `slice_rows`: vocabulary rows of the largest CTA slice.
+TcLayout tc_layout(int T, int slice_rows) {
   TcLayout L;
   L.t_pad = ((T + 7) / 8) * 8;
   L.h_stage_bytes = L.t_pad * 128;
+  // 256-row blocks: narrower MMAs cost more shared-memory reads per W byte
+  // than the overlap of a short slice's epilogue gains
+  (void)slice_rows;
+  L.blk = kBlkMax;
+  L.w_stage_bytes = L.blk * 128;
   const size_t fixed = 1024 + (size_t)kHStages * L.h_stage_bytes + kTcSharedBytes;
-  L.w_stages = (int)std::min<size_t>(kMaxWStages, (kSmemLimit - fixed) / kWStageBytes);
-  L.smem = fixed + (size_t)L.w_stages * kWStageBytes;
+  L.w_stages = (int)std::min<size_t>(kMaxWStages, (kSmemLimit - fixed) / L.w_stage_bytes);
+  L.smem = fixed + (size_t)L.w_stages * L.w_stage_bytes;
   return L;
+}
+
+// 2^x by the SFU's approximate exponential (relative error about 2^-22;
+// subnormal results flush to zero).
+__device__ __forceinline__ float ex2_approx(float x) {
+  float y;
+  asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+  return y;
+}
+
+// Merge partial b into a (same row, disjoint vocabulary): the max with the
+// lowest index on ties; the loser's max competes for second place.
+__device__ __forceinline__ void merge_partial(Partial& a, const Partial& b, float k2) {
+  if (b.m == -INFINITY) return;
+  if (a.m == -INFINITY) {
+    a = b;
+    return;
+  }
+  const bool b_wins = (b.m > a.m) || (b.m == a.m && b.idx < a.idx);
+  const Partial& w = b_wins ? b : a;
+  const Partial& o = b_wins ? a : b;
+  Partial r;
+  r.m = w.m;
+  r.idx = w.idx;
+  r.second = fmaxf(w.second, o.m);
+  r.s = w.s + o.s * ex2_approx((o.m - w.m) * k2);
+  a = r;
 }
 
 __global__ void __launch_bounds__(kTcThreads, 1)
 lmhead_tc_kernel(const __grid_constant__ CUtensorMap map_h, const __grid_constant__ CUtensorMap map_w,
                  int T, int H, int V, float temperature, float* __restrict__ z_out,
-                 Partial* __restrict__ part, int n_units, int h_stage_bytes, int w_stages,
-                 int* status) {
-  pdl_begin();
+                 Partial* __restrict__ part, int n_units, int h_stage_bytes, int blk_max,
+                 int w_stages, int* status) {
   extern __shared__ __align__(1024) unsigned char smem_raw[];
   unsigned char* base = reinterpret_cast<unsigned char*>(
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~(uintptr_t)1023);
   unsigned char* h_smem = base;
   unsigned char* w_smem = base + kHStages * h_stage_bytes;
-  TcShared* sh = reinterpret_cast<TcShared*>(w_smem + (size_t)w_stages * kWStageBytes);
+  const int w_stage_bytes = blk_max * 128;
+  TcShared* sh = reinterpret_cast<TcShared*>(w_smem + (size_t)w_stages * w_stage_bytes);
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int G = gridDim.x;
@@ -285,10 +321,11 @@ lmhead_tc_kernel(const __grid_constant__ CUtensorMap map_h, const __grid_constan
   const int u0 = (int)((long long)n_units * blockIdx.x / G);
   const int u1 = (int)((long long)n_units * (blockIdx.x + 1) / G);
   const int r_begin = u0 * kUnit, r_end = u1 * kUnit;
-  const int n_blocks = (r_end - r_begin + kBlkMax - 1) / kBlkMax;
-  const int n_groups = (n_blocks + kGroupBlocks - 1) / kGroupBlocks;
+  const int n_blocks = (r_end - r_begin + blk_max - 1) / blk_max;
   const int KB = (H + kBK - 1) / kBK;
-  auto blk_rows = [&](int blk) { return min(kBlkMax, r_end - (r_begin + blk * kBlkMax)); };
+  auto blk_rows = [&](int blk) { return min(blk_max, r_end - (r_begin + blk * blk_max)); };
+  // W stages requested before waiting for the previous kernel
+  const int w_early = min(w_stages, n_blocks * KB);
 
   if (threadIdx.x == 0) {
     for (int i = 0; i < kHStages; ++i) {
@@ -299,22 +336,35 @@ lmhead_tc_kernel(const __grid_constant__ CUtensorMap map_h, const __grid_constan
       tc::mbar_init(&sh->w_full[i], 1);
       tc::mbar_init(&sh->w_empty[i], 1);
     }
-    tc::mbar_init(&sh->tmem_full, 1);
-    tc::mbar_init(&sh->tmem_empty, 4);
+    for (int i = 0; i < 2; ++i) {
+      tc::mbar_init(&sh->tmem_full[i], 1);
+      tc::mbar_init(&sh->tmem_empty[i], kEpiWarps);
+    }
+    tc::mbar_init(&sh->xbar, 32 * kEpiWarps);
     tc::mbar_init(&sh->drain, 1);
     sh->abort_flag = 0;
     sh->consumed_w = 0;
     sh->consumed_h = 0;
     tc::fence_barrier_init();
+    tc::prefetch_tensormap(&map_h);
+    tc::prefetch_tensormap(&map_w);
+    // the first W stages: block 0, chunks 0 .. w_early-1 (the loop's order)
+    const uint64_t pol_w = tc::policy_evict_first();
+    for (int i = 0; i < w_early; ++i) {
+      const int blk = i / KB, kb = i % KB;
+      const int rows = blk_rows(blk);
+      tc::mbar_arrive_expect_tx(&sh->w_full[i], (uint32_t)(rows * 128));
+      unsigned char* dst = w_smem + (size_t)i * w_stage_bytes;
+      for (int u = 0; u < rows; u += kUnit)
+        tc::tma_load_2d_hint(dst + u * 128, &map_w, &sh->w_full[i], kb * kBK,
+                             r_begin + blk * blk_max + u, pol_w);
+    }
   }
   if (warp == 1) {
     tc::tmem_alloc(&sh->tmem_base, 512);
     tc::tmem_relinquish();
   }
-  if (warp == 0 && lane == 0) {
-    tc::prefetch_tensormap(&map_h);
-    tc::prefetch_tensormap(&map_w);
-  }
+  pdl_begin();   // h (and the outputs) follow the previous kernel
   tc::fence_before_thread_sync();
   __syncthreads();
   tc::fence_after_thread_sync();
@@ -329,8 +379,9 @@ lmhead_tc_kernel(const __grid_constant__ CUtensorMap map_h, const __grid_constan
       int hs = 0, ws = 0, issued_h = 0, issued_w = 0;
       uint32_t hph = 0, wph = 0;
       bool ok = true;
-      for (int g = 0; g < n_groups && ok; ++g) {
-        const int b0 = g * kGroupBlocks, b1 = min(n_blocks, b0 + kGroupBlocks);
+      for (int blk = 0; blk < n_blocks && ok; ++blk) {
+        const int row0 = r_begin + blk * blk_max;
+        const int rows = blk_rows(blk);
         for (int kb = 0; kb < KB && ok; ++kb) {
           if (!(ok = tc::mbar_wait(&sh->h_empty[hs], hph ^ 1, abort_flag, status))) break;
           tc::mbar_arrive_expect_tx(&sh->h_full[hs], (uint32_t)h_stage_bytes);
@@ -338,24 +389,23 @@ lmhead_tc_kernel(const __grid_constant__ CUtensorMap map_h, const __grid_constan
                                pol_h);
           ++issued_h;
           if (++hs == kHStages) { hs = 0; hph ^= 1; }
-          for (int blk = b0; blk < b1; ++blk) {
-            const int row0 = r_begin + blk * kBlkMax;
-            const int rows = blk_rows(blk);
+          if (issued_w >= w_early) {
             if (!(ok = tc::mbar_wait(&sh->w_empty[ws], wph ^ 1, abort_flag, status))) break;
             tc::mbar_arrive_expect_tx(&sh->w_full[ws], (uint32_t)(rows * 128));
-            unsigned char* dst = w_smem + (size_t)ws * kWStageBytes;
+            unsigned char* dst = w_smem + (size_t)ws * w_stage_bytes;
             for (int u = 0; u < rows; u += kUnit)
               tc::tma_load_2d_hint(dst + u * 128, &map_w, &sh->w_full[ws], kb * kBK, row0 + u,
                                    pol_w);
-            ++issued_w;
-            if (++ws == w_stages) { ws = 0; wph ^= 1; }
           }
+          ++issued_w;
+          if (++ws == w_stages) { ws = 0; wph ^= 1; }
         }
       }
       if (!ok) {
         // let every copy still in flight land before the CTA exits
         int never = 0;
-        for (int i = *(volatile int*)&sh->consumed_w; i < issued_w; ++i)
+        const int issued = max(issued_w, w_early);
+        for (int i = *(volatile int*)&sh->consumed_w; i < issued; ++i)
           tc::mbar_wait(&sh->w_full[i % w_stages], (i / w_stages) & 1, &never, nullptr,
                         200000000ll);
         for (int i = *(volatile int*)&sh->consumed_h; i < issued_h; ++i)
@@ -367,37 +417,36 @@ lmhead_tc_kernel(const __grid_constant__ CUtensorMap map_h, const __grid_constan
     // ------------------------------------------------------------ MMA issuer
     if (lane == 0) {
       int hs = 0, ws = 0;
-      uint32_t hph = 0, wph = 0, tph = 0;
+      uint32_t hph = 0, wph = 0, tph = 0;   // tph bit b: phase of accumulator b
       bool ok = true;
-      for (int g = 0; g < n_groups && ok; ++g) {
-        const int b0 = g * kGroupBlocks, b1 = min(n_blocks, b0 + kGroupBlocks);
-        if (!(ok = tc::mbar_wait(&sh->tmem_empty, tph ^ 1, abort_flag, status))) break;
-        tph ^= 1;
+      for (int blk = 0; blk < n_blocks && ok; ++blk) {
+        const int ab = blk & 1;
+        if (!(ok = tc::mbar_wait(&sh->tmem_empty[ab], ((tph >> ab) & 1u) ^ 1u, abort_flag,
+                                 status)))
+          break;
+        tph ^= 1u << ab;
         tc::fence_after_thread_sync();
+        const uint32_t idesc = tc::idesc_bf16_f32(128, blk_rows(blk));
+        const uint32_t d = tmem + (uint32_t)(ab * kBlkMax);
         for (int kb = 0; kb < KB && ok; ++kb) {
           if (!(ok = tc::mbar_wait(&sh->h_full[hs], hph, abort_flag, status))) break;
+          if (!(ok = tc::mbar_wait(&sh->w_full[ws], wph, abort_flag, status))) break;
+          tc::fence_after_thread_sync();
           const uint32_t a_base = tc::smem_u32(h_smem + hs * h_stage_bytes);
-          for (int blk = b0; blk < b1; ++blk) {
-            if (!(ok = tc::mbar_wait(&sh->w_full[ws], wph, abort_flag, status))) break;
-            tc::fence_after_thread_sync();
-            const uint32_t b_base = tc::smem_u32(w_smem + (size_t)ws * kWStageBytes);
-            const uint32_t idesc = tc::idesc_bf16_f32(128, blk_rows(blk));
-            const uint32_t d = tmem + (uint32_t)((blk - b0) * kBlkMax);
+          const uint32_t b_base = tc::smem_u32(w_smem + (size_t)ws * w_stage_bytes);
 #pragma unroll
-            for (int k16 = 0; k16 < kBK / 16; ++k16)
-              tc::mma_f16(d, tc::desc_kmajor_sw128(a_base + k16 * 32),
-                          tc::desc_kmajor_sw128(b_base + k16 * 32), idesc,
-                          (kb > 0 || k16 > 0) ? 1u : 0u);
-            tc::mma_commit(&sh->w_empty[ws]);
-            *(volatile int*)&sh->consumed_w += 1;
-            if (++ws == w_stages) { ws = 0; wph ^= 1; }
-          }
-          if (!ok) break;
+          for (int k16 = 0; k16 < kBK / 16; ++k16)
+            tc::mma_f16(d, tc::desc_kmajor_sw128(a_base + k16 * 32),
+                        tc::desc_kmajor_sw128(b_base + k16 * 32), idesc,
+                        (kb > 0 || k16 > 0) ? 1u : 0u);
+          tc::mma_commit(&sh->w_empty[ws]);
           tc::mma_commit(&sh->h_empty[hs]);
+          *(volatile int*)&sh->consumed_w += 1;
           *(volatile int*)&sh->consumed_h += 1;
+          if (++ws == w_stages) { ws = 0; wph ^= 1; }
           if (++hs == kHStages) { hs = 0; hph ^= 1; }
         }
-        if (ok) tc::mma_commit(&sh->tmem_full);
+        if (ok) tc::mma_commit(&sh->tmem_full[ab]);
       }
       // every MMA issued by this thread has finished before TMEM is freed
       tc::mma_commit(&sh->drain);
@@ -407,82 +456,102 @@ lmhead_tc_kernel(const __grid_constant__ CUtensorMap map_h, const __grid_constan
   } else {
     // ------------------------------------------------------------ epilogue
     const int quad = warp & 3;
-    const int t = quad * 32 + lane;   // tree row held by this thread
+    const int chalf = (warp - 2) >> 2;   // second or first half of every block's columns
+    const int t = quad * 32 + lane;      // tree row held by this thread
     const bool row_ok = t < T;
+    const bool quad_live = quad * 32 < T;   // warp-uniform
     const float k2 = 1.4426950408889634f / temperature;   // log2(e) / temperature
     const bool vec = ((V & 3) == 0);
-    float m = -INFINITY, s = 0.f, second = -INFINITY;
-    int idx = 0x7fffffff;
+    Partial p;
+    p.m = -INFINITY;
+    p.s = 0.f;
+    p.second = -INFINITY;
+    p.idx = 0x7fffffff;
     bool bad = false;
     uint32_t tph = 0;
-    for (int g = 0; g < n_groups; ++g) {
-      const int b0 = g * kGroupBlocks, b1 = min(n_blocks, b0 + kGroupBlocks);
+    for (int blk = 0; blk < n_blocks; ++blk) {
+      const int ab = blk & 1;
+      const int rows = blk_rows(blk);
       // every lane waits; the warp proceeds only if all of them saw the phase
-      const bool got = tc::mbar_wait(&sh->tmem_full, tph, abort_flag, status);
+      const bool got = tc::mbar_wait(&sh->tmem_full[ab], (tph >> ab) & 1u, abort_flag, status);
       if (!__all_sync(0xffffffffu, got)) break;
-      tph ^= 1;
+      tph ^= 1u << ab;
       tc::fence_after_thread_sync();
-      for (int blk = b0; blk < b1; ++blk) {
-        const int rows = blk_rows(blk);
-        for (int c = 0; c < rows; c += 32) {
-          float v[32];
-          tc::tmem_ld_32x32b_x32(tmem + ((uint32_t)(quad * 32) << 16) +
-                                     (uint32_t)((blk - b0) * kBlkMax + c), v);
-          const int vb = r_begin + blk * kBlkMax + c;
-          const int nvalid = min(min(32, rows - c), V - vb);
-          if (!row_ok || nvalid <= 0) continue;
-          if (z_out) {
-            float* dst = z_out + (size_t)t * V + vb;
-            if (vec && nvalid == 32) {
+      const int half_cols = blk_max / 2;
+      for (int c = chalf * half_cols; c < (chalf + 1) * half_cols && c < rows && quad_live;
+           c += 32) {
+        float v[32];
+        tc::tmem_ld_32x32b_x32(tmem + ((uint32_t)(quad * 32) << 16) +
+                                   (uint32_t)(ab * kBlkMax + c), v);
+        const int vb = r_begin + blk * blk_max + c;
+        const int nvalid = min(min(32, rows - c), V - vb);
+        if (!row_ok || nvalid <= 0) continue;
+        bool fin = true;
+        if (nvalid == 32) {
 #pragma unroll
-              for (int i = 0; i < 32; i += 4)
-                *reinterpret_cast<float4*>(dst + i) = make_float4(v[i], v[i + 1], v[i + 2], v[i + 3]);
-            } else {
-#pragma unroll
-              for (int i = 0; i < 32; ++i)
-                if (i < nvalid) dst[i] = v[i];
-            }
-          }
-          float cm = -INFINITY, cs = -INFINITY;
-          int ci = 0;
+          for (int i = 0; i < 32; ++i) fin &= fabsf(v[i]) < INFINITY;
+        } else {
+          // ragged end of the vocabulary: only real entries count
 #pragma unroll
           for (int i = 0; i < 32; ++i) {
-            const float x = (i < nvalid) ? v[i] : -INFINITY;
-            if (i < nvalid) bad |= !isfinite(x);
-            if (x > cm) {
-              cs = cm;
-              cm = x;
-              ci = i;
-            } else if (x > cs) {
-              cs = x;
-            }
+            if (i < nvalid) fin &= fabsf(v[i]) < INFINITY;
+            else v[i] = -INFINITY;
           }
-          if (cm > m) {
-            second = fmaxf(m, cs);
-            s = (m == -INFINITY) ? 0.f : s * exp2f((m - cm) * k2);
-            m = cm;
-            idx = vb + ci;
-          } else {
-            second = fmaxf(second, cm);
-          }
-          float acc = 0.f;
-#pragma unroll
-          for (int i = 0; i < 32; ++i)
-            if (i < nvalid) acc += exp2f((v[i] - m) * k2);
-          s += acc;
         }
+        bad |= !fin;
+        if (z_out) {
+          float* dst = z_out + (size_t)t * V + vb;
+          if (vec && nvalid == 32) {
+#pragma unroll
+            for (int i = 0; i < 32; i += 4)
+              *reinterpret_cast<float4*>(dst + i) = make_float4(v[i], v[i + 1], v[i + 2], v[i + 3]);
+          } else {
+#pragma unroll
+            for (int i = 0; i < 32; ++i)
+              if (i < nvalid) dst[i] = v[i];
+          }
+        }
+        float cm = -INFINITY, cs = -INFINITY;
+        int ci = 0;
+#pragma unroll
+        for (int i = 0; i < 32; ++i) {
+          const float x = v[i];
+          if (x > cm) {
+            cs = cm;
+            cm = x;
+            ci = i;
+          } else if (x > cs) {
+            cs = x;
+          }
+        }
+        if (cm > p.m) {
+          p.second = fmaxf(p.m, cs);
+          p.s = (p.m == -INFINITY) ? 0.f : p.s * ex2_approx((p.m - cm) * k2);
+          p.m = cm;
+          p.idx = vb + ci;
+        } else {
+          p.second = fmaxf(p.second, cm);
+        }
+        const float mk = p.m * k2;
+        float a0 = 0.f, a1 = 0.f;
+#pragma unroll
+        for (int i = 0; i < 32; i += 2) {
+          a0 += ex2_approx(fmaf(v[i], k2, -mk));
+          a1 += ex2_approx(fmaf(v[i + 1], k2, -mk));
+        }
+        p.s += a0 + a1;
       }
       tc::fence_before_thread_sync();
       __syncwarp();
-      if (lane == 0) tc::mbar_arrive(&sh->tmem_empty);
+      if (lane == 0) tc::mbar_arrive(&sh->tmem_empty[ab]);
     }
     if (bad) fail(status, EAGLE_ERR_NUMERIC);
-    if (row_ok) {
-      Partial p;
-      p.m = m;
-      p.s = s;
-      p.second = second;
-      p.idx = (m == -INFINITY) ? 0x7fffffff : idx;
+    // the two column halves of every row: half 1 hands its partial to half 0
+    if (chalf == 1) sh->xchg[t] = p;
+    tc::mbar_arrive(&sh->xbar);
+    const bool gx = tc::mbar_wait(&sh->xbar, 0, abort_flag, status);
+    if (chalf == 0 && row_ok && gx) {
+      merge_partial(p, sh->xchg[t], k2);
       part[(size_t)t * G + blockIdx.x] = p;
     }
   }
@@ -576,16 +645,17 @@ extern "C" eagle_status eagle_lmhead_softmax(eagle_dtype dtype, int T, int H, in
     }
     const int n_units = (V + kUnit - 1) / kUnit;
     const int grid = std::min(sm_count(), n_units);
+    const int slice_rows = ((n_units + grid - 1) / grid) * kUnit;
     // one pass over W per 128 tree rows (the MMA's M)
     for (int r0 = 0; r0 < T; r0 += 128) {
       const int Ts = std::min(128, T - r0);
-      const TcLayout TL = tc_layout(Ts);
+      const TcLayout TL = tc_layout(Ts, slice_rows);
       const __nv_bfloat16* hs = static_cast<const __nv_bfloat16*>(d_h) + (size_t)r0 * H;
       CUtensorMap map_h;
       if (!make_map_bf16(&map_h, hs, Ts, H, TL.t_pad)) return EAGLE_ERR_CUDA;
       if (launch_pdl(lmhead_tc_kernel, dim3(grid), dim3(kTcThreads), TL.smem, s, map_h, map_w,
                      Ts, H, V, temperature, z ? z + (size_t)r0 * V : nullptr,
-                     part + (size_t)r0 * grid, n_units, TL.h_stage_bytes, TL.w_stages,
+                     part + (size_t)r0 * grid, n_units, TL.h_stage_bytes, TL.blk, TL.w_stages,
                      d_status) != cudaSuccess)
         return EAGLE_ERR_CUDA;
     }

@@ -555,6 +555,30 @@ tree_attn_tc_kernel(const __grid_constant__ CUtensorMap map_q,
       const bool first = (m == -INFINITY);
       const bool rescale = !first && (mn > m + kRescaleLog2);
       const float mu = (first || rescale) ? mn : m;     // reference max for this block's P
+      // P = exp2(s - mu) = hi + lo, both bf16: hi keeps the top 16 bits of
+      // the fp32 value, lo = P - hi (exact in fp32) truncated the same way;
+      // |P - hi - lo| < 2^-14 P.  Computed before waiting for the previous
+      // PV, which still reads the P columns.
+      float psum = 0.f;
+      // a half-row with nothing visible yet keeps mu = -inf: its scores are
+      // all -inf, and any finite offset gives P = 0
+      const float neg_mu = (mu == -INFINITY) ? 0.f : -mu;
+      uint32_t hi0[16], lo0[16], hi1[16], lo1[16];
+      auto split = [&](const float (&v)[32], uint32_t (&hi)[16], uint32_t (&lo)[16]) {
+#pragma unroll
+        for (int i = 0; i < 16; ++i) {
+          const float p0 = ex2_approx(fmaf(v[2 * i], A.scale_log2, neg_mu));
+          const float p1 = ex2_approx(fmaf(v[2 * i + 1], A.scale_log2, neg_mu));
+          const uint32_t b0 = __float_as_uint(p0), b1 = __float_as_uint(p1);
+          hi[i] = __byte_perm(b0, b1, 0x7632);
+          const float r0 = p0 - __uint_as_float(b0 & 0xffff0000u);
+          const float r1 = p1 - __uint_as_float(b1 & 0xffff0000u);
+          lo[i] = __byte_perm(__float_as_uint(r0), __float_as_uint(r1), 0x7632);
+          psum += p0 + p1;
+        }
+      };
+      split(v0, hi0, lo0);
+      split(v1, hi1, lo1);
       if (j >= 1) {
         // the previous PV has read P and finished O (every earlier PV was
         // waited for one block before)
@@ -574,32 +598,12 @@ tree_attn_tc_kernel(const __grid_constant__ CUtensorMap map_q,
         }
         l *= f;
       }
-      // P = exp2(s - mu) = hi + lo, both bf16: hi keeps the top 16 bits of
-      // the fp32 value, lo = P - hi (exact in fp32) truncated the same way;
-      // |P - hi - lo| < 2^-14 P.  hi to the half's columns +0.., lo +32..
-      float psum = 0.f;
-      // a half-row with nothing visible yet keeps mu = -inf: its scores are
-      // all -inf, and any finite offset gives P = 0
-      const float neg_mu = (mu == -INFINITY) ? 0.f : -mu;
-      auto emit = [&](const float (&v)[32], int cc) {
-        uint32_t hi[16], lo[16];
-#pragma unroll
-        for (int i = 0; i < 16; ++i) {
-          const float p0 = ex2_approx(fmaf(v[2 * i], A.scale_log2, neg_mu));
-          const float p1 = ex2_approx(fmaf(v[2 * i + 1], A.scale_log2, neg_mu));
-          const uint32_t b0 = __float_as_uint(p0), b1 = __float_as_uint(p1);
-          hi[i] = __byte_perm(b0, b1, 0x7632);
-          const float r0 = p0 - __uint_as_float(b0 & 0xffff0000u);
-          const float r1 = p1 - __uint_as_float(b1 & 0xffff0000u);
-          lo[i] = __byte_perm(__float_as_uint(r0), __float_as_uint(r1), 0x7632);
-          psum += p0 + p1;
-        }
-        const uint32_t col = trow + (uint32_t)(128 + half * 64 + cc * 16);
-        tmem_st_32x32b_x16(col, hi);
-        tmem_st_32x32b_x16(col + 32u, lo);
-      };
-      emit(v0, 0);
-      emit(v1, 1);
+      // hi to the half's P columns +0 .., lo to +32 ..
+      const uint32_t pcol = trow + (uint32_t)(128 + half * 64);
+      tmem_st_32x32b_x16(pcol, hi0);
+      tmem_st_32x32b_x16(pcol + 16u, hi1);
+      tmem_st_32x32b_x16(pcol + 32u, lo0);
+      tmem_st_32x32b_x16(pcol + 48u, lo1);
       tmem_wait_st();
       l += psum;
       m = mu;
