@@ -64,28 +64,53 @@ class TreeVerifyStep:
         self.max_nodes = int(max(s.n_nodes))
         self.max_kv = int(max(s.L)) if len(s.L) else 0
         z = lambda *shape_, dtype=f32: torch.zeros(shape_, dtype=dtype, device=dev)
-        # inputs
-        self.q = z(T, s.Hq, s.D, dtype=dt)
-        self.k_tree = z(T, s.Hkv, s.D, dtype=dt)
-        self.v_tree = z(T, s.Hkv, s.D, dtype=dt)
+        # Inputs that change every step live in one device buffer (views at
+        # 256-byte offsets), so a step's inputs arrive with a single copy.
+        spec = [("q", (T, s.Hq, s.D), dt), ("k_tree", (T, s.Hkv, s.D), dt),
+                ("v_tree", (T, s.Hkv, s.D), dt), ("h", (T, s.H), dt),
+                ("u_accept", (T,), f32), ("u_sample", (T,), f32)]
+        if s.mode == "stochastic":
+            spec.append(("p_rows", (max(s.rows, 1), s.V), f32))
+        if s.k:
+            spec += [("draft_logp", (max(s.rows, 1), s.V), f32), ("budget", (s.B,), i32),
+                     ("root_token", (s.B,), i32)]
+        else:
+            spec += [("tree_off", (s.B + 1,), i32), ("parent", (T,), i32),
+                     ("tokens", (T,), i32), ("p_row_of_node", (T,), i32)]
+        offs, total = [], 0
+        for _, shp, dty in spec:
+            n = 1
+            for d in shp:
+                n *= d
+            offs.append(total)
+            total += (n * torch.empty((), dtype=dty).element_size() + 255) // 256 * 256
+        self.step_input_names = [n for n, _, _ in spec]
+        self.step_inputs = torch.zeros(max(total, 256), dtype=torch.uint8, device=dev)
+        for (name, shp, dty), off in zip(spec, offs):
+            nb = 1
+            for d in shp:
+                nb *= d
+            nb *= torch.empty((), dtype=dty).element_size()
+            setattr(self, name, self.step_inputs[off:off + nb].view(dty).view(shp))
+        # resident inputs
         self.k_cache = z(max(sumL, 1), s.Hkv, s.D, dtype=dt)
         self.v_cache = z(max(sumL, 1), s.Hkv, s.D, dtype=dt)
         self.kv_off = z(s.B + 1, dtype=i32)
-        self.h = z(T, s.H, dtype=dt)
         self.w_lm = z(s.V, s.H, dtype=dt)
-        self.p_rows = z(max(s.rows, 1), s.V)
-        self.draft_logp = z(max(s.rows, 1), s.V) if s.k else None
-        self.u_accept = z(T)
-        self.u_sample = z(T)
-        self.root_token = z(s.B, dtype=i32)
-        self.budget = z(s.B, dtype=i32)
+        if s.mode != "stochastic":
+            self.p_rows = z(max(s.rows, 1), s.V)
+        if not s.k:
+            self.draft_logp = None
+            self.budget = z(s.B, dtype=i32)
+            self.root_token = z(s.B, dtype=i32)
         # tree (written by the expand kernels, or loaded)
-        self.tree_off = z(s.B + 1, dtype=i32)
-        self.parent = z(T, dtype=i32)
-        self.tokens = z(T, dtype=i32)
+        if s.k:
+            self.tree_off = z(s.B + 1, dtype=i32)
+            self.parent = z(T, dtype=i32)
+            self.tokens = z(T, dtype=i32)
+            self.p_row_of_node = z(T, dtype=i32)
         self.node_depth = z(T, dtype=i32)
         self.score = z(T)
-        self.p_row_of_node = z(T, dtype=i32)
         self.pool = None
         if s.k:
             nbytes = eagle_draft_pool_bytes(s.B, s.k, s.depth, s.V)
@@ -120,6 +145,21 @@ class TreeVerifyStep:
                 raise KeyError(f"{name} is not used by this step")
             src = val if isinstance(val, torch.Tensor) else torch.from_numpy(val)
             t.copy_(src.reshape(t.shape).to(t.dtype), non_blocking=False)
+
+    def host_step_inputs(self, arrays: Dict[str, object]):
+        """Pinned host buffer laid out like `step_inputs`, filled from host
+        arrays named as the step's inputs: one copy moves a whole step."""
+        torch = self.torch
+        host = torch.zeros(self.step_inputs.numel(), dtype=torch.uint8).pin_memory()
+        base = self.step_inputs.data_ptr()
+        for name in self.step_input_names:
+            t = getattr(self, name)
+            off = t.data_ptr() - base
+            nb = t.numel() * t.element_size()
+            src = arrays[name]
+            src = src if isinstance(src, torch.Tensor) else torch.from_numpy(src)
+            host[off:off + nb].view(t.dtype).view(t.shape).copy_(src.reshape(t.shape).to(t.dtype))
+        return host
 
     # ------------------------------------------------------------------
     def run_expand(self, stream=None) -> None:
