@@ -264,12 +264,13 @@ def eagle_draft_pool_bytes(B, k, depth, V) -> int:
 
 
 def eagle_draft_expand(pool, status, *, B: int, V: int, k: int, depth: int, level: int = 0,
-                       finalize: bool = False, draft_logp=None, budget=None, root_token=None,
+                       finalize: int = 0, draft_logp=None, budget=None, root_token=None,
                        tree_off=None, parent=None, tokens=None, node_depth=None, score=None,
                        p_row_of_node=None, stream=None) -> None:
-    """EAGLE-2 expand (one level) or finalize; draft_logp [B, R, V] fp32 with
+    """EAGLE-2 expand (one level), finalize (finalize=1), or the last level
+    with the finalize fused in (finalize=2); draft_logp [B, R, V] fp32 with
     R = 1 + (depth-1)*k."""
-    _call("eagle_draft_expand", B, V, k, depth, int(level), int(bool(finalize)),
+    _call("eagle_draft_expand", B, V, k, depth, int(level), int(finalize),
           _ptr(draft_logp), _ptr(budget), _ptr(root_token), _ptr(pool),
           pool.numel() * pool.element_size(), _ptr(tree_off), _ptr(parent), _ptr(tokens),
           _ptr(node_depth), _ptr(score), _ptr(p_row_of_node), _ptr(status), _stream(stream))

@@ -34,6 +34,7 @@ constexpr int kRowCap = 128;           // row-merge candidates held at once
 constexpr int kMergeRegs = 8;          // chunk-list keys per lane kept in registers
 constexpr int kFinalThreads = 1024;
 constexpr int kMaxV = 1 << 19;
+constexpr size_t kFusedSmemMax = 64 * 1024;  // finalize memory fused into a level
 // Bound-raising rounds never exceed (keys / (cap - k)); past these limits a
 // selection stops with EAGLE_ERR_TIMEOUT instead of looping.
 constexpr int kChunkRounds = 32;   // keys per chunk <= 8192, cap - k >= 480
@@ -119,13 +120,31 @@ PoolPtrs pool_ptrs(void* base, const PoolLayout& L) {
   return p;
 }
 
+struct FinalParams {
+  int B, k, R, P;
+  const int* budget;
+  const int* root_token;
+  PoolPtrs pool;
+  int* tree_off;
+  int* parent;
+  int* tokens;
+  int* node_depth;
+  float* score;
+  int* p_row_of_node;
+  int* status;
+};
+
 struct LevelParams {
   int B, V, k, F, R, S, level, P;
   bool vec_ok;  // rows 16-byte aligned: float4 loads
+  bool fused;   // the last level: also finalize every sequence (fin)
   const float* logp;
   PoolPtrs pool;
+  FinalParams fin;
   int* status;
 };
+
+__device__ void finalize_sequence(const FinalParams& A, int b, unsigned char* smem_raw);
 
 __device__ __forceinline__ unsigned long long umax64(unsigned long long a, unsigned long long b) {
   return a > b ? a : b;
@@ -348,17 +367,19 @@ __global__ void __launch_bounds__(kLvThreads, 2) expand_level_kernel(const Level
     s_top[tid] = 0ull;  // fewer than k tokens in this chunk
   }
   __syncthreads();
-  // ---- publish the chunk list; the sequence's last CTA merges
-  if (warp == 0) {
+  // ---- publish the chunk list; the sequence's last CTA merges.  One thread
+  // writes the list and takes the ticket with an acquire-release atomic: its
+  // stores are visible to the CTA that draws the last ticket, and that CTA's
+  // reads follow the atomic (then a CTA barrier).
+  if (tid == 0) {
     unsigned long long* part = A.pool.partial + ((size_t)row * A.S + chunk) * k;
-    if (lane < k) part[lane] = s_top[lane];
-    __threadfence();
-    __syncwarp();
-    if (lane == 0) {
-      const int t = atomicAdd(&A.pool.ticket[b], 1);
-      __threadfence();
-      s_last = (t == A.F * A.S - 1);
-    }
+    for (int r = 0; r < k; ++r) part[r] = s_top[r];
+    int t;
+    asm volatile("atom.acq_rel.gpu.global.add.s32 %0, [%1], 1;"
+                 : "=r"(t)
+                 : "l"(A.pool.ticket + b)
+                 : "memory");
+    s_last = (t == A.F * A.S - 1);
   }
   __syncthreads();
   if (!s_last) return;
@@ -420,38 +441,32 @@ __global__ void __launch_bounds__(kLvThreads, 2) expand_level_kernel(const Level
     }
   }
   if (tid == 0) A.pool.count[b] = base + nc;
+  if (A.fused) {
+    // the last level: this CTA holds the sequence's complete pool
+    __threadfence_block();
+    __syncthreads();
+    extern __shared__ __align__(16) unsigned char dyn_smem[];
+    finalize_sequence(A.fin, b, dyn_smem);
+  }
 }
 
-struct FinalParams {
-  int B, k, R, P;
-  const int* budget;
-  const int* root_token;
-  PoolPtrs pool;
-  int* tree_off;
-  int* parent;
-  int* tokens;
-  int* node_depth;
-  float* score;
-  int* p_row_of_node;
-  int* status;
-};
-
-// Finalize, one CTA per sequence: keep the `budget` pool entries of largest
-// key (score desc, creation order) -- a radix select of the budget-th key --
-// number the kept nodes by (depth, score desc, creation order) and write the
-// tree.
-__global__ void __launch_bounds__(kFinalThreads) expand_finalize_kernel(const FinalParams A) {
-  pdl_begin();
-  extern __shared__ __align__(16) unsigned char smem_raw[];
+// Finalize one sequence with the calling CTA (any block size that is a
+// multiple of 64): keep the `budget` pool entries of largest key (score
+// desc, creation order) -- a radix select of the budget-th key -- number the
+// kept nodes by (depth, score desc, creation order) and write the tree.
+// `smem_raw`: 20 * P bytes of shared memory.  Every sequence's pool holds
+// P = k + (depth-1) k^2 entries after the last level, which fixes the node
+// offset of each sequence without waiting for the others.
+__device__ void finalize_sequence(const FinalParams& A, int b, unsigned char* smem_raw) {
   unsigned long long* s_key = reinterpret_cast<unsigned long long*>(smem_raw);  // [P]
   int* s_dep = reinterpret_cast<int*>(s_key + A.P);                             // [P]
   int* s_node = s_dep + A.P;                                                    // [P]
   int* s_list = s_node + A.P;                                                   // [P]
   __shared__ int s_hist[256];
   __shared__ int s_digit, s_rem, s_eq, s_nsel, s_off;
-  const int b = blockIdx.x;
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-  const int n = max(0, min(A.pool.count[b], A.P));
+  const int nthreads = blockDim.x;
+  const int n = max(0, min(__ldcg(A.pool.count + b), A.P));
   const int bud = A.budget[b];
   const int keep = min(max(bud, 0), n);
   const float* sco = A.pool.score + (size_t)b * A.P;
@@ -463,15 +478,14 @@ __global__ void __launch_bounds__(kFinalThreads) expand_finalize_kernel(const Fi
   if (warp == 1) {
     // node offset of this sequence: sum over earlier sequences of kept + root
     int off = 0;
-    for (int j = lane; j < b; j += 32)
-      off += min(max(A.budget[j], 0), max(0, min(A.pool.count[j], A.P))) + 1;
+    for (int j = lane; j < b; j += 32) off += min(max(A.budget[j], 0), A.P) + 1;
 #pragma unroll
     for (int o = 16; o > 0; o >>= 1) off += __shfl_xor_sync(0xffffffffu, off, o);
     if (lane == 0) s_off = off;
   }
-  for (int i = tid; i < n; i += blockDim.x) {
-    s_key[i] = desc_key(sco[i], (uint32_t)i);
-    s_dep[i] = dep[i];
+  for (int i = tid; i < n; i += nthreads) {
+    s_key[i] = desc_key(__ldcg(sco + i), (uint32_t)i);
+    s_dep[i] = __ldcg(dep + i);
     s_node[i] = -1;
   }
   // radix select (8 bits at a time, high to low) of the keep-th largest key
@@ -481,7 +495,7 @@ __global__ void __launch_bounds__(kFinalThreads) expand_finalize_kernel(const Fi
     for (int shift = 56; shift >= 0; shift -= 8) {
       if (tid < 256) s_hist[tid] = 0;
       __syncthreads();
-      for (int i0 = 0; i0 < n; i0 += blockDim.x) {   // uniform trip count
+      for (int i0 = 0; i0 < n; i0 += nthreads) {   // uniform trip count
         const int i = i0 + tid;
         const unsigned long long key = (i < n) ? s_key[i] : 0ull;
         const int bin = (i < n && (key & mask) == prefix) ? (int)(key >> shift) & 255 : 256;
@@ -523,7 +537,7 @@ __global__ void __launch_bounds__(kFinalThreads) expand_finalize_kernel(const Fi
   // kept: keys >= the threshold (prefix, low bits zero), exactly `keep` of them
   const unsigned long long tau = (keep == 0) ? ~0ull : (keep == n ? 1ull : prefix);
   __syncthreads();
-  for (int i = tid; i < n; i += blockDim.x)
+  for (int i = tid; i < n; i += nthreads)
     if (keep > 0 && s_key[i] >= tau) s_list[atomicAdd(&s_nsel, 1)] = i;
   __syncthreads();
   const int ns = s_nsel;
@@ -531,9 +545,9 @@ __global__ void __launch_bounds__(kFinalThreads) expand_finalize_kernel(const Fi
   // node number of every kept entry: 1 + rank by (depth, score desc,
   // creation); gs lanes share one entry's count
   int gs = 1;
-  while (gs < 32 && 2 * gs * ns <= kFinalThreads) gs *= 2;
+  while (gs < 32 && 2 * gs * ns <= nthreads) gs *= 2;
   const int sub = lane & (gs - 1);
-  for (int a0 = 0; a0 < ns; a0 += kFinalThreads / gs) {
+  for (int a0 = 0; a0 < ns; a0 += nthreads / gs) {
     const int a = a0 + tid / gs;
     const int ia = (a < ns) ? s_list[a] : 0;
     const int da = (a < ns) ? s_dep[ia] : 0;
@@ -552,17 +566,17 @@ __global__ void __launch_bounds__(kFinalThreads) expand_finalize_kernel(const Fi
   const int* tok = A.pool.token + (size_t)b * A.P;
   const int* par = A.pool.parent + (size_t)b * A.P;
   const int* prw = A.pool.prow + (size_t)b * A.P;
-  for (int a = tid; a < ns; a += blockDim.x) {
+  for (int a = tid; a < ns; a += nthreads) {
     const int ia = s_list[a];
-    const int pp = par[ia];
+    const int pp = __ldcg(par + ia);
     const int pnode = (pp < 0) ? 0 : (pp < n ? s_node[pp] : -1);
     if (pnode < 0) fail(A.status, EAGLE_ERR_INVALID_TREE);  // not parent-closed
     const int at = off + s_node[ia];
     A.parent[at] = pnode;
-    A.tokens[at] = tok[ia];
+    A.tokens[at] = __ldcg(tok + ia);
     A.node_depth[at] = s_dep[ia];
     A.score[at] = key_value(s_key[ia]);
-    A.p_row_of_node[at] = b * A.R + prw[ia];
+    A.p_row_of_node[at] = b * A.R + __ldcg(prw + ia);
   }
   if (tid == 0) {
     A.tree_off[b] = off;
@@ -573,6 +587,12 @@ __global__ void __launch_bounds__(kFinalThreads) expand_finalize_kernel(const Fi
     A.score[off] = 0.f;
     A.p_row_of_node[off] = -1;
   }
+}
+
+__global__ void __launch_bounds__(kFinalThreads) expand_finalize_kernel(const FinalParams A) {
+  pdl_begin();
+  extern __shared__ __align__(16) unsigned char smem_raw[];
+  finalize_sequence(A, blockIdx.x, smem_raw);
 }
 
 }  // namespace
@@ -603,58 +623,74 @@ extern "C" eagle_status eagle_draft_expand(int B, int V, int k, int depth, int l
   const PoolPtrs pp = pool_ptrs(d_pool, L);
   cudaStream_t s = (cudaStream_t)stream;
   const int R = 1 + (depth - 1) * k;
-  if (!finalize) {
-    EAGLE_HOST_CHECK(level >= 0 && level < depth, EAGLE_ERR_INVALID_ARG);
-    EAGLE_HOST_CHECK(d_draft_logp, EAGLE_ERR_INVALID_ARG);
-    if (level == 0) {
-      // fresh tree: zero the pool fill counts and the level tickets
-      cudaError_t e = cudaMemsetAsync(static_cast<char*>(d_pool), 0, L.off_frontier, s);
-      if (e != cudaSuccess) return EAGLE_ERR_CUDA;
-    }
-    const ChunkPlan cp = (level == 0) ? L.c0 : L.c1;
-    LevelParams A;
-    A.B = B;
-    A.V = V;
-    A.k = k;
-    A.F = (level == 0) ? 1 : k;
-    A.R = R;
-    A.S = cp.S;
-    A.level = level;
-    A.P = L.P;
-    A.vec_ok = (V % 4 == 0) && ((uintptr_t)d_draft_logp % 16 == 0);
-    A.logp = d_draft_logp;
-    A.pool = pp;
-    A.status = d_status;
-    const dim3 grid(B * A.F * A.S);
-    void (*kern)(const LevelParams) = (cp.vec == 1)   ? expand_level_kernel<1>
-                                      : (cp.vec == 2) ? expand_level_kernel<2>
-                                                      : expand_level_kernel<4>;
-    return launch_status(launch_pdl(kern, grid, dim3(kLvThreads), 0, s, A));
-  }
-  EAGLE_HOST_CHECK(d_budget && d_tree_off && d_parent && d_tokens && d_node_depth && d_score &&
-                       d_p_row_of_node,
-                   EAGLE_ERR_INVALID_ARG);
+  EAGLE_HOST_CHECK(finalize >= 0 && finalize <= 2, EAGLE_ERR_INVALID_ARG);
   FinalParams F;
-  F.B = B;
-  F.k = k;
-  F.R = R;
-  F.P = L.P;
-  F.budget = d_budget;
-  F.root_token = d_root_token;
-  F.pool = pp;
-  F.tree_off = d_tree_off;
-  F.parent = d_parent;
-  F.tokens = d_tokens;
-  F.node_depth = d_node_depth;
-  F.score = d_score;
-  F.p_row_of_node = d_p_row_of_node;
-  F.status = d_status;
-  const size_t smem = (size_t)L.P * (8 + 4 + 4 + 4);
-  EAGLE_HOST_CHECK(smem <= 200 * 1024, EAGLE_ERR_UNSUPPORTED);
-  if (smem > 40 * 1024) {
-    cudaFuncSetAttribute(expand_finalize_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                         (int)smem);
+  const size_t fin_smem = (size_t)L.P * (8 + 4 + 4 + 4);
+  if (finalize) {
+    EAGLE_HOST_CHECK(d_budget && d_tree_off && d_parent && d_tokens && d_node_depth && d_score &&
+                         d_p_row_of_node,
+                     EAGLE_ERR_INVALID_ARG);
+    EAGLE_HOST_CHECK(fin_smem <= 200 * 1024, EAGLE_ERR_UNSUPPORTED);
+    F.B = B;
+    F.k = k;
+    F.R = R;
+    F.P = L.P;
+    F.budget = d_budget;
+    F.root_token = d_root_token;
+    F.pool = pp;
+    F.tree_off = d_tree_off;
+    F.parent = d_parent;
+    F.tokens = d_tokens;
+    F.node_depth = d_node_depth;
+    F.score = d_score;
+    F.p_row_of_node = d_p_row_of_node;
+    F.status = d_status;
   }
-  return launch_status(launch_pdl(expand_finalize_kernel, dim3(B), dim3(kFinalThreads), smem, s,
-                                  F));
+  auto launch_finalize = [&]() -> eagle_status {
+    if (fin_smem > 40 * 1024 &&
+        cudaFuncSetAttribute(expand_finalize_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             (int)fin_smem) != cudaSuccess)
+      return EAGLE_ERR_CUDA;
+    return launch_status(launch_pdl(expand_finalize_kernel, dim3(B), dim3(kFinalThreads), fin_smem,
+                                    s, F));
+  };
+  if (finalize == 1) return launch_finalize();
+  // one level (finalize == 2: the last level, with the finalize fused in)
+  EAGLE_HOST_CHECK(level >= 0 && level < depth, EAGLE_ERR_INVALID_ARG);
+  EAGLE_HOST_CHECK(finalize == 0 || level == depth - 1, EAGLE_ERR_INVALID_ARG);
+  EAGLE_HOST_CHECK(d_draft_logp, EAGLE_ERR_INVALID_ARG);
+  if (level == 0) {
+    // fresh tree: zero the pool fill counts and the level tickets
+    cudaError_t e = cudaMemsetAsync(static_cast<char*>(d_pool), 0, L.off_frontier, s);
+    if (e != cudaSuccess) return EAGLE_ERR_CUDA;
+  }
+  const ChunkPlan cp = (level == 0) ? L.c0 : L.c1;
+  LevelParams A;
+  A.B = B;
+  A.V = V;
+  A.k = k;
+  A.F = (level == 0) ? 1 : k;
+  A.R = R;
+  A.S = cp.S;
+  A.level = level;
+  A.P = L.P;
+  A.vec_ok = (V % 4 == 0) && ((uintptr_t)d_draft_logp % 16 == 0);
+  A.logp = d_draft_logp;
+  A.pool = pp;
+  A.status = d_status;
+  void (*kern)(const LevelParams) = (cp.vec == 1)   ? expand_level_kernel<1>
+                                    : (cp.vec == 2) ? expand_level_kernel<2>
+                                                    : expand_level_kernel<4>;
+  // fuse the finalize when its shared memory fits beside the level's
+  A.fused = (finalize == 2) && fin_smem <= kFusedSmemMax;
+  A.fin = F;
+  const size_t dyn = A.fused ? fin_smem : 0;
+  if (dyn > 0 &&
+      cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)dyn) !=
+          cudaSuccess)
+    return EAGLE_ERR_CUDA;
+  const eagle_status st =
+      launch_status(launch_pdl(kern, dim3(B * A.F * A.S), dim3(kLvThreads), dyn, s, A));
+  if (st != EAGLE_OK || finalize != 2 || A.fused) return st;
+  return launch_finalize();
 }

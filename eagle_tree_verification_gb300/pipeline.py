@@ -164,11 +164,13 @@ class TreeVerifyStep:
     # ------------------------------------------------------------------
     def run_expand(self, stream=None) -> None:
         s = self.s
-        for lev in range(s.depth):
+        for lev in range(s.depth - 1):
             eagle_draft_expand(self.pool, self.status, B=s.B, V=s.V, k=s.k, depth=s.depth,
                                level=lev, draft_logp=self.draft_logp, stream=stream)
+        # the last level with the finalize fused in
         eagle_draft_expand(self.pool, self.status, B=s.B, V=s.V, k=s.k, depth=s.depth,
-                           finalize=True, budget=self.budget, root_token=self.root_token,
+                           level=s.depth - 1, finalize=2, draft_logp=self.draft_logp,
+                           budget=self.budget, root_token=self.root_token,
                            tree_off=self.tree_off, parent=self.parent, tokens=self.tokens,
                            node_depth=self.node_depth, score=self.score,
                            p_row_of_node=self.p_row_of_node, stream=stream)
@@ -210,7 +212,7 @@ class TreeVerifyStep:
         """Kernels launched by run() (the count the benchmark reports)."""
         n = 0
         if self.s.k:
-            n += self.s.depth + 1                # one per level, finalize
+            n += self.s.depth                    # one per level, finalize fused
         n += 1                                   # attention
         if self.s.dtype == "bf16":               # LM head: one pass per 128 rows
             n += (self.s.T + 127) // 128 + 1     # ... + finalize

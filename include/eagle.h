@@ -256,6 +256,10 @@ EAGLE_API eagle_status eagle_accept_stochastic(int B, int max_nodes, int V, int 
  * children by (score desc, creation order).  Draft rows:
  *   d_draft_logp [B, R, V] fp32 with R = 1 + (depth-1)*k; level 0 reads row
  *   0 (the root's), level d >= 1 reads rows 1+(d-1)*k+f for frontier rank f.
+ * Last level and finalize in one launch (finalize == 2, level == depth-1):
+ * the CTA that completes a sequence's last level also finalizes it
+ * (falls back to two launches when the pool is too large for that CTA's
+ * shared memory); outputs as for finalize == 1.
  * Finalize (finalize == 1, after all `depth` levels): keep the top
  * d_budget[b] pool nodes by (score desc, creation order), number them by
  * (depth, score desc, creation order) after the root (node 0), and write

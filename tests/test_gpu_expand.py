@@ -11,7 +11,7 @@ from gpu_common import cuda_ready, to_np
 pytestmark = pytest.mark.gpu
 
 
-def _gpu_tree(E, lp, B, V, k, depth, budget, root_token):
+def _gpu_tree(E, lp, B, V, k, depth, budget, root_token, fused=False):
     import torch
     R = 1 + (depth - 1) * k
     pool = torch.zeros(E.eagle_draft_pool_bytes(B, k, depth, V), dtype=torch.uint8, device="cuda")
@@ -23,12 +23,15 @@ def _gpu_tree(E, lp, B, V, k, depth, budget, root_token):
            for n in ("parent", "tokens", "node_depth", "p_row_of_node")}
     out["score"] = torch.full((T,), -7.0, dtype=torch.float32, device="cuda")
     out["tree_off"] = torch.full((B + 1,), -7, dtype=torch.int32, device="cuda")
-    for lev in range(depth):
+    fin = dict(budget=torch.tensor(budget, dtype=torch.int32, device="cuda"),
+               root_token=torch.tensor(root_token, dtype=torch.int32, device="cuda"), **out)
+    for lev in range(depth - 1 if fused else depth):
         E.eagle_draft_expand(pool, st, B=B, V=V, k=k, depth=depth, level=lev, draft_logp=d_lp)
-    E.eagle_draft_expand(pool, st, B=B, V=V, k=k, depth=depth, finalize=True,
-                         budget=torch.tensor(budget, dtype=torch.int32, device="cuda"),
-                         root_token=torch.tensor(root_token, dtype=torch.int32, device="cuda"),
-                         **out)
+    if fused:
+        E.eagle_draft_expand(pool, st, B=B, V=V, k=k, depth=depth, level=depth - 1, finalize=2,
+                             draft_logp=d_lp, **fin)
+    else:
+        E.eagle_draft_expand(pool, st, B=B, V=V, k=k, depth=depth, finalize=1, **fin)
     torch.cuda.synchronize()
     return {n: to_np(t) for n, t in out.items()}, int(st.item())
 
@@ -42,13 +45,15 @@ def _gpu_tree(E, lp, B, V, k, depth, budget, root_token):
     (2, 128256, 8, 8, [64, 33], 3.0),         # LLaMA-3-70B / batched shape
     (2, 5000, 32, 3, [500, 0], 0.5),          # k at its limit, an empty budget
 ])
-def test_expand_matches_oracle(B, V, k, depth, budgets, sigma):
+@pytest.mark.parametrize("fused", [False, True])
+def test_expand_matches_oracle(B, V, k, depth, budgets, sigma, fused):
+    # fused: the last level and the finalize in one launch
     E = cuda_ready()
     R = 1 + (depth - 1) * k
     lp, _ = synth.draft_rows(B * 7 + V, "expand", B * R, V, sigma)
     ref = O.build_eagle2_tree(lp, B=B, k=k, depth=depth, budget=budgets,
                               root_token=list(range(B)))
-    got, st = _gpu_tree(E, lp, B, V, k, depth, budgets, list(range(B)))
+    got, st = _gpu_tree(E, lp, B, V, k, depth, budgets, list(range(B)), fused=fused)
     assert st == 0
     for name in ("tree_off", "parent", "tokens", "p_row_of_node", "score"):
         np.testing.assert_array_equal(got[name], ref[name], err_msg=name)
