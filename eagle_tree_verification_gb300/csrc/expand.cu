@@ -19,6 +19,7 @@
 #include <algorithm>
 
 #include "common.cuh"
+#include "tc.cuh"
 
 using namespace eagle;
 
@@ -257,114 +258,119 @@ __device__ void warp_row_topk(const unsigned long long* src, int n, int k,
   __syncwarp();
 }
 
-// One level.  CTA (row, chunk): exact top-k of the chunk -> partial list.
-// The sequence's last CTA: per-row top-k, children, next frontier.
+struct ChunkShared {
+  float grpv[kGroups];
+  unsigned long long cand[kCandCap];
+  unsigned long long top[EAGLE_MAX_TOPK];
+  unsigned long long tau;
+  int cnt, last;
+};
+
+// Exact top-k of one chunk (row, chunk) held in registers -- element
+// c0 + (j * threads + tid) * 4 + e in v[j][e] -- published to the pool's
+// partial lists by thread 0.  With take_ticket, thread 0 also counts the
+// chunk on the sequence's ticket; returns true in the CTA that drew the
+// last one.
 template <int VEC>
-__global__ void __launch_bounds__(kLvThreads, 2) expand_level_kernel(const LevelParams A) {
-  pdl_begin();
-  __shared__ unsigned long long s_grp[kGroups];
-  __shared__ unsigned long long s_cand[kCandCap];
-  __shared__ unsigned long long s_top[EAGLE_MAX_TOPK];
-  __shared__ unsigned long long s_tau;
-  __shared__ int s_cnt, s_last;
-  __shared__ MergeShared M;
+__device__ bool chunk_topk(const LevelParams& A, int row, int chunk, const float (&v)[VEC][4],
+                           ChunkShared& C, bool take_ticket = true) {
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-  const int row = blockIdx.x / A.S, chunk = blockIdx.x % A.S;
-  const int b = row / A.F, f = row % A.F;
+  const int b = row / A.F;
   const int k = A.k;
-  const int local_row = (A.level == 0) ? 0 : 1 + (A.level - 1) * k + f;
-  const float* src = A.logp + ((size_t)b * A.R + local_row) * A.V;
   const int c0 = chunk * (kLvThreads * 4 * VEC);
-  // ---- chunk in registers: element c0 + (j * threads + tid) * 4 + e
-  float v[VEC][4];
-  bool bad = false;
+  // Values (past the row's end: -inf).  Only the few candidates get 64-bit
+  // keys; the per-token work is a max, a finiteness FMA and a compare.
+  const bool ragged = c0 + kLvThreads * 4 * VEC > A.V;   // block-uniform
+  float x[VEC][4];
+  float fin = 0.f;   // sum of v * 0: NaN iff some value is not finite
+  if (!ragged) {
 #pragma unroll
-  for (int j = 0; j < VEC; ++j) {
-    const int i0 = c0 + (j * kLvThreads + tid) * 4;
-    if (A.vec_ok && i0 + 4 <= A.V) {
-      const float4 x = __ldg(reinterpret_cast<const float4*>(src + i0));
-      v[j][0] = x.x;
-      v[j][1] = x.y;
-      v[j][2] = x.z;
-      v[j][3] = x.w;
-    } else {
+    for (int j = 0; j < VEC; ++j)
 #pragma unroll
-      for (int e = 0; e < 4; ++e) v[j][e] = (i0 + e < A.V) ? __ldg(src + i0 + e) : 0.f;
-    }
+      for (int e = 0; e < 4; ++e) {
+        x[j][e] = v[j][e];
+        fin = fmaf(v[j][e], 0.f, fin);
+      }
+  } else {
+#pragma unroll
+    for (int j = 0; j < VEC; ++j)
+#pragma unroll
+      for (int e = 0; e < 4; ++e) {
+        const bool real = c0 + (j * kLvThreads + tid) * 4 + e < A.V;
+        x[j][e] = real ? v[j][e] : -INFINITY;
+        if (real) fin = fmaf(v[j][e], 0.f, fin);
+      }
   }
-  auto key_of = [&](int j, int e) -> unsigned long long {
-    const int i = c0 + (j * kLvThreads + tid) * 4 + e;
-    return (i < A.V) ? desc_key(v[j][e], (uint32_t)i) : 0ull;
-  };
-  unsigned long long tmax = 0;
+  float tmax = -INFINITY;
 #pragma unroll
   for (int j = 0; j < VEC; ++j)
 #pragma unroll
-    for (int e = 0; e < 4; ++e) {
-      const int i = c0 + (j * kLvThreads + tid) * 4 + e;
-      if (i < A.V) bad |= !isfinite(v[j][e]);
-      tmax = umax64(tmax, key_of(j, e));
-    }
+    for (int e = 0; e < 4; ++e) tmax = fmaxf(tmax, x[j][e]);
 #pragma unroll
-  for (int o = 8; o > 0; o >>= 1) tmax = umax64(tmax, __shfl_xor_sync(0xffffffffu, tmax, o));
-  if ((lane & 15) == 0) s_grp[warp * 2 + (lane >> 4)] = tmax;
-  if (tid == 0) s_cnt = 0;
-  if (__syncthreads_or(bad) && tid == 0) fail(A.status, EAGLE_ERR_NUMERIC);
-  // every warp: the k-th largest group maximum (k distinct keys reach it)
-  unsigned long long tau;
+  for (int o = 8; o > 0; o >>= 1) tmax = fmaxf(tmax, __shfl_xor_sync(0xffffffffu, tmax, o));
+  if ((lane & 15) == 0) C.grpv[warp * 2 + (lane >> 4)] = tmax;
+  if (tid == 0) C.cnt = 0;
+  if (__syncthreads_or(!(fin == 0.f)) && tid == 0) fail(A.status, EAGLE_ERR_NUMERIC);
+  // every warp: the largest group maximum that at least k group maxima
+  // reach -- at least k tokens of the chunk are >= it (ties included)
+  float tau_val;
   {
-    const unsigned long long g = s_grp[lane];
-    int rank = 0;
+    const float g = C.grpv[lane];
+    int ge = 0;
 #pragma unroll 8
-    for (int i = 0; i < kGroups; ++i) rank += (s_grp[i] > g);
-    tau = pick_lane(__ballot_sync(0xffffffffu, rank == k - 1), g, 1ull);
+    for (int i = 0; i < kGroups; ++i) ge += (C.grpv[i] >= g);
+    const unsigned ob = __reduce_max_sync(0xffffffffu, (ge >= k) ? ordered_bits(g) : 0u);
+    // fewer than k real tokens: every real (finite) token qualifies
+    tau_val = fmaxf(from_ordered_bits(ob), -3.402823466e38f);
   }
+  unsigned long long tau_key = 0;   // later rounds: the bound as a key
   int cnt;
   for (int round = 0;; ++round) {
 #pragma unroll
     for (int j = 0; j < VEC; ++j)
 #pragma unroll
       for (int e = 0; e < 4; ++e) {
-        const unsigned long long key = key_of(j, e);
-        const bool pred = key >= tau;
+        const float val = x[j][e];
+        const uint32_t idx = (uint32_t)(c0 + (j * kLvThreads + tid) * 4 + e);
+        const bool pred = (val >= tau_val) && (round == 0 || desc_key(val, idx) >= tau_key);
         const unsigned bal = __ballot_sync(0xffffffffu, pred);
         if (bal) {
           const int leader = __ffs(bal) - 1;
           int base = 0;
-          if (lane == leader) base = atomicAdd(&s_cnt, __popc(bal));
+          if (lane == leader) base = atomicAdd(&C.cnt, __popc(bal));
           base = __shfl_sync(0xffffffffu, base, leader);
           const int pos = base + __popc(bal & lanemask_lt());
-          if (pred && pos < kCandCap) s_cand[pos] = key;
+          if (pred && pos < kCandCap) C.cand[pos] = desc_key(val, idx);
         }
       }
     __syncthreads();
-    cnt = s_cnt;
+    cnt = C.cnt;
     if (cnt <= kCandCap) break;
     if (round == kChunkRounds) {
       if (tid == 0) fail(A.status, EAGLE_ERR_TIMEOUT);
       cnt = kCandCap;
       break;
     }
-    // too many: raise the bound to the k-th largest of the held ones
-    // (each round drops at least kCandCap - k keys)
-    const unsigned long long me = s_cand[tid];
+    // too many: raise the bound to the k-th largest of the held keys
+    // (each round drops at least kCandCap - k of them)
+    const unsigned long long me = C.cand[tid];
     int rank = 0;
 #pragma unroll 8
-    for (int i = 0; i < kCandCap; ++i) rank += (s_cand[i] > me);
+    for (int i = 0; i < kCandCap; ++i) rank += (C.cand[i] > me);
     __syncthreads();
-    if (rank == k - 1) s_tau = me;
-    if (tid == 0) s_cnt = 0;
+    if (rank == k - 1) C.tau = me;
+    if (tid == 0) C.cnt = 0;
     __syncthreads();
-    tau = s_tau;
+    tau_key = C.tau;
   }
   if (tid < cnt) {
-    const unsigned long long me = s_cand[tid];
+    const unsigned long long me = C.cand[tid];
     int rank = 0;
 #pragma unroll 8
-    for (int i = 0; i < cnt; ++i) rank += (s_cand[i] > me);
-    if (rank < k) s_top[rank] = me;
+    for (int i = 0; i < cnt; ++i) rank += (C.cand[i] > me);
+    if (rank < k) C.top[rank] = me;
   } else if (tid < k) {
-    s_top[tid] = 0ull;  // fewer than k tokens in this chunk
+    C.top[tid] = 0ull;  // fewer than k tokens in this chunk
   }
   __syncthreads();
   // ---- publish the chunk list; the sequence's last CTA merges.  One thread
@@ -373,16 +379,26 @@ __global__ void __launch_bounds__(kLvThreads, 2) expand_level_kernel(const Level
   // reads follow the atomic (then a CTA barrier).
   if (tid == 0) {
     unsigned long long* part = A.pool.partial + ((size_t)row * A.S + chunk) * k;
-    for (int r = 0; r < k; ++r) part[r] = s_top[r];
-    int t;
-    asm volatile("atom.acq_rel.gpu.global.add.s32 %0, [%1], 1;"
-                 : "=r"(t)
-                 : "l"(A.pool.ticket + b)
-                 : "memory");
-    s_last = (t == A.F * A.S - 1);
+    for (int r = 0; r < k; ++r) part[r] = C.top[r];
+    C.last = 0;
+    if (take_ticket) {
+      int t;
+      asm volatile("atom.acq_rel.gpu.global.add.s32 %0, [%1], 1;"
+                   : "=r"(t)
+                   : "l"(A.pool.ticket + b)
+                   : "memory");
+      C.last = (t == A.F * A.S - 1);
+    }
   }
   __syncthreads();
-  if (!s_last) return;
+  return C.last != 0;
+}
+
+// The sequence's last CTA: per-row top-k over the chunk lists, children,
+// next frontier.
+__device__ void merge_sequence(const LevelParams& A, int b, MergeShared& M) {
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  const int k = A.k;
   const int F = A.F;
   int* front = A.pool.frontier + (size_t)b * k;
   float* fsc = A.pool.fscore + (size_t)b * k;
@@ -441,12 +457,157 @@ __global__ void __launch_bounds__(kLvThreads, 2) expand_level_kernel(const Level
     }
   }
   if (tid == 0) A.pool.count[b] = base + nc;
+}
+
+// One level.  CTA (row, chunk): exact top-k of the chunk -> partial list.
+// The sequence's last CTA: per-row top-k, children, next frontier.
+template <int VEC>
+__global__ void __launch_bounds__(kLvThreads, 2) expand_level_kernel(const LevelParams A) {
+  pdl_begin();
+  __shared__ ChunkShared C;
+  __shared__ MergeShared M;
+  const int tid = threadIdx.x;
+  const int row = blockIdx.x / A.S, chunk = blockIdx.x % A.S;
+  const int b = row / A.F, f = row % A.F;
+  const int k = A.k;
+  const int local_row = (A.level == 0) ? 0 : 1 + (A.level - 1) * k + f;
+  const float* src = A.logp + ((size_t)b * A.R + local_row) * A.V;
+  const int c0 = chunk * (kLvThreads * 4 * VEC);
+  // ---- chunk in registers: element c0 + (j * threads + tid) * 4 + e
+  float v[VEC][4];
+#pragma unroll
+  for (int j = 0; j < VEC; ++j) {
+    const int i0 = c0 + (j * kLvThreads + tid) * 4;
+    if (A.vec_ok && i0 + 4 <= A.V) {
+      const float4 x = __ldg(reinterpret_cast<const float4*>(src + i0));
+      v[j][0] = x.x;
+      v[j][1] = x.y;
+      v[j][2] = x.z;
+      v[j][3] = x.w;
+    } else {
+#pragma unroll
+      for (int e = 0; e < 4; ++e) v[j][e] = (i0 + e < A.V) ? __ldg(src + i0 + e) : 0.f;
+    }
+  }
+  if (!chunk_topk<VEC>(A, row, chunk, v, C)) return;
+  merge_sequence(A, b, M);
   if (A.fused) {
     // the last level: this CTA holds the sequence's complete pool
     __threadfence_block();
     __syncthreads();
     extern __shared__ __align__(16) unsigned char dyn_smem[];
     finalize_sequence(A.fin, b, dyn_smem);
+  }
+}
+
+// Streaming variant for levels larger than one wave of CTAs: persistent CTAs
+// walk a contiguous range of chunks (8192 tokens each) through a two-stage
+// ring of bulk copies into shared memory, so the next chunk arrives while
+// the current one is ranked.  A CTA counts its chunks of a sequence on the
+// sequence's ticket once, when it leaves that sequence; the CTA that
+// completes a sequence merges it before moving on.
+constexpr int kStreamVec = kMaxVec;
+constexpr int kStreamChunk = kLvThreads * 4 * kStreamVec;   // tokens per chunk
+constexpr int kStreamStages = 2;
+constexpr size_t kStreamSmem = (size_t)kStreamStages * kStreamChunk * 4;
+
+__device__ __forceinline__ void bulk_load(void* dst, const void* src, uint32_t bytes,
+                                          uint64_t* bar) {
+  asm volatile(
+      "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::
+          "r"(tc::smem_u32(dst)),
+      "l"(src), "r"(bytes), "r"(tc::smem_u32(bar))
+      : "memory");
+}
+
+__global__ void __launch_bounds__(kLvThreads, 2)
+expand_level_stream_kernel(const LevelParams A, int total_chunks) {
+  pdl_begin();
+  __shared__ ChunkShared C;
+  __shared__ MergeShared M;
+  __shared__ uint64_t full[kStreamStages];
+  __shared__ int abort_flag, s_last;
+  extern __shared__ __align__(128) unsigned char stage_mem[];   // kStreamSmem bytes
+  const int tid = threadIdx.x;
+  const int k = A.k;
+  const int per_seq = A.F * A.S;
+  const int id0 = (int)((long long)total_chunks * blockIdx.x / gridDim.x);
+  const int id1 = (int)((long long)total_chunks * (blockIdx.x + 1) / gridDim.x);
+  auto issue = [&](int id, int st) {
+    const int row = id / A.S, chunk = id % A.S;
+    const int b = row / A.F, f = row % A.F;
+    const int local_row = (A.level == 0) ? 0 : 1 + (A.level - 1) * k + f;
+    const int c0 = chunk * kStreamChunk;
+    const uint32_t bytes = (uint32_t)min(kStreamChunk, A.V - c0) * 4u;   // V % 4 == 0
+    tc::mbar_arrive_expect_tx(&full[st], bytes);
+    bulk_load(stage_mem + (size_t)st * kStreamChunk * 4,
+              A.logp + ((size_t)b * A.R + local_row) * A.V + c0, bytes, &full[st]);
+  };
+  if (tid == 0) {
+    for (int st = 0; st < kStreamStages; ++st) tc::mbar_init(&full[st], 1);
+    abort_flag = 0;
+    tc::fence_barrier_init();
+    for (int st = 0; st < kStreamStages; ++st)
+      if (id0 + st < id1) issue(id0 + st, st);
+  }
+  __syncthreads();
+  // count `n` finished chunks of sequence b; merge it if they were the last
+  auto leave_sequence = [&](int b, int n) {
+    if (tid == 0) {
+      int t;
+      asm volatile("atom.acq_rel.gpu.global.add.s32 %0, [%1], %2;"
+                   : "=r"(t)
+                   : "l"(A.pool.ticket + b), "r"(n)
+                   : "memory");
+      s_last = (t + n == per_seq);
+    }
+    __syncthreads();
+    if (s_last) merge_sequence(A, b, M);
+    __syncthreads();
+  };
+  int i = 0, cur_b = -1, cur_n = 0;
+  bool aborted = false;
+  for (int id = id0; id < id1; ++id, ++i) {
+    const int st = i % kStreamStages;
+    const bool got =
+        tc::mbar_wait(&full[st], (uint32_t)((i / kStreamStages) & 1), &abort_flag, A.status);
+    if (!__syncthreads_and(got)) {
+      aborted = true;
+      break;
+    }
+    float v[kStreamVec][4];
+    const float4* sm4 = reinterpret_cast<const float4*>(stage_mem + (size_t)st * kStreamChunk * 4);
+#pragma unroll
+    for (int j = 0; j < kStreamVec; ++j) {
+      const float4 x = sm4[j * kLvThreads + tid];
+      v[j][0] = x.x;
+      v[j][1] = x.y;
+      v[j][2] = x.z;
+      v[j][3] = x.w;
+    }
+    __syncthreads();   // the stage is in registers: refill it
+    if (tid == 0 && id + kStreamStages < id1) {
+      asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+      issue(id + kStreamStages, st);
+    }
+    const int row = id / A.S, chunk = id % A.S;
+    const int b = row / A.F;
+    if (b != cur_b) {
+      if (cur_b >= 0) leave_sequence(cur_b, cur_n);
+      cur_b = b;
+      cur_n = 0;
+    }
+    chunk_topk<kStreamVec>(A, row, chunk, v, C, false);
+    ++cur_n;
+  }
+  if (!aborted && cur_b >= 0) leave_sequence(cur_b, cur_n);
+  if (aborted && tid == 0) {
+    // let the copies still in flight land before the CTA leaves
+    int never = 0;
+    for (int j = i; j < i + kStreamStages; ++j)
+      if (id0 + j < id1)
+        tc::mbar_wait(&full[j % kStreamStages], (uint32_t)((j / kStreamStages) & 1), &never,
+                      nullptr, 200000000ll);
   }
 }
 
@@ -681,6 +842,28 @@ extern "C" eagle_status eagle_draft_expand(int B, int V, int k, int depth, int l
   void (*kern)(const LevelParams) = (cp.vec == 1)   ? expand_level_kernel<1>
                                     : (cp.vec == 2) ? expand_level_kernel<2>
                                                     : expand_level_kernel<4>;
+  // levels beyond one wave even at the largest chunks stream through
+  // persistent CTAs (no finalize fusion there)
+  const long long total_chunks = (long long)B * A.F * A.S;
+  const bool stream_it = A.vec_ok && cp.vec == kMaxVec && total_chunks > kOneWave;
+  if (stream_it) {
+    A.fused = false;
+    A.fin = F;
+    static bool attr = false;
+    if (!attr) {
+      if (cudaFuncSetAttribute(expand_level_stream_kernel,
+                               cudaFuncAttributeMaxDynamicSharedMemorySize,
+                               (int)kStreamSmem) != cudaSuccess)
+        return EAGLE_ERR_CUDA;
+      attr = true;
+    }
+    const int grid = (int)std::min<long long>(total_chunks, kOneWave);
+    const eagle_status st =
+        launch_status(launch_pdl(expand_level_stream_kernel, dim3(grid), dim3(kLvThreads),
+                                 kStreamSmem, s, A, (int)total_chunks));
+    if (st != EAGLE_OK || finalize != 2) return st;
+    return launch_finalize();
+  }
   // fuse the finalize when its shared memory fits beside the level's
   A.fused = (finalize == 2) && fin_smem <= kFusedSmemMax;
   A.fin = F;

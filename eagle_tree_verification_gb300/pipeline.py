@@ -200,9 +200,10 @@ class TreeVerifyStep:
                                     self.out_tokens, self.status, max_nodes=self.max_nodes,
                                     max_depth=s.max_depth, mode=s.sample_mode, stream=stream)
 
-    def run(self, stream=None) -> None:
-        """The whole step: tree build (if EAGLE-2), attention, LM head, accept."""
-        if self.s.k:
+    def run(self, stream=None, build_tree: bool = True) -> None:
+        """The whole step: tree build (if EAGLE-2), attention, LM head, accept.
+        build_tree=False verifies the tree already in the buffers."""
+        if self.s.k and build_tree:
             self.run_expand(stream)
         self.run_attn(stream)
         self.run_lmhead(stream)
@@ -221,17 +222,17 @@ class TreeVerifyStep:
         n += 1                                   # acceptance
         return n
 
-    def capture(self, stream=None):
+    def capture(self, stream=None, build_tree: bool = True):
         """Capture run() into a CUDA graph (after one eager warm-up)."""
         torch = self.torch
         st = torch.cuda.Stream() if stream is None else stream
         st.wait_stream(torch.cuda.current_stream())
         with torch.cuda.stream(st):
-            self.run()
+            self.run(build_tree=build_tree)
         torch.cuda.current_stream().wait_stream(st)
         torch.cuda.synchronize()
         g = torch.cuda.CUDAGraph()
         with torch.cuda.graph(g, stream=st):
-            self.run()
+            self.run(build_tree=build_tree)
         torch.cuda.synchronize()
         return g

@@ -44,6 +44,10 @@ def _gpu_tree(E, lp, B, V, k, depth, budget, root_token, fused=False):
     (1, 128256, 8, 7, [64], 3.0),             # LLaMA-3-8B shaped tree
     (2, 128256, 8, 8, [64, 33], 3.0),         # LLaMA-3-70B / batched shape
     (2, 5000, 32, 3, [500, 0], 0.5),          # k at its limit, an empty budget
+    # levels larger than one wave of CTAs: persistent streaming through
+    # shared memory, ragged last chunks
+    (8, 40000, 8, 3, [20, 64, 0, 5, 64, 64, 33, 1], 3.0),
+    (8, 70004, 6, 3, [30, 12, 64, 7, 1, 0, 9, 40], 3.0),
 ])
 @pytest.mark.parametrize("fused", [False, True])
 def test_expand_matches_oracle(B, V, k, depth, budgets, sigma, fused):
