@@ -212,6 +212,37 @@ struct RoundSlot {
   float qt, pt;           // q_k[t], p_k[t] if this CTA owns the tested token t
 };
 
+// One pass over this thread's slice entries.  UPD: the rejection update of
+// token t_rej -- q <- fp32(W(max(0, q - p))) * rz (when the residual sum is
+// positive), and in NO_REPLACE mode p <- fp32(W(p)) * rsp with t_rej's entry
+// zeroed.  SUMS (on the updated values): the residual weight sum, the draft
+// weight sum without t_next, and q, p at t_next into `slot`.  One pass per
+// rejection round, the same operations as an update followed by the sums.
+template <int E, bool UPD, bool SUMS>
+__device__ __forceinline__ void walk_pass(float (&q)[E], float (&p)[E], int v0, int nv,
+                                          bool no_replace, int t_rej, float rz, float rsp,
+                                          bool z_pos, int t_next, unsigned long long& sw,
+                                          unsigned long long& sp, RoundSlot& slot) {
+  const int tid = threadIdx.x;
+#pragma unroll
+  for (int e = 0; e < E; ++e) {
+    const int i = tid + e * kStochThreads;
+    if (UPD) {
+      const float qa = q[e], pa = p[e];
+      if (z_pos) q[e] = __fmul_rn(fixed40_f(fmaxf(0.f, __fsub_rn(qa, pa))), rz);
+      if (no_replace) p[e] = (v0 + i == t_rej) ? 0.f : __fmul_rn(fixed40_f(pa), rsp);
+    }
+    if (SUMS) {
+      sw += fixed40_int(fmaxf(0.f, __fsub_rn(q[e], p[e])));
+      if (no_replace && v0 + i != t_next) sp += fixed40_int(p[e]);
+      if (i < nv && v0 + i == t_next) {
+        slot.qt = q[e];
+        slot.pt = p[e];
+      }
+    }
+  }
+}
+
 // Element e of thread `tid` is vocabulary entry v0 + tid + kStochThreads*e.
 template <int E>
 __global__ void __launch_bounds__(kStochThreads)
@@ -323,22 +354,11 @@ accept_stochastic_kernel(const StochParams P) {
       if (__syncthreads_or(bad) && tid == 0) fail(P.status, EAGLE_ERR_NUMERIC);
     }
 
-    bool moved = false;
-    for (int j = 0; j < nk; ++j) {
-      const int c = s_kids[j];
-      const int t = s_tok[c];
-      // sums as if child c were rejected, and the tested values q_k[t], p_k[t]
-      unsigned long long sw = 0, sp = 0;
-#pragma unroll
-      for (int e = 0; e < E; ++e) {
-        const int i = tid + e * kStochThreads;
-        sw += fixed40_int(fmaxf(0.f, __fsub_rn(q[e], p[e])));
-        if (no_replace && v0 + i != t) sp += fixed40_int(p[e]);
-        if (i < nv && v0 + i == t) {
-          s_slot[par].qt = q[e];
-          s_slot[par].pt = p[e];
-        }
-      }
+    // the cluster's totals for one round: residual and draft weight sums,
+    // and q, p at the tested token (from the CTA that owns it)
+    unsigned long long Z = 0, SP = 0;
+    float qt = 0.f, pt = 0.f;
+    auto reduce_round = [&](unsigned long long sw, unsigned long long sp, int t) {
       block_sum2_u64(sw, sp, s_red);
       if (tid == 0) {
         s_slot[par].w = sw;
@@ -363,9 +383,24 @@ accept_stochastic_kernel(const StochParams P) {
         }
       }
       __syncthreads();
-      const unsigned long long Z = s_bc[0], SP = s_bc[1];
-      const float qt = s_test[0], pt = s_test[1];
+      Z = s_bc[0];
+      SP = s_bc[1];
+      qt = s_test[0];
+      pt = s_test[1];
       par ^= 1;
+    };
+    if (nk > 0) {
+      // sums as if the first child were rejected, and its tested values
+      unsigned long long sw = 0, sp = 0;
+      const int t = s_tok[s_kids[0]];
+      walk_pass<E, false, true>(q, p, v0, nv, no_replace, -1, 0.f, 0.f, false, t, sw, sp,
+                                s_slot[par]);
+      reduce_round(sw, sp, t);
+    }
+    bool moved = false;
+    for (int j = 0; j < nk; ++j) {
+      const int c = s_kids[j];
+      const int t = s_tok[c];
       const float ua = P.u_accept[t0 + c];
       if (!(ua >= 0.f && ua < 1.f) && writer && tid == 0) fail(P.status, EAGLE_ERR_INVALID_ARG);
       // exact: a product of two fp32 values is exact in fp64
@@ -389,12 +424,17 @@ accept_stochastic_kernel(const StochParams P) {
       // (NO_REPLACE); every operation rounds to nearest once
       const float rz = (Z > 0ull) ? __frcp_rn(__ull2float_rn(Z)) : 0.f;
       const float rsp = (SP > 0ull) ? __frcp_rn(__ull2float_rn(SP)) : 0.f;
-#pragma unroll
-      for (int e = 0; e < E; ++e) {
-        const int i = tid + e * kStochThreads;
-        const float qa = q[e], pa = p[e];
-        if (Z > 0ull) q[e] = __fmul_rn(fixed40_f(fmaxf(0.f, __fsub_rn(qa, pa))), rz);
-        if (no_replace) p[e] = (v0 + i == t) ? 0.f : __fmul_rn(fixed40_f(pa), rsp);
+      if (j + 1 < nk) {
+        // update, and the next child's sums, in one pass
+        unsigned long long sw = 0, sp = 0;
+        const int tn = s_tok[s_kids[j + 1]];
+        walk_pass<E, true, true>(q, p, v0, nv, no_replace, t, rz, rsp, Z > 0ull, tn, sw, sp,
+                                 s_slot[par]);
+        reduce_round(sw, sp, tn);
+      } else {
+        unsigned long long sw = 0, sp = 0;
+        walk_pass<E, true, false>(q, p, v0, nv, no_replace, t, rz, rsp, Z > 0ull, -1, sw, sp,
+                                  s_slot[par]);
       }
     }
     if (moved) continue;

@@ -402,13 +402,18 @@ __device__ void merge_sequence(const LevelParams& A, int b, MergeShared& M) {
   const int F = A.F;
   int* front = A.pool.frontier + (size_t)b * k;
   float* fsc = A.pool.fscore + (size_t)b * k;
-  if (tid < F) {
-    M.fidx[tid] = (A.level == 0) ? -1 : __ldcg(front + tid);
-    M.fsc[tid] = (A.level == 0) ? 0.f : __ldcg(fsc + tid);
-  }
-  if (tid == 0) {
-    M.base = __ldcg(A.pool.count + b);
-    A.pool.ticket[b] = 0;  // ready for the next level
+  // frontier scores and the pool fill, by the last warp (which has no row
+  // when F < warps), so the row warps start at once
+  {
+    const int lt = tid - (kLvThreads - 32);
+    if (lt >= 0 && lt < F) {
+      M.fidx[lt] = (A.level == 0) ? -1 : __ldcg(front + lt);
+      M.fsc[lt] = (A.level == 0) ? 0.f : __ldcg(fsc + lt);
+    }
+    if (lt == 31) {
+      M.base = __ldcg(A.pool.count + b);
+      A.pool.ticket[b] = 0;  // ready for the next level
+    }
   }
   const int n = A.S * k;
   for (int ff = warp; ff < F; ff += kLvWarps)

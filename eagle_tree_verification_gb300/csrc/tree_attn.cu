@@ -277,7 +277,6 @@ tree_attn_tc_kernel(const __grid_constant__ CUtensorMap map_q,
                     const __grid_constant__ CUtensorMap map_vc,
                     const __grid_constant__ CUtensorMap map_kt,
                     const __grid_constant__ CUtensorMap map_vt, const AttParams A) {
-  pdl_begin();
   extern __shared__ __align__(1024) unsigned char smem_raw[];
   unsigned char* base = reinterpret_cast<unsigned char*>(
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~(uintptr_t)1023);
@@ -295,33 +294,20 @@ tree_attn_tc_kernel(const __grid_constant__ CUtensorMap map_q,
   const int g = (tile / A.MT) % A.Hkv;
   const int b = tile / (A.MT * A.Hkv);
 
-  const int t0 = A.tree_off[b];
-  const int n = A.tree_off[b + 1] - t0;
+  // The KV cache and its offsets are resident state that no earlier kernel
+  // of the step writes: the first cache blocks are requested before waiting
+  // for the previous kernel (the tree and the queries come after the wait).
   const int kv0 = A.kv_off[b];
   const int L = A.kv_off[b + 1] - kv0;
-  const bool bad_seq = (n < 1 || n > A.max_nodes || L < 0 || L > A.max_kv);
-  const int nodes_per_tile = 128 / A.G;
-  // the whole cluster (same tile) leaves together
-  if (bad_seq || mt * nodes_per_tile >= n) {
-    if (bad_seq && c == 0 && mt == 0 && threadIdx.x == 0) fail(A.status, EAGLE_ERR_INVALID_TREE);
-    return;
-  }
+  const bool bad_kv = (L < 0 || L > A.max_kv);
   // chunks that carry cache keys of this sequence; the last one also takes
   // the tree keys
-  const int n_chunks = max(1, (L + A.CK - 1) / A.CK);
+  const int n_chunks = bad_kv ? 1 : max(1, (L + A.CK - 1) / A.CK);
   const int key_begin = c * A.CK;
-  const int key_end = min(L, key_begin + A.CK);
+  const int key_end = bad_kv ? key_begin : min(L, key_begin + A.CK);
   const int n_cache_blk = (key_end > key_begin) ? (key_end - key_begin + kKeyBlk - 1) / kKeyBlk : 0;
-  const bool with_tree = (c == n_chunks - 1);
-  const int n_tree_blk = with_tree ? (n + kKeyBlk - 1) / kKeyBlk : 0;
-  const int nblk = n_cache_blk + n_tree_blk;
-  // row quads (32 rows) holding at least one node of the tile
-  int active_quads = 0;
-  for (int q = 0; q < 4; ++q) active_quads += ((mt * 128 + q * 32) / A.G < n);
-  const int active_warps = 2 * active_quads;
-  volatile int* abort_flag = &sh->abort_flag;
-  int* status = A.status;
-
+  const int early = min(2, n_cache_blk);
+  int t0 = 0;   // set after the dependency wait
   auto block_row = [&](int j) {   // first key row of block j in its tensor
     return (j < n_cache_blk) ? kv0 + key_begin + j * kKeyBlk : t0 + (j - n_cache_blk) * kKeyBlk;
   };
@@ -341,7 +327,6 @@ tree_attn_tc_kernel(const __grid_constant__ CUtensorMap map_q,
     tc::tma_load_3d(vd, mv, &sh->v_full[st], 0, g, block_row(j));
     tc::tma_load_3d(vd + kHalfBytes, mv, &sh->v_full[st], 64, g, block_row(j));
   };
-
   if (threadIdx.x == 0) {
     tc::mbar_init(&sh->q_full, 1);
     for (int i = 0; i < 2; ++i) {
@@ -350,6 +335,42 @@ tree_attn_tc_kernel(const __grid_constant__ CUtensorMap map_q,
       tc::mbar_init(&sh->v_full[i], 1);
       tc::mbar_init(&sh->v_empty[i], 1);
     }
+    tc::fence_barrier_init();
+    for (int j = 0; j < early; ++j) {
+      load_k(j);
+      load_v(j);
+    }
+  }
+  pdl_begin();
+
+  t0 = A.tree_off[b];
+  const int n = A.tree_off[b + 1] - t0;
+  const bool bad_seq = bad_kv || n < 1 || n > A.max_nodes;
+  const int nodes_per_tile = 128 / A.G;
+  // the whole cluster (same tile) leaves together
+  if (bad_seq || mt * nodes_per_tile >= n) {
+    if (bad_seq && c == 0 && mt == 0 && threadIdx.x == 0) fail(A.status, EAGLE_ERR_INVALID_TREE);
+    if (threadIdx.x == 0) {
+      // the cache blocks requested above land before the CTA leaves
+      int never = 0;
+      for (int j = 0; j < early; ++j) {
+        tc::mbar_wait(&sh->k_full[j], 0, &never, nullptr, 200000000ll);
+        tc::mbar_wait(&sh->v_full[j], 0, &never, nullptr, 200000000ll);
+      }
+    }
+    return;
+  }
+  const bool with_tree = (c == n_chunks - 1);
+  const int n_tree_blk = with_tree ? (n + kKeyBlk - 1) / kKeyBlk : 0;
+  const int nblk = n_cache_blk + n_tree_blk;
+  // row quads (32 rows) holding at least one node of the tile
+  int active_quads = 0;
+  for (int q = 0; q < 4; ++q) active_quads += ((mt * 128 + q * 32) / A.G < n);
+  const int active_warps = 2 * active_quads;
+  volatile int* abort_flag = &sh->abort_flag;
+  int* status = A.status;
+
+  if (threadIdx.x == 0) {
     tc::mbar_init(&sh->s_full, 1);
     tc::mbar_init(&sh->s_empty, active_warps);
     tc::mbar_init(&sh->p_full, active_warps);
@@ -359,13 +380,13 @@ tree_attn_tc_kernel(const __grid_constant__ CUtensorMap map_q,
     tc::mbar_init(&sh->fbar, 32 * active_warps);
     sh->abort_flag = 0;
     tc::fence_barrier_init();
-    // the first copies start before the rest of the set-up
+    // the queries and the first blocks not requested before the wait
     if (nblk > 0) {
       tc::mbar_arrive_expect_tx(&sh->q_full, kTileBytes);
       const int node0 = t0 + mt * nodes_per_tile;
       tc::tma_load_3d(q_sm, &map_q, &sh->q_full, 0, g * A.G, node0);
       tc::tma_load_3d(q_sm + kHalfBytes, &map_q, &sh->q_full, 64, g * A.G, node0);
-      for (int j = 0; j < min(2, nblk); ++j) {
+      for (int j = early; j < min(2, nblk); ++j) {
         load_k(j);
         load_v(j);
       }
