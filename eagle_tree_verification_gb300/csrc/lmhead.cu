@@ -225,27 +225,37 @@ lmhead_finalize_kernel(int T, int V, float temperature, const Partial* __restric
 //
 // MMA D[t, v] = sum_k h[t, k] W[v, k]: M = 128 tree rows (TMEM lanes; rows at
 // or past T are don't-care), N = one vocabulary block of up to `blk` rows
-// (128 or 256), K in 64-element chunks (128-byte-swizzled K-major tiles).
-// Each CTA owns a balanced slice of the vocabulary in units of 32 rows, cut
-// into blocks.  Two TMEM accumulators alternate between blocks, so the
-// softmax epilogue of one block overlaps the MMAs of the next.  A W stage is one chunk
-// of one block (<= blk x 128 bytes, TMA boxes of 32 rows); an h stage is one
-// chunk of the real tree rows (T rounded up to 8).  W never depends on an
-// earlier kernel, so the first W stages are requested before the kernel
-// waits for its predecessor.
+// (256), K in 64-element chunks (128-byte-swizzled K-major tiles).  The
+// vocabulary is cut into balanced slices in units of 32 rows, each slice into
+// blocks.  Two TMEM accumulators alternate between blocks, so the softmax
+// epilogue of one block overlaps the MMAs of the next.  A W stage is one
+// chunk of one block (<= blk x 128 bytes, TMA boxes of 32 rows); an h stage is
+// one chunk of the CTA's tree rows.
+//
+// More than 128 tree rows: a cluster of C CTAs shares one vocabulary slice,
+// each CTA holding its own 128-row tile of h and its own accumulators.  Every
+// W stage is loaded once for the whole cluster: each CTA requests every C-th
+// box of it with TMA multicast into the same stage of all C CTAs, and a stage
+// is refilled only after all C CTAs' MMAs have released it (the MMA commit
+// arrives on the stage's barrier in every CTA).  W then streams from memory
+// once per 128*C tree rows while each CTA does the work of the one-tile case.
+// W never depends on an earlier kernel, so the first W stages are requested
+// before the kernel waits for its predecessor.
 // ---------------------------------------------------------------------------
 constexpr int kTcThreads = 320;   // warp 0 TMA, warp 1 MMA, warps 2-9 epilogue
 constexpr int kEpiWarps = 8;      // two per TMEM lane quarter, one per column half
 constexpr int kBK = 64;           // bf16 per 128-byte swizzled row (one chunk)
 constexpr int kUnit = 32;         // vocabulary rows per TMA box
 constexpr int kBlkMax = 256;      // vocabulary rows per MMA (its N), at most
-constexpr int kHStages = 4;
+constexpr int kTileRows = 128;    // tree rows per CTA (the MMA's M)
+constexpr int kMaxCluster = 4;    // row tiles sharing one W stream
+constexpr int kMaxHStages = 4;
 constexpr int kMaxWStages = 12;
 constexpr size_t kSmemLimit = 227 * 1024;
 constexpr size_t kTcSharedBytes = 1024 + 2 * 128 * 16;
 
 struct TcShared {
-  uint64_t h_full[kHStages], h_empty[kHStages];
+  uint64_t h_full[kMaxHStages], h_empty[kMaxHStages];
   uint64_t w_full[kMaxWStages], w_empty[kMaxWStages];
   uint64_t tmem_full[2], tmem_empty[2], xbar, drain;
   uint32_t tmem_base;
@@ -255,21 +265,21 @@ struct TcShared {
 };
 
 struct TcLayout {
-  int t_pad, h_stage_bytes, blk, w_stage_bytes, w_stages;
+  int h_rows, h_stage_bytes, h_stages, blk, w_stage_bytes, w_stages;
   size_t smem;
 };
 
-// `slice_rows`: vocabulary rows of the largest CTA slice.
-TcLayout tc_layout(int T, int slice_rows) {
+// `h_rows`: tree rows of one h stage (one CTA's tile, rounded up to 8).
+TcLayout tc_layout(int h_rows) {
   TcLayout L;
-  L.t_pad = ((T + 7) / 8) * 8;
-  L.h_stage_bytes = L.t_pad * 128;
+  L.h_rows = h_rows;
+  L.h_stage_bytes = h_rows * 128;
   // 256-row blocks: narrower MMAs cost more shared-memory reads per W byte
   // than the overlap of a short slice's epilogue gains
-  (void)slice_rows;
   L.blk = kBlkMax;
+  L.h_stages = kMaxHStages;
   L.w_stage_bytes = L.blk * 128;
-  const size_t fixed = 1024 + (size_t)kHStages * L.h_stage_bytes + kTcSharedBytes;
+  const size_t fixed = 1024 + (size_t)L.h_stages * L.h_stage_bytes + kTcSharedBytes;
   L.w_stages = (int)std::min<size_t>(kMaxWStages, (kSmemLimit - fixed) / L.w_stage_bytes);
   L.smem = fixed + (size_t)L.w_stages * L.w_stage_bytes;
   return L;
@@ -302,39 +312,60 @@ __device__ __forceinline__ void merge_partial(Partial& a, const Partial& b, floa
   a = r;
 }
 
+// T: tree rows of this launch (at most 128 * C); C: CTAs per cluster, 1
+// exactly when MULTI is false.  Partials go to part[t * slices + slice].
+template <bool MULTI>
 __global__ void __launch_bounds__(kTcThreads, 1)
 lmhead_tc_kernel(const __grid_constant__ CUtensorMap map_h, const __grid_constant__ CUtensorMap map_w,
                  int T, int H, int V, float temperature, float* __restrict__ z_out,
-                 Partial* __restrict__ part, int n_units, int h_stage_bytes, int blk_max,
-                 int w_stages, int* status) {
+                 Partial* __restrict__ part, int n_units, int h_stage_bytes, int h_stages,
+                 int blk_max, int w_stages, int C, int* status) {
   extern __shared__ __align__(1024) unsigned char smem_raw[];
   unsigned char* base = reinterpret_cast<unsigned char*>(
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~(uintptr_t)1023);
   unsigned char* h_smem = base;
-  unsigned char* w_smem = base + kHStages * h_stage_bytes;
+  unsigned char* w_smem = base + h_stages * h_stage_bytes;
   const int w_stage_bytes = blk_max * 128;
   TcShared* sh = reinterpret_cast<TcShared*>(w_smem + (size_t)w_stages * w_stage_bytes);
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int G = gridDim.x;
-  // this CTA's slice of the vocabulary: rows [r_begin, r_end), 32-row units
-  const int u0 = (int)((long long)n_units * blockIdx.x / G);
-  const int u1 = (int)((long long)n_units * (blockIdx.x + 1) / G);
+  if (!MULTI) C = 1;
+  const int rank = MULTI ? (int)tc::cluster_ctarank() : 0;   // this CTA's row tile
+  const uint16_t all_ctas = (uint16_t)((1u << C) - 1u);
+  const int slices = gridDim.x / C;
+  const int slice = blockIdx.x / C;
+  // the cluster's slice of the vocabulary: rows [r_begin, r_end), 32-row units
+  const int u0 = (int)((long long)n_units * slice / slices);
+  const int u1 = (int)((long long)n_units * (slice + 1) / slices);
   const int r_begin = u0 * kUnit, r_end = u1 * kUnit;
   const int n_blocks = (r_end - r_begin + blk_max - 1) / blk_max;
   const int KB = (H + kBK - 1) / kBK;
+  const int total = n_blocks * KB;   // (block, chunk) pairs, block-major
   auto blk_rows = [&](int blk) { return min(blk_max, r_end - (r_begin + blk * blk_max)); };
+  // this CTA's share of a W stage (chunk kb of the block at row y0):
+  // boxes rank, rank + C, ... (multicast to all)
+  auto load_w_box = [&](int stage, int rows, int kb, int y0, uint64_t pol) {
+    tc::mbar_arrive_expect_tx(&sh->w_full[stage], (uint32_t)(rows * 128));
+    unsigned char* dst = w_smem + (size_t)stage * w_stage_bytes;
+    for (int u = rank * kUnit; u < rows; u += C * kUnit) {
+      if (MULTI)
+        tc::tma_load_2d_mc_hint(dst + u * 128, &map_w, &sh->w_full[stage], kb * kBK, y0 + u,
+                                all_ctas, pol);
+      else
+        tc::tma_load_2d_hint(dst + u * 128, &map_w, &sh->w_full[stage], kb * kBK, y0 + u, pol);
+    }
+  };
   // W stages requested before waiting for the previous kernel
-  const int w_early = min(w_stages, n_blocks * KB);
+  const int w_early = min(w_stages, total);
 
   if (threadIdx.x == 0) {
-    for (int i = 0; i < kHStages; ++i) {
+    for (int i = 0; i < h_stages; ++i) {
       tc::mbar_init(&sh->h_full[i], 1);
       tc::mbar_init(&sh->h_empty[i], 1);
     }
     for (int i = 0; i < w_stages; ++i) {
       tc::mbar_init(&sh->w_full[i], 1);
-      tc::mbar_init(&sh->w_empty[i], 1);
+      tc::mbar_init(&sh->w_empty[i], C);   // every CTA's MMAs release the stage
     }
     for (int i = 0; i < 2; ++i) {
       tc::mbar_init(&sh->tmem_full[i], 1);
@@ -346,18 +377,16 @@ lmhead_tc_kernel(const __grid_constant__ CUtensorMap map_h, const __grid_constan
     sh->consumed_w = 0;
     sh->consumed_h = 0;
     tc::fence_barrier_init();
+  }
+  // the peers' barriers exist before any multicast reaches them
+  if (MULTI) tc::cluster_sync_all();
+  if (threadIdx.x == 0) {
     tc::prefetch_tensormap(&map_h);
     tc::prefetch_tensormap(&map_w);
-    // the first W stages: block 0, chunks 0 .. w_early-1 (the loop's order)
     const uint64_t pol_w = tc::policy_evict_first();
     for (int i = 0; i < w_early; ++i) {
-      const int blk = i / KB, kb = i % KB;
-      const int rows = blk_rows(blk);
-      tc::mbar_arrive_expect_tx(&sh->w_full[i], (uint32_t)(rows * 128));
-      unsigned char* dst = w_smem + (size_t)i * w_stage_bytes;
-      for (int u = 0; u < rows; u += kUnit)
-        tc::tma_load_2d_hint(dst + u * 128, &map_w, &sh->w_full[i], kb * kBK,
-                             r_begin + blk * blk_max + u, pol_w);
+      const int blk = i / KB;
+      load_w_box(i, blk_rows(blk), i - blk * KB, r_begin + blk * blk_max, pol_w);
     }
   }
   if (warp == 1) {
@@ -376,40 +405,44 @@ lmhead_tc_kernel(const __grid_constant__ CUtensorMap map_h, const __grid_constan
     if (lane == 0) {
       const uint64_t pol_w = tc::policy_evict_first();
       const uint64_t pol_h = tc::policy_evict_last();
-      int hs = 0, ws = 0, issued_h = 0, issued_w = 0;
+      // h chunk i and W stage i (past the ones requested early) in turn;
+      // nested loops keep divisions off the refill path
+      int hs = 0, ws = 0, issued_h = 0, issued_w = w_early;
       uint32_t hph = 0, wph = 0;
       bool ok = true;
+      int i = 0;
       for (int blk = 0; blk < n_blocks && ok; ++blk) {
-        const int row0 = r_begin + blk * blk_max;
         const int rows = blk_rows(blk);
-        for (int kb = 0; kb < KB && ok; ++kb) {
+        const int y0 = r_begin + blk * blk_max;
+        for (int kb = 0; kb < KB && ok; ++kb, ++i) {
           if (!(ok = tc::mbar_wait(&sh->h_empty[hs], hph ^ 1, abort_flag, status))) break;
           tc::mbar_arrive_expect_tx(&sh->h_full[hs], (uint32_t)h_stage_bytes);
-          tc::tma_load_2d_hint(h_smem + hs * h_stage_bytes, &map_h, &sh->h_full[hs], kb * kBK, 0,
-                               pol_h);
+          tc::tma_load_2d_hint(h_smem + hs * h_stage_bytes, &map_h, &sh->h_full[hs], kb * kBK,
+                               rank * kTileRows, pol_h);
           ++issued_h;
-          if (++hs == kHStages) { hs = 0; hph ^= 1; }
-          if (issued_w >= w_early) {
+          if (++hs == h_stages) { hs = 0; hph ^= 1; }
+          if (i >= w_early) {
             if (!(ok = tc::mbar_wait(&sh->w_empty[ws], wph ^ 1, abort_flag, status))) break;
-            tc::mbar_arrive_expect_tx(&sh->w_full[ws], (uint32_t)(rows * 128));
-            unsigned char* dst = w_smem + (size_t)ws * w_stage_bytes;
-            for (int u = 0; u < rows; u += kUnit)
-              tc::tma_load_2d_hint(dst + u * 128, &map_w, &sh->w_full[ws], kb * kBK, row0 + u,
-                                   pol_w);
+            load_w_box(ws, rows, kb, y0, pol_w);
+            ++issued_w;
           }
-          ++issued_w;
           if (++ws == w_stages) { ws = 0; wph ^= 1; }
         }
+      }
+      if (ok && MULTI) {
+        // the last release of every stage, the peers' included, has arrived:
+        // nothing more reaches this CTA's shared memory
+        for (int i = max(0, total - w_stages); i < total && ok; ++i)
+          ok = tc::mbar_wait(&sh->w_empty[i % w_stages], (i / w_stages) & 1, abort_flag, status);
       }
       if (!ok) {
         // let every copy still in flight land before the CTA exits
         int never = 0;
-        const int issued = max(issued_w, w_early);
-        for (int i = *(volatile int*)&sh->consumed_w; i < issued; ++i)
+        for (int i = *(volatile int*)&sh->consumed_w; i < issued_w; ++i)
           tc::mbar_wait(&sh->w_full[i % w_stages], (i / w_stages) & 1, &never, nullptr,
                         200000000ll);
         for (int i = *(volatile int*)&sh->consumed_h; i < issued_h; ++i)
-          tc::mbar_wait(&sh->h_full[i % kHStages], (i / kHStages) & 1, &never, nullptr,
+          tc::mbar_wait(&sh->h_full[i % h_stages], (i / h_stages) & 1, &never, nullptr,
                         200000000ll);
       }
     }
@@ -439,12 +472,15 @@ lmhead_tc_kernel(const __grid_constant__ CUtensorMap map_h, const __grid_constan
             tc::mma_f16(d, tc::desc_kmajor_sw128(a_base + k16 * 32),
                         tc::desc_kmajor_sw128(b_base + k16 * 32), idesc,
                         (kb > 0 || k16 > 0) ? 1u : 0u);
-          tc::mma_commit(&sh->w_empty[ws]);
+          if (MULTI)
+            tc::mma_commit_mc(&sh->w_empty[ws], all_ctas);
+          else
+            tc::mma_commit(&sh->w_empty[ws]);
           tc::mma_commit(&sh->h_empty[hs]);
           *(volatile int*)&sh->consumed_w += 1;
           *(volatile int*)&sh->consumed_h += 1;
           if (++ws == w_stages) { ws = 0; wph ^= 1; }
-          if (++hs == kHStages) { hs = 0; hph ^= 1; }
+          if (++hs == h_stages) { hs = 0; hph ^= 1; }
         }
         if (ok) tc::mma_commit(&sh->tmem_full[ab]);
       }
@@ -457,9 +493,9 @@ lmhead_tc_kernel(const __grid_constant__ CUtensorMap map_h, const __grid_constan
     // ------------------------------------------------------------ epilogue
     const int quad = warp & 3;
     const int chalf = (warp - 2) >> 2;   // second or first half of every block's columns
-    const int t = quad * 32 + lane;      // tree row held by this thread
+    const int t = rank * kTileRows + quad * 32 + lane;   // tree row held by this thread
     const bool row_ok = t < T;
-    const bool quad_live = quad * 32 < T;   // warp-uniform
+    const bool quad_live = rank * kTileRows + quad * 32 < T;   // warp-uniform
     const float k2 = 1.4426950408889634f / temperature;   // log2(e) / temperature
     const bool vec = ((V & 3) == 0);
     Partial p;
@@ -547,12 +583,13 @@ lmhead_tc_kernel(const __grid_constant__ CUtensorMap map_h, const __grid_constan
     }
     if (bad) fail(status, EAGLE_ERR_NUMERIC);
     // the two column halves of every row: half 1 hands its partial to half 0
-    if (chalf == 1) sh->xchg[t] = p;
+    const int tl = quad * 32 + lane;
+    if (chalf == 1) sh->xchg[tl] = p;
     tc::mbar_arrive(&sh->xbar);
     const bool gx = tc::mbar_wait(&sh->xbar, 0, abort_flag, status);
     if (chalf == 0 && row_ok && gx) {
-      merge_partial(p, sh->xchg[t], k2);
-      part[(size_t)t * G + blockIdx.x] = p;
+      merge_partial(p, sh->xchg[tl], k2);
+      part[(size_t)t * slices + slice] = p;
     }
   }
   tc::fence_before_thread_sync();
@@ -561,6 +598,8 @@ lmhead_tc_kernel(const __grid_constant__ CUtensorMap map_h, const __grid_constan
     tc::fence_after_thread_sync();
     tc::tmem_dealloc(tmem, 512);
   }
+  // no CTA leaves while a peer may still deliver into its shared memory
+  if (MULTI) tc::cluster_sync_all();
 }
 
 PFN_cuTensorMapEncodeTiled_v12000 get_encode() {
@@ -601,6 +640,54 @@ int sm_count() {
   return n;
 }
 
+// Clusters of C tensor-core CTAs that fit on the GPU at once (0: none).
+int max_clusters(int C, size_t smem) {
+  static int cached[kMaxCluster + 1] = {};
+  if (!cached[C]) {
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3((unsigned)(C * 64));
+    cfg.blockDim = dim3(kTcThreads);
+    cfg.dynamicSmemBytes = smem;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = (unsigned)C;
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    int n = 0;
+    if (cudaOccupancyMaxActiveClusters(&n, (const void*)lmhead_tc_kernel<true>, &cfg) !=
+        cudaSuccess) {
+      cudaGetLastError();
+      n = 0;
+    }
+    cached[C] = n > 0 ? n : -1;
+  }
+  return std::max(cached[C], 0);
+}
+
+// The tensor-core kernel with programmatic dependent launch, in clusters of
+// C CTAs when C > 1.
+template <typename... Args>
+cudaError_t launch_tc(int C, dim3 grid, size_t smem, cudaStream_t s, Args&&... args) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = grid;
+  cfg.blockDim = dim3(kTcThreads);
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = s;
+  cudaLaunchAttribute attr[2];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  attr[1].id = cudaLaunchAttributeClusterDimension;
+  attr[1].val.clusterDim.x = (unsigned)C;
+  attr[1].val.clusterDim.y = 1;
+  attr[1].val.clusterDim.z = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = (C > 1) ? 2 : 1;
+  return (C > 1) ? cudaLaunchKernelEx(&cfg, lmhead_tc_kernel<true>, std::forward<Args>(args)...)
+                 : cudaLaunchKernelEx(&cfg, lmhead_tc_kernel<false>, std::forward<Args>(args)...);
+}
+
 }  // namespace
 
 // One partial per (row, vocab tile of 64) on the CUDA-core path and per
@@ -638,30 +725,38 @@ extern "C" eagle_status eagle_lmhead_softmax(eagle_dtype dtype, int T, int H, in
     if (!make_map_bf16(&map_w, d_w, V, H, kUnit)) return EAGLE_ERR_CUDA;
     static bool attr = false;
     if (!attr) {
-      if (cudaFuncSetAttribute(lmhead_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+      if (cudaFuncSetAttribute(lmhead_tc_kernel<false>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                               (int)kSmemLimit) != cudaSuccess ||
+          cudaFuncSetAttribute(lmhead_tc_kernel<true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                (int)kSmemLimit) != cudaSuccess)
         return EAGLE_ERR_CUDA;
       attr = true;
     }
     const int n_units = (V + kUnit - 1) / kUnit;
-    const int grid = std::min(sm_count(), n_units);
-    const int slice_rows = ((n_units + grid - 1) / grid) * kUnit;
-    // one pass over W per 128 tree rows (the MMA's M)
-    for (int r0 = 0; r0 < T; r0 += 128) {
-      const int Ts = std::min(128, T - r0);
-      const TcLayout TL = tc_layout(Ts, slice_rows);
+    // row tiles of 128 per launch: one CTA each, sharing the W stream
+    const int tiles = (T + kTileRows - 1) / kTileRows;
+    int C = std::min(kMaxCluster, tiles);
+    int slices = 0;
+    if (C > 1) {
+      slices = std::min(max_clusters(C, tc_layout(kTileRows).smem), n_units);
+      if (slices < 1) C = 1;   // clusters of C cannot be resident: one tile per launch
+    }
+    if (C == 1) slices = std::min(sm_count(), n_units);
+    for (int r0 = 0; r0 < T; r0 += C * kTileRows) {
+      const int Ts = std::min(C * kTileRows, T - r0);
+      const TcLayout TL = tc_layout((C > 1 || Ts > kTileRows) ? kTileRows : ((Ts + 7) / 8) * 8);
       const __nv_bfloat16* hs = static_cast<const __nv_bfloat16*>(d_h) + (size_t)r0 * H;
       CUtensorMap map_h;
-      if (!make_map_bf16(&map_h, hs, Ts, H, TL.t_pad)) return EAGLE_ERR_CUDA;
-      if (launch_pdl(lmhead_tc_kernel, dim3(grid), dim3(kTcThreads), TL.smem, s, map_h, map_w,
-                     Ts, H, V, temperature, z ? z + (size_t)r0 * V : nullptr,
-                     part + (size_t)r0 * grid, n_units, TL.h_stage_bytes, TL.blk, TL.w_stages,
-                     d_status) != cudaSuccess)
+      if (!make_map_bf16(&map_h, hs, Ts, H, TL.h_rows)) return EAGLE_ERR_CUDA;
+      if (launch_tc(C, dim3(slices * C), TL.smem, s, map_h, map_w, Ts, H, V, temperature,
+                    z ? z + (size_t)r0 * V : nullptr, part + (size_t)r0 * slices, n_units,
+                    TL.h_stage_bytes, TL.h_stages, TL.blk, TL.w_stages, C, d_status) !=
+                        cudaSuccess)
         return EAGLE_ERR_CUDA;
     }
     dim3 fgrid(T, z ? (V + kFinChunk - 1) / kFinChunk : 1);
     return launch_status(launch_pdl(lmhead_finalize_kernel, fgrid, dim3(kFinThreads), 0, s, T, V,
-                                    temperature, (const Partial*)part, grid, d_argmax, d_row_max,
+                                    temperature, (const Partial*)part, slices, d_argmax, d_row_max,
                                     d_row_lse, d_top2_gap, z));
   }
   const int n_vtiles = (V + kVT - 1) / kVT;

@@ -69,7 +69,11 @@ def _check(dtype, got, ref, rows):
     ("f32", 1, 64, 1, 1.0),             # a single vocabulary entry
     ("f32", 70, 128, 1000, 0.7),        # ragged row tile and vocab tile
     ("bf16", 61, 4096, 32000, 1.0),     # Vicuna-7B shaped head
-    ("bf16", 130, 512, 4099, 0.7),      # three row tiles, ragged vocab
+    ("bf16", 130, 512, 4099, 0.7),      # two row tiles sharing W, ragged vocab
+    ("bf16", 256, 1024, 5003, 1.0),     # two full row tiles
+    ("bf16", 300, 512, 2111, 0.7),      # three row tiles sharing one W stream
+    ("bf16", 384, 256, 1500, 1.0),      # three full tiles
+    ("bf16", 513, 256, 3001, 1.0),      # four tiles, then a pass of one row
 ])
 @pytest.mark.parametrize("prob", [False, True])
 def test_lmhead_matches_oracle(dtype, T, H, V, temp, prob):
@@ -80,14 +84,17 @@ def test_lmhead_matches_oracle(dtype, T, H, V, temp, prob):
     _check(dtype, got, ref, np.arange(T))
 
 
-@pytest.mark.parametrize("T,H,temp", [(65, 4096, 1.0), (65, 8192, 1.0), (49, 4096, 0.7)])
+@pytest.mark.parametrize("T,H,temp", [(65, 4096, 1.0), (65, 8192, 1.0), (49, 4096, 0.7),
+                                      (790, 4096, 0.7)])   # 16 packed trees
 def test_lmhead_full_vocab_sampled_rows(T, H, temp):
     # LLaMA-3 vocabulary (128256); the oracle checks a sample of rows
     E = cuda_ready()
     V = 128256
     h, w = _inputs(T * 3 + H, T, H, V, "bf16")
     got = _run(E, h, w, "bf16", temp, True)
-    rows = np.unique(np.r_[0, T - 1, np.random.default_rng(T).integers(0, T, size=6)])
+    edges = [r for r in (127, 128, 255, 256, 511, 512) if r < T]   # row-tile and pass edges
+    rows = np.unique(np.r_[0, T - 1, np.random.default_rng(T).integers(0, T, size=6),
+                           np.asarray(edges, dtype=np.int64)]).astype(np.int64)
     ref = O.lmhead_softmax(h, w, temp, rows=rows)
     _check("bf16", got, ref, rows)
 
