@@ -17,10 +17,11 @@ from typing import Optional
 
 __all__ = [
     "EagleError", "build", "lib", "status_string", "version", "check_status",
-    "EAGLE_F32", "EAGLE_BF16", "LMHEAD_GREEDY", "LMHEAD_PROB", "SAMPLE_REPLACE",
+    "EAGLE_F32", "EAGLE_BF16", "LMHEAD_GREEDY", "LMHEAD_PROB", "LMHEAD_LOGITS", "SAMPLE_REPLACE",
     "SAMPLE_NO_REPLACE", "eagle_tree_attn", "eagle_tree_attn_workspace_bytes",
     "eagle_lmhead_softmax", "eagle_lmhead_workspace_bytes", "eagle_accept_greedy",
-    "eagle_accept_stochastic", "eagle_draft_expand", "eagle_draft_pool_bytes",
+    "eagle_accept_stochastic", "eagle_accept_stochastic_logits", "eagle_draft_expand",
+    "eagle_draft_pool_bytes",
     "eagle_lmhead_softmax_noalloc", "eagle_lmhead_noalloc_max_scratch_bytes",
 ]
 
@@ -28,7 +29,7 @@ HERE = os.path.dirname(os.path.abspath(__file__))
 LIB_PATH = os.path.join(HERE, "libeagle.so")
 
 EAGLE_F32, EAGLE_BF16 = 0, 1
-LMHEAD_GREEDY, LMHEAD_PROB = 0, 1
+LMHEAD_GREEDY, LMHEAD_PROB, LMHEAD_LOGITS = 0, 1, 2
 SAMPLE_REPLACE, SAMPLE_NO_REPLACE = 0, 1
 
 _STATUS = {0: "ok", 1: "invalid argument", 2: "invalid tree", 3: "unsupported shape",
@@ -54,6 +55,8 @@ _SIGS = {
     "eagle_lmhead_softmax": ([_i, _i, _i, _i, _f, _i] + [_p] * 8 + [_sz, _p, _p], _i),
     "eagle_accept_greedy": ([_i, _i, _p, _p, _p, _p, _i, _p, _p, _p, _p, _p], _i),
     "eagle_accept_stochastic": ([_i] * 5 + [_p] * 8 + [_i] + [_p] * 5, _i),
+    "eagle_accept_stochastic_logits": ([_i] * 5 + [_p] * 5 + [_f] + [_p] * 4 + [_i] + [_p] * 5,
+                                       _i),
     "eagle_draft_pool_bytes": ([_i] * 4, _sz),
     "eagle_lmhead_noalloc_max_scratch_bytes": ([], _sz),
     "eagle_lmhead_softmax_noalloc": ([_i, _i, _i, _i, _f, _i] + [_p] * 9, _i),
@@ -180,10 +183,12 @@ def eagle_lmhead_workspace_bytes(T, V) -> int:
 
 
 def eagle_lmhead_softmax(h, w, argmax, row_max, row_lse, top2_gap, q, ws, status, *,
-                         temperature: float = 1.0, stream=None) -> None:
+                         temperature: float = 1.0, logits: bool = False, stream=None) -> None:
     """LM head + softmax statistics + argmax; q=None selects greedy mode
     (no [T,V] output).  h [T,H]; w [V,H]; argmax [T] int32; row_max,
-    row_lse, top2_gap [T] fp32; q [T,V] fp32 or None."""
+    row_lse, top2_gap [T] fp32; q [T,V] fp32 or None.  logits=True stores
+    the logits in q instead of the probabilities (for
+    eagle_accept_stochastic_logits)."""
     torch = _torch()
     T, H = h.shape
     V = w.shape[0]
@@ -191,7 +196,7 @@ def eagle_lmhead_softmax(h, w, argmax, row_max, row_lse, top2_gap, q, ws, status
     _need(argmax, torch.int32, "argmax")
     for name, t in (("row_max", row_max), ("row_lse", row_lse), ("top2_gap", top2_gap), ("q", q)):
         _need(t, torch.float32, name)
-    mode = LMHEAD_GREEDY if q is None else LMHEAD_PROB
+    mode = LMHEAD_GREEDY if q is None else (LMHEAD_LOGITS if logits else LMHEAD_PROB)
     _call("eagle_lmhead_softmax", _dtype_code(h), T, H, V, float(temperature), mode, _ptr(h),
           _ptr(w), _ptr(argmax), _ptr(row_max), _ptr(row_lse), _ptr(top2_gap), _ptr(q),
           _ptr(ws), ws.numel() * ws.element_size(), _ptr(status), _stream(stream))
@@ -202,7 +207,8 @@ def eagle_lmhead_noalloc_max_scratch_bytes() -> int:
 
 
 def eagle_lmhead_softmax_noalloc(h, w, argmax, row_max, row_lse, top2_gap, q, status, *,
-                                 temperature: float = 1.0, stream=None) -> None:
+                                 temperature: float = 1.0, logits: bool = False,
+                                 stream=None) -> None:
     """eagle_lmhead_softmax without a workspace: for callers that cannot
     allocate scratch memory (see include/eagle.h).  Its scratch is a fixed
     16 MiB array inside the library, shared by every call; calls that may
@@ -214,7 +220,7 @@ def eagle_lmhead_softmax_noalloc(h, w, argmax, row_max, row_lse, top2_gap, q, st
     _need(argmax, torch.int32, "argmax")
     for name, t in (("row_max", row_max), ("row_lse", row_lse), ("top2_gap", top2_gap), ("q", q)):
         _need(t, torch.float32, name)
-    mode = LMHEAD_GREEDY if q is None else LMHEAD_PROB
+    mode = LMHEAD_GREEDY if q is None else (LMHEAD_LOGITS if logits else LMHEAD_PROB)
     _call("eagle_lmhead_softmax_noalloc", _dtype_code(h), T, H, V, float(temperature), mode,
           _ptr(h), _ptr(w), _ptr(argmax), _ptr(row_max), _ptr(row_lse), _ptr(top2_gap), _ptr(q),
           _ptr(status), _stream(stream))
@@ -257,6 +263,30 @@ def eagle_accept_stochastic(tree_off, parent, tokens, q, p_rows, p_row_of_node, 
           _ptr(tokens), _ptr(q), _ptr(p_rows), _ptr(p_row_of_node), _ptr(u_accept),
           _ptr(u_sample), max_depth, _ptr(accept_len), _ptr(accepted_nodes), _ptr(out_tokens),
           _ptr(status), _stream(stream))
+
+
+def eagle_accept_stochastic_logits(tree_off, parent, tokens, z, row_lse, p_rows, p_row_of_node,
+                                   u_accept, u_sample, accept_len, accepted_nodes, out_tokens,
+                                   status, *, temperature: float, max_nodes: int,
+                                   max_depth: int, mode: int = SAMPLE_NO_REPLACE,
+                                   stream=None) -> None:
+    """Multi-round stochastic walk on logits: z [T,V] fp32 and row_lse [T]
+    fp32 from eagle_lmhead_softmax(logits=True) at the same temperature."""
+    torch = _torch()
+    B = tree_off.numel() - 1
+    V = z.shape[1]
+    R = p_rows.shape[0]
+    for name, t in (("z", z), ("row_lse", row_lse), ("p_rows", p_rows),
+                    ("u_accept", u_accept), ("u_sample", u_sample)):
+        _need(t, torch.float32, name)
+    if p_rows.shape[1] != V:
+        raise ValueError("p_rows and z must have the same vocabulary")
+    if accepted_nodes.numel() < B * (max_depth + 1) or out_tokens.numel() < B * (max_depth + 1):
+        raise ValueError("output rows must hold max_depth+1 entries per sequence")
+    _call("eagle_accept_stochastic_logits", B, max_nodes, V, R, int(mode), _ptr(tree_off),
+          _ptr(parent), _ptr(tokens), _ptr(z), _ptr(row_lse), float(temperature), _ptr(p_rows),
+          _ptr(p_row_of_node), _ptr(u_accept), _ptr(u_sample), max_depth, _ptr(accept_len),
+          _ptr(accepted_nodes), _ptr(out_tokens), _ptr(status), _stream(stream))
 
 
 def eagle_draft_pool_bytes(B, k, depth, V) -> int:

@@ -16,6 +16,8 @@
 // memory behind one cluster barrier; every CTA then takes the identical
 // decision (the data it decides on is bit-identical), so control flow stays
 // uniform across the cluster without any spin-wait.
+#include <math.h>
+
 #include <cooperative_groups.h>
 
 #include "common.cuh"
@@ -116,7 +118,9 @@ struct StochParams {
   const int* tree_off;
   const int* parent;
   const int* tokens;
-  const float* q;
+  const float* q;          // probabilities, or logits when the walk normalises
+  const float* row_lse;    // logits only: log-sum-exp of every row
+  float temperature;       // logits only
   const float* p_rows;
   const int* p_row_of_node;
   const float* u_accept;
@@ -244,7 +248,9 @@ __device__ __forceinline__ void walk_pass(float (&q)[E], float (&p)[E], int v0, 
 }
 
 // Element e of thread `tid` is vocabulary entry v0 + tid + kStochThreads*e.
-template <int E>
+// LOGITS: P.q holds logits; each visited row is normalised as it is loaded,
+// by the LM head's probability-mode expression.
+template <int E, bool LOGITS>
 __global__ void __launch_bounds__(kStochThreads)
 accept_stochastic_kernel(const StochParams P) {
   pdl_begin();
@@ -336,6 +342,7 @@ accept_stochastic_kernel(const StochParams P) {
     {
       const float* qrow = P.q + (size_t)(t0 + cur) * P.V + v0;
       const float* prw = P.p_rows + (size_t)prow * P.V + v0;
+      const float lse = LOGITS ? __ldg(P.row_lse + t0 + cur) : 0.f;
       int bad = 0;
 #pragma unroll
       for (int e = 0; e < E; ++e) {
@@ -344,6 +351,7 @@ accept_stochastic_kernel(const StochParams P) {
         p[e] = 0.f;
         if (i < nv) {
           q[e] = __ldg(qrow + i);
+          if (LOGITS) q[e] = expf(__fdiv_rn(q[e], P.temperature) - lse);
           bad |= !is_prob(q[e]);
           if (nk > 0) {
             p[e] = __ldg(prw + i);
@@ -540,14 +548,22 @@ extern "C" eagle_status eagle_accept_greedy(int B, int max_nodes, const int32_t*
                                   d_out_tokens, d_status));
 }
 
-extern "C" eagle_status eagle_accept_stochastic(
-    int B, int max_nodes, int V, int R, int mode, const int32_t* d_tree_off,
-    const int32_t* d_parent, const int32_t* d_tokens, const float* d_q, const float* d_p_rows,
-    const int32_t* d_p_row_of_node, const float* d_u_accept, const float* d_u_sample,
-    int max_depth, int32_t* d_accept_len, int32_t* d_accepted_nodes, int32_t* d_out_tokens,
-    int* d_status, eagle_stream_t stream) {
+namespace {
+
+// Both stochastic entry points: d_q holds probabilities, or logits with
+// row_lse and temperature (LOGITS).
+eagle_status launch_stochastic(bool logits, int B, int max_nodes, int V, int R, int mode,
+                               const int32_t* d_tree_off, const int32_t* d_parent,
+                               const int32_t* d_tokens, const float* d_q, const float* d_row_lse,
+                               float temperature, const float* d_p_rows,
+                               const int32_t* d_p_row_of_node, const float* d_u_accept,
+                               const float* d_u_sample, int max_depth, int32_t* d_accept_len,
+                               int32_t* d_accepted_nodes, int32_t* d_out_tokens, int* d_status,
+                               eagle_stream_t stream) {
   EAGLE_HOST_CHECK(B >= 0 && V >= 1 && R >= 0 && max_depth >= 0, EAGLE_ERR_INVALID_ARG);
   EAGLE_HOST_CHECK(mode == EAGLE_SAMPLE_REPLACE || mode == EAGLE_SAMPLE_NO_REPLACE,
+                   EAGLE_ERR_INVALID_ARG);
+  EAGLE_HOST_CHECK(!logits || (temperature > 0.f && isfinite(temperature)),
                    EAGLE_ERR_INVALID_ARG);
   EAGLE_HOST_CHECK(max_nodes >= 1 && max_nodes <= EAGLE_MAX_TREE_NODES, EAGLE_ERR_UNSUPPORTED);
   if (B == 0) return EAGLE_OK;
@@ -555,21 +571,25 @@ extern "C" eagle_status eagle_accept_stochastic(
                        d_p_row_of_node && d_accept_len && d_accepted_nodes && d_out_tokens &&
                        d_status,
                    EAGLE_ERR_INVALID_ARG);
+  EAGLE_HOST_CHECK(!logits || d_row_lse, EAGLE_ERR_INVALID_ARG);
   EAGLE_HOST_CHECK(R == 0 || d_p_rows, EAGLE_ERR_INVALID_ARG);
   int slice = 0, elems = 0;
   const int cs = pick_cluster(V, &slice, &elems);
   EAGLE_HOST_CHECK(cs > 0, EAGLE_ERR_UNSUPPORTED);
   const size_t smem = (size_t)slice * sizeof(float) + (size_t)max_nodes * 3 * sizeof(int);
-  void (*kern)(const StochParams) = elems == 4    ? accept_stochastic_kernel<4>
-                                    : elems == 8  ? accept_stochastic_kernel<8>
-                                    : elems == 16 ? accept_stochastic_kernel<16>
-                                                  : accept_stochastic_kernel<32>;
-  static bool attr_done[4] = {false, false, false, false};
+  using Kern = void (*)(const StochParams);
+  static const Kern kerns[2][4] = {
+      {accept_stochastic_kernel<4, false>, accept_stochastic_kernel<8, false>,
+       accept_stochastic_kernel<16, false>, accept_stochastic_kernel<32, false>},
+      {accept_stochastic_kernel<4, true>, accept_stochastic_kernel<8, true>,
+       accept_stochastic_kernel<16, true>, accept_stochastic_kernel<32, true>}};
   const int ai = elems == 4 ? 0 : elems == 8 ? 1 : elems == 16 ? 2 : 3;
-  if (!attr_done[ai]) {
+  const Kern kern = kerns[logits ? 1 : 0][ai];
+  static bool attr_done[2][4] = {};
+  if (!attr_done[logits ? 1 : 0][ai]) {
     cudaFuncSetAttribute(kern, cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
     cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, 160 * 1024);
-    attr_done[ai] = true;
+    attr_done[logits ? 1 : 0][ai] = true;
   }
   StochParams P;
   P.max_nodes = max_nodes;
@@ -582,6 +602,8 @@ extern "C" eagle_status eagle_accept_stochastic(
   P.parent = d_parent;
   P.tokens = d_tokens;
   P.q = d_q;
+  P.row_lse = d_row_lse;
+  P.temperature = temperature;
   P.p_rows = d_p_rows;
   P.p_row_of_node = d_p_row_of_node;
   P.u_accept = d_u_accept;
@@ -606,4 +628,30 @@ extern "C" eagle_status eagle_accept_stochastic(
   cfg.attrs = attr;
   cfg.numAttrs = 2;
   return launch_status(cudaLaunchKernelEx(&cfg, kern, P));
+}
+
+}  // namespace
+
+extern "C" eagle_status eagle_accept_stochastic(
+    int B, int max_nodes, int V, int R, int mode, const int32_t* d_tree_off,
+    const int32_t* d_parent, const int32_t* d_tokens, const float* d_q, const float* d_p_rows,
+    const int32_t* d_p_row_of_node, const float* d_u_accept, const float* d_u_sample,
+    int max_depth, int32_t* d_accept_len, int32_t* d_accepted_nodes, int32_t* d_out_tokens,
+    int* d_status, eagle_stream_t stream) {
+  return launch_stochastic(false, B, max_nodes, V, R, mode, d_tree_off, d_parent, d_tokens, d_q,
+                           nullptr, 1.f, d_p_rows, d_p_row_of_node, d_u_accept, d_u_sample,
+                           max_depth, d_accept_len, d_accepted_nodes, d_out_tokens, d_status,
+                           stream);
+}
+
+extern "C" eagle_status eagle_accept_stochastic_logits(
+    int B, int max_nodes, int V, int R, int mode, const int32_t* d_tree_off,
+    const int32_t* d_parent, const int32_t* d_tokens, const float* d_z, const float* d_row_lse,
+    float temperature, const float* d_p_rows, const int32_t* d_p_row_of_node,
+    const float* d_u_accept, const float* d_u_sample, int max_depth, int32_t* d_accept_len,
+    int32_t* d_accepted_nodes, int32_t* d_out_tokens, int* d_status, eagle_stream_t stream) {
+  return launch_stochastic(true, B, max_nodes, V, R, mode, d_tree_off, d_parent, d_tokens, d_z,
+                           d_row_lse, temperature, d_p_rows, d_p_row_of_node, d_u_accept,
+                           d_u_sample, max_depth, d_accept_len, d_accepted_nodes, d_out_tokens,
+                           d_status, stream);
 }

@@ -706,7 +706,8 @@ extern "C" eagle_status eagle_lmhead_softmax(eagle_dtype dtype, int T, int H, in
                                              eagle_stream_t stream) {
   EAGLE_HOST_CHECK(T >= 0 && H >= 1 && V >= 1, EAGLE_ERR_INVALID_ARG);
   EAGLE_HOST_CHECK(temperature > 0.f && isfinite(temperature), EAGLE_ERR_INVALID_ARG);
-  EAGLE_HOST_CHECK(mode == EAGLE_LMHEAD_GREEDY || mode == EAGLE_LMHEAD_PROB,
+  EAGLE_HOST_CHECK(mode == EAGLE_LMHEAD_GREEDY || mode == EAGLE_LMHEAD_PROB ||
+                       mode == EAGLE_LMHEAD_LOGITS,
                    EAGLE_ERR_INVALID_ARG);
   EAGLE_HOST_CHECK(dtype == EAGLE_F32 || dtype == EAGLE_BF16, EAGLE_ERR_UNSUPPORTED);
   if (T == 0) return EAGLE_OK;
@@ -716,7 +717,9 @@ extern "C" eagle_status eagle_lmhead_softmax(eagle_dtype dtype, int T, int H, in
   EAGLE_HOST_CHECK(ws_bytes >= eagle_lmhead_workspace_bytes(T, V) && d_ws, EAGLE_ERR_WORKSPACE);
   cudaStream_t s = (cudaStream_t)stream;
   Partial* part = static_cast<Partial*>(d_ws);
-  float* z = (mode == EAGLE_LMHEAD_PROB) ? d_q : nullptr;
+  float* z = (mode == EAGLE_LMHEAD_GREEDY) ? nullptr : d_q;
+  // PROB mode normalises the logits in place afterwards; LOGITS keeps them
+  float* q_norm = (mode == EAGLE_LMHEAD_PROB) ? d_q : nullptr;
   const bool tc_ok = dtype == EAGLE_BF16 && (H % 8) == 0 &&
                      (((uintptr_t)d_h | (uintptr_t)d_w) & 15) == 0 &&
                      (!z || ((uintptr_t)z & 15) == 0);
@@ -754,10 +757,10 @@ extern "C" eagle_status eagle_lmhead_softmax(eagle_dtype dtype, int T, int H, in
                         cudaSuccess)
         return EAGLE_ERR_CUDA;
     }
-    dim3 fgrid(T, z ? (V + kFinChunk - 1) / kFinChunk : 1);
+    dim3 fgrid(T, q_norm ? (V + kFinChunk - 1) / kFinChunk : 1);
     return launch_status(launch_pdl(lmhead_finalize_kernel, fgrid, dim3(kFinThreads), 0, s, T, V,
                                     temperature, (const Partial*)part, slices, d_argmax, d_row_max,
-                                    d_row_lse, d_top2_gap, z));
+                                    d_row_lse, d_top2_gap, q_norm));
   }
   const int n_vtiles = (V + kVT - 1) / kVT;
   dim3 grid(n_vtiles, (T + kRT - 1) / kRT);
@@ -771,10 +774,10 @@ extern "C" eagle_status eagle_lmhead_softmax(eagle_dtype dtype, int T, int H, in
                    temperature, static_cast<const float*>(d_h), static_cast<const float*>(d_w), z,
                    part, n_vtiles, d_status);
   if (e != cudaSuccess) return EAGLE_ERR_CUDA;
-  dim3 fgrid(T, z ? (V + kFinChunk - 1) / kFinChunk : 1);
+  dim3 fgrid(T, q_norm ? (V + kFinChunk - 1) / kFinChunk : 1);
   return launch_status(launch_pdl(lmhead_finalize_kernel, fgrid, dim3(kFinThreads), 0, s, T, V,
                                   temperature, (const Partial*)part, n_vtiles, d_argmax,
-                                  d_row_max, d_row_lse, d_top2_gap, z));
+                                  d_row_max, d_row_lse, d_top2_gap, q_norm));
 }
 
 // ---------------------------------------------------------------------------

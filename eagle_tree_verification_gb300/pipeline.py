@@ -4,8 +4,9 @@
                  -- or a caller-given tree (parent/tokens/p_row_of_node)
     attention    eagle_tree_attn
     LM head      eagle_lmhead_softmax (greedy: no [T,V] output; stochastic:
-                 writes q)
-    acceptance   eagle_accept_greedy | eagle_accept_stochastic
+                 writes the logits)
+    acceptance   eagle_accept_greedy | eagle_accept_stochastic_logits (which
+                 normalises only the rows the walk visits)
 
 Every launch goes through the C ABI on one stream with no host
 synchronisation, so `run()` can be captured into a CUDA graph (`capture()`).
@@ -19,7 +20,7 @@ import dataclasses
 from typing import Dict, Optional, Sequence
 
 from . import (SAMPLE_NO_REPLACE, eagle_accept_greedy, eagle_accept_stochastic,
-               eagle_draft_expand, eagle_draft_pool_bytes, eagle_lmhead_softmax,
+               eagle_accept_stochastic_logits, eagle_draft_expand, eagle_draft_pool_bytes, eagle_lmhead_softmax,
                eagle_lmhead_workspace_bytes, eagle_tree_attn, eagle_tree_attn_workspace_bytes)
 
 
@@ -127,7 +128,8 @@ class TreeVerifyStep:
         self.row_max = z(T)
         self.row_lse = z(T)
         self.top2_gap = z(T)
-        self.q_prob = z(T, s.V) if s.mode == "stochastic" else None
+        # stochastic: the target logits; the walk normalises the rows it visits
+        self.logits = z(T, s.V) if s.mode == "stochastic" else None
         W = s.max_depth + 1
         self.accept_len = z(s.B, dtype=i32)
         self.accepted_nodes = z(s.B, W, dtype=i32)
@@ -183,8 +185,8 @@ class TreeVerifyStep:
 
     def run_lmhead(self, stream=None) -> None:
         eagle_lmhead_softmax(self.h, self.w_lm, self.argmax, self.row_max, self.row_lse,
-                             self.top2_gap, self.q_prob, self.lm_ws, self.status,
-                             temperature=self.s.temperature, stream=stream)
+                             self.top2_gap, self.logits, self.lm_ws, self.status,
+                             temperature=self.s.temperature, logits=True, stream=stream)
 
     def run_accept(self, stream=None) -> None:
         s = self.s
@@ -194,11 +196,23 @@ class TreeVerifyStep:
                                 self.status, max_nodes=self.max_nodes, max_depth=s.max_depth,
                                 stream=stream)
         else:
-            eagle_accept_stochastic(self.tree_off, self.parent, self.tokens, self.q_prob,
-                                    self.p_rows, self.p_row_of_node, self.u_accept,
-                                    self.u_sample, self.accept_len, self.accepted_nodes,
-                                    self.out_tokens, self.status, max_nodes=self.max_nodes,
-                                    max_depth=s.max_depth, mode=s.sample_mode, stream=stream)
+            eagle_accept_stochastic_logits(self.tree_off, self.parent, self.tokens, self.logits,
+                                           self.row_lse, self.p_rows, self.p_row_of_node,
+                                           self.u_accept, self.u_sample, self.accept_len,
+                                           self.accepted_nodes, self.out_tokens, self.status,
+                                           temperature=s.temperature, max_nodes=self.max_nodes,
+                                           max_depth=s.max_depth, mode=s.sample_mode,
+                                           stream=stream)
+
+    def run_accept_q(self, q, stream=None) -> None:
+        """The stochastic walk fed with given probabilities q [T,V] fp32 (a
+        device tensor) instead of this step's logits."""
+        s = self.s
+        eagle_accept_stochastic(self.tree_off, self.parent, self.tokens, q, self.p_rows,
+                                self.p_row_of_node, self.u_accept, self.u_sample,
+                                self.accept_len, self.accepted_nodes, self.out_tokens,
+                                self.status, max_nodes=self.max_nodes, max_depth=s.max_depth,
+                                mode=s.sample_mode, stream=stream)
 
     def run(self, stream=None, build_tree: bool = True) -> None:
         """The whole step: tree build (if EAGLE-2), attention, LM head, accept.
@@ -215,8 +229,9 @@ class TreeVerifyStep:
         if self.s.k:
             n += self.s.depth                    # one per level, finalize fused
         n += 1                                   # attention
-        if self.s.dtype == "bf16":               # LM head: one pass per 128 rows
-            n += (self.s.T + 127) // 128 + 1     # ... + finalize
+        if self.s.dtype == "bf16":               # LM head: one pass per cluster of
+            tiles = (self.s.T + 127) // 128      # up to four 128-row tiles
+            n += (tiles + min(4, tiles) - 1) // min(4, tiles) + 1   # ... + finalize
         else:
             n += 2                               # LM head tiles + finalize
         n += 1                                   # acceptance

@@ -5,7 +5,7 @@
  *   eagle_draft_expand   (every level, then finalize) -> draft tree
  *   eagle_tree_attn      tree-masked attention of every tree node
  *   eagle_lmhead_softmax LM-head logits, softmax statistics, argmax (and q)
- *   eagle_accept_greedy  | eagle_accept_stochastic -> accepted tokens
+ *   eagle_accept_greedy  | eagle_accept_stochastic(_logits) -> accepted tokens
  *
  * Sources, by page title and section:
  *   [S4000]   大模型推理效率突破：EAGLE推测解码算法在摩尔线程GPU的实践与优化
@@ -67,7 +67,11 @@ typedef enum {
 } eagle_status;
 
 typedef enum { EAGLE_F32 = 0, EAGLE_BF16 = 1 } eagle_dtype;
-typedef enum { EAGLE_LMHEAD_GREEDY = 0, EAGLE_LMHEAD_PROB = 1 } eagle_lmhead_mode;
+typedef enum {
+  EAGLE_LMHEAD_GREEDY = 0,
+  EAGLE_LMHEAD_PROB = 1,
+  EAGLE_LMHEAD_LOGITS = 2
+} eagle_lmhead_mode;
 typedef enum { EAGLE_SAMPLE_REPLACE = 0, EAGLE_SAMPLE_NO_REPLACE = 1 } eagle_sample_mode;
 
 /* Limits of this implementation. */
@@ -128,12 +132,18 @@ EAGLE_API eagle_status eagle_tree_attn(eagle_dtype dtype, int B, int T, int Hq, 
  * T, H, V     rows (tree nodes), hidden size, vocabulary.
  * temperature > 0.
  * mode        EAGLE_LMHEAD_GREEDY: no [T,V] tensor is written.
- *             EAGLE_LMHEAD_PROB:   d_q [T,V] fp32 receives softmax(z/temp).
+ *             EAGLE_LMHEAD_PROB:   d_q [T,V] fp32 receives softmax(z/temp),
+ *                                  each entry expf(rn(z/temp) - row_lse) in
+ *                                  fp32 (rn: division rounded to nearest).
+ *             EAGLE_LMHEAD_LOGITS: d_q [T,V] fp32 receives the logits z
+ *                                  themselves; with d_row_lse they are what
+ *                                  eagle_accept_stochastic_logits reads.
  * d_h         [T,H];  d_w [V,H] (vocabulary-major, as stored by LM heads).
  * d_argmax    [T] int32: argmax_v z[t,v], lowest index on ties.
  * d_row_max   [T] fp32: max_v z.         d_row_lse [T] fp32: log sum exp(z/temp).
  * d_top2_gap  [T] fp32: largest minus second-largest logit (0 on a tie).
- * d_q         [T,V] fp32 or NULL in GREEDY mode.
+ * d_q         [T,V] fp32 (16-byte aligned for the tensor-core path), or NULL
+ *             in GREEDY mode.
  * d_ws        scratch of eagle_lmhead_workspace_bytes(T, V) bytes.
  * Device errors: NUMERIC (non-finite logit).
  * ---------------------------------------------------------------------- */
@@ -242,6 +252,32 @@ EAGLE_API eagle_status eagle_accept_stochastic(int B, int max_nodes, int V, int 
                                      int max_depth, int32_t *d_accept_len,
                                      int32_t *d_accepted_nodes, int32_t *d_out_tokens,
                                      int *d_status, eagle_stream_t stream);
+
+/* ------------------------------------------------------------------------
+ * eagle_accept_stochastic_logits -- eagle_accept_stochastic reading target
+ * logits instead of probabilities.
+ *
+ * The walk reads q only for the nodes it visits (alpha + 1 of them per
+ * sequence), so normalising every node's row beforehand is wasted work.
+ * Here each visited row is normalised as it is loaded:
+ *   q[t,v] = expf(rn(z[t,v] / temperature) - row_lse[t])   (fp32)
+ * -- the same expression, evaluated by the same library, as
+ * eagle_lmhead_softmax's PROB mode, so given that call's d_row_lse the
+ * probabilities, and with them every decision and token, are identical to
+ * eagle_accept_stochastic fed with PROB mode's d_q.  Everything else is as
+ * eagle_accept_stochastic.
+ *
+ * d_z [T,V] fp32 logits (EAGLE_LMHEAD_LOGITS output); d_row_lse [T] fp32;
+ * temperature > 0, the value given to eagle_lmhead_softmax.
+ * Device errors: as eagle_accept_stochastic (NUMERIC also for a non-finite
+ * logit in a row the walk reads).
+ * ---------------------------------------------------------------------- */
+EAGLE_API eagle_status eagle_accept_stochastic_logits(
+    int B, int max_nodes, int V, int R, int mode, const int32_t *d_tree_off,
+    const int32_t *d_parent, const int32_t *d_tokens, const float *d_z, const float *d_row_lse,
+    float temperature, const float *d_p_rows, const int32_t *d_p_row_of_node,
+    const float *d_u_accept, const float *d_u_sample, int max_depth, int32_t *d_accept_len,
+    int32_t *d_accepted_nodes, int32_t *d_out_tokens, int *d_status, eagle_stream_t stream);
 
 /* ------------------------------------------------------------------------
  * eagle_draft_expand -- EAGLE-2 dynamic draft tree: expand one level, or

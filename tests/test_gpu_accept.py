@@ -162,3 +162,74 @@ def test_stochastic_many_rejections_then_sample_at_full_vocab():
         assert got[3] == 0
         for r, x in zip(ref, got[:3]):
             np.testing.assert_array_equal(x, r)
+
+
+def _lmhead(E, h, w, temperature, logits):
+    import torch
+    T, V = h.shape[0], w.shape[0]
+    am = torch.empty(T, dtype=torch.int32, device="cuda")
+    rm, lse, gap = (torch.empty(T, dtype=torch.float32, device="cuda") for _ in range(3))
+    out = torch.full((T, V), -7.0, dtype=torch.float32, device="cuda")
+    ws = torch.empty(E.eagle_lmhead_workspace_bytes(T, V), dtype=torch.uint8, device="cuda")
+    st = torch.zeros(1, dtype=torch.int32, device="cuda")
+    E.eagle_lmhead_softmax(h, w, am, rm, lse, gap, out, ws, st, temperature=temperature,
+                           logits=logits)
+    torch.cuda.synchronize()
+    assert int(st.item()) == 0
+    return out, lse
+
+
+@pytest.mark.parametrize("dtype,V,H,temp", [("f32", 1024, 256, 0.7), ("bf16", 32000, 256, 1.0),
+                                            ("bf16", 4099, 512, 0.7), ("bf16", 128256, 128, 1.0)])
+def test_walk_on_logits_equals_walk_on_probabilities(dtype, V, H, temp):
+    # The logits walk normalises each visited row itself; fed the LM head's
+    # logits and row log-sum-exp it must take exactly the decisions of the
+    # walk fed the LM head's probability-mode q, and both the oracle's.
+    import torch
+    E = cuda_ready()
+    B = 3
+    tree_off, parent, tokens = _forest(V + H, B, V, [(1, 4, 6, 6, 3), (1, 8, 8, 8)],
+                                       distinct=True)
+    T = len(parent)
+    tdt = torch.bfloat16 if dtype == "bf16" else torch.float32
+    h = torch.from_numpy(synth.normal(V, "h", (T, H))).to(tdt).cuda()
+    w = torch.from_numpy(synth.normal(V, "w", (V, H), std=0.5 / np.sqrt(H) * 8)).to(tdt).cuda()
+    q, _ = _lmhead(E, h, w, temp, logits=False)
+    z, lse = _lmhead(E, h, w, temp, logits=True)
+    qn = to_np(q)
+    g = np.random.default_rng(V)
+    # draft rows: node i's children drafted from row i; some rows equal the
+    # target's (accepts), the rest random (rejections, residual rounds)
+    p_rows = synth.random_probs(V, "p", T, V, sigma=2.0)
+    for t in range(T):
+        if g.random() < 0.6:
+            p_rows[t] = qn[t]
+    prow = np.full(T, -1, np.int32)
+    for b in range(B):
+        t0, t1 = tree_off[b], tree_off[b + 1]
+        for i in range(1, t1 - t0):
+            prow[t0 + i] = t0 + parent[t0 + i]
+    ua = synth.uniforms24(V, "ua", T)
+    us = synth.uniforms24(V, "us", T)
+    depth = max(max(O.tree_depths(parent[tree_off[b]:tree_off[b + 1]])) for b in range(B))
+    for mode in (O.MODE_NO_REPLACE, O.MODE_REPLACE):
+        ref = O.accept_stochastic(tree_off, parent, tokens, qn, p_rows, prow, ua, us,
+                                  max_depth=depth, mode=mode)
+        got_q = _run_stoch(E, tree_off, parent, tokens, qn, p_rows, prow, ua, us, depth, mode)
+        Wd = depth + 1
+        acc = torch.full((B,), -7, dtype=torch.int32, device="cuda")
+        nodes = torch.full((B, Wd), -7, dtype=torch.int32, device="cuda")
+        out = torch.full((B, Wd), -7, dtype=torch.int32, device="cuda")
+        st = torch.zeros(1, dtype=torch.int32, device="cuda")
+        E.eagle_accept_stochastic_logits(_dev(tree_off), _dev(parent), _dev(tokens), z, lse,
+                                         _dev(p_rows), _dev(prow), _dev(ua), _dev(us), acc,
+                                         nodes, out, st, temperature=temp,
+                                         max_nodes=int(np.max(np.diff(tree_off))),
+                                         max_depth=depth, mode=mode)
+        torch.cuda.synchronize()
+        assert got_q[3] == 0 and int(st.item()) == 0
+        got_z = (to_np(acc), to_np(nodes), to_np(out))
+        for r, a, b_ in zip(ref, got_q[:3], got_z):
+            np.testing.assert_array_equal(a, r)
+            np.testing.assert_array_equal(b_, r)
+        assert ref[0].max() >= 1

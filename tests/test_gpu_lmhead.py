@@ -110,3 +110,30 @@ def test_lmhead_planted_ties_pick_the_lowest_index():
     got = _run(E, h, w, "f32", 1.0, True)
     assert list(got[0]) == [7] * T
     assert np.all(got[3] == 0.0)
+
+
+@pytest.mark.parametrize("dtype,T,H,V,temp", [("f32", 26, 256, 1024, 0.7),
+                                               ("bf16", 61, 4096, 32000, 1.0),
+                                               ("bf16", 300, 512, 2111, 0.7)])
+def test_lmhead_logits_mode(dtype, T, H, V, temp):
+    # LOGITS mode stores z itself and the same statistics as the other modes
+    import torch
+    E = cuda_ready()
+    h, w = _inputs(T + V, T, H, V, dtype)
+    tdt = torch.bfloat16 if dtype == "bf16" else torch.float32
+    d_h = torch.from_numpy(h).to(tdt).cuda()
+    d_w = torch.from_numpy(w).to(tdt).cuda()
+    f = lambda: torch.full((T,), -7.0, dtype=torch.float32, device="cuda")
+    am = torch.full((T,), -7, dtype=torch.int32, device="cuda")
+    rm, lse, gap = f(), f(), f()
+    z = torch.full((T, V), -7.0, dtype=torch.float32, device="cuda")
+    ws = torch.empty(E.eagle_lmhead_workspace_bytes(T, V), dtype=torch.uint8, device="cuda")
+    st = torch.zeros(1, dtype=torch.int32, device="cuda")
+    E.eagle_lmhead_softmax(d_h, d_w, am, rm, lse, gap, z, ws, st, temperature=temp, logits=True)
+    torch.cuda.synchronize()
+    ref = O.lmhead_softmax(h, w, temp)
+    _check(dtype, (to_np(am), to_np(rm), to_np(lse), to_np(gap), None, int(st.item())), ref,
+           np.arange(T))
+    zr = ref["z"]
+    atol = (1e-4 if dtype == "bf16" else 1e-5) * max(1.0, float(np.abs(zr).max()))
+    np.testing.assert_allclose(to_np(z), zr, rtol=0, atol=atol)
