@@ -59,9 +59,12 @@ ChunkPlan chunk_plan(int rows, int V) {
 
 size_t align256(size_t x) { return (x + 255) & ~(size_t)255; }
 
+// Tickets and chunk lists come twice, for even and odd levels: a level
+// ranks its chunks while the previous one still merges.
 struct PoolLayout {
   int P;             // candidate capacity per sequence
   ChunkPlan c0, c1;  // level 0 / later levels
+  size_t parts;      // chunk-list keys of one level
   size_t off_count, off_ticket, off_frontier, off_fscore, off_token, off_parent, off_depth,
       off_prow, off_score, off_partial, total;
 };
@@ -71,7 +74,7 @@ PoolLayout pool_layout(int B, int k, int depth, int V) {
   L.P = k + (depth - 1) * k * k;
   L.c0 = chunk_plan(B, V);
   L.c1 = chunk_plan(B * k, V);
-  const size_t parts = std::max((size_t)B * L.c0.S, (size_t)B * k * L.c1.S) * k;
+  L.parts = std::max((size_t)B * L.c0.S, (size_t)B * k * L.c1.S) * k;
   size_t o = 0;
   auto take = [&](size_t bytes) {
     size_t at = o;
@@ -79,7 +82,7 @@ PoolLayout pool_layout(int B, int k, int depth, int V) {
     return at;
   };
   L.off_count = take((size_t)B * 4);
-  L.off_ticket = take((size_t)B * 4);
+  L.off_ticket = take((size_t)2 * B * 4);
   L.off_frontier = take((size_t)B * k * 4);
   L.off_fscore = take((size_t)B * k * 4);
   L.off_token = take((size_t)B * L.P * 4);
@@ -87,14 +90,14 @@ PoolLayout pool_layout(int B, int k, int depth, int V) {
   L.off_depth = take((size_t)B * L.P * 4);
   L.off_prow = take((size_t)B * L.P * 4);
   L.off_score = take((size_t)B * L.P * 4);
-  L.off_partial = take(parts * 8);
+  L.off_partial = take(2 * L.parts * 8);
   L.total = o;
   return L;
 }
 
 struct PoolPtrs {
   int* count;     // [B] pool fill
-  int* ticket;    // [B] CTAs of the running level that have finished
+  int* ticket;    // [2, B] CTAs of a level that have finished, by level parity
   int* frontier;  // [B, k] pool index of the frontier, by rank
   float* fscore;  // [B, k] its score
   int* token;
@@ -102,7 +105,7 @@ struct PoolPtrs {
   int* depth;
   int* prow;
   float* score;
-  unsigned long long* partial;  // chunk top-k lists
+  unsigned long long* partial;  // chunk top-k lists, [2, parts] by level parity
 };
 
 PoolPtrs pool_ptrs(void* base, const PoolLayout& L) {
@@ -468,7 +471,10 @@ __device__ void merge_sequence(const LevelParams& A, int b, MergeShared& M) {
 // The sequence's last CTA: per-row top-k, children, next frontier.
 template <int VEC>
 __global__ void __launch_bounds__(kLvThreads, 2) expand_level_kernel(const LevelParams A) {
-  pdl_begin();
+  // A level's draft rows and its chunk lists do not depend on the level
+  // before it (whose lists are the other parity's), so past level 0 only
+  // the merging CTA waits for it.  Level 0 follows the pool reset.
+  if (A.level == 0) pdl_begin();
   __shared__ ChunkShared C;
   __shared__ MergeShared M;
   const int tid = threadIdx.x;
@@ -495,6 +501,7 @@ __global__ void __launch_bounds__(kLvThreads, 2) expand_level_kernel(const Level
     }
   }
   if (!chunk_topk<VEC>(A, row, chunk, v, C)) return;
+  if (A.level > 0) pdl_begin();   // the frontier and pool fill of the level before
   merge_sequence(A, b, M);
   if (A.fused) {
     // the last level: this CTA holds the sequence's complete pool
@@ -527,7 +534,10 @@ __device__ __forceinline__ void bulk_load(void* dst, const void* src, uint32_t b
 
 __global__ void __launch_bounds__(kLvThreads, 2)
 expand_level_stream_kernel(const LevelParams A, int total_chunks) {
-  pdl_begin();
+  // as expand_level_kernel: past level 0 a CTA waits for the level before
+  // only when it is about to merge
+  bool waited = (A.level == 0);
+  if (waited) pdl_begin();
   __shared__ ChunkShared C;
   __shared__ MergeShared M;
   __shared__ uint64_t full[kStreamStages];
@@ -567,7 +577,13 @@ expand_level_stream_kernel(const LevelParams A, int total_chunks) {
       s_last = (t + n == per_seq);
     }
     __syncthreads();
-    if (s_last) merge_sequence(A, b, M);
+    if (s_last) {
+      if (!waited) {
+        pdl_begin();
+        waited = true;
+      }
+      merge_sequence(A, b, M);
+    }
     __syncthreads();
   };
   int i = 0, cur_b = -1, cur_n = 0;
@@ -843,6 +859,8 @@ extern "C" eagle_status eagle_draft_expand(int B, int V, int k, int depth, int l
   A.vec_ok = (V % 4 == 0) && ((uintptr_t)d_draft_logp % 16 == 0);
   A.logp = d_draft_logp;
   A.pool = pp;
+  A.pool.ticket = pp.ticket + (size_t)(level & 1) * B;
+  A.pool.partial = pp.partial + (size_t)(level & 1) * L.parts;
   A.status = d_status;
   void (*kern)(const LevelParams) = (cp.vec == 1)   ? expand_level_kernel<1>
                                     : (cp.vec == 2) ? expand_level_kernel<2>
