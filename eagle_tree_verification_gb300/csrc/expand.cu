@@ -167,11 +167,27 @@ __device__ __forceinline__ unsigned long long pick_lane(unsigned bal, unsigned l
   return (bal && got) ? got : fallback;
 }
 
+// Number of lanes whose key is larger than this lane's (keys distinct or
+// 0): 32 register shuffles, no shared memory.
+__device__ __forceinline__ int warp_rank_desc(unsigned long long key) {
+  int r = 0;
+#pragma unroll
+  for (int j = 0; j < 32; ++j) r += (__shfl_sync(0xffffffffu, key, j) > key);
+  return r;
+}
+
+// Largest key of the warp (every lane gets it): the high and low words by
+// two warp reductions.
+__device__ __forceinline__ unsigned long long warp_max_key(unsigned long long key) {
+  const uint32_t hi = (uint32_t)(key >> 32);
+  const uint32_t mh = __reduce_max_sync(0xffffffffu, hi);
+  const uint32_t ml = __reduce_max_sync(0xffffffffu, hi == mh ? (uint32_t)key : 0u);
+  return ((unsigned long long)mh << 32) | ml;
+}
+
 struct MergeShared {
-  unsigned long long lane_max[kLvWarps][32];
   unsigned long long cand[kLvWarps][kRowCap];
   unsigned long long row[EAGLE_MAX_TOPK][EAGLE_MAX_TOPK];
-  unsigned long long child[EAGLE_MAX_TOPK * EAGLE_MAX_TOPK];
   int fidx[EAGLE_MAX_TOPK];
   float fsc[EAGLE_MAX_TOPK];
   int base;
@@ -180,8 +196,7 @@ struct MergeShared {
 // Exact top-k (descending) of n keys at `src` (written by other CTAs: read
 // through L2) by one warp; out[0..k) in order, 0 where fewer than k keys.
 __device__ void warp_row_topk(const unsigned long long* src, int n, int k,
-                              unsigned long long* lane_max, unsigned long long* cand,
-                              unsigned long long* out, int* status) {
+                              unsigned long long* cand, unsigned long long* out, int* status) {
   const int lane = threadIdx.x & 31;
   // keys in tiles of 32 x kMergeRegs, loads of a tile in flight together;
   // a single tile stays in registers for the second pass
@@ -201,12 +216,8 @@ __device__ void warp_row_topk(const unsigned long long* src, int n, int k,
     for (int r = 0; r < kMergeRegs; ++r) lmax = umax64(lmax, reg[r]);
   }
   // lower bound of the k-th largest: the k-th largest lane maximum
-  lane_max[lane] = lmax;
-  __syncwarp();
-  int rank = 0;
-#pragma unroll 8
-  for (int j = 0; j < 32; ++j) rank += (lane_max[j] > lmax);
-  unsigned long long tau = pick_lane(__ballot_sync(0xffffffffu, rank == k - 1), lmax, 1ull);
+  const int lrank = warp_rank_desc(lmax);
+  unsigned long long tau = pick_lane(__ballot_sync(0xffffffffu, lrank == k - 1), lmax, 1ull);
   int cnt;
   for (int round = 0;; ++round) {
     cnt = 0;
@@ -250,12 +261,19 @@ __device__ void warp_row_topk(const unsigned long long* src, int n, int k,
       nt = umax64(nt, pick_lane(__ballot_sync(0xffffffffu, rk[t] == k - 1), m[t], 0ull));
     tau = nt;
   }
-  for (int t = lane; t < cnt; t += 32) {
-    const unsigned long long me = cand[t];
-    int r = 0;
+  if (cnt <= 32) {
+    // one candidate per lane: exact ranks by shuffles
+    const unsigned long long me = (lane < cnt) ? cand[lane] : 0ull;
+    const int r = warp_rank_desc(me);
+    if (lane < cnt && r < k) out[r] = me;
+  } else {
+    for (int t = lane; t < cnt; t += 32) {
+      const unsigned long long me = cand[t];
+      int r = 0;
 #pragma unroll 8
-    for (int j = 0; j < cnt; ++j) r += (cand[j] > me);
-    if (r < k) out[r] = me;
+      for (int j = 0; j < cnt; ++j) r += (cand[j] > me);
+      if (r < k) out[r] = me;
+    }
   }
   for (int t = cnt + lane; t < k; t += 32) out[t] = 0ull;
   __syncwarp();
@@ -315,7 +333,8 @@ __device__ bool chunk_topk(const LevelParams& A, int row, int chunk, const float
   if (tid == 0) C.cnt = 0;
   if (__syncthreads_or(!(fin == 0.f)) && tid == 0) fail(A.status, EAGLE_ERR_NUMERIC);
   // every warp: the largest group maximum that at least k group maxima
-  // reach -- at least k tokens of the chunk are >= it (ties included)
+  // reach -- at least k tokens of the chunk are >= it (ties included).
+  // (Measured: warp 0 alone plus a CTA barrier cost ~9x this.)
   float tau_val;
   {
     const float g = C.grpv[lane];
@@ -366,31 +385,43 @@ __device__ bool chunk_topk(const LevelParams& A, int row, int chunk, const float
     __syncthreads();
     tau_key = C.tau;
   }
-  if (tid < cnt) {
-    const unsigned long long me = C.cand[tid];
-    int rank = 0;
+  // ---- exact ranks, and the chunk list published; the sequence's last CTA
+  // merges.  The list's writers meet at a warp barrier, then one thread takes
+  // the ticket with an acquire-release atomic: the stores are visible to the
+  // CTA that draws the last ticket, and that CTA's reads follow the atomic
+  // (then a CTA barrier).
+  unsigned long long* part = A.pool.partial + ((size_t)row * A.S + chunk) * k;
+  if (cnt <= 32) {
+    // one candidate per lane of warp 0: ranks by shuffles, written at once
+    if (warp == 0) {
+      const unsigned long long me = (lane < cnt) ? C.cand[lane] : 0ull;
+      const int rank = warp_rank_desc(me);
+      if (lane < cnt && rank < k) part[rank] = me;
+      if (lane >= cnt && lane < k) part[lane] = 0ull;   // fewer than k tokens
+    }
+  } else {
+    if (tid < cnt) {
+      const unsigned long long me = C.cand[tid];
+      int rank = 0;
 #pragma unroll 8
-    for (int i = 0; i < cnt; ++i) rank += (C.cand[i] > me);
-    if (rank < k) C.top[rank] = me;
-  } else if (tid < k) {
-    C.top[tid] = 0ull;  // fewer than k tokens in this chunk
+      for (int i = 0; i < cnt; ++i) rank += (C.cand[i] > me);
+      if (rank < k) C.top[rank] = me;
+    }
+    __syncthreads();
+    if (warp == 0 && lane < k) part[lane] = C.top[lane];
   }
-  __syncthreads();
-  // ---- publish the chunk list; the sequence's last CTA merges.  One thread
-  // writes the list and takes the ticket with an acquire-release atomic: its
-  // stores are visible to the CTA that draws the last ticket, and that CTA's
-  // reads follow the atomic (then a CTA barrier).
-  if (tid == 0) {
-    unsigned long long* part = A.pool.partial + ((size_t)row * A.S + chunk) * k;
-    for (int r = 0; r < k; ++r) part[r] = C.top[r];
-    C.last = 0;
-    if (take_ticket) {
-      int t;
-      asm volatile("atom.acq_rel.gpu.global.add.s32 %0, [%1], 1;"
-                   : "=r"(t)
-                   : "l"(A.pool.ticket + b)
-                   : "memory");
-      C.last = (t == A.F * A.S - 1);
+  if (warp == 0) {
+    __syncwarp();
+    if (lane == 0) {
+      C.last = 0;
+      if (take_ticket) {
+        int t;
+        asm volatile("atom.acq_rel.gpu.global.add.s32 %0, [%1], 1;"
+                     : "=r"(t)
+                     : "l"(A.pool.ticket + b)
+                     : "memory");
+        C.last = (t == A.F * A.S - 1);
+      }
     }
   }
   __syncthreads();
@@ -420,8 +451,8 @@ __device__ void merge_sequence(const LevelParams& A, int b, MergeShared& M) {
   }
   const int n = A.S * k;
   for (int ff = warp; ff < F; ff += kLvWarps)
-    warp_row_topk(A.pool.partial + (size_t)(b * F + ff) * n, n, k, M.lane_max[warp],
-                  M.cand[warp], M.row[ff], A.status);
+    warp_row_topk(A.pool.partial + (size_t)(b * F + ff) * n, n, k, M.cand[warp], M.row[ff],
+                  A.status);
   __syncthreads();
   const int nc = F * k;  // children in creation order (f-major, rank-minor)
   const int base = M.base;
@@ -434,34 +465,35 @@ __device__ void merge_sequence(const LevelParams& A, int b, MergeShared& M) {
   int* dep = A.pool.depth + (size_t)b * A.P;
   int* prw = A.pool.prow + (size_t)b * A.P;
   float* sco = A.pool.score + (size_t)b * A.P;
-  for (int c = tid; c < nc; c += kLvThreads) {
-    const int ff = c / k, rr = c % k;
-    const unsigned long long key = M.row[ff][rr];
-    const float sc = __fadd_rn(M.fsc[ff], key_value(key));
-    const int at = base + c;
-    tok[at] = (int)key_index(key);
-    par[at] = M.fidx[ff];
-    dep[at] = A.level + 1;
-    prw[at] = (A.level == 0) ? 0 : 1 + (A.level - 1) * k + ff;
-    sco[at] = sc;
-    M.child[c] = desc_key(sc, (uint32_t)c);
-  }
-  __syncthreads();
-  // next frontier: rank of every child by (score desc, creation order);
-  // gs lanes share one child's count
-  int gs = 1;
-  while (gs < 32 && 2 * gs * nc <= kLvThreads) gs *= 2;
-  const int sub = lane & (gs - 1);
-  for (int c0 = 0; c0 < nc; c0 += kLvThreads / gs) {
-    const int c = c0 + tid / gs;
-    const unsigned long long me = (c < nc) ? M.child[c] : ~0ull;
-    int rank = 0;
-#pragma unroll 4
-    for (int j = sub; j < nc; j += gs) rank += (M.child[j] > me);
-    for (int o = gs >> 1; o > 0; o >>= 1) rank += __shfl_xor_sync(0xffffffffu, rank, o);
-    if (c < nc && sub == 0 && rank < k) {
-      front[rank] = base + c;
-      fsc[rank] = key_value(me);
+  if (warp == 0) {
+    // next frontier: the k largest children by (score desc, creation
+    // order).  Row f's children come out of its top-k in descending key
+    // order (fp32 addition of the row's score is monotone, ties fall to the
+    // earlier child), so this is a k-way merge of the rows' lists: lane f
+    // holds row f's next child, one warp maximum per frontier entry.
+    int p = 0;
+    for (int i = 0; i < k; ++i) {
+      unsigned long long key = 0ull;
+      if (lane < F && p < k)
+        key = desc_key(__fadd_rn(M.fsc[lane], key_value(M.row[lane][p])), (uint32_t)(lane * k + p));
+      const unsigned long long mx = warp_max_key(key);
+      if (key == mx && mx != 0ull) {
+        front[i] = base + lane * k + p;
+        fsc[i] = key_value(mx);
+        ++p;
+      }
+    }
+  } else {
+    // the children, in creation order (f-major, rank-minor)
+    for (int c = tid - 32; c < nc; c += kLvThreads - 32) {
+      const int ff = c / k, rr = c % k;
+      const unsigned long long key = M.row[ff][rr];
+      const int at = base + c;
+      tok[at] = (int)key_index(key);
+      par[at] = M.fidx[ff];
+      dep[at] = A.level + 1;
+      prw[at] = (A.level == 0) ? 0 : 1 + (A.level - 1) * k + ff;
+      sco[at] = __fadd_rn(M.fsc[ff], key_value(key));
     }
   }
   if (tid == 0) A.pool.count[b] = base + nc;
@@ -644,8 +676,10 @@ __device__ void finalize_sequence(const FinalParams& A, int b, unsigned char* sm
   int* s_dep = reinterpret_cast<int*>(s_key + A.P);                             // [P]
   int* s_node = s_dep + A.P;                                                    // [P]
   int* s_list = s_node + A.P;                                                   // [P]
-  __shared__ int s_hist[256];
-  __shared__ int s_digit, s_rem, s_eq, s_nsel, s_off;
+  // three histograms in rotation: the one scanned in pass p-1 is cleared in
+  // pass p and filled in pass p+2, so a pass needs a single barrier
+  __shared__ int s_hist[3][256];
+  __shared__ int s_nsel, s_off;
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const int nthreads = blockDim.x;
   const int n = max(0, min(__ldcg(A.pool.count + b), A.P));
@@ -665,6 +699,7 @@ __device__ void finalize_sequence(const FinalParams& A, int b, unsigned char* sm
     for (int o = 16; o > 0; o >>= 1) off += __shfl_xor_sync(0xffffffffu, off, o);
     if (lane == 0) s_off = off;
   }
+  for (int i = tid; i < 2 * 256; i += nthreads) s_hist[i >> 8][i & 255] = 0;
   for (int i = tid; i < n; i += nthreads) {
     s_key[i] = desc_key(__ldcg(sco + i), (uint32_t)i);
     s_dep[i] = __ldcg(dep + i);
@@ -673,47 +708,53 @@ __device__ void finalize_sequence(const FinalParams& A, int b, unsigned char* sm
   // radix select (8 bits at a time, high to low) of the keep-th largest key
   unsigned long long prefix = 0, mask = 0;
   int rem = keep;
+  __syncthreads();
   if (keep > 0 && keep < n) {
-    for (int shift = 56; shift >= 0; shift -= 8) {
-      if (tid < 256) s_hist[tid] = 0;
-      __syncthreads();
+    for (int shift = 56, p = 0; shift >= 0; shift -= 8, ++p) {
+      int* hist = s_hist[p % 3];
       for (int i0 = 0; i0 < n; i0 += nthreads) {   // uniform trip count
         const int i = i0 + tid;
         const unsigned long long key = (i < n) ? s_key[i] : 0ull;
         const int bin = (i < n && (key & mask) == prefix) ? (int)(key >> shift) & 255 : 256;
         const unsigned peers = __match_any_sync(0xffffffffu, bin);
-        if (bin < 256 && lane == __ffs(peers) - 1) atomicAdd(&s_hist[bin], __popc(peers));
+        if (bin < 256 && lane == __ffs(peers) - 1) atomicAdd(&hist[bin], __popc(peers));
       }
       __syncthreads();
-      if (warp == 0) {
-        int h[8], tot = 0;
+      // every warp finds the digit holding the rem-th largest key (the same
+      // answer in each), scanning bins from the top
+      int h[8], tot = 0;
 #pragma unroll
-        for (int d = 0; d < 8; ++d) {
-          h[d] = s_hist[lane * 8 + d];
-          tot += h[d];
-        }
-        int incl = tot;  // sum over this lane and the lanes above it
-#pragma unroll
-        for (int o = 1; o < 32; o <<= 1) {
-          const int t = __shfl_down_sync(0xffffffffu, incl, o);
-          if (lane + o < 32) incl += t;
-        }
-        int above = incl - tot;
-#pragma unroll
-        for (int d = 7; d >= 0; --d) {
-          if (above < rem && rem <= above + h[d]) {
-            s_digit = lane * 8 + d;
-            s_rem = rem - above;
-            s_eq = h[d];
-          }
-          above += h[d];
-        }
+      for (int d = 0; d < 8; ++d) {
+        h[d] = hist[lane * 8 + d];
+        tot += h[d];
       }
-      __syncthreads();
-      prefix |= (unsigned long long)s_digit << shift;
+      int incl = tot;  // sum over this lane and the lanes above it
+#pragma unroll
+      for (int o = 1; o < 32; o <<= 1) {
+        const int t = __shfl_down_sync(0xffffffffu, incl, o);
+        if (lane + o < 32) incl += t;
+      }
+      int above = incl - tot, digit = -1, nrem = 0, eq = 0;
+#pragma unroll
+      for (int d = 7; d >= 0; --d) {
+        if (above < rem && rem <= above + h[d]) {
+          digit = lane * 8 + d;
+          nrem = rem - above;
+          eq = h[d];
+        }
+        above += h[d];
+      }
+      const unsigned owner = __ballot_sync(0xffffffffu, digit >= 0);
+      const int src = owner ? __ffs(owner) - 1 : 0;
+      digit = __shfl_sync(0xffffffffu, digit, src);
+      nrem = __shfl_sync(0xffffffffu, nrem, src);
+      eq = __shfl_sync(0xffffffffu, eq, src);
+      // the histogram scanned in the pass before is free again
+      for (int i = tid; i < 256; i += nthreads) s_hist[(p + 2) % 3][i] = 0;
+      prefix |= (unsigned long long)digit << shift;
       mask |= 255ull << shift;
-      rem = s_rem;
-      if (s_eq == rem) break;  // every key under this prefix is kept
+      rem = nrem;
+      if (eq == rem) break;  // every key under this prefix is kept
     }
   }
   // kept: keys >= the threshold (prefix, low bits zero), exactly `keep` of them
