@@ -668,47 +668,60 @@ expand_level_stream_kernel(const LevelParams A, int total_chunks) {
 // multiple of 64): keep the `budget` pool entries of largest key (score
 // desc, creation order) -- a radix select of the budget-th key -- number the
 // kept nodes by (depth, score desc, creation order) and write the tree.
-// `smem_raw`: 20 * P bytes of shared memory.  Every sequence's pool holds
+// `smem_raw`: 44 * P bytes of shared memory.  Every sequence's pool holds
 // P = k + (depth-1) k^2 entries after the last level, which fixes the node
 // offset of each sequence without waiting for the others.
 __device__ void finalize_sequence(const FinalParams& A, int b, unsigned char* smem_raw) {
+  // every pool array of the sequence in shared memory, loaded in one round
+  // trip (the pool holds P slots whatever its fill)
+  const int P = A.P;
   unsigned long long* s_key = reinterpret_cast<unsigned long long*>(smem_raw);  // [P]
-  int* s_dep = reinterpret_cast<int*>(s_key + A.P);                             // [P]
-  int* s_node = s_dep + A.P;                                                    // [P]
-  int* s_list = s_node + A.P;                                                   // [P]
+  unsigned long long* c_key = s_key + P;     // kept keys, compacted           [P]
+  int* s_dep = reinterpret_cast<int*>(c_key + P);                              // [P]
+  int* s_par = s_dep + P;
+  int* s_tok = s_par + P;
+  int* s_prw = s_tok + P;
+  int* s_node = s_prw + P;
+  int* s_list = s_node + P;                  // pool index of each kept entry
+  int* c_dep = s_list + P;                   // its depth, compacted
   // three histograms in rotation: the one scanned in pass p-1 is cleared in
   // pass p and filled in pass p+2, so a pass needs a single barrier
   __shared__ int s_hist[3][256];
-  __shared__ int s_nsel, s_off;
+  __shared__ int s_nsel, s_off, s_n;
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const int nthreads = blockDim.x;
-  const int n = max(0, min(__ldcg(A.pool.count + b), A.P));
   const int bud = A.budget[b];
-  const int keep = min(max(bud, 0), n);
-  const float* sco = A.pool.score + (size_t)b * A.P;
-  const int* dep = A.pool.depth + (size_t)b * A.P;
   if (tid == 0) {
     s_nsel = 0;
+    s_n = max(0, min(__ldcg(A.pool.count + b), P));
     if (bud < 0) fail(A.status, EAGLE_ERR_INVALID_ARG);
   }
   if (warp == 1) {
     // node offset of this sequence: sum over earlier sequences of kept + root
     int off = 0;
-    for (int j = lane; j < b; j += 32) off += min(max(A.budget[j], 0), A.P) + 1;
+    for (int j = lane; j < b; j += 32) off += min(max(A.budget[j], 0), P) + 1;
 #pragma unroll
     for (int o = 16; o > 0; o >>= 1) off += __shfl_xor_sync(0xffffffffu, off, o);
     if (lane == 0) s_off = off;
   }
   for (int i = tid; i < 2 * 256; i += nthreads) s_hist[i >> 8][i & 255] = 0;
-  for (int i = tid; i < n; i += nthreads) {
-    s_key[i] = desc_key(__ldcg(sco + i), (uint32_t)i);
-    s_dep[i] = __ldcg(dep + i);
-    s_node[i] = -1;
+  {
+    const size_t o = (size_t)b * P;
+    for (int i = tid; i < P; i += nthreads) {
+      s_key[i] = desc_key(__ldcg(A.pool.score + o + i), (uint32_t)i);
+      s_dep[i] = __ldcg(A.pool.depth + o + i);
+      s_par[i] = __ldcg(A.pool.parent + o + i);
+      s_tok[i] = __ldcg(A.pool.token + o + i);
+      s_prw[i] = __ldcg(A.pool.prow + o + i);
+      s_node[i] = -1;
+    }
   }
+  __syncthreads();
+  const int n = s_n;
+  const int keep = min(max(bud, 0), n);
   // radix select (8 bits at a time, high to low) of the keep-th largest key
   unsigned long long prefix = 0, mask = 0;
   int rem = keep;
-  __syncthreads();
   if (keep > 0 && keep < n) {
     for (int shift = 56, p = 0; shift >= 0; shift -= 8, ++p) {
       int* hist = s_hist[p % 3];
@@ -757,11 +770,18 @@ __device__ void finalize_sequence(const FinalParams& A, int b, unsigned char* sm
       if (eq == rem) break;  // every key under this prefix is kept
     }
   }
-  // kept: keys >= the threshold (prefix, low bits zero), exactly `keep` of them
+  // kept: keys >= the threshold (prefix, low bits zero), exactly `keep` of
+  // them; compacted with their depths
   const unsigned long long tau = (keep == 0) ? ~0ull : (keep == n ? 1ull : prefix);
-  __syncthreads();
-  for (int i = tid; i < n; i += nthreads)
-    if (keep > 0 && s_key[i] >= tau) s_list[atomicAdd(&s_nsel, 1)] = i;
+  for (int i = tid; i < n; i += nthreads) {
+    const unsigned long long key = s_key[i];
+    if (keep > 0 && key >= tau) {
+      const int at = atomicAdd(&s_nsel, 1);
+      s_list[at] = i;
+      c_key[at] = key;
+      c_dep[at] = s_dep[i];
+    }
+  }
   __syncthreads();
   const int ns = s_nsel;
   const int off = s_off;
@@ -772,34 +792,29 @@ __device__ void finalize_sequence(const FinalParams& A, int b, unsigned char* sm
   const int sub = lane & (gs - 1);
   for (int a0 = 0; a0 < ns; a0 += nthreads / gs) {
     const int a = a0 + tid / gs;
-    const int ia = (a < ns) ? s_list[a] : 0;
-    const int da = (a < ns) ? s_dep[ia] : 0;
-    const unsigned long long ka = (a < ns) ? s_key[ia] : 0ull;
+    const int da = (a < ns) ? c_dep[a] : 0;
+    const unsigned long long ka = (a < ns) ? c_key[a] : 0ull;
     int rank = 0;
 #pragma unroll 4
     for (int c = sub; c < ns; c += gs) {
-      const int ic = s_list[c];
-      const int dc = s_dep[ic];
-      rank += (dc < da) || (dc == da && s_key[ic] > ka);
+      const int dc = c_dep[c];
+      rank += (dc < da) || (dc == da && c_key[c] > ka);
     }
     for (int o = gs >> 1; o > 0; o >>= 1) rank += __shfl_xor_sync(0xffffffffu, rank, o);
-    if (a < ns && sub == 0) s_node[ia] = 1 + rank;
+    if (a < ns && sub == 0) s_node[s_list[a]] = 1 + rank;
   }
   __syncthreads();
-  const int* tok = A.pool.token + (size_t)b * A.P;
-  const int* par = A.pool.parent + (size_t)b * A.P;
-  const int* prw = A.pool.prow + (size_t)b * A.P;
   for (int a = tid; a < ns; a += nthreads) {
     const int ia = s_list[a];
-    const int pp = __ldcg(par + ia);
+    const int pp = s_par[ia];
     const int pnode = (pp < 0) ? 0 : (pp < n ? s_node[pp] : -1);
     if (pnode < 0) fail(A.status, EAGLE_ERR_INVALID_TREE);  // not parent-closed
     const int at = off + s_node[ia];
     A.parent[at] = pnode;
-    A.tokens[at] = __ldcg(tok + ia);
+    A.tokens[at] = s_tok[ia];
     A.node_depth[at] = s_dep[ia];
     A.score[at] = key_value(s_key[ia]);
-    A.p_row_of_node[at] = b * A.R + __ldcg(prw + ia);
+    A.p_row_of_node[at] = b * A.R + s_prw[ia];
   }
   if (tid == 0) {
     A.tree_off[b] = off;
@@ -848,7 +863,7 @@ extern "C" eagle_status eagle_draft_expand(int B, int V, int k, int depth, int l
   const int R = 1 + (depth - 1) * k;
   EAGLE_HOST_CHECK(finalize >= 0 && finalize <= 2, EAGLE_ERR_INVALID_ARG);
   FinalParams F;
-  const size_t fin_smem = (size_t)L.P * (8 + 4 + 4 + 4);
+  const size_t fin_smem = (size_t)L.P * (2 * 8 + 7 * 4);
   if (finalize) {
     EAGLE_HOST_CHECK(d_budget && d_tree_off && d_parent && d_tokens && d_node_depth && d_score &&
                          d_p_row_of_node,
