@@ -13,7 +13,8 @@
 // so each visited node's q and p rows are read from HBM exactly once and
 // every rejection round runs out of registers.  Each round publishes its
 // integer sums (and the tested token's values) through distributed shared
-// memory behind one cluster barrier; every CTA then takes the identical
+// memory: each CTA pushes its values into every CTA's shared memory, then
+// one cluster barrier; every CTA then takes the identical
 // decision (the data it decides on is bit-identical), so control flow stays
 // uniform across the cluster without any spin-wait.
 #include <math.h>
@@ -133,6 +134,8 @@ struct StochParams {
 
 __device__ __forceinline__ bool is_prob(float x) { return x >= 0.f && x <= 1.f; }
 
+
+
 // Fixed-point weights.  For r in [0, 1], x = r * 2^40 is exact in fp32.
 // W = trunc(x) as an integer, and fp32(W) rounded to nearest, computed with
 // 32-bit operations only: below 2^23 x fits a 32-bit truncation; from 2^23
@@ -145,10 +148,9 @@ __device__ __forceinline__ unsigned long long fixed40_int(float r) {
   const unsigned long long m = (bits & 0x7fffffu) | 0x800000u;
   return m << (e - 23);
 }
-__device__ __forceinline__ float fixed40_f(float r) {
-  const float x = r * kTwo40;
-  return (x < 8388608.f) ? __uint2float_rn(__float2uint_rz(x)) : x;
-}
+// fp32(W) = trunc(x) itself: below 2^23 the truncation is exact in fp32,
+// above it x is already an integer.
+__device__ __forceinline__ float fixed40_f(float r) { return truncf(r * kTwo40); }
 
 // Two sums over the block at once; every thread gets both totals.
 __device__ void block_sum2_u64(unsigned long long& a, unsigned long long& b,
@@ -258,7 +260,7 @@ accept_stochastic_kernel(const StochParams P) {
   const unsigned rank = cluster.block_rank();
   const unsigned CS = cluster.num_blocks();
   const int b = blockIdx.x / CS;
-  const int tid = threadIdx.x;
+  const int tid = threadIdx.x, lane = tid & 31;
 
   extern __shared__ __align__(16) unsigned char smem_raw[];
   float* s_q = reinterpret_cast<float*>(smem_raw);            // slice, for sampling
@@ -267,9 +269,13 @@ accept_stochastic_kernel(const StochParams P) {
   int* s_kids = s_tok + P.max_nodes;
   __shared__ unsigned long long s_red[66];
   __shared__ RoundSlot s_slot[2];            // double-buffered by round parity
-  __shared__ unsigned long long s_tot;
-  __shared__ unsigned long long s_bc[2];
-  __shared__ float s_test[2];
+  // What every CTA of the cluster pushed here, by round parity: its sums,
+  // the tested token's q and p (from the CTA that owns the token), and for
+  // the bonus token its total weight.  Pushing before the cluster barrier
+  // leaves only local reads after it.
+  __shared__ unsigned long long s_all[2][16][2];
+  __shared__ float s_test[2][2];
+  __shared__ unsigned long long s_tots[16];
   __shared__ int s_flag, s_nk;
 
   const int v0 = (int)rank * P.slice;
@@ -321,11 +327,21 @@ accept_stochastic_kernel(const StochParams P) {
   if (writer && tid == 0) o_nodes[0] = 0;
 
   while (true) {
-    if (tid == 0) {
+    // every warp has read the previous node's child list before it is
+    // rewritten
+    __syncthreads();
+    // children of cur in index order, by warp 0 (children follow their
+    // parent: only indices past cur are looked at)
+    if (tid < 32) {
       int c = 0;
-      for (int i = cur + 1; i < n; ++i)
-        if (s_par[i] == cur) s_kids[c++] = i;
-      s_nk = c;
+      for (int base = cur + 1; base < n; base += 32) {
+        const int i = base + tid;
+        const bool kid = (i < n) && s_par[i] == cur;
+        const unsigned bal = __ballot_sync(0xffffffffu, kid);
+        if (kid) s_kids[c + __popc(bal & ((1u << tid) - 1u))] = i;
+        c += __popc(bal);
+      }
+      if (tid == 0) s_nk = c;
     }
     __syncthreads();
     const int nk = s_nk;
@@ -342,7 +358,7 @@ accept_stochastic_kernel(const StochParams P) {
     {
       const float* qrow = P.q + (size_t)(t0 + cur) * P.V + v0;
       const float* prw = P.p_rows + (size_t)prow * P.V + v0;
-      const float lse = LOGITS ? __ldg(P.row_lse + t0 + cur) : 0.f;
+      const ProbScales sc = prob_scales(P.temperature, LOGITS ? __ldg(P.row_lse + t0 + cur) : 0.f);
       int bad = 0;
 #pragma unroll
       for (int e = 0; e < E; ++e) {
@@ -351,7 +367,7 @@ accept_stochastic_kernel(const StochParams P) {
         p[e] = 0.f;
         if (i < nv) {
           q[e] = __ldg(qrow + i);
-          if (LOGITS) q[e] = expf(__fdiv_rn(q[e], P.temperature) - lse);
+          if (LOGITS) q[e] = prob_from_logit(q[e], sc);
           bad |= !is_prob(q[e]);
           if (nk > 0) {
             p[e] = __ldg(prw + i);
@@ -368,33 +384,28 @@ accept_stochastic_kernel(const StochParams P) {
     float qt = 0.f, pt = 0.f;
     auto reduce_round = [&](unsigned long long sw, unsigned long long sp, int t) {
       block_sum2_u64(sw, sp, s_red);
-      if (tid == 0) {
-        s_slot[par].w = sw;
-        s_slot[par].p = sp;
+      const unsigned owner = (unsigned)(t / P.slice);
+      if (tid < (int)CS) {
+        unsigned long long* d = cluster.map_shared_rank(&s_all[par][rank][0], (unsigned)tid);
+        d[0] = sw;
+        d[1] = sp;
+        if (owner == rank) {
+          float* dt = cluster.map_shared_rank(&s_test[par][0], (unsigned)tid);
+          dt[0] = s_slot[par].qt;
+          dt[1] = s_slot[par].pt;
+        }
       }
       cluster.sync();
-      if (tid < 32) {
-        unsigned long long a = 0, bb = 0;
-        if (tid < (int)CS) {
-          const RoundSlot* r = cluster.map_shared_rank(&s_slot[par], tid);
-          a = r->w;
-          bb = r->p;
-        }
-        a = warp_sum_u64(a);
-        bb = warp_sum_u64(bb);
-        if (tid == 0) {
-          s_bc[0] = a;
-          s_bc[1] = bb;
-          const RoundSlot* o = cluster.map_shared_rank(&s_slot[par], (unsigned)(t / P.slice));
-          s_test[0] = o->qt;
-          s_test[1] = o->pt;
-        }
+      // every warp adds the CTAs' sums itself: no barrier after the reads
+      unsigned long long a = 0, bb = 0;
+      if (lane < (int)CS) {
+        a = s_all[par][lane][0];
+        bb = s_all[par][lane][1];
       }
-      __syncthreads();
-      Z = s_bc[0];
-      SP = s_bc[1];
-      qt = s_test[0];
-      pt = s_test[1];
+      Z = warp_sum_u64(a);
+      SP = warp_sum_u64(bb);
+      qt = s_test[par][0];
+      pt = s_test[par][1];
       par ^= 1;
     };
     if (nk > 0) {
@@ -459,26 +470,20 @@ accept_stochastic_kernel(const StochParams P) {
       const int per = (nv + (int)blockDim.x - 1) / (int)blockDim.x;
       const int c0 = min(nv, tid * per), c1 = min(nv, c0 + per);
       unsigned long long mine = 0;
-      for (int i = c0; i < c1; ++i) mine += fixed40_int(s_q[i]);
+      // a rotated start keeps the lanes of a warp on different banks
+      const int len = c1 - c0;
+      for (int j = 0; j < len; ++j) mine += fixed40_int(s_q[c0 + (j + tid) % len]);
       unsigned long long cta_total;
       const unsigned long long excl = block_excl_scan_u64(mine, s_red, &cta_total);
-      if (tid == 0) s_tot = cta_total;
+      if (tid < (int)CS) *cluster.map_shared_rank(&s_tots[rank], (unsigned)tid) = cta_total;
       cluster.sync();
-      if (tid < 32) {
-        unsigned long long all = 0, before = 0;
-        if (tid < (int)CS) {
-          all = *cluster.map_shared_rank(&s_tot, tid);
-          before = (tid < (int)rank) ? all : 0ull;
-        }
-        all = warp_sum_u64(all);
-        before = warp_sum_u64(before);
-        if (tid == 0) {
-          s_bc[0] = before;
-          s_bc[1] = all;
-        }
+      unsigned long long all = 0, bef = 0;
+      if (lane < (int)CS) {
+        all = s_tots[lane];
+        bef = (lane < (int)rank) ? all : 0ull;
       }
-      __syncthreads();
-      const unsigned long long before = s_bc[0], Z = s_bc[1];
+      const unsigned long long Z = warp_sum_u64(all);
+      const unsigned long long before = warp_sum_u64(bef);
       const float us = P.u_sample[t0 + cur];
       if (!(us >= 0.f && us < 1.f)) {
         if (writer && tid == 0) fail(P.status, EAGLE_ERR_INVALID_ARG);
@@ -513,6 +518,8 @@ accept_stochastic_kernel(const StochParams P) {
 
 // Cluster size and per-thread element count for a vocabulary: slices of
 // at most 512 x 32 entries; prefer <= 512 x 16 (registers), up to 16 CTAs.
+// (Measured at 16 sequences of V = 128256: halving the clusters to fit
+// them all at once, 32 entries per thread, was slower than a second wave.)
 int pick_cluster(int V, int* slice_out, int* elems_out) {
   for (int cs = 1; cs <= 16; cs <<= 1) {
     int slice = (V + cs - 1) / cs;
@@ -526,6 +533,7 @@ int pick_cluster(int V, int* slice_out, int* elems_out) {
   }
   return -1;
 }
+
 
 }  // namespace
 

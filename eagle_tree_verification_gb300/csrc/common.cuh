@@ -46,6 +46,27 @@ __device__ __forceinline__ float key_value(unsigned long long k) {
   return from_ordered_bits((uint32_t)(k >> 32));
 }
 
+// Target probability of a logit: q = 2^(z * log2(e)/T - lse * log2(e)),
+// the exponent formed by one fused multiply-add and evaluated by the SFU's
+// ex2 (relative error about 2^-22; results below 2^-126 flush to zero).  The
+// LM head's probability mode and the walk that reads logits both call this
+// with scales from prob_scales, so their q agree bit for bit.
+struct ProbScales {
+  float k2;     // log2(e) / T
+  float lse2;   // lse * log2(e)
+};
+__device__ __forceinline__ ProbScales prob_scales(float temperature, float lse) {
+  ProbScales s;
+  s.k2 = __fdiv_rn(1.4426950408889634f, temperature);
+  s.lse2 = __fmul_rn(lse, 1.4426950408889634f);
+  return s;
+}
+__device__ __forceinline__ float prob_from_logit(float z, ProbScales s) {
+  float y;
+  asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(fmaf(z, s.k2, -s.lse2)));
+  return y;
+}
+
 __device__ __forceinline__ unsigned long long warp_max_u64(unsigned long long v) {
 #pragma unroll
   for (int o = 16; o > 0; o >>= 1) {

@@ -211,11 +211,10 @@ lmhead_finalize_kernel(int T, int V, float temperature, const Partial* __restric
   }
   __syncthreads();
   if (q) {
-    const float lse = s_lse;
+    const ProbScales sc = prob_scales(temperature, s_lse);
     const int c0 = blockIdx.y * kFinChunk, c1 = min(V, c0 + kFinChunk);
     float* row = q + (size_t)r * V;
-    for (int v = c0 + tid; v < c1; v += blockDim.x)
-      row[v] = expf(__fdiv_rn(row[v], temperature) - lse);
+    for (int v = c0 + tid; v < c1; v += blockDim.x) row[v] = prob_from_logit(row[v], sc);
   }
 }
 

@@ -133,8 +133,12 @@ EAGLE_API eagle_status eagle_tree_attn(eagle_dtype dtype, int B, int T, int Hq, 
  * temperature > 0.
  * mode        EAGLE_LMHEAD_GREEDY: no [T,V] tensor is written.
  *             EAGLE_LMHEAD_PROB:   d_q [T,V] fp32 receives softmax(z/temp),
- *                                  each entry expf(rn(z/temp) - row_lse) in
- *                                  fp32 (rn: division rounded to nearest).
+ *                                  each entry 2^fma(z, k2, -lse2) with
+ *                                  k2 = rn(log2(e)/temp), lse2 =
+ *                                  rn(row_lse * log2(e)) (rn: rounded to
+ *                                  nearest), the power by the GPU's
+ *                                  approximate base-2 exponential (relative
+ *                                  error about 2^-22).
  *             EAGLE_LMHEAD_LOGITS: d_q [T,V] fp32 receives the logits z
  *                                  themselves; with d_row_lse they are what
  *                                  eagle_accept_stochastic_logits reads.
@@ -259,10 +263,9 @@ EAGLE_API eagle_status eagle_accept_stochastic(int B, int max_nodes, int V, int 
  *
  * The walk reads q only for the nodes it visits (alpha + 1 of them per
  * sequence), so normalising every node's row beforehand is wasted work.
- * Here each visited row is normalised as it is loaded:
- *   q[t,v] = expf(rn(z[t,v] / temperature) - row_lse[t])   (fp32)
- * -- the same expression, evaluated by the same library, as
- * eagle_lmhead_softmax's PROB mode, so given that call's d_row_lse the
+ * Here each visited row is normalised as it is loaded, with the same fp32
+ * expression and the same instructions as eagle_lmhead_softmax's PROB mode
+ * (see there), so given that call's d_row_lse the
  * probabilities, and with them every decision and token, are identical to
  * eagle_accept_stochastic fed with PROB mode's d_q.  Everything else is as
  * eagle_accept_stochastic.

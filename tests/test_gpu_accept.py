@@ -150,11 +150,13 @@ def test_stochastic_walk_matches_oracle(mode, seed, B, V):
         np.testing.assert_array_equal(x, r)
 
 
-def test_stochastic_many_rejections_then_sample_at_full_vocab():
+@pytest.mark.parametrize("B", [4, 12])
+def test_stochastic_many_rejections_then_sample_at_full_vocab(B):
     # random target vs random draft: almost every child is rejected, so every
-    # sequence runs up to k residual rounds and then the inverse-CDF sampler
+    # sequence runs up to k residual rounds and then the inverse-CDF sampler.
+    # B = 12: more clusters than fit the GPU at once (two waves).
     E = cuda_ready()
-    V, B = 128256, 4
+    V = 128256
     case = _stoch_case(11, B, V, [(1, 8, 8)], plant_frac=0.0)
     for mode in (O.MODE_NO_REPLACE, O.MODE_REPLACE):
         ref = O.accept_stochastic(*case, max_depth=2, mode=mode)
