@@ -483,13 +483,15 @@ tree_attn_tc_kernel(const __grid_constant__ CUtensorMap map_q,
           tc::fence_after_thread_sync();
           const uint32_t v_addr = tc::smem_u32(v_sm + st * kTileBytes);
           // O_h += P_hi V_h + P_lo V_h for key half h: A = P from the half's
-          // TMEM columns, B = V rows of that half (MN-major, 128-byte rows)
+          // TMEM columns, B = V rows of that half (MN-major, 128-byte rows).
+          // The two halves' accumulator chains are interleaved (each in its
+          // own order), so the tensor pipe always has an independent MMA.
 #pragma unroll
-          for (int h = 0; h < 2; ++h) {
+          for (int part = 0; part < 2; ++part) {
 #pragma unroll
-            for (int part = 0; part < 2; ++part) {
+            for (int kk = 0; kk < 4; ++kk) {
 #pragma unroll
-              for (int kk = 0; kk < 4; ++kk) {
+              for (int h = 0; h < 2; ++h) {
                 const uint32_t a_tm = tmem + (uint32_t)(128 + h * 64 + part * 32 + kk * 8);
                 const uint32_t key = (uint32_t)(h * 64 + kk * 16);
                 mma_f16_tmem_a(tmem + 256u + (uint32_t)(h * 128), a_tm,
