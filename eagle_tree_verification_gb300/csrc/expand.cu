@@ -921,6 +921,17 @@ extern "C" eagle_status eagle_draft_expand(int B, int V, int k, int depth, int l
   void (*kern)(const LevelParams) = (cp.vec == 1)   ? expand_level_kernel<1>
                                     : (cp.vec == 2) ? expand_level_kernel<2>
                                                     : expand_level_kernel<4>;
+  static bool carveout = false;
+  if (!carveout) {
+    // the whole unified L1 as shared memory wherever an expand CTA lands
+    // first, so that the LM head running beside the expand still fits
+    for (auto k : {expand_level_kernel<1>, expand_level_kernel<2>, expand_level_kernel<4>})
+      cudaFuncSetAttribute(k, cudaFuncAttributePreferredSharedMemoryCarveout,
+                           cudaSharedmemCarveoutMaxShared);
+    cudaFuncSetAttribute(expand_level_stream_kernel, cudaFuncAttributePreferredSharedMemoryCarveout,
+                         cudaSharedmemCarveoutMaxShared);
+    carveout = true;
+  }
   // levels beyond one wave even at the largest chunks stream through
   // persistent CTAs (no finalize fusion there)
   const long long total_chunks = (long long)B * A.F * A.S;

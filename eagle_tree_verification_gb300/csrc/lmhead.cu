@@ -251,6 +251,10 @@ constexpr int kMaxCluster = 4;    // row tiles sharing one W stream
 constexpr int kMaxHStages = 4;
 constexpr int kMaxWStages = 12;
 constexpr size_t kSmemLimit = 227 * 1024;
+// A W ring within this budget (when it still holds four stages) leaves room
+// on the SM for one CTA of the tree expand (up to ~55 KB), which the step
+// runs concurrently with the LM head.
+constexpr size_t kSmemShared = 171 * 1024;
 constexpr size_t kTcSharedBytes = 1024 + 2 * 128 * 16;
 
 struct TcShared {
@@ -279,7 +283,9 @@ TcLayout tc_layout(int h_rows) {
   L.h_stages = kMaxHStages;
   L.w_stage_bytes = L.blk * 128;
   const size_t fixed = 1024 + (size_t)L.h_stages * L.h_stage_bytes + kTcSharedBytes;
-  L.w_stages = (int)std::min<size_t>(kMaxWStages, (kSmemLimit - fixed) / L.w_stage_bytes);
+  const size_t limit =
+      (fixed + 4 * (size_t)L.w_stage_bytes <= kSmemShared) ? kSmemShared : kSmemLimit;
+  L.w_stages = (int)std::min<size_t>(kMaxWStages, (limit - fixed) / L.w_stage_bytes);
   L.smem = fixed + (size_t)L.w_stages * L.w_stage_bytes;
   return L;
 }
@@ -727,10 +733,15 @@ extern "C" eagle_status eagle_lmhead_softmax(eagle_dtype dtype, int T, int H, in
     if (!make_map_bf16(&map_w, d_w, V, H, kUnit)) return EAGLE_ERR_CUDA;
     static bool attr = false;
     if (!attr) {
+      // the whole unified L1 as shared memory, so that a CTA of the
+      // concurrently running tree expand fits beside this one
       if (cudaFuncSetAttribute(lmhead_tc_kernel<false>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                (int)kSmemLimit) != cudaSuccess ||
           cudaFuncSetAttribute(lmhead_tc_kernel<true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                               (int)kSmemLimit) != cudaSuccess)
+                               (int)kSmemLimit) != cudaSuccess ||
+          cudaFuncSetAttribute(lmhead_tc_kernel<false>,
+                               cudaFuncAttributePreferredSharedMemoryCarveout,
+                               cudaSharedmemCarveoutMaxShared) != cudaSuccess)
         return EAGLE_ERR_CUDA;
       attr = true;
     }

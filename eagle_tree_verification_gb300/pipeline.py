@@ -130,6 +130,7 @@ class TreeVerifyStep:
         self.top2_gap = z(T)
         # stochastic: the target logits; the walk normalises the rows it visits
         self.logits = z(T, s.V) if s.mode == "stochastic" else None
+        self._side = None   # second stream of run() (the LM head)
         W = s.max_depth + 1
         self.accept_len = z(s.B, dtype=i32)
         self.accepted_nodes = z(s.B, W, dtype=i32)
@@ -216,12 +217,25 @@ class TreeVerifyStep:
 
     def run(self, stream=None, build_tree: bool = True) -> None:
         """The whole step: tree build (if EAGLE-2), attention, LM head, accept.
-        build_tree=False verifies the tree already in the buffers."""
+        build_tree=False verifies the tree already in the buffers.
+
+        The LM head needs neither the tree nor the attention output, so it
+        runs on a second stream, forked after everything queued so far and
+        joined before the acceptance walk: its weight stream overlaps the
+        latency-bound tree build (whose CTAs fit beside the LM head's on the
+        same SMs) and the attention."""
+        torch = self.torch
+        main = stream if stream is not None else torch.cuda.current_stream()
+        if self._side is None:
+            self._side = torch.cuda.Stream(device=main.device)
+        side = self._side
+        side.wait_stream(main)
+        self.run_lmhead(side)
         if self.s.k and build_tree:
-            self.run_expand(stream)
-        self.run_attn(stream)
-        self.run_lmhead(stream)
-        self.run_accept(stream)
+            self.run_expand(main)
+        self.run_attn(main)
+        main.wait_stream(side)
+        self.run_accept(main)
 
     def launches_per_step(self) -> int:
         """Kernels launched by run() (the count the benchmark reports)."""
