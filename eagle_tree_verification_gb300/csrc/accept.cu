@@ -211,11 +211,10 @@ __device__ unsigned long long block_excl_scan_u64(unsigned long long v, unsigned
   return s_tmp[w] + inc - v;
 }
 
-// What each CTA publishes to the cluster in one rejection round.
+// The tested token's target and draft values of one rejection round, kept
+// by the CTA that owns the token (its sums go straight to every CTA).
 struct RoundSlot {
-  unsigned long long w;   // sum of the residual weights of this CTA's slice
-  unsigned long long p;   // sum of the draft weights (rejected token excluded)
-  float qt, pt;           // q_k[t], p_k[t] if this CTA owns the tested token t
+  float qt, pt;           // q_k[t], p_k[t]
 };
 
 // One pass over this thread's slice entries.  UPD: the rejection update of
