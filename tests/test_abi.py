@@ -66,6 +66,16 @@ def test_host_argument_checks_return_before_any_device_work(E):
     assert L.eagle_lmhead_softmax(1, 4, 8, 8, 0.0, 0, *([null] * 8), 0, null, null) == 1
     # unknown sampling mode
     assert L.eagle_accept_stochastic(1, 8, 10, 10, 7, *([null] * 8), 3, *([null] * 5)) == 1
+    # the logits walk: temperature must be positive, row_lse given
+    fake = ctypes.c_void_p(256)         # never dereferenced: the calls return first
+    ptrs = [fake] * 5
+    assert L.eagle_accept_stochastic_logits(1, 8, 10, 10, 1, *ptrs, 0.0, *([fake] * 4), 3,
+                                            *([fake] * 4), null) == 1
+    ptrs[4] = null                      # no row_lse
+    assert L.eagle_accept_stochastic_logits(1, 8, 10, 10, 1, *ptrs, 1.0, *([fake] * 4), 3,
+                                            *([fake] * 4), null) == 1
+    # LM head: an unknown mode
+    assert L.eagle_lmhead_softmax(1, 4, 8, 8, 1.0, 3, *([null] * 8), 0, null, null) == 1
     # pool too small
     fake = ctypes.c_void_p(256)         # never dereferenced: the call returns first
     assert L.eagle_draft_expand(1, 100, 4, 3, 0, 0, null, null, null, fake, 16,
