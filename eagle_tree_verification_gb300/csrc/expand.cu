@@ -12,8 +12,11 @@
 // largest key, so only the few keys above it take part in the exact rank
 // count.  The last CTA of a sequence to finish (an atomic ticket) merges the
 // rows' chunk lists the same way (one warp per row), then builds the
-// children and the next frontier.  The finalize is one CTA per sequence: a
-// radix select of the budget-th largest score key, then the numbering.
+// children and the next frontier.  A level's rows do not depend on the
+// level before it, so past level 0 only that merging CTA waits for the
+// previous level: the chunk work overlaps the previous merge.  The finalize
+// is one CTA per sequence: a radix select of the budget-th largest score
+// key, then the numbering.
 // Selection keys are 64-bit integers (ordered value bits | inverted index),
 // so every tie rule is a plain integer comparison and all keys are distinct.
 #include <algorithm>

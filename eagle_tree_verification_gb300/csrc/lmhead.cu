@@ -6,17 +6,20 @@
 // head gives the next-token distribution of every node.
 //
 // Kernels:
-//   lmhead_tc_kernel       bf16, 128 rows per launch: persistent tcgen05 GEMM.  Each
-//                          CTA owns a contiguous slice of the vocabulary and
-//                          streams its rows of W once through a TMA ring;
-//                          tree rows sit on TMEM lanes, so every thread owns
-//                          one row and its softmax statistics are thread-local.
-//                          One partial per (row, CTA).
+//   lmhead_tc_kernel       bf16: persistent tcgen05 GEMM, one 128-row tile of
+//                          tree rows per CTA.  Each CTA (or cluster of up to
+//                          four CTAs, one row tile each, sharing every W stage
+//                          by TMA multicast) owns a contiguous slice of the
+//                          vocabulary and streams its rows of W once through a
+//                          TMA ring; tree rows sit on TMEM lanes, so every
+//                          thread owns one row and its softmax statistics are
+//                          thread-local.  One partial per (row, slice).
 //   lmhead_tile_kernel     CUDA-core kernel for fp32 inputs (tensor cores
 //                          would round them to tf32): per-(row, 64-vocab
 //                          tile) partials.
 //   lmhead_finalize_kernel per (row, vocab chunk): combines the partials of
-//                          the row; in PROB mode rewrites z as softmax(z/T).
+//                          the row; in PROB mode rewrites z as softmax(z/T)
+//                          (LOGITS mode leaves z).
 #include <math.h>
 
 #include <algorithm>
