@@ -258,6 +258,7 @@ constexpr size_t kSmemLimit = 227 * 1024;
 // on the SM for one CTA of the tree expand (up to ~55 KB), which the step
 // runs concurrently with the LM head.
 constexpr size_t kSmemShared = 171 * 1024;
+constexpr int kSmsForOthers = 16;
 constexpr size_t kTcSharedBytes = 1024 + 2 * 128 * 16;
 
 struct TcShared {
@@ -757,7 +758,9 @@ extern "C" eagle_status eagle_lmhead_softmax(eagle_dtype dtype, int T, int H, in
       slices = std::min(max_clusters(C, tc_layout(kTileRows).smem), n_units);
       if (slices < 1) C = 1;   // clusters of C cannot be resident: one tile per launch
     }
-    if (C == 1) slices = std::min(sm_count(), n_units);
+    // one tile: leave a few SMs to the attention, which the step runs while
+    // the LM head is still streaming W (it does not fit beside an LM head CTA)
+    if (C == 1) slices = std::min(std::max(1, sm_count() - kSmsForOthers), n_units);
     for (int r0 = 0; r0 < T; r0 += C * kTileRows) {
       const int Ts = std::min(C * kTileRows, T - r0);
       const TcLayout TL = tc_layout((C > 1 || Ts > kTileRows) ? kTileRows : ((Ts + 7) / 8) * 8);
