@@ -88,5 +88,46 @@ def build(verbose: bool = False, force: bool = False, extra_flags=()) -> str:
     return LIB
 
 
+def build_variant(name: str, sources, defines=(), force: bool = False) -> str:
+    """Build a separate shared library `name` (next to libeagle.so) from a
+    subset of the CUDA sources with extra preprocessor definitions.  Used by
+    tests that need a differently configured copy of some kernels (for
+    example a tiny device wait budget); the product library is untouched."""
+    flags = ["-D" + d for d in defines]
+    srcs = [os.path.join(CSRC, f) for f in sources]
+    out = os.path.join(HERE, name)
+    stamp = out + ".stamp"
+    h = hashlib.sha256(_fingerprint(flags).encode())
+    h.update(" ".join(sorted(sources)).encode())
+    fp = h.hexdigest()
+    if not force and os.path.exists(out) and os.path.exists(stamp):
+        with open(stamp) as f:
+            if f.read().strip() == fp:
+                return out
+    bdir = os.path.join(BUILD, name.replace(".", "_"))
+    os.makedirs(bdir, exist_ok=True)
+    nvcc = _nvcc()
+
+    def compile_one(src):
+        obj = os.path.join(bdir, os.path.basename(src)[:-3] + ".o")
+        r = subprocess.run([nvcc] + NVCC_FLAGS + flags + ["-c", src, "-o", obj],
+                           capture_output=True, text=True)
+        if r.returncode != 0:
+            raise RuntimeError(f"nvcc failed on {src}:\n{r.stdout}\n{r.stderr}")
+        return obj
+
+    with cf.ThreadPoolExecutor(max_workers=min(len(srcs), os.cpu_count() or 4)) as ex:
+        objs = list(ex.map(compile_one, srcs))
+    tmp = out + ".tmp"
+    r = subprocess.run([nvcc] + ARCH + ["-shared", "-o", tmp] + objs, capture_output=True,
+                       text=True)
+    if r.returncode != 0:
+        raise RuntimeError(f"link failed:\n{r.stdout}\n{r.stderr}")
+    os.replace(tmp, out)
+    with open(stamp, "w") as f:
+        f.write(fp)
+    return out
+
+
 if __name__ == "__main__":
     print(build(verbose="-v" in sys.argv, force="-f" in sys.argv))

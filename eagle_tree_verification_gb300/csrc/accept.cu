@@ -218,14 +218,15 @@ struct RoundSlot {
 };
 
 // One pass over this thread's slice entries.  UPD: the rejection update of
-// token t_rej -- q <- fp32(W(max(0, q - p))) * rz (when the residual sum is
-// positive), and in NO_REPLACE mode p <- fp32(W(p)) * rsp with t_rej's entry
-// zeroed.  SUMS (on the updated values): the residual weight sum, the draft
+// token t_rej -- q <- fp32(W(max(0, q - p))) / zf (when the residual sum is
+// positive), and in NO_REPLACE mode p <- fp32(W(p)) / spf with t_rej's entry
+// zeroed; zf and spf are the weight sums rounded to fp32, and each quotient
+// is one IEEE division (round to nearest).  SUMS (on the updated values): the residual weight sum, the draft
 // weight sum without t_next, and q, p at t_next into `slot`.  One pass per
 // rejection round, the same operations as an update followed by the sums.
 template <int E, bool UPD, bool SUMS>
 __device__ __forceinline__ void walk_pass(float (&q)[E], float (&p)[E], int v0, int nv,
-                                          bool no_replace, int t_rej, float rz, float rsp,
+                                          bool no_replace, int t_rej, float zf, float spf,
                                           bool z_pos, int t_next, unsigned long long& sw,
                                           unsigned long long& sp, RoundSlot& slot) {
   const int tid = threadIdx.x;
@@ -234,8 +235,8 @@ __device__ __forceinline__ void walk_pass(float (&q)[E], float (&p)[E], int v0, 
     const int i = tid + e * kStochThreads;
     if (UPD) {
       const float qa = q[e], pa = p[e];
-      if (z_pos) q[e] = __fmul_rn(fixed40_f(fmaxf(0.f, __fsub_rn(qa, pa))), rz);
-      if (no_replace) p[e] = (v0 + i == t_rej) ? 0.f : __fmul_rn(fixed40_f(pa), rsp);
+      if (z_pos) q[e] = __fdiv_rn(fixed40_f(fmaxf(0.f, __fsub_rn(qa, pa))), zf);
+      if (no_replace) p[e] = (v0 + i == t_rej) ? 0.f : (spf > 0.f ? __fdiv_rn(fixed40_f(pa), spf) : 0.f);
     }
     if (SUMS) {
       sw += fixed40_int(fmaxf(0.f, __fsub_rn(q[e], p[e])));
@@ -438,20 +439,20 @@ accept_stochastic_kernel(const StochParams P) {
         moved = true;
         break;
       }
-      // rejected: q_{k+1} = fp32(W) * rn(1/fp32(Z)), p_{k+1} likewise
+      // rejected: q_{k+1} = fp32(W) / fp32(Z), p_{k+1} likewise
       // (NO_REPLACE); every operation rounds to nearest once
-      const float rz = (Z > 0ull) ? __frcp_rn(__ull2float_rn(Z)) : 0.f;
-      const float rsp = (SP > 0ull) ? __frcp_rn(__ull2float_rn(SP)) : 0.f;
+      const float zf = (Z > 0ull) ? __ull2float_rn(Z) : 0.f;
+      const float spf = (SP > 0ull) ? __ull2float_rn(SP) : 0.f;
       if (j + 1 < nk) {
         // update, and the next child's sums, in one pass
         unsigned long long sw = 0, sp = 0;
         const int tn = s_tok[s_kids[j + 1]];
-        walk_pass<E, true, true>(q, p, v0, nv, no_replace, t, rz, rsp, Z > 0ull, tn, sw, sp,
+        walk_pass<E, true, true>(q, p, v0, nv, no_replace, t, zf, spf, Z > 0ull, tn, sw, sp,
                                  s_slot[par]);
         reduce_round(sw, sp, tn);
       } else {
         unsigned long long sw = 0, sp = 0;
-        walk_pass<E, true, false>(q, p, v0, nv, no_replace, t, rz, rsp, Z > 0ull, -1, sw, sp,
+        walk_pass<E, true, false>(q, p, v0, nv, no_replace, t, zf, spf, Z > 0ull, -1, sw, sp,
                                   s_slot[par]);
       }
     }
@@ -592,12 +593,15 @@ eagle_status launch_stochastic(bool logits, int B, int max_nodes, int V, int R, 
        accept_stochastic_kernel<16, true>, accept_stochastic_kernel<32, true>}};
   const int ai = elems == 4 ? 0 : elems == 8 ? 1 : elems == 16 ? 2 : 3;
   const Kern kern = kerns[logits ? 1 : 0][ai];
-  static bool attr_done[2][4] = {};
-  if (!attr_done[logits ? 1 : 0][ai]) {
-    cudaFuncSetAttribute(kern, cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
-    cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, 160 * 1024);
-    attr_done[logits ? 1 : 0][ai] = true;
-  }
+  static PerDeviceOnce attr_once[2][4];
+  if (attr_once[logits ? 1 : 0][ai].run([&] {
+        const cudaError_t e =
+            cudaFuncSetAttribute(kern, cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
+        if (e != cudaSuccess) return e;
+        return cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                    160 * 1024);
+      }) != cudaSuccess)
+    return EAGLE_ERR_CUDA;
   StochParams P;
   P.max_nodes = max_nodes;
   P.V = V;

@@ -5,6 +5,7 @@
 #include <cuda_bf16.h>
 #include <stdint.h>
 
+#include <mutex>
 #include <utility>
 
 #include "../../include/eagle.h"
@@ -112,5 +113,38 @@ inline eagle_status launch_status(cudaError_t e) {
 }
 
 inline int ceil_div(long long a, long long b) { return (int)((a + b - 1) / b); }
+
+// Device ordinals for which host code keeps per-device state (kernel
+// attributes, occupancy answers, resolved symbol addresses).
+constexpr int kMaxDevices = 64;
+
+// Host-side set-up that must run once on every device a process uses
+// (function attributes such as the dynamic shared-memory limit apply to the
+// device that is current when they are set).  run(f) calls f() the first
+// time it is reached with a given device current, and again later only if
+// that call failed.  Thread-safe.
+struct PerDeviceOnce {
+  std::mutex mu;
+  bool done[kMaxDevices] = {};
+  template <typename F>
+  cudaError_t run(F&& f) {
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices)
+      return cudaErrorInvalidDevice;
+    std::lock_guard<std::mutex> lock(mu);
+    if (done[dev]) return cudaSuccess;
+    const cudaError_t e = f();
+    if (e == cudaSuccess) done[dev] = true;
+    return e;
+  }
+};
+
+// The current device's ordinal (0 if it cannot be read or is out of range
+// of kMaxDevices, in which case callers' per-device caches use slot 0).
+inline int current_device_slot() {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return 0;
+  return dev;
+}
 
 }  // namespace eagle

@@ -924,17 +924,20 @@ extern "C" eagle_status eagle_draft_expand(int B, int V, int k, int depth, int l
   void (*kern)(const LevelParams) = (cp.vec == 1)   ? expand_level_kernel<1>
                                     : (cp.vec == 2) ? expand_level_kernel<2>
                                                     : expand_level_kernel<4>;
-  static bool carveout = false;
-  if (!carveout) {
-    // the whole unified L1 as shared memory wherever an expand CTA lands
-    // first, so that the LM head running beside the expand still fits
-    for (auto k : {expand_level_kernel<1>, expand_level_kernel<2>, expand_level_kernel<4>})
-      cudaFuncSetAttribute(k, cudaFuncAttributePreferredSharedMemoryCarveout,
-                           cudaSharedmemCarveoutMaxShared);
-    cudaFuncSetAttribute(expand_level_stream_kernel, cudaFuncAttributePreferredSharedMemoryCarveout,
-                         cudaSharedmemCarveoutMaxShared);
-    carveout = true;
-  }
+  static PerDeviceOnce carveout_once;
+  // the whole unified L1 as shared memory wherever an expand CTA lands
+  // first, so that the LM head running beside the expand still fits
+  if (carveout_once.run([] {
+        for (auto k : {expand_level_kernel<1>, expand_level_kernel<2>, expand_level_kernel<4>}) {
+          const cudaError_t e = cudaFuncSetAttribute(
+              k, cudaFuncAttributePreferredSharedMemoryCarveout, cudaSharedmemCarveoutMaxShared);
+          if (e != cudaSuccess) return e;
+        }
+        return cudaFuncSetAttribute(expand_level_stream_kernel,
+                                    cudaFuncAttributePreferredSharedMemoryCarveout,
+                                    cudaSharedmemCarveoutMaxShared);
+      }) != cudaSuccess)
+    return EAGLE_ERR_CUDA;
   // levels beyond one wave even at the largest chunks stream through
   // persistent CTAs (no finalize fusion there)
   const long long total_chunks = (long long)B * A.F * A.S;
@@ -942,14 +945,13 @@ extern "C" eagle_status eagle_draft_expand(int B, int V, int k, int depth, int l
   if (stream_it) {
     A.fused = false;
     A.fin = F;
-    static bool attr = false;
-    if (!attr) {
-      if (cudaFuncSetAttribute(expand_level_stream_kernel,
-                               cudaFuncAttributeMaxDynamicSharedMemorySize,
-                               (int)kStreamSmem) != cudaSuccess)
-        return EAGLE_ERR_CUDA;
-      attr = true;
-    }
+    static PerDeviceOnce attr_once;
+    if (attr_once.run([] {
+          return cudaFuncSetAttribute(expand_level_stream_kernel,
+                                      cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                      (int)kStreamSmem);
+        }) != cudaSuccess)
+      return EAGLE_ERR_CUDA;
     const int grid = (int)std::min<long long>(total_chunks, kOneWave);
     const eagle_status st =
         launch_status(launch_pdl(expand_level_stream_kernel, dim3(grid), dim3(kLvThreads),

@@ -250,7 +250,12 @@ constexpr int kBK = 64;           // bf16 per 128-byte swizzled row (one chunk)
 constexpr int kUnit = 32;         // vocabulary rows per TMA box
 constexpr int kBlkMax = 256;      // vocabulary rows per MMA (its N), at most
 constexpr int kTileRows = 128;    // tree rows per CTA (the MMA's M)
-constexpr int kMaxCluster = 4;    // row tiles sharing one W stream
+// Row tiles sharing one W stream: at most a portable cluster of 8 (a
+// build-time option, so that other cluster caps can be measured).
+#ifndef EAGLE_LMHEAD_MAX_CLUSTER
+#define EAGLE_LMHEAD_MAX_CLUSTER 8
+#endif
+constexpr int kMaxCluster = EAGLE_LMHEAD_MAX_CLUSTER;
 constexpr int kMaxHStages = 4;
 constexpr int kMaxWStages = 12;
 constexpr size_t kSmemLimit = 227 * 1024;
@@ -639,19 +644,32 @@ bool make_map_bf16(CUtensorMap* map, const void* ptr, int rows, int cols, int bo
 }
 
 int sm_count() {
-  static int n = 0;
-  if (!n) {
-    int dev = 0;
-    cudaGetDevice(&dev);
-    cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev);
-    if (n <= 0) n = 148;
+  static int n[kMaxDevices] = {};
+  const int dev = current_device_slot();
+  if (!n[dev]) {
+    int c = 0;
+    int d = 0;
+    cudaGetDevice(&d);
+    if (cudaDeviceGetAttribute(&c, cudaDevAttrMultiProcessorCount, d) != cudaSuccess || c <= 0)
+      c = 148;
+    n[dev] = c;
   }
-  return n;
+  return n[dev];
 }
 
-// Clusters of C tensor-core CTAs that fit on the GPU at once (0: none).
+// Clusters of C tensor-core CTAs that fit on the current GPU at once (0:
+// none), per device and shared-memory size.
 int max_clusters(int C, size_t smem) {
-  static int cached[kMaxCluster + 1] = {};
+  static std::mutex mu;
+  static int cached_all[kMaxDevices][kMaxCluster + 1] = {};
+  static size_t cached_smem[kMaxDevices][kMaxCluster + 1] = {};
+  std::lock_guard<std::mutex> lock(mu);
+  const int dev = current_device_slot();
+  int* cached = cached_all[dev];
+  if (cached_smem[dev][C] != smem) {
+    cached[C] = 0;
+    cached_smem[dev][C] = smem;
+  }
   if (!cached[C]) {
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3((unsigned)(C * 64));
@@ -735,42 +753,56 @@ extern "C" eagle_status eagle_lmhead_softmax(eagle_dtype dtype, int T, int H, in
   if (tc_ok) {
     CUtensorMap map_w;
     if (!make_map_bf16(&map_w, d_w, V, H, kUnit)) return EAGLE_ERR_CUDA;
-    static bool attr = false;
-    if (!attr) {
-      // the whole unified L1 as shared memory, so that a CTA of the
-      // concurrently running tree expand fits beside this one
-      if (cudaFuncSetAttribute(lmhead_tc_kernel<false>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                               (int)kSmemLimit) != cudaSuccess ||
-          cudaFuncSetAttribute(lmhead_tc_kernel<true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                               (int)kSmemLimit) != cudaSuccess ||
-          cudaFuncSetAttribute(lmhead_tc_kernel<false>,
-                               cudaFuncAttributePreferredSharedMemoryCarveout,
-                               cudaSharedmemCarveoutMaxShared) != cudaSuccess)
-        return EAGLE_ERR_CUDA;
-      attr = true;
-    }
+    static PerDeviceOnce attr_once;
+    // the whole unified L1 as shared memory, so that a CTA of the
+    // concurrently running tree expand fits beside this one
+    if (attr_once.run([] {
+          cudaError_t e = cudaFuncSetAttribute(lmhead_tc_kernel<false>,
+                                               cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                               (int)kSmemLimit);
+          if (e == cudaSuccess)
+            e = cudaFuncSetAttribute(lmhead_tc_kernel<true>,
+                                     cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kSmemLimit);
+          if (e == cudaSuccess)
+            e = cudaFuncSetAttribute(lmhead_tc_kernel<false>,
+                                     cudaFuncAttributePreferredSharedMemoryCarveout,
+                                     cudaSharedmemCarveoutMaxShared);
+          return e;
+        }) != cudaSuccess)
+      return EAGLE_ERR_CUDA;
     const int n_units = (V + kUnit - 1) / kUnit;
-    // row tiles of 128 per launch: one CTA each, sharing the W stream
+    // Row tiles of 128, one CTA each; the tiles of one launch form clusters
+    // that share the W stream.  As few launches as the largest resident
+    // cluster allows, with the tiles spread evenly over them (every CTA of
+    // a launch holds real rows), so W is streamed once per launch.
     const int tiles = (T + kTileRows - 1) / kTileRows;
-    int C = std::min(kMaxCluster, tiles);
-    int slices = 0;
-    if (C > 1) {
-      slices = std::min(max_clusters(C, tc_layout(kTileRows).smem), n_units);
-      if (slices < 1) C = 1;   // clusters of C cannot be resident: one tile per launch
+    int passes = 1, C = tiles;
+    while (C > 1 && (C > kMaxCluster || max_clusters(C, tc_layout(kTileRows).smem) < 1)) {
+      ++passes;
+      C = (tiles + passes - 1) / passes;
     }
-    // one tile: leave a few SMs to the attention, which the step runs while
-    // the LM head is still streaming W (it does not fit beside an LM head CTA)
-    if (C == 1) slices = std::min(std::max(1, sm_count() - kSmsForOthers), n_units);
-    for (int r0 = 0; r0 < T; r0 += C * kTileRows) {
-      const int Ts = std::min(C * kTileRows, T - r0);
-      const TcLayout TL = tc_layout((C > 1 || Ts > kTileRows) ? kTileRows : ((Ts + 7) / 8) * 8);
+    // one slice per resident cluster of C CTAs; one tile: leave a few SMs to
+    // the attention, which the step runs while the LM head is still
+    // streaming W (it does not fit beside an LM head CTA)
+    const int slices =
+        (C > 1) ? std::min(max_clusters(C, tc_layout(kTileRows).smem), n_units)
+                : std::min(std::max(1, sm_count() - kSmsForOthers), n_units);
+    for (int p = 0, tile0 = 0; p < passes; ++p) {
+      const int nt = std::min(C, tiles - tile0);    // tiles of this launch
+      const int r0 = tile0 * kTileRows;
+      const int Ts = std::min(nt * kTileRows, T - r0);
+      tile0 += nt;
+      const int Cp = (C > 1) ? nt : 1;
+      const TcLayout TL = tc_layout((Cp > 1 || Ts > kTileRows) ? kTileRows : ((Ts + 7) / 8) * 8);
       const __nv_bfloat16* hs = static_cast<const __nv_bfloat16*>(d_h) + (size_t)r0 * H;
       CUtensorMap map_h;
       if (!make_map_bf16(&map_h, hs, Ts, H, TL.h_rows)) return EAGLE_ERR_CUDA;
-      if (launch_tc(C, dim3(slices * C), TL.smem, s, map_h, map_w, Ts, H, V, temperature,
+      // a last launch with fewer tiles keeps the slice count of the others
+      // (its clusters are smaller, so they are resident too)
+      if (launch_tc(Cp, dim3(slices * Cp), TL.smem, s, map_h, map_w, Ts, H, V, temperature,
                     z ? z + (size_t)r0 * V : nullptr, part + (size_t)r0 * slices, n_units,
-                    TL.h_stage_bytes, TL.h_stages, TL.blk, TL.w_stages, C, d_status) !=
-                        cudaSuccess)
+                    TL.h_stage_bytes, TL.h_stages, TL.blk, TL.w_stages, Cp, d_status) !=
+          cudaSuccess)
         return EAGLE_ERR_CUDA;
     }
     dim3 fgrid(T, q_norm ? (V + kFinChunk - 1) / kFinChunk : 1);
@@ -803,12 +835,9 @@ extern "C" eagle_status eagle_lmhead_softmax(eagle_dtype dtype, int T, int H, in
 // device memory instead of a caller-provided workspace.  Every GPU that
 // loads the library holds this array until the process exits.
 // ---------------------------------------------------------------------------
-#include <mutex>
-
 namespace {
 
 constexpr size_t kNoAllocScratchBytes = (size_t)16 << 20;  // 16 MiB
-constexpr int kMaxDevices = 64;
 
 static __device__ __align__(256) unsigned char g_lmhead_scratch[kNoAllocScratchBytes];
 

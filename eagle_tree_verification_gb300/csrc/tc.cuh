@@ -47,12 +47,20 @@ __device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, uint32_t parity) {
   return ok != 0;
 }
 
+// Budget of a pipeline wait, in SM cycles (about 2 s at 2 GHz).  A build
+// made only for testing the time-out path defines a tiny budget here; the
+// waits that let copies in flight land before a CTA exits pass their own
+// budget and are not affected by it.
+#ifndef EAGLE_WAIT_CYCLES
+#define EAGLE_WAIT_CYCLES 4000000000ll
+#endif
+
 // Wait for the phase with the given parity to complete, for at most about
 // `max_cycles` SM cycles.  On time-out the shared abort flag is raised and
 // the device status records EAGLE_ERR_TIMEOUT; the caller then stops
 // waiting for anything else.  Returns false if the wait did not succeed.
 __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, volatile int* abort_flag,
-                                          int* status, long long max_cycles = 4000000000ll) {
+                                          int* status, long long max_cycles = EAGLE_WAIT_CYCLES) {
   if (*abort_flag) return false;
   if (mbar_try_wait(bar, parity)) return true;
   const long long t0 = clock64();

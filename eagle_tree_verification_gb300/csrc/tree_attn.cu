@@ -792,10 +792,12 @@ bool make_map_3d(CUtensorMap* map, const void* ptr, int rows, int heads, int box
 // Largest cluster size <= kMaxSplit such that `tiles` clusters of the
 // attention kernel are resident at once (one wave), per device.
 int split_cap_for(int tiles) {
-  static int cache[64][kMaxSplit + 1];
-  static bool filled[64];
+  static std::mutex mu;
+  static int cache[kMaxDevices][kMaxSplit + 1];
+  static bool filled[kMaxDevices];
   int dev = 0;
-  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return 1;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return 1;
+  std::lock_guard<std::mutex> lock(mu);
   if (!filled[dev]) {
     for (int nc = 1; nc <= kMaxSplit; ++nc) {
       cudaLaunchConfig_t cfg = {};
@@ -870,13 +872,12 @@ extern "C" eagle_status eagle_tree_attn(eagle_dtype dtype, int B, int T, int Hq,
   const uintptr_t align = (uintptr_t)d_q | (uintptr_t)d_k_tree | (uintptr_t)d_v_tree |
                           (uintptr_t)d_k_cache | (uintptr_t)d_v_cache | (uintptr_t)d_out;
   if (tc_shape_ok(dtype, Hq, Hkv, D) && (align & 15) == 0) {
-    static bool attr = false;
-    if (!attr) {
-      if (cudaFuncSetAttribute(tree_attn_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                               (int)kAttSmem) != cudaSuccess)
-        return EAGLE_ERR_CUDA;
-      attr = true;
-    }
+    static PerDeviceOnce attr_once;
+    if (attr_once.run([] {
+          return cudaFuncSetAttribute(tree_attn_tc_kernel,
+                                      cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kAttSmem);
+        }) != cudaSuccess)
+      return EAGLE_ERR_CUDA;
     const int G = Hq / Hkv;
     const int tiles = B * Hkv * ((max_nodes * G + 127) / 128);
     const AttPlan P = att_plan(B, Hq, Hkv, max_nodes, max_kv, split_cap_for(tiles));

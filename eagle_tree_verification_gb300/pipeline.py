@@ -243,9 +243,9 @@ class TreeVerifyStep:
         if self.s.k:
             n += self.s.depth                    # one per level, finalize fused
         n += 1                                   # attention
-        if self.s.dtype == "bf16":               # LM head: one pass per cluster of
-            tiles = (self.s.T + 127) // 128      # up to four 128-row tiles
-            n += (tiles + min(4, tiles) - 1) // min(4, tiles) + 1   # ... + finalize
+        if self.s.dtype == "bf16":               # LM head: one launch per cluster of
+            tiles = (self.s.T + 127) // 128      # up to eight 128-row tiles
+            n += (tiles + 7) // 8 + 1            # ... + finalize
         else:
             n += 2                               # LM head tiles + finalize
         n += 1                                   # acceptance

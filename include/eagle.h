@@ -226,10 +226,10 @@ EAGLE_API eagle_status eagle_accept_greedy(int B, int max_nodes, const int32_t *
  * each child c (ascending index, token t):
  *   accept iff (double)u_accept[c] * p_k[t] < (double)q_k[t];
  *   on reject:  W_j = trunc(max(0, q_k[j]-p_k[j]) * 2^40), Z = sum W (exact),
- *               q_{k+1}[j] = float(W_j) * rn(1 / float(Z))  (kept as q_k if
- *               Z == 0);
+ *               q_{k+1}[j] = float(W_j) / float(Z), one IEEE fp32 division
+ *               (kept as q_k if Z == 0);
  *               NO_REPLACE: P_j = trunc(p_k[j]*2^40), P_t = 0,
- *               p_{k+1}[j] = float(P_j) * rn(1 / float(sum P)) (0 if the sum is 0);
+ *               p_{k+1}[j] = float(P_j) / float(sum P) (0 if the sum is 0);
  *               REPLACE: p_{k+1} = p_k.
  * When every child is rejected, or cur is a leaf, the bonus token is drawn
  * from q_final by inverse CDF over trunc(q*2^40): target =

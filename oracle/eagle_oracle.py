@@ -40,19 +40,18 @@ its reason, in the design notes):
       - test:    accept child c (token t) iff u_accept[c] * p_k[t] < q_k[t],
                  evaluated exactly (fp32 x fp32 is exact in fp64);
       - reject:  r = max(0, q_k - p_k) (fp32), W = trunc(r * 2^40) (integer),
-                 Z = sum W (exact), q_{k+1} = fp32(W) * rn(1 / fp32(Z));
-                 Z == 0 keeps q_{k+1} = q_k;
+                 Z = sum W (exact), q_{k+1} = fp32(W) / fp32(Z), the plain fp32
+                 quotient; Z == 0 keeps q_{k+1} = q_k;
       - p update, NO_REPLACE (siblings drawn without replacement): P =
                  trunc(p_k * 2^40) with the rejected token's entry zeroed,
-                 p_{k+1} = fp32(P) * rn(1 / fp32(sum P))  (all zero if the sum
-                 is 0);
+                 p_{k+1} = fp32(P) / fp32(sum P)  (all zero if the sum is 0);
                  REPLACE (siblings drawn i.i.d.): p_{k+1} = p_k;
       - stop:    sample from q_final by inverse CDF over W = trunc(q*2^40):
                  U = trunc(u_sample*2^24), target = (U*Z) >> 24, token =
                  smallest j whose inclusive prefix sum exceeds target.
     Mass below 2^-40 per token is dropped (at most V*2^-40 in total).  Every
-    operation rounds to nearest once (rn), so the result is reproducible bit
-    for bit; the normalised value is within 1.5 ulp of fp32(W) / fp32(Z).
+    operation rounds to nearest once (IEEE), so the result is reproducible
+    bit for bit on any IEEE machine.
   * EAGLE-2 expand/rerank: a node's value is its cumulative draft log-prob
     (the log of the product of draft confidences along its path).  Level d:
     every frontier node takes the top-k tokens of its draft row (value
@@ -125,7 +124,8 @@ def _check_tree(parent_local):
 # a1: tree attention
 # --------------------------------------------------------------------------
 def tree_attn(q, k_tree, v_tree, k_cache, v_cache, kv_off, tree_off, parent,
-              scale: Optional[float] = None, nodes: Optional[Sequence[int]] = None):
+              scale: Optional[float] = None, nodes: Optional[Sequence[int]] = None,
+              with_abs: bool = False):
     """Tree-masked attention of every draft-tree node over [KV cache | its
     ancestors and itself].
 
@@ -137,6 +137,9 @@ def tree_attn(q, k_tree, v_tree, k_cache, v_cache, kv_off, tree_off, parent,
     q [T,Hq,D], k_tree/v_tree [T,Hkv,D], k_cache/v_cache [sum L,Hkv,D],
     kv_off/tree_off [B+1], parent [T] (local per sequence, -1 at the root).
     Returns O [T,Hq,D] float64 (rows outside `nodes`, if given, stay zero).
+    With `with_abs`, also returns A [T,Hq,D] = sum_j p_j |v_j| with the same
+    softmax weights p: the magnitude of the terms each output element sums,
+    which is the scale its rounding error is measured against.
     """
     q = np.asarray(q, dtype=np.float64)
     kt = np.asarray(k_tree, dtype=np.float64)
@@ -150,6 +153,7 @@ def tree_attn(q, k_tree, v_tree, k_cache, v_cache, kv_off, tree_off, parent,
     G = Hq // Hkv
     s = (1.0 / np.sqrt(D)) if scale is None else float(scale)
     out = np.zeros((T, Hq, D), dtype=np.float64)
+    absout = np.zeros((T, Hq, D), dtype=np.float64) if with_abs else None
     B = len(tree_off) - 1
     want = None if nodes is None else set(int(n) for n in nodes)
     for b in range(B):
@@ -169,7 +173,10 @@ def tree_attn(q, k_tree, v_tree, k_cache, v_cache, kv_off, tree_off, parent,
             w = np.exp(sc)
             o = np.einsum("kgn,nkd->kgd", w, vals) / w.sum(axis=2)[..., None]
             out[t0 + i] = o.reshape(Hq, D)
-    return out
+            if with_abs:
+                a = np.einsum("kgn,nkd->kgd", w, np.abs(vals)) / w.sum(axis=2)[..., None]
+                absout[t0 + i] = a.reshape(Hq, D)
+    return (out, absout) if with_abs else out
 
 
 def causal_attn(q_seq, k_seq, v_seq, n_prefix: int, scale: Optional[float] = None):
@@ -318,12 +325,13 @@ def _fixed40(x: np.ndarray) -> np.ndarray:
 
 
 def _normalise(Wint: np.ndarray, Z: int) -> np.ndarray:
-    """fp32(W) * (1 / fp32(Z)): the conversions, the reciprocal and the
-    product each round to nearest once.  W <= 2^40 < 2^53, so W -> fp64 is
-    exact and fp64 -> fp32 rounds once."""
+    """The renormalised weights W / Z as the plain fp32 quotient
+    fp32(W) / fp32(Z): each operand rounded to nearest once, then one IEEE
+    division (round to nearest).  W <= 2^40 < 2^53, so W -> fp64 is exact
+    and fp64 -> fp32 rounds once."""
     wf = Wint.astype(np.float64).astype(np.float32)
-    rz = np.float32(np.float32(1.0) / f32_of_int(Z))
-    return (wf * rz).astype(np.float32)
+    zf = f32_of_int(Z)
+    return (wf / zf).astype(np.float32)
 
 
 def _check_row(x: np.ndarray, what: str):

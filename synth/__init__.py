@@ -135,6 +135,14 @@ def workloads() -> Dict[str, Workload]:
             name="llama3_70b", dtype="bf16", B=1, Hq=64, Hkv=8, D=128, H=8192,
             V=128256, L=(4096,), tree="eagle2", k=8, depth=8, budget=(64,),
             modes=("greedy", "stochastic"), temperature=1.0, seed=3),
+        # small bf16 case for the start-up check: three sequences (157 tree
+        # rows, so the LM head takes its two-tile cluster path), GQA 32/8,
+        # a ragged vocabulary, EAGLE-2 trees; greedy and stochastic.
+        "smoke_bf16": Workload(
+            name="smoke_bf16", dtype="bf16", B=3, Hq=32, Hkv=8, D=128, H=1024,
+            V=4099, L=(512, 300, 700), tree="eagle2", k=8, depth=8,
+            budget=(64, 40, 50), modes=("greedy", "stochastic"), temperature=0.8,
+            seed=7),
         # batched LLaMA-3-8B shaped layer: 16 sequences, L ~ U[512,16384],
         # budget ~ U[32,64], depth 8, top-8, stochastic at T=0.7; seed 5.
         "llama3_8b_batch16": Workload(

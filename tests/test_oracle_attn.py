@@ -143,3 +143,29 @@ def test_sibling_subtrees_do_not_see_each_other():
         in_subtree = victim in O.tree_path(parent, i)
         same = np.allclose(out[i], base[i], rtol=0, atol=0)
         assert same != in_subtree
+
+
+def test_abs_scale_is_the_weighted_mean_of_absolute_values():
+    # the error scale of an output element, sum_j p_j |v_j|: the same
+    # softmax weights applied to |v| (closed form on a star tree), never
+    # below |out| (triangle inequality), and equal to out where every v >= 0
+    g = np.random.default_rng(5)
+    Hq = Hkv = 1
+    D, L, N = 8, 4, 5
+    parent = np.array([-1] + [0] * (N - 1), dtype=np.int32)
+    q = g.standard_normal((N, Hq, D))
+    kt, vt = g.standard_normal((N, Hkv, D)), g.standard_normal((N, Hkv, D))
+    kc, vc = g.standard_normal((L, Hkv, D)), g.standard_normal((L, Hkv, D))
+    out, ab = O.tree_attn(q, kt, vt, kc, vc, [0, L], [0, N], parent, with_abs=True)
+    for i in range(1, N):
+        keys = np.concatenate([kc[:, 0], kt[[0, i], 0]])
+        vals = np.concatenate([vc[:, 0], vt[[0, i], 0]])
+        s = keys @ q[i, 0] / np.sqrt(D)
+        w = np.exp(s - s.max())
+        np.testing.assert_allclose(ab[i, 0], w @ np.abs(vals) / w.sum(), rtol=1e-12)
+    assert np.all(ab >= np.abs(out) - 1e-15)
+    pos_out, pos_ab = O.tree_attn(q, kt, np.abs(vt), kc, np.abs(vc), [0, L], [0, N], parent,
+                                  with_abs=True)
+    np.testing.assert_allclose(pos_ab, pos_out, rtol=1e-14)
+    # the plain output is unchanged by asking for the scale
+    np.testing.assert_array_equal(out, O.tree_attn(q, kt, vt, kc, vc, [0, L], [0, N], parent))
