@@ -82,6 +82,7 @@ __all__ = [
     "tree_path", "tree_children", "tree_depths", "tree_attn", "causal_attn",
     "lmhead_softmax", "accept_greedy", "accept_stochastic",
     "expand_level", "expand_finalize", "build_eagle2_tree", "f32_of_int",
+    "static_template_full", "build_static_tree",
 ]
 
 
@@ -540,6 +541,85 @@ def expand_finalize(pools: List[_Pool], budget: Sequence[int],
     return {"tree_off": tree_off, "parent": cat(0, np.int32), "tokens": cat(1, np.int32),
             "depth": cat(2, np.int32), "score": cat(3, np.float32),
             "p_row_of_node": cat(4, np.int32)}
+
+
+def static_template_full(K: int, m: int):
+    """The full static top-K tree of m draft steps: every node of depth < m
+    has K children, its K most probable draft tokens ([S4000] "EAGLE的创新点"
+    item 1: keep top tokens at every step; K^m root-to-leaf paths).
+    Returns (parent, rank, row) lists in level order: node i's token is the
+    rank[i]-th most probable token of the distribution its parent was
+    expanded with, and row[i] is the draft row that node i itself is expanded
+    with (-1 for a leaf); expanded nodes take rows 0, 1, ... in node order."""
+    parent, rank, row = [-1], [0], []
+    level = [0]
+    for _ in range(m):
+        nxt = []
+        for p in level:
+            for r in range(K):
+                parent.append(p)
+                rank.append(r)
+                nxt.append(len(parent) - 1)
+        level = nxt
+    has_kids = set(parent[1:])
+    n_rows = 0
+    for i in range(len(parent)):
+        if i in has_kids:
+            row.append(n_rows)
+            n_rows += 1
+        else:
+            row.append(-1)
+    return parent, rank, row
+
+
+def build_static_tree(draft_logp, B: int, tmpl_parent, tmpl_rank, tmpl_row, root_token):
+    """EAGLE-1 static draft tree ([EAGLE-2] §2, the fixed top-k tree that the
+    dynamic tree replaces; [S4000] "EAGLE的创新点" item 1).
+
+    The tree's shape is a fixed template, the same for every sequence and
+    step: template node i (i >= 1) is the tmpl_rank[i]-th most probable token
+    (value descending, token ascending) of the draft row its parent
+    tmpl_parent[i] was expanded with, row tmpl_row[parent] of the sequence's
+    draft_logp [B, R, V].  Its score is fp32(parent score + logp), the same
+    cumulative log-prob as the dynamic tree's.  Nodes keep the template's
+    numbering (parent before child).  Returns the arrays of
+    expand_finalize."""
+    lp = np.asarray(draft_logp, dtype=np.float32)
+    R, V = lp.shape[-2], lp.shape[-1]
+    lp = lp.reshape(B, R, V)
+    n = len(tmpl_parent)
+    _check_tree(tmpl_parent)
+    par, tok, dep, sc, prow = [], [], [], [], []
+    for b in range(B):
+        order = {}
+        t = [int(root_token[b])] + [0] * (n - 1)
+        d = [0] * n
+        s = [np.float32(0)] * n
+        pr = [-1] * n
+        for i in range(1, n):
+            p = int(tmpl_parent[i])
+            r = int(tmpl_row[p])
+            if not (0 <= r < R):
+                raise ValueError("an expanded template node has no draft row")
+            if r not in order:
+                order[r] = _topk_tokens(lp[b, r], V)
+            k = int(tmpl_rank[i])
+            if not (0 <= k < V):
+                raise ValueError("template rank outside the vocabulary")
+            t[i] = int(order[r][k])
+            d[i] = d[p] + 1
+            s[i] = np.float32(np.float32(s[p]) + lp[b, r, t[i]])
+            pr[i] = b * R + r
+        par.append([int(x) for x in tmpl_parent])
+        tok.append(t)
+        dep.append(d)
+        sc.append(s)
+        prow.append(pr)
+    tree_off = np.arange(B + 1, dtype=np.int32) * n
+    cat = lambda xs, dt: np.concatenate([np.asarray(x, dtype=dt) for x in xs])
+    return {"tree_off": tree_off, "parent": cat(par, np.int32), "tokens": cat(tok, np.int32),
+            "depth": cat(dep, np.int32), "score": cat(sc, np.float32),
+            "p_row_of_node": cat(prow, np.int32)}
 
 
 def build_eagle2_tree(draft_logp, B: int, k: int, depth: int, budget, root_token):
