@@ -21,7 +21,7 @@ __all__ = [
     "SAMPLE_NO_REPLACE", "eagle_tree_attn", "eagle_tree_attn_workspace_bytes",
     "eagle_lmhead_softmax", "eagle_lmhead_workspace_bytes", "eagle_accept_greedy",
     "eagle_accept_stochastic", "eagle_accept_stochastic_logits", "eagle_draft_expand",
-    "eagle_draft_pool_bytes",
+    "eagle_draft_pool_bytes", "eagle_draft_static",
     "eagle_lmhead_softmax_noalloc", "eagle_lmhead_noalloc_max_scratch_bytes",
 ]
 
@@ -61,6 +61,7 @@ _SIGS = {
     "eagle_lmhead_noalloc_max_scratch_bytes": ([], _sz),
     "eagle_lmhead_softmax_noalloc": ([_i, _i, _i, _i, _f, _i] + [_p] * 9, _i),
     "eagle_draft_expand": ([_i] * 6 + [_p] * 4 + [_sz] + [_p] * 8, _i),
+    "eagle_draft_static": ([_i] * 5 + [_p] * 12 + [_p], _i),
 }
 
 
@@ -304,3 +305,26 @@ def eagle_draft_expand(pool, status, *, B: int, V: int, k: int, depth: int, leve
           _ptr(draft_logp), _ptr(budget), _ptr(root_token), _ptr(pool),
           pool.numel() * pool.element_size(), _ptr(tree_off), _ptr(parent), _ptr(tokens),
           _ptr(node_depth), _ptr(score), _ptr(p_row_of_node), _ptr(status), _stream(stream))
+
+
+def eagle_draft_static(tmpl_parent, tmpl_rank, tmpl_row, draft_logp, root_token, tree_off,
+                       parent, tokens, node_depth, score, p_row_of_node, status, *,
+                       max_rank: int, stream=None) -> None:
+    """EAGLE-1 static tree from a fixed template (int32 device tensors of N
+    entries); draft_logp [B, R, V] fp32; outputs [B*N] (tree_off [B+1])."""
+    torch = _torch()
+    B, R, V = draft_logp.shape
+    N = tmpl_parent.numel()
+    for name, t in (("tmpl_parent", tmpl_parent), ("tmpl_rank", tmpl_rank),
+                    ("tmpl_row", tmpl_row), ("root_token", root_token), ("tree_off", tree_off),
+                    ("parent", parent), ("tokens", tokens), ("node_depth", node_depth),
+                    ("p_row_of_node", p_row_of_node)):
+        _need(t, torch.int32, name)
+    _need(draft_logp, torch.float32, "draft_logp")
+    _need(score, torch.float32, "score")
+    if parent.numel() < B * N or tree_off.numel() < B + 1:
+        raise ValueError("tree outputs must hold B*N nodes")
+    _call("eagle_draft_static", B, V, N, R, int(max_rank), _ptr(tmpl_parent), _ptr(tmpl_rank),
+          _ptr(tmpl_row), _ptr(draft_logp), _ptr(root_token), _ptr(tree_off), _ptr(parent),
+          _ptr(tokens), _ptr(node_depth), _ptr(score), _ptr(p_row_of_node), _ptr(status),
+          _stream(stream))

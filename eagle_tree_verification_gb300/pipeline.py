@@ -1,7 +1,8 @@
 """One tree-verify step on the GPU: device buffers + the launch sequence.
 
-    draft tree   eagle_draft_expand (levels 0..depth-1, then finalize)
-                 -- or a caller-given tree (parent/tokens/p_row_of_node)
+    draft tree   eagle_draft_expand (levels 0..depth-1, then finalize), or
+                 eagle_draft_static (EAGLE-1's fixed template), or a
+                 caller-given tree (parent/tokens/p_row_of_node)
     attention    eagle_tree_attn
     LM head      eagle_lmhead_softmax (greedy: no [T,V] output; stochastic:
                  writes the logits)
@@ -20,8 +21,9 @@ import dataclasses
 from typing import Dict, Optional, Sequence
 
 from . import (SAMPLE_NO_REPLACE, eagle_accept_greedy, eagle_accept_stochastic,
-               eagle_accept_stochastic_logits, eagle_draft_expand, eagle_draft_pool_bytes, eagle_lmhead_softmax,
-               eagle_lmhead_workspace_bytes, eagle_tree_attn, eagle_tree_attn_workspace_bytes)
+               eagle_accept_stochastic_logits, eagle_draft_expand, eagle_draft_pool_bytes,
+               eagle_draft_static, eagle_lmhead_softmax, eagle_lmhead_workspace_bytes,
+               eagle_tree_attn, eagle_tree_attn_workspace_bytes)
 
 
 @dataclasses.dataclass
@@ -44,6 +46,12 @@ class StepShape:
     k: int = 0
     depth: int = 0
     budget: Sequence[int] = ()
+    # EAGLE-1 static tree: template (parent, rank, row) lists; k must be 0
+    static: tuple = ()
+
+    @property
+    def builds_tree(self) -> bool:
+        return bool(self.k) or bool(self.static)
 
     @property
     def T(self) -> int:
@@ -75,6 +83,8 @@ class TreeVerifyStep:
         if s.k:
             spec += [("draft_logp", (max(s.rows, 1), s.V), f32), ("budget", (s.B,), i32),
                      ("root_token", (s.B,), i32)]
+        elif s.static:
+            spec += [("draft_logp", (max(s.rows, 1), s.V), f32), ("root_token", (s.B,), i32)]
         else:
             spec += [("tree_off", (s.B + 1,), i32), ("parent", (T,), i32),
                      ("tokens", (T,), i32), ("p_row_of_node", (T,), i32)]
@@ -100,12 +110,18 @@ class TreeVerifyStep:
         self.w_lm = z(s.V, s.H, dtype=dt)
         if s.mode != "stochastic":
             self.p_rows = z(max(s.rows, 1), s.V)
-        if not s.k:
+        if not s.builds_tree:
             self.draft_logp = None
-            self.budget = z(s.B, dtype=i32)
             self.root_token = z(s.B, dtype=i32)
+        if not s.k:
+            self.budget = z(s.B, dtype=i32)
+        self.tmpl = None
+        if s.static:
+            par, rank, row = s.static
+            self.tmpl = [torch.tensor(list(a), dtype=i32, device=dev) for a in (par, rank, row)]
+            self.tmpl_max_rank = int(max(list(rank)[1:] or [0])) + 1
         # tree (written by the expand kernels, or loaded)
-        if s.k:
+        if s.builds_tree:
             self.tree_off = z(s.B + 1, dtype=i32)
             self.parent = z(T, dtype=i32)
             self.tokens = z(T, dtype=i32)
@@ -167,6 +183,13 @@ class TreeVerifyStep:
     # ------------------------------------------------------------------
     def run_expand(self, stream=None) -> None:
         s = self.s
+        if s.static:
+            R = self.draft_logp.shape[0] // s.B
+            eagle_draft_static(*self.tmpl, self.draft_logp.view(s.B, R, s.V), self.root_token,
+                               self.tree_off, self.parent, self.tokens, self.node_depth,
+                               self.score, self.p_row_of_node, self.status,
+                               max_rank=self.tmpl_max_rank, stream=stream)
+            return
         for lev in range(s.depth - 1):
             eagle_draft_expand(self.pool, self.status, B=s.B, V=s.V, k=s.k, depth=s.depth,
                                level=lev, draft_logp=self.draft_logp, stream=stream)
@@ -231,7 +254,7 @@ class TreeVerifyStep:
         side = self._side
         side.wait_stream(main)
         self.run_lmhead(side)
-        if self.s.k and build_tree:
+        if self.s.builds_tree and build_tree:
             self.run_expand(main)
         self.run_attn(main)
         main.wait_stream(side)
@@ -242,6 +265,8 @@ class TreeVerifyStep:
         n = 0
         if self.s.k:
             n += self.s.depth                    # one per level, finalize fused
+        elif self.s.static:
+            n += 2 if len(self.s.static[0]) > 1 else 1   # ranks + finish
         n += 1                                   # attention
         if self.s.dtype == "bf16":               # LM head: one launch per cluster of
             tiles = (self.s.T + 127) // 128      # up to eight 128-row tiles

@@ -3,6 +3,7 @@
  * (sm_103a).  One verify step is:
  *
  *   eagle_draft_expand   (every level, then finalize) -> draft tree
+ *                        (or eagle_draft_static: EAGLE-1's fixed template)
  *   eagle_tree_attn      tree-masked attention of every tree node
  *   eagle_lmhead_softmax LM-head logits, softmax statistics, argmax (and q)
  *   eagle_accept_greedy  | eagle_accept_stochastic(_logits) -> accepted tokens
@@ -320,6 +321,40 @@ EAGLE_API eagle_status eagle_draft_expand(int B, int V, int k, int depth, int le
                                 int32_t *d_tree_off, int32_t *d_parent, int32_t *d_tokens,
                                 int32_t *d_node_depth, float *d_score,
                                 int32_t *d_p_row_of_node, int *d_status,
+                                eagle_stream_t stream);
+
+/* ------------------------------------------------------------------------
+ * eagle_draft_static -- EAGLE-1 static draft tree from a fixed template.
+ * [EAGLE-2] §2 "EAGLE-2 的核心創新：動態草稿樹" (EAGLE-1's fixed top-k tree,
+ * which the dynamic tree replaces); [S4000] "EAGLE的创新点" item 1 (the draft
+ * keeps the top tokens at every step: K^m candidate paths for K per step
+ * over m steps).
+ *
+ * The template (N nodes, root first, parents before children) is the same
+ * for every sequence: node i >= 1 is the d_tmpl_rank[i]-th most probable
+ * token (log-prob descending, token ascending) of the draft row that its
+ * parent p = d_tmpl_parent[i] was expanded with, row d_tmpl_row[p] of the
+ * sequence's rows.  Its score is fp32(score[p] + logp), as in
+ * eagle_draft_expand.  Outputs use the template's numbering:
+ *   d_tree_off [B+1] (= b*N), d_parent [B*N] (= the template), d_tokens
+ *   (root: d_root_token[b]), d_node_depth, d_score (root 0),
+ *   d_p_row_of_node (global row b*R + d_tmpl_row[p]; root -1).
+ *
+ * N          template nodes, 1 .. EAGLE_MAX_TREE_NODES.
+ * R          draft rows per sequence: d_draft_logp is [B, R, V] fp32.
+ * max_rank   every d_tmpl_rank[i] < max_rank <= min(EAGLE_MAX_TOPK, V).
+ * d_tmpl_parent, d_tmpl_rank, d_tmpl_row [N] int32 (device); d_tmpl_row[i]
+ *            is -1 (or anything) for a node without children.
+ * Device errors: INVALID_TREE (template parents not topological),
+ * INVALID_ARG (rank >= max_rank, an expanded node without a valid row),
+ * NUMERIC (non-finite log-prob in a row that is read).
+ * ---------------------------------------------------------------------- */
+EAGLE_API eagle_status eagle_draft_static(int B, int V, int N, int R, int max_rank,
+                                const int32_t *d_tmpl_parent, const int32_t *d_tmpl_rank,
+                                const int32_t *d_tmpl_row, const float *d_draft_logp,
+                                const int32_t *d_root_token, int32_t *d_tree_off,
+                                int32_t *d_parent, int32_t *d_tokens, int32_t *d_node_depth,
+                                float *d_score, int32_t *d_p_row_of_node, int *d_status,
                                 eagle_stream_t stream);
 
 #ifdef __cplusplus

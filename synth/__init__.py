@@ -43,9 +43,10 @@ class Workload:
     H: int                     # hidden size (LM-head input width)
     V: int                     # vocabulary
     L: tuple                   # KV-cache length per sequence
-    tree: str                  # "levels" (random tree of given level sizes) or "eagle2"
-    k: int = 0                 # EAGLE-2 top-k per expanded node
-    depth: int = 0             # EAGLE-2 expansion levels
+    tree: str                  # "levels" (random tree of given level sizes), "eagle2"
+                               # (dynamic tree) or "static" (full K-ary template)
+    k: int = 0                 # EAGLE-2 top-k per expanded node; static: K children
+    depth: int = 0             # EAGLE-2 expansion levels; static: draft steps m
     budget: tuple = ()         # EAGLE-2 draft-token budget per sequence
     level_sizes: tuple = ()    # random-tree level sizes (root level first)
     modes: tuple = ("greedy",)
@@ -60,6 +61,8 @@ class Workload:
         """Tree nodes per sequence, root included."""
         if self.tree == "levels":
             return [int(sum(self.level_sizes))] * self.B
+        if self.tree == "static":
+            return [sum(self.k ** i for i in range(self.depth + 1))] * self.B
         pool = self.pool_size
         return [min(int(b), pool) + 1 for b in self.budget]
 
@@ -79,6 +82,8 @@ class Workload:
         were drafted from)."""
         if self.tree == "eagle2":
             return 1 + (self.depth - 1) * self.k
+        if self.tree == "static":
+            return sum(self.k ** i for i in range(self.depth))
         return int(sum(self.level_sizes))
 
     @property
@@ -87,9 +92,30 @@ class Workload:
 
     @property
     def max_depth(self) -> int:
-        if self.tree == "eagle2":
+        if self.tree in ("eagle2", "static"):
             return self.depth
         return len(self.level_sizes) - 1
+
+    def static_template(self):
+        """The fixed tree shape of a "static" workload, as input structure:
+        (parent, rank, row) lists in level order -- every node above the
+        last level has k children of ranks 0..k-1, and the expanded nodes
+        use draft rows 0, 1, ... in node order (leaves: -1)."""
+        parent, rank = [-1], [0]
+        level = [0]
+        for _ in range(self.depth):
+            nxt = []
+            for p in level:
+                for r in range(self.k):
+                    parent.append(p)
+                    rank.append(r)
+                    nxt.append(len(parent) - 1)
+            level = nxt
+        expanded = sorted(set(parent[1:]))
+        row = [-1] * len(parent)
+        for i, node in enumerate(expanded):
+            row[node] = i
+        return parent, rank, row
 
     def scaled(self, **kw) -> "Workload":
         return dataclasses.replace(self, **kw)
@@ -143,6 +169,12 @@ def workloads() -> Dict[str, Workload]:
             V=4099, L=(512, 300, 700), tree="eagle2", k=8, depth=8,
             budget=(64, 40, 50), modes=("greedy", "stochastic"), temperature=0.8,
             seed=7),
+        # Vicuna-7B shaped layer verifying an EAGLE-1 static tree: the full
+        # 4-ary template of 3 draft steps (85 nodes, 64 root-to-leaf paths).
+        "vicuna7b_static": Workload(
+            name="vicuna7b_static", dtype="bf16", B=1, Hq=32, Hkv=32, D=128, H=4096,
+            V=32000, L=(2048,), tree="static", k=4, depth=3,
+            modes=("greedy", "stochastic"), seed=11),
         # batched LLaMA-3-8B shaped layer: 16 sequences, L ~ U[512,16384],
         # budget ~ U[32,64], depth 8, top-8, stochastic at T=0.7; seed 5.
         "llama3_8b_batch16": Workload(
@@ -279,6 +311,11 @@ def make_inputs(w: Workload, parts=("attn", "lmhead", "draft", "accept"),
                 np.where(par >= 0, par + b * R, -1).astype(np.int32)
                 for b, par in enumerate(parents)])
             out["p_row_of_node"] = prow
+        elif w.tree == "static":
+            par, rank, row = w.static_template()
+            out["tmpl_parent"] = np.array(par, dtype=np.int32)
+            out["tmpl_rank"] = np.array(rank, dtype=np.int32)
+            out["tmpl_row"] = np.array(row, dtype=np.int32)
         else:
             out["budget"] = np.array(w.budget, dtype=np.int32)
     if "accept" in parts:

@@ -22,6 +22,8 @@ def step_shape(w: synth.Workload, mode: str, **over):
               dtype=w.dtype, mode=mode, temperature=w.temperature)
     if w.tree == "eagle2":
         kw.update(k=w.k, depth=w.depth, budget=list(w.budget))
+    elif w.tree == "static":
+        kw.update(static=w.static_template())
     kw.update(over)
     return StepShape(**kw)
 
@@ -34,6 +36,8 @@ def load_step(step, w: synth.Workload, inp):
     if w.tree == "eagle2":
         arrs["draft_logp"] = inp["draft_logp"]
         arrs["budget"] = inp["budget"]
+    elif w.tree == "static":
+        arrs["draft_logp"] = inp["draft_logp"]
     else:
         arrs["tree_off"] = inp["tree_off"]
         arrs["parent"] = inp["parent"]

@@ -25,7 +25,7 @@ def _declared():
 
 def test_every_declared_symbol_is_exported(E):
     names = _declared()
-    assert len(names) == 13
+    assert len(names) == 14
     lib = ctypes.CDLL(E.LIB_PATH)
     for n in names:
         assert hasattr(lib, n), n
@@ -80,8 +80,14 @@ def test_host_argument_checks_return_before_any_device_work(E):
     fake = ctypes.c_void_p(256)         # never dereferenced: the call returns first
     assert L.eagle_draft_expand(1, 100, 4, 3, 0, 0, null, null, null, fake, 16,
                                 *([null] * 6), fake, null) == 7
+    # static tree: more template nodes than allowed, a rank set above the
+    # top-k limit, missing pointers
+    assert L.eagle_draft_static(1, 100, 257, 4, 2, *([null] * 12), null) == 3
+    assert L.eagle_draft_static(1, 100, 7, 4, 33, *([null] * 12), null) == 3
+    assert L.eagle_draft_static(1, 100, 7, 4, 2, *([null] * 12), null) == 1
     # empty batches are no-ops
     assert L.eagle_accept_greedy(0, 8, *([null] * 4), 3, *([null] * 5)) == 0
+    assert L.eagle_draft_static(0, 100, 7, 4, 2, *([null] * 12), null) == 0
 
 
 def test_product_path_does_not_reach_the_oracle():

@@ -34,6 +34,9 @@ def _oracle_tree(w, inp):
     if w.tree == "eagle2":
         return O.build_eagle2_tree(inp["draft_logp"], B=w.B, k=w.k, depth=w.depth,
                                    budget=inp["budget"], root_token=inp["root_token"])
+    if w.tree == "static":
+        return O.build_static_tree(inp["draft_logp"], w.B, inp["tmpl_parent"], inp["tmpl_rank"],
+                                   inp["tmpl_row"], inp["root_token"])
     return {"tree_off": inp["tree_off"], "parent": inp["parent"], "tokens": inp["tokens"],
             "p_row_of_node": inp["p_row_of_node"]}
 
