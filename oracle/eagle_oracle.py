@@ -80,6 +80,7 @@ MODE_NO_REPLACE = 1
 __all__ = [
     "FRAC_BITS", "MODE_REPLACE", "MODE_NO_REPLACE", "OracleNumericError",
     "tree_path", "tree_children", "tree_depths", "tree_attn", "causal_attn",
+    "gather_pages", "tree_attn_paged",
     "lmhead_softmax", "accept_greedy", "accept_stochastic",
     "expand_level", "expand_finalize", "build_eagle2_tree", "f32_of_int",
     "static_template_full", "build_static_tree",
@@ -178,6 +179,41 @@ def tree_attn(q, k_tree, v_tree, k_cache, v_cache, kv_off, tree_off, parent,
                 a = np.einsum("kgn,nkd->kgd", w, np.abs(vals)) / w.sum(axis=2)[..., None]
                 absout[t0 + i] = a.reshape(Hq, D)
     return (out, absout) if with_abs else out
+
+
+def gather_pages(pages, block_table, kv_len):
+    """A paged KV cache read back as the packed cache of tree_attn: sequence
+    b's keys are its first kv_len[b] positions, position p sitting at row
+    p % page_size of page block_table[b][p // page_size] of the pool
+    pages [n_pages, page_size, Hkv, D].  Returns (packed [sum L, Hkv, D],
+    kv_off [B+1])."""
+    pages = np.asarray(pages)
+    P = pages.shape[1]
+    rows, off = [], [0]
+    for b, L in enumerate(kv_len):
+        L = int(L)
+        for p in range(L):
+            page = int(block_table[b][p // P])
+            if not (0 <= page < pages.shape[0]):
+                raise ValueError("block table names a page outside the pool")
+            rows.append(pages[page, p % P])
+        off.append(off[-1] + L)
+    packed = (np.stack(rows) if rows
+              else np.zeros((0,) + pages.shape[2:], dtype=pages.dtype))
+    return packed, np.asarray(off, dtype=np.int64)
+
+
+def tree_attn_paged(q, k_tree, v_tree, k_pages, v_pages, block_table, kv_len, tree_off,
+                    parent, scale: Optional[float] = None,
+                    nodes: Optional[Sequence[int]] = None, with_abs: bool = False):
+    """tree_attn over a paged KV cache: the same attention, with each
+    sequence's cached keys and values read through its block table
+    (gather_pages).  Paging changes where the cache is stored, not what is
+    computed."""
+    kc, kv_off = gather_pages(k_pages, block_table, kv_len)
+    vc, _ = gather_pages(v_pages, block_table, kv_len)
+    return tree_attn(q, k_tree, v_tree, kc, vc, kv_off, tree_off, parent, scale=scale,
+                     nodes=nodes, with_abs=with_abs)
 
 
 def causal_attn(q_seq, k_seq, v_seq, n_prefix: int, scale: Optional[float] = None):

@@ -169,3 +169,42 @@ def test_abs_scale_is_the_weighted_mean_of_absolute_values():
     np.testing.assert_allclose(pos_ab, pos_out, rtol=1e-14)
     # the plain output is unchanged by asking for the scale
     np.testing.assert_array_equal(out, O.tree_attn(q, kt, vt, kc, vc, [0, L], [0, N], parent))
+
+
+def test_paged_cache_reads_the_same_keys_as_the_packed_cache():
+    # scatter each sequence's packed cache over shuffled pages of a pool
+    # (page size 4, partial last pages, an empty sequence, unused pool
+    # pages): attention over the paged cache equals attention over the packed
+    # one exactly, and gathering the pages gives back the packed rows
+    g = np.random.default_rng(12)
+    Hq, Hkv, D, P = 4, 2, 8, 4
+    Ls = [9, 0, 4, 13]
+    q, kt, vt, kc, vc, kv_off, tree_off, parent = _case(4, Ls, (1, 3, 2), Hq, Hkv, D, 31)
+    n_pages = sum((L + P - 1) // P for L in Ls) + 3
+    perm = g.permutation(n_pages)
+    kp = g.standard_normal((n_pages, P, Hkv, D))
+    vp = g.standard_normal((n_pages, P, Hkv, D))
+    max_pages = max((L + P - 1) // P for L in Ls)
+    table = np.full((4, max_pages), -1)
+    nxt = 0
+    for b, L in enumerate(Ls):
+        for j in range((L + P - 1) // P):
+            page = perm[nxt]
+            nxt += 1
+            table[b, j] = page
+            for r in range(P):
+                pos = j * P + r
+                if pos < L:
+                    kp[page, r] = kc[kv_off[b] + pos]
+                    vp[page, r] = vc[kv_off[b] + pos]
+    packed, off = O.gather_pages(kp, table, Ls)
+    np.testing.assert_array_equal(packed, kc)
+    np.testing.assert_array_equal(off, kv_off)
+    ref = O.tree_attn(q, kt, vt, kc, vc, kv_off, tree_off, parent)
+    got = O.tree_attn_paged(q, kt, vt, kp, vp, table, Ls, tree_off, parent)
+    np.testing.assert_array_equal(got, ref)
+    # a table entry outside the pool is an error
+    bad = table.copy()
+    bad[0, 0] = n_pages
+    with pytest.raises(ValueError):
+        O.gather_pages(kp, bad, Ls)
