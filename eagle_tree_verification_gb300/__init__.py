@@ -21,7 +21,7 @@ __all__ = [
     "SAMPLE_NO_REPLACE", "eagle_tree_attn", "eagle_tree_attn_workspace_bytes",
     "eagle_lmhead_softmax", "eagle_lmhead_workspace_bytes", "eagle_accept_greedy",
     "eagle_accept_stochastic", "eagle_accept_stochastic_logits", "eagle_draft_expand",
-    "eagle_draft_pool_bytes", "eagle_draft_static",
+    "eagle_draft_pool_bytes", "eagle_draft_static", "eagle_tree_attn_paged",
     "eagle_lmhead_softmax_noalloc", "eagle_lmhead_noalloc_max_scratch_bytes",
 ]
 
@@ -62,6 +62,7 @@ _SIGS = {
     "eagle_lmhead_softmax_noalloc": ([_i, _i, _i, _i, _f, _i] + [_p] * 9, _i),
     "eagle_draft_expand": ([_i] * 6 + [_p] * 4 + [_sz] + [_p] * 8, _i),
     "eagle_draft_static": ([_i] * 5 + [_p] * 12 + [_p], _i),
+    "eagle_tree_attn_paged": ([_i] * 6 + [_f] + [_i] * 5 + [_p] * 12, _i),
 }
 
 
@@ -328,3 +329,31 @@ def eagle_draft_static(tmpl_parent, tmpl_rank, tmpl_row, draft_logp, root_token,
           _ptr(tmpl_row), _ptr(draft_logp), _ptr(root_token), _ptr(tree_off), _ptr(parent),
           _ptr(tokens), _ptr(node_depth), _ptr(score), _ptr(p_row_of_node), _ptr(status),
           _stream(stream))
+
+
+def eagle_tree_attn_paged(q, k_tree, v_tree, k_pages, v_pages, block_table, kv_len, tree_off,
+                          parent, out, status, *, max_nodes: int, max_kv: int,
+                          scale: Optional[float] = None, stream=None) -> None:
+    """Tree attention over a paged KV cache; see eagle_tree_attn_paged in
+    include/eagle.h.  k_pages/v_pages [n_pages, page_size, Hkv, D];
+    block_table [B, max_pages] int32; kv_len [B] int32."""
+    torch = _torch()
+    T, Hq, D = q.shape
+    Hkv = k_tree.shape[1]
+    B = tree_off.numel() - 1
+    n_pages, page_size = k_pages.shape[0], k_pages.shape[1]
+    max_pages = block_table.shape[1] if block_table.dim() == 2 else 0
+    for name, t in (("k_tree", k_tree), ("v_tree", v_tree), ("k_pages", k_pages),
+                    ("v_pages", v_pages)):
+        _need(t, q.dtype, name)
+    for name, t in (("block_table", block_table), ("kv_len", kv_len), ("tree_off", tree_off),
+                    ("parent", parent)):
+        _need(t, torch.int32, name)
+    _need(out, torch.float32, "out")
+    if block_table.shape[0] != B or kv_len.numel() != B:
+        raise ValueError("block_table and kv_len need one row / entry per sequence")
+    sc = (1.0 / D ** 0.5) if scale is None else float(scale)
+    _call("eagle_tree_attn_paged", _dtype_code(q), B, T, Hq, Hkv, D, sc, max_nodes, max_kv,
+          page_size, n_pages, max_pages, _ptr(q), _ptr(k_tree), _ptr(v_tree), _ptr(k_pages),
+          _ptr(v_pages), _ptr(block_table), _ptr(kv_len), _ptr(tree_off), _ptr(parent), _ptr(out),
+          _ptr(status), _stream(stream))

@@ -38,12 +38,22 @@ namespace {
 
 constexpr int kWarpsPerBlock = 4;
 
+// Where the cache keys of a sequence live: contiguous rows kv_off[b] ..
+// kv_off[b+1]-1, or (page_size > 0) pages of a pool named by a block table,
+// with the sequence's length in kv_len[b].
+struct CacheIndex {
+  const int* kv_off;
+  const int* kv_len;
+  const int* block_table;
+  int page_size, max_pages, n_pages;
+};
+
 template <typename TIn, int D>
 __global__ void __launch_bounds__(kWarpsPerBlock * 32)
 tree_attn_warp_kernel(int B, int T, int Hq, int Hkv, float scale, int max_nodes, int max_kv,
                       const TIn* __restrict__ q, const TIn* __restrict__ k_tree,
                       const TIn* __restrict__ v_tree, const TIn* __restrict__ k_cache,
-                      const TIn* __restrict__ v_cache, const int* __restrict__ kv_off,
+                      const TIn* __restrict__ v_cache, const CacheIndex ci,
                       const int* __restrict__ tree_off, const int* __restrict__ parent,
                       float* __restrict__ out, int* status) {
   pdl_begin();
@@ -62,7 +72,9 @@ tree_attn_warp_kernel(int B, int T, int Hq, int Hkv, float scale, int max_nodes,
   }
   const int b = lo;
   const int t0 = tree_off[b], n = tree_off[b + 1] - t0;
-  const int c0 = kv_off[b], L = kv_off[b + 1] - c0;
+  const bool paged = ci.page_size > 0;
+  const int c0 = paged ? 0 : ci.kv_off[b];
+  const int L = paged ? ci.kv_len[b] : ci.kv_off[b + 1] - c0;
   if (n > max_nodes || L > max_kv || L < 0) {
     if (lane == 0) fail(status, EAGLE_ERR_INVALID_TREE);
     return;
@@ -90,7 +102,16 @@ tree_attn_warp_kernel(int B, int T, int Hq, int Hkv, float scale, int max_nodes,
     m = mn;
   };
   for (int j = 0; j < L; ++j) {
-    const size_t off = ((size_t)(c0 + j) * Hkv + g) * D;
+    int row = c0 + j;
+    if (paged) {
+      int page = ci.block_table[(size_t)b * ci.max_pages + j / ci.page_size];
+      if (page < 0 || page >= ci.n_pages) {
+        if (lane == 0) fail(status, EAGLE_ERR_INVALID_ARG);
+        page = 0;
+      }
+      row = page * ci.page_size + j % ci.page_size;
+    }
+    const size_t off = ((size_t)row * Hkv + g) * D;
     visit(k_cache + off, v_cache + off);
   }
   // ancestors and the node itself, following parent[] (order is irrelevant)
@@ -115,8 +136,9 @@ tree_attn_warp_kernel(int B, int T, int Hq, int Hkv, float scale, int max_nodes,
 template <typename TIn>
 eagle_status launch_warp(int D, int B, int T, int Hq, int Hkv, float scale, int max_nodes,
                          int max_kv, const void* q, const void* kt, const void* vt,
-                         const void* kc, const void* vc, const int* kv_off, const int* tree_off,
-                         const int* parent, float* out, int* status, cudaStream_t s) {
+                         const void* kc, const void* vc, const CacheIndex& ci,
+                         const int* tree_off, const int* parent, float* out, int* status,
+                         cudaStream_t s) {
   const int warps = T * Hq;
   const int grid = (warps + kWarpsPerBlock - 1) / kWarpsPerBlock;
   const TIn* Q = static_cast<const TIn*>(q);
@@ -126,7 +148,7 @@ eagle_status launch_warp(int D, int B, int T, int Hq, int Hkv, float scale, int 
   const TIn* VC = static_cast<const TIn*>(vc);
   auto kern = (D == 64) ? tree_attn_warp_kernel<TIn, 64> : tree_attn_warp_kernel<TIn, 128>;
   return launch_status(launch_pdl(kern, dim3(grid), dim3(kWarpsPerBlock * 32), 0, s, B, T, Hq,
-                                  Hkv, scale, max_nodes, max_kv, Q, KT, VT, KC, VC, kv_off,
+                                  Hkv, scale, max_nodes, max_kv, Q, KT, VT, KC, VC, ci,
                                   tree_off, parent, out, status));
 }
 
@@ -187,7 +209,13 @@ AttPlan att_plan(int B, int Hq, int Hkv, int max_nodes, int max_kv, int split_ca
 struct AttParams {
   int B, Hq, Hkv, G, MT, NC, CK, max_nodes, max_kv;
   float scale_log2;
-  const int* kv_off;
+  const int* kv_off;       // contiguous cache: rows kv_off[b] .. kv_off[b+1]-1
+  // paged cache (page_size > 0): sequence b's key pos lives in row
+  // block_table[b * max_pages + pos / page_size] * page_size + pos % page_size
+  // of the page pool; its length is kv_len[b]
+  int page_size, max_pages, n_pages;
+  const int* block_table;
+  const int* kv_len;
   const int* tree_off;
   const int* parent;
   float* out;
@@ -294,11 +322,15 @@ tree_attn_tc_kernel(const __grid_constant__ CUtensorMap map_q,
   const int g = (tile / A.MT) % A.Hkv;
   const int b = tile / (A.MT * A.Hkv);
 
-  // The KV cache and its offsets are resident state that no earlier kernel
-  // of the step writes: the first cache blocks are requested before waiting
-  // for the previous kernel (the tree and the queries come after the wait).
-  const int kv0 = A.kv_off[b];
-  const int L = A.kv_off[b + 1] - kv0;
+  // A contiguous KV cache and its offsets are resident state that the
+  // kernel queued just before this one does not write: the first cache
+  // blocks are requested before waiting for it (the tree and the queries
+  // come after the wait).  A paged cache is read only after the wait (a
+  // commit of accepted tokens may have just written its pages).
+  const bool paged = A.page_size > 0;
+  if (paged) pdl_begin();
+  const int kv0 = paged ? 0 : A.kv_off[b];
+  const int L = paged ? A.kv_len[b] : A.kv_off[b + 1] - kv0;
   const bool bad_kv = (L < 0 || L > A.max_kv);
   // chunks that carry cache keys of this sequence; the last one also takes
   // the tree keys
@@ -306,10 +338,21 @@ tree_attn_tc_kernel(const __grid_constant__ CUtensorMap map_q,
   const int key_begin = c * A.CK;
   const int key_end = bad_kv ? key_begin : min(L, key_begin + A.CK);
   const int n_cache_blk = (key_end > key_begin) ? (key_end - key_begin + kKeyBlk - 1) / kKeyBlk : 0;
-  const int early = min(2, n_cache_blk);
+  const int early = paged ? 0 : min(2, n_cache_blk);
   int t0 = 0;   // set after the dependency wait
+  // row of cache key pos in the cache tensor (128 keys from a multiple of
+  // 128 never straddle a page: page sizes are multiples of 128)
+  auto cache_row = [&](int pos) -> int {
+    if (!paged) return kv0 + pos;
+    int page = A.block_table[(size_t)b * A.max_pages + pos / A.page_size];
+    if (page < 0 || page >= A.n_pages) {
+      fail(A.status, EAGLE_ERR_INVALID_ARG);
+      page = 0;
+    }
+    return page * A.page_size + pos % A.page_size;
+  };
   auto block_row = [&](int j) {   // first key row of block j in its tensor
-    return (j < n_cache_blk) ? kv0 + key_begin + j * kKeyBlk : t0 + (j - n_cache_blk) * kKeyBlk;
+    return (j < n_cache_blk) ? cache_row(key_begin + j * kKeyBlk) : t0 + (j - n_cache_blk) * kKeyBlk;
   };
   auto load_k = [&](int j) {
     const int st = j & 1;
@@ -341,7 +384,7 @@ tree_attn_tc_kernel(const __grid_constant__ CUtensorMap map_q,
       load_v(j);
     }
   }
-  pdl_begin();
+  if (!paged) pdl_begin();
 
   t0 = A.tree_off[b];
   const int n = A.tree_off[b + 1] - t0;
@@ -845,6 +888,85 @@ extern "C" size_t eagle_tree_attn_workspace_bytes(int B, int T, int Hq, int Hkv,
   return 0;
 }
 
+namespace {
+
+// Both entry points: the cache is `cache_rows` rows of [Hkv, D] in kc / vc,
+// indexed by `ci`.
+eagle_status attn_impl(eagle_dtype dtype, int B, int T, int Hq, int Hkv, int D, float scale,
+                       int max_nodes, int max_kv, int cache_rows, const void* d_q,
+                       const void* d_k_tree, const void* d_v_tree, const void* d_k_cache,
+                       const void* d_v_cache, const CacheIndex& ci, const int32_t* d_tree_off,
+                       const int32_t* d_parent, float* d_out, int* d_status, cudaStream_t s) {
+  const uintptr_t align = (uintptr_t)d_q | (uintptr_t)d_k_tree | (uintptr_t)d_v_tree |
+                          (uintptr_t)d_k_cache | (uintptr_t)d_v_cache | (uintptr_t)d_out;
+  const bool pages_ok = ci.page_size == 0 || ci.page_size % kKeyBlk == 0;
+  if (tc_shape_ok(dtype, Hq, Hkv, D) && (align & 15) == 0 && pages_ok) {
+    static PerDeviceOnce attr_once;
+    if (attr_once.run([] {
+          return cudaFuncSetAttribute(tree_attn_tc_kernel,
+                                      cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kAttSmem);
+        }) != cudaSuccess)
+      return EAGLE_ERR_CUDA;
+    const int G = Hq / Hkv;
+    const int tiles = B * Hkv * ((max_nodes * G + 127) / 128);
+    const AttPlan P = att_plan(B, Hq, Hkv, max_nodes, max_kv, split_cap_for(tiles));
+    CUtensorMap mq, mkc, mvc, mkt, mvt;
+    const void* kc = (cache_rows > 0) ? d_k_cache : d_k_tree;   // never read when empty
+    const void* vc = (cache_rows > 0) ? d_v_cache : d_v_tree;
+    const int rows_c = (cache_rows > 0) ? cache_rows : T;
+    if (!make_map_3d(&mq, d_q, T, Hq, P.G, 128 / P.G) ||
+        !make_map_3d(&mkc, kc, rows_c, Hkv, 1, kKeyBlk) ||
+        !make_map_3d(&mvc, vc, rows_c, Hkv, 1, kKeyBlk) ||
+        !make_map_3d(&mkt, d_k_tree, T, Hkv, 1, kKeyBlk) ||
+        !make_map_3d(&mvt, d_v_tree, T, Hkv, 1, kKeyBlk))
+      return EAGLE_ERR_CUDA;
+    AttParams A;
+    A.B = B;
+    A.Hq = Hq;
+    A.Hkv = Hkv;
+    A.G = P.G;
+    A.MT = P.MT;
+    A.NC = P.NC;
+    A.CK = P.CK;
+    A.max_nodes = max_nodes;
+    A.max_kv = max_kv;
+    A.scale_log2 = scale * 1.4426950408889634f;
+    A.kv_off = ci.kv_off;
+    A.page_size = ci.page_size;
+    A.max_pages = ci.max_pages;
+    A.n_pages = ci.n_pages;
+    A.block_table = ci.block_table;
+    A.kv_len = ci.kv_len;
+    A.tree_off = d_tree_off;
+    A.parent = d_parent;
+    A.out = d_out;
+    A.status = d_status;
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3((unsigned)(B * Hkv * P.MT * P.NC));
+    cfg.blockDim = dim3(kAttThreads);
+    cfg.dynamicSmemBytes = kAttSmem;
+    cfg.stream = s;
+    cudaLaunchAttribute attrs[2];
+    attrs[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attrs[0].val.programmaticStreamSerializationAllowed = 1;
+    attrs[1].id = cudaLaunchAttributeClusterDimension;
+    attrs[1].val.clusterDim.x = (unsigned)P.NC;
+    attrs[1].val.clusterDim.y = 1;
+    attrs[1].val.clusterDim.z = 1;
+    cfg.attrs = attrs;
+    cfg.numAttrs = (P.NC > 1) ? 2 : 1;
+    return launch_status(cudaLaunchKernelEx(&cfg, tree_attn_tc_kernel, mq, mkc, mvc, mkt, mvt, A));
+  }
+  if (dtype == EAGLE_BF16)
+    return launch_warp<__nv_bfloat16>(D, B, T, Hq, Hkv, scale, max_nodes, max_kv, d_q, d_k_tree,
+                                      d_v_tree, d_k_cache, d_v_cache, ci, d_tree_off, d_parent,
+                                      d_out, d_status, s);
+  return launch_warp<float>(D, B, T, Hq, Hkv, scale, max_nodes, max_kv, d_q, d_k_tree, d_v_tree,
+                            d_k_cache, d_v_cache, ci, d_tree_off, d_parent, d_out, d_status, s);
+}
+
+}  // namespace
+
 extern "C" eagle_status eagle_tree_attn(eagle_dtype dtype, int B, int T, int Hq, int Hkv, int D,
                                         float scale, int max_nodes, int max_kv, int kv_rows,
                                         const void* d_q,
@@ -868,66 +990,35 @@ extern "C" eagle_status eagle_tree_attn(eagle_dtype dtype, int B, int T, int Hq,
                    EAGLE_ERR_WORKSPACE);
   EAGLE_HOST_CHECK(kv_rows >= 0, EAGLE_ERR_INVALID_ARG);
   (void)d_ws;
-  cudaStream_t s = (cudaStream_t)stream;
-  const uintptr_t align = (uintptr_t)d_q | (uintptr_t)d_k_tree | (uintptr_t)d_v_tree |
-                          (uintptr_t)d_k_cache | (uintptr_t)d_v_cache | (uintptr_t)d_out;
-  if (tc_shape_ok(dtype, Hq, Hkv, D) && (align & 15) == 0) {
-    static PerDeviceOnce attr_once;
-    if (attr_once.run([] {
-          return cudaFuncSetAttribute(tree_attn_tc_kernel,
-                                      cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kAttSmem);
-        }) != cudaSuccess)
-      return EAGLE_ERR_CUDA;
-    const int G = Hq / Hkv;
-    const int tiles = B * Hkv * ((max_nodes * G + 127) / 128);
-    const AttPlan P = att_plan(B, Hq, Hkv, max_nodes, max_kv, split_cap_for(tiles));
-    CUtensorMap mq, mkc, mvc, mkt, mvt;
-    const void* kc = (kv_rows > 0) ? d_k_cache : d_k_tree;   // never read when empty
-    const void* vc = (kv_rows > 0) ? d_v_cache : d_v_tree;
-    const int rows_c = (kv_rows > 0) ? kv_rows : T;
-    if (!make_map_3d(&mq, d_q, T, Hq, P.G, 128 / P.G) ||
-        !make_map_3d(&mkc, kc, rows_c, Hkv, 1, kKeyBlk) ||
-        !make_map_3d(&mvc, vc, rows_c, Hkv, 1, kKeyBlk) ||
-        !make_map_3d(&mkt, d_k_tree, T, Hkv, 1, kKeyBlk) ||
-        !make_map_3d(&mvt, d_v_tree, T, Hkv, 1, kKeyBlk))
-      return EAGLE_ERR_CUDA;
-    AttParams A;
-    A.B = B;
-    A.Hq = Hq;
-    A.Hkv = Hkv;
-    A.G = P.G;
-    A.MT = P.MT;
-    A.NC = P.NC;
-    A.CK = P.CK;
-    A.max_nodes = max_nodes;
-    A.max_kv = max_kv;
-    A.scale_log2 = scale * 1.4426950408889634f;
-    A.kv_off = d_kv_off;
-    A.tree_off = d_tree_off;
-    A.parent = d_parent;
-    A.out = d_out;
-    A.status = d_status;
-    cudaLaunchConfig_t cfg = {};
-    cfg.gridDim = dim3((unsigned)(B * Hkv * P.MT * P.NC));
-    cfg.blockDim = dim3(kAttThreads);
-    cfg.dynamicSmemBytes = kAttSmem;
-    cfg.stream = s;
-    cudaLaunchAttribute attrs[2];
-    attrs[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
-    attrs[0].val.programmaticStreamSerializationAllowed = 1;
-    attrs[1].id = cudaLaunchAttributeClusterDimension;
-    attrs[1].val.clusterDim.x = (unsigned)P.NC;
-    attrs[1].val.clusterDim.y = 1;
-    attrs[1].val.clusterDim.z = 1;
-    cfg.attrs = attrs;
-    cfg.numAttrs = (P.NC > 1) ? 2 : 1;
-    return launch_status(cudaLaunchKernelEx(&cfg, tree_attn_tc_kernel, mq, mkc, mvc, mkt, mvt, A));
-  }
-  if (dtype == EAGLE_BF16)
-    return launch_warp<__nv_bfloat16>(D, B, T, Hq, Hkv, scale, max_nodes, max_kv, d_q, d_k_tree,
-                                      d_v_tree, d_k_cache, d_v_cache, d_kv_off, d_tree_off,
-                                      d_parent, d_out, d_status, s);
-  return launch_warp<float>(D, B, T, Hq, Hkv, scale, max_nodes, max_kv, d_q, d_k_tree, d_v_tree,
-                            d_k_cache, d_v_cache, d_kv_off, d_tree_off, d_parent, d_out, d_status,
-                            s);
+  CacheIndex ci = {d_kv_off, nullptr, nullptr, 0, 0, 0};
+  return attn_impl(dtype, B, T, Hq, Hkv, D, scale, max_nodes, max_kv, kv_rows, d_q, d_k_tree,
+                   d_v_tree, d_k_cache, d_v_cache, ci, d_tree_off, d_parent, d_out, d_status,
+                   (cudaStream_t)stream);
+}
+
+extern "C" eagle_status eagle_tree_attn_paged(
+    eagle_dtype dtype, int B, int T, int Hq, int Hkv, int D, float scale, int max_nodes,
+    int max_kv, int page_size, int n_pages, int max_pages, const void* d_q,
+    const void* d_k_tree, const void* d_v_tree, const void* d_k_pages, const void* d_v_pages,
+    const int32_t* d_block_table, const int32_t* d_kv_len, const int32_t* d_tree_off,
+    const int32_t* d_parent, float* d_out, int* d_status, eagle_stream_t stream) {
+  EAGLE_HOST_CHECK(B >= 1 && T >= 0 && Hq >= 1 && Hkv >= 1 && max_kv >= 0, EAGLE_ERR_INVALID_ARG);
+  EAGLE_HOST_CHECK(Hq % Hkv == 0, EAGLE_ERR_UNSUPPORTED);
+  EAGLE_HOST_CHECK(D == 64 || D == 128, EAGLE_ERR_UNSUPPORTED);
+  EAGLE_HOST_CHECK(dtype == EAGLE_F32 || dtype == EAGLE_BF16, EAGLE_ERR_UNSUPPORTED);
+  EAGLE_HOST_CHECK(max_nodes >= 1 && max_nodes <= EAGLE_MAX_TREE_NODES, EAGLE_ERR_UNSUPPORTED);
+  EAGLE_HOST_CHECK(isfinite(scale), EAGLE_ERR_INVALID_ARG);
+  EAGLE_HOST_CHECK(page_size >= 1 && n_pages >= 0 && max_pages >= 0, EAGLE_ERR_INVALID_ARG);
+  EAGLE_HOST_CHECK((long long)max_pages * page_size >= max_kv, EAGLE_ERR_INVALID_ARG);
+  EAGLE_HOST_CHECK((long long)n_pages * page_size <= 0x7fffffffll, EAGLE_ERR_UNSUPPORTED);
+  if (T == 0) return EAGLE_OK;
+  EAGLE_HOST_CHECK(d_q && d_k_tree && d_v_tree && d_kv_len && d_tree_off && d_parent && d_out &&
+                       d_status,
+                   EAGLE_ERR_INVALID_ARG);
+  EAGLE_HOST_CHECK(max_kv == 0 || (d_k_pages && d_v_pages && d_block_table && n_pages >= 1),
+                   EAGLE_ERR_INVALID_ARG);
+  CacheIndex ci = {nullptr, d_kv_len, d_block_table, page_size, max_pages, n_pages};
+  return attn_impl(dtype, B, T, Hq, Hkv, D, scale, max_nodes, max_kv,
+                   max_kv > 0 ? n_pages * page_size : 0, d_q, d_k_tree, d_v_tree, d_k_pages,
+                   d_v_pages, ci, d_tree_off, d_parent, d_out, d_status, (cudaStream_t)stream);
 }

@@ -112,6 +112,10 @@ EAGLE_API const char *eagle_version(void);
  *            initialisation.
  * Device errors: INVALID_TREE (malformed parent[] or a sequence with more
  * than max_nodes nodes or a cache longer than max_kv).
+ * Ordering: the first cache blocks are requested before the kernel waits
+ * for the kernel queued just before it on `stream` (programmatic dependent
+ * launch), so d_k_cache, d_v_cache and d_kv_off must not be written by that
+ * immediately preceding kernel (any earlier one may write them).
  * ---------------------------------------------------------------------- */
 EAGLE_API size_t eagle_tree_attn_workspace_bytes(int B, int T, int Hq, int Hkv, int D,
                                        int max_nodes, int max_kv);
@@ -123,6 +127,33 @@ EAGLE_API eagle_status eagle_tree_attn(eagle_dtype dtype, int B, int T, int Hq, 
                              const int32_t *d_parent, float *d_out,
                              void *d_ws, size_t ws_bytes, int *d_status,
                              eagle_stream_t stream);
+
+/* ------------------------------------------------------------------------
+ * eagle_tree_attn_paged -- eagle_tree_attn over a paged KV cache.
+ * Same attention as eagle_tree_attn (same sources); only where the cached
+ * keys live differs.  The cache is a pool of n_pages pages of page_size
+ * positions, d_k_pages / d_v_pages [n_pages, page_size, Hkv, D]; sequence
+ * b's cache position p is row p % page_size of page
+ * d_block_table[b * max_pages + p / page_size], and its length is
+ * d_kv_len[b] (<= max_kv <= max_pages * page_size).  Pages need not be
+ * contiguous or in order, and a sequence grows by appending pages to its
+ * table (the pages' fragmentation and batching problems named in [EAGLE-2]
+ * §4, limitations).  bf16 with D = 128 runs on the tensor cores when
+ * page_size is a multiple of 128; other page sizes and fp32 run the
+ * CUDA-core kernel.  The cache is read only after the preceding kernel on
+ * `stream` has finished, so a commit of accepted tokens may come right
+ * before this call.  No scratch is needed.
+ * Device errors: as eagle_tree_attn, plus INVALID_ARG for a table entry
+ * outside [0, n_pages).
+ * ---------------------------------------------------------------------- */
+EAGLE_API eagle_status eagle_tree_attn_paged(eagle_dtype dtype, int B, int T, int Hq, int Hkv,
+                                   int D, float scale, int max_nodes, int max_kv,
+                                   int page_size, int n_pages, int max_pages, const void *d_q,
+                                   const void *d_k_tree, const void *d_v_tree,
+                                   const void *d_k_pages, const void *d_v_pages,
+                                   const int32_t *d_block_table, const int32_t *d_kv_len,
+                                   const int32_t *d_tree_off, const int32_t *d_parent,
+                                   float *d_out, int *d_status, eagle_stream_t stream);
 
 /* ------------------------------------------------------------------------
  * eagle_lmhead_softmax -- frozen LM head over every tree node.

@@ -25,7 +25,7 @@ def _declared():
 
 def test_every_declared_symbol_is_exported(E):
     names = _declared()
-    assert len(names) == 14
+    assert len(names) == 15
     lib = ctypes.CDLL(E.LIB_PATH)
     for n in names:
         assert hasattr(lib, n), n
@@ -99,3 +99,14 @@ def test_product_path_does_not_reach_the_oracle():
                     src = fh.read()
                 assert not re.search(r"^\s*(import|from)\s+oracle", src, re.M), f
                 assert "oracle/" not in src, f
+
+
+def test_binding_argument_counts_match_the_header(E):
+    # every ctypes signature of the binding has as many arguments as the
+    # C prototype in include/eagle.h
+    with open(os.path.join(ROOT, "include", "eagle.h")) as f:
+        text = f.read()
+    for m in re.finditer(r"EAGLE_API\s+[\w\s\*]+?\b(eagle_\w+)\s*\(([^)]*)\)", text):
+        name, params = m.group(1), m.group(2).strip()
+        n = 0 if params in ("", "void") else params.count(",") + 1
+        assert len(E._SIGS[name][0]) == n, name
