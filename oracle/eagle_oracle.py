@@ -84,6 +84,8 @@ __all__ = [
     "lmhead_softmax", "accept_greedy", "accept_stochastic",
     "expand_level", "expand_finalize", "build_eagle2_tree", "f32_of_int",
     "static_template_full", "build_static_tree",
+    "bf16_round", "rmsnorm", "rope", "silu", "tree_positions", "decoder_layer",
+    "decoder_layer_causal",
 ]
 
 
@@ -239,6 +241,129 @@ def causal_attn(q_seq, k_seq, v_seq, n_prefix: int, scale: Optional[float] = Non
         e = np.exp(sc)
         out[:, h, :] = (e / e.sum(axis=1, keepdims=True)) @ v_seq[:, g, :]
     return out
+
+
+# --------------------------------------------------------------------------
+# f1: one decoder layer of the target model over the tree
+# --------------------------------------------------------------------------
+# [EAGLE] workflow paragraph and [S4000] "EAGLE的创新点" item 2: the verify
+# pass is one forward pass of the target model over all tree tokens, whose
+# attention sees the cache and each node's ancestors.  The pages name the
+# target models (Vicuna, LLaMA-2/3, Mixtral) but not their layer, so the
+# layer here is the plain reading of "a LLaMA-shaped layer": pre-norm
+# RMSNorm, Q/K/V projections, rotary position embedding on q and k, tree
+# attention, output projection plus residual, RMSNorm, SwiGLU MLP plus
+# residual.  A tree node's position is its sequence's cache length plus its
+# depth (the position it would have on its own root-to-node path).
+
+def bf16_round(x) -> np.ndarray:
+    """Round to the nearest bf16 value (ties to even), returned as float64:
+    the storage format of the layer's matrix-multiply operands."""
+    x32 = np.ascontiguousarray(np.asarray(x, dtype=np.float64)).astype(np.float32)
+    u = x32.view(np.uint32)
+    lsb = (u >> 16) & np.uint32(1)
+    r = ((u + np.uint32(0x7FFF) + lsb) & np.uint32(0xFFFF0000)).view(np.float32)
+    return r.astype(np.float64)
+
+
+def rmsnorm(x, g, eps: float):
+    """x / sqrt(mean(x^2) + eps) * g over the last axis, in fp64."""
+    x = np.asarray(x, dtype=np.float64)
+    return x / np.sqrt(np.mean(x * x, axis=-1, keepdims=True) + eps) * np.asarray(g, np.float64)
+
+
+def rope(x, pos, theta: float):
+    """Rotary position embedding of x [T, heads, D] at positions pos [T]:
+    the pair (x_j, x_{j+D/2}) is rotated by pos * theta^(-2j/D), in fp64."""
+    x = np.asarray(x, dtype=np.float64)
+    D = x.shape[-1]
+    j = np.arange(D // 2, dtype=np.float64)
+    ang = np.asarray(pos, np.float64)[:, None] * theta ** (-2.0 * j / D)     # [T, D/2]
+    c, s_ = np.cos(ang)[:, None, :], np.sin(ang)[:, None, :]
+    a, b = x[..., :D // 2], x[..., D // 2:]
+    return np.concatenate([a * c - b * s_, a * s_ + b * c], axis=-1)
+
+
+def silu(x):
+    x = np.asarray(x, dtype=np.float64)
+    return x / (1.0 + np.exp(-x))
+
+
+def tree_positions(kv_len, tree_off, parent):
+    """Position of every tree node: its sequence's cache length plus its
+    depth in the tree."""
+    pos = np.zeros(int(tree_off[-1]), dtype=np.int64)
+    for b in range(len(tree_off) - 1):
+        t0, t1 = int(tree_off[b]), int(tree_off[b + 1])
+        dep = tree_depths([int(x) for x in parent[t0:t1]])
+        pos[t0:t1] = int(kv_len[b]) + np.asarray(dep)
+    return pos
+
+
+def decoder_layer(x, wts: Dict[str, np.ndarray], k_cache, v_cache, kv_off, tree_off, parent,
+                  Hq: int, Hkv: int, theta: float, eps: float, with_abs: bool = False):
+    """One pre-norm decoder layer over every tree node.
+
+    x [T, H] residual stream in; wts: g_attn [H], wq [Hq*D, H], wk, wv
+    [Hkv*D, H], wo [H, Hq*D], g_mlp [H], wg, wu [I, H], wd [H, I] (rows are
+    output features).  k_cache / v_cache hold the cached keys (already
+    rotated at their positions) and values of each sequence.
+
+    Every value that the layer feeds to a matrix multiply or to the
+    attention is stored in bf16 (the tensor-core operand format): the normed
+    activations, q / k / v after the rotation, the attention output and the
+    gated MLP activation.  All arithmetic is fp64.  Returns a dict with the
+    output residual stream "out" [T, H] and the intermediates; with
+    `with_abs`, "out_abs" is the elementwise sum of the magnitudes of the
+    terms that make up each output (|x| + |o|·|wo| + |m|·|wd|), the scale
+    its rounding error is measured against."""
+    x = np.asarray(x, dtype=np.float64)
+    T, H = x.shape
+    D = wts["wq"].shape[0] // Hq
+    f = {k: np.asarray(v, dtype=np.float64) for k, v in wts.items()}
+    kv_len = np.diff(np.asarray(kv_off, dtype=np.int64))
+    pos = tree_positions(kv_len, tree_off, parent)
+    a = bf16_round(rmsnorm(x, f["g_attn"], eps))
+    q = bf16_round(rope((a @ f["wq"].T).reshape(T, Hq, D), pos, theta))
+    k = bf16_round(rope((a @ f["wk"].T).reshape(T, Hkv, D), pos, theta))
+    v = bf16_round((a @ f["wv"].T).reshape(T, Hkv, D))
+    o = tree_attn(q, k, v, k_cache, v_cache, kv_off, tree_off, parent)
+    ob = bf16_round(o.reshape(T, Hq * D))
+    h1 = x + ob @ f["wo"].T
+    bn = bf16_round(rmsnorm(h1, f["g_mlp"], eps))
+    gt = bn @ f["wg"].T
+    up = bn @ f["wu"].T
+    m = bf16_round(silu(gt) * up)
+    out = h1 + m @ f["wd"].T
+    res = {"out": out, "h1": h1, "q": q, "k": k, "v": v, "attn": o, "pos": pos}
+    if with_abs:
+        res["out_abs"] = np.abs(x) + np.abs(ob) @ np.abs(f["wo"]).T + np.abs(m) @ np.abs(f["wd"]).T
+    return res
+
+
+def decoder_layer_causal(x_seq, wts: Dict[str, np.ndarray], k_prefix, v_prefix, pos0: int,
+                         Hq: int, Hkv: int, theta: float, eps: float):
+    """The same layer run as an ordinary causal sequence: tokens x_seq
+    [S, H] at positions pos0 .. pos0+S-1 after a cached prefix (k_prefix,
+    v_prefix [pos0, Hkv, D]); token p attends to the prefix and tokens
+    0..p.  Independent of the tree routines (causal_attn); used to pin
+    decoder_layer.  Same bf16 storage points.  Returns out [S, H]."""
+    x = np.asarray(x_seq, dtype=np.float64)
+    S, H = x.shape
+    D = wts["wq"].shape[0] // Hq
+    f = {k: np.asarray(v, dtype=np.float64) for k, v in wts.items()}
+    pos = pos0 + np.arange(S)
+    a = bf16_round(rmsnorm(x, f["g_attn"], eps))
+    q = bf16_round(rope((a @ f["wq"].T).reshape(S, Hq, D), pos, theta))
+    k = bf16_round(rope((a @ f["wk"].T).reshape(S, Hkv, D), pos, theta))
+    v = bf16_round((a @ f["wv"].T).reshape(S, Hkv, D))
+    kk = np.concatenate([np.asarray(k_prefix, np.float64), k], axis=0)
+    vv = np.concatenate([np.asarray(v_prefix, np.float64), v], axis=0)
+    o = causal_attn(q, kk, vv, n_prefix=pos0)
+    h1 = x + bf16_round(o.reshape(S, Hq * D)) @ f["wo"].T
+    bn = bf16_round(rmsnorm(h1, f["g_mlp"], eps))
+    m = bf16_round(silu(bn @ f["wg"].T) * (bn @ f["wu"].T))
+    return h1 + m @ f["wd"].T
 
 
 # --------------------------------------------------------------------------
