@@ -22,6 +22,8 @@ __all__ = [
     "eagle_lmhead_softmax", "eagle_lmhead_workspace_bytes", "eagle_accept_greedy",
     "eagle_accept_stochastic", "eagle_accept_stochastic_logits", "eagle_draft_expand",
     "eagle_draft_pool_bytes", "eagle_draft_static", "eagle_tree_attn_paged",
+    "eagle_rmsnorm", "eagle_cast_bf16", "eagle_tree_rope_table", "eagle_gemm",
+    "EPI_STORE", "EPI_ACCUM", "EPI_SWIGLU", "EPI_QKV_ROPE",
     "eagle_lmhead_softmax_noalloc", "eagle_lmhead_noalloc_max_scratch_bytes",
 ]
 
@@ -31,6 +33,7 @@ LIB_PATH = os.path.join(HERE, "libeagle.so")
 EAGLE_F32, EAGLE_BF16 = 0, 1
 LMHEAD_GREEDY, LMHEAD_PROB, LMHEAD_LOGITS = 0, 1, 2
 SAMPLE_REPLACE, SAMPLE_NO_REPLACE = 0, 1
+EPI_STORE, EPI_ACCUM, EPI_SWIGLU, EPI_QKV_ROPE = 0, 1, 2, 3
 
 _STATUS = {0: "ok", 1: "invalid argument", 2: "invalid tree", 3: "unsupported shape",
            4: "numeric error", 5: "device wait timed out", 6: "CUDA error",
@@ -63,6 +66,10 @@ _SIGS = {
     "eagle_draft_expand": ([_i] * 6 + [_p] * 4 + [_sz] + [_p] * 8, _i),
     "eagle_draft_static": ([_i] * 5 + [_p] * 12 + [_p], _i),
     "eagle_tree_attn_paged": ([_i] * 6 + [_f] + [_i] * 5 + [_p] * 12, _i),
+    "eagle_rmsnorm": ([_i, _i, _f] + [_p] * 5, _i),
+    "eagle_cast_bf16": ([_sz, _p, _p, _p], _i),
+    "eagle_tree_rope_table": ([_i, _i, _f] + [_p] * 8, _i),
+    "eagle_gemm": ([_i] * 4 + [_p] * 9 + [_i] * 3 + [_p, _p], _i),
 }
 
 
@@ -356,4 +363,48 @@ def eagle_tree_attn_paged(q, k_tree, v_tree, k_pages, v_pages, block_table, kv_l
     _call("eagle_tree_attn_paged", _dtype_code(q), B, T, Hq, Hkv, D, sc, max_nodes, max_kv,
           page_size, n_pages, max_pages, _ptr(q), _ptr(k_tree), _ptr(v_tree), _ptr(k_pages),
           _ptr(v_pages), _ptr(block_table), _ptr(kv_len), _ptr(tree_off), _ptr(parent), _ptr(out),
+          _ptr(status), _stream(stream))
+
+
+def eagle_rmsnorm(x, gain, y, status, *, eps: float, stream=None) -> None:
+    """y [T,H] bf16 = rmsnorm(x [T,H] fp32) * gain [H] bf16."""
+    torch = _torch()
+    T, H = x.shape
+    _need(x, torch.float32, "x")
+    _need(gain, torch.bfloat16, "gain")
+    _need(y, torch.bfloat16, "y")
+    _call("eagle_rmsnorm", T, H, float(eps), _ptr(x), _ptr(gain), _ptr(y), _ptr(status),
+          _stream(stream))
+
+
+def eagle_cast_bf16(x, y, stream=None) -> None:
+    """y = bf16(x) elementwise (x fp32, y bf16, same number of elements)."""
+    torch = _torch()
+    _need(x, torch.float32, "x")
+    _need(y, torch.bfloat16, "y")
+    if x.numel() != y.numel():
+        raise ValueError("x and y differ in size")
+    _call("eagle_cast_bf16", x.numel(), _ptr(x), _ptr(y), _stream(stream))
+
+
+def eagle_tree_rope_table(tree_off, parent, pos, cos_sin, status, *, D: int, theta: float,
+                          kv_off=None, kv_len=None, stream=None) -> None:
+    """Node positions (cache length + depth) and their rotation table
+    cos_sin [T, D/2, 2] fp32; give kv_off [B+1] or kv_len [B]."""
+    B = tree_off.numel() - 1
+    _call("eagle_tree_rope_table", B, int(D), float(theta), _ptr(tree_off), _ptr(parent),
+          _ptr(kv_off), _ptr(kv_len), _ptr(pos), _ptr(cos_sin), _ptr(status), _stream(stream))
+
+
+def eagle_gemm(epilogue, a, w, status, *, y=None, accum=None, resid=None, q=None, k=None, v=None,
+               cos_sin=None, Hq: int = 0, Hkv: int = 0, D: int = 0, stream=None) -> None:
+    """Y = a [T,K] bf16 x w [N,K]^T bf16 with a layer epilogue (see
+    eagle_gemm in include/eagle.h)."""
+    torch = _torch()
+    T, K = a.shape
+    N = w.shape[0]
+    _need(a, torch.bfloat16, "a")
+    _need(w, torch.bfloat16, "w")
+    _call("eagle_gemm", int(epilogue), T, N, K, _ptr(a), _ptr(w), _ptr(y), _ptr(accum),
+          _ptr(resid), _ptr(q), _ptr(k), _ptr(v), _ptr(cos_sin), int(Hq), int(Hkv), int(D),
           _ptr(status), _stream(stream))

@@ -257,6 +257,12 @@ constexpr int kTileRows = 128;    // tree rows per CTA (the MMA's M)
 #endif
 constexpr int kMaxCluster = EAGLE_LMHEAD_MAX_CLUSTER;
 constexpr int kMaxHStages = 4;
+// h stages of a CTA that takes the whole shared memory (a build-time option,
+// so that the split between the h and W rings can be measured)
+#ifndef EAGLE_LMHEAD_BIG_HSTAGES
+#define EAGLE_LMHEAD_BIG_HSTAGES 3
+#endif
+constexpr int kBigHStages = EAGLE_LMHEAD_BIG_HSTAGES;
 constexpr int kMaxWStages = 12;
 constexpr size_t kSmemLimit = 227 * 1024;
 // A W ring within this budget (when it still holds four stages) leaves room
@@ -291,9 +297,16 @@ TcLayout tc_layout(int h_rows) {
   L.blk = kBlkMax;
   L.h_stages = kMaxHStages;
   L.w_stage_bytes = L.blk * 128;
-  const size_t fixed = 1024 + (size_t)L.h_stages * L.h_stage_bytes + kTcSharedBytes;
-  const size_t limit =
-      (fixed + 4 * (size_t)L.w_stage_bytes <= kSmemShared) ? kSmemShared : kSmemLimit;
+  size_t fixed = 1024 + (size_t)L.h_stages * L.h_stage_bytes + kTcSharedBytes;
+  size_t limit = kSmemShared;
+  if (fixed + 4 * (size_t)L.w_stage_bytes > kSmemShared) {
+    // the whole shared memory: h is re-read from L2 every block, W comes
+    // from HBM (and in a cluster only once all its CTAs released a stage),
+    // so W gets the deeper ring
+    limit = kSmemLimit;
+    L.h_stages = kBigHStages;
+    fixed = 1024 + (size_t)L.h_stages * L.h_stage_bytes + kTcSharedBytes;
+  }
   L.w_stages = (int)std::min<size_t>(kMaxWStages, (limit - fixed) / L.w_stage_bytes);
   L.smem = fixed + (size_t)L.w_stages * L.w_stage_bytes;
   return L;

@@ -65,9 +65,12 @@ static_rank_kernel(const StaticParams P) {
     s_bad = 0;
   }
   __syncthreads();
-  // children of j: the largest rank among them
+  // the template must be topological (checked by every CTA, so none reads
+  // a bad parent); children of j: the largest rank among them
   for (int i = tid; i < P.N; i += kStThreads) {
-    if (i > 0 && P.tmpl_parent[i] == j) {
+    const int p = P.tmpl_parent[i];
+    if ((i == 0) ? (p != -1) : (p < 0 || p >= i)) atomicOr(&s_bad, 2);
+    if (i > 0 && p == j) {
       const int r = P.tmpl_rank[i];
       if (r < 0 || r >= P.K) atomicOr(&s_bad, 1);
       else atomicMax(&s_k, r + 1);
@@ -75,7 +78,10 @@ static_rank_kernel(const StaticParams P) {
   }
   __syncthreads();
   if (s_bad) {
-    if (tid == 0 && b == 0) fail(P.status, EAGLE_ERR_INVALID_ARG);
+    // a template error is seen by every CTA and reported once; a bad rank
+    // by the CTA of the parent that has it
+    if (tid == 0 && b == 0 && (!(s_bad & 2) || j == 0))
+      fail(P.status, (s_bad & 2) ? EAGLE_ERR_INVALID_TREE : EAGLE_ERR_INVALID_ARG);
     return;
   }
   const int K = s_k;

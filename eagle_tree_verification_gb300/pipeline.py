@@ -20,10 +20,38 @@ from __future__ import annotations
 import dataclasses
 from typing import Dict, Optional, Sequence
 
-from . import (SAMPLE_NO_REPLACE, eagle_accept_greedy, eagle_accept_stochastic,
-               eagle_accept_stochastic_logits, eagle_draft_expand, eagle_draft_pool_bytes,
-               eagle_draft_static, eagle_lmhead_softmax, eagle_lmhead_workspace_bytes,
-               eagle_tree_attn, eagle_tree_attn_workspace_bytes)
+from . import (EPI_ACCUM, EPI_QKV_ROPE, EPI_SWIGLU, SAMPLE_NO_REPLACE, eagle_accept_greedy,
+               eagle_accept_stochastic, eagle_accept_stochastic_logits, eagle_cast_bf16,
+               eagle_draft_expand, eagle_draft_pool_bytes, eagle_draft_static, eagle_gemm,
+               eagle_lmhead_softmax, eagle_lmhead_workspace_bytes, eagle_rmsnorm,
+               eagle_tree_attn, eagle_tree_attn_workspace_bytes, eagle_tree_rope_table)
+
+
+def pack_qkv_weight(wq, wk, wv, Hq: int, Hkv: int, D: int):
+    """[Wq; Wk; Wv] in the row order eagle_gemm's QKV_ROPE epilogue reads:
+    inside every q and k head, dimension j on row 2j and dimension j + D/2 on
+    row 2j + 1 (a weight layout prepared once, when the weights are loaded)."""
+    import torch
+    half = D // 2
+    perm = torch.stack([torch.arange(half), torch.arange(half) + half], dim=1).reshape(-1)
+
+    def pair(w, heads):
+        w = w.reshape(heads, D, -1)
+        return w[:, perm.to(w.device), :].reshape(heads * D, -1)
+
+    return torch.cat([pair(wq, Hq), pair(wk, Hkv), wv], dim=0).contiguous()
+
+
+def pack_gate_up_weight(wg, wu):
+    """Gate and up projections [I, H] interleaved in groups of 16 rows (16
+    gate rows, then the 16 matching up rows), the order eagle_gemm's SWIGLU
+    epilogue reads."""
+    import torch
+    I, H = wg.shape
+    if I % 16:
+        raise ValueError("the MLP width must be a multiple of 16")
+    return torch.stack([wg.reshape(I // 16, 16, H), wu.reshape(I // 16, 16, H)],
+                       dim=1).reshape(2 * I, H).contiguous()
 
 
 @dataclasses.dataclass
@@ -48,6 +76,12 @@ class StepShape:
     budget: Sequence[int] = ()
     # EAGLE-1 static tree: template (parent, rank, row) lists; k must be 0
     static: tuple = ()
+    # the full decoder layer (RMSNorm, Q/K/V + rotary, attention, Wo,
+    # RMSNorm, SwiGLU MLP) feeds the attention and the LM head
+    layer: bool = False
+    I: int = 0
+    theta: float = 10000.0
+    eps: float = 1e-5
 
     @property
     def builds_tree(self) -> bool:
@@ -75,9 +109,12 @@ class TreeVerifyStep:
         z = lambda *shape_, dtype=f32: torch.zeros(shape_, dtype=dtype, device=dev)
         # Inputs that change every step live in one device buffer (views at
         # 256-byte offsets), so a step's inputs arrive with a single copy.
-        spec = [("q", (T, s.Hq, s.D), dt), ("k_tree", (T, s.Hkv, s.D), dt),
-                ("v_tree", (T, s.Hkv, s.D), dt), ("h", (T, s.H), dt),
-                ("u_accept", (T,), f32), ("u_sample", (T,), f32)]
+        if s.layer:
+            spec = [("x", (T, s.H), f32)]
+        else:
+            spec = [("q", (T, s.Hq, s.D), dt), ("k_tree", (T, s.Hkv, s.D), dt),
+                    ("v_tree", (T, s.Hkv, s.D), dt), ("h", (T, s.H), dt)]
+        spec += [("u_accept", (T,), f32), ("u_sample", (T,), f32)]
         if s.mode == "stochastic":
             spec.append(("p_rows", (max(s.rows, 1), s.V), f32))
         if s.k:
@@ -103,6 +140,31 @@ class TreeVerifyStep:
                 nb *= d
             nb *= torch.empty((), dtype=dty).element_size()
             setattr(self, name, self.step_inputs[off:off + nb].view(dty).view(shp))
+        if s.layer:
+            if s.dtype != "bf16":
+                raise ValueError("the full layer runs in bf16")
+            bf = torch.bfloat16
+            # the layer's outputs that the attention and the LM head read
+            self.q = z(T, s.Hq, s.D, dtype=bf)
+            self.k_tree = z(T, s.Hkv, s.D, dtype=bf)
+            self.v_tree = z(T, s.Hkv, s.D, dtype=bf)
+            self.h = z(T, s.H, dtype=bf)
+            # weights (resident) and work buffers
+            qd = s.Hq * s.D
+            self.g_attn = z(s.H, dtype=bf)
+            self.g_mlp = z(s.H, dtype=bf)
+            self.g_final = z(s.H, dtype=bf)
+            self.w_qkv = z((s.Hq + 2 * s.Hkv) * s.D, s.H, dtype=bf)
+            self.wo = z(s.H, qd, dtype=bf)
+            self.w_gu = z(2 * s.I, s.H, dtype=bf)
+            self.wd = z(s.H, s.I, dtype=bf)
+            self.a = z(T, s.H, dtype=bf)
+            self.pos = z(T, dtype=i32)
+            self.cos_sin = z(T, s.D // 2, 2)
+            self.o_bf = z(T, qd, dtype=bf)
+            self.resid = z(T, s.H)
+            self.bn = z(T, s.H, dtype=bf)
+            self.m = z(T, s.I, dtype=bf)
         # resident inputs
         self.k_cache = z(max(sumL, 1), s.Hkv, s.D, dtype=dt)
         self.v_cache = z(max(sumL, 1), s.Hkv, s.D, dtype=dt)
@@ -165,6 +227,21 @@ class TreeVerifyStep:
             src = val if isinstance(val, torch.Tensor) else torch.from_numpy(val)
             t.copy_(src.reshape(t.shape).to(t.dtype), non_blocking=False)
 
+    def load_layer(self, arrays: Dict[str, object]) -> None:
+        """Copy the layer's weights (standard layouts: wq [Hq*D, H], wk, wv
+        [Hkv*D, H], wo [H, Hq*D], wg, wu [I, H], wd [H, I], gains [H]) into
+        the device buffers, packing W_qkv and W_gate/up as the GEMM reads
+        them."""
+        torch = self.torch
+        s = self.s
+        dev = lambda a: (a if isinstance(a, torch.Tensor) else torch.from_numpy(a)).to(
+            device=self.w_qkv.device, dtype=torch.bfloat16)
+        for name in ("g_attn", "g_mlp", "g_final", "wo", "wd"):
+            getattr(self, name).copy_(dev(arrays[name]).reshape(getattr(self, name).shape))
+        self.w_qkv.copy_(pack_qkv_weight(dev(arrays["wq"]), dev(arrays["wk"]), dev(arrays["wv"]),
+                                         s.Hq, s.Hkv, s.D))
+        self.w_gu.copy_(pack_gate_up_weight(dev(arrays["wg"]), dev(arrays["wu"])))
+
     def host_step_inputs(self, arrays: Dict[str, object]):
         """Pinned host buffer laid out like `step_inputs`, filled from host
         arrays named as the step's inputs: one copy moves a whole step."""
@@ -200,6 +277,24 @@ class TreeVerifyStep:
                            tree_off=self.tree_off, parent=self.parent, tokens=self.tokens,
                            node_depth=self.node_depth, score=self.score,
                            p_row_of_node=self.p_row_of_node, stream=stream)
+
+    def run_layer(self, stream=None) -> None:
+        """The decoder layer over every tree node, ending in the final
+        RMSNorm that feeds the LM head (h)."""
+        s = self.s
+        eagle_rmsnorm(self.x, self.g_attn, self.a, self.status, eps=s.eps, stream=stream)
+        eagle_tree_rope_table(self.tree_off, self.parent, self.pos, self.cos_sin, self.status,
+                              D=s.D, theta=s.theta, kv_off=self.kv_off, stream=stream)
+        eagle_gemm(EPI_QKV_ROPE, self.a, self.w_qkv, self.status, q=self.q, k=self.k_tree,
+                   v=self.v_tree, cos_sin=self.cos_sin, Hq=s.Hq, Hkv=s.Hkv, D=s.D, stream=stream)
+        self.run_attn(stream)
+        eagle_cast_bf16(self.attn_out.view(-1), self.o_bf.view(-1), stream=stream)
+        eagle_gemm(EPI_ACCUM, self.o_bf, self.wo, self.status, accum=self.resid, resid=self.x,
+                   stream=stream)
+        eagle_rmsnorm(self.resid, self.g_mlp, self.bn, self.status, eps=s.eps, stream=stream)
+        eagle_gemm(EPI_SWIGLU, self.bn, self.w_gu, self.status, y=self.m, stream=stream)
+        eagle_gemm(EPI_ACCUM, self.m, self.wd, self.status, accum=self.resid, stream=stream)
+        eagle_rmsnorm(self.resid, self.g_final, self.h, self.status, eps=s.eps, stream=stream)
 
     def run_attn(self, stream=None) -> None:
         eagle_tree_attn(self.q, self.k_tree, self.v_tree, self.k_cache, self.v_cache,
@@ -249,6 +344,14 @@ class TreeVerifyStep:
         same SMs) and the attention."""
         torch = self.torch
         main = stream if stream is not None else torch.cuda.current_stream()
+        if self.s.layer:
+            # the LM head reads the layer's output: one stream, in order
+            if self.s.builds_tree and build_tree:
+                self.run_expand(main)
+            self.run_layer(main)
+            self.run_lmhead(main)
+            self.run_accept(main)
+            return
         if self._side is None:
             self._side = torch.cuda.Stream(device=main.device)
         side = self._side
@@ -268,6 +371,9 @@ class TreeVerifyStep:
         elif self.s.static:
             n += 2 if len(self.s.static[0]) > 1 else 1   # ranks + finish
         n += 1                                   # attention
+        if self.s.layer:                         # norms, rope table, 4 GEMMs (+ one
+            tiles = (self.s.T + 127) // 128      # per extra cluster pass), cast
+            n += 3 + 1 + 4 * ((tiles + 7) // 8) + 1
         if self.s.dtype == "bf16":               # LM head: one launch per cluster of
             tiles = (self.s.T + 127) // 128      # up to eight 128-row tiles
             n += (tiles + 7) // 8 + 1            # ... + finalize

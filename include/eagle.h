@@ -74,6 +74,12 @@ typedef enum {
   EAGLE_LMHEAD_LOGITS = 2
 } eagle_lmhead_mode;
 typedef enum { EAGLE_SAMPLE_REPLACE = 0, EAGLE_SAMPLE_NO_REPLACE = 1 } eagle_sample_mode;
+typedef enum {
+  EAGLE_EPI_STORE = 0,    /* y = A W^T, bf16                                  */
+  EAGLE_EPI_ACCUM = 1,    /* accum += A W^T, fp32 (the residual stream)       */
+  EAGLE_EPI_SWIGLU = 2,   /* y = silu(gate) * up, bf16                        */
+  EAGLE_EPI_QKV_ROPE = 3  /* q, k rotated to their positions, v; bf16         */
+} eagle_epilogue;
 
 /* Limits of this implementation. */
 #define EAGLE_MAX_TREE_NODES 256  /* nodes per sequence, root included       */
@@ -387,6 +393,72 @@ EAGLE_API eagle_status eagle_draft_static(int B, int V, int N, int R, int max_ra
                                 int32_t *d_parent, int32_t *d_tokens, int32_t *d_node_depth,
                                 float *d_score, int32_t *d_p_row_of_node, int *d_status,
                                 eagle_stream_t stream);
+
+/* ------------------------------------------------------------------------
+ * The decoder layer around the tree attention.
+ * [EAGLE] workflow paragraph; [S4000] "EAGLE的创新点" item 2: the verify pass
+ * is one forward pass of the target model over every tree token.  The pages
+ * name LLaMA-family targets without giving their layer, which is read here
+ * as a pre-norm LLaMA layer:
+ *     a  = rmsnorm(x) * g_attn                    eagle_rmsnorm
+ *     q, k, v = a Wq^T, a Wk^T, a Wv^T, q and k rotated to each node's
+ *               position (cache length + depth)  eagle_tree_rope_table +
+ *                                                 eagle_gemm(QKV_ROPE)
+ *     o  = tree attention                          eagle_tree_attn(_paged)
+ *     h  = x + bf16(o) Wo^T                       eagle_cast_bf16 +
+ *                                                 eagle_gemm(ACCUM)
+ *     b  = rmsnorm(h) * g_mlp                     eagle_rmsnorm
+ *     m  = silu(b Wg^T) * (b Wu^T)                eagle_gemm(SWIGLU)
+ *     h += m Wd^T                                 eagle_gemm(ACCUM)
+ * x, h are the fp32 residual stream [T, H]; every matrix-multiply operand and
+ * q / k / v are bf16, accumulation fp32.
+ * ---------------------------------------------------------------------- */
+
+/* y [T,H] bf16 = x / sqrt(mean_j x[t,j]^2 + eps) * gain, x fp32 [T,H],
+ * gain bf16 [H].  Device errors: NUMERIC (non-finite x). */
+EAGLE_API eagle_status eagle_rmsnorm(int T, int H, float eps, const float *d_x,
+                                     const void *d_gain, void *d_y, int *d_status,
+                                     eagle_stream_t stream);
+
+/* y[i] = bf16(x[i]) (round to nearest even), n elements. */
+EAGLE_API eagle_status eagle_cast_bf16(size_t n, const float *d_x, void *d_y,
+                                       eagle_stream_t stream);
+
+/* Positions and rotations of the tree nodes.  Node i of sequence b sits at
+ * position pos = L_b + depth(i) (where it would stand on its own
+ * root-to-node path after the cache), L_b = kv_off[b+1] - kv_off[b] or
+ * kv_len[b] (give exactly one of d_kv_off [B+1], d_kv_len [B]).  Writes
+ * d_pos [T] and d_cos_sin [T, D/2, 2] fp32 = (cos, sin) of
+ * pos * theta^(-2j/D) (angle and trigonometry in fp64, rounded once).
+ * Device errors: INVALID_TREE. */
+EAGLE_API eagle_status eagle_tree_rope_table(int B, int D, float theta,
+                                             const int32_t *d_tree_off, const int32_t *d_parent,
+                                             const int32_t *d_kv_off, const int32_t *d_kv_len,
+                                             int32_t *d_pos, float *d_cos_sin, int *d_status,
+                                             eagle_stream_t stream);
+
+/* Tensor-core GEMM of the layer: Y = A W^T with A [T,K] bf16 (tree rows)
+ * and W [N,K] bf16 (rows = output features, K contiguous), fp32
+ * accumulation; N % 32 == 0, K % 8 == 0, pointers 16-byte aligned.  W is
+ * streamed from memory once per 1024 rows of A.  The epilogue decides what
+ * is written:
+ *   EAGLE_EPI_STORE     d_y [T,N] bf16.
+ *   EAGLE_EPI_ACCUM     d_accum [T,N] fp32 = R + Y with R = d_resid [T,N]
+ *                       fp32 if given, else d_accum itself (in place).
+ *   EAGLE_EPI_SWIGLU    W rows alternate 16 gate rows and the 16 matching
+ *                       up rows; d_y [T,N/2] bf16 = silu(gate) * up.
+ *   EAGLE_EPI_QKV_ROPE  N = (Hq + 2 Hkv) D; W = [Wq; Wk; Wv] with, inside
+ *                       every q and k head, the rows of dimensions j and
+ *                       j + D/2 adjacent (row 2j holds dimension j, row
+ *                       2j+1 dimension j + D/2); q, k are rotated by
+ *                       d_cos_sin (eagle_tree_rope_table) and written to
+ *                       d_q [T,Hq,D], d_k [T,Hkv,D]; v to d_v [T,Hkv,D].
+ * Arguments an epilogue does not use may be NULL / 0. */
+EAGLE_API eagle_status eagle_gemm(int epilogue, int T, int N, int K, const void *d_a,
+                                  const void *d_w, void *d_y, float *d_accum,
+                                  const float *d_resid, void *d_q,
+                                  void *d_k, void *d_v, const float *d_cos_sin, int Hq, int Hkv,
+                                  int D, int *d_status, eagle_stream_t stream);
 
 #ifdef __cplusplus
 }

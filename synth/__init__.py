@@ -54,6 +54,10 @@ class Workload:
     seed: int = 0
     draft_sigma: float = 3.0   # draft logits ~ N(0, draft_sigma)
     w_sigma: float = 0.02      # LM-head weights ~ N(0, w_sigma)
+    # the full decoder layer around the attention (0: attention alone)
+    I: int = 0                 # MLP intermediate size
+    theta: float = 10000.0     # rotary base
+    eps: float = 1e-5          # RMSNorm epsilon
 
     # ---- derived sizes -------------------------------------------------
     @property
@@ -148,19 +152,20 @@ def workloads() -> Dict[str, Workload]:
         "vicuna7b": Workload(
             name="vicuna7b", dtype="bf16", B=1, Hq=32, Hkv=32, D=128, H=4096,
             V=32000, L=(2048,), tree="eagle2", k=10, depth=6, budget=(60,),
-            modes=("greedy",), seed=0),
+            modes=("greedy",), seed=0, I=11008, theta=10000.0, eps=1e-5),
         # LLaMA-3-8B shaped layer: GQA 32/8 x 128, vocab 128256, L=8192,
         # budget 64, depth 7, top-8; stochastic acceptance at T=1.
         "llama3_8b": Workload(
             name="llama3_8b", dtype="bf16", B=1, Hq=32, Hkv=8, D=128, H=4096,
             V=128256, L=(8192,), tree="eagle2", k=8, depth=7, budget=(64,),
-            modes=("stochastic",), temperature=1.0, seed=0),
+            modes=("stochastic",), temperature=1.0, seed=0, I=14336, theta=500000.0),
         # LLaMA-3-70B shaped layer: GQA 64/8 x 128, hidden 8192, vocab 128256,
         # L=4096, budget 64, depth 8, top-8; greedy and stochastic; seed 3.
         "llama3_70b": Workload(
             name="llama3_70b", dtype="bf16", B=1, Hq=64, Hkv=8, D=128, H=8192,
             V=128256, L=(4096,), tree="eagle2", k=8, depth=8, budget=(64,),
-            modes=("greedy", "stochastic"), temperature=1.0, seed=3),
+            modes=("greedy", "stochastic"), temperature=1.0, seed=3, I=28672,
+            theta=500000.0),
         # small bf16 case for the start-up check: three sequences (157 tree
         # rows, so the LM head takes its two-tile cluster path), GQA 32/8,
         # a ragged vocabulary, EAGLE-2 trees; greedy and stochastic.
@@ -168,7 +173,7 @@ def workloads() -> Dict[str, Workload]:
             name="smoke_bf16", dtype="bf16", B=3, Hq=32, Hkv=8, D=128, H=1024,
             V=4099, L=(512, 300, 700), tree="eagle2", k=8, depth=8,
             budget=(64, 40, 50), modes=("greedy", "stochastic"), temperature=0.8,
-            seed=7),
+            seed=7, I=2816, theta=10000.0),
         # Vicuna-7B shaped layer verifying an EAGLE-1 static tree: the full
         # 4-ary template of 3 draft steps (85 nodes, 64 root-to-leaf paths).
         "vicuna7b_static": Workload(
@@ -180,7 +185,8 @@ def workloads() -> Dict[str, Workload]:
         "llama3_8b_batch16": Workload(
             name="llama3_8b_batch16", dtype="bf16", B=16, Hq=32, Hkv=8, D=128,
             H=4096, V=128256, L=_C5_L, tree="eagle2", k=8, depth=8,
-            budget=_C5_BUDGET, modes=("stochastic",), temperature=0.7, seed=5),
+            budget=_C5_BUDGET, modes=("stochastic",), temperature=0.7, seed=5,
+            I=14336, theta=500000.0),
     }
 
 
@@ -332,3 +338,25 @@ def random_probs(seed: int, name: str, rows: int, V: int, sigma: float = 2.0,
     z -= z.max(axis=1, keepdims=True)
     e = np.exp(z)
     return (e / e.sum(axis=1, keepdims=True)).astype(np.float32)
+
+
+def make_layer_inputs(w: Workload, set_index: int = 0) -> Dict[str, np.ndarray]:
+    """Inputs of the full decoder layer: the residual stream x [T, H] fp32
+    entering the layer at every tree node (~ N(0, 1)), the layer's weights
+    (rows = output features; ~ N(0, w_sigma), stored as bf16 values), the
+    RMSNorm gains (1 + N(0, 0.02), bf16) and the final norm's gain.  The
+    weights are the same for every set (they are the model's); x changes."""
+    if not w.I:
+        raise ValueError(f"workload {w.name} has no layer")
+    s = w.seed
+    tag = "" if set_index == 0 else f"#{set_index}"
+    bf = to_bf16_values
+    qd, kd = w.Hq * w.D, w.Hkv * w.D
+    out = {"x": normal(s, "layer-x" + tag, (w.T, w.H))}
+    for name, shape in (("wq", (qd, w.H)), ("wk", (kd, w.H)), ("wv", (kd, w.H)),
+                        ("wo", (w.H, qd)), ("wg", (w.I, w.H)), ("wu", (w.I, w.H)),
+                        ("wd", (w.H, w.I))):
+        out[name] = bf(normal(s, "layer-" + name, shape, std=w.w_sigma))
+    for name in ("g_attn", "g_mlp", "g_final"):
+        out[name] = bf(np.float32(1.0) + normal(s, "layer-" + name, (w.H,), std=0.02))
+    return out

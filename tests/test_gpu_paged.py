@@ -96,6 +96,8 @@ def test_paged_attention_matches_oracle_and_packed(dtype, Ls, levels, Hq, Hkv, p
     q, kt, vt, kp, vp, table, kv_len, tree_off, parent = case
     ref, ab = O.tree_attn_paged(*case, with_abs=True)
     assert report_attn_err(f"paged {dtype} page={page}", got, ref, ab) <= tol_for(dtype)
+    if dtype == "bf16" and page % 128:
+        return        # this page size runs the CUDA-core kernel, the packed cache does not
     kc, kv_off = O.gather_pages(kp, table, kv_len)
     vc, _ = O.gather_pages(vp, table, kv_len)
     packed, st = _run_packed(E, dtype, q, kt, vt, kc, vc, kv_off.astype(np.int32), tree_off,
