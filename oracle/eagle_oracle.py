@@ -80,7 +80,7 @@ MODE_NO_REPLACE = 1
 __all__ = [
     "FRAC_BITS", "MODE_REPLACE", "MODE_NO_REPLACE", "OracleNumericError",
     "tree_path", "tree_children", "tree_depths", "tree_attn", "causal_attn",
-    "gather_pages", "tree_attn_paged",
+    "gather_pages", "tree_attn_paged", "kv_commit_paged",
     "lmhead_softmax", "accept_greedy", "accept_stochastic",
     "expand_level", "expand_finalize", "build_eagle2_tree", "f32_of_int",
     "static_template_full", "build_static_tree",
@@ -216,6 +216,35 @@ def tree_attn_paged(q, k_tree, v_tree, k_pages, v_pages, block_table, kv_len, tr
     vc, _ = gather_pages(v_pages, block_table, kv_len)
     return tree_attn(q, k_tree, v_tree, kc, vc, kv_off, tree_off, parent, scale=scale,
                      nodes=nodes, with_abs=with_abs)
+
+
+def kv_commit_paged(k_pages, v_pages, block_table, kv_len, tree_off, k_tree, v_tree,
+                    accept_len, accepted_nodes):
+    """Commit a verify step's accepted tokens to a paged KV cache.
+
+    [EAGLE] speculative-sampling paragraph: alpha accepted drafts turn into
+    alpha + 1 tokens; the root of the tree (the last token of the previous
+    step) and the alpha accepted nodes now belong to the context, so their
+    keys and values (computed by the verify pass, rotated to their
+    positions) are appended to the sequence's cache: path entry i goes to
+    cache position kv_len[b] + i.  Returns (k_pages, v_pages, kv_len), new
+    arrays; the block table must already hold pages for the new length."""
+    kp = np.array(k_pages, copy=True)
+    vp = np.array(v_pages, copy=True)
+    P = kp.shape[1]
+    new_len = np.array(kv_len, dtype=np.int64, copy=True)
+    for b in range(len(kv_len)):
+        t0 = int(tree_off[b])
+        for i in range(int(accept_len[b]) + 1):
+            node = int(accepted_nodes[b][i])
+            pos = int(kv_len[b]) + i
+            page = int(block_table[b][pos // P])
+            if not (0 <= page < kp.shape[0]):
+                raise ValueError("no page for the committed position")
+            kp[page, pos % P] = k_tree[t0 + node]
+            vp[page, pos % P] = v_tree[t0 + node]
+        new_len[b] = int(kv_len[b]) + int(accept_len[b]) + 1
+    return kp, vp, new_len
 
 
 def causal_attn(q_seq, k_seq, v_seq, n_prefix: int, scale: Optional[float] = None):

@@ -208,3 +208,53 @@ def test_paged_cache_reads_the_same_keys_as_the_packed_cache():
     bad[0, 0] = n_pages
     with pytest.raises(ValueError):
         O.gather_pages(kp, bad, Ls)
+
+
+def test_commit_appends_the_accepted_path_and_preserves_its_attention():
+    # after committing the root and the accepted nodes, the cache is the old
+    # cache followed by their K/V rows, and the deepest accepted node's query
+    # sees exactly the keys its tree attention saw: the same output
+    g = np.random.default_rng(21)
+    Hq, Hkv, D, P = 4, 2, 8, 4
+    Ls = [5, 0]
+    q, kt, vt, kc, vc, kv_off, tree_off, parent = _case(2, Ls, (1, 3, 3, 3), Hq, Hkv, D, 41)
+    n_pages = 12
+    kp = g.standard_normal((n_pages, P, Hkv, D))
+    vp = g.standard_normal((n_pages, P, Hkv, D))
+    table = np.array([[3, 7, 1, 9], [0, 5, 11, 2]])
+    for b, L in enumerate(Ls):
+        for pos in range(L):
+            kp[table[b, pos // P], pos % P] = kc[kv_off[b] + pos]
+            vp[table[b, pos // P], pos % P] = vc[kv_off[b] + pos]
+    before = O.tree_attn_paged(q, kt, vt, kp, vp, table, Ls, tree_off, parent)
+    # an accepted path in each tree: root, then the first child chain
+    accept_len, nodes = [], np.full((2, 4), -1)
+    for b in range(2):
+        par = parent[tree_off[b]:tree_off[b + 1]]
+        path, cur = [0], 0
+        while True:
+            kids = O.tree_children(par, cur)
+            if not kids or len(path) == 3:
+                break
+            cur = kids[-1]
+            path.append(cur)
+        nodes[b, :len(path)] = path
+        accept_len.append(len(path) - 1)
+    kp2, vp2, L2 = O.kv_commit_paged(kp, vp, table, Ls, tree_off, kt, vt, accept_len, nodes)
+    for b in range(2):
+        packed, _ = O.gather_pages(kp2, table[b:b + 1], [L2[b]])
+        path = [tree_off[b] + n for n in nodes[b, :accept_len[b] + 1]]
+        np.testing.assert_array_equal(packed, np.concatenate([kc[kv_off[b]:kv_off[b + 1]],
+                                                              kt[path]]))
+        last = path[-1]
+        keys, vals = packed, O.gather_pages(vp2, table[b:b + 1], [L2[b]])[0]
+        for h in range(Hq):
+            s = keys[:, h // (Hq // Hkv)] @ q[last, h] / np.sqrt(D)
+            w = np.exp(s - s.max())
+            np.testing.assert_allclose(w @ vals[:, h // (Hq // Hkv)] / w.sum(), before[last, h],
+                                       rtol=1e-12, atol=1e-13)
+    # pages not named by the table are untouched
+    used = set(table.reshape(-1).tolist())
+    for page in range(n_pages):
+        if page not in used:
+            np.testing.assert_array_equal(kp2[page], kp[page])
