@@ -23,6 +23,7 @@ __all__ = [
     "eagle_accept_stochastic", "eagle_accept_stochastic_logits", "eagle_draft_expand",
     "eagle_draft_pool_bytes", "eagle_draft_static", "eagle_tree_attn_paged",
     "eagle_rmsnorm", "eagle_cast_bf16", "eagle_tree_rope_table", "eagle_gemm",
+    "eagle_kv_commit_paged",
     "EPI_STORE", "EPI_ACCUM", "EPI_SWIGLU", "EPI_QKV_ROPE",
     "eagle_lmhead_softmax_noalloc", "eagle_lmhead_noalloc_max_scratch_bytes",
 ]
@@ -70,6 +71,7 @@ _SIGS = {
     "eagle_cast_bf16": ([_sz, _p, _p, _p], _i),
     "eagle_tree_rope_table": ([_i, _i, _f] + [_p] * 8, _i),
     "eagle_gemm": ([_i] * 4 + [_p] * 9 + [_i] * 3 + [_p, _p], _i),
+    "eagle_kv_commit_paged": ([_i] * 8 + [_p] * 11, _i),
 }
 
 
@@ -408,3 +410,26 @@ def eagle_gemm(epilogue, a, w, status, *, y=None, accum=None, resid=None, q=None
     _call("eagle_gemm", int(epilogue), T, N, K, _ptr(a), _ptr(w), _ptr(y), _ptr(accum),
           _ptr(resid), _ptr(q), _ptr(k), _ptr(v), _ptr(cos_sin), int(Hq), int(Hkv), int(D),
           _ptr(status), _stream(stream))
+
+
+def eagle_kv_commit_paged(tree_off, accept_len, accepted_nodes, k_tree, v_tree, k_pages, v_pages,
+                          block_table, kv_len, status, *, max_depth: int, stream=None) -> None:
+    """Append the root and accepted nodes' K/V rows (k_tree/v_tree [T,Hkv,D])
+    to the paged cache (k_pages/v_pages [n_pages, page_size, Hkv, D]) and
+    advance kv_len [B] in place; accepted_nodes [B, max_depth+1]."""
+    torch = _torch()
+    B = tree_off.numel() - 1
+    T, Hkv, D = k_tree.shape
+    n_pages, page_size = k_pages.shape[0], k_pages.shape[1]
+    for name, t in (("v_tree", v_tree), ("k_pages", k_pages), ("v_pages", v_pages)):
+        _need(t, k_tree.dtype, name)
+    for name, t in (("tree_off", tree_off), ("accept_len", accept_len),
+                    ("accepted_nodes", accepted_nodes), ("block_table", block_table),
+                    ("kv_len", kv_len)):
+        _need(t, torch.int32, name)
+    if accepted_nodes.numel() < B * (max_depth + 1):
+        raise ValueError("accepted_nodes must hold max_depth+1 entries per sequence")
+    _call("eagle_kv_commit_paged", _dtype_code(k_tree), B, Hkv, D, page_size, n_pages,
+          block_table.shape[1], int(max_depth), _ptr(tree_off), _ptr(accept_len),
+          _ptr(accepted_nodes), _ptr(k_tree), _ptr(v_tree), _ptr(k_pages), _ptr(v_pages),
+          _ptr(block_table), _ptr(kv_len), _ptr(status), _stream(stream))

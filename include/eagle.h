@@ -162,6 +162,30 @@ EAGLE_API eagle_status eagle_tree_attn_paged(eagle_dtype dtype, int B, int T, in
                                    float *d_out, int *d_status, eagle_stream_t stream);
 
 /* ------------------------------------------------------------------------
+ * eagle_kv_commit_paged -- append a verify step's accepted tokens to a
+ * paged KV cache.
+ * [EAGLE] speculative-sampling paragraph: alpha accepted drafts give alpha+1
+ * tokens; the tree's root (the last token of the previous step) and the
+ * alpha accepted nodes join the context.  For every sequence b, path entry
+ * i = 0 .. d_accept_len[b] (node d_accepted_nodes[b*(max_depth+1) + i], the
+ * acceptance walk's output; entry 0 is the root) has its K and V rows of
+ * d_k_tree / d_v_tree [T,Hkv,D] copied to cache position d_kv_len[b] + i of
+ * the pages (layout as eagle_tree_attn_paged); then d_kv_len[b] grows by
+ * d_accept_len[b] + 1.  The block table must already name pages for the
+ * new length.  Rows are copied bit for bit (dtype gives the element size).
+ * Device errors: INVALID_ARG (accept length outside [0, max_depth], a node
+ * outside its tree, a position without a page); that sequence is left
+ * unchanged.
+ * ---------------------------------------------------------------------- */
+EAGLE_API eagle_status eagle_kv_commit_paged(eagle_dtype dtype, int B, int Hkv, int D,
+                                   int page_size, int n_pages, int max_pages, int max_depth,
+                                   const int32_t *d_tree_off, const int32_t *d_accept_len,
+                                   const int32_t *d_accepted_nodes, const void *d_k_tree,
+                                   const void *d_v_tree, void *d_k_pages, void *d_v_pages,
+                                   const int32_t *d_block_table, int32_t *d_kv_len,
+                                   int *d_status, eagle_stream_t stream);
+
+/* ------------------------------------------------------------------------
  * eagle_lmhead_softmax -- frozen LM head over every tree node.
  * [EAGLE] workflow paragraph: the frozen classification head gives each
  * node's next-token distribution, q = softmax(z / temperature), z = h W^T.
