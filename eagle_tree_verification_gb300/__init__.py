@@ -23,7 +23,8 @@ __all__ = [
     "eagle_accept_stochastic", "eagle_accept_stochastic_logits", "eagle_draft_expand",
     "eagle_draft_pool_bytes", "eagle_draft_static", "eagle_tree_attn_paged",
     "eagle_rmsnorm", "eagle_cast_bf16", "eagle_tree_rope_table", "eagle_gemm",
-    "eagle_kv_commit_paged",
+    "eagle_kv_commit_paged", "eagle_draft_expand_dep", "eagle_draft_head_input",
+    "eagle_draft_rows", "eagle_embed_rows", "eagle_loop_advance",
     "EPI_STORE", "EPI_ACCUM", "EPI_SWIGLU", "EPI_QKV_ROPE",
     "eagle_lmhead_softmax_noalloc", "eagle_lmhead_noalloc_max_scratch_bytes",
 ]
@@ -72,6 +73,11 @@ _SIGS = {
     "eagle_tree_rope_table": ([_i, _i, _f] + [_p] * 8, _i),
     "eagle_gemm": ([_i] * 4 + [_p] * 9 + [_i] * 3 + [_p, _p], _i),
     "eagle_kv_commit_paged": ([_i] * 8 + [_p] * 11, _i),
+    "eagle_draft_expand_dep": ([_i] * 6 + [_p] * 4 + [_sz] + [_p] * 8, _i),
+    "eagle_draft_head_input": ([_i] * 6 + [_p, _sz] + [_p] * 9, _i),
+    "eagle_draft_rows": ([_i] * 5 + [_p] * 5, _i),
+    "eagle_embed_rows": ([_i] * 3 + [_p] * 5, _i),
+    "eagle_loop_advance": ([_i] * 3 + [_p] * 9, _i),
 }
 
 
@@ -307,11 +313,14 @@ def eagle_draft_pool_bytes(B, k, depth, V) -> int:
 def eagle_draft_expand(pool, status, *, B: int, V: int, k: int, depth: int, level: int = 0,
                        finalize: int = 0, draft_logp=None, budget=None, root_token=None,
                        tree_off=None, parent=None, tokens=None, node_depth=None, score=None,
-                       p_row_of_node=None, stream=None) -> None:
+                       p_row_of_node=None, rows_from_previous_kernel: bool = False,
+                       stream=None) -> None:
     """EAGLE-2 expand (one level), finalize (finalize=1), or the last level
     with the finalize fused in (finalize=2); draft_logp [B, R, V] fp32 with
-    R = 1 + (depth-1)*k."""
-    _call("eagle_draft_expand", B, V, k, depth, int(level), int(finalize),
+    R = 1 + (depth-1)*k.  rows_from_previous_kernel selects
+    eagle_draft_expand_dep (rows written by the kernel just before)."""
+    name = "eagle_draft_expand_dep" if rows_from_previous_kernel else "eagle_draft_expand"
+    _call(name, B, V, k, depth, int(level), int(finalize),
           _ptr(draft_logp), _ptr(budget), _ptr(root_token), _ptr(pool),
           pool.numel() * pool.element_size(), _ptr(tree_off), _ptr(parent), _ptr(tokens),
           _ptr(node_depth), _ptr(score), _ptr(p_row_of_node), _ptr(status), _stream(stream))
@@ -433,3 +442,40 @@ def eagle_kv_commit_paged(tree_off, accept_len, accepted_nodes, k_tree, v_tree, 
           block_table.shape[1], int(max_depth), _ptr(tree_off), _ptr(accept_len),
           _ptr(accepted_nodes), _ptr(k_tree), _ptr(v_tree), _ptr(k_pages), _ptr(v_pages),
           _ptr(block_table), _ptr(kv_len), _ptr(status), _stream(stream))
+
+
+def eagle_draft_head_input(pool, node_cur, f_ctx, root_token, emb, a, status, *, B: int, V: int,
+                           k: int, depth: int, level: int, node_prev=None, feat_prev=None,
+                           stream=None) -> None:
+    """Draft-head input rows [B*F, 2H] bf16 for one EAGLE-2 level (see
+    include/eagle.h)."""
+    H = emb.shape[1]
+    _call("eagle_draft_head_input", B, V, k, depth, int(level), H, _ptr(pool),
+          pool.numel() * pool.element_size(), _ptr(node_prev), _ptr(node_cur), _ptr(feat_prev),
+          _ptr(f_ctx), _ptr(root_token), _ptr(emb), _ptr(a), _ptr(status), _stream(stream))
+
+
+def eagle_draft_rows(z, lse, logp, prob, *, B: int, k: int, depth: int, level: int,
+                     stream=None) -> None:
+    """The level's draft rows (log-probs, and probabilities if prob is
+    given) from the LM head's logits of its draft nodes."""
+    V = z.shape[1]
+    _call("eagle_draft_rows", B, V, k, depth, int(level), _ptr(z), _ptr(lse), _ptr(logp),
+          _ptr(prob), _stream(stream))
+
+
+def eagle_embed_rows(tokens, emb, x, status, stream=None) -> None:
+    """x [T, H] fp32 = emb[tokens] (emb [V, H] bf16)."""
+    V, H = emb.shape
+    _call("eagle_embed_rows", tokens.numel(), H, V, _ptr(tokens), _ptr(emb), _ptr(x),
+          _ptr(status), _stream(stream))
+
+
+def eagle_loop_advance(tree_off, accept_len, accepted_nodes, out_tokens, resid, f_ctx,
+                       root_token, status, *, max_depth: int, stream=None) -> None:
+    """Next step's root token (bonus token) and context feature."""
+    B = tree_off.numel() - 1
+    H = resid.shape[1]
+    _call("eagle_loop_advance", B, H, int(max_depth), _ptr(tree_off), _ptr(accept_len),
+          _ptr(accepted_nodes), _ptr(out_tokens), _ptr(resid), _ptr(f_ctx), _ptr(root_token),
+          _ptr(status), _stream(stream))

@@ -143,8 +143,9 @@ struct FinalParams {
 
 struct LevelParams {
   int B, V, k, F, R, S, level, P;
-  bool vec_ok;  // rows 16-byte aligned: float4 loads
-  bool fused;   // the last level: also finalize every sequence (fin)
+  bool vec_ok;     // rows 16-byte aligned: float4 loads
+  bool fused;      // the last level: also finalize every sequence (fin)
+  bool rows_wait;  // the rows come from the kernel just before: read them after the wait
   const float* logp;
   PoolPtrs pool;
   FinalParams fin;
@@ -508,8 +509,9 @@ template <int VEC>
 __global__ void __launch_bounds__(kLvThreads, 2) expand_level_kernel(const LevelParams A) {
   // A level's draft rows and its chunk lists do not depend on the level
   // before it (whose lists are the other parity's), so past level 0 only
-  // the merging CTA waits for it.  Level 0 follows the pool reset.
-  if (A.level == 0) pdl_begin();
+  // the merging CTA waits for it.  Level 0 follows the pool reset.  Rows
+  // written by the kernel just before this one are read after the wait.
+  if (A.level == 0 || A.rows_wait) pdl_begin();
   __shared__ ChunkShared C;
   __shared__ MergeShared M;
   const int tid = threadIdx.x;
@@ -536,7 +538,7 @@ __global__ void __launch_bounds__(kLvThreads, 2) expand_level_kernel(const Level
     }
   }
   if (!chunk_topk<VEC>(A, row, chunk, v, C)) return;
-  if (A.level > 0) pdl_begin();   // the frontier and pool fill of the level before
+  if (A.level > 0 && !A.rows_wait) pdl_begin();   // the level before: frontier, pool fill
   merge_sequence(A, b, M);
   if (A.fused) {
     // the last level: this CTA holds the sequence's complete pool
@@ -571,7 +573,7 @@ __global__ void __launch_bounds__(kLvThreads, 2)
 expand_level_stream_kernel(const LevelParams A, int total_chunks) {
   // as expand_level_kernel: past level 0 a CTA waits for the level before
   // only when it is about to merge
-  bool waited = (A.level == 0);
+  bool waited = (A.level == 0 || A.rows_wait);
   if (waited) pdl_begin();
   __shared__ ChunkShared C;
   __shared__ MergeShared M;
@@ -845,14 +847,14 @@ extern "C" size_t eagle_draft_pool_bytes(int B, int k, int depth, int V) {
   return pool_layout(B, k, depth, V).total;
 }
 
-extern "C" eagle_status eagle_draft_expand(int B, int V, int k, int depth, int level,
-                                           int finalize, const float* d_draft_logp,
-                                           const int32_t* d_budget, const int32_t* d_root_token,
-                                           void* d_pool, size_t pool_bytes, int32_t* d_tree_off,
-                                           int32_t* d_parent, int32_t* d_tokens,
-                                           int32_t* d_node_depth, float* d_score,
-                                           int32_t* d_p_row_of_node, int* d_status,
-                                           eagle_stream_t stream) {
+namespace {
+
+eagle_status expand_impl(bool rows_wait, int B, int V, int k, int depth, int level, int finalize,
+                         const float* d_draft_logp, const int32_t* d_budget,
+                         const int32_t* d_root_token, void* d_pool, size_t pool_bytes,
+                         int32_t* d_tree_off, int32_t* d_parent, int32_t* d_tokens,
+                         int32_t* d_node_depth, float* d_score, int32_t* d_p_row_of_node,
+                         int* d_status, eagle_stream_t stream) {
   EAGLE_HOST_CHECK(B >= 1 && V >= 1, EAGLE_ERR_INVALID_ARG);
   EAGLE_HOST_CHECK(k >= 1 && k <= EAGLE_MAX_TOPK && k <= V, EAGLE_ERR_UNSUPPORTED);
   EAGLE_HOST_CHECK(depth >= 1 && depth <= EAGLE_MAX_DEPTH, EAGLE_ERR_UNSUPPORTED);
@@ -916,6 +918,7 @@ extern "C" eagle_status eagle_draft_expand(int B, int V, int k, int depth, int l
   A.level = level;
   A.P = L.P;
   A.vec_ok = (V % 4 == 0) && ((uintptr_t)d_draft_logp % 16 == 0);
+  A.rows_wait = rows_wait;
   A.logp = d_draft_logp;
   A.pool = pp;
   A.pool.ticket = pp.ticket + (size_t)(level & 1) * B;
@@ -971,4 +974,117 @@ extern "C" eagle_status eagle_draft_expand(int B, int V, int k, int depth, int l
       launch_status(launch_pdl(kern, dim3(B * A.F * A.S), dim3(kLvThreads), dyn, s, A));
   if (st != EAGLE_OK || finalize != 2 || A.fused) return st;
   return launch_finalize();
+}
+
+}  // namespace
+
+extern "C" eagle_status eagle_draft_expand(int B, int V, int k, int depth, int level,
+                                           int finalize, const float* d_draft_logp,
+                                           const int32_t* d_budget, const int32_t* d_root_token,
+                                           void* d_pool, size_t pool_bytes, int32_t* d_tree_off,
+                                           int32_t* d_parent, int32_t* d_tokens,
+                                           int32_t* d_node_depth, float* d_score,
+                                           int32_t* d_p_row_of_node, int* d_status,
+                                           eagle_stream_t stream) {
+  return expand_impl(false, B, V, k, depth, level, finalize, d_draft_logp, d_budget, d_root_token,
+                     d_pool, pool_bytes, d_tree_off, d_parent, d_tokens, d_node_depth, d_score,
+                     d_p_row_of_node, d_status, stream);
+}
+
+extern "C" eagle_status eagle_draft_expand_dep(int B, int V, int k, int depth, int level,
+                                               int finalize, const float* d_draft_logp,
+                                               const int32_t* d_budget,
+                                               const int32_t* d_root_token, void* d_pool,
+                                               size_t pool_bytes, int32_t* d_tree_off,
+                                               int32_t* d_parent, int32_t* d_tokens,
+                                               int32_t* d_node_depth, float* d_score,
+                                               int32_t* d_p_row_of_node, int* d_status,
+                                               eagle_stream_t stream) {
+  return expand_impl(true, B, V, k, depth, level, finalize, d_draft_logp, d_budget, d_root_token,
+                     d_pool, pool_bytes, d_tree_off, d_parent, d_tokens, d_node_depth, d_score,
+                     d_p_row_of_node, d_status, stream);
+}
+
+// ---------------------------------------------------------------------------
+// Input rows of the draft head for one level (the draft-tree loop).
+// Level 0: row b = [f_ctx[b] ; emb[root_token[b]]] (the root).  Level d >= 1:
+// the frontier left by level d-1, by rank: row b*k + f = [feature of the
+// node's parent ; emb[node's token]], the parent's feature found among the
+// previous level's rows (feat_prev / node_prev, F_prev per sequence, node
+// -1 = the root).  node_cur receives the rows' pool indices.
+// ---------------------------------------------------------------------------
+namespace {
+
+__global__ void __launch_bounds__(256)
+head_input_kernel(PoolPtrs pool, int k, int P, int H, int level, int F_prev,
+                  const int* __restrict__ node_prev, int* __restrict__ node_cur,
+                  const __nv_bfloat16* __restrict__ feat_prev,
+                  const __nv_bfloat16* __restrict__ f_ctx, const int* __restrict__ root_token,
+                  const __nv_bfloat16* __restrict__ emb, int V,
+                  __nv_bfloat16* __restrict__ a_out, int* status) {
+  pdl_begin();
+  const int F = (level == 0) ? 1 : k;
+  const int r = blockIdx.x, b = r / F, f = r % F;
+  __shared__ int s_src, s_tok;
+  if (threadIdx.x == 0) {
+    int tok, src;
+    if (level == 0) {
+      tok = root_token[b];
+      src = -1;
+      node_cur[r] = -1;
+    } else {
+      const int q = __ldcg(pool.frontier + (size_t)b * k + f);
+      tok = __ldcg(pool.token + (size_t)b * P + q);
+      const int p = __ldcg(pool.parent + (size_t)b * P + q);
+      src = -2;
+      for (int j = 0; j < F_prev; ++j)
+        if (node_prev[b * F_prev + j] == p) {
+          src = b * F_prev + j;
+          break;
+        }
+      node_cur[r] = q;
+    }
+    if (tok < 0 || tok >= V || src == -2) {
+      fail(status, EAGLE_ERR_INVALID_ARG);
+      tok = 0;
+      src = (level == 0) ? -1 : b * F_prev;
+    }
+    s_src = src;
+    s_tok = tok;
+  }
+  __syncthreads();
+  const __nv_bfloat16* fs = (s_src < 0) ? f_ctx + (size_t)b * H : feat_prev + (size_t)s_src * H;
+  const __nv_bfloat16* es = emb + (size_t)s_tok * H;
+  __nv_bfloat16* dst = a_out + (size_t)r * 2 * H;
+  for (int i = threadIdx.x; i < H; i += blockDim.x) {
+    dst[i] = fs[i];
+    dst[H + i] = es[i];
+  }
+}
+
+}  // namespace
+
+extern "C" eagle_status eagle_draft_head_input(int B, int V, int k, int depth, int level, int H,
+                                               const void* d_pool, size_t pool_bytes,
+                                               const int32_t* d_node_prev, int32_t* d_node_cur,
+                                               const void* d_feat_prev, const void* d_f_ctx,
+                                               const int32_t* d_root_token, const void* d_emb,
+                                               void* d_a, int* d_status, eagle_stream_t stream) {
+  EAGLE_HOST_CHECK(B >= 1 && V >= 1 && H >= 1, EAGLE_ERR_INVALID_ARG);
+  EAGLE_HOST_CHECK(k >= 1 && k <= EAGLE_MAX_TOPK && k <= V, EAGLE_ERR_UNSUPPORTED);
+  EAGLE_HOST_CHECK(depth >= 1 && depth <= EAGLE_MAX_DEPTH && level >= 0 && level < depth,
+                   EAGLE_ERR_INVALID_ARG);
+  EAGLE_HOST_CHECK(d_pool && d_node_cur && d_f_ctx && d_root_token && d_emb && d_a && d_status,
+                   EAGLE_ERR_INVALID_ARG);
+  EAGLE_HOST_CHECK(level == 0 || (d_node_prev && d_feat_prev), EAGLE_ERR_INVALID_ARG);
+  const PoolLayout L = pool_layout(B, k, depth, V);
+  EAGLE_HOST_CHECK(pool_bytes >= L.total, EAGLE_ERR_WORKSPACE);
+  const PoolPtrs pp = pool_ptrs(const_cast<void*>(d_pool), L);
+  const int F = (level == 0) ? 1 : k;
+  const int F_prev = (level <= 1) ? 1 : k;
+  return launch_status(launch_pdl(
+      head_input_kernel, dim3(B * F), dim3(256), 0, (cudaStream_t)stream, pp, k, L.P, H, level,
+      F_prev, d_node_prev, d_node_cur, static_cast<const __nv_bfloat16*>(d_feat_prev),
+      static_cast<const __nv_bfloat16*>(d_f_ctx), d_root_token,
+      static_cast<const __nv_bfloat16*>(d_emb), V, static_cast<__nv_bfloat16*>(d_a), d_status));
 }

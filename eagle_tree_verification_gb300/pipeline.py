@@ -20,7 +20,9 @@ from __future__ import annotations
 import dataclasses
 from typing import Dict, Optional, Sequence
 
-from . import (EPI_ACCUM, EPI_QKV_ROPE, EPI_SWIGLU, SAMPLE_NO_REPLACE, eagle_accept_greedy,
+from . import (EPI_ACCUM, EPI_QKV_ROPE, EPI_STORE, EPI_SWIGLU, SAMPLE_NO_REPLACE,
+               eagle_accept_greedy, eagle_draft_head_input, eagle_draft_rows, eagle_embed_rows,
+               eagle_kv_commit_paged, eagle_loop_advance, eagle_tree_attn_paged,
                eagle_accept_stochastic, eagle_accept_stochastic_logits, eagle_cast_bf16,
                eagle_draft_expand, eagle_draft_pool_bytes, eagle_draft_static, eagle_gemm,
                eagle_lmhead_softmax, eagle_lmhead_workspace_bytes, eagle_rmsnorm,
@@ -82,6 +84,11 @@ class StepShape:
     I: int = 0
     theta: float = 10000.0
     eps: float = 1e-5
+    # paged KV cache: pool of n_pages pages of page_size positions (0: the
+    # packed cache of kv_off)
+    page_size: int = 0
+    n_pages: int = 0
+    max_pages: int = 0
 
     @property
     def builds_tree(self) -> bool:
@@ -166,9 +173,16 @@ class TreeVerifyStep:
             self.bn = z(T, s.H, dtype=bf)
             self.m = z(T, s.I, dtype=bf)
         # resident inputs
-        self.k_cache = z(max(sumL, 1), s.Hkv, s.D, dtype=dt)
-        self.v_cache = z(max(sumL, 1), s.Hkv, s.D, dtype=dt)
-        self.kv_off = z(s.B + 1, dtype=i32)
+        if s.page_size:
+            self.k_pages = z(s.n_pages, s.page_size, s.Hkv, s.D, dtype=dt)
+            self.v_pages = z(s.n_pages, s.page_size, s.Hkv, s.D, dtype=dt)
+            self.block_table = z(s.B, s.max_pages, dtype=i32)
+            self.kv_len = z(s.B, dtype=i32)
+            self.max_kv = s.max_pages * s.page_size
+        else:
+            self.k_cache = z(max(sumL, 1), s.Hkv, s.D, dtype=dt)
+            self.v_cache = z(max(sumL, 1), s.Hkv, s.D, dtype=dt)
+            self.kv_off = z(s.B + 1, dtype=i32)
         self.w_lm = z(s.V, s.H, dtype=dt)
         if s.mode != "stochastic":
             self.p_rows = z(max(s.rows, 1), s.V)
@@ -283,8 +297,9 @@ class TreeVerifyStep:
         RMSNorm that feeds the LM head (h)."""
         s = self.s
         eagle_rmsnorm(self.x, self.g_attn, self.a, self.status, eps=s.eps, stream=stream)
+        cache_len = dict(kv_len=self.kv_len) if s.page_size else dict(kv_off=self.kv_off)
         eagle_tree_rope_table(self.tree_off, self.parent, self.pos, self.cos_sin, self.status,
-                              D=s.D, theta=s.theta, kv_off=self.kv_off, stream=stream)
+                              D=s.D, theta=s.theta, stream=stream, **cache_len)
         eagle_gemm(EPI_QKV_ROPE, self.a, self.w_qkv, self.status, q=self.q, k=self.k_tree,
                    v=self.v_tree, cos_sin=self.cos_sin, Hq=s.Hq, Hkv=s.Hkv, D=s.D, stream=stream)
         self.run_attn(stream)
@@ -297,6 +312,12 @@ class TreeVerifyStep:
         eagle_rmsnorm(self.resid, self.g_final, self.h, self.status, eps=s.eps, stream=stream)
 
     def run_attn(self, stream=None) -> None:
+        if self.s.page_size:
+            eagle_tree_attn_paged(self.q, self.k_tree, self.v_tree, self.k_pages, self.v_pages,
+                                  self.block_table, self.kv_len, self.tree_off, self.parent,
+                                  self.attn_out, self.status, max_nodes=self.max_nodes,
+                                  max_kv=self.max_kv, stream=stream)
+            return
         eagle_tree_attn(self.q, self.k_tree, self.v_tree, self.k_cache, self.v_cache,
                         self.kv_off, self.tree_off, self.parent, self.attn_out, self.status,
                         max_nodes=self.max_nodes, max_kv=self.max_kv, ws=self.attn_ws,
@@ -396,3 +417,169 @@ class TreeVerifyStep:
             self.run(build_tree=build_tree)
         torch.cuda.synchronize()
         return g
+
+
+@dataclasses.dataclass
+class LoopShape:
+    """Sizes of a draft -> verify -> accept -> commit loop (greedy or
+    stochastic acceptance) over B sequences with paged KV caches."""
+    B: int
+    Hq: int
+    Hkv: int
+    D: int
+    H: int
+    I: int
+    V: int
+    k: int                           # EAGLE-2 top-k per expanded node
+    depth: int                       # EAGLE-2 levels
+    budget: Sequence[int]            # draft-token budget per sequence
+    L0: Sequence[int]                # cache length per sequence at the start
+    steps: int                       # steps the page tables are sized for
+    page_size: int = 128
+    theta: float = 10000.0
+    eps: float = 1e-5
+    mode: str = "greedy"
+    temperature: float = 1.0
+
+
+class SpeculativeLoop:
+    """The steps on either side of the verify pass, on the GPU.
+
+    Per step: the EAGLE-2 tree is drafted level by level (draft head input
+    rows, the head's one matrix, the frozen LM head in logits mode, the
+    level's draft rows, the expand level that reads them); the target's one
+    decoder layer verifies the tree over the paged cache, the LM head and
+    the acceptance walk follow; the root and accepted nodes' K/V are
+    committed to the cache and the bonus token becomes the next root.
+    Everything is queued on one stream without host synchronisation.
+
+    The draft head is deliberately small: f' = [f ; e] Wd^T (f the parent's
+    feature, e the embedding of the node's token, Wd [H, 2H]); the root's
+    parent feature is the target's output at the last accepted node."""
+
+    def __init__(self, shape: LoopShape, device: str = "cuda"):
+        import torch
+        self.torch = torch
+        s = self.s = shape
+        dev = torch.device(device)
+        bf, f32, i32 = torch.bfloat16, torch.float32, torch.int32
+        z = lambda *shp, dtype=f32: torch.zeros(shp, dtype=dtype, device=dev)
+        n_nodes = [min(int(b), s.k + (s.depth - 1) * s.k * s.k) + 1 for b in s.budget]
+        cap = [(int(L) + s.steps * (s.depth + 1) + s.page_size - 1) // s.page_size
+               for L in s.L0]
+        self.max_pages = max(cap)
+        self.n_pages = sum(cap)
+        self.step = TreeVerifyStep(StepShape(
+            B=s.B, Hq=s.Hq, Hkv=s.Hkv, D=s.D, H=s.H, V=s.V, L=list(s.L0), n_nodes=n_nodes,
+            rows=s.B * (1 + (s.depth - 1) * s.k), max_depth=s.depth, dtype="bf16", mode=s.mode,
+            temperature=s.temperature, k=s.k, depth=s.depth, budget=list(s.budget), layer=True,
+            I=s.I, theta=s.theta, eps=s.eps, page_size=s.page_size, n_pages=self.n_pages,
+            max_pages=self.max_pages), device=device)
+        st = self.step
+        # a fixed page assignment for the whole run (every sequence owns the
+        # pages its longest possible context needs)
+        table = torch.full((s.B, self.max_pages), -1, dtype=i32)
+        nxt = 0
+        for b in range(s.B):
+            for j in range(cap[b]):
+                table[b, j] = nxt
+                nxt += 1
+        st.block_table.copy_(table)
+        # model state and draft-loop buffers
+        self.emb = z(s.V, s.H, dtype=bf)            # shared token embedding
+        self.w_draft = z(s.H, 2 * s.H, dtype=bf)     # the draft head
+        self.f_ctx = z(s.B, s.H, dtype=bf)           # context feature per sequence
+        self.a_draft = z(s.B * s.k, 2 * s.H, dtype=bf)
+        self.feat = [z(s.B * s.k, s.H, dtype=bf) for _ in range(2)]
+        self.nodes = [z(s.B * s.k, dtype=i32) for _ in range(2)]
+        self.z_draft = z(s.B * s.k, s.V)
+        self.d_argmax = z(s.B * s.k, dtype=i32)
+        self.d_stats = [z(s.B * s.k) for _ in range(3)]
+        self.d_ws = z(max(eagle_lmhead_workspace_bytes(s.B * s.k, s.V), 16), dtype=torch.uint8)
+        if st.draft_logp is None:
+            raise ValueError("the loop builds its tree")
+
+    def load(self, arrays: Dict[str, object], kv: Dict[str, object]) -> None:
+        """Weights (layer weights as TreeVerifyStep.load_layer, w_lm, emb,
+        w_draft), the initial context feature f_ctx, root tokens, and the
+        initial caches kv["k"], kv["v"] as packed [sum L0, Hkv, D] rows with
+        their lengths L0."""
+        torch = self.torch
+        st = self.step
+        st.load_layer(arrays)
+        t = lambda a: a if isinstance(a, torch.Tensor) else torch.from_numpy(a)
+        st.w_lm.copy_(t(arrays["w_lm"]).to(st.w_lm.dtype))
+        self.emb.copy_(t(arrays["emb"]).to(self.emb.dtype))
+        self.w_draft.copy_(t(arrays["w_draft"]).to(self.w_draft.dtype))
+        self.f_ctx.copy_(t(arrays["f_ctx"]).to(self.f_ctx.dtype))
+        st.root_token.copy_(t(arrays["root_token"]).to(torch.int32))
+        st.budget.copy_(torch.tensor(list(self.s.budget), dtype=torch.int32))
+        # scatter the initial caches into the pages (set-up, not a step)
+        k, v = t(kv["k"]), t(kv["v"])
+        table = st.block_table.cpu()
+        P = self.s.page_size
+        off = 0
+        for b, L in enumerate(self.s.L0):
+            for j in range((L + P - 1) // P):
+                n = min(P, L - j * P)
+                page = int(table[b, j])
+                st.k_pages[page, :n].copy_(k[off + j * P: off + j * P + n].to(st.k_pages.dtype))
+                st.v_pages[page, :n].copy_(v[off + j * P: off + j * P + n].to(st.v_pages.dtype))
+            off += L
+        st.kv_len.copy_(torch.tensor(list(self.s.L0), dtype=torch.int32))
+
+    def run_draft(self, stream=None) -> None:
+        s, st = self.s, self.step
+        R = 1 + (s.depth - 1) * s.k
+        logp = st.draft_logp.view(s.B, R, s.V)
+        prob = st.p_rows.view(s.B, R, s.V) if s.mode == "stochastic" else None
+        for lev in range(s.depth):
+            F = 1 if lev == 0 else s.k
+            cur, prev = lev % 2, (lev - 1) % 2
+            eagle_draft_head_input(st.pool, self.nodes[cur], self.f_ctx, st.root_token, self.emb,
+                                   self.a_draft, st.status, B=s.B, V=s.V, k=s.k, depth=s.depth,
+                                   level=lev, node_prev=self.nodes[prev],
+                                   feat_prev=self.feat[prev], stream=stream)
+            feat = self.feat[cur][:s.B * F]
+            eagle_gemm(EPI_STORE, self.a_draft[:s.B * F], self.w_draft, st.status, y=feat,
+                       stream=stream)
+            eagle_lmhead_softmax(feat, st.w_lm, self.d_argmax[:s.B * F],
+                                 self.d_stats[0][:s.B * F], self.d_stats[1][:s.B * F],
+                                 self.d_stats[2][:s.B * F], self.z_draft[:s.B * F], self.d_ws,
+                                 st.status, temperature=1.0, logits=True, stream=stream)
+            eagle_draft_rows(self.z_draft[:s.B * F], self.d_stats[1][:s.B * F], logp, prob,
+                             B=s.B, k=s.k, depth=s.depth, level=lev, stream=stream)
+            last = lev == s.depth - 1
+            eagle_draft_expand(st.pool, st.status, B=s.B, V=s.V, k=s.k, depth=s.depth, level=lev,
+                               finalize=2 if last else 0, draft_logp=st.draft_logp,
+                               budget=st.budget if last else None,
+                               root_token=st.root_token if last else None,
+                               tree_off=st.tree_off if last else None,
+                               parent=st.parent if last else None,
+                               tokens=st.tokens if last else None,
+                               node_depth=st.node_depth if last else None,
+                               score=st.score if last else None,
+                               p_row_of_node=st.p_row_of_node if last else None,
+                               rows_from_previous_kernel=True, stream=stream)
+
+    def run_verify(self, stream=None) -> None:
+        st = self.step
+        eagle_embed_rows(st.tokens, self.emb, st.x, st.status, stream=stream)
+        st.run_layer(stream)
+        st.run_lmhead(stream)
+        st.run_accept(stream)
+
+    def run_commit(self, stream=None) -> None:
+        s, st = self.s, self.step
+        eagle_kv_commit_paged(st.tree_off, st.accept_len, st.accepted_nodes, st.k_tree, st.v_tree,
+                              st.k_pages, st.v_pages, st.block_table, st.kv_len, st.status,
+                              max_depth=s.depth, stream=stream)
+        eagle_loop_advance(st.tree_off, st.accept_len, st.accepted_nodes, st.out_tokens, st.resid,
+                           self.f_ctx, st.root_token, st.status, max_depth=s.depth,
+                           stream=stream)
+
+    def run(self, stream=None) -> None:
+        """One whole step: draft, verify, accept, commit."""
+        self.run_draft(stream)
+        self.run_verify(stream)
+        self.run_commit(stream)

@@ -384,6 +384,73 @@ EAGLE_API eagle_status eagle_draft_expand(int B, int V, int k, int depth, int le
                                 int32_t *d_p_row_of_node, int *d_status,
                                 eagle_stream_t stream);
 
+/* eagle_draft_expand for draft rows written by the kernel queued just before
+ * it on `stream` (the draft head of a draft -> verify loop): the same level
+ * or finalize, with every row read only after that kernel has finished.
+ * (eagle_draft_expand itself starts ranking a level's rows before the
+ * previous kernel ends, which needs rows that were ready earlier.) */
+EAGLE_API eagle_status eagle_draft_expand_dep(int B, int V, int k, int depth, int level,
+                                    int finalize, const float *d_draft_logp,
+                                    const int32_t *d_budget, const int32_t *d_root_token,
+                                    void *d_pool, size_t pool_bytes, int32_t *d_tree_off,
+                                    int32_t *d_parent, int32_t *d_tokens, int32_t *d_node_depth,
+                                    float *d_score, int32_t *d_p_row_of_node, int *d_status,
+                                    eagle_stream_t stream);
+
+/* ------------------------------------------------------------------------
+ * The draft -> verify -> accept -> commit loop.
+ * [EAGLE] workflow paragraph: the draft ("auto-regression") head reads the
+ * target's feature and the embedding of the sampled token and predicts the
+ * next feature; the frozen LM head gives the next-token distribution of
+ * every draft node; the target verifies the whole tree in one pass; the
+ * accepted tokens join the context.  A draft head is [f ; e] -> f' (one
+ * matrix, eagle_gemm STORE) here, the LM head eagle_lmhead_softmax (LOGITS).
+ * ---------------------------------------------------------------------- */
+
+/* Input rows of the draft head for EAGLE-2 level `level` of a tree built by
+ * eagle_draft_expand(_dep) in d_pool (same B, V, k, depth).  Level 0: row b
+ * = [d_f_ctx[b] ; d_emb[d_root_token[b]]] (the root), d_node_cur[b] = -1.
+ * Level d >= 1: the frontier the previous level left, by rank: row b*k + f =
+ * [feature of the node's parent ; d_emb[node's token]], the parent's
+ * feature taken from d_feat_prev [B*F_prev, H] bf16 (the previous call's
+ * head output; F_prev = 1 at d = 1, else k) by matching the parent's pool
+ * index in d_node_prev [B*F_prev]; d_node_cur [B*F] receives the rows' pool
+ * indices.  d_a [B*F, 2H] bf16 (F = 1 at level 0, else k); d_emb [V, H]
+ * bf16; d_f_ctx [B, H] bf16.  Device errors: INVALID_ARG. */
+EAGLE_API eagle_status eagle_draft_head_input(int B, int V, int k, int depth, int level, int H,
+                                    const void *d_pool, size_t pool_bytes,
+                                    const int32_t *d_node_prev, int32_t *d_node_cur,
+                                    const void *d_feat_prev, const void *d_f_ctx,
+                                    const int32_t *d_root_token, const void *d_emb, void *d_a,
+                                    int *d_status, eagle_stream_t stream);
+
+/* Draft rows of one level from the LM head's logits of the level's B*F
+ * draft nodes (d_z [B*F, V] fp32, d_lse [B*F]; F = 1 at level 0, else k):
+ * row r = b*F + f becomes local row 0 (level 0) or 1 + (level-1)*k + f of
+ * sequence b in d_logp [B, R, V] (R = 1 + (depth-1)*k) as z - lse (fp32),
+ * and, if d_prob is given, in d_prob [B, R, V] as the probability with
+ * eagle_lmhead_softmax's PROB-mode expression at temperature 1. */
+EAGLE_API eagle_status eagle_draft_rows(int B, int V, int k, int depth, int level,
+                                        const float *d_z, const float *d_lse, float *d_logp,
+                                        float *d_prob, eagle_stream_t stream);
+
+/* x [T, H] fp32 = d_emb[d_tokens[t]] (bf16 rows): the target's input rows
+ * of the tree tokens.  Device errors: INVALID_ARG (token out of range). */
+EAGLE_API eagle_status eagle_embed_rows(int T, int H, int V, const int32_t *d_tokens,
+                                        const void *d_emb, float *d_x, int *d_status,
+                                        eagle_stream_t stream);
+
+/* After the acceptance walk: the next step's root token is the bonus token
+ * d_out_tokens[b*(max_depth+1) + alpha], and its context feature
+ * d_f_ctx [B, H] bf16 is the target's output (d_resid [T, H] fp32) at the
+ * last accepted node.  Device errors: INVALID_ARG. */
+EAGLE_API eagle_status eagle_loop_advance(int B, int H, int max_depth, const int32_t *d_tree_off,
+                                          const int32_t *d_accept_len,
+                                          const int32_t *d_accepted_nodes,
+                                          const int32_t *d_out_tokens, const float *d_resid,
+                                          void *d_f_ctx, int32_t *d_root_token, int *d_status,
+                                          eagle_stream_t stream);
+
 /* ------------------------------------------------------------------------
  * eagle_draft_static -- EAGLE-1 static draft tree from a fixed template.
  * [EAGLE-2] §2 "EAGLE-2 的核心創新：動態草稿樹" (EAGLE-1's fixed top-k tree,

@@ -84,6 +84,7 @@ __all__ = [
     "lmhead_softmax", "accept_greedy", "accept_stochastic",
     "expand_level", "expand_finalize", "build_eagle2_tree", "f32_of_int",
     "static_template_full", "build_static_tree",
+    "draft_head", "draft_logp_row", "build_eagle2_tree_with_head",
     "bf16_round", "rmsnorm", "rope", "silu", "tree_positions", "decoder_layer",
     "decoder_layer_causal",
 ]
@@ -810,6 +811,56 @@ def build_static_tree(draft_logp, B: int, tmpl_parent, tmpl_rank, tmpl_row, root
     return {"tree_off": tree_off, "parent": cat(par, np.int32), "tokens": cat(tok, np.int32),
             "depth": cat(dep, np.int32), "score": cat(sc, np.float32),
             "p_row_of_node": cat(prow, np.int32)}
+
+
+def draft_head(f_parent, e_token, w_draft):
+    """The draft ("auto-regression") head of the loop: the next feature from
+    the parent's feature and the embedding of the node's token ([EAGLE]
+    workflow paragraph), one matrix: bf16([f ; e] Wd^T), Wd [H, 2H]."""
+    x = np.concatenate([np.asarray(f_parent, np.float64), np.asarray(e_token, np.float64)],
+                       axis=-1)
+    return bf16_round(x @ np.asarray(w_draft, np.float64).T)
+
+
+def draft_logp_row(feature, w_lm):
+    """Draft distribution of a node: the frozen LM head on its feature, as
+    fp32 log-probabilities fp32(z - lse(z)) (z and lse in fp64)."""
+    z = np.asarray(w_lm, np.float64) @ np.asarray(feature, np.float64)
+    m = z.max()
+    lse = m + np.log(np.exp(z - m).sum())
+    return (z - lse).astype(np.float32)
+
+
+def build_eagle2_tree_with_head(f_ctx, root_token, emb, w_draft, w_lm, B: int, k: int,
+                                depth: int, budget, rows=None):
+    """The EAGLE-2 tree drafted level by level: the root's feature is
+    draft_head(f_ctx[b], emb[root token]); every frontier node's feature is
+    draft_head(its parent's feature, emb[its token]); its draft row is
+    draft_logp_row(feature).  Returns (tree, own_rows [B, R, V] fp32).  If
+    `rows` [B, R, V] is given, the tree's decisions read those rows (so a
+    tree built from another implementation's rows can be checked with
+    identical inputs) while own_rows still holds this function's rows,
+    computed on that tree's frontiers."""
+    V = np.asarray(w_lm).shape[0]
+    R = 1 + (depth - 1) * k
+    own = np.zeros((B, R, V), dtype=np.float32)
+    use = own if rows is None else np.asarray(rows, dtype=np.float32).reshape(B, R, V)
+    pools = [_Pool() for _ in range(B)]
+    feats = [dict() for _ in range(B)]      # pool index (-1: root) -> feature
+    for lev in range(depth):
+        for b in range(B):
+            if lev == 0:
+                f = draft_head(f_ctx[b], emb[int(root_token[b])], w_draft)
+                feats[b][-1] = f
+                own[b, 0] = draft_logp_row(f, w_lm)
+            else:
+                pool = pools[b]
+                for r, q in enumerate(pool.frontier):
+                    f = draft_head(feats[b][pool.parent[q]], emb[pool.token[q]], w_draft)
+                    feats[b][q] = f
+                    own[b, 1 + (lev - 1) * k + r] = draft_logp_row(f, w_lm)
+        expand_level(pools, use, lev, k, R)
+    return expand_finalize(pools, budget, root_token, R), own
 
 
 def build_eagle2_tree(draft_logp, B: int, k: int, depth: int, budget, root_token):

@@ -169,7 +169,7 @@ def test_full_layer_matches_oracle(name):
     assert err.max() <= 2e-3
     # the LM head on the layer's output, then the walk on identical inputs
     h_ref = O.bf16_round(O.rmsnorm(ref["out"], lay["g_final"], w.eps))
-    hb = to_np(step.h).astype(np.float64)
+    hb = to_np(step.h.float()).astype(np.float64)
     assert np.mean(np.abs(hb - h_ref) > 2.0 ** -8 * np.abs(h_ref) + 1e-6) < 1e-3
     lm = O.lmhead_softmax(hb, inp["w_lm"], w.temperature, want_q=False)
     gap = lm["top2_gap"]
