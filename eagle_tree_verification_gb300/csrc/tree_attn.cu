@@ -298,7 +298,7 @@ __device__ __forceinline__ void tmem_wait_st() {
 // output accumulator, so the halves never wait for each other inside the
 // key loop and are merged once at the end.  TMEM columns: S at 0 (refilled
 // with the next block as soon as every row has read it), P at 128 (per key
-// half: bf16 hi at +0, lo at +32), O of key half 0 at 256, of half 1 at 384.
+// half: 64 keys as bf16 pairs at +0), O of key half 0 at 256, of half 1 at 384.
 __global__ void __launch_bounds__(kAttThreads, 1)
 tree_attn_tc_kernel(const __grid_constant__ CUtensorMap map_q,
                     const __grid_constant__ CUtensorMap map_kc,
@@ -525,22 +525,19 @@ tree_attn_tc_kernel(const __grid_constant__ CUtensorMap map_q,
           vph ^= 1u << st;
           tc::fence_after_thread_sync();
           const uint32_t v_addr = tc::smem_u32(v_sm + st * kTileBytes);
-          // O_h += P_hi V_h + P_lo V_h for key half h: A = P from the half's
+          // O_h += P_h V_h for key half h: A = P (bf16) from the half's
           // TMEM columns, B = V rows of that half (MN-major, 128-byte rows).
           // The two halves' accumulator chains are interleaved (each in its
           // own order), so the tensor pipe always has an independent MMA.
 #pragma unroll
-          for (int part = 0; part < 2; ++part) {
+          for (int kk = 0; kk < 4; ++kk) {
 #pragma unroll
-            for (int kk = 0; kk < 4; ++kk) {
-#pragma unroll
-              for (int h = 0; h < 2; ++h) {
-                const uint32_t a_tm = tmem + (uint32_t)(128 + h * 64 + part * 32 + kk * 8);
-                const uint32_t key = (uint32_t)(h * 64 + kk * 16);
-                mma_f16_tmem_a(tmem + 256u + (uint32_t)(h * 128), a_tm,
-                               desc_mnmajor_sw128(v_addr + key * 128u, kHalfBytes), idesc_o,
-                               (j > 0 || part > 0 || kk > 0) ? 1u : 0u);
-              }
+            for (int h = 0; h < 2; ++h) {
+              const uint32_t a_tm = tmem + (uint32_t)(128 + h * 64 + kk * 8);
+              const uint32_t key = (uint32_t)(h * 64 + kk * 16);
+              mma_f16_tmem_a(tmem + 256u + (uint32_t)(h * 128), a_tm,
+                             desc_mnmajor_sw128(v_addr + key * 128u, kHalfBytes), idesc_o,
+                             (j > 0 || kk > 0) ? 1u : 0u);
             }
           }
           tc::mma_commit(&sh->pv_done);
@@ -621,30 +618,27 @@ tree_attn_tc_kernel(const __grid_constant__ CUtensorMap map_q,
       const bool first = (m == -INFINITY);
       const bool rescale = !first && (mn > m + kRescaleLog2);
       const float mu = (first || rescale) ? mn : m;     // reference max for this block's P
-      // P = exp2(s - mu) = hi + lo, both bf16: hi keeps the top 16 bits of
-      // the fp32 value, lo = P - hi (exact in fp32) truncated the same way;
-      // |P - hi - lo| < 2^-14 P.  Computed before waiting for the previous
-      // PV, which still reads the P columns.
+      // P = exp2(s - mu) rounded to nearest bf16 for the PV product (at most
+      // 2^-9 relative per weight, so the output moves by at most 2^-9 of
+      // sum_j p_j |v_j| / sum_j p_j); the row sum takes the unrounded
+      // values.  Computed before waiting for the previous PV, which still
+      // reads the P columns.
       float psum = 0.f;
       // a half-row with nothing visible yet keeps mu = -inf: its scores are
       // all -inf, and any finite offset gives P = 0
       const float neg_mu = (mu == -INFINITY) ? 0.f : -mu;
-      uint32_t hi0[16], lo0[16], hi1[16], lo1[16];
-      auto split = [&](const float (&v)[32], uint32_t (&hi)[16], uint32_t (&lo)[16]) {
+      uint32_t pb0[16], pb1[16];
+      auto round_p = [&](const float (&v)[32], uint32_t (&pb)[16]) {
 #pragma unroll
         for (int i = 0; i < 16; ++i) {
           const float p0 = ex2_approx(fmaf(v[2 * i], A.scale_log2, neg_mu));
           const float p1 = ex2_approx(fmaf(v[2 * i + 1], A.scale_log2, neg_mu));
-          const uint32_t b0 = __float_as_uint(p0), b1 = __float_as_uint(p1);
-          hi[i] = __byte_perm(b0, b1, 0x7632);
-          const float r0 = p0 - __uint_as_float(b0 & 0xffff0000u);
-          const float r1 = p1 - __uint_as_float(b1 & 0xffff0000u);
-          lo[i] = __byte_perm(__float_as_uint(r0), __float_as_uint(r1), 0x7632);
+          pb[i] = pack_bf16(p0, p1);
           psum += p0 + p1;
         }
       };
-      split(v0, hi0, lo0);
-      split(v1, hi1, lo1);
+      round_p(v0, pb0);
+      round_p(v1, pb1);
       if (j >= 1) {
         // the previous PV has read P and finished O (every earlier PV was
         // waited for one block before)
@@ -664,12 +658,10 @@ tree_attn_tc_kernel(const __grid_constant__ CUtensorMap map_q,
         }
         l *= f;
       }
-      // hi to the half's P columns +0 .., lo to +32 ..
+      // P of the half's 64 keys (two per 32-bit column) to its P columns
       const uint32_t pcol = trow + (uint32_t)(128 + half * 64);
-      tmem_st_32x32b_x16(pcol, hi0);
-      tmem_st_32x32b_x16(pcol + 16u, hi1);
-      tmem_st_32x32b_x16(pcol + 32u, lo0);
-      tmem_st_32x32b_x16(pcol + 48u, lo1);
+      tmem_st_32x32b_x16(pcol, pb0);
+      tmem_st_32x32b_x16(pcol + 16u, pb1);
       tmem_wait_st();
       l += psum;
       m = mu;

@@ -256,6 +256,40 @@ class TreeVerifyStep:
                                          s.Hq, s.Hkv, s.D))
         self.w_gu.copy_(pack_gate_up_weight(dev(arrays["wg"]), dev(arrays["wu"])))
 
+    def load_paged_cache(self, k, v, lengths: Sequence[int]) -> None:
+        """Scatter packed caches k, v [sum L, Hkv, D] (sequence b's rows
+        after those of the sequences before it) into the pages its block
+        table names, and set kv_len (set-up, not a step)."""
+        torch = self.torch
+        t = lambda a: a if isinstance(a, torch.Tensor) else torch.from_numpy(a)
+        k, v = t(k), t(v)
+        table = self.block_table.cpu()
+        P = self.s.page_size
+        off = 0
+        for b, L in enumerate(lengths):
+            for j in range((int(L) + P - 1) // P):
+                n = min(P, int(L) - j * P)
+                page = int(table[b, j])
+                self.k_pages[page, :n].copy_(k[off + j * P: off + j * P + n].to(self.k_pages.dtype))
+                self.v_pages[page, :n].copy_(v[off + j * P: off + j * P + n].to(self.v_pages.dtype))
+            off += int(L)
+        self.kv_len.copy_(torch.tensor([int(L) for L in lengths], dtype=torch.int32))
+
+    def assign_pages(self, capacity: Sequence[int]) -> None:
+        """A block table giving sequence b the next ceil(capacity[b] /
+        page_size) pages of the pool, in order."""
+        torch = self.torch
+        P = self.s.page_size
+        table = torch.full((self.s.B, self.s.max_pages), -1, dtype=torch.int32)
+        nxt = 0
+        for b, c in enumerate(capacity):
+            for j in range((int(c) + P - 1) // P):
+                table[b, j] = nxt
+                nxt += 1
+        if nxt > self.s.n_pages:
+            raise ValueError("the page pool is too small")
+        self.block_table.copy_(table)
+
     def host_step_inputs(self, arrays: Dict[str, object]):
         """Pinned host buffer laid out like `step_inputs`, filled from host
         arrays named as the step's inputs: one copy moves a whole step."""
@@ -478,13 +512,7 @@ class SpeculativeLoop:
         st = self.step
         # a fixed page assignment for the whole run (every sequence owns the
         # pages its longest possible context needs)
-        table = torch.full((s.B, self.max_pages), -1, dtype=i32)
-        nxt = 0
-        for b in range(s.B):
-            for j in range(cap[b]):
-                table[b, j] = nxt
-                nxt += 1
-        st.block_table.copy_(table)
+        st.assign_pages([c * s.page_size for c in cap])
         # model state and draft-loop buffers
         self.emb = z(s.V, s.H, dtype=bf)            # shared token embedding
         self.w_draft = z(s.H, 2 * s.H, dtype=bf)     # the draft head
@@ -515,18 +543,7 @@ class SpeculativeLoop:
         st.root_token.copy_(t(arrays["root_token"]).to(torch.int32))
         st.budget.copy_(torch.tensor(list(self.s.budget), dtype=torch.int32))
         # scatter the initial caches into the pages (set-up, not a step)
-        k, v = t(kv["k"]), t(kv["v"])
-        table = st.block_table.cpu()
-        P = self.s.page_size
-        off = 0
-        for b, L in enumerate(self.s.L0):
-            for j in range((L + P - 1) // P):
-                n = min(P, L - j * P)
-                page = int(table[b, j])
-                st.k_pages[page, :n].copy_(k[off + j * P: off + j * P + n].to(st.k_pages.dtype))
-                st.v_pages[page, :n].copy_(v[off + j * P: off + j * P + n].to(st.v_pages.dtype))
-            off += L
-        st.kv_len.copy_(torch.tensor(list(self.s.L0), dtype=torch.int32))
+        st.load_paged_cache(kv["k"], kv["v"], self.s.L0)
 
     def run_draft(self, stream=None) -> None:
         s, st = self.s, self.step
