@@ -256,13 +256,14 @@ constexpr int kTileRows = 128;    // tree rows per CTA (the MMA's M)
 #define EAGLE_LMHEAD_MAX_CLUSTER 8
 #endif
 constexpr int kMaxCluster = EAGLE_LMHEAD_MAX_CLUSTER;
-constexpr int kMaxHStages = 4;
+constexpr int kMaxHStages = 6;       // h ring barriers held (stages used: 4 or kBigHStages)
 // h stages of a CTA that takes the whole shared memory (a build-time option,
 // so that the split between the h and W rings can be measured)
 #ifndef EAGLE_LMHEAD_BIG_HSTAGES
 #define EAGLE_LMHEAD_BIG_HSTAGES 4
 #endif
 constexpr int kBigHStages = EAGLE_LMHEAD_BIG_HSTAGES;
+static_assert(kBigHStages >= 1 && kBigHStages <= kMaxHStages, "h stages beyond the barriers held");
 constexpr int kMaxWStages = 12;
 constexpr size_t kSmemLimit = 227 * 1024;
 // A W ring within this budget (when it still holds four stages) leaves room
@@ -282,6 +283,8 @@ struct TcShared {
   Partial xchg[128];   // column half 1's partial of every row
 };
 
+static_assert(sizeof(TcShared) <= kTcSharedBytes, "TcShared must fit its shared-memory slot");
+
 struct TcLayout {
   int h_rows, h_stage_bytes, h_stages, blk, w_stage_bytes, w_stages;
   size_t smem;
@@ -295,7 +298,7 @@ TcLayout tc_layout(int h_rows) {
   // 256-row blocks: narrower MMAs cost more shared-memory reads per W byte
   // than the overlap of a short slice's epilogue gains
   L.blk = kBlkMax;
-  L.h_stages = kMaxHStages;
+  L.h_stages = 4;
   L.w_stage_bytes = L.blk * 128;
   size_t fixed = 1024 + (size_t)L.h_stages * L.h_stage_bytes + kTcSharedBytes;
   size_t limit = kSmemShared;

@@ -840,10 +840,15 @@ def build_eagle2_tree_with_head(f_ctx, root_token, emb, w_draft, w_lm, B: int, k
     `rows` [B, R, V] is given, the tree's decisions read those rows (so a
     tree built from another implementation's rows can be checked with
     identical inputs) while own_rows still holds this function's rows,
-    computed on that tree's frontiers."""
+    computed on that tree's frontiers.  Also returns scale [B, R]: for each
+    row, sum_i |f_i| max_j |w_lm[j, i]|, the most a logit of the row moves
+    per unit of relative change of every feature entry (the scale against
+    which another implementation's rounding of the feature is measured)."""
     V = np.asarray(w_lm).shape[0]
     R = 1 + (depth - 1) * k
     own = np.zeros((B, R, V), dtype=np.float32)
+    scale = np.zeros((B, R))
+    wmax = np.abs(np.asarray(w_lm, np.float64)).max(axis=0)
     use = own if rows is None else np.asarray(rows, dtype=np.float32).reshape(B, R, V)
     pools = [_Pool() for _ in range(B)]
     feats = [dict() for _ in range(B)]      # pool index (-1: root) -> feature
@@ -853,14 +858,16 @@ def build_eagle2_tree_with_head(f_ctx, root_token, emb, w_draft, w_lm, B: int, k
                 f = draft_head(f_ctx[b], emb[int(root_token[b])], w_draft)
                 feats[b][-1] = f
                 own[b, 0] = draft_logp_row(f, w_lm)
+                scale[b, 0] = np.abs(f) @ wmax
             else:
                 pool = pools[b]
                 for r, q in enumerate(pool.frontier):
                     f = draft_head(feats[b][pool.parent[q]], emb[pool.token[q]], w_draft)
                     feats[b][q] = f
                     own[b, 1 + (lev - 1) * k + r] = draft_logp_row(f, w_lm)
+                    scale[b, 1 + (lev - 1) * k + r] = np.abs(f) @ wmax
         expand_level(pools, use, lev, k, R)
-    return expand_finalize(pools, budget, root_token, R), own
+    return expand_finalize(pools, budget, root_token, R), own, scale
 
 
 def build_eagle2_tree(draft_logp, B: int, k: int, depth: int, budget, root_token):

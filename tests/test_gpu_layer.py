@@ -10,7 +10,7 @@ Tolerances (bf16 operands, fp32 accumulation; derived from the arithmetic):
     accumulation's rounding, a small multiple of 2^-24 * sum_k |a_k w_k|:
     checked at 1e-4 of that magnitude;
   * a bf16 result may in addition land on the other side of a rounding
-    boundary: one bf16 step, 2^-8 of its magnitude;
+    boundary: one bf16 step, at most 2^-7 of its magnitude;
   * the whole layer's output, against the scale of the terms that make it
     (|x| + |o|.|Wo| + |m|.|Wd|, the oracle's out_abs): 2e-3, the bf16
     tolerance of the attention."""
@@ -39,7 +39,7 @@ def _bf_ok(got, ref, scale):
     """bf16 results: within one bf16 step of the exact value, plus the
     accumulation's share."""
     got = np.asarray(got, np.float64)
-    return np.abs(got - ref) <= 2.0 ** -8 * np.abs(ref) + 1e-4 * scale
+    return np.abs(got - ref) <= 2.0 ** -7 * np.abs(ref) + 1e-4 * scale
 
 
 @pytest.mark.parametrize("T,K,N", [(1, 256, 64), (65, 4096, 6144), (200, 1024, 4096),
@@ -161,16 +161,20 @@ def test_full_layer_matches_oracle(name):
     for nm, t in (("q", step.q), ("k", step.k_tree), ("v", step.v_tree)):
         g = to_np(t.float()).astype(np.float64)
         r = ref[nm]
-        bad = np.abs(g - r) > 2.0 ** -8 * np.abs(r) + 1e-3 * np.abs(r).mean()
+        bad = np.abs(g - r) > 2.0 ** -7 * np.abs(r) + 1e-3 * np.abs(r).mean()
         assert bad.mean() < 1e-3, (nm, bad.mean())
     out = to_np(step.resid).astype(np.float64)
     err = np.abs(out - ref["out"]) / np.maximum(np.abs(ref["out"]), ref["out_abs"])
     print(f"[layer error] {name}: max |g-r|/max(|r|, out_abs) = {err.max():.3e}")
     assert err.max() <= 2e-3
     # the LM head on the layer's output, then the walk on identical inputs
+    # the final norm: the layer output's error (bounded above) scaled by the
+    # norm, plus one bf16 step of the rounded result
     h_ref = O.bf16_round(O.rmsnorm(ref["out"], lay["g_final"], w.eps))
     hb = to_np(step.h.float()).astype(np.float64)
-    assert np.mean(np.abs(hb - h_ref) > 2.0 ** -8 * np.abs(h_ref) + 1e-6) < 1e-3
+    inv = 1.0 / np.sqrt(np.mean(ref["out"] ** 2, axis=1, keepdims=True) + w.eps)
+    tol = 2.0 ** -7 * np.abs(h_ref) + 2e-3 * ref["out_abs"] * inv * np.abs(lay["g_final"])
+    assert np.all(np.abs(hb - h_ref) <= tol)
     lm = O.lmhead_softmax(hb, inp["w_lm"], w.temperature, want_q=False)
     gap = lm["top2_gap"]
     am = to_np(step.argmax)

@@ -81,8 +81,9 @@ def test_loop_steps_match_the_oracle():
         torch.cuda.synchronize()
         assert int(st.status.item()) == 0
         rows = to_np(st.draft_logp).reshape(B, R, V)
-        tree, own = O.build_eagle2_tree_with_head(f_ctx, root, w["emb"], w["w_draft"], w["w_lm"],
-                                                  B, k, depth, budget, rows=rows)
+        tree, own, scale = O.build_eagle2_tree_with_head(f_ctx, root, w["emb"], w["w_draft"],
+                                                         w["w_lm"], B, k, depth, budget,
+                                                         rows=rows)
         for nm in ("tree_off", "parent", "tokens", "p_row_of_node"):
             np.testing.assert_array_equal(to_np(getattr(st, nm)), tree[nm], err_msg=nm)
         used = np.zeros((B, R), bool)                      # rows the draft filled
@@ -90,7 +91,11 @@ def test_loop_steps_match_the_oracle():
         for b in range(B):
             p = tree["p_row_of_node"][tree["tree_off"][b]:tree["tree_off"][b + 1]]
             used[b, p[p >= 0] - b * R] = True
-        assert np.abs(rows[used] - own[used]).max() <= 1e-3
+        # a feature entry that lands on the other side of a bf16 rounding
+        # boundary moves by one bf16 step (at most 2^-7 of itself): a logit by
+        # at most 2^-7 sum_i |f_i| max_j |w_ji|, a log-prob by twice that
+        diff = np.abs(rows - own).max(axis=-1)
+        assert np.all(diff[used] <= 2 * 2.0 ** -7 * scale[used] + 1e-5)
         # ---- verify
         loop.run_verify()
         torch.cuda.synchronize()

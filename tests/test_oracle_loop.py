@@ -39,12 +39,14 @@ def test_level_by_level_tree_equals_the_tree_of_its_own_rows():
     f_ctx = O.bf16_round(g.standard_normal((B, H)))
     root = [5, 9]
     budget = [10, 7]
-    tree, rows = O.build_eagle2_tree_with_head(f_ctx, root, emb, wd, wl, B, k, depth, budget)
+    tree, rows, scale = O.build_eagle2_tree_with_head(f_ctx, root, emb, wd, wl, B, k, depth,
+                                                      budget)
+    assert np.all(scale[:, 0] > 0)
     ref = O.build_eagle2_tree(rows, B=B, k=k, depth=depth, budget=budget, root_token=root)
     for key in ("tree_off", "parent", "tokens", "depth", "score", "p_row_of_node"):
         np.testing.assert_array_equal(tree[key], ref[key], err_msg=key)
-    tree2, rows2 = O.build_eagle2_tree_with_head(f_ctx, root, emb, wd, wl, B, k, depth, budget,
-                                                 rows=rows)
+    tree2, rows2, _ = O.build_eagle2_tree_with_head(f_ctx, root, emb, wd, wl, B, k, depth,
+                                                    budget, rows=rows)
     np.testing.assert_array_equal(rows2, rows)
     np.testing.assert_array_equal(tree2["tokens"], tree["tokens"])
     # the root's row is the head applied to the context and the root token
