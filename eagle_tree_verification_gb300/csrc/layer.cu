@@ -132,13 +132,13 @@ constexpr int kGThreads = 320;   // warp 0 TMA, warp 1 MMA, warps 2-9 epilogue
 constexpr int kGEpiWarps = 8;    // two per TMEM lane quarter, one per column half
 constexpr int kGBK = 64;         // bf16 per 128-byte swizzled row (one K chunk)
 constexpr int kGUnit = 32;       // W rows per TMA box (and per epilogue chunk)
-constexpr int kGBlk = 256;       // W rows per MMA (its N), at most
+constexpr int kGBlk = 256;       // W rows per MMA (its N), at most; TMEM accumulator stride
 constexpr int kGTile = 128;      // tree rows per CTA (the MMA's M)
 constexpr int kGMaxCluster = 8;
 constexpr int kGHStages = 4;
-constexpr int kGMaxWStages = 12;
+constexpr int kGMaxWStages = 48;   // a slice of few W rows streams through many small stages
 constexpr size_t kGSmemLimit = 227 * 1024;
-constexpr size_t kGShared = 1024;
+constexpr size_t kGShared = 2048;
 
 enum Epi { EPI_STORE = 0, EPI_ACCUM = 1, EPI_SWIGLU = 2, EPI_QKV_ROPE = 3 };
 
@@ -155,6 +155,7 @@ static_assert(sizeof(GemmShared) <= kGShared, "GemmShared must fit its slot");
 struct GemmArgs {
   int T, N, K, C;           // rows, W rows, reduction length, CTAs per cluster
   int n_units, w_stages, h_stage_bytes;
+  int blk_max;              // W rows per block (and per W stage), a multiple of 32, <= 256
   int epi;
   // outputs of the epilogues
   __nv_bfloat16* y;         // STORE [T, N]; SWIGLU [T, N/2]
@@ -264,7 +265,8 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap map_a, const __grid_constant_
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~(uintptr_t)1023);
   unsigned char* h_smem = base;
   unsigned char* w_smem = base + kGHStages * A.h_stage_bytes;
-  const int w_stage_bytes = kGBlk * 128;
+  const int blk_max = A.blk_max;
+  const int w_stage_bytes = blk_max * 128;
   const int w_stages = A.w_stages;
   GemmShared* sh = reinterpret_cast<GemmShared*>(w_smem + (size_t)w_stages * w_stage_bytes);
 
@@ -277,11 +279,11 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap map_a, const __grid_constant_
   const int u0 = (int)((long long)A.n_units * slice / slices);
   const int u1 = (int)((long long)A.n_units * (slice + 1) / slices);
   const int r_begin = u0 * kGUnit, r_end = u1 * kGUnit;
-  const int n_blocks = (r_end - r_begin + kGBlk - 1) / kGBlk;
+  const int n_blocks = (r_end - r_begin + blk_max - 1) / blk_max;
   const int KB = (A.K + kGBK - 1) / kGBK;
   const int total = n_blocks * KB;
   int* status = A.status;
-  auto blk_rows = [&](int blk) { return min(kGBlk, r_end - (r_begin + blk * kGBlk)); };
+  auto blk_rows = [&](int blk) { return min(blk_max, r_end - (r_begin + blk * blk_max)); };
   auto load_w = [&](int stage, int rows, int kb, int y0, uint64_t pol) {
     tc::mbar_arrive_expect_tx(&sh->w_full[stage], (uint32_t)(rows * 128));
     unsigned char* dst = w_smem + (size_t)stage * w_stage_bytes;
@@ -323,7 +325,7 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap map_a, const __grid_constant_
     const uint64_t pol_w = tc::policy_evict_first();
     for (int i = 0; i < w_early; ++i) {
       const int blk = i / KB;
-      load_w(i, blk_rows(blk), i - blk * KB, r_begin + blk * kGBlk, pol_w);
+      load_w(i, blk_rows(blk), i - blk * KB, r_begin + blk * blk_max, pol_w);
     }
   }
   if (warp == 1) {
@@ -347,7 +349,7 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap map_a, const __grid_constant_
       int i = 0;
       for (int blk = 0; blk < n_blocks && ok; ++blk) {
         const int rows = blk_rows(blk);
-        const int y0 = r_begin + blk * kGBlk;
+        const int y0 = r_begin + blk * blk_max;
         for (int kb = 0; kb < KB && ok; ++kb, ++i) {
           if (!(ok = tc::mbar_wait(&sh->h_empty[hs], hph ^ 1, abort_flag, status))) break;
           tc::mbar_arrive_expect_tx(&sh->h_full[hs], (uint32_t)A.h_stage_bytes);
@@ -433,13 +435,14 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap map_a, const __grid_constant_
       if (!__all_sync(0xffffffffu, got)) break;
       tph ^= 1u << ab;
       tc::fence_after_thread_sync();
-      const int half_cols = kGBlk / 2;
+      // two warps per lane quarter split a block's columns at a multiple of 32
+      const int half_cols = ((blk_max / 2 + kGUnit - 1) / kGUnit) * kGUnit;
       for (int c = chalf * half_cols; c < (chalf + 1) * half_cols && c < rows && quad_live;
            c += kGUnit) {
         float v[32];
         tc::tmem_ld_32x32b_x32(tmem + ((uint32_t)(quad * 32) << 16) +
                                    (uint32_t)(ab * kGBlk + c), v);
-        if (row_ok) gemm_epilogue(A, t, r_begin + blk * kGBlk + c, v);
+        if (row_ok) gemm_epilogue(A, t, r_begin + blk * blk_max + c, v);
       }
       tc::fence_before_thread_sync();
       __syncwarp();
@@ -495,16 +498,20 @@ int g_sm_count() {
 }
 
 struct GLayout {
-  int h_stage_bytes, w_stages;
+  int h_stage_bytes, w_stages, blk;
   size_t smem;
 };
 
-GLayout g_layout(int h_rows) {
+// `blk`: W rows per block (a multiple of 32); the W ring gets every byte
+// left, in as many stages as fit, so that a slice of few rows still keeps
+// enough bytes in flight.
+GLayout g_layout(int h_rows, int blk) {
   GLayout L;
   L.h_stage_bytes = h_rows * 128;
+  L.blk = blk;
   const size_t fixed = 1024 + (size_t)kGHStages * L.h_stage_bytes + kGShared;
-  L.w_stages = (int)std::min<size_t>(kGMaxWStages, (kGSmemLimit - fixed) / (kGBlk * 128));
-  L.smem = fixed + (size_t)L.w_stages * kGBlk * 128;
+  L.w_stages = (int)std::min<size_t>(kGMaxWStages, (kGSmemLimit - fixed) / ((size_t)blk * 128));
+  L.smem = fixed + (size_t)L.w_stages * blk * 128;
   return L;
 }
 
@@ -553,7 +560,7 @@ eagle_status gemm_launch(int T, int N, int K, const void* d_a, const void* d_w, 
   if (!g_map(&map_w, d_w, N, K, kGUnit)) return EAGLE_ERR_CUDA;
   const int n_units = N / kGUnit;
   const int tiles = (T + kGTile - 1) / kGTile;
-  const GLayout TL = g_layout(kGTile);
+  const GLayout TL = g_layout(kGTile, kGBlk);
   int passes = 1, C = tiles;
   while (C > 1 && (C > kGMaxCluster || g_max_clusters(C, TL.smem) < 1)) {
     ++passes;
@@ -567,7 +574,9 @@ eagle_status gemm_launch(int T, int N, int K, const void* d_a, const void* d_w, 
     const int Ts = std::min(nt * kGTile, T - r0);
     tile0 += nt;
     const int Cp = (C > 1) ? nt : 1;
-    const GLayout L = g_layout((Cp > 1 || Ts > kGTile) ? kGTile : ((Ts + 7) / 8) * 8);
+    const int slice_units = (n_units + slices - 1) / slices;
+    const GLayout L = g_layout((Cp > 1 || Ts > kGTile) ? kGTile : ((Ts + 7) / 8) * 8,
+                               std::min(kGBlk, slice_units * kGUnit));
     CUtensorMap map_a;
     const __nv_bfloat16* ap = static_cast<const __nv_bfloat16*>(d_a) + (size_t)r0 * K;
     if (!g_map(&map_a, ap, Ts, K, L.h_stage_bytes / 128)) return EAGLE_ERR_CUDA;
@@ -579,6 +588,7 @@ eagle_status gemm_launch(int T, int N, int K, const void* d_a, const void* d_w, 
     P.n_units = n_units;
     P.w_stages = L.w_stages;
     P.h_stage_bytes = L.h_stage_bytes;
+    P.blk_max = L.blk;
     // the pass's rows: shift every row-indexed output
     if (P.y) P.y += (size_t)r0 * (A.epi == EPI_SWIGLU ? N / 2 : N);
     if (P.acc_out) P.acc_out += (size_t)r0 * N;

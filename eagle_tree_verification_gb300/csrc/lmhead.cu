@@ -264,6 +264,12 @@ constexpr int kMaxHStages = 6;       // h ring barriers held (stages used: 4 or 
 #endif
 constexpr int kBigHStages = EAGLE_LMHEAD_BIG_HSTAGES;
 static_assert(kBigHStages >= 1 && kBigHStages <= kMaxHStages, "h stages beyond the barriers held");
+// Cluster launches (row tiles sharing W) use 512-row blocks over both TMEM
+// accumulators (a build-time option, so that 256-row blocks can be measured)
+#ifndef EAGLE_LMHEAD_DUAL
+#define EAGLE_LMHEAD_DUAL 1
+#endif
+constexpr bool kDualCluster = EAGLE_LMHEAD_DUAL != 0;
 constexpr int kMaxWStages = 12;
 constexpr size_t kSmemLimit = 227 * 1024;
 // A W ring within this budget (when it still holds four stages) leaves room
@@ -345,7 +351,13 @@ __device__ __forceinline__ void merge_partial(Partial& a, const Partial& b, floa
 
 // T: tree rows of this launch (at most 128 * C); C: CTAs per cluster, 1
 // exactly when MULTI is false.  Partials go to part[t * slices + slice].
-template <bool MULTI>
+// DUAL: a block is blk_max = 512 vocabulary rows, its two 256-row halves
+// accumulated in the two TMEM accumulators by turns for every h chunk, so
+// each h chunk serves twice the MMA work (half the h traffic and twice the
+// time to refill an h stage); the epilogue of a block then no longer
+// overlaps the next block's MMAs.  Otherwise a block is one accumulator and
+// consecutive blocks alternate.
+template <bool MULTI, bool DUAL>
 __global__ void __launch_bounds__(kTcThreads, 1)
 lmhead_tc_kernel(const __grid_constant__ CUtensorMap map_h, const __grid_constant__ CUtensorMap map_w,
                  int T, int H, int V, float temperature, float* __restrict__ z_out,
@@ -356,7 +368,8 @@ lmhead_tc_kernel(const __grid_constant__ CUtensorMap map_h, const __grid_constan
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~(uintptr_t)1023);
   unsigned char* h_smem = base;
   unsigned char* w_smem = base + h_stages * h_stage_bytes;
-  const int w_stage_bytes = blk_max * 128;
+  const int w_rows_max = DUAL ? blk_max / 2 : blk_max;   // W rows of one stage
+  const int w_stage_bytes = w_rows_max * 128;
   TcShared* sh = reinterpret_cast<TcShared*>(w_smem + (size_t)w_stages * w_stage_bytes);
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -371,8 +384,13 @@ lmhead_tc_kernel(const __grid_constant__ CUtensorMap map_h, const __grid_constan
   const int r_begin = u0 * kUnit, r_end = u1 * kUnit;
   const int n_blocks = (r_end - r_begin + blk_max - 1) / blk_max;
   const int KB = (H + kBK - 1) / kBK;
-  const int total = n_blocks * KB;   // (block, chunk) pairs, block-major
   auto blk_rows = [&](int blk) { return min(blk_max, r_end - (r_begin + blk * blk_max)); };
+  // W stages of a block's chunk (halves with rows), their rows and first row
+  auto n_halves = [&](int blk) { return (DUAL && blk_rows(blk) > w_rows_max) ? 2 : 1; };
+  auto half_rows = [&](int blk, int hf) { return min(w_rows_max, blk_rows(blk) - hf * w_rows_max); };
+  auto half_y0 = [&](int blk, int hf) { return r_begin + blk * blk_max + hf * w_rows_max; };
+  // W stages in all, (block, chunk, half) block-major
+  const int total = n_blocks == 0 ? 0 : ((n_blocks - 1) * n_halves(0) + n_halves(n_blocks - 1)) * KB;
   // this CTA's share of a W stage (chunk kb of the block at row y0):
   // boxes rank, rank + C, ... (multicast to all)
   auto load_w_box = [&](int stage, int rows, int kb, int y0, uint64_t pol) {
@@ -415,10 +433,11 @@ lmhead_tc_kernel(const __grid_constant__ CUtensorMap map_h, const __grid_constan
     tc::prefetch_tensormap(&map_h);
     tc::prefetch_tensormap(&map_w);
     const uint64_t pol_w = tc::policy_evict_first();
-    for (int i = 0; i < w_early; ++i) {
-      const int blk = i / KB;
-      load_w_box(i, blk_rows(blk), i - blk * KB, r_begin + blk * blk_max, pol_w);
-    }
+    int i = 0;
+    for (int blk = 0; blk < n_blocks && i < w_early; ++blk)
+      for (int kb = 0; kb < KB && i < w_early; ++kb)
+        for (int hf = 0; hf < n_halves(blk) && i < w_early; ++hf, ++i)
+          load_w_box(i, half_rows(blk, hf), kb, half_y0(blk, hf), pol_w);
   }
   if (warp == 1) {
     tc::tmem_alloc(&sh->tmem_base, 512);
@@ -443,21 +462,22 @@ lmhead_tc_kernel(const __grid_constant__ CUtensorMap map_h, const __grid_constan
       bool ok = true;
       int i = 0;
       for (int blk = 0; blk < n_blocks && ok; ++blk) {
-        const int rows = blk_rows(blk);
-        const int y0 = r_begin + blk * blk_max;
-        for (int kb = 0; kb < KB && ok; ++kb, ++i) {
+        const int nh = n_halves(blk);
+        for (int kb = 0; kb < KB && ok; ++kb) {
           if (!(ok = tc::mbar_wait(&sh->h_empty[hs], hph ^ 1, abort_flag, status))) break;
           tc::mbar_arrive_expect_tx(&sh->h_full[hs], (uint32_t)h_stage_bytes);
           tc::tma_load_2d_hint(h_smem + hs * h_stage_bytes, &map_h, &sh->h_full[hs], kb * kBK,
                                rank * kTileRows, pol_h);
           ++issued_h;
           if (++hs == h_stages) { hs = 0; hph ^= 1; }
-          if (i >= w_early) {
-            if (!(ok = tc::mbar_wait(&sh->w_empty[ws], wph ^ 1, abort_flag, status))) break;
-            load_w_box(ws, rows, kb, y0, pol_w);
-            ++issued_w;
+          for (int hf = 0; hf < nh && ok; ++hf, ++i) {
+            if (i >= w_early) {
+              if (!(ok = tc::mbar_wait(&sh->w_empty[ws], wph ^ 1, abort_flag, status))) break;
+              load_w_box(ws, half_rows(blk, hf), kb, half_y0(blk, hf), pol_w);
+              ++issued_w;
+            }
+            if (++ws == w_stages) { ws = 0; wph ^= 1; }
           }
-          if (++ws == w_stages) { ws = 0; wph ^= 1; }
         }
       }
       if (ok && MULTI) {
@@ -484,33 +504,38 @@ lmhead_tc_kernel(const __grid_constant__ CUtensorMap map_h, const __grid_constan
       uint32_t hph = 0, wph = 0, tph = 0;   // tph bit b: phase of accumulator b
       bool ok = true;
       for (int blk = 0; blk < n_blocks && ok; ++blk) {
-        const int ab = blk & 1;
+        const int ab = DUAL ? 0 : (blk & 1);
         if (!(ok = tc::mbar_wait(&sh->tmem_empty[ab], ((tph >> ab) & 1u) ^ 1u, abort_flag,
                                  status)))
           break;
         tph ^= 1u << ab;
         tc::fence_after_thread_sync();
-        const uint32_t idesc = tc::idesc_bf16_f32(128, blk_rows(blk));
-        const uint32_t d = tmem + (uint32_t)(ab * kBlkMax);
+        const int nh = n_halves(blk);
         for (int kb = 0; kb < KB && ok; ++kb) {
           if (!(ok = tc::mbar_wait(&sh->h_full[hs], hph, abort_flag, status))) break;
-          if (!(ok = tc::mbar_wait(&sh->w_full[ws], wph, abort_flag, status))) break;
-          tc::fence_after_thread_sync();
           const uint32_t a_base = tc::smem_u32(h_smem + hs * h_stage_bytes);
-          const uint32_t b_base = tc::smem_u32(w_smem + (size_t)ws * w_stage_bytes);
+          for (int hf = 0; hf < nh && ok; ++hf) {
+            if (!(ok = tc::mbar_wait(&sh->w_full[ws], wph, abort_flag, status))) break;
+            tc::fence_after_thread_sync();
+            // DUAL: half hf accumulates at TMEM column 256 * hf
+            const uint32_t d = tmem + (uint32_t)((ab + hf) * kBlkMax);
+            const uint32_t idesc = tc::idesc_bf16_f32(128, half_rows(blk, hf));
+            const uint32_t b_base = tc::smem_u32(w_smem + (size_t)ws * w_stage_bytes);
 #pragma unroll
-          for (int k16 = 0; k16 < kBK / 16; ++k16)
-            tc::mma_f16(d, tc::desc_kmajor_sw128(a_base + k16 * 32),
-                        tc::desc_kmajor_sw128(b_base + k16 * 32), idesc,
-                        (kb > 0 || k16 > 0) ? 1u : 0u);
-          if (MULTI)
-            tc::mma_commit_mc(&sh->w_empty[ws], all_ctas);
-          else
-            tc::mma_commit(&sh->w_empty[ws]);
+            for (int k16 = 0; k16 < kBK / 16; ++k16)
+              tc::mma_f16(d, tc::desc_kmajor_sw128(a_base + k16 * 32),
+                          tc::desc_kmajor_sw128(b_base + k16 * 32), idesc,
+                          (kb > 0 || k16 > 0) ? 1u : 0u);
+            if (MULTI)
+              tc::mma_commit_mc(&sh->w_empty[ws], all_ctas);
+            else
+              tc::mma_commit(&sh->w_empty[ws]);
+            *(volatile int*)&sh->consumed_w += 1;
+            if (++ws == w_stages) { ws = 0; wph ^= 1; }
+          }
+          if (!ok) break;
           tc::mma_commit(&sh->h_empty[hs]);
-          *(volatile int*)&sh->consumed_w += 1;
           *(volatile int*)&sh->consumed_h += 1;
-          if (++ws == w_stages) { ws = 0; wph ^= 1; }
           if (++hs == h_stages) { hs = 0; hph ^= 1; }
         }
         if (ok) tc::mma_commit(&sh->tmem_full[ab]);
@@ -537,7 +562,7 @@ lmhead_tc_kernel(const __grid_constant__ CUtensorMap map_h, const __grid_constan
     bool bad = false;
     uint32_t tph = 0;
     for (int blk = 0; blk < n_blocks; ++blk) {
-      const int ab = blk & 1;
+      const int ab = DUAL ? 0 : (blk & 1);
       const int rows = blk_rows(blk);
       // every lane waits; the warp proceeds only if all of them saw the phase
       const bool got = tc::mbar_wait(&sh->tmem_full[ab], (tph >> ab) & 1u, abort_flag, status);
@@ -700,7 +725,8 @@ int max_clusters(int C, size_t smem) {
     cfg.attrs = attr;
     cfg.numAttrs = 1;
     int n = 0;
-    if (cudaOccupancyMaxActiveClusters(&n, (const void*)lmhead_tc_kernel<true>, &cfg) !=
+    if (cudaOccupancyMaxActiveClusters(&n, (const void*)lmhead_tc_kernel<true, kDualCluster>,
+                                       &cfg) !=
         cudaSuccess) {
       cudaGetLastError();
       n = 0;
@@ -728,8 +754,10 @@ cudaError_t launch_tc(int C, dim3 grid, size_t smem, cudaStream_t s, Args&&... a
   attr[1].val.clusterDim.z = 1;
   cfg.attrs = attr;
   cfg.numAttrs = (C > 1) ? 2 : 1;
-  return (C > 1) ? cudaLaunchKernelEx(&cfg, lmhead_tc_kernel<true>, std::forward<Args>(args)...)
-                 : cudaLaunchKernelEx(&cfg, lmhead_tc_kernel<false>, std::forward<Args>(args)...);
+  return (C > 1) ? cudaLaunchKernelEx(&cfg, lmhead_tc_kernel<true, kDualCluster>,
+                                      std::forward<Args>(args)...)
+                 : cudaLaunchKernelEx(&cfg, lmhead_tc_kernel<false, false>,
+                                      std::forward<Args>(args)...);
 }
 
 }  // namespace
@@ -774,14 +802,14 @@ extern "C" eagle_status eagle_lmhead_softmax(eagle_dtype dtype, int T, int H, in
     // the whole unified L1 as shared memory, so that a CTA of the
     // concurrently running tree expand fits beside this one
     if (attr_once.run([] {
-          cudaError_t e = cudaFuncSetAttribute(lmhead_tc_kernel<false>,
+          cudaError_t e = cudaFuncSetAttribute(lmhead_tc_kernel<false, false>,
                                                cudaFuncAttributeMaxDynamicSharedMemorySize,
                                                (int)kSmemLimit);
           if (e == cudaSuccess)
-            e = cudaFuncSetAttribute(lmhead_tc_kernel<true>,
+            e = cudaFuncSetAttribute(lmhead_tc_kernel<true, kDualCluster>,
                                      cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kSmemLimit);
           if (e == cudaSuccess)
-            e = cudaFuncSetAttribute(lmhead_tc_kernel<false>,
+            e = cudaFuncSetAttribute(lmhead_tc_kernel<false, false>,
                                      cudaFuncAttributePreferredSharedMemoryCarveout,
                                      cudaSharedmemCarveoutMaxShared);
           return e;
@@ -818,7 +846,9 @@ extern "C" eagle_status eagle_lmhead_softmax(eagle_dtype dtype, int T, int H, in
       // (its clusters are smaller, so they are resident too)
       if (launch_tc(Cp, dim3(slices * Cp), TL.smem, s, map_h, map_w, Ts, H, V, temperature,
                     z ? z + (size_t)r0 * V : nullptr, part + (size_t)r0 * slices, n_units,
-                    TL.h_stage_bytes, TL.h_stages, TL.blk, TL.w_stages, Cp, d_status) !=
+                    TL.h_stage_bytes, TL.h_stages,
+                    (Cp > 1 && kDualCluster) ? 2 * TL.blk : TL.blk, TL.w_stages, Cp,
+                    d_status) !=
           cudaSuccess)
         return EAGLE_ERR_CUDA;
     }

@@ -162,6 +162,12 @@ constexpr int kHalfBytes = 128 * 128;   // 128 rows x 64 bf16 (one swizzle atom 
 constexpr int kTileBytes = 2 * kHalfBytes;  // 128 rows x 128 bf16
 constexpr int kTargetCtas = 152;        // SMs of a GB300
 constexpr int kMaxSplit = 8;            // cache chunks of one tile: one portable cluster
+// Split long caches of multi-wave launches (a build-time option, so that the
+// unsplit plan can be measured against it).
+#ifndef EAGLE_ATTN_BALANCE
+#define EAGLE_ATTN_BALANCE 1
+#endif
+constexpr bool kBalanceSplit = EAGLE_ATTN_BALANCE != 0;
 constexpr size_t kAttSharedBytes = 5120;
 // cluster merge inside the K/V stage memory: O rows [NC][rows per owner][32]
 // float4 (at most 136 x 512 B), then (max, sum) pairs
@@ -192,13 +198,25 @@ struct AttPlan {
 };
 
 // `split_cap`: the largest number of cache chunks per row tile whose
-// clusters all fit on the GPU at once.
-AttPlan att_plan(int B, int Hq, int Hkv, int max_nodes, int max_kv, int split_cap) {
+// clusters all fit on the GPU at once.  `kv_rows`: cache rows of all
+// sequences (an upper bound of their total length).
+AttPlan att_plan(int B, int Hq, int Hkv, int max_nodes, int max_kv, long long kv_rows,
+                 int split_cap) {
   AttPlan P;
   P.G = Hq / Hkv;
   P.MT = (max_nodes * P.G + 127) / 128;
   const int tiles = std::max(1, B * Hkv * P.MT);
-  const int nc = std::min(split_cap, std::max(1, kTargetCtas / tiles));
+  int nc = std::min(split_cap, std::max(1, kTargetCtas / tiles));
+  if (kBalanceSplit && tiles >= kTargetCtas && kv_rows > 0) {
+    // Several waves of tiles: split the longest caches until one chunk is
+    // at most half an SM's share of all the tiles' keys, so that a long
+    // sequence's tile scheduled late does not become the tail (ragged
+    // batches: L from 512 to 16384).
+    const double share = (double)kv_rows * Hkv * P.MT / kTargetCtas;
+    int want = 1;
+    while (want < kMaxSplit && (double)max_kv / want > share / 2) want *= 2;
+    nc = std::max(nc, want);
+  }
   int ck = (max_kv + nc - 1) / nc;
   ck = std::max(256, ((ck + kKeyBlk - 1) / kKeyBlk) * kKeyBlk);
   P.CK = ck;
@@ -298,7 +316,7 @@ __device__ __forceinline__ void tmem_wait_st() {
 // output accumulator, so the halves never wait for each other inside the
 // key loop and are merged once at the end.  TMEM columns: S at 0 (refilled
 // with the next block as soon as every row has read it), P at 128 (per key
-// half: 64 keys as bf16 pairs at +0), O of key half 0 at 256, of half 1 at 384.
+// half: bf16 hi at +0, lo at +32), O of key half 0 at 256, of half 1 at 384.
 __global__ void __launch_bounds__(kAttThreads, 1)
 tree_attn_tc_kernel(const __grid_constant__ CUtensorMap map_q,
                     const __grid_constant__ CUtensorMap map_kc,
@@ -525,19 +543,25 @@ tree_attn_tc_kernel(const __grid_constant__ CUtensorMap map_q,
           vph ^= 1u << st;
           tc::fence_after_thread_sync();
           const uint32_t v_addr = tc::smem_u32(v_sm + st * kTileBytes);
-          // O_h += P_h V_h for key half h: A = P (bf16) from the half's
+          // O_h += P_hi V_h + P_lo V_h for key half h: A = P from the half's
           // TMEM columns, B = V rows of that half (MN-major, 128-byte rows).
           // The two halves' accumulator chains are interleaved (each in its
           // own order), so the tensor pipe always has an independent MMA.
+          // (One bf16 P alone would round every weight by up to 2^-8 of
+          // itself -- up to 2^-8 of sum_j p_j |v_j| in the output when few
+          // keys dominate, above the 2e-3 bound; hi + lo keep 2^-16.)
 #pragma unroll
-          for (int kk = 0; kk < 4; ++kk) {
+          for (int part = 0; part < 2; ++part) {
 #pragma unroll
-            for (int h = 0; h < 2; ++h) {
-              const uint32_t a_tm = tmem + (uint32_t)(128 + h * 64 + kk * 8);
-              const uint32_t key = (uint32_t)(h * 64 + kk * 16);
-              mma_f16_tmem_a(tmem + 256u + (uint32_t)(h * 128), a_tm,
-                             desc_mnmajor_sw128(v_addr + key * 128u, kHalfBytes), idesc_o,
-                             (j > 0 || kk > 0) ? 1u : 0u);
+            for (int kk = 0; kk < 4; ++kk) {
+#pragma unroll
+              for (int h = 0; h < 2; ++h) {
+                const uint32_t a_tm = tmem + (uint32_t)(128 + h * 64 + part * 32 + kk * 8);
+                const uint32_t key = (uint32_t)(h * 64 + kk * 16);
+                mma_f16_tmem_a(tmem + 256u + (uint32_t)(h * 128), a_tm,
+                               desc_mnmajor_sw128(v_addr + key * 128u, kHalfBytes), idesc_o,
+                               (j > 0 || part > 0 || kk > 0) ? 1u : 0u);
+              }
             }
           }
           tc::mma_commit(&sh->pv_done);
@@ -618,27 +642,30 @@ tree_attn_tc_kernel(const __grid_constant__ CUtensorMap map_q,
       const bool first = (m == -INFINITY);
       const bool rescale = !first && (mn > m + kRescaleLog2);
       const float mu = (first || rescale) ? mn : m;     // reference max for this block's P
-      // P = exp2(s - mu) rounded to nearest bf16 for the PV product (at most
-      // 2^-9 relative per weight, so the output moves by at most 2^-9 of
-      // sum_j p_j |v_j| / sum_j p_j); the row sum takes the unrounded
-      // values.  Computed before waiting for the previous PV, which still
-      // reads the P columns.
+      // P = exp2(s - mu) = hi + lo, both bf16: hi keeps the top 16 bits of
+      // the fp32 value, lo = P - hi (exact in fp32) truncated the same way;
+      // |P - hi - lo| < 2^-14 P.  Computed before waiting for the previous
+      // PV, which still reads the P columns.
       float psum = 0.f;
       // a half-row with nothing visible yet keeps mu = -inf: its scores are
       // all -inf, and any finite offset gives P = 0
       const float neg_mu = (mu == -INFINITY) ? 0.f : -mu;
-      uint32_t pb0[16], pb1[16];
-      auto round_p = [&](const float (&v)[32], uint32_t (&pb)[16]) {
+      uint32_t hi0[16], lo0[16], hi1[16], lo1[16];
+      auto split = [&](const float (&v)[32], uint32_t (&hi)[16], uint32_t (&lo)[16]) {
 #pragma unroll
         for (int i = 0; i < 16; ++i) {
           const float p0 = ex2_approx(fmaf(v[2 * i], A.scale_log2, neg_mu));
           const float p1 = ex2_approx(fmaf(v[2 * i + 1], A.scale_log2, neg_mu));
-          pb[i] = pack_bf16(p0, p1);
+          const uint32_t b0 = __float_as_uint(p0), b1 = __float_as_uint(p1);
+          hi[i] = __byte_perm(b0, b1, 0x7632);
+          const float r0 = p0 - __uint_as_float(b0 & 0xffff0000u);
+          const float r1 = p1 - __uint_as_float(b1 & 0xffff0000u);
+          lo[i] = __byte_perm(__float_as_uint(r0), __float_as_uint(r1), 0x7632);
           psum += p0 + p1;
         }
       };
-      round_p(v0, pb0);
-      round_p(v1, pb1);
+      split(v0, hi0, lo0);
+      split(v1, hi1, lo1);
       if (j >= 1) {
         // the previous PV has read P and finished O (every earlier PV was
         // waited for one block before)
@@ -658,10 +685,12 @@ tree_attn_tc_kernel(const __grid_constant__ CUtensorMap map_q,
         }
         l *= f;
       }
-      // P of the half's 64 keys (two per 32-bit column) to its P columns
+      // hi to the half's P columns +0 .., lo to +32 ..
       const uint32_t pcol = trow + (uint32_t)(128 + half * 64);
-      tmem_st_32x32b_x16(pcol, pb0);
-      tmem_st_32x32b_x16(pcol + 16u, pb1);
+      tmem_st_32x32b_x16(pcol, hi0);
+      tmem_st_32x32b_x16(pcol + 16u, hi1);
+      tmem_st_32x32b_x16(pcol + 32u, lo0);
+      tmem_st_32x32b_x16(pcol + 48u, lo1);
       tmem_wait_st();
       l += psum;
       m = mu;
@@ -901,7 +930,7 @@ eagle_status attn_impl(eagle_dtype dtype, int B, int T, int Hq, int Hkv, int D, 
       return EAGLE_ERR_CUDA;
     const int G = Hq / Hkv;
     const int tiles = B * Hkv * ((max_nodes * G + 127) / 128);
-    const AttPlan P = att_plan(B, Hq, Hkv, max_nodes, max_kv, split_cap_for(tiles));
+    const AttPlan P = att_plan(B, Hq, Hkv, max_nodes, max_kv, cache_rows, split_cap_for(tiles));
     CUtensorMap mq, mkc, mvc, mkt, mvt;
     const void* kc = (cache_rows > 0) ? d_k_cache : d_k_tree;   // never read when empty
     const void* vc = (cache_rows > 0) ? d_v_cache : d_v_tree;
