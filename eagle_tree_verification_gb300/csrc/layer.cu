@@ -83,14 +83,17 @@ cast_bf16_kernel(size_t n, const float* __restrict__ x, __nv_bfloat16* __restric
 
 // Positions (cache length + depth) and the rotation of every (node, pair j)
 // by pos * theta^(-2j/D); the angle, its reduction and sin / cos in fp64,
-// rounded once to fp32.
-__global__ void __launch_bounds__(EAGLE_MAX_TREE_NODES)
+// rounded once to fp32.  One CTA per sequence finds the depths; the (node,
+// pair) entries are then spread over all its threads.
+constexpr int kRopeThreads = 1024;
+__global__ void __launch_bounds__(kRopeThreads)
 rope_table_kernel(int D, double log2_theta, const int* __restrict__ tree_off,
                   const int* __restrict__ parent, const int* __restrict__ kv_off,
                   const int* __restrict__ kv_len, int* __restrict__ pos,
                   float2* __restrict__ cs, int* status) {
   pdl_begin();
   __shared__ int s_par[EAGLE_MAX_TREE_NODES];
+  __shared__ int s_pos[EAGLE_MAX_TREE_NODES];
   __shared__ int s_bad;
   const int b = blockIdx.x, i = threadIdx.x;
   const int t0 = tree_off[b], n = tree_off[b + 1] - t0;
@@ -111,17 +114,20 @@ rope_table_kernel(int D, double log2_theta, const int* __restrict__ tree_off,
     if (i == 0) fail(status, EAGLE_ERR_INVALID_TREE);
     return;
   }
-  if (i >= n) return;
-  int d = 0;
-  for (int a = i; a > 0; a = s_par[a]) ++d;
-  const int ps = L + d;
-  pos[t0 + i] = ps;
+  if (i < n) {
+    int d = 0;
+    for (int a = i; a > 0; a = s_par[a]) ++d;
+    s_pos[i] = L + d;
+    pos[t0 + i] = L + d;
+  }
+  __syncthreads();
   const int half = D / 2;
-  for (int j = 0; j < half; ++j) {
-    const double ang = (double)ps * exp2(-2.0 * (double)j / (double)D * log2_theta);
+  for (int e = i; e < n * half; e += kRopeThreads) {
+    const int node = e / half, j = e % half;
+    const double ang = (double)s_pos[node] * exp2(-2.0 * (double)j / (double)D * log2_theta);
     double sn, cn;
     sincos(ang, &sn, &cn);
-    cs[(size_t)(t0 + i) * half + j] = make_float2((float)cn, (float)sn);
+    cs[(size_t)(t0 + node) * half + j] = make_float2((float)cn, (float)sn);
   }
 }
 
@@ -655,7 +661,7 @@ extern "C" eagle_status eagle_tree_rope_table(int B, int D, float theta, const i
   EAGLE_HOST_CHECK(d_tree_off && d_parent && d_pos && d_cos_sin && d_status,
                    EAGLE_ERR_INVALID_ARG);
   EAGLE_HOST_CHECK((d_kv_off != nullptr) != (d_kv_len != nullptr), EAGLE_ERR_INVALID_ARG);
-  return launch_status(launch_pdl(rope_table_kernel, dim3(B), dim3(EAGLE_MAX_TREE_NODES), 0,
+  return launch_status(launch_pdl(rope_table_kernel, dim3(B), dim3(kRopeThreads), 0,
                                   (cudaStream_t)stream, D, log2((double)theta), d_tree_off,
                                   d_parent, d_kv_off, d_kv_len, d_pos,
                                   reinterpret_cast<float2*>(d_cos_sin), d_status));

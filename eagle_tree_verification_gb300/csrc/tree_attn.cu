@@ -162,12 +162,6 @@ constexpr int kHalfBytes = 128 * 128;   // 128 rows x 64 bf16 (one swizzle atom 
 constexpr int kTileBytes = 2 * kHalfBytes;  // 128 rows x 128 bf16
 constexpr int kTargetCtas = 152;        // SMs of a GB300
 constexpr int kMaxSplit = 8;            // cache chunks of one tile: one portable cluster
-// Split long caches of multi-wave launches (a build-time option, so that the
-// unsplit plan can be measured against it).
-#ifndef EAGLE_ATTN_BALANCE
-#define EAGLE_ATTN_BALANCE 1
-#endif
-constexpr bool kBalanceSplit = EAGLE_ATTN_BALANCE != 0;
 constexpr size_t kAttSharedBytes = 5120;
 // cluster merge inside the K/V stage memory: O rows [NC][rows per owner][32]
 // float4 (at most 136 x 512 B), then (max, sum) pairs
@@ -198,25 +192,17 @@ struct AttPlan {
 };
 
 // `split_cap`: the largest number of cache chunks per row tile whose
-// clusters all fit on the GPU at once.  `kv_rows`: cache rows of all
-// sequences (an upper bound of their total length).
-AttPlan att_plan(int B, int Hq, int Hkv, int max_nodes, int max_kv, long long kv_rows,
-                 int split_cap) {
+// clusters all fit on the GPU at once.  (Measured at 16 ragged sequences of
+// 512..16384 keys, 256 tiles: splitting the longest caches into clusters of
+// four chunks took 461 us against 224 us unsplit -- clusters of 170 KB CTAs
+// wait for four free SMs of one GPC -- so launches of more tiles than SMs
+// stay unsplit.)
+AttPlan att_plan(int B, int Hq, int Hkv, int max_nodes, int max_kv, int split_cap) {
   AttPlan P;
   P.G = Hq / Hkv;
   P.MT = (max_nodes * P.G + 127) / 128;
   const int tiles = std::max(1, B * Hkv * P.MT);
-  int nc = std::min(split_cap, std::max(1, kTargetCtas / tiles));
-  if (kBalanceSplit && tiles >= kTargetCtas && kv_rows > 0) {
-    // Several waves of tiles: split the longest caches until one chunk is
-    // at most half an SM's share of all the tiles' keys, so that a long
-    // sequence's tile scheduled late does not become the tail (ragged
-    // batches: L from 512 to 16384).
-    const double share = (double)kv_rows * Hkv * P.MT / kTargetCtas;
-    int want = 1;
-    while (want < kMaxSplit && (double)max_kv / want > share / 2) want *= 2;
-    nc = std::max(nc, want);
-  }
+  const int nc = std::min(split_cap, std::max(1, kTargetCtas / tiles));
   int ck = (max_kv + nc - 1) / nc;
   ck = std::max(256, ((ck + kKeyBlk - 1) / kKeyBlk) * kKeyBlk);
   P.CK = ck;
@@ -930,7 +916,7 @@ eagle_status attn_impl(eagle_dtype dtype, int B, int T, int Hq, int Hkv, int D, 
       return EAGLE_ERR_CUDA;
     const int G = Hq / Hkv;
     const int tiles = B * Hkv * ((max_nodes * G + 127) / 128);
-    const AttPlan P = att_plan(B, Hq, Hkv, max_nodes, max_kv, cache_rows, split_cap_for(tiles));
+    const AttPlan P = att_plan(B, Hq, Hkv, max_nodes, max_kv, split_cap_for(tiles));
     CUtensorMap mq, mkc, mvc, mkt, mvt;
     const void* kc = (cache_rows > 0) ? d_k_cache : d_k_tree;   // never read when empty
     const void* vc = (cache_rows > 0) ? d_v_cache : d_v_tree;
