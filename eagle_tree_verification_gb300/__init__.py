@@ -70,7 +70,7 @@ _SIGS = {
     "eagle_tree_attn_paged": ([_i] * 6 + [_f] + [_i] * 5 + [_p] * 12, _i),
     "eagle_rmsnorm": ([_i, _i, _f] + [_p] * 5, _i),
     "eagle_cast_bf16": ([_sz, _p, _p, _p], _i),
-    "eagle_tree_rope_table": ([_i, _i, _f] + [_p] * 8, _i),
+    "eagle_tree_rope_table": ([_i, _i, _i, _f] + [_p] * 8, _i),
     "eagle_gemm": ([_i] * 4 + [_p] * 9 + [_i] * 3 + [_p, _p], _i),
     "eagle_kv_commit_paged": ([_i] * 8 + [_p] * 11, _i),
     "eagle_draft_expand_dep": ([_i] * 6 + [_p] * 4 + [_sz] + [_p] * 8, _i),
@@ -403,7 +403,8 @@ def eagle_tree_rope_table(tree_off, parent, pos, cos_sin, status, *, D: int, the
     """Node positions (cache length + depth) and their rotation table
     cos_sin [T, D/2, 2] fp32; give kv_off [B+1] or kv_len [B]."""
     B = tree_off.numel() - 1
-    _call("eagle_tree_rope_table", B, int(D), float(theta), _ptr(tree_off), _ptr(parent),
+    _call("eagle_tree_rope_table", B, parent.numel(), int(D), float(theta), _ptr(tree_off),
+          _ptr(parent),
           _ptr(kv_off), _ptr(kv_len), _ptr(pos), _ptr(cos_sin), _ptr(status), _stream(stream))
 
 

@@ -503,121 +503,6 @@ __device__ void merge_sequence(const LevelParams& A, int b, MergeShared& M) {
   if (tid == 0) A.pool.count[b] = base + nc;
 }
 
-// Streaming selection: a CTA walks consecutive chunks of a row (a row
-// segment) and keeps the segment's exact top-k in shared memory (seg[0..*sn),
-// descending).  A chunk only offers keys at or above the segment's k-th key
-// once the segment holds k keys, so after the first chunk most tokens cost a
-// compare; the first chunk of a segment takes the group-maxima bound of
-// chunk_topk.  The new top-k is ranked over the union of the held keys and
-// the chunk's candidates (all keys are distinct).
-template <int VEC>
-__device__ void chunk_merge(const LevelParams& A, int chunk, float (&x)[VEC][4],
-                            ChunkShared& C, unsigned long long* seg, int* sn) {
-  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-  const int k = A.k;
-  const int c0 = chunk * (kLvThreads * 4 * VEC);
-  const bool ragged = c0 + kLvThreads * 4 * VEC > A.V;   // block-uniform
-  // x: the chunk's values in place (past the row's end they become -inf)
-  float fin = 0.f;   // NaN iff some real value is not finite
-#pragma unroll
-  for (int j = 0; j < VEC; ++j)
-#pragma unroll
-    for (int e = 0; e < 4; ++e) {
-      const bool real = !ragged || c0 + (j * kLvThreads + tid) * 4 + e < A.V;
-      if (real) fin = fmaf(x[j][e], 0.f, fin);
-      else x[j][e] = -INFINITY;
-    }
-  const int held = *sn;   // block-uniform (written before the last barrier)
-  const unsigned long long floor_key = (held == k) ? seg[k - 1] : 0ull;
-  float tau_val;
-  if (floor_key) {
-    if (tid == 0) C.cnt = 0;
-    if (__syncthreads_or(!(fin == 0.f)) && tid == 0) fail(A.status, EAGLE_ERR_NUMERIC);
-    tau_val = key_value(floor_key);
-  } else {
-    // as chunk_topk: the largest group maximum that k group maxima reach
-    float tmax = -INFINITY;
-#pragma unroll
-    for (int j = 0; j < VEC; ++j)
-#pragma unroll
-      for (int e = 0; e < 4; ++e) tmax = fmaxf(tmax, x[j][e]);
-#pragma unroll
-    for (int o = 8; o > 0; o >>= 1) tmax = fmaxf(tmax, __shfl_xor_sync(0xffffffffu, tmax, o));
-    if ((lane & 15) == 0) C.grpv[warp * 2 + (lane >> 4)] = tmax;
-    if (tid == 0) C.cnt = 0;
-    if (__syncthreads_or(!(fin == 0.f)) && tid == 0) fail(A.status, EAGLE_ERR_NUMERIC);
-    const float g = C.grpv[lane];
-    int ge = 0;
-#pragma unroll 8
-    for (int i = 0; i < kGroups; ++i) ge += (C.grpv[i] >= g);
-    const unsigned ob = __reduce_max_sync(0xffffffffu, (ge >= k) ? ordered_bits(g) : 0u);
-    tau_val = fmaxf(from_ordered_bits(ob), -3.402823466e38f);
-  }
-  unsigned long long tau_key = floor_key;
-  int cnt;
-  for (int round = 0;; ++round) {
-#pragma unroll
-    for (int j = 0; j < VEC; ++j)
-#pragma unroll
-      for (int e = 0; e < 4; ++e) {
-        const float val = x[j][e];
-        const uint32_t idx = (uint32_t)(c0 + (j * kLvThreads + tid) * 4 + e);
-        const bool pred = (val >= tau_val) && (tau_key == 0ull || desc_key(val, idx) >= tau_key);
-        const unsigned bal = __ballot_sync(0xffffffffu, pred);
-        if (bal) {
-          const int leader = __ffs(bal) - 1;
-          int base = 0;
-          if (lane == leader) base = atomicAdd(&C.cnt, __popc(bal));
-          base = __shfl_sync(0xffffffffu, base, leader);
-          const int pos = base + __popc(bal & lanemask_lt());
-          if (pred && pos < kCandCap) C.cand[pos] = desc_key(val, idx);
-        }
-      }
-    __syncthreads();
-    cnt = C.cnt;
-    if (cnt <= kCandCap) break;
-    if (round == kChunkRounds) {
-      if (tid == 0) fail(A.status, EAGLE_ERR_TIMEOUT);
-      cnt = kCandCap;
-      break;
-    }
-    // too many: raise the bound to the k-th largest of the held candidates
-    const unsigned long long me = C.cand[tid];
-    int rank = 0;
-#pragma unroll 8
-    for (int i = 0; i < kCandCap; ++i) rank += (C.cand[i] > me);
-    __syncthreads();
-    if (rank == k - 1) C.tau = me;
-    if (tid == 0) C.cnt = 0;
-    __syncthreads();
-    tau_key = C.tau;
-    tau_val = key_value(tau_key);
-  }
-  // ---- the segment's new top-k over (held keys) + (candidates)
-  const int n = cnt + held;
-  if (n <= 32) {
-    if (warp == 0) {
-      const unsigned long long me =
-          (lane < cnt) ? C.cand[lane] : (lane < n ? seg[lane - cnt] : 0ull);
-      const int rank = warp_rank_desc(me);
-      if (lane < n && rank < k) C.top[rank] = me;
-    }
-  } else {
-    for (int t = tid; t < n; t += kLvThreads) {
-      const unsigned long long me = (t < cnt) ? C.cand[t] : seg[t - cnt];
-      int rank = 0;
-      for (int i = 0; i < cnt; ++i) rank += (C.cand[i] > me);
-      for (int i = 0; i < held; ++i) rank += (seg[i] > me);
-      if (rank < k) C.top[rank] = me;
-    }
-  }
-  __syncthreads();
-  const int kept = min(n, k);
-  if (tid < kept) seg[tid] = C.top[tid];
-  if (tid == 0) *sn = kept;
-  __syncthreads();
-}
-
 // One level.  CTA (row, chunk): exact top-k of the chunk -> partial list.
 // The sequence's last CTA: per-row top-k, children, next frontier.
 template <int VEC>
@@ -694,8 +579,6 @@ expand_level_stream_kernel(const LevelParams A, int total_chunks) {
   __shared__ MergeShared M;
   __shared__ uint64_t full[kStreamStages];
   __shared__ int abort_flag, s_last;
-  __shared__ unsigned long long s_seg[EAGLE_MAX_TOPK];   // the row segment's top-k
-  __shared__ int s_seg_n;
   extern __shared__ __align__(128) unsigned char stage_mem[];   // kStreamSmem bytes
   const int tid = threadIdx.x;
   const int k = A.k;
@@ -740,17 +623,6 @@ expand_level_stream_kernel(const LevelParams A, int total_chunks) {
     }
     __syncthreads();
   };
-  // the row segment this CTA is walking: its top-k goes to the partial list
-  // of its first chunk, the lists of its other chunks are emptied
-  int seg_row = -1, seg_first = 0, seg_len = 0;
-  auto flush_segment = [&]() {
-    if (tid < 32) {
-      unsigned long long* part = A.pool.partial + ((size_t)seg_row * A.S + seg_first) * k;
-      const int sn = s_seg_n;
-      for (int t = tid; t < seg_len * k; t += 32) part[t] = (t < sn) ? s_seg[t] : 0ull;
-      __syncwarp();
-    }
-  };
   int i = 0, cur_b = -1, cur_n = 0;
   bool aborted = false;
   for (int id = id0; id < id1; ++id, ++i) {
@@ -778,24 +650,14 @@ expand_level_stream_kernel(const LevelParams A, int total_chunks) {
     }
     const int row = id / A.S, chunk = id % A.S;
     const int b = row / A.F;
-    if (row != seg_row) {
-      if (seg_row >= 0) flush_segment();   // before its sequence is counted
-      if (b != cur_b) {
-        if (cur_b >= 0) leave_sequence(cur_b, cur_n);
-        cur_b = b;
-        cur_n = 0;
-      }
-      seg_row = row;
-      seg_first = chunk;
-      seg_len = 0;
-      if (tid == 0) s_seg_n = 0;
-      __syncthreads();
+    if (b != cur_b) {
+      if (cur_b >= 0) leave_sequence(cur_b, cur_n);
+      cur_b = b;
+      cur_n = 0;
     }
-    chunk_merge<kStreamVec>(A, chunk, v, C, s_seg, &s_seg_n);
-    ++seg_len;
+    chunk_topk<kStreamVec>(A, row, chunk, v, C, false);
     ++cur_n;
   }
-  if (!aborted && seg_row >= 0) flush_segment();
   if (!aborted && cur_b >= 0) leave_sequence(cur_b, cur_n);
   if (aborted && tid == 0) {
     // let the copies still in flight land before the CTA leaves

@@ -82,53 +82,53 @@ cast_bf16_kernel(size_t n, const float* __restrict__ x, __nv_bfloat16* __restric
 }
 
 // Positions (cache length + depth) and the rotation of every (node, pair j)
-// by pos * theta^(-2j/D); the angle, its reduction and sin / cos in fp64,
-// rounded once to fp32.  One CTA per sequence finds the depths; the (node,
-// pair) entries are then spread over all its threads.
-constexpr int kRopeThreads = 1024;
+// by pos * theta^(-2j/D).  One thread per (node, pair) over the whole grid:
+// the node's sequence by binary search of tree_off, its depth by walking
+// parent[] (a parent precedes its child, so the walk ends; a parent that
+// does not is reported), the angle formed in fp64 and reduced modulo 2 pi in
+// fp64 (2 pi as a head and tail pair), then sine and cosine in fp32 on the
+// reduced angle (|r| <= pi).
+constexpr int kRopeThreads = 256;
 __global__ void __launch_bounds__(kRopeThreads)
-rope_table_kernel(int D, double log2_theta, const int* __restrict__ tree_off,
+rope_table_kernel(int B, int T, int D, double log2_theta, const int* __restrict__ tree_off,
                   const int* __restrict__ parent, const int* __restrict__ kv_off,
                   const int* __restrict__ kv_len, int* __restrict__ pos,
                   float2* __restrict__ cs, int* status) {
   pdl_begin();
-  __shared__ int s_par[EAGLE_MAX_TREE_NODES];
-  __shared__ int s_pos[EAGLE_MAX_TREE_NODES];
-  __shared__ int s_bad;
-  const int b = blockIdx.x, i = threadIdx.x;
-  const int t0 = tree_off[b], n = tree_off[b + 1] - t0;
-  const int L = kv_off ? kv_off[b + 1] - kv_off[b] : kv_len[b];
-  if (n < 1 || n > EAGLE_MAX_TREE_NODES || L < 0) {
-    if (i == 0) fail(status, EAGLE_ERR_INVALID_TREE);
-    return;
-  }
-  if (i == 0) s_bad = 0;
-  __syncthreads();
-  if (i < n) {
-    const int p = parent[t0 + i];
-    s_par[i] = p;
-    if ((i == 0) ? (p != -1) : (p < 0 || p >= i)) atomicOr(&s_bad, 1);
-  }
-  __syncthreads();
-  if (s_bad) {
-    if (i == 0) fail(status, EAGLE_ERR_INVALID_TREE);
-    return;
-  }
-  if (i < n) {
-    int d = 0;
-    for (int a = i; a > 0; a = s_par[a]) ++d;
-    s_pos[i] = L + d;
-    pos[t0 + i] = L + d;
-  }
-  __syncthreads();
   const int half = D / 2;
-  for (int e = i; e < n * half; e += kRopeThreads) {
-    const int node = e / half, j = e % half;
-    const double ang = (double)s_pos[node] * exp2(-2.0 * (double)j / (double)D * log2_theta);
-    double sn, cn;
-    sincos(ang, &sn, &cn);
-    cs[(size_t)(t0 + node) * half + j] = make_float2((float)cn, (float)sn);
+  const long long e = (long long)blockIdx.x * kRopeThreads + threadIdx.x;
+  if (e >= (long long)T * half) return;
+  const int t = (int)(e / half), j = (int)(e % half);
+  int lo = 0, hi = B;   // tree_off[lo] <= t < tree_off[hi]
+  while (hi - lo > 1) {
+    const int mid = (lo + hi) >> 1;
+    if (tree_off[mid] <= t) lo = mid;
+    else hi = mid;
   }
+  const int b = lo, t0 = tree_off[b], n = tree_off[b + 1] - t0;
+  const int L = kv_off ? kv_off[b + 1] - kv_off[b] : kv_len[b];
+  int d = 0;
+  bool bad = (L < 0 || n < 1);
+  for (int a = t - t0; a > 0 && !bad; ++d) {
+    const int p = parent[t0 + a];
+    bad = (p < 0 || p >= a);
+    a = p;
+  }
+  if (t - t0 == 0 && parent[t0] != -1) bad = true;
+  if (bad) {
+    if (j == 0) fail(status, EAGLE_ERR_INVALID_TREE);
+    return;
+  }
+  const int ps = L + d;
+  if (j == 0) pos[t] = ps;
+  const double ang = (double)ps * exp2(-2.0 * (double)j / (double)D * log2_theta);
+  const double two_pi_hi = 6.283185307179586;              // 2 pi rounded to fp64
+  const double two_pi_lo = 2.4492935982947064e-16;         // 2 pi - two_pi_hi
+  const double k = rint(ang / two_pi_hi);
+  const double r = fma(-k, two_pi_lo, fma(-k, two_pi_hi, ang));
+  float sn, cn;
+  sincosf((float)r, &sn, &cn);
+  cs[(size_t)t * half + j] = make_float2(cn, sn);
 }
 
 // ---------------------------------------------------------------------------
@@ -650,7 +650,8 @@ extern "C" eagle_status eagle_cast_bf16(size_t n, const float* d_x, void* d_y,
                                   static_cast<__nv_bfloat16*>(d_y)));
 }
 
-extern "C" eagle_status eagle_tree_rope_table(int B, int D, float theta, const int32_t* d_tree_off,
+extern "C" eagle_status eagle_tree_rope_table(int B, int T, int D, float theta,
+                                              const int32_t* d_tree_off,
                                               const int32_t* d_parent, const int32_t* d_kv_off,
                                               const int32_t* d_kv_len, int32_t* d_pos,
                                               float* d_cos_sin, int* d_status,
@@ -661,10 +662,14 @@ extern "C" eagle_status eagle_tree_rope_table(int B, int D, float theta, const i
   EAGLE_HOST_CHECK(d_tree_off && d_parent && d_pos && d_cos_sin && d_status,
                    EAGLE_ERR_INVALID_ARG);
   EAGLE_HOST_CHECK((d_kv_off != nullptr) != (d_kv_len != nullptr), EAGLE_ERR_INVALID_ARG);
-  return launch_status(launch_pdl(rope_table_kernel, dim3(B), dim3(kRopeThreads), 0,
-                                  (cudaStream_t)stream, D, log2((double)theta), d_tree_off,
-                                  d_parent, d_kv_off, d_kv_len, d_pos,
-                                  reinterpret_cast<float2*>(d_cos_sin), d_status));
+  EAGLE_HOST_CHECK(T >= 0, EAGLE_ERR_INVALID_ARG);
+  if (T == 0) return EAGLE_OK;
+  const long long work = (long long)T * (D / 2);
+  return launch_status(launch_pdl(rope_table_kernel,
+                                  dim3((unsigned)((work + kRopeThreads - 1) / kRopeThreads)),
+                                  dim3(kRopeThreads), 0, (cudaStream_t)stream, B, T, D,
+                                  log2((double)theta), d_tree_off, d_parent, d_kv_off, d_kv_len,
+                                  d_pos, reinterpret_cast<float2*>(d_cos_sin), d_status));
 }
 
 extern "C" eagle_status eagle_gemm(int epilogue, int T, int N, int K, const void* d_a,

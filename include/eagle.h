@@ -518,11 +518,12 @@ EAGLE_API eagle_status eagle_cast_bf16(size_t n, const float *d_x, void *d_y,
 /* Positions and rotations of the tree nodes.  Node i of sequence b sits at
  * position pos = L_b + depth(i) (where it would stand on its own
  * root-to-node path after the cache), L_b = kv_off[b+1] - kv_off[b] or
- * kv_len[b] (give exactly one of d_kv_off [B+1], d_kv_len [B]).  Writes
- * d_pos [T] and d_cos_sin [T, D/2, 2] fp32 = (cos, sin) of
- * pos * theta^(-2j/D) (angle and trigonometry in fp64, rounded once).
+ * kv_len[b] (give exactly one of d_kv_off [B+1], d_kv_len [B]).  T =
+ * tree_off[B] nodes.  Writes d_pos [T] and d_cos_sin [T, D/2, 2] fp32 =
+ * (cos, sin) of pos * theta^(-2j/D): the angle formed and reduced modulo
+ * 2 pi in fp64, sine and cosine in fp32 (within a few 1e-7).
  * Device errors: INVALID_TREE. */
-EAGLE_API eagle_status eagle_tree_rope_table(int B, int D, float theta,
+EAGLE_API eagle_status eagle_tree_rope_table(int B, int T, int D, float theta,
                                              const int32_t *d_tree_off, const int32_t *d_parent,
                                              const int32_t *d_kv_off, const int32_t *d_kv_len,
                                              int32_t *d_pos, float *d_cos_sin, int *d_status,

@@ -114,8 +114,10 @@ def test_rope_table_and_rmsnorm():
     np.testing.assert_array_equal(to_np(pos), ref_pos)
     ang = ref_pos[:, None] * theta ** (-2.0 * np.arange(D // 2) / D)
     got = to_np(cs).astype(np.float64)
-    assert np.abs(got[..., 0] - np.cos(ang)).max() <= 1e-7
-    assert np.abs(got[..., 1] - np.sin(ang)).max() <= 1e-7
+    # the reduced angle rounded to fp32 (up to 2^-24 pi) and fp32 sine and
+    # cosine (about one ulp): a few 1e-7
+    assert np.abs(got[..., 0] - np.cos(ang)).max() <= 5e-7
+    assert np.abs(got[..., 1] - np.sin(ang)).max() <= 5e-7
     # RMSNorm: bf16 output within one bf16 step of the fp64 definition
     H = 4096
     x = synth.normal(5, "norm-x", (T, H)) * 3.0
