@@ -141,15 +141,19 @@ constexpr int kGUnit = 32;       // W rows per TMA box (and per epilogue chunk)
 constexpr int kGBlk = 256;       // W rows per MMA (its N), at most; TMEM accumulator stride
 constexpr int kGTile = 128;      // tree rows per CTA (the MMA's M)
 constexpr int kGMaxCluster = 8;
-constexpr int kGHStages = 4;
-constexpr int kGMaxWStages = 48;   // a slice of few W rows streams through many small stages
+// The A (tree rows) and W rings advance together, one K chunk per stage, so
+// the bytes in flight are (A chunk + W chunk) x the stages of the shorter
+// ring.  A narrow W slice (few W rows per CTA) makes its A chunk the larger
+// one: the stages are then many and small.
+constexpr int kGMaxHStages = 24;
+constexpr int kGMaxWStages = 48;
 constexpr size_t kGSmemLimit = 227 * 1024;
 constexpr size_t kGShared = 2048;
 
 enum Epi { EPI_STORE = 0, EPI_ACCUM = 1, EPI_SWIGLU = 2, EPI_QKV_ROPE = 3 };
 
 struct GemmShared {
-  uint64_t h_full[kGHStages], h_empty[kGHStages];
+  uint64_t h_full[kGMaxHStages], h_empty[kGMaxHStages];
   uint64_t w_full[kGMaxWStages], w_empty[kGMaxWStages];
   uint64_t tmem_full[2], tmem_empty[2], drain;
   uint32_t tmem_base;
@@ -160,7 +164,7 @@ static_assert(sizeof(GemmShared) <= kGShared, "GemmShared must fit its slot");
 
 struct GemmArgs {
   int T, N, K, C;           // rows, W rows, reduction length, CTAs per cluster
-  int n_units, w_stages, h_stage_bytes;
+  int n_units, w_stages, h_stages, h_stage_bytes;
   int blk_max;              // W rows per block (and per W stage), a multiple of 32, <= 256
   int epi;
   // outputs of the epilogues
@@ -270,7 +274,8 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap map_a, const __grid_constant_
   unsigned char* base = reinterpret_cast<unsigned char*>(
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~(uintptr_t)1023);
   unsigned char* h_smem = base;
-  unsigned char* w_smem = base + kGHStages * A.h_stage_bytes;
+  const int h_stages = A.h_stages;
+  unsigned char* w_smem = base + h_stages * A.h_stage_bytes;
   const int blk_max = A.blk_max;
   const int w_stage_bytes = blk_max * 128;
   const int w_stages = A.w_stages;
@@ -304,7 +309,7 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap map_a, const __grid_constant_
   const int w_early = min(w_stages, total);
 
   if (threadIdx.x == 0) {
-    for (int i = 0; i < kGHStages; ++i) {
+    for (int i = 0; i < h_stages; ++i) {
       tc::mbar_init(&sh->h_full[i], 1);
       tc::mbar_init(&sh->h_empty[i], 1);
     }
@@ -362,7 +367,7 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap map_a, const __grid_constant_
           tc::tma_load_2d_hint(h_smem + hs * A.h_stage_bytes, &map_a, &sh->h_full[hs],
                                kb * kGBK, rank * kGTile, pol_h);
           ++issued_h;
-          if (++hs == kGHStages) { hs = 0; hph ^= 1; }
+          if (++hs == h_stages) { hs = 0; hph ^= 1; }
           if (i >= w_early) {
             if (!(ok = tc::mbar_wait(&sh->w_empty[ws], wph ^ 1, abort_flag, status))) break;
             load_w(ws, rows, kb, y0, pol_w);
@@ -381,7 +386,7 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap map_a, const __grid_constant_
           tc::mbar_wait(&sh->w_full[j % w_stages], (j / w_stages) & 1, &never, nullptr,
                         200000000ll);
         for (int j = *(volatile int*)&sh->consumed_h; j < issued_h; ++j)
-          tc::mbar_wait(&sh->h_full[j % kGHStages], (j / kGHStages) & 1, &never, nullptr,
+          tc::mbar_wait(&sh->h_full[j % h_stages], (j / h_stages) & 1, &never, nullptr,
                         200000000ll);
       }
     }
@@ -418,7 +423,7 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap map_a, const __grid_constant_
           *(volatile int*)&sh->consumed_w += 1;
           *(volatile int*)&sh->consumed_h += 1;
           if (++ws == w_stages) { ws = 0; wph ^= 1; }
-          if (++hs == kGHStages) { hs = 0; hph ^= 1; }
+          if (++hs == h_stages) { hs = 0; hph ^= 1; }
         }
         if (ok) tc::mma_commit(&sh->tmem_full[ab]);
       }
@@ -504,20 +509,24 @@ int g_sm_count() {
 }
 
 struct GLayout {
-  int h_stage_bytes, w_stages, blk;
+  int h_stage_bytes, h_stages, w_stages, blk;
   size_t smem;
 };
 
-// `blk`: W rows per block (a multiple of 32); the W ring gets every byte
-// left, in as many stages as fit, so that a slice of few rows still keeps
-// enough bytes in flight.
+// `blk`: W rows per block (a multiple of 32).  Both rings get as many
+// stages as fit side by side (each K chunk needs its A and its W stage);
+// bytes left over go to extra W stages, which are requested before the
+// kernel waits for its predecessor.
 GLayout g_layout(int h_rows, int blk) {
   GLayout L;
   L.h_stage_bytes = h_rows * 128;
   L.blk = blk;
-  const size_t fixed = 1024 + (size_t)kGHStages * L.h_stage_bytes + kGShared;
-  L.w_stages = (int)std::min<size_t>(kGMaxWStages, (kGSmemLimit - fixed) / ((size_t)blk * 128));
-  L.smem = fixed + (size_t)L.w_stages * blk * 128;
+  const size_t wb = (size_t)blk * 128;
+  const size_t room = kGSmemLimit - 1024 - kGShared;
+  L.h_stages = (int)std::min<size_t>(kGMaxHStages, room / (L.h_stage_bytes + wb));
+  const size_t left = room - (size_t)L.h_stages * L.h_stage_bytes;
+  L.w_stages = (int)std::min<size_t>(kGMaxWStages, left / wb);
+  L.smem = 1024 + kGShared + (size_t)L.h_stages * L.h_stage_bytes + (size_t)L.w_stages * wb;
   return L;
 }
 
@@ -593,6 +602,7 @@ eagle_status gemm_launch(int T, int N, int K, const void* d_a, const void* d_w, 
     P.C = Cp;
     P.n_units = n_units;
     P.w_stages = L.w_stages;
+    P.h_stages = L.h_stages;
     P.h_stage_bytes = L.h_stage_bytes;
     P.blk_max = L.blk;
     // the pass's rows: shift every row-indexed output

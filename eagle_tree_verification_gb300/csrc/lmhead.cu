@@ -278,6 +278,13 @@ constexpr size_t kSmemLimit = 227 * 1024;
 constexpr size_t kSmemShared = 171 * 1024;
 constexpr int kSmsForOthers = 16;
 constexpr size_t kTcSharedBytes = 1024 + 2 * 128 * 16;
+// LOGITS / PROB mode: every epilogue warp stages its 32 rows x 8 logits in one
+// of two 1 KB shared-memory boxes (32-byte swizzle) and writes them with a
+// bulk tensor store, so each global write covers whole 32-byte row segments
+// instead of one 16-byte piece of 32 rows per store instruction.
+constexpr int kZBoxCols = 8;
+constexpr int kZBoxBytes = 32 * kZBoxCols * 4;
+constexpr size_t kZStageBytes = (size_t)8 * 2 * kZBoxBytes;   // 8 warps x 2 boxes
 
 struct TcShared {
   uint64_t h_full[kMaxHStages], h_empty[kMaxHStages];
@@ -293,11 +300,14 @@ static_assert(sizeof(TcShared) <= kTcSharedBytes, "TcShared must fit its shared-
 
 struct TcLayout {
   int h_rows, h_stage_bytes, h_stages, blk, w_stage_bytes, w_stages;
+  bool z_tma;   // logits staged for bulk tensor stores
   size_t smem;
 };
 
-// `h_rows`: tree rows of one h stage (one CTA's tile, rounded up to 8).
-TcLayout tc_layout(int h_rows) {
+// `h_rows`: tree rows of one h stage (one CTA's tile, rounded up to 8);
+// `z_tma`: logits are written and the staging boxes should be held when
+// they fit beside the rings (a smaller CTA writes logits directly).
+TcLayout tc_layout(int h_rows, bool z_tma) {
   TcLayout L;
   L.h_rows = h_rows;
   L.h_stage_bytes = h_rows * 128;
@@ -317,6 +327,9 @@ TcLayout tc_layout(int h_rows) {
     L.h_stages = kBigHStages;
     fixed = 1024 + (size_t)L.h_stages * L.h_stage_bytes + kTcSharedBytes;
   }
+  // the staging boxes only where four W stages still fit beside them
+  L.z_tma = z_tma && fixed + kZStageBytes + 4 * (size_t)L.w_stage_bytes <= limit;
+  if (L.z_tma) fixed += kZStageBytes;
   L.w_stages = (int)std::min<size_t>(kMaxWStages, (limit - fixed) / L.w_stage_bytes);
   L.smem = fixed + (size_t)L.w_stages * L.w_stage_bytes;
   return L;
@@ -360,7 +373,8 @@ __device__ __forceinline__ void merge_partial(Partial& a, const Partial& b, floa
 template <bool MULTI, bool DUAL>
 __global__ void __launch_bounds__(kTcThreads, 1)
 lmhead_tc_kernel(const __grid_constant__ CUtensorMap map_h, const __grid_constant__ CUtensorMap map_w,
-                 int T, int H, int V, float temperature, float* __restrict__ z_out,
+                 const __grid_constant__ CUtensorMap map_z, int T, int H, int V,
+                 float temperature, float* __restrict__ z_out, int z_tma,
                  Partial* __restrict__ part, int n_units, int h_stage_bytes, int h_stages,
                  int blk_max, int w_stages, int C, int* status) {
   extern __shared__ __align__(1024) unsigned char smem_raw[];
@@ -371,6 +385,8 @@ lmhead_tc_kernel(const __grid_constant__ CUtensorMap map_h, const __grid_constan
   const int w_rows_max = DUAL ? blk_max / 2 : blk_max;   // W rows of one stage
   const int w_stage_bytes = w_rows_max * 128;
   TcShared* sh = reinterpret_cast<TcShared*>(w_smem + (size_t)w_stages * w_stage_bytes);
+  // logit staging boxes (1024-byte aligned: every ring stage is a multiple of 1 KB)
+  unsigned char* z_smem = w_smem + (size_t)w_stages * w_stage_bytes + kTcSharedBytes;
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   if (!MULTI) C = 1;
@@ -561,6 +577,11 @@ lmhead_tc_kernel(const __grid_constant__ CUtensorMap map_h, const __grid_constan
     p.idx = 0x7fffffff;
     bool bad = false;
     uint32_t tph = 0;
+    // this warp's two staging boxes: row `lane` at lane * 32 bytes, its two
+    // 16-byte halves swapped on rows 4-7 of every 8 (the 32-byte swizzle)
+    unsigned char* zbox = z_smem + (size_t)(warp - 2) * 2 * kZBoxBytes;
+    const int zsw = (lane >> 2) & 1;
+    int zb = 0;
     for (int blk = 0; blk < n_blocks; ++blk) {
       const int ab = DUAL ? 0 : (blk & 1);
       const int rows = blk_rows(blk);
@@ -577,6 +598,28 @@ lmhead_tc_kernel(const __grid_constant__ CUtensorMap map_h, const __grid_constan
                                    (uint32_t)(ab * kBlkMax + c), v);
         const int vb = r_begin + blk * blk_max + c;
         const int nvalid = min(min(32, rows - c), V - vb);
+        if (z_tma && nvalid > 0) {
+          // boxes of 8 columns x the warp's 32 rows; columns past V and rows
+          // past T fall outside the tensor and are not written
+#pragma unroll
+          for (int j = 0; j < 32; j += kZBoxCols) {
+            if (vb + j < V) {   // warp-uniform
+              unsigned char* box = zbox + zb * kZBoxBytes;
+              if (lane == 0) tc::bulk_wait_read<1>();   // the box's previous store has read it
+              __syncwarp();
+              float4* row = reinterpret_cast<float4*>(box + lane * 32);
+              row[zsw] = make_float4(v[j], v[j + 1], v[j + 2], v[j + 3]);
+              row[zsw ^ 1] = make_float4(v[j + 4], v[j + 5], v[j + 6], v[j + 7]);
+              tc::fence_proxy_async_smem();
+              __syncwarp();
+              if (lane == 0) {
+                tc::tma_store_2d(&map_z, box, vb + j, rank * kTileRows + quad * 32);
+                tc::bulk_commit();
+              }
+              zb ^= 1;
+            }
+          }
+        }
         if (!row_ok || nvalid <= 0) continue;
         bool fin = true;
         if (nvalid == 32) {
@@ -591,7 +634,7 @@ lmhead_tc_kernel(const __grid_constant__ CUtensorMap map_h, const __grid_constan
           }
         }
         bad |= !fin;
-        if (z_out) {
+        if (z_out && !z_tma) {
           float* dst = z_out + (size_t)t * V + vb;
           if (vec && nvalid == 32) {
 #pragma unroll
@@ -637,6 +680,8 @@ lmhead_tc_kernel(const __grid_constant__ CUtensorMap map_h, const __grid_constan
       __syncwarp();
       if (lane == 0) tc::mbar_arrive(&sh->tmem_empty[ab]);
     }
+    // the logits are written before the kernel ends
+    if (z_tma && lane == 0) tc::bulk_wait_all();
     if (bad) fail(status, EAGLE_ERR_NUMERIC);
     // the two column halves of every row: half 1 hands its partial to half 0
     const int tl = quad * 32 + lane;
@@ -683,6 +728,20 @@ bool make_map_bf16(CUtensorMap* map, const void* ptr, int rows, int cols, int bo
   return enc(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(ptr), dims, strides, box,
              estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
              CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+// 2-D fp32 logits [rows, cols] (cols contiguous, cols % 4 == 0) written in
+// boxes of kZBoxCols columns x 32 rows from 32-byte-swizzled shared memory.
+bool make_map_z(CUtensorMap* map, float* ptr, int rows, int cols) {
+  auto enc = get_encode();
+  if (!enc) return false;
+  cuuint64_t dims[2] = {(cuuint64_t)cols, (cuuint64_t)rows};
+  cuuint64_t strides[1] = {(cuuint64_t)cols * 4};
+  cuuint32_t box[2] = {(cuuint32_t)kZBoxCols, 32};
+  cuuint32_t estr[2] = {1, 1};
+  return enc(map, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 2, ptr, dims, strides, box, estr,
+             CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_32B,
+             CU_TENSOR_MAP_L2_PROMOTION_NONE, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
 int sm_count() {
@@ -821,8 +880,11 @@ extern "C" eagle_status eagle_lmhead_softmax(eagle_dtype dtype, int T, int H, in
     // cluster allows, with the tiles spread evenly over them (every CTA of
     // a launch holds real rows), so W is streamed once per launch.
     const int tiles = (T + kTileRows - 1) / kTileRows;
+    // logits through bulk tensor stores need 16-byte row strides
+    const bool z_want = z && (V % 4) == 0;
+    const size_t tile_smem = tc_layout(kTileRows, z_want).smem;
     int passes = 1, C = tiles;
-    while (C > 1 && (C > kMaxCluster || max_clusters(C, tc_layout(kTileRows).smem) < 1)) {
+    while (C > 1 && (C > kMaxCluster || max_clusters(C, tile_smem) < 1)) {
       ++passes;
       C = (tiles + passes - 1) / passes;
     }
@@ -830,7 +892,7 @@ extern "C" eagle_status eagle_lmhead_softmax(eagle_dtype dtype, int T, int H, in
     // the attention, which the step runs while the LM head is still
     // streaming W (it does not fit beside an LM head CTA)
     const int slices =
-        (C > 1) ? std::min(max_clusters(C, tc_layout(kTileRows).smem), n_units)
+        (C > 1) ? std::min(max_clusters(C, tile_smem), n_units)
                 : std::min(std::max(1, sm_count() - kSmsForOthers), n_units);
     for (int p = 0, tile0 = 0; p < passes; ++p) {
       const int nt = std::min(C, tiles - tile0);    // tiles of this launch
@@ -838,14 +900,17 @@ extern "C" eagle_status eagle_lmhead_softmax(eagle_dtype dtype, int T, int H, in
       const int Ts = std::min(nt * kTileRows, T - r0);
       tile0 += nt;
       const int Cp = (C > 1) ? nt : 1;
-      const TcLayout TL = tc_layout((Cp > 1 || Ts > kTileRows) ? kTileRows : ((Ts + 7) / 8) * 8);
+      const TcLayout TL =
+          tc_layout((Cp > 1 || Ts > kTileRows) ? kTileRows : ((Ts + 7) / 8) * 8, z_want);
       const __nv_bfloat16* hs = static_cast<const __nv_bfloat16*>(d_h) + (size_t)r0 * H;
-      CUtensorMap map_h;
+      float* zs = z ? z + (size_t)r0 * V : nullptr;
+      CUtensorMap map_h, map_z = map_w;   // without staging map_z is never read
       if (!make_map_bf16(&map_h, hs, Ts, H, TL.h_rows)) return EAGLE_ERR_CUDA;
+      if (TL.z_tma && !make_map_z(&map_z, zs, Ts, V)) return EAGLE_ERR_CUDA;
       // a last launch with fewer tiles keeps the slice count of the others
       // (its clusters are smaller, so they are resident too)
-      if (launch_tc(Cp, dim3(slices * Cp), TL.smem, s, map_h, map_w, Ts, H, V, temperature,
-                    z ? z + (size_t)r0 * V : nullptr, part + (size_t)r0 * slices, n_units,
+      if (launch_tc(Cp, dim3(slices * Cp), TL.smem, s, map_h, map_w, map_z, Ts, H, V,
+                    temperature, zs, (int)TL.z_tma, part + (size_t)r0 * slices, n_units,
                     TL.h_stage_bytes, TL.h_stages,
                     (Cp > 1 && kDualCluster) ? 2 * TL.blk : TL.blk, TL.w_stages, Cp,
                     d_status) !=

@@ -224,11 +224,10 @@ EAGLE_API eagle_status eagle_lmhead_softmax(eagle_dtype dtype, int T, int H, int
  * eagle_lmhead_softmax_noalloc -- eagle_lmhead_softmax without a workspace
  * argument.  The paper has no counterpart to this entry point.
  *
- * Some callers cannot hand the library a scratch buffer: code that runs
- * while a CUDA graph is being captured in a mode that forbids cudaMalloc,
- * plain-C hosts without an allocator of their own, or serving loops that run
- * under a framework's pooled allocator and may not allocate (or pay the
- * device synchronisation an allocation can cause) in the middle of a step.
+ * Some callers cannot hand the library a scratch buffer: plain-C hosts
+ * without an allocator of their own, or serving loops that run under a
+ * framework's pooled allocator and may not allocate (or pay the device
+ * synchronisation an allocation can cause) in the middle of a step.
  * This entry point keeps the LM head's per-row partial statistics in a
  * fixed array of the library's own device memory instead, and otherwise
  * takes the same arguments and produces the same results as
@@ -240,8 +239,7 @@ EAGLE_API eagle_status eagle_lmhead_softmax(eagle_dtype dtype, int T, int H, int
  *   - Every GPU that loads the library holds the 16 MiB array until the
  *     process exits.
  *   - The first call on each device looks up the array's device address
- *     (with that device current); make that first call before any stream
- *     capture on the device.
+ *     (with that device current) and keeps it for later calls.
  *   - All calls share the one array and it keeps the last call's contents.
  *     Calls whose work can overlap on a GPU (different streams without
  *     ordering between them) race on it and give undefined results; order

@@ -114,7 +114,12 @@ def test_lmhead_planted_ties_pick_the_lowest_index():
 
 @pytest.mark.parametrize("dtype,T,H,V,temp", [("f32", 26, 256, 1024, 0.7),
                                                ("bf16", 61, 4096, 32000, 1.0),
-                                               ("bf16", 300, 512, 2111, 0.7)])
+                                               ("bf16", 300, 512, 2111, 0.7),
+                                               # V % 4 == 0: logits staged and written by
+                                               # bulk tensor stores (one tile, then three
+                                               # sharing W), ragged last 8-column box
+                                               ("bf16", 100, 512, 4100, 1.0),
+                                               ("bf16", 300, 512, 2116, 0.7)])
 def test_lmhead_logits_mode(dtype, T, H, V, temp):
     # LOGITS mode stores z itself and the same statistics as the other modes
     import torch

@@ -1,8 +1,8 @@
 """The allocation-free LM head entry point, through the C ABI.
 
 eagle_lmhead_softmax_noalloc serves callers that cannot give the library a
-scratch buffer (for example code running under stream capture that forbids
-cudaMalloc, or a serving loop that must not allocate mid-step).  It keeps
+scratch buffer (for example a serving loop that must not allocate
+mid-step).  It keeps
 its scratch in a fixed array inside the library.  Its results must match
 eagle_lmhead_softmax's on the same inputs, call after call (the array keeps
 the previous call's contents, which must not leak into the next result).
