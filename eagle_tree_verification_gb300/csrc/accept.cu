@@ -28,7 +28,28 @@ using namespace eagle;
 
 namespace {
 
-constexpr int kStochThreads = 512;
+// Stochastic walk launch shape (build-time options, so that other shapes
+// can be measured): threads per CTA, CTAs resident per SM (the register cap
+// follows), the largest per-thread element count taken before a larger
+// cluster is, and the largest cluster.
+#ifndef EAGLE_WALK_THREADS
+#define EAGLE_WALK_THREADS 1024
+#endif
+#ifndef EAGLE_WALK_CTAS_PER_SM
+#define EAGLE_WALK_CTAS_PER_SM 1
+#endif
+#ifndef EAGLE_WALK_PREFER_ELEMS
+#define EAGLE_WALK_PREFER_ELEMS 8
+#endif
+#ifndef EAGLE_WALK_MAX_CLUSTER
+#define EAGLE_WALK_MAX_CLUSTER 16
+#endif
+constexpr int kStochThreads = EAGLE_WALK_THREADS;
+constexpr int kWalkCtasPerSm = EAGLE_WALK_CTAS_PER_SM;
+constexpr int kWalkPreferElems = EAGLE_WALK_PREFER_ELEMS;
+constexpr int kWalkMaxCluster = EAGLE_WALK_MAX_CLUSTER;
+static_assert(kStochThreads % 32 == 0 && kStochThreads <= 1024, "walk threads");
+static_assert(kWalkMaxCluster >= 1 && kWalkMaxCluster <= 16, "walk cluster");
 constexpr float kTwo40 = 1099511627776.0f;  // 2^40
 constexpr float kTwo24 = 16777216.0f;       // 2^24
 
@@ -253,7 +274,7 @@ __device__ __forceinline__ void walk_pass(float (&q)[E], float (&p)[E], int v0, 
 // LOGITS: P.q holds logits; each visited row is normalised as it is loaded,
 // by the LM head's probability-mode expression.
 template <int E, bool LOGITS>
-__global__ void __launch_bounds__(kStochThreads)
+__global__ void __launch_bounds__(kStochThreads, kWalkCtasPerSm)
 accept_stochastic_kernel(const StochParams P) {
   pdl_begin();
   cg::cluster_group cluster = cg::this_cluster();
@@ -521,11 +542,11 @@ accept_stochastic_kernel(const StochParams P) {
 // (Measured at 16 sequences of V = 128256: halving the clusters to fit
 // them all at once, 32 entries per thread, was slower than a second wave.)
 int pick_cluster(int V, int* slice_out, int* elems_out) {
-  for (int cs = 1; cs <= 16; cs <<= 1) {
+  for (int cs = 1; cs <= kWalkMaxCluster; cs <<= 1) {
     int slice = (V + cs - 1) / cs;
     slice = (slice + 3) & ~3;
     const int e = (slice + kStochThreads - 1) / kStochThreads;
-    if (e > 16 && cs < 16) continue;
+    if (e > kWalkPreferElems && cs < kWalkMaxCluster) continue;
     if (e > 32) return -1;
     *slice_out = slice;
     *elems_out = e <= 4 ? 4 : e <= 8 ? 8 : e <= 16 ? 16 : 32;
@@ -595,8 +616,13 @@ eagle_status launch_stochastic(bool logits, int B, int max_nodes, int V, int R, 
   const Kern kern = kerns[logits ? 1 : 0][ai];
   static PerDeviceOnce attr_once[2][4];
   if (attr_once[logits ? 1 : 0][ai].run([&] {
-        const cudaError_t e =
+        cudaError_t e =
             cudaFuncSetAttribute(kern, cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
+        if (e != cudaSuccess) return e;
+        // room for kWalkCtasPerSm CTAs' slices side by side
+        if (kWalkCtasPerSm > 1)
+          e = cudaFuncSetAttribute(kern, cudaFuncAttributePreferredSharedMemoryCarveout,
+                                   cudaSharedmemCarveoutMaxShared);
         if (e != cudaSuccess) return e;
         return cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                     160 * 1024);

@@ -32,6 +32,7 @@
 
 #include <algorithm>
 
+#include <cooperative_groups.h>
 #include <cudaTypedefs.h>
 
 #include "common.cuh"
@@ -147,6 +148,20 @@ constexpr int kGMaxCluster = 8;
 // one: the stages are then many and small.
 constexpr int kGMaxHStages = 24;
 constexpr int kGMaxWStages = 48;
+// A GEMM with few W rows for the GPU (one row tile, fewer 256-row blocks
+// than half the SMs) splits K over a cluster of up to this many CTAs per
+// block; their fp32 partial blocks are summed in rank order through
+// distributed shared memory before the epilogue.
+constexpr int kGMaxSplit = 8;
+// ... and only where every CTA still keeps this many K chunks (measured at
+// 65 rows: K = 14336 over 8 CTAs 80 us against 95 us unsplit; K = 4096 over
+// 6 or 8 CTAs 52-56 us against 35-37 us); a build-time option
+#ifndef EAGLE_GEMM_MIN_SPLIT_CHUNKS
+#define EAGLE_GEMM_MIN_SPLIT_CHUNKS 16
+#endif
+constexpr int kGMinSplitChunks = EAGLE_GEMM_MIN_SPLIT_CHUNKS;
+constexpr int kPartStride = kGBlk + 4;   // floats per partial row (bank spread)
+enum { CL_NONE = 0, CL_ROWS = 1, CL_SPLITK = 2 };
 constexpr size_t kGSmemLimit = 227 * 1024;
 constexpr size_t kGShared = 2048;
 
@@ -158,7 +173,6 @@ struct GemmShared {
   uint64_t tmem_full[2], tmem_empty[2], drain;
   uint32_t tmem_base;
   int abort_flag;
-  int consumed_w, consumed_h;
 };
 static_assert(sizeof(GemmShared) <= kGShared, "GemmShared must fit its slot");
 
@@ -166,6 +180,7 @@ struct GemmArgs {
   int T, N, K, C;           // rows, W rows, reduction length, CTAs per cluster
   int n_units, w_stages, h_stages, h_stage_bytes;
   int blk_max;              // W rows per block (and per W stage), a multiple of 32, <= 256
+  int ks;                   // split-K: CTAs of a cluster sharing one block (else 1)
   int epi;
   // outputs of the epilogues
   __nv_bfloat16* y;         // STORE [T, N]; SWIGLU [T, N/2]
@@ -266,10 +281,14 @@ __device__ __forceinline__ void gemm_epilogue(const GemmArgs& A, int t, int n0, 
   }
 }
 
-template <bool MULTI>
+// CL_ROWS: the row tiles of a cluster share every W stage by multicast.
+// CL_SPLITK: the CTAs of a cluster take consecutive K ranges of one block.
+template <int CL>
 __global__ void __launch_bounds__(kGThreads, 1)
 gemm_tc_kernel(const __grid_constant__ CUtensorMap map_a, const __grid_constant__ CUtensorMap map_w,
                const GemmArgs A) {
+  constexpr bool MULTI = (CL == CL_ROWS);
+  constexpr bool SPLITK = (CL == CL_SPLITK);
   extern __shared__ __align__(1024) unsigned char smem_raw[];
   unsigned char* base = reinterpret_cast<unsigned char*>(
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~(uintptr_t)1023);
@@ -283,15 +302,20 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap map_a, const __grid_constant_
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int C = MULTI ? A.C : 1;
-  const int rank = MULTI ? (int)tc::cluster_ctarank() : 0;   // this CTA's row tile
+  const int KS = SPLITK ? A.ks : 1;
+  const int rank = MULTI ? (int)tc::cluster_ctarank() : 0;    // this CTA's row tile
+  const int krank = SPLITK ? (int)tc::cluster_ctarank() : 0;  // this CTA's K range
   const uint16_t all_ctas = (uint16_t)((1u << C) - 1u);
-  const int slices = gridDim.x / C;
-  const int slice = blockIdx.x / C;
+  const int slices = gridDim.x / (C * KS);
+  const int slice = blockIdx.x / (C * KS);
   const int u0 = (int)((long long)A.n_units * slice / slices);
   const int u1 = (int)((long long)A.n_units * (slice + 1) / slices);
   const int r_begin = u0 * kGUnit, r_end = u1 * kGUnit;
   const int n_blocks = (r_end - r_begin + blk_max - 1) / blk_max;
-  const int KB = (A.K + kGBK - 1) / kGBK;
+  // K chunks kb0 .. kb0 + KB - 1 (split-K: this CTA's share)
+  const int KB_all = (A.K + kGBK - 1) / kGBK;
+  const int kb0 = (int)((long long)KB_all * krank / KS);
+  const int KB = (int)((long long)KB_all * (krank + 1) / KS) - kb0;
   const int total = n_blocks * KB;
   int* status = A.status;
   auto blk_rows = [&](int blk) { return min(blk_max, r_end - (r_begin + blk * blk_max)); };
@@ -300,10 +324,11 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap map_a, const __grid_constant_
     unsigned char* dst = w_smem + (size_t)stage * w_stage_bytes;
     for (int u = rank * kGUnit; u < rows; u += C * kGUnit) {
       if (MULTI)
-        tc::tma_load_2d_mc_hint(dst + u * 128, &map_w, &sh->w_full[stage], kb * kGBK, y0 + u,
-                                all_ctas, pol);
+        tc::tma_load_2d_mc_hint(dst + u * 128, &map_w, &sh->w_full[stage], (kb0 + kb) * kGBK,
+                                y0 + u, all_ctas, pol);
       else
-        tc::tma_load_2d_hint(dst + u * 128, &map_w, &sh->w_full[stage], kb * kGBK, y0 + u, pol);
+        tc::tma_load_2d_hint(dst + u * 128, &map_w, &sh->w_full[stage], (kb0 + kb) * kGBK,
+                             y0 + u, pol);
     }
   };
   const int w_early = min(w_stages, total);
@@ -323,8 +348,6 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap map_a, const __grid_constant_
     }
     tc::mbar_init(&sh->drain, 1);
     sh->abort_flag = 0;
-    sh->consumed_w = 0;
-    sh->consumed_h = 0;
     tc::fence_barrier_init();
   }
   if (MULTI) tc::cluster_sync_all();
@@ -365,7 +388,7 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap map_a, const __grid_constant_
           if (!(ok = tc::mbar_wait(&sh->h_empty[hs], hph ^ 1, abort_flag, status))) break;
           tc::mbar_arrive_expect_tx(&sh->h_full[hs], (uint32_t)A.h_stage_bytes);
           tc::tma_load_2d_hint(h_smem + hs * A.h_stage_bytes, &map_a, &sh->h_full[hs],
-                               kb * kGBK, rank * kGTile, pol_h);
+                               (kb0 + kb) * kGBK, rank * kGTile, pol_h);
           ++issued_h;
           if (++hs == h_stages) { hs = 0; hph ^= 1; }
           if (i >= w_early) {
@@ -382,48 +405,57 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap map_a, const __grid_constant_
       }
       if (!ok) {
         int never = 0;
-        for (int j = *(volatile int*)&sh->consumed_w; j < issued_w; ++j)
+        // (the last copy issued into each slot: waiting for its phase
+        // returns at once if it has landed, whether consumed or not)
+        for (int j = max(0, issued_w - w_stages); j < issued_w; ++j)
           tc::mbar_wait(&sh->w_full[j % w_stages], (j / w_stages) & 1, &never, nullptr,
                         200000000ll);
-        for (int j = *(volatile int*)&sh->consumed_h; j < issued_h; ++j)
+        for (int j = max(0, issued_h - h_stages); j < issued_h; ++j)
           tc::mbar_wait(&sh->h_full[j % h_stages], (j / h_stages) & 1, &never, nullptr,
                         200000000ll);
       }
     }
   } else if (warp == 1) {
+    // A K chunk's stages are released (its MMAs committed) right after its
+    // MMAs are issued; the next chunk's waits follow.
     if (lane == 0) {
       int hs = 0, ws = 0;
       uint32_t hph = 0, wph = 0, tph = 0;
       bool ok = true;
+      auto wait_chunk = [&](int& h_at, int& w_at) -> bool {
+        h_at = hs;
+        w_at = ws;
+        if (!tc::mbar_wait(&sh->h_full[hs], hph, abort_flag, status)) return false;
+        if (!tc::mbar_wait(&sh->w_full[ws], wph, abort_flag, status)) return false;
+        if (++hs == h_stages) { hs = 0; hph ^= 1; }
+        if (++ws == w_stages) { ws = 0; wph ^= 1; }
+        return true;
+      };
       for (int blk = 0; blk < n_blocks && ok; ++blk) {
         const int ab = blk & 1;
         if (!(ok = tc::mbar_wait(&sh->tmem_empty[ab], ((tph >> ab) & 1u) ^ 1u, abort_flag,
                                  status)))
           break;
         tph ^= 1u << ab;
-        tc::fence_after_thread_sync();
         const uint32_t idesc = tc::idesc_bf16_f32(128, blk_rows(blk));
         const uint32_t d = tmem + (uint32_t)(ab * kGBlk);
-        for (int kb = 0; kb < KB && ok; ++kb) {
-          if (!(ok = tc::mbar_wait(&sh->h_full[hs], hph, abort_flag, status))) break;
-          if (!(ok = tc::mbar_wait(&sh->w_full[ws], wph, abort_flag, status))) break;
+        int h_at, w_at;
+        if (!(ok = wait_chunk(h_at, w_at))) break;
+        for (int kb = 0; kb < KB; ++kb) {
           tc::fence_after_thread_sync();
-          const uint32_t a_base = tc::smem_u32(h_smem + hs * A.h_stage_bytes);
-          const uint32_t b_base = tc::smem_u32(w_smem + (size_t)ws * w_stage_bytes);
-#pragma unroll
-          for (int k16 = 0; k16 < kGBK / 16; ++k16)
-            tc::mma_f16(d, tc::desc_kmajor_sw128(a_base + k16 * 32),
-                        tc::desc_kmajor_sw128(b_base + k16 * 32), idesc,
-                        (kb > 0 || k16 > 0) ? 1u : 0u);
+          const uint64_t da = tc::desc_kmajor_sw128(tc::smem_u32(h_smem + h_at * A.h_stage_bytes));
+          const uint64_t db = tc::desc_kmajor_sw128(tc::smem_u32(w_smem + (size_t)w_at * w_stage_bytes));
+          // K steps of 16 advance the descriptors' start address by 32 bytes
+          tc::mma_f16(d, da, db, idesc, kb > 0 ? 1u : 0u);
+          tc::mma_f16(d, da + 2, db + 2, idesc, 1u);
+          tc::mma_f16(d, da + 4, db + 4, idesc, 1u);
+          tc::mma_f16(d, da + 6, db + 6, idesc, 1u);
           if (MULTI)
-            tc::mma_commit_mc(&sh->w_empty[ws], all_ctas);
+            tc::mma_commit_mc(&sh->w_empty[w_at], all_ctas);
           else
-            tc::mma_commit(&sh->w_empty[ws]);
-          tc::mma_commit(&sh->h_empty[hs]);
-          *(volatile int*)&sh->consumed_w += 1;
-          *(volatile int*)&sh->consumed_h += 1;
-          if (++ws == w_stages) { ws = 0; wph ^= 1; }
-          if (++hs == h_stages) { hs = 0; hph ^= 1; }
+            tc::mma_commit(&sh->w_empty[w_at]);
+          tc::mma_commit(&sh->h_empty[h_at]);
+          if (kb + 1 < KB && !(ok = wait_chunk(h_at, w_at))) break;
         }
         if (ok) tc::mma_commit(&sh->tmem_full[ab]);
       }
@@ -453,12 +485,53 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap map_a, const __grid_constant_
         float v[32];
         tc::tmem_ld_32x32b_x32(tmem + ((uint32_t)(quad * 32) << 16) +
                                    (uint32_t)(ab * kGBlk + c), v);
-        if (row_ok) gemm_epilogue(A, t, r_begin + blk * blk_max + c, v);
+        if (SPLITK) {
+          // this K range's partial of (row, c .. c+31) into the (idle) rings
+          if (row_ok) {
+            float4* dst = reinterpret_cast<float4*>(reinterpret_cast<float*>(base) +
+                                                    (size_t)t * kPartStride + c);
+#pragma unroll
+            for (int i = 0; i < 8; ++i)
+              dst[i] = make_float4(v[4 * i], v[4 * i + 1], v[4 * i + 2], v[4 * i + 3]);
+          }
+        } else if (row_ok) {
+          gemm_epilogue(A, t, r_begin + blk * blk_max + c, v);
+        }
       }
       tc::fence_before_thread_sync();
       __syncwarp();
       if (lane == 0) tc::mbar_arrive(&sh->tmem_empty[ab]);
     }
+  }
+  if (SPLITK) {
+    // every CTA's partial is in its shared memory: sum the K ranges in rank
+    // order, CTA krank taking every KS-th (row, 32-column) piece, then the
+    // epilogue on the sum
+    tc::cluster_sync_all();
+    cooperative_groups::cluster_group cluster = cooperative_groups::this_cluster();
+    const int rows = blk_rows(0);
+    const int pieces = A.T * (rows / kGUnit);
+    for (int j = krank + KS * (int)threadIdx.x; j < pieces; j += KS * (int)blockDim.x) {
+      const int row = j / (rows / kGUnit), c = (j % (rows / kGUnit)) * kGUnit;
+      float* mine = reinterpret_cast<float*>(base) + (size_t)row * kPartStride + c;
+      float v[32];
+#pragma unroll
+      for (int i = 0; i < 32; ++i) v[i] = 0.f;
+      for (int r = 0; r < KS; ++r) {
+        const float4* src = reinterpret_cast<const float4*>(cluster.map_shared_rank(mine, r));
+#pragma unroll
+        for (int i = 0; i < 8; ++i) {
+          const float4 x = src[i];
+          v[4 * i] += x.x;
+          v[4 * i + 1] += x.y;
+          v[4 * i + 2] += x.z;
+          v[4 * i + 3] += x.w;
+        }
+      }
+      gemm_epilogue(A, row, r_begin + c, v);
+    }
+    // no CTA leaves while a peer may still read its shared memory
+    tc::cluster_sync_all();
   }
   tc::fence_before_thread_sync();
   __syncthreads();
@@ -548,7 +621,7 @@ int g_max_clusters(int C, size_t smem) {
     cfg.attrs = attr;
     cfg.numAttrs = 1;
     int n = 0;
-    if (cudaOccupancyMaxActiveClusters(&n, (const void*)gemm_tc_kernel<true>, &cfg) !=
+    if (cudaOccupancyMaxActiveClusters(&n, (const void*)gemm_tc_kernel<CL_ROWS>, &cfg) !=
         cudaSuccess) {
       cudaGetLastError();
       n = 0;
@@ -562,12 +635,11 @@ eagle_status gemm_launch(int T, int N, int K, const void* d_a, const void* d_w, 
                          cudaStream_t s) {
   static PerDeviceOnce attr_once;
   if (attr_once.run([] {
-        cudaError_t e = cudaFuncSetAttribute(gemm_tc_kernel<false>,
-                                             cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                             (int)kGSmemLimit);
-        if (e == cudaSuccess)
-          e = cudaFuncSetAttribute(gemm_tc_kernel<true>,
-                                   cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kGSmemLimit);
+        cudaError_t e = cudaSuccess;
+        for (auto k : {gemm_tc_kernel<CL_NONE>, gemm_tc_kernel<CL_ROWS>, gemm_tc_kernel<CL_SPLITK>})
+          if (e == cudaSuccess)
+            e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                     (int)kGSmemLimit);
         return e;
       }) != cudaSuccess)
     return EAGLE_ERR_CUDA;
@@ -575,6 +647,45 @@ eagle_status gemm_launch(int T, int N, int K, const void* d_a, const void* d_w, 
   if (!g_map(&map_w, d_w, N, K, kGUnit)) return EAGLE_ERR_CUDA;
   const int n_units = N / kGUnit;
   const int tiles = (T + kGTile - 1) / kGTile;
+  const int KB_all = (K + kGBK - 1) / kGBK;
+  // one row tile and few 256-row blocks: split K over clusters instead
+  const int n_blk = (N + kGBlk - 1) / kGBlk;
+  const int ks = (tiles == 1) ? std::min({kGMaxSplit, g_sm_count() / n_blk,
+                                          KB_all / kGMinSplitChunks})
+                              : 1;
+  if (ks >= 2 && 2 * n_blk <= g_sm_count()) {
+    const GLayout L = g_layout(((T + 7) / 8) * 8, kGBlk);
+    CUtensorMap map_a;
+    if (!g_map(&map_a, d_a, T, K, L.h_stage_bytes / 128)) return EAGLE_ERR_CUDA;
+    GemmArgs P = A;
+    P.T = T;
+    P.N = N;
+    P.K = K;
+    P.C = 1;
+    P.ks = ks;
+    P.n_units = n_units;
+    P.w_stages = L.w_stages;
+    P.h_stages = L.h_stages;
+    P.h_stage_bytes = L.h_stage_bytes;
+    P.blk_max = L.blk;
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3((unsigned)(n_blk * ks));
+    cfg.blockDim = dim3(kGThreads);
+    cfg.dynamicSmemBytes = L.smem;
+    cfg.stream = s;
+    cudaLaunchAttribute attr[2];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    attr[1].id = cudaLaunchAttributeClusterDimension;
+    attr[1].val.clusterDim.x = (unsigned)ks;
+    attr[1].val.clusterDim.y = 1;
+    attr[1].val.clusterDim.z = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 2;
+    return cudaLaunchKernelEx(&cfg, gemm_tc_kernel<CL_SPLITK>, map_a, map_w, P) == cudaSuccess
+               ? EAGLE_OK
+               : EAGLE_ERR_CUDA;
+  }
   const GLayout TL = g_layout(kGTile, kGBlk);
   int passes = 1, C = tiles;
   while (C > 1 && (C > kGMaxCluster || g_max_clusters(C, TL.smem) < 1)) {
@@ -600,6 +711,7 @@ eagle_status gemm_launch(int T, int N, int K, const void* d_a, const void* d_w, 
     P.N = N;
     P.K = K;
     P.C = Cp;
+    P.ks = 1;
     P.n_units = n_units;
     P.w_stages = L.w_stages;
     P.h_stages = L.h_stages;
@@ -627,8 +739,9 @@ eagle_status gemm_launch(int T, int N, int K, const void* d_a, const void* d_w, 
     attr[1].val.clusterDim.z = 1;
     cfg.attrs = attr;
     cfg.numAttrs = (Cp > 1) ? 2 : 1;
-    const cudaError_t e = (Cp > 1) ? cudaLaunchKernelEx(&cfg, gemm_tc_kernel<true>, map_a, map_w, P)
-                                   : cudaLaunchKernelEx(&cfg, gemm_tc_kernel<false>, map_a, map_w, P);
+    const cudaError_t e =
+        (Cp > 1) ? cudaLaunchKernelEx(&cfg, gemm_tc_kernel<CL_ROWS>, map_a, map_w, P)
+                 : cudaLaunchKernelEx(&cfg, gemm_tc_kernel<CL_NONE>, map_a, map_w, P);
     if (e != cudaSuccess) return EAGLE_ERR_CUDA;
   }
   return EAGLE_OK;

@@ -292,7 +292,6 @@ struct TcShared {
   uint64_t tmem_full[2], tmem_empty[2], xbar, drain;
   uint32_t tmem_base;
   int abort_flag;
-  int consumed_w, consumed_h;
   Partial xchg[128];   // column half 1's partial of every row
 };
 
@@ -439,8 +438,6 @@ lmhead_tc_kernel(const __grid_constant__ CUtensorMap map_h, const __grid_constan
     tc::mbar_init(&sh->xbar, 32 * kEpiWarps);
     tc::mbar_init(&sh->drain, 1);
     sh->abort_flag = 0;
-    sh->consumed_w = 0;
-    sh->consumed_h = 0;
     tc::fence_barrier_init();
   }
   // the peers' barriers exist before any multicast reaches them
@@ -504,17 +501,22 @@ lmhead_tc_kernel(const __grid_constant__ CUtensorMap map_h, const __grid_constan
       }
       if (!ok) {
         // let every copy still in flight land before the CTA exits
+        // (the last copy issued into each slot: waiting for its phase
+        // returns at once if it has landed, whether consumed or not)
         int never = 0;
-        for (int i = *(volatile int*)&sh->consumed_w; i < issued_w; ++i)
+        for (int i = max(0, issued_w - w_stages); i < issued_w; ++i)
           tc::mbar_wait(&sh->w_full[i % w_stages], (i / w_stages) & 1, &never, nullptr,
                         200000000ll);
-        for (int i = *(volatile int*)&sh->consumed_h; i < issued_h; ++i)
+        for (int i = max(0, issued_h - h_stages); i < issued_h; ++i)
           tc::mbar_wait(&sh->h_full[i % h_stages], (i / h_stages) & 1, &never, nullptr,
                         200000000ll);
       }
     }
   } else if (warp == 1) {
     // ------------------------------------------------------------ MMA issuer
+    // Each W stage is released (its MMAs committed) as soon as its MMAs are
+    // issued: with clusters, a stage is refilled only once every CTA has
+    // released it, so an early release keeps the shared ring full.
     if (lane == 0) {
       int hs = 0, ws = 0;
       uint32_t hph = 0, wph = 0, tph = 0;   // tph bit b: phase of accumulator b
@@ -529,29 +531,29 @@ lmhead_tc_kernel(const __grid_constant__ CUtensorMap map_h, const __grid_constan
         const int nh = n_halves(blk);
         for (int kb = 0; kb < KB && ok; ++kb) {
           if (!(ok = tc::mbar_wait(&sh->h_full[hs], hph, abort_flag, status))) break;
-          const uint32_t a_base = tc::smem_u32(h_smem + hs * h_stage_bytes);
+          const uint64_t da = tc::desc_kmajor_sw128(tc::smem_u32(h_smem + hs * h_stage_bytes));
+          const uint32_t acc = kb > 0 ? 1u : 0u;
           for (int hf = 0; hf < nh && ok; ++hf) {
             if (!(ok = tc::mbar_wait(&sh->w_full[ws], wph, abort_flag, status))) break;
             tc::fence_after_thread_sync();
             // DUAL: half hf accumulates at TMEM column 256 * hf
             const uint32_t d = tmem + (uint32_t)((ab + hf) * kBlkMax);
             const uint32_t idesc = tc::idesc_bf16_f32(128, half_rows(blk, hf));
-            const uint32_t b_base = tc::smem_u32(w_smem + (size_t)ws * w_stage_bytes);
-#pragma unroll
-            for (int k16 = 0; k16 < kBK / 16; ++k16)
-              tc::mma_f16(d, tc::desc_kmajor_sw128(a_base + k16 * 32),
-                          tc::desc_kmajor_sw128(b_base + k16 * 32), idesc,
-                          (kb > 0 || k16 > 0) ? 1u : 0u);
+            const uint64_t db =
+                tc::desc_kmajor_sw128(tc::smem_u32(w_smem + (size_t)ws * w_stage_bytes));
+            // K steps of 16 advance the descriptors' start address by 32 bytes
+            tc::mma_f16(d, da, db, idesc, acc);
+            tc::mma_f16(d, da + 2, db + 2, idesc, 1u);
+            tc::mma_f16(d, da + 4, db + 4, idesc, 1u);
+            tc::mma_f16(d, da + 6, db + 6, idesc, 1u);
             if (MULTI)
               tc::mma_commit_mc(&sh->w_empty[ws], all_ctas);
             else
               tc::mma_commit(&sh->w_empty[ws]);
-            *(volatile int*)&sh->consumed_w += 1;
             if (++ws == w_stages) { ws = 0; wph ^= 1; }
           }
           if (!ok) break;
           tc::mma_commit(&sh->h_empty[hs]);
-          *(volatile int*)&sh->consumed_h += 1;
           if (++hs == h_stages) { hs = 0; hph ^= 1; }
         }
         if (ok) tc::mma_commit(&sh->tmem_full[ab]);

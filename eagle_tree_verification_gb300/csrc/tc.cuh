@@ -61,8 +61,10 @@ __device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, uint32_t parity) {
 // waiting for anything else.  Returns false if the wait did not succeed.
 __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, volatile int* abort_flag,
                                           int* status, long long max_cycles = EAGLE_WAIT_CYCLES) {
-  if (*abort_flag) return false;
+  // a completed phase is taken even after an abort elsewhere (the caller
+  // then stops at its next unfinished wait)
   if (mbar_try_wait(bar, parity)) return true;
+  if (*abort_flag) return false;
   const long long t0 = clock64();
   while (true) {
     if (mbar_try_wait(bar, parity)) return true;
