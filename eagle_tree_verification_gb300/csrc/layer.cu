@@ -153,11 +153,12 @@ constexpr int kGMaxWStages = 48;
 // block; their fp32 partial blocks are summed in rank order through
 // distributed shared memory before the epilogue.
 constexpr int kGMaxSplit = 8;
-// ... and only where every CTA still keeps this many K chunks (measured at
-// 65 rows: K = 14336 over 8 CTAs 80 us against 95 us unsplit; K = 4096 over
-// 6 or 8 CTAs 52-56 us against 35-37 us); a build-time option
+// ... with every CTA keeping at least this many K chunks, and all clusters
+// resident at once (a second wave of clusters cost more than the split
+// gains: 65 rows x K = 4096 in 16 clusters of 8 with 15 resident took 56 us
+// against 37 us unsplit, 29 us in 16 clusters of 4); a build-time option
 #ifndef EAGLE_GEMM_MIN_SPLIT_CHUNKS
-#define EAGLE_GEMM_MIN_SPLIT_CHUNKS 16
+#define EAGLE_GEMM_MIN_SPLIT_CHUNKS 8
 #endif
 constexpr int kGMinSplitChunks = EAGLE_GEMM_MIN_SPLIT_CHUNKS;
 constexpr int kPartStride = kGBlk + 4;   // floats per partial row (bank spread)
@@ -603,11 +604,19 @@ GLayout g_layout(int h_rows, int blk) {
   return L;
 }
 
+// Clusters of C CTAs of the given kind resident at once (0: none), per
+// device, cluster size and shared-memory size.
+template <int CL>
 int g_max_clusters(int C, size_t smem) {
   static std::mutex mu;
   static int cached[kMaxDevices][kGMaxCluster + 1] = {};
+  static size_t cached_smem[kMaxDevices][kGMaxCluster + 1] = {};
   std::lock_guard<std::mutex> lock(mu);
   const int dev = current_device_slot();
+  if (cached_smem[dev][C] != smem) {
+    cached[dev][C] = 0;
+    cached_smem[dev][C] = smem;
+  }
   if (!cached[dev][C]) {
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3((unsigned)(C * 64));
@@ -621,7 +630,7 @@ int g_max_clusters(int C, size_t smem) {
     cfg.attrs = attr;
     cfg.numAttrs = 1;
     int n = 0;
-    if (cudaOccupancyMaxActiveClusters(&n, (const void*)gemm_tc_kernel<CL_ROWS>, &cfg) !=
+    if (cudaOccupancyMaxActiveClusters(&n, (const void*)gemm_tc_kernel<CL>, &cfg) !=
         cudaSuccess) {
       cudaGetLastError();
       n = 0;
@@ -650,11 +659,13 @@ eagle_status gemm_launch(int T, int N, int K, const void* d_a, const void* d_w, 
   const int KB_all = (K + kGBK - 1) / kGBK;
   // one row tile and few 256-row blocks: split K over clusters instead
   const int n_blk = (N + kGBlk - 1) / kGBlk;
-  const int ks = (tiles == 1) ? std::min({kGMaxSplit, g_sm_count() / n_blk,
-                                          KB_all / kGMinSplitChunks})
-                              : 1;
-  if (ks >= 2 && 2 * n_blk <= g_sm_count()) {
-    const GLayout L = g_layout(((T + 7) / 8) * 8, kGBlk);
+  int ks = (tiles == 1 && 2 * n_blk <= g_sm_count())
+               ? std::min({kGMaxSplit, g_sm_count() / n_blk, KB_all / kGMinSplitChunks})
+               : 1;
+  const GLayout LS = g_layout(((T + 7) / 8) * 8, kGBlk);
+  while (ks >= 2 && g_max_clusters<CL_SPLITK>(ks, LS.smem) < n_blk) --ks;
+  if (ks >= 2) {
+    const GLayout& L = LS;
     CUtensorMap map_a;
     if (!g_map(&map_a, d_a, T, K, L.h_stage_bytes / 128)) return EAGLE_ERR_CUDA;
     GemmArgs P = A;
@@ -688,11 +699,11 @@ eagle_status gemm_launch(int T, int N, int K, const void* d_a, const void* d_w, 
   }
   const GLayout TL = g_layout(kGTile, kGBlk);
   int passes = 1, C = tiles;
-  while (C > 1 && (C > kGMaxCluster || g_max_clusters(C, TL.smem) < 1)) {
+  while (C > 1 && (C > kGMaxCluster || g_max_clusters<CL_ROWS>(C, TL.smem) < 1)) {
     ++passes;
     C = (tiles + passes - 1) / passes;
   }
-  const int slices = (C > 1) ? std::min(g_max_clusters(C, TL.smem), n_units)
+  const int slices = (C > 1) ? std::min(g_max_clusters<CL_ROWS>(C, TL.smem), n_units)
                              : std::min(g_sm_count(), n_units);
   for (int p = 0, tile0 = 0; p < passes; ++p) {
     const int nt = std::min(C, tiles - tile0);
