@@ -197,12 +197,16 @@ struct AttPlan {
 // four chunks took 461 us against 224 us unsplit -- clusters of 170 KB CTAs
 // wait for four free SMs of one GPC -- so launches of more tiles than SMs
 // stay unsplit.)
+#ifndef EAGLE_ATTN_MIN_SPLIT
+#define EAGLE_ATTN_MIN_SPLIT 1
+#endif
 AttPlan att_plan(int B, int Hq, int Hkv, int max_nodes, int max_kv, int split_cap) {
   AttPlan P;
   P.G = Hq / Hkv;
   P.MT = (max_nodes * P.G + 127) / 128;
   const int tiles = std::max(1, B * Hkv * P.MT);
-  const int nc = std::min(split_cap, std::max(1, kTargetCtas / tiles));
+  const int nc = std::max(EAGLE_ATTN_MIN_SPLIT,
+                          std::min(split_cap, std::max(1, kTargetCtas / tiles)));
   int ck = (max_kv + nc - 1) / nc;
   ck = std::max(256, ((ck + kKeyBlk - 1) / kKeyBlk) * kKeyBlk);
   P.CK = ck;
