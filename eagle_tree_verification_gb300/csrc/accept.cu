@@ -173,32 +173,23 @@ __device__ __forceinline__ unsigned long long fixed40_int(float r) {
 // above it x is already an integer.
 __device__ __forceinline__ float fixed40_f(float r) { return truncf(r * kTwo40); }
 
-// Two sums over the block at once; every thread gets both totals.
+// Two sums over the block at once; every thread gets both totals.  One
+// barrier: the warps' partial sums go to s_tmp[par] (alternate the parity
+// from one call to the next, so a call never overwrites partials another
+// warp may still be reading), and every warp adds them up itself.
 __device__ void block_sum2_u64(unsigned long long& a, unsigned long long& b,
-                               unsigned long long* s_tmp /* 66 */) {
+                               unsigned long long (*s_tmp)[2][32], int par) {
   a = warp_sum_u64(a);
   b = warp_sum_u64(b);
   const int w = threadIdx.x >> 5, l = threadIdx.x & 31;
-  __syncthreads();
   if (l == 0) {
-    s_tmp[w] = a;
-    s_tmp[33 + w] = b;
+    s_tmp[par][0][w] = a;
+    s_tmp[par][1][w] = b;
   }
   __syncthreads();
-  if (w == 0) {
-    const int nw = blockDim.x >> 5;
-    unsigned long long x = (l < nw) ? s_tmp[l] : 0ull;
-    unsigned long long y = (l < nw) ? s_tmp[33 + l] : 0ull;
-    x = warp_sum_u64(x);
-    y = warp_sum_u64(y);
-    if (l == 0) {
-      s_tmp[32] = x;
-      s_tmp[65] = y;
-    }
-  }
-  __syncthreads();
-  a = s_tmp[32];
-  b = s_tmp[65];
+  const int nw = blockDim.x >> 5;
+  a = warp_sum_u64((l < nw) ? s_tmp[par][0][l] : 0ull);
+  b = warp_sum_u64((l < nw) ? s_tmp[par][1][l] : 0ull);
 }
 
 // Exclusive scan over the block of one value per thread; returns the
@@ -289,6 +280,7 @@ accept_stochastic_kernel(const StochParams P) {
   int* s_tok = s_par + P.max_nodes;
   int* s_kids = s_tok + P.max_nodes;
   __shared__ unsigned long long s_red[66];
+  __shared__ unsigned long long s_sum2[2][2][32];   // block_sum2_u64 partials, by round parity
   __shared__ RoundSlot s_slot[2];            // double-buffered by round parity
   // What every CTA of the cluster pushed here, by round parity: its sums,
   // the tested token's q and p (from the CTA that owns the token), and for
@@ -404,7 +396,7 @@ accept_stochastic_kernel(const StochParams P) {
     unsigned long long Z = 0, SP = 0;
     float qt = 0.f, pt = 0.f;
     auto reduce_round = [&](unsigned long long sw, unsigned long long sp, int t) {
-      block_sum2_u64(sw, sp, s_red);
+      block_sum2_u64(sw, sp, s_sum2, par);
       const unsigned owner = (unsigned)(t / P.slice);
       if (tid < (int)CS) {
         unsigned long long* d = cluster.map_shared_rank(&s_all[par][rank][0], (unsigned)tid);
