@@ -155,18 +155,14 @@ eagle_status launch_warp(int D, int B, int T, int Hq, int Hkv, float scale, int 
 // ---------------------------------------------------------------------------
 // tcgen05 path (bf16, D = 128)
 // ---------------------------------------------------------------------------
-constexpr int kAttThreads = 576;        // warp 0 TMA, warp 1 MMA, warps 2-17 rows
-constexpr int kRowWarps = 16;           // four per TMEM lane quarter, one per key quarter
-static_assert(kAttThreads == 64 + 32 * kRowWarps, "TMA warp, MMA warp, row warps");
-// TMEM columns: two S slots, P (bf16 hi | lo per key quarter), O
-constexpr uint32_t kColS = 0, kColP = 256, kColO = 384;
+constexpr int kAttThreads = 320;        // warp 0 TMA, warp 1 MMA, warps 2-9 rows
 constexpr float kRescaleLog2 = 8.f;     // rescale O only when the max grows by > 2^8
 constexpr int kKeyBlk = 128;            // keys per block (the S MMA's N)
 constexpr int kHalfBytes = 128 * 128;   // 128 rows x 64 bf16 (one swizzle atom wide)
 constexpr int kTileBytes = 2 * kHalfBytes;  // 128 rows x 128 bf16
 constexpr int kTargetCtas = 152;        // SMs of a GB300
 constexpr int kMaxSplit = 8;            // cache chunks of one tile: one portable cluster
-constexpr size_t kAttSharedBytes = 9216;
+constexpr size_t kAttSharedBytes = 5120;
 // cluster merge inside the K/V stage memory: O rows [NC][rows per owner][32]
 // float4 (at most 136 x 512 B), then (max, sum) pairs
 constexpr int kMergeMlOffset = 73728;
@@ -178,13 +174,14 @@ constexpr size_t kAttSmem = 1024 + 5 * (size_t)kTileBytes + kAttSharedBytes;
 struct AttShared {
   uint64_t q_full;
   uint64_t k_full[2], k_empty[2], v_full[2], v_empty[2];
-  uint64_t s_full[2], s_empty[2];  // S slot ready / read by every row warp
+  uint64_t s_full, s_empty;        // S ready / read by every row warp
   uint64_t p_full;                 // P written by every row warp
   uint64_t pv_done, o_done, drain;
+  uint64_t fbar;                   // row-half exchange after the key loop
   uint32_t tmem_base;
   int abort_flag;
-  float xmax[2][4][128];           // block maxima of the key quarters, by block parity
-  float xl[4][128];                // the key quarters' sums after the key loop
+  float xchg[2][2][128];           // [m | l][half][row]
+  float2 ml[128];                  // (m, l) of every row, read by the cluster
   int par[EAGLE_MAX_TREE_NODES];   // parent[] of the sequence
 };
 
@@ -239,6 +236,11 @@ __device__ __forceinline__ float ex2_approx(float x) {
   float y;
   asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
   return y;
+}
+
+__device__ __forceinline__ uint32_t pack_bf16(float a, float b) {
+  __nv_bfloat162 v = __floats2bfloat162_rn(a, b);
+  return *reinterpret_cast<uint32_t*>(&v);
 }
 
 // MN-major (rows of 64 N-elements, one row per K index) 128-byte-swizzled
@@ -297,31 +299,14 @@ __device__ __forceinline__ void tmem_wait_st() {
   asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
 }
 
-// AND of `pred` over the `count` threads meeting at named barrier `id`
-// (also a barrier for their shared-memory accesses).
-__device__ __forceinline__ bool bar_and(int id, int count, bool pred) {
-  uint32_t out;
-  asm volatile(
-      "{\n\t.reg .pred pi, po;\n\t"
-      "setp.ne.u32 pi, %1, 0;\n\t"
-      "bar.red.and.pred po, %2, %3, pi;\n\t"
-      "selp.u32 %0, 1, 0, po;\n\t}"
-      : "=r"(out)
-      : "r"((uint32_t)pred), "r"(id), "r"(count)
-      : "memory");
-  return out != 0;
-}
-
 // One CTA per (sequence, kv head, 128-row tile, cache chunk); the chunks of
 // a tile form a thread-block cluster and merge their partial softmax rows
-// through distributed shared memory.  Four threads per query row (warps of
-// one TMEM lane quarter), one per 32-key quarter of every key block; they
-// share the row's running max (block maxima exchanged through shared
-// memory at a named barrier of the quarter's four warps) and one output
-// accumulator, and keep their own partial sums.  TMEM columns: two S slots
-// at 0 and 128 (block j in slot j % 2, so the next block's S is computed
-// while this one is read), P at 256 (per key quarter: bf16 hi at +0, lo at
-// +16), O at 384.
+// through distributed shared memory.  Two threads per query row, one per
+// half of every key block; each half keeps its own running max, sum and
+// output accumulator, so the halves never wait for each other inside the
+// key loop and are merged once at the end.  TMEM columns: S at 0 (refilled
+// with the next block as soon as every row has read it), P at 128 (per key
+// half: bf16 hi at +0, lo at +32), O of key half 0 at 256, of half 1 at 384.
 __global__ void __launch_bounds__(kAttThreads, 1)
 tree_attn_tc_kernel(const __grid_constant__ CUtensorMap map_q,
                     const __grid_constant__ CUtensorMap map_kc,
@@ -335,6 +320,7 @@ tree_attn_tc_kernel(const __grid_constant__ CUtensorMap map_q,
   unsigned char* k_sm = base + kTileBytes;          // 2 stages
   unsigned char* v_sm = base + 3 * kTileBytes;      // 2 stages
   AttShared* sh = reinterpret_cast<AttShared*>(base + 5 * kTileBytes);
+  float4* obuf = reinterpret_cast<float4*>(k_sm);   // merge: [128 rows][32 float4], swizzled
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   // work item: tile * NC + c, the cache chunks of a tile adjacent (one cluster)
@@ -431,19 +417,18 @@ tree_attn_tc_kernel(const __grid_constant__ CUtensorMap map_q,
   // row quads (32 rows) holding at least one node of the tile
   int active_quads = 0;
   for (int q = 0; q < 4; ++q) active_quads += ((mt * 128 + q * 32) / A.G < n);
-  const int active_warps = 4 * active_quads;
+  const int active_warps = 2 * active_quads;
   volatile int* abort_flag = &sh->abort_flag;
   int* status = A.status;
 
   if (threadIdx.x == 0) {
-    for (int i = 0; i < 2; ++i) {
-      tc::mbar_init(&sh->s_full[i], 1);
-      tc::mbar_init(&sh->s_empty[i], active_warps);
-    }
+    tc::mbar_init(&sh->s_full, 1);
+    tc::mbar_init(&sh->s_empty, active_warps);
     tc::mbar_init(&sh->p_full, active_warps);
     tc::mbar_init(&sh->pv_done, 1);
     tc::mbar_init(&sh->o_done, 1);
     tc::mbar_init(&sh->drain, 1);
+    tc::mbar_init(&sh->fbar, 32 * active_warps);
     sh->abort_flag = 0;
     tc::fence_barrier_init();
     // the queries and the first blocks not requested before the wait
@@ -469,12 +454,11 @@ tree_attn_tc_kernel(const __grid_constant__ CUtensorMap map_q,
   const uint32_t tmem = sh->tmem_base;
 
   // row-thread state carried into the merge
-  const int quad = warp & 3;                        // TMEM lane quarter
-  const int kq = (warp - 2) >> 2;                   // key quarter of every block
+  const int quad = warp & 3;
+  const int half = (warp - 2) >> 2;                 // key half of every block
   const int r = quad * 32 + lane;                   // row in the tile
   const bool row_warp = warp >= 2 && quad < active_quads;
-  const int qbar = 1 + quad;                        // named barrier of the quarter's warps
-  float o[32];                                      // output columns kq*32 .. +31
+  float o0[32], o1[32];                             // output columns half*64 .. +63
   float m_row = -INFINITY, l_row = 0.f;
   bool ok = true;
 
@@ -520,59 +504,58 @@ tree_attn_tc_kernel(const __grid_constant__ CUtensorMap map_q,
         const uint32_t q_addr = tc::smem_u32(q_sm);
         bool mok = tc::mbar_wait(&sh->q_full, 0, abort_flag, status);
         uint32_t kph = 0, vph = 0;   // bit st: phase parity per stage
-        // S of block j into slot j % 2 (the K stage of the same parity)
         auto issue_s = [&](int j) -> bool {
           const int st = j & 1;
           if (!tc::mbar_wait(&sh->k_full[st], (kph >> st) & 1u, abort_flag, status)) return false;
           kph ^= 1u << st;
           tc::fence_after_thread_sync();
           const uint32_t k_addr = tc::smem_u32(k_sm + st * kTileBytes);
-          const uint32_t d = tmem + kColS + (uint32_t)(st * kKeyBlk);
 #pragma unroll
           for (int k16 = 0; k16 < 8; ++k16) {
             const uint32_t off = (uint32_t)((k16 >> 2) * kHalfBytes + (k16 & 3) * 32);
-            tc::mma_f16(d, tc::desc_kmajor_sw128(q_addr + off), tc::desc_kmajor_sw128(k_addr + off),
-                        idesc_s, k16 > 0 ? 1u : 0u);
+            tc::mma_f16(tmem, tc::desc_kmajor_sw128(q_addr + off),
+                        tc::desc_kmajor_sw128(k_addr + off), idesc_s, k16 > 0 ? 1u : 0u);
           }
-          tc::mma_commit(&sh->s_full[st]);
+          tc::mma_commit(&sh->s_full);
           tc::mma_commit(&sh->k_empty[st]);
           return true;
         };
         if (mok) mok = issue_s(0);
-        if (mok && nblk > 1) mok = issue_s(1);
         for (int j = 0; j < nblk && mok; ++j) {
           const int st = j & 1;
+          if (j + 1 < nblk) {
+            // the next S goes into the slot as soon as every row has read this one
+            if (!(mok = tc::mbar_wait(&sh->s_empty, (uint32_t)(j & 1), abort_flag, status))) break;
+            if (!(mok = issue_s(j + 1))) break;
+          }
           if (!(mok = tc::mbar_wait(&sh->p_full, (uint32_t)(j & 1), abort_flag, status))) break;
           if (!(mok = tc::mbar_wait(&sh->v_full[st], (vph >> st) & 1u, abort_flag, status))) break;
           vph ^= 1u << st;
           tc::fence_after_thread_sync();
           const uint32_t v_addr = tc::smem_u32(v_sm + st * kTileBytes);
-          // O += P_hi V + P_lo V over the block's 128 keys in steps of 16:
-          // A = P from the key quarter's TMEM columns, B = V rows of the step
-          // (MN-major, 128-byte rows).  (One bf16 P alone would round every
-          // weight by up to 2^-8 of itself -- up to 2^-8 of sum_j p_j |v_j|
-          // in the output when few keys dominate, above the 2e-3 bound;
-          // hi + lo keep 2^-16.)
+          // O_h += P_hi V_h + P_lo V_h for key half h: A = P from the half's
+          // TMEM columns, B = V rows of that half (MN-major, 128-byte rows).
+          // The two halves' accumulator chains are interleaved (each in its
+          // own order), so the tensor pipe always has an independent MMA.
+          // (One bf16 P alone would round every weight by up to 2^-8 of
+          // itself -- up to 2^-8 of sum_j p_j |v_j| in the output when few
+          // keys dominate, above the 2e-3 bound; hi + lo keep 2^-16.)
 #pragma unroll
           for (int part = 0; part < 2; ++part) {
 #pragma unroll
-            for (int ks = 0; ks < 8; ++ks) {
-              const uint32_t a_tm =
-                  tmem + kColP + (uint32_t)((ks >> 1) * 32 + part * 16 + (ks & 1) * 8);
-              mma_f16_tmem_a(tmem + kColO, a_tm,
-                             desc_mnmajor_sw128(v_addr + (uint32_t)(ks * 16) * 128u, kHalfBytes),
-                             idesc_o, (j > 0 || part > 0 || ks > 0) ? 1u : 0u);
+            for (int kk = 0; kk < 4; ++kk) {
+#pragma unroll
+              for (int h = 0; h < 2; ++h) {
+                const uint32_t a_tm = tmem + (uint32_t)(128 + h * 64 + part * 32 + kk * 8);
+                const uint32_t key = (uint32_t)(h * 64 + kk * 16);
+                mma_f16_tmem_a(tmem + 256u + (uint32_t)(h * 128), a_tm,
+                               desc_mnmajor_sw128(v_addr + key * 128u, kHalfBytes), idesc_o,
+                               (j > 0 || part > 0 || kk > 0) ? 1u : 0u);
+              }
             }
           }
           tc::mma_commit(&sh->pv_done);
           tc::mma_commit(&sh->v_empty[st]);
-          if (j + 2 < nblk) {
-            // slot st takes block j + 2 once every row has read block j
-            if (!(mok = tc::mbar_wait(&sh->s_empty[st], (uint32_t)((j >> 1) & 1), abort_flag,
-                                      status)))
-              break;
-            if (!(mok = issue_s(j + 2))) break;
-          }
         }
         if (mok) tc::mma_commit(&sh->o_done);
       }
@@ -585,63 +568,66 @@ tree_attn_tc_kernel(const __grid_constant__ CUtensorMap map_q,
     const int qrow = mt * 128 + r;                    // (node, head) row of (b, g)
     const int node = qrow / A.G;
     const bool row_ok = node < n;
-    // ancestor-or-self bits of this row's node among tree keys
-    // tb * 128 + kq * 32 .. +31 (tree block tb = 0, 1)
-    uint32_t anc0 = 0u, anc1 = 0u;
+    // ancestor-or-self bits of this row's node: word w covers tree nodes
+    // 32*w .. 32*w+31
+    uint32_t anc[EAGLE_MAX_TREE_NODES / 32];
+#pragma unroll
+    for (int w = 0; w < EAGLE_MAX_TREE_NODES / 32; ++w) anc[w] = 0u;
     if (row_ok && with_tree) {
       int j = node, steps = 0;
       while (j >= 0) {
-        if ((j >> 5) == kq) anc0 |= 1u << (j & 31);
-        if ((j >> 5) == 4 + kq) anc1 |= 1u << (j & 31);
+#pragma unroll
+        for (int w = 0; w < EAGLE_MAX_TREE_NODES / 32; ++w)
+          if ((j >> 5) == w) anc[w] |= 1u << (j & 31);
         const int p = sh->par[j];
         if ((j == 0) ? (p != -1) : (p < 0 || p >= j) || ++steps > n) {
-          if (kq == 0) fail(status, EAGLE_ERR_INVALID_TREE);
+          if (half == 0) fail(status, EAGLE_ERR_INVALID_TREE);
           break;
         }
         j = p;
       }
     }
     const uint32_t trow = tmem + ((uint32_t)(quad * 32) << 16);
-    const uint32_t o_cols = trow + kColO + (uint32_t)(kq * 32);   // this thread's O columns
-    float m = -INFINITY, l = 0.f;   // the row's running max (log2 units); this quarter's sum
-    for (int j = 0; j < nblk; ++j) {
-      const int st = j & 1;
-      const bool got = tc::mbar_wait(&sh->s_full[st], (uint32_t)((j >> 1) & 1), abort_flag, status);
+    const uint32_t o_own = trow + 256u + (uint32_t)(half * 128);   // this key half's O
+    float m = -INFINITY, l = 0.f;   // this key half's running max (log2 units) and sum
+    for (int j = 0; j < nblk && ok; ++j) {
+      const bool got = tc::mbar_wait(&sh->s_full, (uint32_t)(j & 1), abort_flag, status);
+      if (!(ok = __all_sync(0xffffffffu, got))) break;
+      tc::fence_after_thread_sync();
       const bool tree_blk = j >= n_cache_blk;
       const int tb = tree_blk ? j - n_cache_blk : 0;          // tree block 0 or 1
-      const int key0 = (tree_blk ? tb * kKeyBlk : key_begin + j * kKeyBlk) + kq * 32;
+      const int key0 = (tree_blk ? tb * kKeyBlk : key_begin + j * kKeyBlk) + half * 64;
       const int key_lim = tree_blk ? n : key_end;
-      float v[32];
-      if (__all_sync(0xffffffffu, got)) {
-        tc::fence_after_thread_sync();
-        tc::tmem_ld_32x32b_x32(trow + kColS + (uint32_t)(st * kKeyBlk + kq * 32), v);
-      } else {
-#pragma unroll
-        for (int i = 0; i < 32; ++i) v[i] = -INFINITY;
-      }
-      // the S slot may take block j + 2
+      const uint32_t s_addr = trow + (uint32_t)(half * 64);
+      float v0[32], v1[32];
+      tc::tmem_ld_32x32b_x32(s_addr, v0);
+      tc::tmem_ld_32x32b_x32(s_addr + 32u, v1);
+      // the S slot may take the next block
       tc::fence_before_thread_sync();
       __syncwarp();
-      if (lane == 0) tc::mbar_arrive(&sh->s_empty[st]);
-      const uint32_t wm = !tree_blk ? 0xffffffffu : (tb ? anc1 : anc0);
-      const int nv = min(32, max(0, key_lim - key0));
-      if (tree_blk || nv < 32) {
+      if (lane == 0) tc::mbar_arrive(&sh->s_empty);
+      // bitset words for key columns half*64 .. +63 of tree block tb (static indices)
+      const uint32_t w0 = !tree_blk ? 0xffffffffu
+                          : tb ? (half ? anc[6] : anc[4]) : (half ? anc[2] : anc[0]);
+      const uint32_t w1 = !tree_blk ? 0xffffffffu
+                          : tb ? (half ? anc[7] : anc[5]) : (half ? anc[3] : anc[1]);
+      const int nv0 = min(32, max(0, key_lim - key0));
+      const int nv1 = min(32, max(0, key_lim - key0 - 32));
+      if (tree_blk || nv1 < 32) {
         // masked or ragged block (warp-uniform): hidden scores become -inf
 #pragma unroll
-        for (int i = 0; i < 32; ++i)
-          if (!(i < nv && ((wm >> i) & 1u))) v[i] = -INFINITY;
+        for (int i = 0; i < 32; ++i) {
+          if (!(i < nv0 && ((w0 >> i) & 1u))) v0[i] = -INFINITY;
+          if (!(i < nv1 && ((w1 >> i) & 1u))) v1[i] = -INFINITY;
+        }
       }
-      float bm0 = v[0], bm1 = v[1];
+      float bm0 = v0[0], bm1 = v1[0];
 #pragma unroll
-      for (int i = 2; i < 32; i += 2) {
-        bm0 = fmaxf(bm0, v[i]);
-        bm1 = fmaxf(bm1, v[i + 1]);
+      for (int i = 1; i < 32; ++i) {
+        bm0 = fmaxf(bm0, v0[i]);
+        bm1 = fmaxf(bm1, v1[i]);
       }
-      sh->xmax[st][kq][r] = fmaxf(bm0, bm1) * A.scale_log2;
-      // the four quarters' maxima (and whether every quarter got S)
-      if (!(ok = bar_and(qbar, 128, got))) break;
-      const float bm = fmaxf(fmaxf(sh->xmax[st][0][r], sh->xmax[st][1][r]),
-                             fmaxf(sh->xmax[st][2][r], sh->xmax[st][3][r]));
+      const float bm = fmaxf(bm0, bm1) * A.scale_log2;
       const float mn = fmaxf(m, bm);
       const bool first = (m == -INFINITY);
       const bool rescale = !first && (mn > m + kRescaleLog2);
@@ -649,42 +635,52 @@ tree_attn_tc_kernel(const __grid_constant__ CUtensorMap map_q,
       // P = exp2(s - mu) = hi + lo, both bf16: hi keeps the top 16 bits of
       // the fp32 value, lo = P - hi (exact in fp32) truncated the same way;
       // |P - hi - lo| < 2^-14 P.  Computed before waiting for the previous
-      // PV, which still reads the P columns.  A row with nothing visible yet
-      // keeps mu = -inf: its scores are all -inf, and any finite offset
-      // gives P = 0.
-      const float neg_mu = (mu == -INFINITY) ? 0.f : -mu;
+      // PV, which still reads the P columns.
       float psum = 0.f;
-      uint32_t hi[16], lo[16];
+      // a half-row with nothing visible yet keeps mu = -inf: its scores are
+      // all -inf, and any finite offset gives P = 0
+      const float neg_mu = (mu == -INFINITY) ? 0.f : -mu;
+      uint32_t hi0[16], lo0[16], hi1[16], lo1[16];
+      auto split = [&](const float (&v)[32], uint32_t (&hi)[16], uint32_t (&lo)[16]) {
 #pragma unroll
-      for (int i = 0; i < 16; ++i) {
-        const float p0 = ex2_approx(fmaf(v[2 * i], A.scale_log2, neg_mu));
-        const float p1 = ex2_approx(fmaf(v[2 * i + 1], A.scale_log2, neg_mu));
-        const uint32_t b0 = __float_as_uint(p0), b1 = __float_as_uint(p1);
-        hi[i] = __byte_perm(b0, b1, 0x7632);
-        const float r0 = p0 - __uint_as_float(b0 & 0xffff0000u);
-        const float r1 = p1 - __uint_as_float(b1 & 0xffff0000u);
-        lo[i] = __byte_perm(__float_as_uint(r0), __float_as_uint(r1), 0x7632);
-        psum += p0 + p1;
+        for (int i = 0; i < 16; ++i) {
+          const float p0 = ex2_approx(fmaf(v[2 * i], A.scale_log2, neg_mu));
+          const float p1 = ex2_approx(fmaf(v[2 * i + 1], A.scale_log2, neg_mu));
+          const uint32_t b0 = __float_as_uint(p0), b1 = __float_as_uint(p1);
+          hi[i] = __byte_perm(b0, b1, 0x7632);
+          const float r0 = p0 - __uint_as_float(b0 & 0xffff0000u);
+          const float r1 = p1 - __uint_as_float(b1 & 0xffff0000u);
+          lo[i] = __byte_perm(__float_as_uint(r0), __float_as_uint(r1), 0x7632);
+          psum += p0 + p1;
+        }
+      };
+      split(v0, hi0, lo0);
+      split(v1, hi1, lo1);
+      if (j >= 1) {
+        // the previous PV has read P and finished O (every earlier PV was
+        // waited for one block before)
+        const bool g4 = tc::mbar_wait(&sh->pv_done, (uint32_t)((j - 1) & 1), abort_flag, status);
+        if (!(ok = __all_sync(0xffffffffu, g4))) break;
+        tc::fence_after_thread_sync();
       }
-      // the previous PV has read P and finished O (every earlier PV was
-      // waited for one block before); every quarter goes on or none does
-      const bool g4 =
-          (j == 0) || tc::mbar_wait(&sh->pv_done, (uint32_t)((j - 1) & 1), abort_flag, status);
-      if (!(ok = bar_and(qbar, 128, g4))) break;
-      tc::fence_after_thread_sync();
       if (__any_sync(0xffffffffu, rescale)) {
-        // every quarter rescales its own 32 columns of the row's O
         const float f = rescale ? ex2_approx(m - mu) : 1.f;
-        float ov[32];
-        tc::tmem_ld_32x32b_x32(o_cols, ov);
+        float o[32];
 #pragma unroll
-        for (int i = 0; i < 32; ++i) ov[i] *= f;
-        tmem_st_32x32b_x32(o_cols, ov);
+        for (int cc = 0; cc < 4; ++cc) {
+          tc::tmem_ld_32x32b_x32(o_own + (uint32_t)(cc * 32), o);
+#pragma unroll
+          for (int i = 0; i < 32; ++i) o[i] *= f;
+          tmem_st_32x32b_x32(o_own + (uint32_t)(cc * 32), o);
+        }
         l *= f;
       }
-      const uint32_t pcol = trow + kColP + (uint32_t)(kq * 32);
-      tmem_st_32x32b_x16(pcol, hi);
-      tmem_st_32x32b_x16(pcol + 16u, lo);
+      // hi to the half's P columns +0 .., lo to +32 ..
+      const uint32_t pcol = trow + (uint32_t)(128 + half * 64);
+      tmem_st_32x32b_x16(pcol, hi0);
+      tmem_st_32x32b_x16(pcol + 16u, hi1);
+      tmem_st_32x32b_x16(pcol + 32u, lo0);
+      tmem_st_32x32b_x16(pcol + 48u, lo1);
       tmem_wait_st();
       l += psum;
       m = mu;
@@ -692,23 +688,48 @@ tree_attn_tc_kernel(const __grid_constant__ CUtensorMap map_q,
       __syncwarp();
       if (lane == 0) tc::mbar_arrive(&sh->p_full);
     }
-    // ---- the row's sum over the four quarters, then this thread's output
-    // columns kq*32 .. +31 of O
+    if (!ok) {
+      m = -INFINITY;
+      l = 0.f;
+    }
+    // ---- merge the two key halves: (m, l) exchange, then this thread's
+    // output columns half*64 .. +63 from both accumulators
+    sh->xchg[0][half][r] = m;
+    sh->xchg[1][half][r] = l;
+    tc::mbar_arrive(&sh->fbar);
+    const bool gf = tc::mbar_wait(&sh->fbar, 0, abort_flag, status);
+    ok = __all_sync(0xffffffffu, gf) && ok;
+    const float mo = sh->xchg[0][half ^ 1][r], lo_ = sh->xchg[1][half ^ 1][r];
+    const float M = fmaxf(m, mo);
+    const float ws = (m == -INFINITY) ? 0.f : ex2_approx(m - M);
+    const float wo = (mo == -INFINITY) ? 0.f : ex2_approx(mo - M);
+    m_row = M;
+    l_row = ws * l + wo * lo_;
     bool have_o = false;
     if (ok && nblk > 0) {
       const bool got = tc::mbar_wait(&sh->o_done, 0, abort_flag, status);
-      have_o = __all_sync(0xffffffffu, got);
-    }
-    sh->xl[kq][r] = l;
-    ok = bar_and(qbar, 128, ok && (have_o || nblk == 0));
-    m_row = ok ? m : -INFINITY;
-    l_row = ok ? (sh->xl[0][r] + sh->xl[1][r]) + (sh->xl[2][r] + sh->xl[3][r]) : 0.f;
-    if (ok && have_o) {
-      tc::fence_after_thread_sync();
-      tc::tmem_ld_32x32b_x32(o_cols, o);
-    } else {
+      if ((ok = __all_sync(0xffffffffu, got))) {
+        have_o = true;
+        tc::fence_after_thread_sync();
+        const uint32_t o_oth = trow + 256u + (uint32_t)((half ^ 1) * 128);
+        float t[32];
+        tc::tmem_ld_32x32b_x32(o_own + (uint32_t)(half * 64), o0);
+        tc::tmem_ld_32x32b_x32(o_oth + (uint32_t)(half * 64), t);
 #pragma unroll
-      for (int i = 0; i < 32; ++i) o[i] = 0.f;
+        for (int i = 0; i < 32; ++i) o0[i] = ws * o0[i] + wo * t[i];
+        tc::tmem_ld_32x32b_x32(o_own + (uint32_t)(half * 64 + 32), o1);
+        tc::tmem_ld_32x32b_x32(o_oth + (uint32_t)(half * 64 + 32), t);
+#pragma unroll
+        for (int i = 0; i < 32; ++i) o1[i] = ws * o1[i] + wo * t[i];
+      }
+    }
+    if (!have_o) {
+#pragma unroll
+      for (int i = 0; i < 32; ++i) o0[i] = o1[i] = 0.f;
+    }
+    if (!ok) {
+      m_row = -INFINITY;
+      l_row = 0.f;
     }
   }
 
@@ -718,12 +739,15 @@ tree_attn_tc_kernel(const __grid_constant__ CUtensorMap map_q,
       const int qrow = mt * 128 + r;
       const int node = qrow / A.G, hh = qrow % A.G;
       if (node < n && ok) {
-        float* orow = A.out + ((size_t)(t0 + node) * A.Hq + g * A.G + hh) * 128 + kq * 32;
+        float* orow = A.out + ((size_t)(t0 + node) * A.Hq + g * A.G + hh) * 128 + half * 64;
         const float inv = 1.f / l_row;
 #pragma unroll
-        for (int d = 0; d < 32; d += 4)
+        for (int d = 0; d < 32; d += 4) {
           *reinterpret_cast<float4*>(orow + d) =
-              make_float4(o[d] * inv, o[d + 1] * inv, o[d + 2] * inv, o[d + 3] * inv);
+              make_float4(o0[d] * inv, o0[d + 1] * inv, o0[d + 2] * inv, o0[d + 3] * inv);
+          *reinterpret_cast<float4*>(orow + 32 + d) =
+              make_float4(o1[d] * inv, o1[d + 1] * inv, o1[d + 2] * inv, o1[d + 3] * inv);
+        }
       }
     }
   } else {
@@ -745,10 +769,15 @@ tree_attn_tc_kernel(const __grid_constant__ CUtensorMap map_q,
       float4* dst = cluster.map_shared_rank(mbuf, owner) + (size_t)(c * RPO + lrow) * 32;
 #pragma unroll
       for (int i = 0; i < 8; ++i) {
-        const int c4 = kq * 8 + i;
-        dst[c4 ^ (lrow & 31)] = make_float4(o[4 * i], o[4 * i + 1], o[4 * i + 2], o[4 * i + 3]);
+        const int c4 = half * 16 + i;
+        dst[c4 ^ (lrow & 31)] = make_float4(o0[4 * i], o0[4 * i + 1], o0[4 * i + 2], o0[4 * i + 3]);
       }
-      if (kq == 0) cluster.map_shared_rank(mlbuf, owner)[c * RPO + lrow] = make_float2(m_row, l_row);
+#pragma unroll
+      for (int i = 0; i < 8; ++i) {
+        const int c4 = half * 16 + 8 + i;
+        dst[c4 ^ (lrow & 31)] = make_float4(o1[4 * i], o1[4 * i + 1], o1[4 * i + 2], o1[4 * i + 3]);
+      }
+      if (half == 0) cluster.map_shared_rank(mlbuf, owner)[c * RPO + lrow] = make_float2(m_row, l_row);
     }
     cluster.sync();
     const int R0 = row0(c), R1 = row0(c + 1);
