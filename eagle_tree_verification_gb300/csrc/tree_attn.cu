@@ -162,6 +162,7 @@ constexpr int kHalfBytes = 128 * 128;   // 128 rows x 64 bf16 (one swizzle atom 
 constexpr int kTileBytes = 2 * kHalfBytes;  // 128 rows x 128 bf16
 constexpr int kTargetCtas = 152;        // SMs of a GB300
 constexpr int kMaxSplit = 8;            // cache chunks of one tile: one portable cluster
+constexpr int kMaxOrder = 256;          // sequences ordered by cache length (more: as given)
 constexpr size_t kAttSharedBytes = 5120;
 // cluster merge inside the K/V stage memory: O rows [NC][rows per owner][32]
 // float4 (at most 136 x 512 B), then (max, sum) pairs
@@ -236,11 +237,6 @@ __device__ __forceinline__ float ex2_approx(float x) {
   float y;
   asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
   return y;
-}
-
-__device__ __forceinline__ uint32_t pack_bf16(float a, float b) {
-  __nv_bfloat162 v = __floats2bfloat162_rn(a, b);
-  return *reinterpret_cast<uint32_t*>(&v);
 }
 
 // MN-major (rows of 64 N-elements, one row per K index) 128-byte-swizzled
@@ -320,16 +316,8 @@ tree_attn_tc_kernel(const __grid_constant__ CUtensorMap map_q,
   unsigned char* k_sm = base + kTileBytes;          // 2 stages
   unsigned char* v_sm = base + 3 * kTileBytes;      // 2 stages
   AttShared* sh = reinterpret_cast<AttShared*>(base + 5 * kTileBytes);
-  float4* obuf = reinterpret_cast<float4*>(k_sm);   // merge: [128 rows][32 float4], swizzled
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  // work item: tile * NC + c, the cache chunks of a tile adjacent (one cluster)
-  const int c = blockIdx.x % A.NC;
-  const int tile = blockIdx.x / A.NC;
-  const int mt = tile % A.MT;
-  const int g = (tile / A.MT) % A.Hkv;
-  const int b = tile / (A.MT * A.Hkv);
-
   // A contiguous KV cache and its offsets are resident state that the
   // kernel queued just before this one does not write: the first cache
   // blocks are requested before waiting for it (the tree and the queries
@@ -337,6 +325,29 @@ tree_attn_tc_kernel(const __grid_constant__ CUtensorMap map_q,
   // commit of accepted tokens may have just written its pages).
   const bool paged = A.page_size > 0;
   if (paged) pdl_begin();
+  // work item: tile * NC + c, the cache chunks of a tile adjacent (one
+  // cluster); tiles go to the sequences longest cache first (ties: lower
+  // index), so the longest work starts in the first wave
+  auto seq_len = [&](int u) { return paged ? A.kv_len[u] : A.kv_off[u + 1] - A.kv_off[u]; };
+  __shared__ int s_seq[kMaxOrder];
+  const int c = blockIdx.x % A.NC;
+  const int tile = blockIdx.x / A.NC;
+  const int mt = tile % A.MT;
+  const int g = (tile / A.MT) % A.Hkv;
+  int b = tile / (A.MT * A.Hkv);
+  if (A.B <= kMaxOrder) {
+    for (int t = threadIdx.x; t < A.B; t += blockDim.x) {
+      const int Lt = seq_len(t);
+      int rank = 0;
+      for (int u = 0; u < A.B; ++u) {
+        const int Lu = seq_len(u);
+        rank += (Lu > Lt) || (Lu == Lt && u < t);
+      }
+      s_seq[rank] = t;
+    }
+    __syncthreads();
+    b = s_seq[b];
+  }
   const int kv0 = paged ? 0 : A.kv_off[b];
   const int L = paged ? A.kv_len[b] : A.kv_off[b + 1] - kv0;
   const bool bad_kv = (L < 0 || L > A.max_kv);
