@@ -279,6 +279,7 @@ accept_stochastic_kernel(const StochParams P) {
   int* s_par = reinterpret_cast<int*>(s_q + P.slice);
   int* s_tok = s_par + P.max_nodes;
   int* s_kids = s_tok + P.max_nodes;
+  float* s_ua = reinterpret_cast<float*>(s_kids + P.max_nodes);   // u_accept of each child
   __shared__ unsigned long long s_red[66];
   __shared__ unsigned long long s_sum2[2][2][32];   // block_sum2_u64 partials, by round parity
   __shared__ RoundSlot s_slot[2];            // double-buffered by round parity
@@ -351,7 +352,12 @@ accept_stochastic_kernel(const StochParams P) {
         const int i = base + tid;
         const bool kid = (i < n) && s_par[i] == cur;
         const unsigned bal = __ballot_sync(0xffffffffu, kid);
-        if (kid) s_kids[c + __popc(bal & ((1u << tid) - 1u))] = i;
+        if (kid) {
+          // the child's acceptance uniform comes along: no global load in a round
+          const int pos = c + __popc(bal & ((1u << tid) - 1u));
+          s_kids[pos] = i;
+          s_ua[pos] = P.u_accept[t0 + i];
+        }
         c += __popc(bal);
       }
       if (tid == 0) s_nk = c;
@@ -433,10 +439,13 @@ accept_stochastic_kernel(const StochParams P) {
     for (int j = 0; j < nk; ++j) {
       const int c = s_kids[j];
       const int t = s_tok[c];
-      const float ua = P.u_accept[t0 + c];
+      const float ua = s_ua[j];
       if (!(ua >= 0.f && ua < 1.f) && writer && tid == 0) fail(P.status, EAGLE_ERR_INVALID_ARG);
-      // exact: a product of two fp32 values is exact in fp64
-      const bool accept = (double)ua * (double)pt < (double)qt;
+      // exact: a product of two fp32 values is exact in fp64.  (fp64 and
+      // 64-bit integer conversions run on a narrow pipe: one lane of each
+      // warp evaluates them and the warp shares the result.)
+      const bool accept =
+          __shfl_sync(0xffffffffu, lane == 0 ? (double)ua * (double)pt < (double)qt : false, 0);
       if (accept) {
         if (alpha + 1 > P.max_depth) {
           if (writer && tid == 0) fail(P.status, EAGLE_ERR_INVALID_ARG);
@@ -454,8 +463,13 @@ accept_stochastic_kernel(const StochParams P) {
       }
       // rejected: q_{k+1} = fp32(W) / fp32(Z), p_{k+1} likewise
       // (NO_REPLACE); every operation rounds to nearest once
-      const float zf = (Z > 0ull) ? __ull2float_rn(Z) : 0.f;
-      const float spf = (SP > 0ull) ? __ull2float_rn(SP) : 0.f;
+      float zf = 0.f, spf = 0.f;
+      if (lane == 0) {
+        zf = (Z > 0ull) ? __ull2float_rn(Z) : 0.f;
+        spf = (SP > 0ull) ? __ull2float_rn(SP) : 0.f;
+      }
+      zf = __shfl_sync(0xffffffffu, zf, 0);
+      spf = __shfl_sync(0xffffffffu, spf, 0);
       if (j + 1 < nk) {
         // update, and the next child's sums, in one pass
         unsigned long long sw = 0, sp = 0;
@@ -597,7 +611,7 @@ eagle_status launch_stochastic(bool logits, int B, int max_nodes, int V, int R, 
   int slice = 0, elems = 0;
   const int cs = pick_cluster(V, &slice, &elems);
   EAGLE_HOST_CHECK(cs > 0, EAGLE_ERR_UNSUPPORTED);
-  const size_t smem = (size_t)slice * sizeof(float) + (size_t)max_nodes * 3 * sizeof(int);
+  const size_t smem = (size_t)slice * sizeof(float) + (size_t)max_nodes * 4 * sizeof(int);
   using Kern = void (*)(const StochParams);
   static const Kern kerns[2][4] = {
       {accept_stochastic_kernel<4, false>, accept_stochastic_kernel<8, false>,

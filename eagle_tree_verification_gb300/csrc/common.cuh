@@ -76,10 +76,17 @@ __device__ __forceinline__ unsigned long long warp_max_u64(unsigned long long v)
   }
   return v;
 }
+// Sum over the warp of a 64-bit value (every lane gets it), exact whenever
+// the sum fits 64 bits: the 22-bit pieces of the 32 values are added by the
+// warp's integer reduction unit (no piece sum reaches 2^27), then recombined.
 __device__ __forceinline__ unsigned long long warp_sum_u64(unsigned long long v) {
-#pragma unroll
-  for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
-  return v;
+  const uint32_t a = (uint32_t)(v & 0x3FFFFFull);
+  const uint32_t b = (uint32_t)((v >> 22) & 0x3FFFFFull);
+  const uint32_t c = (uint32_t)(v >> 44);
+  const uint32_t sa = __reduce_add_sync(0xffffffffu, a);
+  const uint32_t sb = __reduce_add_sync(0xffffffffu, b);
+  const uint32_t sc = __reduce_add_sync(0xffffffffu, c);
+  return (unsigned long long)sa + ((unsigned long long)sb << 22) + ((unsigned long long)sc << 44);
 }
 
 // Programmatic dependent launch.  Every kernel of the library starts with
