@@ -296,9 +296,16 @@ struct ChunkShared {
 // partial lists by thread 0.  With take_ticket, thread 0 also counts the
 // chunk on the sequence's ticket; returns true in the CTA that drew the
 // last one.
-template <int VEC>
+struct NoRefill {
+  __device__ void operator()() const {}
+};
+
+// `refill` runs on thread 32 once the candidates are counted (warp 1 is
+// idle while warp 0 ranks them): the streaming kernel requests its next
+// stage there, off the other phases' barriers.
+template <int VEC, typename Refill = NoRefill>
 __device__ bool chunk_topk(const LevelParams& A, int row, int chunk, const float (&v)[VEC][4],
-                           ChunkShared& C, bool take_ticket = true) {
+                           ChunkShared& C, bool take_ticket = true, const Refill& refill = Refill()) {
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const int b = row / A.F;
   const int k = A.k;
@@ -374,6 +381,7 @@ __device__ bool chunk_topk(const LevelParams& A, int row, int chunk, const float
         }
       }
     __syncthreads();
+    if (round == 0 && tid == 32) refill();
     cnt = C.cnt;
     if (cnt <= kCandCap) break;
     if (round == kChunkRounds) {
@@ -633,25 +641,28 @@ expand_level_stream_kernel(const LevelParams A, int total_chunks) {
     const int st = i % kStreamStages;
     const bool got =
         tc::mbar_wait(&full[st], (uint32_t)((i / kStreamStages) & 1), &abort_flag, A.status);
-    if (!__syncthreads_and(got)) {
-      aborted = true;
-      break;
-    }
     float v[kStreamVec][4];
     const float4* sm4 = reinterpret_cast<const float4*>(stage_mem + (size_t)st * kStreamChunk * 4);
 #pragma unroll
     for (int j = 0; j < kStreamVec; ++j) {
-      const float4 x = sm4[j * kLvThreads + tid];
+      const float4 x = got ? sm4[j * kLvThreads + tid] : make_float4(0.f, 0.f, 0.f, 0.f);
       v[j][0] = x.x;
       v[j][1] = x.y;
       v[j][2] = x.z;
       v[j][3] = x.w;
     }
-    __syncthreads();   // the stage is in registers: refill it
-    if (tid == 0 && id + kStreamStages < id1) {
-      asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
-      issue(id + kStreamStages, st);
+    // every thread has the stage in registers (it is refilled during the
+    // ranking below)
+    if (!__syncthreads_and(got)) {
+      aborted = true;
+      break;
     }
+    auto refill = [&]() {
+      if (id + kStreamStages < id1) {
+        asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+        issue(id + kStreamStages, st);
+      }
+    };
     const int row = id / A.S, chunk = id % A.S;
     const int b = row / A.F;
     if (b != cur_b) {
@@ -659,7 +670,7 @@ expand_level_stream_kernel(const LevelParams A, int total_chunks) {
       cur_b = b;
       cur_n = 0;
     }
-    chunk_topk<kStreamVec>(A, row, chunk, v, C, false);
+    chunk_topk<kStreamVec>(A, row, chunk, v, C, false, refill);
     ++cur_n;
   }
   if (!aborted && cur_b >= 0) leave_sequence(cur_b, cur_n);
