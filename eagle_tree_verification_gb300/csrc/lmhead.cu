@@ -8,8 +8,9 @@
 // Kernels:
 //   lmhead_tc_kernel       bf16: persistent tcgen05 GEMM, one 128-row tile of
 //                          tree rows per CTA.  Each CTA (or cluster of up to
-//                          four CTAs, one row tile each, sharing every W stage
-//                          by TMA multicast) owns a contiguous slice of the
+//                          eight CTAs, one row tile each, in pairs that issue
+//                          256-row MMAs together and share every W stage by
+//                          TMA multicast) owns a contiguous slice of the
 //                          vocabulary and streams its rows of W once through a
 //                          TMA ring; tree rows sit on TMEM lanes, so every
 //                          thread owns one row and its softmax statistics are
@@ -236,15 +237,27 @@ lmhead_finalize_kernel(int T, int V, float temperature, const Partial* __restric
 //
 // More than 128 tree rows: a cluster of C CTAs shares one vocabulary slice,
 // each CTA holding its own 128-row tile of h and its own accumulators.  Every
-// W stage is loaded once for the whole cluster: each CTA requests every C-th
-// box of it with TMA multicast into the same stage of all C CTAs, and a stage
-// is refilled only after all C CTAs' MMAs have released it (the MMA commit
-// arrives on the stage's barrier in every CTA).  W then streams from memory
-// once per 128*C tree rows while each CTA does the work of the one-tile case.
-// W never depends on an earlier kernel, so the first W stages are requested
-// before the kernel waits for its predecessor.
+// W stage is loaded once for the whole cluster by TMA multicast, and a stage
+// is refilled only after every MMA issuer of the cluster has released it
+// (the MMA commit arrives on the stage's barrier in every CTA).  W then
+// streams from memory once per 128*C tree rows.  The CTAs form pairs
+// (cta_group::2; an odd tile count gets one CTA of rows past T): the even
+// CTA of a pair issues MMAs of M = 256 (its rows, then its peer's) x N = 256,
+// each CTA holding its own h tile and one 128-row half of every W stage
+// (even CTAs the first half, odd CTAs the second, each half multicast to the
+// CTAs of its parity).  So each SM receives and reads half of every W stage
+// instead of all of it, per MMA of its own 128 rows.  The odd CTA reports
+// each of its stages to the even one as it lands (a remote mbarrier arrive),
+// and its epilogue releases the accumulators into the even CTA's barrier.
+// W and h are requested by two threads of their own, so the W ring (from
+// memory) runs as far ahead as its stages allow while the h ring (from L2)
+// keeps fewer.  W never depends on an earlier kernel, so the first W stages
+// are requested before the kernel waits for its predecessor.
 // ---------------------------------------------------------------------------
-constexpr int kTcThreads = 320;   // warp 0 TMA, warp 1 MMA, warps 2-9 epilogue
+// warp 0 W copies, warp 1 MMA (or, in the odd CTA of a pair, stage reports),
+// warps 2-9 epilogue, warp 10 h copies
+constexpr int kTcThreads = 352;
+constexpr int kHWarp = 10;
 constexpr int kEpiWarps = 8;      // two per TMEM lane quarter, one per column half
 constexpr int kBK = 64;           // bf16 per 128-byte swizzled row (one chunk)
 constexpr int kUnit = 32;         // vocabulary rows per TMA box
@@ -264,10 +277,22 @@ constexpr int kMaxHStages = 6;       // h ring barriers held (stages used: 4 or 
 #endif
 constexpr int kBigHStages = EAGLE_LMHEAD_BIG_HSTAGES;
 static_assert(kBigHStages >= 1 && kBigHStages <= kMaxHStages, "h stages beyond the barriers held");
-// Cluster launches (row tiles sharing W) use 512-row blocks over both TMEM
-// accumulators (a build-time option, so that 256-row blocks can be measured)
+// Cluster launches (row tiles sharing W) pair their CTAs: cta_group::2 MMAs
+// of M = 256 over two SMs, each SM holding its own 128 tree rows and half of
+// every W stage, so each SM writes and reads half the W bytes per MMA of
+// its own rows (a build-time option, so that unpaired clusters can be
+// measured).
+#ifndef EAGLE_LMHEAD_PAIR
+#define EAGLE_LMHEAD_PAIR 1
+#endif
+constexpr bool kPairCluster = EAGLE_LMHEAD_PAIR != 0;
+constexpr int kPairRows = 2 * kTileRows;   // tree rows of one pair MMA (its M)
+// Unpaired cluster launches use 512-row blocks over both TMEM accumulators
+// (each h chunk then serves two W halves); paired ones 256-row blocks in
+// alternating accumulators, so that the epilogue of one block overlaps the
+// MMAs of the next (a build-time option, so that both can be measured).
 #ifndef EAGLE_LMHEAD_DUAL
-#define EAGLE_LMHEAD_DUAL 1
+#define EAGLE_LMHEAD_DUAL (EAGLE_LMHEAD_PAIR ? 0 : 1)
 #endif
 constexpr bool kDualCluster = EAGLE_LMHEAD_DUAL != 0;
 constexpr int kMaxWStages = 12;
@@ -306,7 +331,8 @@ struct TcLayout {
 // `h_rows`: tree rows of one h stage (one CTA's tile, rounded up to 8);
 // `z_tma`: logits are written and the staging boxes should be held when
 // they fit beside the rings (a smaller CTA writes logits directly).
-TcLayout tc_layout(int h_rows, bool z_tma) {
+// `pair`: a CTA of a pair holds half of every W stage.
+TcLayout tc_layout(int h_rows, bool z_tma, bool pair = false) {
   TcLayout L;
   L.h_rows = h_rows;
   L.h_stage_bytes = h_rows * 128;
@@ -314,10 +340,12 @@ TcLayout tc_layout(int h_rows, bool z_tma) {
   // than the overlap of a short slice's epilogue gains
   L.blk = kBlkMax;
   L.h_stages = 4;
-  L.w_stage_bytes = L.blk * 128;
+  L.w_stage_bytes = (pair ? L.blk / 2 : L.blk) * 128;
   size_t fixed = 1024 + (size_t)L.h_stages * L.h_stage_bytes + kTcSharedBytes;
-  size_t limit = kSmemShared;
-  if (fixed + 4 * (size_t)L.w_stage_bytes > kSmemShared) {
+  // a pair takes the whole shared memory: its W ring (16 KB stages) covers
+  // the memory latency only with about eight stages
+  size_t limit = pair ? kSmemLimit : kSmemShared;
+  if (!pair && fixed + 4 * (size_t)L.w_stage_bytes > kSmemShared) {
     // the whole shared memory, split between the h ring (re-read from L2
     // for every block) and the W ring (measured at 128 rows x 4096 x 128256
     // in clusters of six: 3 h + 5 W stages 881 us, 4 + 4 781 us, 2 + 6
@@ -369,7 +397,7 @@ __device__ __forceinline__ void merge_partial(Partial& a, const Partial& b, floa
 // time to refill an h stage); the epilogue of a block then no longer
 // overlaps the next block's MMAs.  Otherwise a block is one accumulator and
 // consecutive blocks alternate.
-template <bool MULTI, bool DUAL>
+template <bool MULTI, bool DUAL, bool PAIR>
 __global__ void __launch_bounds__(kTcThreads, 1)
 lmhead_tc_kernel(const __grid_constant__ CUtensorMap map_h, const __grid_constant__ CUtensorMap map_w,
                  const __grid_constant__ CUtensorMap map_z, int T, int H, int V,
@@ -381,8 +409,10 @@ lmhead_tc_kernel(const __grid_constant__ CUtensorMap map_h, const __grid_constan
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~(uintptr_t)1023);
   unsigned char* h_smem = base;
   unsigned char* w_smem = base + h_stages * h_stage_bytes;
+  static_assert(!PAIR || MULTI, "pairs are cluster launches");
   const int w_rows_max = DUAL ? blk_max / 2 : blk_max;   // W rows of one stage
-  const int w_stage_bytes = w_rows_max * 128;
+  // PAIR: a CTA holds rows 0-127 (even rank) or 128-255 (odd) of every stage
+  const int w_stage_bytes = (PAIR ? w_rows_max / 2 : w_rows_max) * 128;
   TcShared* sh = reinterpret_cast<TcShared*>(w_smem + (size_t)w_stages * w_stage_bytes);
   // logit staging boxes (1024-byte aligned: every ring stage is a multiple of 1 KB)
   unsigned char* z_smem = w_smem + (size_t)w_stages * w_stage_bytes + kTcSharedBytes;
@@ -391,6 +421,15 @@ lmhead_tc_kernel(const __grid_constant__ CUtensorMap map_h, const __grid_constan
   if (!MULTI) C = 1;
   const int rank = MULTI ? (int)tc::cluster_ctarank() : 0;   // this CTA's row tile
   const uint16_t all_ctas = (uint16_t)((1u << C) - 1u);
+  // PAIR: par 0 is the pair's leader (it issues the pair's MMAs); a W box
+  // goes to the CTAs of one parity (`group`), requested by each of them in
+  // turn
+  const int par = PAIR ? (rank & 1) : 0;
+  const int leader = rank & ~1;
+  const int groups = PAIR ? C / 2 : C;
+  const int gi = PAIR ? rank >> 1 : rank;
+  const uint16_t group_mask = PAIR ? (uint16_t)((par ? 0xAAAAu : 0x5555u) & all_ctas) : all_ctas;
+  const uint16_t pair_mask = (uint16_t)(3u << leader);
   const int slices = gridDim.x / C;
   const int slice = blockIdx.x / C;
   // the cluster's slice of the vocabulary: rows [r_begin, r_end), 32-row units
@@ -409,12 +448,17 @@ lmhead_tc_kernel(const __grid_constant__ CUtensorMap map_h, const __grid_constan
   // this CTA's share of a W stage (chunk kb of the block at row y0):
   // boxes rank, rank + C, ... (multicast to all)
   auto load_w_box = [&](int stage, int rows, int kb, int y0, uint64_t pol) {
+    if (PAIR) {
+      // this CTA's half; rows past the block are never read by the epilogue
+      rows = min(w_rows_max / 2, max(0, rows - par * (w_rows_max / 2)));
+      y0 += par * (w_rows_max / 2);
+    }
     tc::mbar_arrive_expect_tx(&sh->w_full[stage], (uint32_t)(rows * 128));
     unsigned char* dst = w_smem + (size_t)stage * w_stage_bytes;
-    for (int u = rank * kUnit; u < rows; u += C * kUnit) {
+    for (int u = gi * kUnit; u < rows; u += groups * kUnit) {
       if (MULTI)
         tc::tma_load_2d_mc_hint(dst + u * 128, &map_w, &sh->w_full[stage], kb * kBK, y0 + u,
-                                all_ctas, pol);
+                                group_mask, pol);
       else
         tc::tma_load_2d_hint(dst + u * 128, &map_w, &sh->w_full[stage], kb * kBK, y0 + u, pol);
     }
@@ -423,17 +467,21 @@ lmhead_tc_kernel(const __grid_constant__ CUtensorMap map_h, const __grid_constan
   const int w_early = min(w_stages, total);
 
   if (threadIdx.x == 0) {
+    // a leader's stages are full once its own copies landed and its peer
+    // reported its own; its accumulators are free once both CTAs' epilogues
+    // have read them
+    const uint32_t full_count = (PAIR && par == 0) ? 2 : 1;
     for (int i = 0; i < h_stages; ++i) {
-      tc::mbar_init(&sh->h_full[i], 1);
+      tc::mbar_init(&sh->h_full[i], full_count);
       tc::mbar_init(&sh->h_empty[i], 1);
     }
     for (int i = 0; i < w_stages; ++i) {
-      tc::mbar_init(&sh->w_full[i], 1);
-      tc::mbar_init(&sh->w_empty[i], C);   // every CTA's MMAs release the stage
+      tc::mbar_init(&sh->w_full[i], full_count);
+      tc::mbar_init(&sh->w_empty[i], PAIR ? C / 2 : C);   // every MMA issuer releases the stage
     }
     for (int i = 0; i < 2; ++i) {
       tc::mbar_init(&sh->tmem_full[i], 1);
-      tc::mbar_init(&sh->tmem_empty[i], kEpiWarps);
+      tc::mbar_init(&sh->tmem_empty[i], (PAIR && par == 0) ? 2 * kEpiWarps : kEpiWarps);
     }
     tc::mbar_init(&sh->xbar, 32 * kEpiWarps);
     tc::mbar_init(&sh->drain, 1);
@@ -453,8 +501,13 @@ lmhead_tc_kernel(const __grid_constant__ CUtensorMap map_h, const __grid_constan
           load_w_box(i, half_rows(blk, hf), kb, half_y0(blk, hf), pol_w);
   }
   if (warp == 1) {
-    tc::tmem_alloc(&sh->tmem_base, 512);
-    tc::tmem_relinquish();
+    if constexpr (PAIR) {
+      tc::tmem_alloc_pair(&sh->tmem_base, 512);
+      tc::tmem_relinquish_pair();
+    } else {
+      tc::tmem_alloc(&sh->tmem_base, 512);
+      tc::tmem_relinquish();
+    }
   }
   pdl_begin();   // h (and the outputs) follow the previous kernel
   tc::fence_before_thread_sync();
@@ -464,25 +517,18 @@ lmhead_tc_kernel(const __grid_constant__ CUtensorMap map_h, const __grid_constan
   volatile int* abort_flag = &sh->abort_flag;
 
   if (warp == 0) {
-    // ------------------------------------------------------------ producer
+    // ------------------------------------------------------------ W copies
     if (lane == 0) {
       const uint64_t pol_w = tc::policy_evict_first();
-      const uint64_t pol_h = tc::policy_evict_last();
-      // h chunk i and W stage i (past the ones requested early) in turn;
-      // nested loops keep divisions off the refill path
-      int hs = 0, ws = 0, issued_h = 0, issued_w = w_early;
-      uint32_t hph = 0, wph = 0;
+      // W stage i (past the ones requested early) as soon as its slot is
+      // free; nested loops keep divisions off the refill path
+      int ws = 0, issued_w = w_early;
+      uint32_t wph = 0;
       bool ok = true;
       int i = 0;
       for (int blk = 0; blk < n_blocks && ok; ++blk) {
         const int nh = n_halves(blk);
         for (int kb = 0; kb < KB && ok; ++kb) {
-          if (!(ok = tc::mbar_wait(&sh->h_empty[hs], hph ^ 1, abort_flag, status))) break;
-          tc::mbar_arrive_expect_tx(&sh->h_full[hs], (uint32_t)h_stage_bytes);
-          tc::tma_load_2d_hint(h_smem + hs * h_stage_bytes, &map_h, &sh->h_full[hs], kb * kBK,
-                               rank * kTileRows, pol_h);
-          ++issued_h;
-          if (++hs == h_stages) { hs = 0; hph ^= 1; }
           for (int hf = 0; hf < nh && ok; ++hf, ++i) {
             if (i >= w_early) {
               if (!(ok = tc::mbar_wait(&sh->w_empty[ws], wph ^ 1, abort_flag, status))) break;
@@ -507,9 +553,54 @@ lmhead_tc_kernel(const __grid_constant__ CUtensorMap map_h, const __grid_constan
         for (int i = max(0, issued_w - w_stages); i < issued_w; ++i)
           tc::mbar_wait(&sh->w_full[i % w_stages], (i / w_stages) & 1, &never, nullptr,
                         200000000ll);
+      }
+    }
+  } else if (warp == kHWarp) {
+    // ------------------------------------------------------------ h copies
+    // (a ring of its own, so that the W ring runs as far ahead as its
+    // stages allow: h comes from L2, W from memory)
+    if (lane == 0) {
+      const uint64_t pol_h = tc::policy_evict_last();
+      int hs = 0, issued_h = 0;
+      uint32_t hph = 0;
+      bool ok = true;
+      for (int blk = 0; blk < n_blocks && ok; ++blk) {
+        for (int kb = 0; kb < KB && ok; ++kb) {
+          if (!(ok = tc::mbar_wait(&sh->h_empty[hs], hph ^ 1, abort_flag, status))) break;
+          tc::mbar_arrive_expect_tx(&sh->h_full[hs], (uint32_t)h_stage_bytes);
+          tc::tma_load_2d_hint(h_smem + hs * h_stage_bytes, &map_h, &sh->h_full[hs], kb * kBK,
+                               rank * kTileRows, pol_h);
+          ++issued_h;
+          if (++hs == h_stages) { hs = 0; hph ^= 1; }
+        }
+      }
+      if (!ok) {
+        int never = 0;
         for (int i = max(0, issued_h - h_stages); i < issued_h; ++i)
           tc::mbar_wait(&sh->h_full[i % h_stages], (i / h_stages) & 1, &never, nullptr,
                         200000000ll);
+      }
+    }
+  } else if (warp == 1 && PAIR && par == 1) {
+    // ------------------------------------------------------------ pair peer
+    // The leader issues the pair's MMAs: report every h and W stage of this
+    // CTA to it as soon as the stage has landed here.
+    if (lane == 0) {
+      int hs = 0, ws = 0;
+      uint32_t hph = 0, wph = 0;
+      bool ok = true;
+      for (int blk = 0; blk < n_blocks && ok; ++blk) {
+        const int nh = n_halves(blk);
+        for (int kb = 0; kb < KB && ok; ++kb) {
+          if (!(ok = tc::mbar_wait(&sh->h_full[hs], hph, abort_flag, status))) break;
+          tc::mbar_arrive_remote<true>(&sh->h_full[hs], (uint32_t)leader);
+          if (++hs == h_stages) { hs = 0; hph ^= 1; }
+          for (int hf = 0; hf < nh && ok; ++hf) {
+            if (!(ok = tc::mbar_wait(&sh->w_full[ws], wph, abort_flag, status))) break;
+            tc::mbar_arrive_remote<true>(&sh->w_full[ws], (uint32_t)leader);
+            if (++ws == w_stages) { ws = 0; wph ^= 1; }
+          }
+        }
       }
     }
   } else if (warp == 1) {
@@ -524,7 +615,7 @@ lmhead_tc_kernel(const __grid_constant__ CUtensorMap map_h, const __grid_constan
       for (int blk = 0; blk < n_blocks && ok; ++blk) {
         const int ab = DUAL ? 0 : (blk & 1);
         if (!(ok = tc::mbar_wait(&sh->tmem_empty[ab], ((tph >> ab) & 1u) ^ 1u, abort_flag,
-                                 status)))
+                                       status)))
           break;
         tph ^= 1u << ab;
         tc::fence_after_thread_sync();
@@ -538,32 +629,53 @@ lmhead_tc_kernel(const __grid_constant__ CUtensorMap map_h, const __grid_constan
             tc::fence_after_thread_sync();
             // DUAL: half hf accumulates at TMEM column 256 * hf
             const uint32_t d = tmem + (uint32_t)((ab + hf) * kBlkMax);
-            const uint32_t idesc = tc::idesc_bf16_f32(128, half_rows(blk, hf));
             const uint64_t db =
                 tc::desc_kmajor_sw128(tc::smem_u32(w_smem + (size_t)ws * w_stage_bytes));
             // K steps of 16 advance the descriptors' start address by 32 bytes
-            tc::mma_f16(d, da, db, idesc, acc);
-            tc::mma_f16(d, da + 2, db + 2, idesc, 1u);
-            tc::mma_f16(d, da + 4, db + 4, idesc, 1u);
-            tc::mma_f16(d, da + 6, db + 6, idesc, 1u);
-            if (MULTI)
-              tc::mma_commit_mc(&sh->w_empty[ws], all_ctas);
-            else
-              tc::mma_commit(&sh->w_empty[ws]);
+            if constexpr (PAIR) {
+              // always all 256 columns: those past the block are never read
+              const uint32_t idesc = tc::idesc_bf16_f32(kPairRows, kBlkMax);
+              tc::mma_f16_pair(d, da, db, idesc, acc);
+              tc::mma_f16_pair(d, da + 2, db + 2, idesc, 1u);
+              tc::mma_f16_pair(d, da + 4, db + 4, idesc, 1u);
+              tc::mma_f16_pair(d, da + 6, db + 6, idesc, 1u);
+              tc::mma_commit_pair_mc(&sh->w_empty[ws], all_ctas);
+            } else {
+              const uint32_t idesc = tc::idesc_bf16_f32(128, half_rows(blk, hf));
+              tc::mma_f16(d, da, db, idesc, acc);
+              tc::mma_f16(d, da + 2, db + 2, idesc, 1u);
+              tc::mma_f16(d, da + 4, db + 4, idesc, 1u);
+              tc::mma_f16(d, da + 6, db + 6, idesc, 1u);
+              if (MULTI)
+                tc::mma_commit_mc(&sh->w_empty[ws], all_ctas);
+              else
+                tc::mma_commit(&sh->w_empty[ws]);
+            }
             if (++ws == w_stages) { ws = 0; wph ^= 1; }
           }
           if (!ok) break;
-          tc::mma_commit(&sh->h_empty[hs]);
+          if constexpr (PAIR)
+            tc::mma_commit_pair_mc(&sh->h_empty[hs], pair_mask);
+          else
+            tc::mma_commit(&sh->h_empty[hs]);
           if (++hs == h_stages) { hs = 0; hph ^= 1; }
         }
-        if (ok) tc::mma_commit(&sh->tmem_full[ab]);
+        if (ok) {
+          if constexpr (PAIR)
+            tc::mma_commit_pair_mc(&sh->tmem_full[ab], pair_mask);
+          else
+            tc::mma_commit(&sh->tmem_full[ab]);
+        }
       }
       // every MMA issued by this thread has finished before TMEM is freed
-      tc::mma_commit(&sh->drain);
+      if constexpr (PAIR)
+        tc::mma_commit_pair_mc(&sh->drain, (uint16_t)(1u << rank));
+      else
+        tc::mma_commit(&sh->drain);
       int never = 0;
       tc::mbar_wait(&sh->drain, 0, &never, nullptr, 200000000ll);
     }
-  } else {
+  } else if (warp >= 2 && warp < 2 + kEpiWarps) {
     // ------------------------------------------------------------ epilogue
     const int quad = warp & 3;
     const int chalf = (warp - 2) >> 2;   // second or first half of every block's columns
@@ -588,7 +700,8 @@ lmhead_tc_kernel(const __grid_constant__ CUtensorMap map_h, const __grid_constan
       const int ab = DUAL ? 0 : (blk & 1);
       const int rows = blk_rows(blk);
       // every lane waits; the warp proceeds only if all of them saw the phase
-      const bool got = tc::mbar_wait(&sh->tmem_full[ab], (tph >> ab) & 1u, abort_flag, status);
+      const bool got =
+          tc::mbar_wait(&sh->tmem_full[ab], (tph >> ab) & 1u, abort_flag, status);
       if (!__all_sync(0xffffffffu, got)) break;
       tph ^= 1u << ab;
       tc::fence_after_thread_sync();
@@ -680,7 +793,12 @@ lmhead_tc_kernel(const __grid_constant__ CUtensorMap map_h, const __grid_constan
       }
       tc::fence_before_thread_sync();
       __syncwarp();
-      if (lane == 0) tc::mbar_arrive(&sh->tmem_empty[ab]);
+      if (lane == 0) {
+        if (PAIR && par == 1)
+          tc::mbar_arrive_remote(&sh->tmem_empty[ab], (uint32_t)leader);
+        else
+          tc::mbar_arrive(&sh->tmem_empty[ab]);
+      }
     }
     // the logits are written before the kernel ends
     if (z_tma && lane == 0) tc::bulk_wait_all();
@@ -697,12 +815,23 @@ lmhead_tc_kernel(const __grid_constant__ CUtensorMap map_h, const __grid_constan
   }
   tc::fence_before_thread_sync();
   __syncthreads();
-  if (warp == 1) {
-    tc::fence_after_thread_sync();
-    tc::tmem_dealloc(tmem, 512);
+  if constexpr (PAIR) {
+    // both CTAs' epilogues are past their last TMEM read and the leader's
+    // MMAs have finished before the pair frees its columns; no CTA leaves
+    // while a peer may still deliver into its shared memory
+    tc::cluster_sync_all();
+    if (warp == 1) {
+      tc::fence_after_thread_sync();
+      tc::tmem_dealloc_pair(tmem, 512);
+    }
+  } else {
+    if (warp == 1) {
+      tc::fence_after_thread_sync();
+      tc::tmem_dealloc(tmem, 512);
+    }
+    // no CTA leaves while a peer may still deliver into its shared memory
+    if (MULTI) tc::cluster_sync_all();
   }
-  // no CTA leaves while a peer may still deliver into its shared memory
-  if (MULTI) tc::cluster_sync_all();
 }
 
 PFN_cuTensorMapEncodeTiled_v12000 get_encode() {
@@ -786,8 +915,9 @@ int max_clusters(int C, size_t smem) {
     cfg.attrs = attr;
     cfg.numAttrs = 1;
     int n = 0;
-    if (cudaOccupancyMaxActiveClusters(&n, (const void*)lmhead_tc_kernel<true, kDualCluster>,
-                                       &cfg) !=
+    if (cudaOccupancyMaxActiveClusters(
+            &n, (const void*)lmhead_tc_kernel<true, kDualCluster, kPairCluster>,
+            &cfg) !=
         cudaSuccess) {
       cudaGetLastError();
       n = 0;
@@ -815,9 +945,10 @@ cudaError_t launch_tc(int C, dim3 grid, size_t smem, cudaStream_t s, Args&&... a
   attr[1].val.clusterDim.z = 1;
   cfg.attrs = attr;
   cfg.numAttrs = (C > 1) ? 2 : 1;
-  return (C > 1) ? cudaLaunchKernelEx(&cfg, lmhead_tc_kernel<true, kDualCluster>,
-                                      std::forward<Args>(args)...)
-                 : cudaLaunchKernelEx(&cfg, lmhead_tc_kernel<false, false>,
+  return (C > 1) ? cudaLaunchKernelEx(
+                       &cfg, lmhead_tc_kernel<true, kDualCluster, kPairCluster>,
+                       std::forward<Args>(args)...)
+                 : cudaLaunchKernelEx(&cfg, lmhead_tc_kernel<false, false, false>,
                                       std::forward<Args>(args)...);
 }
 
@@ -863,14 +994,15 @@ extern "C" eagle_status eagle_lmhead_softmax(eagle_dtype dtype, int T, int H, in
     // the whole unified L1 as shared memory, so that a CTA of the
     // concurrently running tree expand fits beside this one
     if (attr_once.run([] {
-          cudaError_t e = cudaFuncSetAttribute(lmhead_tc_kernel<false, false>,
+          cudaError_t e = cudaFuncSetAttribute(lmhead_tc_kernel<false, false, false>,
                                                cudaFuncAttributeMaxDynamicSharedMemorySize,
                                                (int)kSmemLimit);
           if (e == cudaSuccess)
-            e = cudaFuncSetAttribute(lmhead_tc_kernel<true, kDualCluster>,
-                                     cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kSmemLimit);
+            e = cudaFuncSetAttribute(
+                lmhead_tc_kernel<true, kDualCluster, kPairCluster>,
+                cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kSmemLimit);
           if (e == cudaSuccess)
-            e = cudaFuncSetAttribute(lmhead_tc_kernel<false, false>,
+            e = cudaFuncSetAttribute(lmhead_tc_kernel<false, false, false>,
                                      cudaFuncAttributePreferredSharedMemoryCarveout,
                                      cudaSharedmemCarveoutMaxShared);
           return e;
@@ -884,9 +1016,12 @@ extern "C" eagle_status eagle_lmhead_softmax(eagle_dtype dtype, int T, int H, in
     const int tiles = (T + kTileRows - 1) / kTileRows;
     // logits through bulk tensor stores need 16-byte row strides
     const bool z_want = z && (V % 4) == 0;
-    const size_t tile_smem = tc_layout(kTileRows, z_want).smem;
+    const size_t tile_smem = tc_layout(kTileRows, z_want, kPairCluster).smem;
+    // CTAs of a cluster of c row tiles: paired clusters take an even count
+    // (a last CTA past the rows computes zero rows and writes nothing)
+    auto ctas = [](int c) { return (kPairCluster && c > 1) ? (c + 1) & ~1 : c; };
     int passes = 1, C = tiles;
-    while (C > 1 && (C > kMaxCluster || max_clusters(C, tile_smem) < 1)) {
+    while (C > 1 && (ctas(C) > kMaxCluster || max_clusters(ctas(C), tile_smem) < 1)) {
       ++passes;
       C = (tiles + passes - 1) / passes;
     }
@@ -894,16 +1029,17 @@ extern "C" eagle_status eagle_lmhead_softmax(eagle_dtype dtype, int T, int H, in
     // the attention, which the step runs while the LM head is still
     // streaming W (it does not fit beside an LM head CTA)
     const int slices =
-        (C > 1) ? std::min(max_clusters(C, tile_smem), n_units)
+        (C > 1) ? std::min(max_clusters(ctas(C), tile_smem), n_units)
                 : std::min(std::max(1, sm_count() - kSmsForOthers), n_units);
     for (int p = 0, tile0 = 0; p < passes; ++p) {
       const int nt = std::min(C, tiles - tile0);    // tiles of this launch
       const int r0 = tile0 * kTileRows;
       const int Ts = std::min(nt * kTileRows, T - r0);
       tile0 += nt;
-      const int Cp = (C > 1) ? nt : 1;
+      const int Cp = (C > 1) ? ctas(nt) : 1;
       const TcLayout TL =
-          tc_layout((Cp > 1 || Ts > kTileRows) ? kTileRows : ((Ts + 7) / 8) * 8, z_want);
+          tc_layout((Cp > 1 || Ts > kTileRows) ? kTileRows : ((Ts + 7) / 8) * 8, z_want,
+                    Cp > 1 && kPairCluster);
       const __nv_bfloat16* hs = static_cast<const __nv_bfloat16*>(d_h) + (size_t)r0 * H;
       float* zs = z ? z + (size_t)r0 * V : nullptr;
       CUtensorMap map_h, map_z = map_w;   // without staging map_z is never read
@@ -914,7 +1050,8 @@ extern "C" eagle_status eagle_lmhead_softmax(eagle_dtype dtype, int T, int H, in
       if (launch_tc(Cp, dim3(slices * Cp), TL.smem, s, map_h, map_w, map_z, Ts, H, V,
                     temperature, zs, (int)TL.z_tma, part + (size_t)r0 * slices, n_units,
                     TL.h_stage_bytes, TL.h_stages,
-                    (Cp > 1 && kDualCluster) ? 2 * TL.blk : TL.blk, TL.w_stages, Cp,
+                    (Cp > 1 && kDualCluster) ? 2 * TL.blk : TL.blk, TL.w_stages,
+                    Cp,
                     d_status) !=
           cudaSuccess)
         return EAGLE_ERR_CUDA;
