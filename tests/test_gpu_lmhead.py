@@ -69,11 +69,13 @@ def _check(dtype, got, ref, rows):
     ("f32", 1, 64, 1, 1.0),             # a single vocabulary entry
     ("f32", 70, 128, 1000, 0.7),        # ragged row tile and vocab tile
     ("bf16", 61, 4096, 32000, 1.0),     # Vicuna-7B shaped head
-    ("bf16", 130, 512, 4099, 0.7),      # two row tiles sharing W, ragged vocab
+    ("bf16", 130, 512, 4099, 0.7),      # two row tiles (one CTA pair) sharing W, ragged vocab
     ("bf16", 256, 1024, 5003, 1.0),     # two full row tiles
-    ("bf16", 300, 512, 2111, 0.7),      # three row tiles sharing one W stream
+    ("bf16", 300, 512, 2111, 0.7),      # three row tiles: two pairs, one CTA past the rows
     ("bf16", 384, 256, 1500, 1.0),      # three full tiles
-    ("bf16", 513, 256, 3001, 1.0),      # four tiles, then a pass of one row
+    ("bf16", 513, 256, 3001, 1.0),      # five tiles, the last of one row
+    ("bf16", 1100, 256, 1500, 0.7),     # nine tiles: launches of five and four tiles
+    ("bf16", 1153, 256, 2003, 1.0),     # ten tiles, the last of one row
 ])
 @pytest.mark.parametrize("prob", [False, True])
 def test_lmhead_matches_oracle(dtype, T, H, V, temp, prob):
@@ -119,7 +121,8 @@ def test_lmhead_planted_ties_pick_the_lowest_index():
                                                # bulk tensor stores (one tile, then three
                                                # sharing W), ragged last 8-column box
                                                ("bf16", 100, 512, 4100, 1.0),
-                                               ("bf16", 300, 512, 2116, 0.7)])
+                                               ("bf16", 300, 512, 2116, 0.7),
+                                               ("bf16", 1100, 256, 1504, 0.7)])
 def test_lmhead_logits_mode(dtype, T, H, V, temp):
     # LOGITS mode stores z itself and the same statistics as the other modes
     import torch
