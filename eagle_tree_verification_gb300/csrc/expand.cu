@@ -288,6 +288,7 @@ struct ChunkShared {
   unsigned long long cand[kCandCap];
   unsigned long long top[EAGLE_MAX_TOPK];
   unsigned long long tau;
+  unsigned long long kth;   // the chunk's k-th largest key (0: fewer than k found)
   int cnt, last;
 };
 
@@ -303,10 +304,18 @@ struct NoRefill {
 // `refill` runs on thread 32 once the candidates are counted (warp 1 is
 // idle while warp 0 ranks them): the streaming kernel requests its next
 // stage there, off the other phases' barriers.
+// `bound` (optional, the same in every thread): a key that at least k keys
+// of the row reach, e.g. the k-th largest key of another chunk of the row;
+// 0 when none is known.  Then only keys above it are kept (a key below it
+// is below the row's k-th, and keys are unique), the bound search over the
+// group maxima is skipped, and the chunk may publish fewer than k keys.  On
+// return it is raised to this chunk's k-th largest key when that is larger.
 template <int VEC, typename Refill = NoRefill>
 __device__ bool chunk_topk(const LevelParams& A, int row, int chunk, const float (&v)[VEC][4],
-                           ChunkShared& C, bool take_ticket = true, const Refill& refill = Refill()) {
+                           ChunkShared& C, bool take_ticket = true, const Refill& refill = Refill(),
+                           unsigned long long* bound = nullptr) {
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  const unsigned long long b_in = bound ? *bound : 0ull;
   const int b = row / A.F;
   const int k = A.k;
   const int c0 = chunk * (kLvThreads * 4 * VEC);
@@ -333,23 +342,37 @@ __device__ bool chunk_topk(const LevelParams& A, int row, int chunk, const float
         if (real) fin = fmaf(v[j][e], 0.f, fin);
       }
   }
-  float tmax = -INFINITY;
+  if (b_in == 0) {
+    float tmax = -INFINITY;
 #pragma unroll
-  for (int j = 0; j < VEC; ++j)
+    for (int j = 0; j < VEC; ++j)
 #pragma unroll
-    for (int e = 0; e < 4; ++e) tmax = fmaxf(tmax, x[j][e]);
+      for (int e = 0; e < 4; ++e) tmax = fmaxf(tmax, x[j][e]);
 #pragma unroll
-  for (int o = 8; o > 0; o >>= 1) tmax = fmaxf(tmax, __shfl_xor_sync(0xffffffffu, tmax, o));
-  if ((lane & 15) == 0) C.grpv[warp * 2 + (lane >> 4)] = tmax;
-  if (tid == 0) C.cnt = 0;
-  if (__syncthreads_or(!(fin == 0.f)) && tid == 0) fail(A.status, EAGLE_ERR_NUMERIC);
+    for (int o = 8; o > 0; o >>= 1) tmax = fmaxf(tmax, __shfl_xor_sync(0xffffffffu, tmax, o));
+    if ((lane & 15) == 0) C.grpv[warp * 2 + (lane >> 4)] = tmax;
+  }
+  // With a bound no barrier comes before the candidates: the count was
+  // reset at the end of the previous call (of the same row), and the
+  // finiteness check joins the candidates' barrier.  A stale C.kth there is
+  // the previous chunk's, already folded into the bound.
+  if (b_in == 0) {
+    if (tid == 0) {
+      C.cnt = 0;
+      C.kth = 0ull;
+    }
+    if (__syncthreads_or(!(fin == 0.f)) && tid == 0) fail(A.status, EAGLE_ERR_NUMERIC);
+  }
   // every warp: the largest group maximum that at least k group maxima
   // reach -- at least k tokens of the chunk are >= it (ties included): the
   // k-th largest of the 32 group maxima counted with multiplicity, found by
   // taking the largest remaining value (and its copies) until k are taken.
   // (Measured: warp 0 alone plus a CTA barrier cost ~9x this.)
   float tau_val;
-  {
+  unsigned long long tau_key = b_in;   // later rounds (or a given bound): the bound as a key
+  if (b_in != 0) {
+    tau_val = key_value(b_in);
+  } else {
     uint32_t ob = ordered_bits(C.grpv[lane]);
     uint32_t top = 0u;
     for (int need = k; need > 0;) {   // at most k rounds (k <= 32 lanes)
@@ -360,9 +383,12 @@ __device__ bool chunk_topk(const LevelParams& A, int row, int chunk, const float
     // fewer than k real tokens: every real (finite) token qualifies
     tau_val = fmaxf(from_ordered_bits(top), -3.402823466e38f);
   }
-  unsigned long long tau_key = 0;   // later rounds: the bound as a key
   int cnt;
   for (int round = 0;; ++round) {
+    // round 0 compares values only (with a key bound this also keeps the
+    // few tokens whose value equals the bound's but whose key is below it:
+    // they rank below the chunk's true list and never displace it); later
+    // rounds compare keys
 #pragma unroll
     for (int j = 0; j < VEC; ++j)
 #pragma unroll
@@ -380,7 +406,11 @@ __device__ bool chunk_topk(const LevelParams& A, int row, int chunk, const float
           if (pred && pos < kCandCap) C.cand[pos] = desc_key(val, idx);
         }
       }
-    __syncthreads();
+    if (round == 0 && b_in != 0) {
+      if (__syncthreads_or(!(fin == 0.f)) && tid == 0) fail(A.status, EAGLE_ERR_NUMERIC);
+    } else {
+      __syncthreads();
+    }
     if (round == 0 && tid == 32) refill();
     cnt = C.cnt;
     if (cnt <= kCandCap) break;
@@ -413,7 +443,8 @@ __device__ bool chunk_topk(const LevelParams& A, int row, int chunk, const float
       const unsigned long long me = (lane < cnt) ? C.cand[lane] : 0ull;
       const int rank = warp_rank_desc(me);
       if (lane < cnt && rank < k) part[rank] = me;
-      if (lane >= cnt && lane < k) part[lane] = 0ull;   // fewer than k tokens
+      if (lane < cnt && rank == k - 1) C.kth = me;
+      if (lane >= cnt && lane < k) part[lane] = 0ull;   // fewer than k tokens (or above the bound)
     }
   } else {
     if (tid < cnt) {
@@ -425,6 +456,7 @@ __device__ bool chunk_topk(const LevelParams& A, int row, int chunk, const float
     }
     __syncthreads();
     if (warp == 0 && lane < k) part[lane] = C.top[lane];
+    if (tid == 0) C.kth = C.top[k - 1];
   }
   if (warp == 0) {
     __syncwarp();
@@ -441,6 +473,10 @@ __device__ bool chunk_topk(const LevelParams& A, int row, int chunk, const float
     }
   }
   __syncthreads();
+  if (bound && C.kth > *bound) *bound = C.kth;
+  // nothing reads the count past the barrier above; the next call's
+  // candidates follow a barrier of the caller's
+  if (tid == 0) C.cnt = 0;
   return C.last != 0;
 }
 
@@ -637,6 +673,9 @@ expand_level_stream_kernel(const LevelParams A, int total_chunks) {
   };
   int i = 0, cur_b = -1, cur_n = 0;
   bool aborted = false;
+  // the k-th largest key of this CTA's earlier chunks of the current row
+  int bound_row = -1;
+  unsigned long long bound = 0ull;
   for (int id = id0; id < id1; ++id, ++i) {
     const int st = i % kStreamStages;
     const bool got =
@@ -670,7 +709,11 @@ expand_level_stream_kernel(const LevelParams A, int total_chunks) {
       cur_b = b;
       cur_n = 0;
     }
-    chunk_topk<kStreamVec>(A, row, chunk, v, C, false, refill);
+    if (row != bound_row) {
+      bound_row = row;
+      bound = 0ull;
+    }
+    chunk_topk<kStreamVec>(A, row, chunk, v, C, false, refill, &bound);
     ++cur_n;
   }
   if (!aborted && cur_b >= 0) leave_sequence(cur_b, cur_n);
