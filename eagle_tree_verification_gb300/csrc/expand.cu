@@ -342,12 +342,13 @@ __device__ bool chunk_topk(const LevelParams& A, int row, int chunk, const float
         if (real) fin = fmaf(v[j][e], 0.f, fin);
       }
   }
+  float own_max = -INFINITY;   // this thread's largest value
+#pragma unroll
+  for (int j = 0; j < VEC; ++j)
+#pragma unroll
+    for (int e = 0; e < 4; ++e) own_max = fmaxf(own_max, x[j][e]);
   if (b_in == 0) {
-    float tmax = -INFINITY;
-#pragma unroll
-    for (int j = 0; j < VEC; ++j)
-#pragma unroll
-      for (int e = 0; e < 4; ++e) tmax = fmaxf(tmax, x[j][e]);
+    float tmax = own_max;
 #pragma unroll
     for (int o = 8; o > 0; o >>= 1) tmax = fmaxf(tmax, __shfl_xor_sync(0xffffffffu, tmax, o));
     if ((lane & 15) == 0) C.grpv[warp * 2 + (lane >> 4)] = tmax;
@@ -388,7 +389,9 @@ __device__ bool chunk_topk(const LevelParams& A, int row, int chunk, const float
     // round 0 compares values only (with a key bound this also keeps the
     // few tokens whose value equals the bound's but whose key is below it:
     // they rank below the chunk's true list and never displace it); later
-    // rounds compare keys
+    // rounds compare keys.  A warp none of whose threads holds a value at
+    // the bound offers nothing (most warps: a chunk has few candidates).
+    if (__any_sync(0xffffffffu, own_max >= tau_val))
 #pragma unroll
     for (int j = 0; j < VEC; ++j)
 #pragma unroll
