@@ -28,28 +28,17 @@ using namespace eagle;
 
 namespace {
 
-// Stochastic walk launch shape (build-time options, so that other shapes
-// can be measured): threads per CTA, CTAs resident per SM (the register cap
-// follows), the largest per-thread element count taken before a larger
-// cluster is, and the largest cluster.
-#ifndef EAGLE_WALK_THREADS
-#define EAGLE_WALK_THREADS 1024
-#endif
-#ifndef EAGLE_WALK_CTAS_PER_SM
-#define EAGLE_WALK_CTAS_PER_SM 1
-#endif
-#ifndef EAGLE_WALK_PREFER_ELEMS
-#define EAGLE_WALK_PREFER_ELEMS 8
-#endif
-#ifndef EAGLE_WALK_MAX_CLUSTER
-#define EAGLE_WALK_MAX_CLUSTER 16
-#endif
-constexpr int kStochThreads = EAGLE_WALK_THREADS;
-constexpr int kWalkCtasPerSm = EAGLE_WALK_CTAS_PER_SM;
-constexpr int kWalkPreferElems = EAGLE_WALK_PREFER_ELEMS;
-constexpr int kWalkMaxCluster = EAGLE_WALK_MAX_CLUSTER;
-static_assert(kStochThreads % 32 == 0 && kStochThreads <= 1024, "walk threads");
-static_assert(kWalkMaxCluster >= 1 && kWalkMaxCluster <= 16, "walk cluster");
+// Stochastic walk launch shapes.  Wide: 1024-thread CTAs, one per SM, at
+// most 8 vocabulary entries per thread before the cluster doubles (the
+// fastest per sequence).  Narrow: 512-thread CTAs, two per SM, at most 16
+// entries per thread -- twice the sequences resident at once, each slower.
+// The wide shape is taken when every sequence's cluster is resident at once.
+// (Measured at 16 sequences of V = 128256, one visited node and 8 rejection
+// rounds each: wide 206.7 us in three waves of clusters of 16, narrow
+// 195.0 us; clusters of 8 with 16 or 32 entries per thread 237.8 / 274.6 us.)
+constexpr int kWideThreads = 1024, kWidePrefer = 8;
+constexpr int kNarrowThreads = 512, kNarrowPrefer = 16;
+constexpr int kWalkMaxCluster = 16;
 constexpr float kTwo40 = 1099511627776.0f;  // 2^40
 constexpr float kTwo24 = 16777216.0f;       // 2^24
 
@@ -236,7 +225,7 @@ struct RoundSlot {
 // is one IEEE division (round to nearest).  SUMS (on the updated values): the residual weight sum, the draft
 // weight sum without t_next, and q, p at t_next into `slot`.  One pass per
 // rejection round, the same operations as an update followed by the sums.
-template <int E, bool UPD, bool SUMS>
+template <int E, int THREADS, bool UPD, bool SUMS>
 __device__ __forceinline__ void walk_pass(float (&q)[E], float (&p)[E], int v0, int nv,
                                           bool no_replace, int t_rej, float zf, float spf,
                                           bool z_pos, int t_next, unsigned long long& sw,
@@ -244,7 +233,7 @@ __device__ __forceinline__ void walk_pass(float (&q)[E], float (&p)[E], int v0, 
   const int tid = threadIdx.x;
 #pragma unroll
   for (int e = 0; e < E; ++e) {
-    const int i = tid + e * kStochThreads;
+    const int i = tid + e * THREADS;
     if (UPD) {
       const float qa = q[e], pa = p[e];
       if (z_pos) q[e] = __fdiv_rn(fixed40_f(fmaxf(0.f, __fsub_rn(qa, pa))), zf);
@@ -261,11 +250,11 @@ __device__ __forceinline__ void walk_pass(float (&q)[E], float (&p)[E], int v0, 
   }
 }
 
-// Element e of thread `tid` is vocabulary entry v0 + tid + kStochThreads*e.
+// Element e of thread `tid` is vocabulary entry v0 + tid + THREADS*e.
 // LOGITS: P.q holds logits; each visited row is normalised as it is loaded,
 // by the LM head's probability-mode expression.
-template <int E, bool LOGITS>
-__global__ void __launch_bounds__(kStochThreads, kWalkCtasPerSm)
+template <int E, bool LOGITS, int THREADS>
+__global__ void __launch_bounds__(THREADS, THREADS == kWideThreads ? 1 : 2)
 accept_stochastic_kernel(const StochParams P) {
   pdl_begin();
   cg::cluster_group cluster = cg::this_cluster();
@@ -381,7 +370,7 @@ accept_stochastic_kernel(const StochParams P) {
       int bad = 0;
 #pragma unroll
       for (int e = 0; e < E; ++e) {
-        const int i = tid + e * kStochThreads;
+        const int i = tid + e * THREADS;
         q[e] = 0.f;
         p[e] = 0.f;
         if (i < nv) {
@@ -431,7 +420,7 @@ accept_stochastic_kernel(const StochParams P) {
       // sums as if the first child were rejected, and its tested values
       unsigned long long sw = 0, sp = 0;
       const int t = s_tok[s_kids[0]];
-      walk_pass<E, false, true>(q, p, v0, nv, no_replace, -1, 0.f, 0.f, false, t, sw, sp,
+      walk_pass<E, THREADS, false, true>(q, p, v0, nv, no_replace, -1, 0.f, 0.f, false, t, sw, sp,
                                 s_slot[par]);
       reduce_round(sw, sp, t);
     }
@@ -474,12 +463,12 @@ accept_stochastic_kernel(const StochParams P) {
         // update, and the next child's sums, in one pass
         unsigned long long sw = 0, sp = 0;
         const int tn = s_tok[s_kids[j + 1]];
-        walk_pass<E, true, true>(q, p, v0, nv, no_replace, t, zf, spf, Z > 0ull, tn, sw, sp,
+        walk_pass<E, THREADS, true, true>(q, p, v0, nv, no_replace, t, zf, spf, Z > 0ull, tn, sw, sp,
                                  s_slot[par]);
         reduce_round(sw, sp, tn);
       } else {
         unsigned long long sw = 0, sp = 0;
-        walk_pass<E, true, false>(q, p, v0, nv, no_replace, t, zf, spf, Z > 0ull, -1, sw, sp,
+        walk_pass<E, THREADS, true, false>(q, p, v0, nv, no_replace, t, zf, spf, Z > 0ull, -1, sw, sp,
                                   s_slot[par]);
       }
     }
@@ -489,7 +478,7 @@ accept_stochastic_kernel(const StochParams P) {
     // Bonus token: inverse CDF of the current q over integer weights.
 #pragma unroll
     for (int e = 0; e < E; ++e) {
-      const int i = tid + e * kStochThreads;
+      const int i = tid + e * THREADS;
       if (i < nv) s_q[i] = q[e];
     }
     __syncthreads();
@@ -543,16 +532,15 @@ accept_stochastic_kernel(const StochParams P) {
   cluster.sync();
 }
 
-// Cluster size and per-thread element count for a vocabulary: slices of
-// at most 512 x 32 entries; prefer <= 512 x 16 (registers), up to 16 CTAs.
-// (Measured at 16 sequences of V = 128256: halving the clusters to fit
-// them all at once, 32 entries per thread, was slower than a second wave.)
-int pick_cluster(int V, int* slice_out, int* elems_out) {
+// Cluster size and per-thread element count for a vocabulary: the smallest
+// cluster (up to 16 CTAs) whose slices need at most `prefer` entries per
+// thread, at most 32.
+int pick_cluster(int V, int threads, int prefer, int* slice_out, int* elems_out) {
   for (int cs = 1; cs <= kWalkMaxCluster; cs <<= 1) {
     int slice = (V + cs - 1) / cs;
     slice = (slice + 3) & ~3;
-    const int e = (slice + kStochThreads - 1) / kStochThreads;
-    if (e > kWalkPreferElems && cs < kWalkMaxCluster) continue;
+    const int e = (slice + threads - 1) / threads;
+    if (e > prefer && cs < kWalkMaxCluster) continue;
     if (e > 32) return -1;
     *slice_out = slice;
     *elems_out = e <= 4 ? 4 : e <= 8 ? 8 : e <= 16 ? 16 : 32;
@@ -585,6 +573,44 @@ extern "C" eagle_status eagle_accept_greedy(int B, int max_nodes, const int32_t*
 
 namespace {
 
+// Clusters of `cs` CTAs of `kern` resident on the current GPU at once (0 if
+// the query fails), cached per device and configuration.
+int resident_clusters(const void* kern, int threads, int cs, size_t smem) {
+  struct Entry {
+    const void* kern;
+    int dev, cs;
+    size_t smem;
+    int n;
+  };
+  static std::mutex mu;
+  static Entry cache[32];
+  static int used = 0;
+  int dev = 0;
+  cudaGetDevice(&dev);
+  std::lock_guard<std::mutex> lock(mu);
+  for (int i = 0; i < used; ++i)
+    if (cache[i].kern == kern && cache[i].dev == dev && cache[i].cs == cs && cache[i].smem == smem)
+      return cache[i].n;
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3((unsigned)cs, 1, 1);
+  cfg.blockDim = dim3((unsigned)threads, 1, 1);
+  cfg.dynamicSmemBytes = smem;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeClusterDimension;
+  attr[0].val.clusterDim.x = (unsigned)cs;
+  attr[0].val.clusterDim.y = 1;
+  attr[0].val.clusterDim.z = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  int n = 0;
+  if (cudaOccupancyMaxActiveClusters(&n, kern, &cfg) != cudaSuccess) {
+    cudaGetLastError();
+    n = 0;
+  }
+  if (used < 32) cache[used++] = Entry{kern, dev, cs, smem, n};
+  return n;
+}
+
 // Both stochastic entry points: d_q holds probabilities, or logits with
 // row_lse and temperature (LOGITS).
 eagle_status launch_stochastic(bool logits, int B, int max_nodes, int V, int R, int mode,
@@ -608,39 +634,61 @@ eagle_status launch_stochastic(bool logits, int B, int max_nodes, int V, int R, 
                    EAGLE_ERR_INVALID_ARG);
   EAGLE_HOST_CHECK(!logits || d_row_lse, EAGLE_ERR_INVALID_ARG);
   EAGLE_HOST_CHECK(R == 0 || d_p_rows, EAGLE_ERR_INVALID_ARG);
-  int slice = 0, elems = 0;
-  const int cs = pick_cluster(V, &slice, &elems);
-  EAGLE_HOST_CHECK(cs > 0, EAGLE_ERR_UNSUPPORTED);
-  const size_t smem = (size_t)slice * sizeof(float) + (size_t)max_nodes * 4 * sizeof(int);
   using Kern = void (*)(const StochParams);
-  static const Kern kerns[2][4] = {
-      {accept_stochastic_kernel<4, false>, accept_stochastic_kernel<8, false>,
-       accept_stochastic_kernel<16, false>, accept_stochastic_kernel<32, false>},
-      {accept_stochastic_kernel<4, true>, accept_stochastic_kernel<8, true>,
-       accept_stochastic_kernel<16, true>, accept_stochastic_kernel<32, true>}};
-  const int ai = elems == 4 ? 0 : elems == 8 ? 1 : elems == 16 ? 2 : 3;
-  const Kern kern = kerns[logits ? 1 : 0][ai];
-  static PerDeviceOnce attr_once[2][4];
-  if (attr_once[logits ? 1 : 0][ai].run([&] {
-        cudaError_t e =
-            cudaFuncSetAttribute(kern, cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
-        if (e != cudaSuccess) return e;
-        // room for kWalkCtasPerSm CTAs' slices side by side
-        if (kWalkCtasPerSm > 1)
-          e = cudaFuncSetAttribute(kern, cudaFuncAttributePreferredSharedMemoryCarveout,
-                                   cudaSharedmemCarveoutMaxShared);
-        if (e != cudaSuccess) return e;
-        return cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                    160 * 1024);
-      }) != cudaSuccess)
-    return EAGLE_ERR_CUDA;
+  static const Kern kerns[2][2][4] = {
+      {{accept_stochastic_kernel<4, false, kWideThreads>, accept_stochastic_kernel<8, false, kWideThreads>,
+        accept_stochastic_kernel<16, false, kWideThreads>, accept_stochastic_kernel<32, false, kWideThreads>},
+       {accept_stochastic_kernel<4, true, kWideThreads>, accept_stochastic_kernel<8, true, kWideThreads>,
+        accept_stochastic_kernel<16, true, kWideThreads>, accept_stochastic_kernel<32, true, kWideThreads>}},
+      {{accept_stochastic_kernel<4, false, kNarrowThreads>, accept_stochastic_kernel<8, false, kNarrowThreads>,
+        accept_stochastic_kernel<16, false, kNarrowThreads>, accept_stochastic_kernel<32, false, kNarrowThreads>},
+       {accept_stochastic_kernel<4, true, kNarrowThreads>, accept_stochastic_kernel<8, true, kNarrowThreads>,
+        accept_stochastic_kernel<16, true, kNarrowThreads>, accept_stochastic_kernel<32, true, kNarrowThreads>}}};
+  static PerDeviceOnce attr_once[2][2][4];
+  // a shape's cluster size, slice, kernel and shared memory, attributes set
+  struct Shape {
+    int cs, slice, threads;
+    Kern kern;
+    size_t smem;
+  };
+  auto shape = [&](int narrow, Shape* sh) -> eagle_status {
+    int elems = 0;
+    sh->threads = narrow ? kNarrowThreads : kWideThreads;
+    sh->cs = pick_cluster(V, sh->threads, narrow ? kNarrowPrefer : kWidePrefer, &sh->slice, &elems);
+    if (sh->cs <= 0) return EAGLE_ERR_UNSUPPORTED;
+    sh->smem = (size_t)sh->slice * sizeof(float) + (size_t)max_nodes * 4 * sizeof(int);
+    const int ai = elems == 4 ? 0 : elems == 8 ? 1 : elems == 16 ? 2 : 3;
+    sh->kern = kerns[narrow][logits ? 1 : 0][ai];
+    const Kern kern = sh->kern;
+    if (attr_once[narrow][logits ? 1 : 0][ai].run([&] {
+          cudaError_t e =
+              cudaFuncSetAttribute(kern, cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
+          if (e != cudaSuccess) return e;
+          // room for two CTAs' slices side by side
+          if (narrow)
+            e = cudaFuncSetAttribute(kern, cudaFuncAttributePreferredSharedMemoryCarveout,
+                                     cudaSharedmemCarveoutMaxShared);
+          if (e != cudaSuccess) return e;
+          return cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                      160 * 1024);
+        }) != cudaSuccess)
+      return EAGLE_ERR_CUDA;
+    return EAGLE_OK;
+  };
+  Shape sh;
+  eagle_status st = shape(0, &sh);
+  if (st != EAGLE_OK) return st;
+  if (B > 1 && sh.cs > 1 && B > resident_clusters((const void*)sh.kern, sh.threads, sh.cs, sh.smem)) {
+    Shape nw;
+    if (shape(1, &nw) == EAGLE_OK) sh = nw;
+  }
   StochParams P;
   P.max_nodes = max_nodes;
   P.V = V;
   P.R = R;
   P.mode = mode;
   P.max_depth = max_depth;
-  P.slice = slice;
+  P.slice = sh.slice;
   P.tree_off = d_tree_off;
   P.parent = d_parent;
   P.tokens = d_tokens;
@@ -657,20 +705,20 @@ eagle_status launch_stochastic(bool logits, int B, int max_nodes, int V, int R, 
   P.status = d_status;
 
   cudaLaunchConfig_t cfg = {};
-  cfg.gridDim = dim3((unsigned)(B * cs), 1, 1);
-  cfg.blockDim = dim3(kStochThreads, 1, 1);
-  cfg.dynamicSmemBytes = smem;
+  cfg.gridDim = dim3((unsigned)(B * sh.cs), 1, 1);
+  cfg.blockDim = dim3((unsigned)sh.threads, 1, 1);
+  cfg.dynamicSmemBytes = sh.smem;
   cfg.stream = (cudaStream_t)stream;
   cudaLaunchAttribute attr[2];
   attr[0].id = cudaLaunchAttributeClusterDimension;
-  attr[0].val.clusterDim.x = (unsigned)cs;
+  attr[0].val.clusterDim.x = (unsigned)sh.cs;
   attr[0].val.clusterDim.y = 1;
   attr[0].val.clusterDim.z = 1;
   attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
   attr[1].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
   cfg.numAttrs = 2;
-  return launch_status(cudaLaunchKernelEx(&cfg, kern, P));
+  return launch_status(cudaLaunchKernelEx(&cfg, sh.kern, P));
 }
 
 }  // namespace
