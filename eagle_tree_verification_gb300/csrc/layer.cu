@@ -511,25 +511,48 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap map_a, const __grid_constant_
     tc::cluster_sync_all();
     cooperative_groups::cluster_group cluster = cooperative_groups::this_cluster();
     const int rows = blk_rows(0);
-    const int pieces = A.T * (rows / kGUnit);
-    for (int j = krank + KS * (int)threadIdx.x; j < pieces; j += KS * (int)blockDim.x) {
-      const int row = j / (rows / kGUnit), c = (j % (rows / kGUnit)) * kGUnit;
-      float* mine = reinterpret_cast<float*>(base) + (size_t)row * kPartStride + c;
+    const int ppr = rows / kGUnit;                 // pieces per row
+    const int pieces = A.T * ppr;
+    const int mine_n = (pieces > krank) ? (pieces - krank + KS - 1) / KS : 0;   // this CTA's
+    auto piece_at = [&](int m) {                   // m-th piece of this CTA: its partial here
+      const int j = krank + KS * m;
+      return reinterpret_cast<float*>(base) + (size_t)(j / ppr) * kPartStride + (j % ppr) * kGUnit;
+    };
+    // every thread sums 4-column slices of this CTA's pieces over the K
+    // ranges (the ranks' loads in flight together, added in rank order) into
+    // this CTA's own partial, which no other CTA reads ...
+    for (int it = threadIdx.x; it < mine_n * (kGUnit / 4); it += blockDim.x) {
+      float* slot = piece_at(it / (kGUnit / 4)) + (it % (kGUnit / 4)) * 4;
+      float4 x[kGMaxSplit];
+#pragma unroll
+      for (int r = 0; r < kGMaxSplit; ++r)
+        if (r < KS) x[r] = *reinterpret_cast<const float4*>(cluster.map_shared_rank(slot, r));
+      float4 sum = make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll
+      for (int r = 0; r < kGMaxSplit; ++r)
+        if (r < KS) {
+          sum.x += x[r].x;
+          sum.y += x[r].y;
+          sum.z += x[r].z;
+          sum.w += x[r].w;
+        }
+      *reinterpret_cast<float4*>(slot) = sum;
+    }
+    __syncthreads();
+    // ... then one thread per piece runs the epilogue from it
+    for (int m = threadIdx.x; m < mine_n; m += blockDim.x) {
+      const int j = krank + KS * m;
+      const float4* src = reinterpret_cast<const float4*>(piece_at(m));
       float v[32];
 #pragma unroll
-      for (int i = 0; i < 32; ++i) v[i] = 0.f;
-      for (int r = 0; r < KS; ++r) {
-        const float4* src = reinterpret_cast<const float4*>(cluster.map_shared_rank(mine, r));
-#pragma unroll
-        for (int i = 0; i < 8; ++i) {
-          const float4 x = src[i];
-          v[4 * i] += x.x;
-          v[4 * i + 1] += x.y;
-          v[4 * i + 2] += x.z;
-          v[4 * i + 3] += x.w;
-        }
+      for (int i = 0; i < 8; ++i) {
+        const float4 x = src[i];
+        v[4 * i] = x.x;
+        v[4 * i + 1] = x.y;
+        v[4 * i + 2] = x.z;
+        v[4 * i + 3] = x.w;
       }
-      gemm_epilogue(A, row, r_begin + c, v);
+      gemm_epilogue(A, j / ppr, r_begin + (j % ppr) * kGUnit, v);
     }
     // no CTA leaves while a peer may still read its shared memory
     tc::cluster_sync_all();
