@@ -225,8 +225,29 @@ struct RoundSlot {
 // is one IEEE division (round to nearest).  SUMS (on the updated values): the residual weight sum, the draft
 // weight sum without t_next, and q, p at t_next into `slot`.  One pass per
 // rejection round, the same operations as an update followed by the sums.
-template <int E, int THREADS, bool UPD, bool SUMS>
-__device__ __forceinline__ void walk_pass(float (&q)[E], float (&p)[E], int v0, int nv,
+// This thread's entries of the draft row: in registers, or (SMEM) in shared
+// memory at sm[e * THREADS] (element e of the thread), which keeps a narrow
+// CTA's 16 entries per thread within the registers of two CTAs per SM.
+template <int E, int THREADS, bool SMEM>
+struct DraftSlice {
+  float reg[SMEM ? 1 : E];
+  float* sm;
+  __device__ __forceinline__ float get(int e) const {
+    if constexpr (SMEM) return sm[e * THREADS];
+    else return reg[e];
+  }
+  __device__ __forceinline__ void set(int e, float v) {
+    if constexpr (SMEM) sm[e * THREADS] = v;
+    else reg[e] = v;
+  }
+};
+
+__host__ __device__ constexpr bool draft_in_smem(int e, int threads) {
+  return threads == kNarrowThreads || e == 16;
+}
+
+template <int E, int THREADS, bool UPD, bool SUMS, bool SMEM>
+__device__ __forceinline__ void walk_pass(float (&q)[E], DraftSlice<E, THREADS, SMEM>& p, int v0, int nv,
                                           bool no_replace, int t_rej, float zf, float spf,
                                           bool z_pos, int t_next, unsigned long long& sw,
                                           unsigned long long& sp, RoundSlot& slot) {
@@ -234,17 +255,21 @@ __device__ __forceinline__ void walk_pass(float (&q)[E], float (&p)[E], int v0, 
 #pragma unroll
   for (int e = 0; e < E; ++e) {
     const int i = tid + e * THREADS;
+    float pe = p.get(e);
     if (UPD) {
-      const float qa = q[e], pa = p[e];
+      const float qa = q[e], pa = pe;
       if (z_pos) q[e] = __fdiv_rn(fixed40_f(fmaxf(0.f, __fsub_rn(qa, pa))), zf);
-      if (no_replace) p[e] = (v0 + i == t_rej) ? 0.f : (spf > 0.f ? __fdiv_rn(fixed40_f(pa), spf) : 0.f);
+      if (no_replace) {
+        pe = (v0 + i == t_rej) ? 0.f : (spf > 0.f ? __fdiv_rn(fixed40_f(pa), spf) : 0.f);
+        p.set(e, pe);
+      }
     }
     if (SUMS) {
-      sw += fixed40_int(fmaxf(0.f, __fsub_rn(q[e], p[e])));
-      if (no_replace && v0 + i != t_next) sp += fixed40_int(p[e]);
+      sw += fixed40_int(fmaxf(0.f, __fsub_rn(q[e], pe)));
+      if (no_replace && v0 + i != t_next) sp += fixed40_int(pe);
       if (i < nv && v0 + i == t_next) {
         slot.qt = q[e];
-        slot.pt = p[e];
+        slot.pt = pe;
       }
     }
   }
@@ -269,6 +294,11 @@ accept_stochastic_kernel(const StochParams P) {
   int* s_tok = s_par + P.max_nodes;
   int* s_kids = s_tok + P.max_nodes;
   float* s_ua = reinterpret_cast<float*>(s_kids + P.max_nodes);   // u_accept of each child
+  // narrow CTAs and 16 entries per thread: the draft row's entries in
+  // shared memory, E per thread (16-byte aligned)
+  constexpr bool kPSmem = draft_in_smem(E, THREADS);
+  float* s_p = reinterpret_cast<float*>(
+      (reinterpret_cast<uintptr_t>(s_ua + P.max_nodes) + 15) & ~(uintptr_t)15);
   __shared__ unsigned long long s_red[66];
   __shared__ unsigned long long s_sum2[2][2][32];   // block_sum2_u64 partials, by round parity
   __shared__ RoundSlot s_slot[2];            // double-buffered by round parity
@@ -324,7 +354,9 @@ accept_stochastic_kernel(const StochParams P) {
   }
 
   const bool no_replace = (P.mode == EAGLE_SAMPLE_NO_REPLACE);
-  float q[E], p[E];
+  float q[E];
+  DraftSlice<E, THREADS, kPSmem> p;
+  p.sm = s_p + tid;
   int cur = 0, alpha = 0, par = 0;
   bool stop = false;
   if (writer && tid == 0) o_nodes[0] = 0;
@@ -372,14 +404,15 @@ accept_stochastic_kernel(const StochParams P) {
       for (int e = 0; e < E; ++e) {
         const int i = tid + e * THREADS;
         q[e] = 0.f;
-        p[e] = 0.f;
+        p.set(e, 0.f);
         if (i < nv) {
           q[e] = __ldg(qrow + i);
           if (LOGITS) q[e] = prob_from_logit(q[e], sc);
           bad |= !is_prob(q[e]);
           if (nk > 0) {
-            p[e] = __ldg(prw + i);
-            bad |= !is_prob(p[e]);
+            const float pv = __ldg(prw + i);
+            p.set(e, pv);
+            bad |= !is_prob(pv);
           }
         }
       }
@@ -420,7 +453,7 @@ accept_stochastic_kernel(const StochParams P) {
       // sums as if the first child were rejected, and its tested values
       unsigned long long sw = 0, sp = 0;
       const int t = s_tok[s_kids[0]];
-      walk_pass<E, THREADS, false, true>(q, p, v0, nv, no_replace, -1, 0.f, 0.f, false, t, sw, sp,
+      walk_pass<E, THREADS, false, true, kPSmem>(q, p, v0, nv, no_replace, -1, 0.f, 0.f, false, t, sw, sp,
                                 s_slot[par]);
       reduce_round(sw, sp, t);
     }
@@ -463,12 +496,12 @@ accept_stochastic_kernel(const StochParams P) {
         // update, and the next child's sums, in one pass
         unsigned long long sw = 0, sp = 0;
         const int tn = s_tok[s_kids[j + 1]];
-        walk_pass<E, THREADS, true, true>(q, p, v0, nv, no_replace, t, zf, spf, Z > 0ull, tn, sw, sp,
+        walk_pass<E, THREADS, true, true, kPSmem>(q, p, v0, nv, no_replace, t, zf, spf, Z > 0ull, tn, sw, sp,
                                  s_slot[par]);
         reduce_round(sw, sp, tn);
       } else {
         unsigned long long sw = 0, sp = 0;
-        walk_pass<E, THREADS, true, false>(q, p, v0, nv, no_replace, t, zf, spf, Z > 0ull, -1, sw, sp,
+        walk_pass<E, THREADS, true, false, kPSmem>(q, p, v0, nv, no_replace, t, zf, spf, Z > 0ull, -1, sw, sp,
                                   s_slot[par]);
       }
     }
@@ -656,7 +689,9 @@ eagle_status launch_stochastic(bool logits, int B, int max_nodes, int V, int R, 
     sh->threads = narrow ? kNarrowThreads : kWideThreads;
     sh->cs = pick_cluster(V, sh->threads, narrow ? kNarrowPrefer : kWidePrefer, &sh->slice, &elems);
     if (sh->cs <= 0) return EAGLE_ERR_UNSUPPORTED;
-    sh->smem = (size_t)sh->slice * sizeof(float) + (size_t)max_nodes * 4 * sizeof(int);
+    sh->smem = (size_t)sh->slice * sizeof(float) + (size_t)max_nodes * 4 * sizeof(int) +
+               (draft_in_smem(elems, sh->threads) ? (size_t)elems * sh->threads * sizeof(float) + 16
+                                                  : 0);
     const int ai = elems == 4 ? 0 : elems == 8 ? 1 : elems == 16 ? 2 : 3;
     sh->kern = kerns[narrow][logits ? 1 : 0][ai];
     const Kern kern = sh->kern;
