@@ -162,6 +162,34 @@ __device__ __forceinline__ unsigned long long fixed40_int(float r) {
 // above it x is already an integer.
 __device__ __forceinline__ float fixed40_f(float r) { return truncf(r * kTwo40); }
 
+// Divisor of one rejection round: z, an estimate of 1/z and z/2.
+struct RoundDiv {
+  float z, rz, hz;
+};
+__device__ __forceinline__ RoundDiv round_div(float z) {
+  return RoundDiv{z, (z > 0.f) ? __frcp_rn(z) : 0.f, 0.5f * z};
+}
+
+// x / z rounded to nearest, for finite x >= 0 and z > 0 with the quotient
+// in [2^-64, 2^64] (here x, z < 2^41 are integers).  Markstein's correction
+// of the reciprocal estimate (P. Markstein, IBM J. Res. Dev. 34(1), 1990):
+// q0 = x * rz, then q1 = q0 + (x - q0 z) rz with fused multiply-adds.  q1 is
+// kept only when the exact remainder r = x - q1 z (one fused multiply-add;
+// exact because q1 is within an ulp of x/z) proves it is the nearest float:
+// |r| < z ulp(q1) / 2, or z ulp(q1) / 4 when q1 is a power of two (the
+// floats below it are half as far apart).  Anything else -- a tie, or an
+// estimate that is not provably nearest -- goes to the IEEE division.
+__device__ __forceinline__ float div_rn_by(float x, const RoundDiv& d) {
+  if (x == 0.f) return 0.f;
+  const float q0 = x * d.rz;
+  const float q1 = fmaf(fmaf(-q0, d.z, x), d.rz, q0);
+  const float r = fmaf(-q1, d.z, x);
+  const uint32_t b = __float_as_uint(q1);
+  const float ulp = __uint_as_float((b & 0x7f800000u) - (23u << 23));   // 2^(exponent - 23)
+  const float lim = ((b & 0x7fffffu) == 0u) ? 0.5f * ulp * d.hz : ulp * d.hz;
+  return (fabsf(r) < lim) ? q1 : __fdiv_rn(x, d.z);
+}
+
 // Two sums over the block at once; every thread gets both totals.  One
 // barrier: the warps' partial sums go to s_tmp[par] (alternate the parity
 // from one call to the next, so a call never overwrites partials another
@@ -248,7 +276,8 @@ __host__ __device__ constexpr bool draft_in_smem(int e, int threads) {
 
 template <int E, int THREADS, bool UPD, bool SUMS, bool SMEM>
 __device__ __forceinline__ void walk_pass(float (&q)[E], DraftSlice<E, THREADS, SMEM>& p, int v0, int nv,
-                                          bool no_replace, int t_rej, float zf, float spf,
+                                          bool no_replace, int t_rej, const RoundDiv& zf,
+                                          const RoundDiv& spf,
                                           bool z_pos, int t_next, unsigned long long& sw,
                                           unsigned long long& sp, RoundSlot& slot) {
   const int tid = threadIdx.x;
@@ -258,9 +287,9 @@ __device__ __forceinline__ void walk_pass(float (&q)[E], DraftSlice<E, THREADS, 
     float pe = p.get(e);
     if (UPD) {
       const float qa = q[e], pa = pe;
-      if (z_pos) q[e] = __fdiv_rn(fixed40_f(fmaxf(0.f, __fsub_rn(qa, pa))), zf);
+      if (z_pos) q[e] = div_rn_by(fixed40_f(fmaxf(0.f, __fsub_rn(qa, pa))), zf);
       if (no_replace) {
-        pe = (v0 + i == t_rej) ? 0.f : (spf > 0.f ? __fdiv_rn(fixed40_f(pa), spf) : 0.f);
+        pe = (v0 + i == t_rej) ? 0.f : (spf.z > 0.f ? div_rn_by(fixed40_f(pa), spf) : 0.f);
         p.set(e, pe);
       }
     }
@@ -453,8 +482,9 @@ accept_stochastic_kernel(const StochParams P) {
       // sums as if the first child were rejected, and its tested values
       unsigned long long sw = 0, sp = 0;
       const int t = s_tok[s_kids[0]];
-      walk_pass<E, THREADS, false, true, kPSmem>(q, p, v0, nv, no_replace, -1, 0.f, 0.f, false, t, sw, sp,
-                                s_slot[par]);
+      const RoundDiv none{0.f, 0.f, 0.f};
+      walk_pass<E, THREADS, false, true, kPSmem>(q, p, v0, nv, no_replace, -1, none, none, false, t,
+                                                 sw, sp, s_slot[par]);
       reduce_round(sw, sp, t);
     }
     bool moved = false;
@@ -492,17 +522,18 @@ accept_stochastic_kernel(const StochParams P) {
       }
       zf = __shfl_sync(0xffffffffu, zf, 0);
       spf = __shfl_sync(0xffffffffu, spf, 0);
+      const RoundDiv zd = round_div(zf), spd = round_div(spf);
       if (j + 1 < nk) {
         // update, and the next child's sums, in one pass
         unsigned long long sw = 0, sp = 0;
         const int tn = s_tok[s_kids[j + 1]];
-        walk_pass<E, THREADS, true, true, kPSmem>(q, p, v0, nv, no_replace, t, zf, spf, Z > 0ull, tn, sw, sp,
-                                 s_slot[par]);
+        walk_pass<E, THREADS, true, true, kPSmem>(q, p, v0, nv, no_replace, t, zd, spd, Z > 0ull, tn,
+                                                  sw, sp, s_slot[par]);
         reduce_round(sw, sp, tn);
       } else {
         unsigned long long sw = 0, sp = 0;
-        walk_pass<E, THREADS, true, false, kPSmem>(q, p, v0, nv, no_replace, t, zf, spf, Z > 0ull, -1, sw, sp,
-                                  s_slot[par]);
+        walk_pass<E, THREADS, true, false, kPSmem>(q, p, v0, nv, no_replace, t, zd, spd, Z > 0ull, -1,
+                                                   sw, sp, s_slot[par]);
       }
     }
     if (moved) continue;
@@ -644,6 +675,15 @@ int resident_clusters(const void* kern, int threads, int cs, size_t smem) {
   return n;
 }
 
+#ifdef EAGLE_WALK_DIV_TEST
+// Test build only: out[i] = div_rn_by(x[i], z[i]), to compare with the
+// IEEE division on many operand pairs.
+__global__ void walk_div_test_kernel(const float* x, const float* z, float* out, int n) {
+  const int i = blockIdx.x * blockDim.x + threadIdx.x;
+  if (i < n) out[i] = div_rn_by(x[i], round_div(z[i]));
+}
+#endif
+
 // Both stochastic entry points: d_q holds probabilities, or logits with
 // row_lse and temperature (LOGITS).
 eagle_status launch_stochastic(bool logits, int B, int max_nodes, int V, int R, int mode,
@@ -781,3 +821,12 @@ extern "C" eagle_status eagle_accept_stochastic_logits(
                            d_u_sample, max_depth, d_accept_len, d_accepted_nodes, d_out_tokens,
                            d_status, stream);
 }
+
+#ifdef EAGLE_WALK_DIV_TEST
+extern "C" EAGLE_API int eagle_test_walk_div(const float* d_x, const float* d_z, float* d_out, int n,
+                                             eagle_stream_t stream) {
+  if (n <= 0) return 0;
+  walk_div_test_kernel<<<(n + 255) / 256, 256, 0, (cudaStream_t)stream>>>(d_x, d_z, d_out, n);
+  return cudaGetLastError() == cudaSuccess ? 0 : 1;
+}
+#endif
