@@ -607,10 +607,22 @@ int pick_cluster(int V, int threads, int prefer, int* slice_out, int* elems_out)
     if (e > prefer && cs < kWalkMaxCluster) continue;
     if (e > 32) return -1;
     *slice_out = slice;
-    *elems_out = e <= 4 ? 4 : e <= 8 ? 8 : e <= 16 ? 16 : 32;
+    *elems_out = e <= 4 ? 4 : e <= 8 ? 8 : e <= 16 ? 16 : e <= 24 ? 24 : 32;
     return cs;
   }
   return -1;
+}
+
+// The same with a given cluster size (0 if a slice needs more than 32
+// entries per thread).
+int fixed_cluster(int V, int threads, int cs, int* slice_out, int* elems_out) {
+  int slice = (V + cs - 1) / cs;
+  slice = (slice + 3) & ~3;
+  const int e = (slice + threads - 1) / threads;
+  if (e > 32) return 0;
+  *slice_out = slice;
+  *elems_out = e <= 4 ? 4 : e <= 8 ? 8 : e <= 16 ? 16 : e <= 24 ? 24 : 32;
+  return cs;
 }
 
 
@@ -708,31 +720,35 @@ eagle_status launch_stochastic(bool logits, int B, int max_nodes, int V, int R, 
   EAGLE_HOST_CHECK(!logits || d_row_lse, EAGLE_ERR_INVALID_ARG);
   EAGLE_HOST_CHECK(R == 0 || d_p_rows, EAGLE_ERR_INVALID_ARG);
   using Kern = void (*)(const StochParams);
-  static const Kern kerns[2][2][4] = {
-      {{accept_stochastic_kernel<4, false, kWideThreads>, accept_stochastic_kernel<8, false, kWideThreads>,
-        accept_stochastic_kernel<16, false, kWideThreads>, accept_stochastic_kernel<32, false, kWideThreads>},
-       {accept_stochastic_kernel<4, true, kWideThreads>, accept_stochastic_kernel<8, true, kWideThreads>,
-        accept_stochastic_kernel<16, true, kWideThreads>, accept_stochastic_kernel<32, true, kWideThreads>}},
-      {{accept_stochastic_kernel<4, false, kNarrowThreads>, accept_stochastic_kernel<8, false, kNarrowThreads>,
-        accept_stochastic_kernel<16, false, kNarrowThreads>, accept_stochastic_kernel<32, false, kNarrowThreads>},
-       {accept_stochastic_kernel<4, true, kNarrowThreads>, accept_stochastic_kernel<8, true, kNarrowThreads>,
-        accept_stochastic_kernel<16, true, kNarrowThreads>, accept_stochastic_kernel<32, true, kNarrowThreads>}}};
-  static PerDeviceOnce attr_once[2][2][4];
+  // shapes: 0 wide; 1 narrow; 2 narrow in clusters of three quarters the
+  // size (more entries per thread, a third more clusters resident)
+#define EAGLE_WALK_KERNS(L, T)                                                              \
+  {accept_stochastic_kernel<4, L, T>, accept_stochastic_kernel<8, L, T>,                   \
+   accept_stochastic_kernel<16, L, T>, accept_stochastic_kernel<24, L, T>,                  \
+   accept_stochastic_kernel<32, L, T>}
+  static const Kern kerns[2][2][5] = {
+      {EAGLE_WALK_KERNS(false, kWideThreads), EAGLE_WALK_KERNS(true, kWideThreads)},
+      {EAGLE_WALK_KERNS(false, kNarrowThreads), EAGLE_WALK_KERNS(true, kNarrowThreads)}};
+#undef EAGLE_WALK_KERNS
+  static PerDeviceOnce attr_once[2][2][5];
   // a shape's cluster size, slice, kernel and shared memory, attributes set
   struct Shape {
     int cs, slice, threads;
     Kern kern;
     size_t smem;
   };
-  auto shape = [&](int narrow, Shape* sh) -> eagle_status {
+  auto shape = [&](int kind, Shape* sh) -> eagle_status {
     int elems = 0;
+    const int narrow = kind > 0 ? 1 : 0;
     sh->threads = narrow ? kNarrowThreads : kWideThreads;
     sh->cs = pick_cluster(V, sh->threads, narrow ? kNarrowPrefer : kWidePrefer, &sh->slice, &elems);
+    if (kind == 2)
+      sh->cs = (sh->cs >= 4) ? fixed_cluster(V, sh->threads, sh->cs / 4 * 3, &sh->slice, &elems) : 0;
     if (sh->cs <= 0) return EAGLE_ERR_UNSUPPORTED;
     sh->smem = (size_t)sh->slice * sizeof(float) + (size_t)max_nodes * 4 * sizeof(int) +
                (draft_in_smem(elems, sh->threads) ? (size_t)elems * sh->threads * sizeof(float) + 16
                                                   : 0);
-    const int ai = elems == 4 ? 0 : elems == 8 ? 1 : elems == 16 ? 2 : 3;
+    const int ai = elems == 4 ? 0 : elems == 8 ? 1 : elems == 16 ? 2 : elems == 24 ? 3 : 4;
     sh->kern = kerns[narrow][logits ? 1 : 0][ai];
     const Kern kern = sh->kern;
     if (attr_once[narrow][logits ? 1 : 0][ai].run([&] {
@@ -750,12 +766,22 @@ eagle_status launch_stochastic(bool logits, int B, int max_nodes, int V, int R, 
       return EAGLE_ERR_CUDA;
     return EAGLE_OK;
   };
+  // the first shape whose clusters are all resident at once, else the one
+  // with the most resident
   Shape sh;
   eagle_status st = shape(0, &sh);
   if (st != EAGLE_OK) return st;
-  if (B > 1 && sh.cs > 1 && B > resident_clusters((const void*)sh.kern, sh.threads, sh.cs, sh.smem)) {
-    Shape nw;
-    if (shape(1, &nw) == EAGLE_OK) sh = nw;
+  if (B > 1 && sh.cs > 1) {
+    int best_n = resident_clusters((const void*)sh.kern, sh.threads, sh.cs, sh.smem);
+    for (int kind = 1; kind <= 2 && B > best_n; ++kind) {
+      Shape c;
+      if (shape(kind, &c) != EAGLE_OK) continue;
+      const int n = resident_clusters((const void*)c.kern, c.threads, c.cs, c.smem);
+      if (n > best_n) {
+        best_n = n;
+        sh = c;
+      }
+    }
   }
   StochParams P;
   P.max_nodes = max_nodes;
