@@ -23,7 +23,8 @@ __all__ = [
     "eagle_accept_stochastic", "eagle_accept_stochastic_logits", "eagle_draft_expand",
     "eagle_draft_pool_bytes", "eagle_draft_static", "eagle_tree_attn_paged",
     "eagle_rmsnorm", "eagle_cast_bf16", "eagle_tree_rope_table", "eagle_gemm",
-    "eagle_kv_commit_paged", "eagle_draft_expand_dep", "eagle_draft_head_input",
+    "eagle_kv_commit_paged", "eagle_draft_expand_dep", "eagle_draft_expand_all",
+    "eagle_draft_head_input",
     "eagle_draft_rows", "eagle_embed_rows", "eagle_loop_advance",
     "EPI_STORE", "EPI_ACCUM", "EPI_SWIGLU", "EPI_QKV_ROPE",
     "eagle_lmhead_softmax_noalloc", "eagle_lmhead_noalloc_max_scratch_bytes",
@@ -74,6 +75,7 @@ _SIGS = {
     "eagle_gemm": ([_i] * 4 + [_p] * 9 + [_i] * 3 + [_p, _p], _i),
     "eagle_kv_commit_paged": ([_i] * 8 + [_p] * 11, _i),
     "eagle_draft_expand_dep": ([_i] * 6 + [_p] * 4 + [_sz] + [_p] * 8, _i),
+    "eagle_draft_expand_all": ([_i] * 4 + [_p] * 4 + [_sz] + [_p] * 8, _i),
     "eagle_draft_head_input": ([_i] * 6 + [_p, _sz] + [_p] * 9, _i),
     "eagle_draft_rows": ([_i] * 5 + [_p] * 5, _i),
     "eagle_embed_rows": ([_i] * 3 + [_p] * 5, _i),
@@ -324,6 +326,17 @@ def eagle_draft_expand(pool, status, *, B: int, V: int, k: int, depth: int, leve
           _ptr(draft_logp), _ptr(budget), _ptr(root_token), _ptr(pool),
           pool.numel() * pool.element_size(), _ptr(tree_off), _ptr(parent), _ptr(tokens),
           _ptr(node_depth), _ptr(score), _ptr(p_row_of_node), _ptr(status), _stream(stream))
+
+
+def eagle_draft_expand_all(pool, status, *, B: int, V: int, k: int, depth: int, draft_logp,
+                           budget, root_token, tree_off, parent, tokens, node_depth, score,
+                           p_row_of_node, stream=None) -> None:
+    """EAGLE-2 tree build in one call (every level, then the finalize);
+    draft_logp [B, R, V] fp32 with R = 1 + (depth-1)*k, all rows ready."""
+    _call("eagle_draft_expand_all", B, V, k, depth, _ptr(draft_logp), _ptr(budget),
+          _ptr(root_token), _ptr(pool), pool.numel() * pool.element_size(), _ptr(tree_off),
+          _ptr(parent), _ptr(tokens), _ptr(node_depth), _ptr(score), _ptr(p_row_of_node),
+          _ptr(status), _stream(stream))
 
 
 def eagle_draft_static(tmpl_parent, tmpl_rank, tmpl_row, draft_logp, root_token, tree_off,

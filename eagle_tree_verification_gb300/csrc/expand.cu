@@ -62,8 +62,9 @@ ChunkPlan chunk_plan(int rows, int V) {
 
 size_t align256(size_t x) { return (x + 255) & ~(size_t)255; }
 
-// Tickets and chunk lists come twice, for even and odd levels: a level
-// ranks its chunks while the previous one still merges.
+// Tickets come twice, for even and odd levels: a level ranks its chunks
+// while the previous one still merges.  Chunk lists likewise, or (all
+// levels ranked in one launch) once per level.
 struct PoolLayout {
   int P;             // candidate capacity per sequence
   ChunkPlan c0, c1;  // level 0 / later levels
@@ -93,7 +94,9 @@ PoolLayout pool_layout(int B, int k, int depth, int V) {
   L.off_depth = take((size_t)B * L.P * 4);
   L.off_prow = take((size_t)B * L.P * 4);
   L.off_score = take((size_t)B * L.P * 4);
-  L.off_partial = take(2 * L.parts * 8);
+  // chunk lists: by level parity for level-by-level builds, one slice per
+  // level when every level is ranked in one launch
+  L.off_partial = take((size_t)std::max(2, depth) * L.parts * 8);
   L.total = o;
   return L;
 }
@@ -730,6 +733,117 @@ expand_level_stream_kernel(const LevelParams A, int total_chunks) {
   }
 }
 
+// Every level's chunk lists in one launch, when all draft rows are ready
+// before it: chunk ids run level by level (level 0's B rows, then B k rows
+// per later level, S chunks each); each persistent CTA walks a contiguous
+// range through the same two-stage ring as the streaming level kernel, with
+// the row bound carried along a row, and writes its lists to the level's
+// slice of the pool (`level_keys` keys apart).  The levels are merged
+// afterwards, one launch each (expand_merge_kernel).
+__global__ void __launch_bounds__(kLvThreads, 2)
+expand_all_stream_kernel(const LevelParams A, long long level_keys, int total_chunks) {
+  pdl_begin();   // the pool reset comes just before
+  __shared__ ChunkShared C;
+  __shared__ uint64_t full[kStreamStages];
+  __shared__ int abort_flag;
+  extern __shared__ __align__(128) unsigned char stage_mem[];   // kStreamSmem bytes
+  const int tid = threadIdx.x;
+  const int k = A.k, S = A.S;
+  const int n0 = A.B * S, n1 = A.B * k * S;   // chunks of level 0, of a later level
+  auto decode = [&](int id, int& level, int& row, int& chunk) {
+    int x = id;
+    level = 0;
+    if (id >= n0) {
+      level = 1 + (id - n0) / n1;
+      x = (id - n0) % n1;
+    }
+    row = x / S;
+    chunk = x % S;
+  };
+  const int id0 = (int)((long long)total_chunks * blockIdx.x / gridDim.x);
+  const int id1 = (int)((long long)total_chunks * (blockIdx.x + 1) / gridDim.x);
+  auto issue = [&](int id, int st) {
+    int level, row, chunk;
+    decode(id, level, row, chunk);
+    const int F = level ? k : 1;
+    const int b = row / F, f = row % F;
+    const int local_row = (level == 0) ? 0 : 1 + (level - 1) * k + f;
+    const int c0 = chunk * kStreamChunk;
+    const uint32_t bytes = (uint32_t)min(kStreamChunk, A.V - c0) * 4u;   // V % 4 == 0
+    tc::mbar_arrive_expect_tx(&full[st], bytes);
+    bulk_load(stage_mem + (size_t)st * kStreamChunk * 4,
+              A.logp + ((size_t)b * A.R + local_row) * A.V + c0, bytes, &full[st]);
+  };
+  if (tid == 0) {
+    for (int st = 0; st < kStreamStages; ++st) tc::mbar_init(&full[st], 1);
+    abort_flag = 0;
+    tc::fence_barrier_init();
+    for (int st = 0; st < kStreamStages; ++st)
+      if (id0 + st < id1) issue(id0 + st, st);
+  }
+  __syncthreads();
+  LevelParams Al = A;   // the current level's view: F, level, its pool slice
+  int cur_level = -1, bound_row = -1;
+  unsigned long long bound = 0ull;
+  int i = 0;
+  bool aborted = false;
+  for (int id = id0; id < id1; ++id, ++i) {
+    const int st = i % kStreamStages;
+    const bool got =
+        tc::mbar_wait(&full[st], (uint32_t)((i / kStreamStages) & 1), &abort_flag, A.status);
+    float v[kStreamVec][4];
+    const float4* sm4 = reinterpret_cast<const float4*>(stage_mem + (size_t)st * kStreamChunk * 4);
+#pragma unroll
+    for (int j = 0; j < kStreamVec; ++j) {
+      const float4 x = got ? sm4[j * kLvThreads + tid] : make_float4(0.f, 0.f, 0.f, 0.f);
+      v[j][0] = x.x;
+      v[j][1] = x.y;
+      v[j][2] = x.z;
+      v[j][3] = x.w;
+    }
+    if (!__syncthreads_and(got)) {
+      aborted = true;
+      break;
+    }
+    auto refill = [&]() {
+      if (id + kStreamStages < id1) {
+        asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+        issue(id + kStreamStages, st);
+      }
+    };
+    int level, row, chunk;
+    decode(id, level, row, chunk);
+    if (level != cur_level) {
+      cur_level = level;
+      Al.level = level;
+      Al.F = level ? k : 1;
+      Al.pool.partial = A.pool.partial + (size_t)level * level_keys;
+      bound_row = -1;
+    }
+    if (row != bound_row) {
+      bound_row = row;
+      bound = 0ull;
+    }
+    chunk_topk<kStreamVec>(Al, row, chunk, v, C, false, refill, &bound);
+  }
+  if (aborted && tid == 0) {
+    // let the copies still in flight land before the CTA leaves
+    int never = 0;
+    for (int j = i; j < i + kStreamStages; ++j)
+      if (id0 + j < id1)
+        tc::mbar_wait(&full[j % kStreamStages], (uint32_t)((j / kStreamStages) & 1), &never,
+                      nullptr, 200000000ll);
+  }
+}
+
+// One level's merge for every sequence (one CTA each), after its chunk
+// lists and the level before are complete.
+__global__ void __launch_bounds__(kLvThreads, 1) expand_merge_kernel(const LevelParams A) {
+  pdl_begin();
+  __shared__ MergeShared M;
+  merge_sequence(A, blockIdx.x, M);
+}
+
 // Finalize one sequence with the calling CTA (any block size that is a
 // multiple of 64): keep the `budget` pool entries of largest key (score
 // desc, creation order) -- a radix select of the budget-th key -- number the
@@ -1050,6 +1164,92 @@ extern "C" eagle_status eagle_draft_expand(int B, int V, int k, int depth, int l
   return expand_impl(false, B, V, k, depth, level, finalize, d_draft_logp, d_budget, d_root_token,
                      d_pool, pool_bytes, d_tree_off, d_parent, d_tokens, d_node_depth, d_score,
                      d_p_row_of_node, d_status, stream);
+}
+
+// Every level and the finalize in one call (all draft rows ready): one
+// launch ranks every level's chunks, then one merge launch per level and
+// the finalize.  Rows that are not 16-byte aligned rows of a multiple of 4
+// entries take the level-by-level path instead.
+extern "C" eagle_status eagle_draft_expand_all(int B, int V, int k, int depth,
+                                               const float* d_draft_logp,
+                                               const int32_t* d_budget,
+                                               const int32_t* d_root_token, void* d_pool,
+                                               size_t pool_bytes, int32_t* d_tree_off,
+                                               int32_t* d_parent, int32_t* d_tokens,
+                                               int32_t* d_node_depth, float* d_score,
+                                               int32_t* d_p_row_of_node, int* d_status,
+                                               eagle_stream_t stream) {
+  EAGLE_HOST_CHECK(B >= 1 && V >= 1, EAGLE_ERR_INVALID_ARG);
+  EAGLE_HOST_CHECK(k >= 1 && k <= EAGLE_MAX_TOPK && k <= V, EAGLE_ERR_UNSUPPORTED);
+  EAGLE_HOST_CHECK(depth >= 1 && depth <= EAGLE_MAX_DEPTH, EAGLE_ERR_UNSUPPORTED);
+  EAGLE_HOST_CHECK(V <= kMaxV, EAGLE_ERR_UNSUPPORTED);
+  EAGLE_HOST_CHECK(d_pool && d_status && d_draft_logp && d_budget && d_tree_off && d_parent &&
+                       d_tokens && d_node_depth && d_score && d_p_row_of_node,
+                   EAGLE_ERR_INVALID_ARG);
+  const PoolLayout L = pool_layout(B, k, depth, V);
+  EAGLE_HOST_CHECK(pool_bytes >= L.total, EAGLE_ERR_WORKSPACE);
+  EAGLE_HOST_CHECK(((uintptr_t)d_pool & 255) == 0, EAGLE_ERR_INVALID_ARG);
+  auto level_call = [&](int level, int finalize) {
+    return expand_impl(false, B, V, k, depth, level, finalize, d_draft_logp, d_budget,
+                       d_root_token, d_pool, pool_bytes, d_tree_off, d_parent, d_tokens,
+                       d_node_depth, d_score, d_p_row_of_node, d_status, stream);
+  };
+  if (V % 4 != 0 || ((uintptr_t)d_draft_logp & 15) != 0) {
+    for (int level = 0; level < depth; ++level) {
+      const eagle_status st = level_call(level, level == depth - 1 ? 2 : 0);
+      if (st != EAGLE_OK) return st;
+    }
+    return EAGLE_OK;
+  }
+  const PoolPtrs pp = pool_ptrs(d_pool, L);
+  cudaStream_t s = (cudaStream_t)stream;
+  const int R = 1 + (depth - 1) * k;
+  const int S = (int)ceil_div(V, (long long)kStreamChunk);
+  // fresh tree: zero the pool fill counts and the level tickets
+  if (cudaMemsetAsync(static_cast<char*>(d_pool), 0, L.off_frontier, s) != cudaSuccess)
+    return EAGLE_ERR_CUDA;
+  LevelParams A = {};
+  A.B = B;
+  A.V = V;
+  A.k = k;
+  A.F = 1;
+  A.R = R;
+  A.S = S;
+  A.level = 0;
+  A.P = L.P;
+  A.vec_ok = true;
+  A.fused = false;
+  A.rows_wait = false;
+  A.logp = d_draft_logp;
+  A.pool = pp;
+  A.status = d_status;
+  static PerDeviceOnce attr_once;
+  if (attr_once.run([] {
+        cudaError_t e = cudaFuncSetAttribute(expand_all_stream_kernel,
+                                             cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                             (int)kStreamSmem);
+        if (e == cudaSuccess)
+          e = cudaFuncSetAttribute(expand_all_stream_kernel,
+                                   cudaFuncAttributePreferredSharedMemoryCarveout,
+                                   cudaSharedmemCarveoutMaxShared);
+        return e;
+      }) != cudaSuccess)
+    return EAGLE_ERR_CUDA;
+  const long long total = (long long)B * S + (long long)(depth - 1) * B * k * S;
+  EAGLE_HOST_CHECK(total < (1ll << 31), EAGLE_ERR_UNSUPPORTED);
+  const int grid = (int)std::min<long long>(total, kOneWave);
+  eagle_status st = launch_status(launch_pdl(expand_all_stream_kernel, dim3(grid),
+                                             dim3(kLvThreads), kStreamSmem, s, A,
+                                             (long long)L.parts, (int)total));
+  for (int level = 0; level < depth && st == EAGLE_OK; ++level) {
+    LevelParams M = A;
+    M.level = level;
+    M.F = level ? k : 1;
+    M.pool.partial = pp.partial + (size_t)level * L.parts;
+    st = launch_status(launch_pdl(expand_merge_kernel, dim3(B), dim3(kLvThreads), 0, s, M));
+  }
+  if (st != EAGLE_OK) return st;
+  return level_call(depth - 1, 1);
 }
 
 extern "C" eagle_status eagle_draft_expand_dep(int B, int V, int k, int depth, int level,

@@ -24,7 +24,8 @@ from . import (EPI_ACCUM, EPI_QKV_ROPE, EPI_STORE, EPI_SWIGLU, SAMPLE_NO_REPLACE
                eagle_accept_greedy, eagle_draft_head_input, eagle_draft_rows, eagle_embed_rows,
                eagle_kv_commit_paged, eagle_loop_advance, eagle_tree_attn_paged,
                eagle_accept_stochastic, eagle_accept_stochastic_logits, eagle_cast_bf16,
-               eagle_draft_expand, eagle_draft_pool_bytes, eagle_draft_static, eagle_gemm,
+               eagle_draft_expand, eagle_draft_expand_all, eagle_draft_pool_bytes,
+               eagle_draft_static, eagle_gemm,
                eagle_lmhead_softmax, eagle_lmhead_workspace_bytes, eagle_rmsnorm,
                eagle_tree_attn, eagle_tree_attn_workspace_bytes, eagle_tree_rope_table)
 
@@ -315,16 +316,13 @@ class TreeVerifyStep:
                                self.score, self.p_row_of_node, self.status,
                                max_rank=self.tmpl_max_rank, stream=stream)
             return
-        for lev in range(s.depth - 1):
-            eagle_draft_expand(self.pool, self.status, B=s.B, V=s.V, k=s.k, depth=s.depth,
-                               level=lev, draft_logp=self.draft_logp, stream=stream)
-        # the last level with the finalize fused in
-        eagle_draft_expand(self.pool, self.status, B=s.B, V=s.V, k=s.k, depth=s.depth,
-                           level=s.depth - 1, finalize=2, draft_logp=self.draft_logp,
-                           budget=self.budget, root_token=self.root_token,
-                           tree_off=self.tree_off, parent=self.parent, tokens=self.tokens,
-                           node_depth=self.node_depth, score=self.score,
-                           p_row_of_node=self.p_row_of_node, stream=stream)
+        # every draft row is an input of the step: all levels in one call
+        eagle_draft_expand_all(self.pool, self.status, B=s.B, V=s.V, k=s.k, depth=s.depth,
+                               draft_logp=self.draft_logp, budget=self.budget,
+                               root_token=self.root_token, tree_off=self.tree_off,
+                               parent=self.parent, tokens=self.tokens,
+                               node_depth=self.node_depth, score=self.score,
+                               p_row_of_node=self.p_row_of_node, stream=stream)
 
     def run_layer(self, stream=None) -> None:
         """The decoder layer over every tree node, ending in the final
@@ -422,7 +420,9 @@ class TreeVerifyStep:
         """Kernels launched by run() (the count the benchmark reports)."""
         n = 0
         if self.s.k:
-            n += self.s.depth                    # one per level, finalize fused
+            # all levels' chunks, one merge per level, the finalize (rows of a
+            # multiple of 4 entries); else one per level, finalize fused
+            n += self.s.depth + 2 if self.s.V % 4 == 0 else self.s.depth
         elif self.s.static:
             n += 2 if len(self.s.static[0]) > 1 else 1   # ranks + finish
         n += 1                                   # attention

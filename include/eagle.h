@@ -382,6 +382,23 @@ EAGLE_API eagle_status eagle_draft_expand(int B, int V, int k, int depth, int le
                                 int32_t *d_p_row_of_node, int *d_status,
                                 eagle_stream_t stream);
 
+/* eagle_draft_expand_all -- the whole EAGLE-2 tree build in one call: every
+ * level (0 .. depth-1) and the finalize, with the same results as
+ * eagle_draft_expand called for each level and then finalize (same
+ * arguments, same outputs; budget, root_token and the tree outputs are
+ * required).  Every level's draft rows must be ready before the previous
+ * kernel on `stream` ends: one launch ranks the chunks of all levels at once,
+ * then the levels are merged one launch each.  (Rows whose length is not a
+ * multiple of 4 or that are not 16-byte aligned are built level by level.)
+ * d_pool: eagle_draft_pool_bytes(B, k, depth, V) bytes, as above. */
+EAGLE_API eagle_status eagle_draft_expand_all(int B, int V, int k, int depth,
+                                    const float *d_draft_logp, const int32_t *d_budget,
+                                    const int32_t *d_root_token, void *d_pool, size_t pool_bytes,
+                                    int32_t *d_tree_off, int32_t *d_parent, int32_t *d_tokens,
+                                    int32_t *d_node_depth, float *d_score,
+                                    int32_t *d_p_row_of_node, int *d_status,
+                                    eagle_stream_t stream);
+
 /* eagle_draft_expand for draft rows written by the kernel queued just before
  * it on `stream` (the draft head of a draft -> verify loop): the same level
  * or finalize, with every row read only after that kernel has finished.

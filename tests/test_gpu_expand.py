@@ -11,7 +11,7 @@ from gpu_common import cuda_ready, to_np
 pytestmark = pytest.mark.gpu
 
 
-def _gpu_tree(E, lp, B, V, k, depth, budget, root_token, fused=False):
+def _gpu_tree(E, lp, B, V, k, depth, budget, root_token, fused=False, all_levels=False):
     import torch
     R = 1 + (depth - 1) * k
     pool = torch.zeros(E.eagle_draft_pool_bytes(B, k, depth, V), dtype=torch.uint8, device="cuda")
@@ -25,6 +25,10 @@ def _gpu_tree(E, lp, B, V, k, depth, budget, root_token, fused=False):
     out["tree_off"] = torch.full((B + 1,), -7, dtype=torch.int32, device="cuda")
     fin = dict(budget=torch.tensor(budget, dtype=torch.int32, device="cuda"),
                root_token=torch.tensor(root_token, dtype=torch.int32, device="cuda"), **out)
+    if all_levels:
+        E.eagle_draft_expand_all(pool, st, B=B, V=V, k=k, depth=depth, draft_logp=d_lp, **fin)
+        torch.cuda.synchronize()
+        return {n: to_np(t) for n, t in out.items()}, int(st.item())
     for lev in range(depth - 1 if fused else depth):
         E.eagle_draft_expand(pool, st, B=B, V=V, k=k, depth=depth, level=lev, draft_logp=d_lp)
     if fused:
@@ -49,15 +53,17 @@ def _gpu_tree(E, lp, B, V, k, depth, budget, root_token, fused=False):
     (8, 40000, 8, 3, [20, 64, 0, 5, 64, 64, 33, 1], 3.0),
     (8, 70004, 6, 3, [30, 12, 64, 7, 1, 0, 9, 40], 3.0),
 ])
-@pytest.mark.parametrize("fused", [False, True])
-def test_expand_matches_oracle(B, V, k, depth, budgets, sigma, fused):
-    # fused: the last level and the finalize in one launch
+@pytest.mark.parametrize("mode", ["levels", "fused", "all"])
+def test_expand_matches_oracle(B, V, k, depth, budgets, sigma, mode):
+    # fused: the last level and the finalize in one launch; all: every level
+    # in one call (all levels' chunks ranked in one launch, then the merges)
     E = cuda_ready()
     R = 1 + (depth - 1) * k
     lp, _ = synth.draft_rows(B * 7 + V, "expand", B * R, V, sigma)
     ref = O.build_eagle2_tree(lp, B=B, k=k, depth=depth, budget=budgets,
                               root_token=list(range(B)))
-    got, st = _gpu_tree(E, lp, B, V, k, depth, budgets, list(range(B)), fused=fused)
+    got, st = _gpu_tree(E, lp, B, V, k, depth, budgets, list(range(B)), fused=(mode == "fused"),
+                        all_levels=(mode == "all"))
     assert st == 0
     for name in ("tree_off", "parent", "tokens", "p_row_of_node", "score"):
         np.testing.assert_array_equal(got[name], ref[name], err_msg=name)
