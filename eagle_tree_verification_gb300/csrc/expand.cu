@@ -39,6 +39,7 @@ constexpr int kMergeRegs = 8;          // chunk-list keys per lane kept in regis
 constexpr int kFinalThreads = 1024;
 constexpr int kMaxV = 1 << 19;
 constexpr size_t kFusedSmemMax = 64 * 1024;  // finalize memory fused into a level
+constexpr size_t kFinishSmemMax = 160 * 1024;  // finalize memory beside the merges of all levels
 // Bound-raising rounds never exceed (keys / (cap - k)); past these limits a
 // selection stops with EAGLE_ERR_TIMEOUT instead of looping.
 constexpr int kChunkRounds = 32;   // keys per chunk <= 8192, cap - k >= 480
@@ -844,6 +845,29 @@ __global__ void __launch_bounds__(kLvThreads, 1) expand_merge_kernel(const Level
   merge_sequence(A, blockIdx.x, M);
 }
 
+// Every level's merge of one sequence in turn, then its finalize: a
+// sequence's levels depend only on its own earlier levels, so one CTA per
+// sequence runs them all (`smem_raw`: the finalize's P * 44 bytes).
+__global__ void __launch_bounds__(kLvThreads, 1)
+expand_finish_kernel(const LevelParams A, int depth, long long level_keys) {
+  pdl_begin();
+  __shared__ MergeShared M;
+  extern __shared__ __align__(16) unsigned char smem_raw[];
+  const int b = blockIdx.x;
+  LevelParams Al = A;
+  for (int level = 0; level < depth; ++level) {
+    Al.level = level;
+    Al.F = level ? A.k : 1;
+    Al.pool.partial = A.pool.partial + (size_t)level * level_keys;
+    merge_sequence(Al, b, M);
+    // the frontier, its scores and the pool fill went to global memory:
+    // the next level (this CTA) reads them back
+    __threadfence_block();
+    __syncthreads();
+  }
+  finalize_sequence(A.fin, b, smem_raw);
+}
+
 // Finalize one sequence with the calling CTA (any block size that is a
 // multiple of 64): keep the `budget` pool entries of largest key (score
 // desc, creation order) -- a radix select of the budget-th key -- number the
@@ -1241,6 +1265,38 @@ extern "C" eagle_status eagle_draft_expand_all(int B, int V, int k, int depth,
   eagle_status st = launch_status(launch_pdl(expand_all_stream_kernel, dim3(grid),
                                              dim3(kLvThreads), kStreamSmem, s, A,
                                              (long long)L.parts, (int)total));
+  if (st != EAGLE_OK) return st;
+  // every level's merge and the finalize in one launch (one CTA per
+  // sequence), when the finalize's shared memory fits beside the merge's
+  const size_t fin_smem = (size_t)L.P * (2 * 8 + 7 * 4);
+  if (fin_smem <= kFinishSmemMax) {
+    FinalParams F;
+    F.B = B;
+    F.k = k;
+    F.R = R;
+    F.P = L.P;
+    F.budget = d_budget;
+    F.root_token = d_root_token;
+    F.pool = pp;
+    F.tree_off = d_tree_off;
+    F.parent = d_parent;
+    F.tokens = d_tokens;
+    F.node_depth = d_node_depth;
+    F.score = d_score;
+    F.p_row_of_node = d_p_row_of_node;
+    F.status = d_status;
+    A.fin = F;
+    // (its static shared memory plus the finalize's may pass 48 KB)
+    static PerDeviceOnce finish_once;
+    if (finish_once.run([] {
+          return cudaFuncSetAttribute(expand_finish_kernel,
+                                      cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                      (int)kFinishSmemMax);
+        }) != cudaSuccess)
+      return EAGLE_ERR_CUDA;
+    return launch_status(launch_pdl(expand_finish_kernel, dim3(B), dim3(kLvThreads), fin_smem, s,
+                                    A, depth, (long long)L.parts));
+  }
   for (int level = 0; level < depth && st == EAGLE_OK; ++level) {
     LevelParams M = A;
     M.level = level;

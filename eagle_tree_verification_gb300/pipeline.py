@@ -420,9 +420,16 @@ class TreeVerifyStep:
         """Kernels launched by run() (the count the benchmark reports)."""
         n = 0
         if self.s.k:
-            # all levels' chunks, one merge per level, the finalize (rows of a
-            # multiple of 4 entries); else one per level, finalize fused
-            n += self.s.depth + 2 if self.s.V % 4 == 0 else self.s.depth
+            # all levels' chunks, then every merge and the finalize (or one
+            # merge launch per level and the finalize when the finalize's
+            # shared memory is too large), for rows of a multiple of 4
+            # entries; else one per level, finalize fused
+            k, d = self.s.k, self.s.depth
+            fin_smem = (k + (d - 1) * k * k) * 44
+            if self.s.V % 4 == 0:
+                n += 2 if fin_smem <= 160 * 1024 else d + 2
+            else:
+                n += d
         elif self.s.static:
             n += 2 if len(self.s.static[0]) > 1 else 1   # ranks + finish
         n += 1                                   # attention
