@@ -293,6 +293,7 @@ struct ChunkShared {
   unsigned long long top[EAGLE_MAX_TOPK];
   unsigned long long tau;
   unsigned long long kth;   // the chunk's k-th largest key (0: fewer than k found)
+  int kth_row;              // ... and its row
   int cnt, last;
 };
 
@@ -314,10 +315,19 @@ struct NoRefill {
 // is below the row's k-th, and keys are unique), the bound search over the
 // group maxima is skipped, and the chunk may publish fewer than k keys.  On
 // return it is raised to this chunk's k-th largest key when that is larger.
-template <int VEC, typename Refill = NoRefill>
+// PIPE (a streaming CTA with two ChunkShared buffers used by turns, `other`
+// the previous chunk's): no barrier before the candidates and none after the
+// ranking, so warp 0 ranks this chunk while the other warps load and offer
+// the next one; they all meet at the next chunk's candidate barrier (no warp
+// gets two chunks ahead).  There, thread 0 resets the other buffer's count
+// and every thread folds the previous chunk's k-th key into the bound (the
+// bound lags one chunk).  A timed-out wait shows in `abort` after that
+// barrier; the call then returns true at once (else false).
+template <int VEC, bool PIPE = false, typename Refill = NoRefill>
 __device__ bool chunk_topk(const LevelParams& A, int row, int chunk, const float (&v)[VEC][4],
                            ChunkShared& C, bool take_ticket = true, const Refill& refill = Refill(),
-                           unsigned long long* bound = nullptr) {
+                           unsigned long long* bound = nullptr, ChunkShared* other = nullptr,
+                           volatile int* abort = nullptr) {
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const unsigned long long b_in = bound ? *bound : 0ull;
   const int b = row / A.F;
@@ -367,6 +377,9 @@ __device__ bool chunk_topk(const LevelParams& A, int row, int chunk, const float
       C.kth = 0ull;
     }
     if (__syncthreads_or(!(fin == 0.f)) && tid == 0) fail(A.status, EAGLE_ERR_NUMERIC);
+    if constexpr (PIPE) {
+      if (*abort) return true;
+    }
   }
   // every warp: the largest group maximum that at least k group maxima
   // reach -- at least k tokens of the chunk are >= it (ties included): the
@@ -418,6 +431,13 @@ __device__ bool chunk_topk(const LevelParams& A, int row, int chunk, const float
     } else {
       __syncthreads();
     }
+    if constexpr (PIPE) {
+      if (round == 0) {
+        if (*abort) return true;
+        if (tid == 0) other->cnt = 0;
+        if (other->kth_row == row && other->kth > *bound) *bound = other->kth;
+      }
+    }
     if (round == 0 && tid == 32) refill();
     cnt = C.cnt;
     if (cnt <= kCandCap) break;
@@ -450,8 +470,14 @@ __device__ bool chunk_topk(const LevelParams& A, int row, int chunk, const float
       const unsigned long long me = (lane < cnt) ? C.cand[lane] : 0ull;
       const int rank = warp_rank_desc(me);
       if (lane < cnt && rank < k) part[rank] = me;
-      if (lane < cnt && rank == k - 1) C.kth = me;
       if (lane >= cnt && lane < k) part[lane] = 0ull;   // fewer than k tokens (or above the bound)
+      const unsigned kb = __ballot_sync(0xffffffffu, lane < cnt && rank == k - 1);
+      const unsigned long long kv = __shfl_sync(0xffffffffu, me, kb ? __ffs(kb) - 1 : 0);
+      if (lane == 0) {
+        if (kb) C.kth = kv;
+        else if (PIPE) C.kth = 0ull;
+        C.kth_row = row;
+      }
     }
   } else {
     if (tid < cnt) {
@@ -463,7 +489,10 @@ __device__ bool chunk_topk(const LevelParams& A, int row, int chunk, const float
     }
     __syncthreads();
     if (warp == 0 && lane < k) part[lane] = C.top[lane];
-    if (tid == 0) C.kth = C.top[k - 1];
+    if (tid == 0) {
+      C.kth = C.top[k - 1];
+      C.kth_row = row;
+    }
   }
   if (warp == 0) {
     __syncwarp();
@@ -479,6 +508,7 @@ __device__ bool chunk_topk(const LevelParams& A, int row, int chunk, const float
       }
     }
   }
+  if constexpr (PIPE) return false;
   __syncthreads();
   if (bound && C.kth > *bound) *bound = C.kth;
   // nothing reads the count past the barrier above; the next call's
@@ -744,7 +774,7 @@ expand_level_stream_kernel(const LevelParams A, int total_chunks) {
 __global__ void __launch_bounds__(kLvThreads, 2)
 expand_all_stream_kernel(const LevelParams A, long long level_keys, int total_chunks) {
   pdl_begin();   // the pool reset comes just before
-  __shared__ ChunkShared C;
+  __shared__ ChunkShared C2[2];   // by chunk parity (chunk_topk's PIPE mode)
   __shared__ uint64_t full[kStreamStages];
   __shared__ int abort_flag;
   extern __shared__ __align__(128) unsigned char stage_mem[];   // kStreamSmem bytes
@@ -778,6 +808,11 @@ expand_all_stream_kernel(const LevelParams A, long long level_keys, int total_ch
   if (tid == 0) {
     for (int st = 0; st < kStreamStages; ++st) tc::mbar_init(&full[st], 1);
     abort_flag = 0;
+    for (int c = 0; c < 2; ++c) {
+      C2[c].cnt = 0;
+      C2[c].kth = 0ull;
+      C2[c].kth_row = -1;
+    }
     tc::fence_barrier_init();
     for (int st = 0; st < kStreamStages; ++st)
       if (id0 + st < id1) issue(id0 + st, st);
@@ -802,10 +837,8 @@ expand_all_stream_kernel(const LevelParams A, long long level_keys, int total_ch
       v[j][2] = x.z;
       v[j][3] = x.w;
     }
-    if (!__syncthreads_and(got)) {
-      aborted = true;
-      break;
-    }
+    // no barrier here: the stage is refilled only after the candidates'
+    // barrier, by which every thread has read it
     auto refill = [&]() {
       if (id + kStreamStages < id1) {
         asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
@@ -825,7 +858,11 @@ expand_all_stream_kernel(const LevelParams A, long long level_keys, int total_ch
       bound_row = row;
       bound = 0ull;
     }
-    chunk_topk<kStreamVec>(Al, row, chunk, v, C, false, refill, &bound);
+    if (chunk_topk<kStreamVec, true>(Al, row, chunk, v, C2[i & 1], false, refill, &bound,
+                                     &C2[(i & 1) ^ 1], &abort_flag)) {
+      aborted = true;
+      break;
+    }
   }
   if (aborted && tid == 0) {
     // let the copies still in flight land before the CTA leaves
