@@ -642,7 +642,10 @@ __global__ void __launch_bounds__(kLvThreads, 2) expand_level_kernel(const Level
 // completes a sequence merges it before moving on.
 constexpr int kStreamVec = kMaxVec;
 constexpr int kStreamChunk = kLvThreads * 4 * kStreamVec;   // tokens per chunk
-constexpr int kStreamStages = 2;
+#ifndef EAGLE_EXPAND_STAGES
+#define EAGLE_EXPAND_STAGES 2
+#endif
+constexpr int kStreamStages = EAGLE_EXPAND_STAGES;   // chunk stages in flight per streaming CTA
 constexpr size_t kStreamSmem = (size_t)kStreamStages * kStreamChunk * 4;
 
 __device__ __forceinline__ void bulk_load(void* dst, const void* src, uint32_t bytes,
