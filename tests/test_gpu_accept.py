@@ -150,11 +150,13 @@ def test_stochastic_walk_matches_oracle(mode, seed, B, V):
         np.testing.assert_array_equal(x, r)
 
 
-@pytest.mark.parametrize("B", [4, 12])
+@pytest.mark.parametrize("B", [4, 12, 16])
 def test_stochastic_many_rejections_then_sample_at_full_vocab(B):
     # random target vs random draft: almost every child is rejected, so every
     # sequence runs up to k residual rounds and then the inverse-CDF sampler.
-    # B = 12: more clusters than fit the GPU at once (two waves).
+    # The walk's launch shape follows B: 4 sequences fit at once as 16 CTAs
+    # of 1024 threads; 12 do not, and run as 16 CTAs of 512 threads, two per
+    # SM; 16 do not fit either way and run as 12 CTAs of 512 threads.
     E = cuda_ready()
     V = 128256
     case = _stoch_case(11, B, V, [(1, 8, 8)], plant_frac=0.0)
