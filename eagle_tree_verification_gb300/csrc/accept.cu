@@ -32,10 +32,15 @@ namespace {
 // most 8 vocabulary entries per thread before the cluster doubles (the
 // fastest per sequence).  Narrow: 512-thread CTAs, two per SM, at most 16
 // entries per thread -- twice the sequences resident at once, each slower.
-// The wide shape is taken when every sequence's cluster is resident at once.
+// Narrow-3/4: the narrow shape with three quarters of its cluster size (up
+// to 24 entries per thread), for when the narrow clusters do not all fit.
+// The wide shape is taken when every sequence's cluster is resident at once,
+// else whichever of the three has the most clusters resident.
 // (Measured at 16 sequences of V = 128256, one visited node and 8 rejection
 // rounds each: wide 206.7 us in three waves of clusters of 16, narrow
-// 195.0 us; clusters of 8 with 16 or 32 entries per thread 237.8 / 274.6 us.)
+// 195.0 us with 14 of 16 resident; clusters of 8 with 16 or 32 entries per
+// thread 237.8 / 274.6 us; narrow-3/4, clusters of 12, all 16 resident,
+// 127.3 us with the later per-entry changes.)
 constexpr int kWideThreads = 1024, kWidePrefer = 8;
 constexpr int kNarrowThreads = 512, kNarrowPrefer = 16;
 constexpr int kWalkMaxCluster = 16;

@@ -5,7 +5,9 @@
 // selection under a fixed draft-token budget.  A node's value is its
 // cumulative draft log-prob.
 //
-// One launch per level.  The level's draft rows (the only large data:
+// One launch per level, or (eagle_draft_expand_all, every draft row ready
+// before the call) every level's chunk lists in one launch and the merges
+// and finalize in one more.  The level's draft rows (the only large data:
 // F x V fp32) are cut into chunks spread over the whole GPU; each CTA keeps
 // its chunk in registers and finds the chunk's exact top-k with a threshold:
 // the k-th largest of 32 group maxima is a lower bound of the chunk's k-th
@@ -773,7 +775,10 @@ expand_level_stream_kernel(const LevelParams A, int total_chunks) {
 // range through the same two-stage ring as the streaming level kernel, with
 // the row bound carried along a row, and writes its lists to the level's
 // slice of the pool (`level_keys` keys apart).  The levels are merged
-// afterwards, one launch each (expand_merge_kernel).
+// afterwards: every level of a sequence and its finalize by one CTA
+// (expand_finish_kernel), or, when the finalize's shared memory does not fit
+// beside the merge's, one launch per level (expand_merge_kernel) and the
+// finalize launch.
 __global__ void __launch_bounds__(kLvThreads, 2)
 expand_all_stream_kernel(const LevelParams A, long long level_keys, int total_chunks) {
   pdl_begin();   // the pool reset comes just before

@@ -10,14 +10,16 @@
 //                          chunk).  TMA brings Q (once) and 128-key K/V blocks
 //                          (two-stage ring) into 128-byte-swizzled shared
 //                          memory; tcgen05.mma computes S = Q K^T into TMEM;
-//                          one thread per query row applies the mask (cache
-//                          bound, or the row's ancestor bitset built on chip
-//                          from parent[]) and the online softmax, writes P
-//                          (bf16) back to shared memory, and tcgen05.mma
-//                          forms P V into TMEM, which the same thread folds
-//                          into its fp32 output row.  Chunks of one
-//                          (sequence, head, tile) are merged by the last CTA
-//                          to finish (atomic ticket, no waiting).
+//                          two threads per query row (one per key half)
+//                          apply the mask (cache bound, or the row's
+//                          ancestor bitset built on chip from parent[]) and
+//                          the online softmax, write P (bf16 hi + lo) into
+//                          TMEM, and tcgen05.mma adds P V into the half's
+//                          fp32 accumulator in TMEM (rescaled only when the
+//                          running max grows by more than a set margin).
+//                          The cache chunks of one (sequence, head, tile)
+//                          form a thread-block cluster and merge their
+//                          partial rows through distributed shared memory.
 //   tree_attn_warp_kernel  CUDA-core kernel for fp32 inputs and other shapes:
 //                          one warp per (node, query head).
 // The ancestor mask is never stored: it is derived from parent[] on the fly.
