@@ -32,15 +32,16 @@ namespace {
 // most 8 vocabulary entries per thread before the cluster doubles (the
 // fastest per sequence).  Narrow: 512-thread CTAs, two per SM, at most 16
 // entries per thread -- twice the sequences resident at once, each slower.
-// Narrow-3/4: the narrow shape with three quarters of its cluster size (up
-// to 24 entries per thread), for when the narrow clusters do not all fit.
-// The wide shape is taken when every sequence's cluster is resident at once,
-// else whichever of the three has the most clusters resident.
+// Narrow in smaller clusters, for when the narrow clusters do not all fit:
+// among the sizes down to half the narrow one whose clusters are all
+// resident, the fewest entries per thread (a rejection round's cost follows
+// them), then the fewest CTAs; if none fits, the most clusters resident.
+// The wide shape is taken when every sequence's cluster is resident at once.
 // (Measured at 16 sequences of V = 128256, one visited node and 8 rejection
 // rounds each: wide 206.7 us in three waves of clusters of 16, narrow
 // 195.0 us with 14 of 16 resident; clusters of 8 with 16 or 32 entries per
-// thread 237.8 / 274.6 us; narrow-3/4, clusters of 12, all 16 resident,
-// 127.3 us with the later per-entry changes.)
+// thread 237.8 / 274.6 us; clusters of 12, all 16 resident, 24 entries per
+// thread (21 used), 127.3 us with the later per-entry changes.)
 constexpr int kWideThreads = 1024, kWidePrefer = 8;
 constexpr int kNarrowThreads = 512, kNarrowPrefer = 16;
 constexpr int kWalkMaxCluster = 16;
@@ -277,6 +278,15 @@ struct DraftSlice {
 
 __host__ __device__ constexpr bool draft_in_smem(int e, int threads) {
   return threads == kNarrowThreads || e == 16;
+}
+
+// Entries per thread the walk kernel is built for: the smallest that holds e.
+__host__ __device__ constexpr int walk_elems(int e) {
+  return e <= 4 ? 4 : e <= 8 ? 8 : e <= 16 ? 16 : e <= 20 ? 20 : e <= 24 ? 24 : 32;
+}
+constexpr int kWalkElemKinds = 6;
+__host__ __device__ constexpr int walk_elems_index(int E) {
+  return E == 4 ? 0 : E == 8 ? 1 : E == 16 ? 2 : E == 20 ? 3 : E == 24 ? 4 : 5;
 }
 
 template <int E, int THREADS, bool UPD, bool SUMS, bool SMEM>
@@ -612,7 +622,7 @@ int pick_cluster(int V, int threads, int prefer, int* slice_out, int* elems_out)
     if (e > prefer && cs < kWalkMaxCluster) continue;
     if (e > 32) return -1;
     *slice_out = slice;
-    *elems_out = e <= 4 ? 4 : e <= 8 ? 8 : e <= 16 ? 16 : e <= 24 ? 24 : 32;
+    *elems_out = walk_elems(e);
     return cs;
   }
   return -1;
@@ -626,7 +636,7 @@ int fixed_cluster(int V, int threads, int cs, int* slice_out, int* elems_out) {
   const int e = (slice + threads - 1) / threads;
   if (e > 32) return 0;
   *slice_out = slice;
-  *elems_out = e <= 4 ? 4 : e <= 8 ? 8 : e <= 16 ? 16 : e <= 24 ? 24 : 32;
+  *elems_out = walk_elems(e);
   return cs;
 }
 
@@ -725,35 +735,39 @@ eagle_status launch_stochastic(bool logits, int B, int max_nodes, int V, int R, 
   EAGLE_HOST_CHECK(!logits || d_row_lse, EAGLE_ERR_INVALID_ARG);
   EAGLE_HOST_CHECK(R == 0 || d_p_rows, EAGLE_ERR_INVALID_ARG);
   using Kern = void (*)(const StochParams);
-  // shapes: 0 wide; 1 narrow; 2 narrow in clusters of three quarters the
-  // size (more entries per thread, a third more clusters resident)
+  // shapes: 0 wide; 1 narrow; 2 narrow in smaller clusters (more entries
+  // per thread, more clusters resident)
 #define EAGLE_WALK_KERNS(L, T)                                                              \
-  {accept_stochastic_kernel<4, L, T>, accept_stochastic_kernel<8, L, T>,                   \
-   accept_stochastic_kernel<16, L, T>, accept_stochastic_kernel<24, L, T>,                  \
-   accept_stochastic_kernel<32, L, T>}
-  static const Kern kerns[2][2][5] = {
+  {accept_stochastic_kernel<4, L, T>,  accept_stochastic_kernel<8, L, T>,                  \
+   accept_stochastic_kernel<16, L, T>, accept_stochastic_kernel<20, L, T>,                 \
+   accept_stochastic_kernel<24, L, T>, accept_stochastic_kernel<32, L, T>}
+  static const Kern kerns[2][2][kWalkElemKinds] = {
       {EAGLE_WALK_KERNS(false, kWideThreads), EAGLE_WALK_KERNS(true, kWideThreads)},
       {EAGLE_WALK_KERNS(false, kNarrowThreads), EAGLE_WALK_KERNS(true, kNarrowThreads)}};
 #undef EAGLE_WALK_KERNS
-  static PerDeviceOnce attr_once[2][2][5];
+  static PerDeviceOnce attr_once[2][2][kWalkElemKinds];
   // a shape's cluster size, slice, kernel and shared memory, attributes set
   struct Shape {
-    int cs, slice, threads;
+    int cs, slice, threads, elems;
     Kern kern;
     size_t smem;
   };
-  auto shape = [&](int kind, Shape* sh) -> eagle_status {
+  // kind 2: the narrow shape with `cs2` CTAs per cluster
+  auto shape = [&](int kind, Shape* sh, int cs2 = 0) -> eagle_status {
     int elems = 0;
     const int narrow = kind > 0 ? 1 : 0;
     sh->threads = narrow ? kNarrowThreads : kWideThreads;
-    sh->cs = pick_cluster(V, sh->threads, narrow ? kNarrowPrefer : kWidePrefer, &sh->slice, &elems);
     if (kind == 2)
-      sh->cs = (sh->cs >= 4) ? fixed_cluster(V, sh->threads, sh->cs / 4 * 3, &sh->slice, &elems) : 0;
+      sh->cs = fixed_cluster(V, sh->threads, cs2, &sh->slice, &elems);
+    else
+      sh->cs = pick_cluster(V, sh->threads, narrow ? kNarrowPrefer : kWidePrefer, &sh->slice,
+                            &elems);
     if (sh->cs <= 0) return EAGLE_ERR_UNSUPPORTED;
+    sh->elems = elems;
     sh->smem = (size_t)sh->slice * sizeof(float) + (size_t)max_nodes * 4 * sizeof(int) +
                (draft_in_smem(elems, sh->threads) ? (size_t)elems * sh->threads * sizeof(float) + 16
                                                   : 0);
-    const int ai = elems == 4 ? 0 : elems == 8 ? 1 : elems == 16 ? 2 : elems == 24 ? 3 : 4;
+    const int ai = walk_elems_index(elems);
     sh->kern = kerns[narrow][logits ? 1 : 0][ai];
     const Kern kern = sh->kern;
     if (attr_once[narrow][logits ? 1 : 0][ai].run([&] {
@@ -778,13 +792,30 @@ eagle_status launch_stochastic(bool logits, int B, int max_nodes, int V, int R, 
   if (st != EAGLE_OK) return st;
   if (B > 1 && sh.cs > 1) {
     int best_n = resident_clusters((const void*)sh.kern, sh.threads, sh.cs, sh.smem);
-    for (int kind = 1; kind <= 2 && B > best_n; ++kind) {
-      Shape c;
-      if (shape(kind, &c) != EAGLE_OK) continue;
+    Shape c;
+    if (B > best_n && shape(1, &c) == EAGLE_OK) {
       const int n = resident_clusters((const void*)c.kern, c.threads, c.cs, c.smem);
       if (n > best_n) {
         best_n = n;
         sh = c;
+      }
+      // smaller narrow clusters: the fewest entries per thread (a rejection
+      // round's cost follows them) among the sizes whose clusters are all
+      // resident; if none is, the most resident
+      if (B > best_n && c.cs >= 4) {
+        int found = 0;
+        for (int cs2 = c.cs - 1; cs2 >= (c.cs + 1) / 2; --cs2) {
+          Shape d;
+          if (shape(2, &d, cs2) != EAGLE_OK) continue;
+          const int nd = resident_clusters((const void*)d.kern, d.threads, d.cs, d.smem);
+          if (nd >= B) {
+            if (!found || d.elems < sh.elems || (d.elems == sh.elems && d.cs < sh.cs)) sh = d;
+            found = 1;
+          } else if (!found && nd > best_n) {
+            best_n = nd;
+            sh = d;
+          }
+        }
       }
     }
   }
