@@ -156,7 +156,8 @@ def test_stochastic_many_rejections_then_sample_at_full_vocab(B):
     # sequence runs up to k residual rounds and then the inverse-CDF sampler.
     # The walk's launch shape follows B: 4 sequences fit at once as 16 CTAs
     # of 1024 threads; 12 do not, and run as 16 CTAs of 512 threads, two per
-    # SM; 16 do not fit either way and run as 12 CTAs of 512 threads.
+    # SM; 16 do not fit either way and run in smaller clusters of 512-thread
+    # CTAs (13 of them, 20 entries per thread, when all 16 clusters fit).
     E = cuda_ready()
     V = 128256
     case = _stoch_case(11, B, V, [(1, 8, 8)], plant_frac=0.0)
