@@ -675,7 +675,9 @@ int resident_clusters(const void* kern, int threads, int cs, size_t smem) {
     int n;
   };
   static std::mutex mu;
-  static Entry cache[32];
+  // (up to ten shapes are looked at per vocabulary size, tree size and mode)
+  constexpr int kCache = 128;
+  static Entry cache[kCache];
   static int used = 0;
   int dev = 0;
   cudaGetDevice(&dev);
@@ -699,7 +701,7 @@ int resident_clusters(const void* kern, int threads, int cs, size_t smem) {
     cudaGetLastError();
     n = 0;
   }
-  if (used < 32) cache[used++] = Entry{kern, dev, cs, smem, n};
+  if (used < kCache) cache[used++] = Entry{kern, dev, cs, smem, n};
   return n;
 }
 
